@@ -1,0 +1,436 @@
+#!/usr/bin/env python
+"""Benchmark of the lossless BF16 weight restore (afx) on GB300.
+
+One step restores every tensor of one Qwen3-14B-shaped decoder layer
+(q/k/v/o, gate/up/down and the two norm vectors: 330,311,680 BF16 weights,
+0.66 GB) from containers already resident in HBM, through the C ABI
+(afx_decode per tensor, captured once in a CUDA graph and replayed).
+
+Reported: decoded BF16 GB/s (2 bytes x weights / step time) as `value`,
+weights/s, HBM GB/s (compressed bytes read + BF16 bytes written) against
+the measured copy bandwidth, the per-launch roofline of the decode kernel,
+an end-to-end number through the C ABI from pinned host containers to a
+host BF16 result, and the CPU oracle on the host cores.
+
+`--impl reference` times the CPU oracle itself (the reference arm): the
+bit-serial decoder of the same containers on the host cores.
+
+The decode is the t_unpack term of "Why Weight Offloading Slows
+Inference", Eq. (1); the break-even it must meet is that page's Eq. (2).
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decoded BF16 GB/s (and weights/s) per GB300; % of HBM roofline"
+WORKLOAD = "qwen3-14b-shaped decoder layer: q,o 5120x5120; k,v 1024x5120; gate,up 17408x5120; down 5120x17408; 2 norms 5120"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[1])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--no-extras", action="store_true", help="skip e2e and cpu_baseline legs")
+    return p.parse_args(argv)
+
+
+# ---- distributed plumbing (barrier and max over ranks only) ----------------------
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---- workload ------------------------------------------------------------------------
+
+def build_layer(seed: int, rank: int = 0):
+    """Generate and encode one layer on the host: [(name, w, container, desc)]."""
+    from weight_streaming_canonical_gb300 import afx, synth
+
+    names = [name for name, _, _ in synth.LAYER_TENSORS]
+
+    def one(name):
+        w = synth.layer_tensor(name, seed=seed, layer=rank).reshape(-1)
+        c, d = afx.encode(w)
+        return name, w, c, d
+
+    with cf.ThreadPoolExecutor(len(names)) as ex:
+        return list(ex.map(one, names))
+
+
+def algorithmic_bytes(d) -> int:
+    """Bytes a restore must move: coded exponent bits, sign|mantissa bytes,
+    chunk and block index entries read; 2 bytes per weight written."""
+    return (d.total_bits + 7) // 8 + d.n + 2 * d.n_chunks + 8 * (d.n_blocks + 1) + 2 * d.n
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+            return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---- CPU oracle leg ------------------------------------------------------------------
+
+def oracle_sample(parts, slice_elems: int = 1 << 24):
+    """Containers for the CPU oracle: every tensor of the layer cut into
+    independent slices of 2**24 weights, each its own container."""
+    from weight_streaming_canonical_gb300 import afx
+    work = []
+    for name, w, c, d in parts:
+        for s in range(0, w.size, slice_elems):
+            work.append(w[s:s + slice_elems])
+    with cf.ThreadPoolExecutor(16) as ex:
+        return list(ex.map(lambda a: afx.encode(a)[0], work))
+
+
+def time_oracle(containers, threads: int) -> tuple[float, int]:
+    """Seconds for the oracle to decode every container on `threads` threads
+    (ctypes releases the GIL, so the C decoder runs in parallel)."""
+    import oracle
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(threads) as ex:
+        results = list(ex.map(oracle.decode, containers))
+    dt = time.perf_counter() - t0
+    assert all(st == oracle.OK for _, st in results)
+    return dt, sum(out.size for out, _ in results)
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return "unknown"
+
+
+# ---- reference arm (the CPU oracle) ----------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), 0
+    if rank != 0:
+        return  # rank 0 alone runs the CPU reference
+    parts = build_layer(args.seed)
+    containers = oracle_sample(parts)
+    threads = os.cpu_count() or 1
+    n_total = sum(w.size for _, w, _, _ in parts)
+    # one step = the oracle restoring a bounded sample: 1/8 of the layer's slices
+    per_step = containers[: max(1, len(containers) // 8)]
+    for _ in range(args.warmup):
+        time_oracle(per_step, threads)
+    times, weights = [], 0
+    for _ in range(args.steps):
+        dt, nw = time_oracle(per_step, threads)
+        times.append(dt)
+        weights = nw
+    sec = sum(times) / len(times)
+    value = 2 * weights / sec / 1e9
+    sample = f"{len(per_step)} oracle containers of <= 2^24 weights ({weights} weights) per step, from the layer's {n_total} weights"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "weights_per_step": weights},
+        "weights_per_s": weights / sec,
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample,
+                         "cpu": cpu_model()},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---- our arm ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+
+    from weight_streaming_canonical_gb300 import afx
+
+    rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    parts = build_layer(args.seed, rank)
+    n_total = sum(d.n for _, _, _, d in parts)
+    comp_total = sum(d.container_bytes for _, _, _, d in parts)
+    alg_total = sum(algorithmic_bytes(d) for _, _, _, d in parts)
+
+    # resident containers and outputs
+    offs, o = [], 0
+    for _, _, c, _ in parts:
+        offs.append(o)
+        o += c.size
+    host_blob = torch.empty(o, dtype=torch.uint8).pin_memory()
+    hb = host_blob.numpy()
+    for (_, _, c, _), off in zip(parts, offs):
+        hb[off:off + c.size] = c
+    dev_blob = host_blob.to(dev)
+    out_offs, oo = [], 0
+    for _, _, _, d in parts:
+        out_offs.append(oo)
+        oo += d.n
+    out = torch.empty(oo, dtype=torch.int16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    views = [(d, dev_blob[off:off + d.container_bytes], out[oo_:oo_ + d.n])
+             for (_, _, _, d), off, oo_ in zip(parts, offs, out_offs)]
+
+    def step():
+        for d, cview, oview in views:
+            afx.afx_decode(d, cview, oview, status_dev=status)
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    torch.cuda.synchronize()
+    # correctness of what is timed: the restored layer equals the original bits
+    with torch.cuda.stream(stream):
+        out.zero_()
+        graph.replay()
+    torch.cuda.synchronize()
+    host_out = out.cpu().numpy().view(np.uint16)
+    for (name, w, _, _), oo_ in zip(parts, out_offs):
+        if not np.array_equal(host_out[oo_:oo_ + w.size], w):
+            raise SystemExit(f"restore of {name} is not bit-exact")
+    if status.item() != 0:
+        raise SystemExit(f"device status {status.item()}")
+
+    # timed region: K graph replays
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier(world)
+    ms = start.elapsed_time(end) / args.steps
+    ms = max_over_ranks(ms, world)
+
+    # per-launch durations of the decode kernel (same stream, events around each launch)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in views]
+          for _ in range(args.steps)]
+    with torch.cuda.stream(stream):
+        for k in range(args.steps):
+            for (d, cview, oview), (e0, e1) in zip(views, ev[k]):
+                e0.record(stream)
+                afx.afx_decode(d, cview, oview, status_dev=status)
+                e1.record(stream)
+    torch.cuda.synchronize()
+    launch_ms = [sum(e0.elapsed_time(e1) for e0, e1 in row) for row in ev]
+    kernel_ms = statistics.median(launch_ms)
+    peak, peak_kind = measured_hbm_peak()
+    achieved = alg_total / (kernel_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": None, "kernel": "decode_store_kernel", "peak_kind": peak_kind,
+                "launches_per_step": len(views), "algorithmic_bytes_per_step": alg_total,
+                "kernel_ms_per_step": kernel_ms}
+
+    sec = ms * 1e-3
+    total_weights = n_total * world
+    value = 2 * total_weights / sec / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u32",
+        "data": "synthetic: seeded N(0,0.02) BF16 matrices, N(1,0.05) norms, Qwen3-14B layer shapes",
+        "config": {"workload": WORKLOAD, "weights": n_total, "compressed_bytes": comp_total,
+                   "bits_per_weight": 8 * comp_total / n_total,
+                   "l2": "inputs larger than L2: %.0f MB compressed read and %.0f MB written per step"
+                         % (comp_total / 1e6, 2 * n_total / 1e6),
+                   "launch": "one CUDA graph of 9 afx_decode launches per step", "parallelism": f"replicas x{world}"},
+        "weights_per_s": total_weights / sec,
+        "hbm_gbs": alg_total * world / sec / 1e9,
+        "hbm_frac": alg_total / sec / 1e9 / peak,
+        "roofline": roofline,
+        "gpu_launches": len(views) * args.steps,
+        "clocks": clocks,
+    }
+
+    if not args.no_extras and rank == 0:
+        line["e2e"] = run_e2e(afx, parts, views, dev, args)
+        line["cpu_baseline"] = run_cpu_baseline(parts)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(afx, parts, views, dev, args):
+    """Pinned host containers -> device (afx_stream_run pipelines the copy of
+    tensor i+1 with the restore of tensor i) -> BF16 back to pinned host."""
+    import torch
+    blobs, ops_all, outs = [], [], []
+    for (_, w, c, d) in parts:
+        blob = torch.empty(c.size, dtype=torch.uint8).pin_memory()
+        blob.numpy()[:] = c
+        o = torch.empty(d.n, dtype=torch.int16, device=dev)
+        op = afx.afx_op()
+        op.desc = d
+        op.offset = 0
+        op.kind = afx.AFX_OP_DECODE
+        op.out_dev = o.data_ptr()
+        blobs.append(blob)
+        ops_all.append([op])
+        outs.append(o)
+    host_out = torch.empty(sum(d.n for _, _, _, d in parts), dtype=torch.int16).pin_memory()
+    buf_bytes = max(b.numel() for b in blobs)
+    bufs = [torch.empty(buf_bytes, dtype=torch.uint8, device=dev) for _ in range(3)]
+    compute, copy = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    layers = list(zip(blobs, ops_all))
+
+    def step():
+        afx.afx_stream_run(layers, bufs, buf_bytes, compute, copy)
+        o = 0
+        with torch.cuda.stream(compute):
+            for t in outs:
+                host_out[o:o + t.numel()].copy_(t, non_blocking=True)
+                o += t.numel()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    steps = max(3, args.steps // 2)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(compute)
+    for _ in range(steps):
+        step()
+    end.record(compute)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    n = sum(d.n for _, _, _, d in parts)
+    ok = all(np.array_equal(host_out.numpy().view(np.uint16)[s:s + w.size], w)
+             for s, w in zip(np.cumsum([0] + [w.size for _, w, _, _ in parts])[:-1], [w for _, w, _, _ in parts]))
+    return {"value": 2 * n / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": int(sum(b.numel() for b in blobs)), "d2h_bytes_per_step": 2 * n,
+            "bit_exact": bool(ok), "path": "afx_stream_run (pinned host containers) + D2H of the BF16 layer"}
+
+
+def run_cpu_baseline(parts):
+    containers = oracle_sample(parts)
+    sample = containers[: max(1, len(containers) // 4)]
+    threads = os.cpu_count() or 1
+    dt, nw = time_oracle(sample, threads)
+    dt1, nw1 = time_oracle(sample[:1], 1)
+    return {"value": 2 * nw / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(sample)} containers of <= 2^24 weights ({nw} weights) from the layer, one per thread",
+            "weights_per_s": nw / dt, "one_core_weights_per_s": nw1 / dt1, "cpu": cpu_model()}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,232 @@
+/*
+ * afx -- lossless BF16 weight unpack for NVIDIA GB300 (sm_103a).
+ *
+ * The operation: "Why Weight Offloading Slows Inference", section "Lossless
+ * compression: fewer bytes to read, more work to unpack" -- weights are
+ * stored without loss by giving common BF16 exponent values shorter codes
+ * (Huffman's minimum-redundancy code, that page's reference [2]), and every
+ * released bit is restored before computation.  The time this restore takes
+ * is the t_unpack term of that page's Eq. (1), and Eq. (2) says compression
+ * only pays when the read time it saves, (S - S_disk) / b_disk, exceeds it.
+ * "Memory requirements of language model inference on a consumer GPU",
+ * section "Number formats for weights", fixes BF16 as the released format
+ * and requires the weights to stay exact.
+ *
+ * The container format is this library's own (the pages fix none):
+ *   - a canonical Huffman code over the 8-bit BF16 exponent, code lengths
+ *     at most 24 bits (package-merge);
+ *   - a raw byte per weight holding sign and mantissa, (sign << 7) | mantissa;
+ *   - a chunk index: for every chunk of 8*T stream bits, the bit offset of
+ *     the first codeword that starts in it and how many codewords start in
+ *     it (the per-chunk bit-offset and output-count indices);
+ *   - a block index: for every block of C chunks, the number of weights that
+ *     come before it.
+ * Byte layout (little-endian; every section 256-byte aligned):
+ *   header 512 B: magic "AFX1" (0x31584641), version 1, n, total code bits,
+ *     T, C, chunk and block counts, section offsets and sizes, longest code
+ *     length, number of present exponents, fill exponent, then the 256 code
+ *     lengths at byte 256;
+ *   exp section: u32 words, stream bit i = bit (31 - i % 32) of word i / 32,
+ *     (chunks * T rounded up to 16) + 16 zero bytes long;
+ *   sm section: n bytes;  chunk index: u16 per chunk = offset | count << 5;
+ *   block index: u64 per block plus a final entry equal to n.
+ *
+ * Memory ownership: the caller allocates and frees every buffer.  No entry
+ * point allocates device memory.  Entry points that take a stream are
+ * asynchronous on that stream; the return value reports argument, format
+ * and launch errors found on the host.  Errors found by a kernel (a corrupt
+ * stream or index) are OR-ed into *status_dev (an int32 in device memory
+ * that the caller zeroes and reads after synchronising; may be NULL).  No
+ * entry point traps, aborts or waits on the device without a bound.
+ * Every entry point is thread-safe and keeps no state between calls.
+ */
+#ifndef AFX_H
+#define AFX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* afx_stream_t;
+
+typedef enum afx_status {
+    AFX_OK = 0,
+    AFX_E_ARG = -1,     /* bad argument: null pointer, size, alignment, geometry */
+    AFX_E_FORMAT = -2,  /* container header or code lengths are not valid */
+    AFX_E_CORRUPT = -3, /* host found a corrupt stream (encoder input check) */
+    AFX_E_CUDA = -4,    /* a CUDA runtime call failed */
+    AFX_E_NOSPACE = -5, /* destination or workspace smaller than required */
+    AFX_E_TIMEOUT = -6  /* a bounded host wait ran out */
+} afx_status;
+
+/* Bits OR-ed into *status_dev by the kernels. */
+#define AFX_DEV_BAD_BLOCK 0x1 /* a block's chunk counts disagree with the block index */
+#define AFX_DEV_BAD_CHUNK 0x2 /* a chunk's codewords do not end where the next chunk begins */
+#define AFX_DEV_BAD_CODE 0x4  /* a bit pattern that is no codeword */
+#define AFX_DEV_BAD_SHAPE 0x8 /* GEMV rows x cols disagree with the block index */
+
+#define AFX_MAX_CODE_LEN 24
+/* At most this many codewords start in one block (the decoder's per-block
+   staging capacity); the encoder picks T so that this always holds. */
+#define AFX_BLOCK_CAPACITY 32768
+#define AFX_HEADER_BYTES 512
+
+/* A code over the 256 exponent values. */
+typedef struct afx_code {
+    uint64_t count[256]; /* how many weights have each exponent */
+    uint32_t code[256];  /* canonical code, right-aligned in len bits */
+    uint8_t len[256];    /* code length; 0 = exponent absent (or the only one) */
+    uint32_t nsym;       /* number of exponents present */
+    uint32_t max_len;    /* longest code length (0 when nsym <= 1) */
+    uint32_t fill;       /* the exponent when nsym == 1, else 0 */
+    uint32_t reserved;
+} afx_code;
+
+/* Host-side description of one container: its geometry and section
+   offsets.  Filled by afx_encode_bound or afx_parse_header. */
+typedef struct afx_desc {
+    uint64_t n;               /* weights */
+    uint64_t total_bits;      /* sum of all code lengths */
+    uint32_t chunk_bytes;     /* T: stream bytes per chunk, 4..64, power of two */
+    uint32_t block_chunks;    /* C: chunks per block (the decoder runs C = 256) */
+    uint64_t n_chunks;        /* ceil(total_bits / (8 T)) */
+    uint64_t n_blocks;        /* ceil(n_chunks / C) */
+    uint64_t off_exp, exp_bytes;
+    uint64_t off_sm;
+    uint64_t off_chunk;
+    uint64_t off_block;
+    uint64_t container_bytes; /* whole container, a multiple of 256 */
+    uint32_t max_len, nsym, fill, reserved;
+    uint8_t len[256];
+} afx_desc;
+
+/* Histogram of the exponents of w_host[0..n) and an optimal prefix code of
+ * at most max_len bits (1..24; 24 is the format's cap) with canonical codes.
+ * w_host: n BF16 bit patterns in host memory.  Host only, multithreaded.
+ * Cites: "Why Weight Offloading Slows Inference", section "Lossless
+ * compression: fewer bytes to read, more work to unpack" (shorter codes for
+ * common BF16 exponents; Huffman, reference [2]).
+ * Errors: AFX_E_ARG on a null pointer or a max_len too small for the
+ * number of present exponents. */
+afx_status afx_build_code(const uint16_t* w_host, uint64_t n, uint32_t max_len, afx_code* out);
+
+/* Plans the container for n weights coded with `code`: fills *out with the
+ * geometry, section offsets and total size.  chunk_bytes = 0 picks T (32,
+ * or 16 when some code is 1 bit long, so a block never exceeds
+ * AFX_BLOCK_CAPACITY codewords); block_chunks = 0 picks C = 256.
+ * Host only.  Errors: AFX_E_ARG on a bad geometry or a T that could
+ * overflow the block capacity. */
+afx_status afx_encode_bound(uint64_t n, const afx_code* code, uint32_t chunk_bytes,
+                            uint32_t block_chunks, afx_desc* out);
+
+/* Writes the container for w_host[0..n) into dst_host (dst_bytes >=
+ * desc->container_bytes), using the code and the plan from
+ * afx_encode_bound.  Host only.  Errors: AFX_E_ARG when w holds an exponent
+ * that the code does not cover or n differs from the plan; AFX_E_NOSPACE
+ * when dst is too small. */
+afx_status afx_encode(const uint16_t* w_host, uint64_t n, const afx_code* code, const afx_desc* desc,
+                      uint8_t* dst_host, uint64_t dst_bytes);
+
+/* Validates the header of a container held in host memory (magic, version,
+ * geometry, section offsets, code lengths with the Kraft equality) and fills
+ * *out.  Only the first AFX_HEADER_BYTES are read; bytes is the size the
+ * caller holds (at least the header).  Errors: AFX_E_FORMAT. */
+afx_status afx_parse_header(const uint8_t* header_host, uint64_t bytes, afx_desc* out);
+
+/* Restores all n BF16 weights of one container: out_dev[i] = the i-th
+ * weight, bit for bit.  container_dev: the whole container in device
+ * memory, 16-byte aligned.  out_dev: n uint16 in device memory, 16-byte
+ * aligned.  desc: host copy of the container's description.  Runs
+ * asynchronously on `stream`; never reads outside the container or writes
+ * outside out_dev[0..n).  A corrupt stream or index sets AFX_DEV_* bits in
+ * *status_dev (the output is then unspecified).
+ * Cites: "Why Weight Offloading Slows Inference", section "Lossless
+ * compression: fewer bytes to read, more work to unpack" (restore the
+ * released bits before computation; t_unpack of Eq. (1)).
+ * Errors: AFX_E_ARG (null or misaligned pointers), AFX_E_FORMAT (desc),
+ * AFX_E_CUDA (launch). */
+afx_status afx_decode(const afx_desc* desc, const void* container_dev, uint16_t* out_dev,
+                      afx_stream_t stream, int32_t* status_dev);
+
+/* Device workspace (bytes) that afx_decode_gemv needs for this container
+ * and batch: one float per batch row for the two partial output rows of
+ * every block. */
+afx_status afx_decode_gemv_workspace(const afx_desc* desc, uint32_t batch, uint64_t* bytes);
+
+/* Fused restore + GEMV: y_dev[b][r] = sum_c W[r][c] * x_dev[b][c] for
+ * b < batch (1..4), where W is the container's weights viewed row-major as
+ * [rows][cols] (rows * cols == n; a row is one output, PyTorch nn.Linear
+ * layout) and x_dev is BF16 [batch][cols].  The restored weights never go
+ * to global memory.  Products and sums are float32; y_dev is float32
+ * [batch][rows], overwritten, and bitwise reproducible run to run.
+ * workspace_dev: afx_decode_gemv_workspace bytes of device memory, 16-byte
+ * aligned, contents ignored.  Requires cols >= 64, x_dev 16-byte aligned.
+ * Cites: same passage as afx_decode -- the restored weights feed the
+ * computation directly.
+ * Errors: AFX_E_ARG (shape, batch, alignment), AFX_E_NOSPACE (workspace),
+ * AFX_E_FORMAT, AFX_E_CUDA. */
+afx_status afx_decode_gemv(const afx_desc* desc, const void* container_dev, uint32_t rows, uint32_t cols,
+                           const uint16_t* x_dev, uint32_t batch, float* y_dev, void* workspace_dev,
+                           uint64_t workspace_bytes, afx_stream_t stream, int32_t* status_dev);
+
+/* One tensor of a streamed layer. */
+typedef enum afx_op_kind { AFX_OP_DECODE = 0, AFX_OP_GEMV = 1 } afx_op_kind;
+
+typedef struct afx_op {
+    afx_desc desc;          /* the tensor's container description */
+    uint64_t offset;        /* byte offset of its container inside the layer blob (multiple of 256) */
+    uint32_t kind;          /* afx_op_kind */
+    uint32_t rows, cols;    /* AFX_OP_GEMV: weight shape */
+    uint32_t batch;         /* AFX_OP_GEMV: 1..4 */
+    const uint16_t* x_dev;  /* AFX_OP_GEMV: [batch][cols] BF16 */
+    void* out_dev;          /* AFX_OP_DECODE: uint16[n];  AFX_OP_GEMV: float[batch][rows] */
+    void* workspace_dev;    /* AFX_OP_GEMV */
+    uint64_t workspace_bytes;
+} afx_op;
+
+typedef struct afx_layer {
+    const void* host_blob;  /* the layer's containers, pinned host memory (cudaHostAlloc) */
+    uint64_t blob_bytes;
+    const afx_op* ops;
+    uint32_t n_ops;
+    uint32_t reserved;
+} afx_layer;
+
+/* Streams layers from pinned host memory and runs their ops on one GPU:
+ * layer l is copied (cudaMemcpyAsync on copy_stream) into device buffer
+ * l % n_bufs while the ops of layer l-1 run on compute_stream; a buffer is
+ * reused only after the ops that read it have finished (CUDA events, no
+ * host waits).  dev_bufs: n_bufs (>= 2) device buffers of buf_bytes
+ * (>= every blob_bytes), 256-byte aligned; they may be passed again to a
+ * later call, whose first copy waits for all work already queued on
+ * compute_stream.  Enqueues everything and returns; synchronise
+ * compute_stream to wait for the results.
+ * Cites: "Why Weight Offloading Slows Inference", section "Loading during
+ * computation" and Figure 2 (load layer l+1 while layer l computes; a load
+ * is free only if it finishes before the GPU needs it), and "Memory
+ * requirements of language model inference on a consumer GPU", section
+ * "Loading one part of the model at a time" (load, use, release each
+ * layer in turn).
+ * Errors: AFX_E_ARG, AFX_E_NOSPACE (a blob larger than buf_bytes),
+ * AFX_E_FORMAT, AFX_E_CUDA. */
+afx_status afx_stream_run(const afx_layer* layers, uint32_t n_layers, void* const* dev_bufs, uint32_t n_bufs,
+                          uint64_t buf_bytes, afx_stream_t compute_stream, afx_stream_t copy_stream,
+                          int32_t* status_dev);
+
+/* Static text for a status code. */
+const char* afx_status_string(afx_status status);
+
+/* The message of the last error an entry point returned on this thread
+ * (with the CUDA error name when a CUDA call failed).  Never NULL; valid
+ * until the next call into afx on this thread. */
+const char* afx_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AFX_H */

@@ -18,3 +18,12 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return GOLDEN
+
+
+@pytest.fixture(scope="session")
+def afx():
+    """The product binding, built in-tree first if needed (nvcc cross-compiles here)."""
+    from weight_streaming_canonical_gb300 import build as _build
+    _build.build()
+    from weight_streaming_canonical_gb300 import afx as _afx
+    return _afx

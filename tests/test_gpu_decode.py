@@ -1,0 +1,170 @@
+"""GPU decode parity: afx_decode (through the C ABI) against the CPU oracle,
+bit for bit, from tiny ragged inputs to the full workloads."""
+import numpy as np
+import pytest
+
+import oracle
+from afx_testutil import gpu_decode
+from weight_streaming_canonical_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(afx, w, chunk_bytes=0, **kw):
+    w = np.ascontiguousarray(w).reshape(-1)
+    c, d = afx.encode(w, chunk_bytes=chunk_bytes)
+    ref, st = oracle.decode(c)
+    assert st == oracle.OK and np.array_equal(ref, w)
+    out, status, intact = gpu_decode(afx, c, d, **kw)
+    assert status == 0
+    assert intact, "wrote outside the output range"
+    mism = np.flatnonzero(out != ref)
+    assert mism.size == 0, f"{mism.size} mismatches, first at {mism[:5]}"
+    return c, d
+
+
+@pytest.mark.parametrize("n", [1, 2, 7, 8, 9, 15, 16, 17, 255, 256, 257, 1000, 4095, 4097, 25_000, 65_537,
+                               300_007, 1_000_003])
+def test_ragged_sizes(afx, n):
+    _check(afx, synth.normal(n, seed=n), out_pad=24)
+
+
+@pytest.mark.parametrize("T", [4, 8, 16, 32])
+def test_every_bf16_pattern_every_chunk_size(afx, T):
+    w = synth.all_bf16_patterns()
+    rng = np.random.default_rng(T)
+    _check(afx, np.concatenate([w, rng.permutation(w), w[::-1]]), chunk_bytes=T)
+
+
+@pytest.mark.parametrize("offset", [0, 8, 16, 24])
+def test_output_offsets_keep_guards(afx, offset):
+    _check(afx, synth.normal(123_457, seed=3), out_offset=offset, out_pad=16)
+
+
+def test_single_exponent_tensor(afx):
+    w = (np.full(100_003, 0x3F80, np.uint16) | (np.arange(100_003) % 128).astype(np.uint16)
+         | ((np.arange(100_003) % 3 == 0).astype(np.uint16) << 15))
+    c, d = _check(afx, w, out_pad=8)
+    assert d.nsym == 1 and d.total_bits == 0
+
+
+def test_two_exponent_tensor_uses_one_bit_codes(afx):
+    w = np.where(np.random.default_rng(1).random(200_001) < 0.7, 0x3F80, 0x3F00).astype(np.uint16)
+    c, d = _check(afx, w)
+    assert d.chunk_bytes == 16 and d.total_bits == w.size
+
+
+def test_norm_vector(afx):
+    _check(afx, synth.layer_tensor("input_layernorm", seed=0))
+
+
+def test_long_codes(afx):
+    c, d = _check(afx, synth.adversarial(1 << 22, seed=1))
+    assert d.max_len > 12  # exercises the second table level
+
+
+def test_repeat_is_deterministic(afx):
+    w = synth.normal(500_000, seed=9)
+    c, d = afx.encode(w)
+    a, s1, _ = gpu_decode(afx, c, d)
+    b, s2, _ = gpu_decode(afx, c, d)
+    assert s1 == s2 == 0 and np.array_equal(a, b) and np.array_equal(a, w)
+
+
+def test_matrix_4096(afx):
+    _check(afx, synth.matrix_4096(seed=0))
+
+
+@pytest.mark.slow
+def test_qwen3_layer_all_tensors(afx):
+    for name, tensor in synth.layer(seed=0).items():
+        _check(afx, tensor.reshape(-1))
+
+
+@pytest.mark.slow
+def test_adversarial_2_28(afx):
+    w = synth.adversarial(1 << 28, seed=0)
+    c, d = _check(afx, w)
+    assert d.max_len == 24  # the 24-bit cap is exercised
+
+
+# ---- corrupt input: status bits or a detected mismatch, never a hang ----------
+
+def _decode_bad(afx, c, d, w):
+    out, status, intact = gpu_decode(afx, c, d, out_pad=64)
+    assert intact
+    return status, out
+
+
+def test_corrupt_chunk_index_is_flagged(afx):
+    w = synth.normal(400_000, seed=11)
+    c, d = afx.encode(w)
+    for k in (0, 5, 300, d.n_chunks - 1):
+        for flip in (1, 1 << 5, 1 << 9, 1 << 15):
+            bad = c.copy()
+            e = bad[d.off_chunk + 2 * k: d.off_chunk + 2 * k + 2].view(np.uint16)
+            e[0] ^= flip
+            status, out = _decode_bad(afx, bad, d, w)
+            assert status != 0 or np.array_equal(out, w)
+
+
+def test_corrupt_block_index_is_flagged(afx):
+    w = synth.normal(400_000, seed=12)
+    c, d = afx.encode(w)
+    for b in range(d.n_blocks + 1):
+        bad = c.copy()
+        bad[d.off_block + 8 * b] ^= 0x3
+        status, out = _decode_bad(afx, bad, d, w)
+        assert status & afx.AFX_DEV_BAD_BLOCK
+
+
+def test_corrupt_stream_is_detected(afx):
+    w = synth.normal(400_000, seed=13)
+    c, d = afx.encode(w)
+    rng = np.random.default_rng(0)
+    for pos in rng.integers(0, d.total_bits // 8, size=12):  # inside the coded bits, not the padding
+        bad = c.copy()
+        bad[d.off_exp + int(pos)] ^= 0x20
+        status, out = _decode_bad(afx, bad, d, w)
+        assert status != 0 or not np.array_equal(out, w)
+
+
+def test_header_n_mismatch_is_flagged(afx):
+    w = synth.normal(70_000, seed=5)
+    c, d = afx.encode(w)
+    bad = c.copy()
+    bad[8] ^= 0x04  # n changes, section layout does not
+    d2 = afx.afx_parse_header(bad)
+    status, _ = _decode_bad(afx, bad, d2, w)
+    assert status & afx.AFX_DEV_BAD_BLOCK
+
+
+def test_garbage_stream_never_hangs(afx):
+    w = synth.normal(300_000, seed=14)
+    c, d = afx.encode(w)
+    bad = c.copy()
+    rng = np.random.default_rng(1)
+    bad[d.off_exp: d.off_exp + d.n_chunks * d.chunk_bytes] = rng.integers(
+        0, 256, size=d.n_chunks * d.chunk_bytes, dtype=np.uint8)
+    status, _ = _decode_bad(afx, bad, d, w)
+    assert status != 0
+
+
+def test_host_side_argument_errors(afx):
+    import torch
+    w = synth.normal(10_000, seed=15)
+    c, d = afx.encode(w)
+    dev = torch.from_numpy(c).cuda()
+    out = torch.empty(d.n + 8, dtype=torch.int16, device="cuda")
+    with pytest.raises(afx.AfxError):
+        afx.afx_decode(d, dev, out[1:])  # output not 16-byte aligned
+    with pytest.raises(afx.AfxError):
+        afx.afx_decode(d, dev[1:], out)  # container not 16-byte aligned
+    d_bad = afx.afx_parse_header(c)
+    d_bad.off_sm += 256
+    with pytest.raises(afx.AfxError):
+        afx.afx_decode(d_bad, dev, out)
+    c32 = oracle.encode(w, np.array(afx.afx_build_code(w).len[:], np.uint8), 8, 32)
+    d32 = afx.afx_parse_header(c32)
+    with pytest.raises(afx.AfxError):  # the decoder runs 256 chunks per block
+        afx.afx_decode(d32, torch.from_numpy(c32).cuda(), out)

@@ -1,0 +1,104 @@
+"""Fused decode + GEMV parity: afx_decode_gemv (through the C ABI) against the
+oracle GEMV on the oracle-decoded weights, |err| <= 2e-3 * sum|w x| per
+output, plus closed forms and run-to-run reproducibility."""
+import numpy as np
+import pytest
+
+import oracle
+from afx_testutil import gpu_gemv, within_gemv_tolerance
+from weight_streaming_canonical_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(afx, W, x):
+    rows, cols = W.shape
+    c, d = afx.encode(W.reshape(-1))
+    Wd, st = oracle.decode(c)
+    assert st == oracle.OK
+    y_ref, A = oracle.gemv(Wd.reshape(rows, cols), x)
+    y, status = gpu_gemv(afx, c, d, rows, cols, x)
+    assert status == 0
+    assert not np.isnan(y).any(), "an output was never written"
+    assert within_gemv_tolerance(y, y_ref, A), float(np.max(np.abs(y - y_ref) / np.maximum(A, 1e-30)))
+    return y, c, d
+
+
+SHAPES = [(64, 64), (3, 5120), (257, 1000), (100, 5120), (7, 17408), (1024, 72), (41, 4099), (2000, 128)]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("B", [1, 2, 3, 4])
+def test_shapes_and_batches(afx, shape, B):
+    rows, cols = shape
+    W = synth.normal(rows * cols, seed=rows + cols).reshape(rows, cols)
+    x = synth.activations(B, cols, seed=B)
+    _check(afx, W, x)
+
+
+def test_unit_vector_gives_a_column_exactly(afx):
+    rows, cols = 300, 5120
+    W = synth.normal(rows * cols, seed=1).reshape(rows, cols)
+    for j in (0, 4095, 5119):
+        x = np.zeros((1, cols), np.uint16)
+        x[0, j] = 0x3F80
+        c, d = afx.encode(W.reshape(-1))
+        y, status = gpu_gemv(afx, c, d, rows, cols, x)
+        assert status == 0
+        col = (W[:, j].astype(np.uint32) << 16).view(np.float32)
+        assert np.array_equal(y[0], col)
+
+
+def test_zero_activation_gives_zero(afx):
+    W = synth.normal(64 * 5120, seed=2).reshape(64, 5120)
+    c, d = afx.encode(W.reshape(-1))
+    y, status = gpu_gemv(afx, c, d, 64, 5120, np.zeros((4, 5120), np.uint16))
+    assert status == 0 and not y.any()
+
+
+def test_reproducible_bit_for_bit(afx):
+    W = synth.normal(333 * 5120, seed=3).reshape(333, 5120)
+    x = synth.activations(4, 5120, seed=3)
+    c, d = afx.encode(W.reshape(-1))
+    y1, _ = gpu_gemv(afx, c, d, 333, 5120, x)
+    y2, _ = gpu_gemv(afx, c, d, 333, 5120, x)
+    assert np.array_equal(y1, y2)
+
+
+def test_row_longer_than_a_block(afx):
+    # one row spans several decode blocks: the fix-up pass joins the partials
+    W = synth.normal(3 * 200_000, seed=4).reshape(3, 200_000)
+    x = synth.activations(2, 200_000, seed=4)
+    _check(afx, W, x)
+
+
+def test_single_exponent_matrix(afx):
+    W = (np.full((50, 640), 0x3F80, np.uint16) | (np.arange(50 * 640).reshape(50, 640) % 128).astype(np.uint16))
+    _check(afx, W, synth.activations(3, 640, seed=5))
+
+
+def test_bad_arguments(afx):
+    import torch
+    W = synth.normal(64 * 128, seed=6).reshape(64, 128)
+    c, d = afx.encode(W.reshape(-1))
+    dev = torch.from_numpy(c).cuda()
+    x = torch.zeros((5, 128), dtype=torch.int16, device="cuda")
+    y = torch.zeros((5, 64), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(1 << 16, dtype=torch.float32, device="cuda")
+    with pytest.raises(afx.AfxError):
+        afx.afx_decode_gemv(d, dev, 64, 128, x, y, ws)  # batch 5
+    with pytest.raises(afx.AfxError):
+        afx.afx_decode_gemv(d, dev, 32, 128, x[:1], y, ws)  # rows * cols != n
+    with pytest.raises(afx.AfxError):
+        afx.afx_decode_gemv(d, dev, 64, 128, x[:1], y, ws[:1])  # workspace too small
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("B", [1, 4])
+def test_qwen3_layer_matrices(afx, B):
+    for name, shape, kind in synth.LAYER_TENSORS:
+        if kind != "matrix":
+            continue
+        W = synth.layer_tensor(name, seed=0)
+        x = synth.activations(B, shape[1], seed=10 + B)
+        _check(afx, W, x)

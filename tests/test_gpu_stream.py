@@ -1,0 +1,89 @@
+"""Layer streaming through afx_stream_run: compressed layers copied from pinned
+host memory while earlier layers decode; every output checked against the
+oracle."""
+import numpy as np
+import pytest
+
+import oracle
+from afx_testutil import within_gemv_tolerance
+from weight_streaming_canonical_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _layer(afx, seed, shapes):
+    """Containers of one small layer packed into one blob, with their ops."""
+    import torch
+    parts, metas, off = [], [], 0
+    for i, (kind, shape) in enumerate(shapes):
+        n = int(np.prod(shape))
+        w = synth.normal(n, 1.0 if kind == "norm" else 0.0, 0.05 if kind == "norm" else 0.02, seed=seed, stream=i)
+        c, d = afx.encode(w)
+        parts.append(c)
+        metas.append((kind, shape, w, c, d, off))
+        off += c.size
+    blob = torch.empty(off, dtype=torch.uint8).pin_memory()
+    blob.numpy()[:] = np.concatenate(parts)
+    return blob, metas
+
+
+def _ops(afx, metas, B, keep):
+    import torch
+    ops = []
+    for kind, shape, w, c, d, off in metas:
+        op = afx.afx_op()
+        op.desc = d
+        op.offset = off
+        if kind == "norm" or kind == "decode":
+            out = torch.empty(d.n, dtype=torch.int16, device="cuda")
+            op.kind = afx.AFX_OP_DECODE
+            op.out_dev = out.data_ptr()
+            keep.append(("decode", out, w, None))
+        else:
+            rows, cols = shape
+            x = synth.activations(B, cols, seed=rows)
+            xd = torch.from_numpy(x.view(np.int16)).cuda()
+            y = torch.full((B, rows), float("nan"), dtype=torch.float32, device="cuda")
+            ws = torch.empty(afx.afx_decode_gemv_workspace(d, B) // 4 + 4, dtype=torch.float32, device="cuda")
+            op.kind = afx.AFX_OP_GEMV
+            op.rows, op.cols, op.batch = rows, cols, B
+            op.x_dev, op.out_dev, op.workspace_dev = xd.data_ptr(), y.data_ptr(), ws.data_ptr()
+            op.workspace_bytes = ws.numel() * 4
+            keep.append(("gemv", y, (w, c, x, rows, cols), (xd, ws)))
+        ops.append(op)
+    return ops
+
+
+@pytest.mark.parametrize("n_bufs", [2, 3])
+def test_streamed_layers_match_the_oracle(afx, n_bufs):
+    import torch
+    shapes = [("norm", (640,)), ("gemv", (96, 640)), ("gemv", (640, 1024)), ("decode", (256, 640)),
+              ("norm", (640,)), ("gemv", (1024, 640))]
+    keep, layers = [], []
+    for l in range(5):
+        blob, metas = _layer(afx, 100 + l, shapes)
+        layers.append((blob, _ops(afx, metas, 1 + l % 4, keep)))
+    buf_bytes = max(b.numel() for b, _ in layers)
+    bufs = [torch.empty(buf_bytes, dtype=torch.uint8, device="cuda") for _ in range(n_bufs)]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    copy = torch.cuda.Stream()
+    afx.afx_stream_run(layers, bufs, buf_bytes, torch.cuda.current_stream(), copy, status_dev=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    for kind, out, ref, _ in keep:
+        if kind == "decode":
+            assert np.array_equal(out.cpu().numpy().view(np.uint16), ref)
+        else:
+            w, c, x, rows, cols = ref
+            y_ref, A = oracle.gemv(w.reshape(rows, cols), x)
+            assert within_gemv_tolerance(out.cpu().numpy(), y_ref, A)
+
+
+def test_blob_larger_than_buffer_is_rejected(afx):
+    import torch
+    blob, metas = _layer(afx, 7, [("decode", (64, 640))])
+    keep = []
+    ops = _ops(afx, metas, 1, keep)
+    bufs = [torch.empty(256, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    with pytest.raises(afx.AfxError):
+        afx.afx_stream_run([(blob, ops)], bufs, 256)

@@ -1,0 +1,133 @@
+"""Host side of the library (no GPU): the encoder against the oracle, header
+validation, geometry choice, and the exported C ABI."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from weight_streaming_canonical_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _cost(hist, lens):
+    return int(sum(int(hist[s]) * int(lens[s]) for s in range(256)))
+
+
+def test_every_declared_entry_point_is_exported(afx):
+    header = open(os.path.join(ROOT, "include", "afx.h")).read()
+    body = re.sub(r"/\*.*?\*/", "", header, flags=re.S)
+    names = set(re.findall(r"\b(afx_[a-z_]+)\s*\(", body))
+    assert {"afx_build_code", "afx_encode_bound", "afx_encode", "afx_decode", "afx_decode_gemv",
+            "afx_stream_run", "afx_parse_header"} <= names
+    lib = ctypes.CDLL(afx.LIB_PATH)
+    for name in sorted(names):
+        assert hasattr(lib, name), name
+
+
+def test_struct_sizes_match_the_c_layout(afx):
+    # afx_code: 256 u64 + 256 u32 + 256 u8 + 4 u32; afx_desc: fixed fields + 256 lengths
+    assert ctypes.sizeof(afx.afx_code) == 2048 + 1024 + 256 + 16
+    assert ctypes.sizeof(afx.afx_desc) == 8 * 2 + 4 * 2 + 8 * 2 + 8 * 6 + 4 * 4 + 256
+
+
+CASES = {
+    "normal": lambda: synth.normal(300_001, seed=1),
+    "norm_vector": lambda: synth.normal(5120, 1.0, 0.05, seed=2),
+    "all_patterns": synth.all_bf16_patterns,
+    "adversarial": lambda: synth.adversarial(1 << 20, seed=3),
+    "two_symbols": lambda: np.array([0x3F80, 0x4000] * 999, np.uint16),
+    "single": lambda: np.full(777, 0x3F80, np.uint16),
+    "empty": lambda: np.zeros(0, np.uint16),
+    "tiny": lambda: np.array([0x3F80, 0x0001, 0xFFC1], np.uint16),
+}
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_code_is_optimal_and_canonical(afx, case):
+    w = CASES[case]()
+    code = afx.afx_build_code(w)
+    hist = oracle.histogram(w)
+    assert np.array_equal(np.array(code.count[:], np.uint64), hist)
+    lens = np.array(code.len[:], np.uint8)
+    ref = oracle.code_lengths(hist, 24)
+    assert _cost(hist, lens) == _cost(hist, ref)
+    assert lens.max() <= 24
+    if code.nsym >= 2:
+        assert sum(1 << (24 - int(l)) for l in lens if l) == 1 << 24
+    assert np.array_equal(np.array(code.code[:], np.uint32), oracle.canonical_codes(lens))
+
+
+@pytest.mark.parametrize("case", sorted(CASES))
+@pytest.mark.parametrize("T", [0, 4, 16, 64])
+def test_container_is_byte_identical_to_the_oracle(afx, case, T):
+    w = CASES[case]()
+    code = afx.afx_build_code(w)
+    try:
+        desc = afx.afx_encode_bound(w.size, code, T, 256)
+    except afx.AfxError:
+        assert T == 64  # a 64-byte chunk can exceed the block capacity
+        return
+    c = afx.afx_encode(w, code, desc)
+    ref = oracle.encode(w, np.array(code.len[:], np.uint8), desc.chunk_bytes, 256)
+    assert np.array_equal(c, ref)
+    out, st = oracle.decode(c)
+    assert st == oracle.OK and np.array_equal(out, w)
+
+
+def test_geometry_choice_respects_block_capacity(afx):
+    w = synth.normal(100_000, seed=4)
+    d = afx.afx_encode_bound(w.size, afx.afx_build_code(w))
+    assert d.chunk_bytes == 32 and d.block_chunks == 256
+    # a dominant exponent gets a 1-bit code: 32-byte chunks could hold 65536 codewords per block
+    v = np.where(np.arange(50_000) % 3 == 0, 0x4000, 0x3F80).astype(np.uint16)
+    code = afx.afx_build_code(v)
+    assert min(l for l in code.len if l) == 1
+    d = afx.afx_encode_bound(v.size, code)
+    assert d.chunk_bytes == 16
+    with pytest.raises(afx.AfxError):
+        afx.afx_encode_bound(v.size, code, 32, 256)
+
+
+def test_parse_header_roundtrip_and_rejections(afx):
+    w = synth.normal(70_000, seed=5)
+    c, d = afx.encode(w)
+    p = afx.afx_parse_header(c)
+    assert afx.desc_dict(p) == afx.desc_dict(d)
+    # n and total_bits (offsets 8, 16) can change without moving any section;
+    # the header alone cannot show that, the kernels check n against the block index
+    for off in (0, 4, 6, 24, 28, 32, 40, 56, 64, 88, 96, 100, 104, 150):
+        bad = c.copy()
+        bad[off] ^= 0x04
+        with pytest.raises(afx.AfxError):
+            afx.afx_parse_header(bad)
+    bad = c.copy()
+    bad[256 + int(np.argmax(c[256:512]))] += 1  # Kraft equality broken
+    with pytest.raises(afx.AfxError):
+        afx.afx_parse_header(bad)
+    with pytest.raises(afx.AfxError):
+        afx.afx_parse_header(c[:100])
+
+
+def test_encode_rejects_data_the_code_does_not_cover(afx):
+    w = synth.normal(10_000, seed=6)
+    code = afx.afx_build_code(w)
+    desc = afx.afx_encode_bound(w.size, code)
+    other = w.copy()
+    other[17] = 0x7F80  # +inf: exponent 255, absent from the code
+    with pytest.raises(afx.AfxError):
+        afx.afx_encode(other, code, desc)
+    with pytest.raises(afx.AfxError):
+        afx.afx_encode(w, code, desc, out=np.zeros(desc.container_bytes - 256, np.uint8))
+
+
+def test_gemv_workspace_size(afx):
+    w = synth.normal(5120 * 64, seed=7)
+    _, d = afx.encode(w)
+    for b in (1, 2, 3, 4):
+        assert afx.afx_decode_gemv_workspace(d, b) >= d.n_blocks * 2 * b * 4
+    with pytest.raises(afx.AfxError):
+        afx.afx_decode_gemv_workspace(d, 5)

@@ -1,0 +1,240 @@
+"""ctypes binding of libafx (include/afx.h): same names, argument marshalling only.
+
+Host arrays are numpy; device buffers and streams are torch CUDA tensors
+and torch streams (torch is used only for device memory and streams).
+Every step of the unpack runs in libafx.  Importing this module loads the
+library and raises ImportError if it has not been built: there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libafx.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libafx.so is not built ({LIB_PATH} missing); run "
+        "`python -m weight_streaming_canonical_gb300.build` (needs nvcc)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+AFX_OK, AFX_E_ARG, AFX_E_FORMAT, AFX_E_CORRUPT, AFX_E_CUDA, AFX_E_NOSPACE, AFX_E_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
+AFX_DEV_BAD_BLOCK, AFX_DEV_BAD_CHUNK, AFX_DEV_BAD_CODE, AFX_DEV_BAD_SHAPE = 0x1, 0x2, 0x4, 0x8
+AFX_MAX_CODE_LEN = 24
+AFX_BLOCK_CAPACITY = 32768
+AFX_HEADER_BYTES = 512
+AFX_OP_DECODE, AFX_OP_GEMV = 0, 1
+
+
+class afx_code(ctypes.Structure):
+    _fields_ = [
+        ("count", ctypes.c_uint64 * 256),
+        ("code", ctypes.c_uint32 * 256),
+        ("len", ctypes.c_uint8 * 256),
+        ("nsym", ctypes.c_uint32),
+        ("max_len", ctypes.c_uint32),
+        ("fill", ctypes.c_uint32),
+        ("reserved", ctypes.c_uint32),
+    ]
+
+
+class afx_desc(ctypes.Structure):
+    _fields_ = [
+        ("n", ctypes.c_uint64),
+        ("total_bits", ctypes.c_uint64),
+        ("chunk_bytes", ctypes.c_uint32),
+        ("block_chunks", ctypes.c_uint32),
+        ("n_chunks", ctypes.c_uint64),
+        ("n_blocks", ctypes.c_uint64),
+        ("off_exp", ctypes.c_uint64),
+        ("exp_bytes", ctypes.c_uint64),
+        ("off_sm", ctypes.c_uint64),
+        ("off_chunk", ctypes.c_uint64),
+        ("off_block", ctypes.c_uint64),
+        ("container_bytes", ctypes.c_uint64),
+        ("max_len", ctypes.c_uint32),
+        ("nsym", ctypes.c_uint32),
+        ("fill", ctypes.c_uint32),
+        ("reserved", ctypes.c_uint32),
+        ("len", ctypes.c_uint8 * 256),
+    ]
+
+
+class afx_op(ctypes.Structure):
+    _fields_ = [
+        ("desc", afx_desc),
+        ("offset", ctypes.c_uint64),
+        ("kind", ctypes.c_uint32),
+        ("rows", ctypes.c_uint32),
+        ("cols", ctypes.c_uint32),
+        ("batch", ctypes.c_uint32),
+        ("x_dev", ctypes.c_void_p),
+        ("out_dev", ctypes.c_void_p),
+        ("workspace_dev", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_uint64),
+    ]
+
+
+class afx_layer(ctypes.Structure):
+    _fields_ = [
+        ("host_blob", ctypes.c_void_p),
+        ("blob_bytes", ctypes.c_uint64),
+        ("ops", ctypes.POINTER(afx_op)),
+        ("n_ops", ctypes.c_uint32),
+        ("reserved", ctypes.c_uint32),
+    ]
+
+
+_vp, _u32, _u64, _i32p = ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_void_p
+_lib.afx_build_code.argtypes = [_vp, _u64, _u32, ctypes.POINTER(afx_code)]
+_lib.afx_encode_bound.argtypes = [_u64, ctypes.POINTER(afx_code), _u32, _u32, ctypes.POINTER(afx_desc)]
+_lib.afx_encode.argtypes = [_vp, _u64, ctypes.POINTER(afx_code), ctypes.POINTER(afx_desc), _vp, _u64]
+_lib.afx_parse_header.argtypes = [_vp, _u64, ctypes.POINTER(afx_desc)]
+_lib.afx_decode.argtypes = [ctypes.POINTER(afx_desc), _vp, _vp, _vp, _i32p]
+_lib.afx_decode_gemv_workspace.argtypes = [ctypes.POINTER(afx_desc), _u32, ctypes.POINTER(ctypes.c_uint64)]
+_lib.afx_decode_gemv.argtypes = [ctypes.POINTER(afx_desc), _vp, _u32, _u32, _vp, _u32, _vp, _vp, _u64, _vp, _i32p]
+_lib.afx_stream_run.argtypes = [ctypes.POINTER(afx_layer), _u32, ctypes.POINTER(ctypes.c_void_p), _u32, _u64, _vp,
+                                _vp, _i32p]
+_lib.afx_last_error.argtypes = []
+_lib.afx_last_error.restype = ctypes.c_char_p
+_lib.afx_status_string.argtypes = [ctypes.c_int]
+_lib.afx_status_string.restype = ctypes.c_char_p
+for _f in (_lib.afx_build_code, _lib.afx_encode_bound, _lib.afx_encode, _lib.afx_parse_header, _lib.afx_decode,
+           _lib.afx_decode_gemv_workspace, _lib.afx_decode_gemv, _lib.afx_stream_run):
+    _f.restype = ctypes.c_int
+
+
+class AfxError(RuntimeError):
+    def __init__(self, fn: str, status: int, detail: str = ""):
+        super().__init__(f"{fn}: {afx_status_string(status)} ({status})" + (f": {detail}" if detail else ""))
+        self.status = status
+
+
+def afx_last_error() -> str:
+    return _lib.afx_last_error().decode()
+
+
+def afx_status_string(status: int) -> str:
+    return _lib.afx_status_string(int(status)).decode()
+
+
+def _check(fn: str, st: int) -> None:
+    if st != AFX_OK:
+        raise AfxError(fn, st, afx_last_error() if st == AFX_E_CUDA else "")
+
+
+def _host_u16(w) -> np.ndarray:
+    a = np.ascontiguousarray(w).reshape(-1)
+    if a.dtype != np.uint16:
+        raise TypeError(f"expected BF16 bit patterns as uint16, got {a.dtype}")
+    return a
+
+
+def _dev_ptr(t) -> int:
+    if t is None:
+        return 0
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("expected a contiguous CUDA tensor")
+    return t.data_ptr()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+# ---- C entry points ---------------------------------------------------------
+
+def afx_build_code(w, max_len: int = AFX_MAX_CODE_LEN) -> afx_code:
+    a = _host_u16(w)
+    code = afx_code()
+    _check("afx_build_code", _lib.afx_build_code(a.ctypes.data, a.size, max_len, ctypes.byref(code)))
+    return code
+
+
+def afx_encode_bound(n: int, code: afx_code, chunk_bytes: int = 0, block_chunks: int = 0) -> afx_desc:
+    d = afx_desc()
+    _check("afx_encode_bound", _lib.afx_encode_bound(n, ctypes.byref(code), chunk_bytes, block_chunks, ctypes.byref(d)))
+    return d
+
+
+def afx_encode(w, code: afx_code, desc: afx_desc, out: np.ndarray | None = None) -> np.ndarray:
+    a = _host_u16(w)
+    if out is None:
+        out = np.empty(desc.container_bytes, np.uint8)
+    if out.dtype != np.uint8 or not out.flags["C_CONTIGUOUS"]:
+        raise ValueError("out must be a contiguous uint8 array")
+    _check("afx_encode", _lib.afx_encode(a.ctypes.data, a.size, ctypes.byref(code), ctypes.byref(desc),
+                                          out.ctypes.data, out.size))
+    return out
+
+
+def afx_parse_header(container) -> afx_desc:
+    c = np.ascontiguousarray(container, dtype=np.uint8).reshape(-1)
+    d = afx_desc()
+    _check("afx_parse_header", _lib.afx_parse_header(c.ctypes.data, c.size, ctypes.byref(d)))
+    return d
+
+
+def afx_decode(desc: afx_desc, container_dev, out_dev, stream=None, status_dev=None) -> None:
+    """out_dev: CUDA tensor of n 16-bit elements (uint16/int16/bfloat16)."""
+    if out_dev.numel() < desc.n or out_dev.element_size() != 2:
+        raise ValueError("out_dev must hold n 16-bit elements")
+    _check("afx_decode", _lib.afx_decode(ctypes.byref(desc), _dev_ptr(container_dev), _dev_ptr(out_dev),
+                                          _stream_handle(stream), _dev_ptr(status_dev)))
+
+
+def afx_decode_gemv_workspace(desc: afx_desc, batch: int) -> int:
+    v = ctypes.c_uint64(0)
+    _check("afx_decode_gemv_workspace", _lib.afx_decode_gemv_workspace(ctypes.byref(desc), batch, ctypes.byref(v)))
+    return int(v.value)
+
+
+def afx_decode_gemv(desc: afx_desc, container_dev, rows: int, cols: int, x_dev, y_dev, workspace_dev,
+                    stream=None, status_dev=None) -> None:
+    """x_dev: CUDA [batch][cols] 16-bit BF16; y_dev: CUDA float32 [batch][rows]."""
+    batch = x_dev.shape[0] if x_dev.dim() == 2 else 1
+    if y_dev.numel() < batch * rows:
+        raise ValueError("y_dev too small")
+    ws_bytes = workspace_dev.numel() * workspace_dev.element_size() if workspace_dev is not None else 0
+    _check("afx_decode_gemv", _lib.afx_decode_gemv(
+        ctypes.byref(desc), _dev_ptr(container_dev), rows, cols, _dev_ptr(x_dev), batch, _dev_ptr(y_dev),
+        _dev_ptr(workspace_dev), ws_bytes, _stream_handle(stream), _dev_ptr(status_dev)))
+
+
+def afx_stream_run(layers, dev_bufs, buf_bytes: int, compute_stream=None, copy_stream=None, status_dev=None) -> None:
+    """layers: list of (pinned host uint8 tensor, [afx_op, ...]); dev_bufs: list of CUDA uint8 tensors."""
+    arr = (afx_layer * len(layers))()
+    keep = []
+    for i, (blob, ops) in enumerate(layers):
+        op_arr = (afx_op * len(ops))(*ops)
+        keep.append(op_arr)
+        arr[i].host_blob = blob.data_ptr()
+        arr[i].blob_bytes = blob.numel() * blob.element_size()
+        arr[i].ops = op_arr
+        arr[i].n_ops = len(ops)
+    bufs = (ctypes.c_void_p * len(dev_bufs))(*[_dev_ptr(b) for b in dev_bufs])
+    _check("afx_stream_run", _lib.afx_stream_run(arr, len(layers), bufs, len(dev_bufs), buf_bytes,
+                                                  _stream_handle(compute_stream), _stream_handle(copy_stream),
+                                                  _dev_ptr(status_dev)))
+
+
+# ---- conveniences over the entry points ---------------------------------------
+
+def encode(w, chunk_bytes: int = 0, max_len: int = AFX_MAX_CODE_LEN) -> tuple[np.ndarray, afx_desc]:
+    """Container (uint8 numpy) and its description for the BF16 patterns w."""
+    a = _host_u16(w)
+    code = afx_build_code(a, max_len)
+    desc = afx_encode_bound(a.size, code, chunk_bytes, 0)
+    return afx_encode(a, code, desc), desc
+
+
+def desc_dict(d: afx_desc) -> dict:
+    return {f: (list(getattr(d, f)) if f == "len" else int(getattr(d, f))) for f, _ in afx_desc._fields_}

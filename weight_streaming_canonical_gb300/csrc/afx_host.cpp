@@ -1,0 +1,403 @@
+// Host side of afx: exponent histogram, length-limited canonical code,
+// container planning, bit packing and header validation.
+//
+// The operation: "Why Weight Offloading Slows Inference", section
+// "Lossless compression: fewer bytes to read, more work to unpack" --
+// shorter codes for common BF16 exponent values (Huffman's
+// minimum-redundancy code, that page's reference [2]); sign and mantissa
+// stay raw.  Code lengths are capped at AFX_MAX_CODE_LEN bits with
+// package-merge (Larmore and Hirschberg 1990), which is optimal among
+// codes obeying the cap.
+#include <algorithm>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+#include "afx_internal.h"
+
+namespace {
+
+uint64_t round_up(uint64_t v, uint64_t m) { return (v + m - 1) / m * m; }
+
+void put_le(uint8_t* p, unsigned bytes, uint64_t v) {
+    for (unsigned i = 0; i < bytes; ++i) p[i] = static_cast<uint8_t>(v >> (8 * i));
+}
+
+uint64_t get_le(const uint8_t* p, unsigned bytes) {
+    uint64_t v = 0;
+    for (unsigned i = 0; i < bytes; ++i) v |= static_cast<uint64_t>(p[i]) << (8 * i);
+    return v;
+}
+
+unsigned worker_count(uint64_t n) {
+    unsigned hw = std::thread::hardware_concurrency();
+    if (hw == 0) hw = 1;
+    uint64_t by_size = n / (1u << 20) + 1;  // at least 1M weights per worker
+    return static_cast<unsigned>(std::min<uint64_t>({hw, 32, by_size}));
+}
+
+// Package-merge by level selection.  Lists are built bottom-up (the
+// deepest level holds the leaves; every shallower level merges the leaves
+// with packages of adjacent pairs from the level below).  Then 2(m-1)
+// items are selected at the top level; a selected leaf adds one to its
+// symbol's length, and p selected packages select the first 2p items one
+// level down.
+struct PmItem {
+    uint64_t weight;
+    int leaf;  // symbol of a leaf, -1 for a package
+};
+
+afx_status package_merge(const uint64_t count[256], uint32_t max_len, uint8_t len[256]) {
+    std::vector<int> syms;
+    for (int s = 0; s < 256; ++s)
+        if (count[s]) syms.push_back(s);
+    std::memset(len, 0, 256);
+    const size_t m = syms.size();
+    if (m <= 1) return AFX_OK;
+    if (max_len < 1 || max_len > AFX_MAX_CODE_LEN) return AFX_E_ARG;
+    if ((uint64_t{1} << max_len) < m) return AFX_E_ARG;
+    std::stable_sort(syms.begin(), syms.end(), [&](int a, int b) {
+        return count[a] != count[b] ? count[a] < count[b] : a < b;
+    });
+    std::vector<PmItem> leaves(m);
+    for (size_t i = 0; i < m; ++i) leaves[i] = {count[syms[i]], syms[i]};
+
+    // level[d] for d = 1..max_len; level[max_len] = leaves
+    std::vector<std::vector<PmItem>> level(max_len + 1);
+    level[max_len] = leaves;
+    for (uint32_t d = max_len - 1; d >= 1; --d) {
+        const std::vector<PmItem>& below = level[d + 1];
+        std::vector<PmItem> packages(below.size() / 2);
+        for (size_t i = 0; i < packages.size(); ++i)
+            packages[i] = {below[2 * i].weight + below[2 * i + 1].weight, -1};
+        std::vector<PmItem>& cur = level[d];
+        cur.reserve(m + packages.size());
+        size_t a = 0, b = 0;
+        while (a < m || b < packages.size()) {
+            bool take_leaf = b >= packages.size() || (a < m && leaves[a].weight <= packages[b].weight);
+            cur.push_back(take_leaf ? leaves[a++] : packages[b++]);
+        }
+        if (d == 1) break;
+    }
+    size_t select = 2 * (m - 1);
+    for (uint32_t d = 1; d <= max_len && select > 0; ++d) {
+        size_t packs = 0;
+        for (size_t i = 0; i < select; ++i) {
+            const PmItem& it = level[d][i];
+            if (it.leaf >= 0)
+                ++len[it.leaf];
+            else
+                ++packs;
+        }
+        select = 2 * packs;
+    }
+    return AFX_OK;
+}
+
+// Canonical codes: walk the symbols in (length, value) order; the next
+// code is the previous one plus one, shifted left by the length increase.
+void canonical_codes(const uint8_t len[256], uint32_t code[256]) {
+    std::vector<int> order;
+    for (int s = 0; s < 256; ++s) {
+        code[s] = 0;
+        if (len[s]) order.push_back(s);
+    }
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return len[a] < len[b]; });
+    uint32_t c = 0;
+    unsigned prev = 0;
+    for (size_t i = 0; i < order.size(); ++i) {
+        unsigned l = len[order[i]];
+        if (i == 0)
+            c = 0;
+        else
+            c = (c + 1) << (l - prev);
+        code[order[i]] = c;
+        prev = l;
+    }
+}
+
+bool geometry_ok(uint32_t T, uint32_t C) {
+    bool t_ok = T == 4 || T == 8 || T == 16 || T == 32 || T == 64;
+    return t_ok && C >= 32 && C <= 1024 && C % 32 == 0;
+}
+
+void layout(uint64_t n, uint64_t total_bits, uint32_t T, uint32_t C, afx_desc* d) {
+    d->n = n;
+    d->total_bits = total_bits;
+    d->chunk_bytes = T;
+    d->block_chunks = C;
+    const uint64_t chunk_bits = 8ull * T;
+    d->n_chunks = (total_bits + chunk_bits - 1) / chunk_bits;
+    d->n_blocks = (d->n_chunks + C - 1) / C;
+    d->off_exp = AFX_HEADER_BYTES;
+    d->exp_bytes = round_up(d->n_chunks * T, 16) + 16;
+    d->off_sm = round_up(d->off_exp + d->exp_bytes, 256);
+    d->off_chunk = round_up(d->off_sm + n, 256);
+    d->off_block = round_up(d->off_chunk + 2 * d->n_chunks, 256);
+    d->container_bytes = round_up(d->off_block + 8 * (d->n_blocks + 1), 256);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* afx_status_string(afx_status s) {
+    switch (s) {
+        case AFX_OK: return "ok";
+        case AFX_E_ARG: return "invalid argument";
+        case AFX_E_FORMAT: return "invalid container format";
+        case AFX_E_CORRUPT: return "corrupt stream";
+        case AFX_E_CUDA: return "CUDA error";
+        case AFX_E_NOSPACE: return "buffer too small";
+        case AFX_E_TIMEOUT: return "timed out";
+    }
+    return "unknown status";
+}
+
+afx_status afx_build_code(const uint16_t* w, uint64_t n, uint32_t max_len, afx_code* out) {
+    if (!out || (n && !w)) return AFX_E_ARG;
+    std::memset(out, 0, sizeof(*out));
+    const unsigned workers = worker_count(n);
+    std::vector<std::vector<uint64_t>> part(workers, std::vector<uint64_t>(256, 0));
+    auto count_range = [&](unsigned k) {
+        uint64_t lo = n * k / workers, hi = n * (k + 1) / workers;
+        uint64_t* h = part[k].data();
+        for (uint64_t i = lo; i < hi; ++i) ++h[(w[i] >> 7) & 0xFFu];
+    };
+    if (workers == 1) {
+        count_range(0);
+    } else {
+        std::vector<std::thread> pool;
+        for (unsigned k = 0; k < workers; ++k) pool.emplace_back(count_range, k);
+        for (auto& t : pool) t.join();
+    }
+    for (unsigned k = 0; k < workers; ++k)
+        for (int s = 0; s < 256; ++s) out->count[s] += part[k][s];
+    for (int s = 0; s < 256; ++s)
+        if (out->count[s]) {
+            ++out->nsym;
+            out->fill = static_cast<uint32_t>(s);
+        }
+    if (out->nsym != 1) out->fill = 0;
+    afx_status st = package_merge(out->count, max_len, out->len);
+    if (st != AFX_OK) return st;
+    canonical_codes(out->len, out->code);
+    for (int s = 0; s < 256; ++s) out->max_len = std::max<uint32_t>(out->max_len, out->len[s]);
+    return AFX_OK;
+}
+
+afx_status afx_encode_bound(uint64_t n, const afx_code* code, uint32_t T, uint32_t C, afx_desc* out) {
+    if (!code || !out) return AFX_E_ARG;
+    if (C == 0) C = 256;
+    uint64_t total_bits = 0, present = 0;
+    unsigned min_len = 255;
+    for (int s = 0; s < 256; ++s) {
+        if (!code->count[s]) continue;
+        ++present;
+        total_bits += code->count[s] * code->len[s];
+        min_len = std::min<unsigned>(min_len, code->len[s]);
+    }
+    uint64_t counted = 0;
+    for (int s = 0; s < 256; ++s) counted += code->count[s];
+    if (counted != n || present != code->nsym) return AFX_E_ARG;
+    if (present >= 2 && min_len == 0) return AFX_E_ARG;
+    if (present <= 1) min_len = 1;
+    if (T == 0) {
+        // Largest of 32, 16, 8, 4 whose worst case fits the block capacity.
+        T = 32;
+        while (T > 4 && 8ull * T * C > static_cast<uint64_t>(AFX_BLOCK_CAPACITY) * min_len) T /= 2;
+    }
+    if (!geometry_ok(T, C)) return AFX_E_ARG;
+    if (8ull * T * C > static_cast<uint64_t>(AFX_BLOCK_CAPACITY) * min_len) return AFX_E_ARG;
+    std::memset(out, 0, sizeof(*out));
+    layout(n, total_bits, T, C, out);
+    out->nsym = code->nsym;
+    out->fill = code->nsym == 1 ? code->fill : 0;
+    out->max_len = code->nsym >= 2 ? code->max_len : 0;
+    std::memcpy(out->len, code->len, 256);
+    return AFX_OK;
+}
+
+afx_status afx_encode(const uint16_t* w, uint64_t n, const afx_code* code, const afx_desc* d, uint8_t* dst,
+                      uint64_t dst_bytes) {
+    if (!code || !d || !dst || (n && !w)) return AFX_E_ARG;
+    if (d->n != n || !geometry_ok(d->chunk_bytes, d->block_chunks)) return AFX_E_ARG;
+    if (dst_bytes < d->container_bytes) return AFX_E_NOSPACE;
+    afx_desc check;
+    layout(n, d->total_bits, d->chunk_bytes, d->block_chunks, &check);
+    if (check.container_bytes != d->container_bytes || check.off_block != d->off_block) return AFX_E_ARG;
+    if (std::memcmp(d->len, code->len, 256) != 0) return AFX_E_ARG;
+    std::memset(dst, 0, d->container_bytes);
+
+    uint8_t* h = dst;
+    put_le(h + 0, 4, AFX_MAGIC);
+    put_le(h + 4, 2, 1);
+    put_le(h + 6, 2, AFX_HEADER_BYTES);
+    put_le(h + 8, 8, d->n);
+    put_le(h + 16, 8, d->total_bits);
+    put_le(h + 24, 4, d->chunk_bytes);
+    put_le(h + 28, 4, d->block_chunks);
+    put_le(h + 32, 8, d->n_chunks);
+    put_le(h + 40, 8, d->n_blocks);
+    put_le(h + 48, 8, d->off_exp);
+    put_le(h + 56, 8, d->exp_bytes);
+    put_le(h + 64, 8, d->off_sm);
+    put_le(h + 72, 8, d->off_chunk);
+    put_le(h + 80, 8, d->off_block);
+    put_le(h + 88, 8, d->container_bytes);
+    put_le(h + 96, 4, d->max_len);
+    put_le(h + 100, 4, d->nsym);
+    put_le(h + 104, 4, d->fill);
+    std::memcpy(h + 256, code->len, 256);
+
+    uint8_t* sm = dst + d->off_sm;
+    for (uint64_t i = 0; i < n; ++i) sm[i] = static_cast<uint8_t>(((w[i] >> 8) & 0x80u) | (w[i] & 0x7Fu));
+
+    if (d->nsym <= 1) {
+        for (uint64_t i = 0; i < n; ++i)
+            if (((w[i] >> 7) & 0xFFu) != d->fill) return AFX_E_ARG;
+        if (d->total_bits != 0) return AFX_E_ARG;
+        put_le(dst + d->off_block, 8, n);
+        return AFX_OK;
+    }
+
+    // Bit packing into u32 words, most significant bit first, with the
+    // chunk index updated as each codeword starts.
+    uint8_t* words = dst + d->off_exp;
+    uint8_t* chunk_index = dst + d->off_chunk;
+    const unsigned chunk_shift = static_cast<unsigned>(__builtin_ctz(8u * d->chunk_bytes));
+    uint64_t acc = 0;
+    unsigned acc_bits = 0;
+    uint64_t pos = 0, word_i = 0;
+    uint64_t cur_chunk = ~uint64_t{0};
+    uint32_t cur_count = 0, cur_gap = 0;
+    auto flush_chunk = [&]() {
+        if (cur_chunk != ~uint64_t{0}) put_le(chunk_index + 2 * cur_chunk, 2, cur_gap | (cur_count << 5));
+    };
+    for (uint64_t i = 0; i < n; ++i) {
+        const unsigned e = (w[i] >> 7) & 0xFFu;
+        const unsigned l = code->len[e];
+        if (l == 0) return AFX_E_ARG;
+        const uint64_t chunk = pos >> chunk_shift;
+        if (chunk != cur_chunk) {
+            flush_chunk();
+            cur_chunk = chunk;
+            cur_count = 0;
+            cur_gap = static_cast<uint32_t>(pos - (chunk << chunk_shift));
+        }
+        ++cur_count;
+        acc = (acc << l) | code->code[e];
+        acc_bits += l;
+        pos += l;
+        if (acc_bits >= 32) {
+            acc_bits -= 32;
+            put_le(words + 4 * word_i++, 4, static_cast<uint32_t>(acc >> acc_bits));
+            acc &= (uint64_t{1} << acc_bits) - 1;
+        }
+    }
+    flush_chunk();
+    if (acc_bits) put_le(words + 4 * word_i, 4, static_cast<uint32_t>(acc << (32 - acc_bits)));
+    if (pos != d->total_bits) return AFX_E_ARG;
+
+    // Block index: weights before each block's first chunk.
+    uint8_t* block_index = dst + d->off_block;
+    uint64_t before = 0;
+    for (uint64_t b = 0; b < d->n_blocks; ++b) {
+        put_le(block_index + 8 * b, 8, before);
+        const uint64_t c_end = std::min<uint64_t>((b + 1) * d->block_chunks, d->n_chunks);
+        for (uint64_t c = b * d->block_chunks; c < c_end; ++c) before += get_le(chunk_index + 2 * c, 2) >> 5;
+    }
+    put_le(block_index + 8 * d->n_blocks, 8, n);
+    return before == n ? AFX_OK : AFX_E_ARG;
+}
+
+afx_status afx_parse_header(const uint8_t* h, uint64_t bytes, afx_desc* out) {
+    if (!h || !out || bytes < AFX_HEADER_BYTES) return AFX_E_ARG;
+    if (get_le(h, 4) != AFX_MAGIC || get_le(h + 4, 2) != 1 || get_le(h + 6, 2) != AFX_HEADER_BYTES)
+        return AFX_E_FORMAT;
+    afx_desc d;
+    std::memset(&d, 0, sizeof d);
+    const uint64_t n = get_le(h + 8, 8), total_bits = get_le(h + 16, 8);
+    const uint32_t T = static_cast<uint32_t>(get_le(h + 24, 4)), C = static_cast<uint32_t>(get_le(h + 28, 4));
+    if (!geometry_ok(T, C)) return AFX_E_FORMAT;
+    if (n > (uint64_t{1} << 48) || total_bits > 24 * n) return AFX_E_FORMAT;
+    layout(n, total_bits, T, C, &d);
+    if (get_le(h + 32, 8) != d.n_chunks || get_le(h + 40, 8) != d.n_blocks || get_le(h + 48, 8) != d.off_exp ||
+        get_le(h + 56, 8) != d.exp_bytes || get_le(h + 64, 8) != d.off_sm || get_le(h + 72, 8) != d.off_chunk ||
+        get_le(h + 80, 8) != d.off_block || get_le(h + 88, 8) != d.container_bytes)
+        return AFX_E_FORMAT;
+    for (unsigned i = 108; i < 256; ++i)
+        if (h[i]) return AFX_E_FORMAT;
+    d.max_len = static_cast<uint32_t>(get_le(h + 96, 4));
+    d.nsym = static_cast<uint32_t>(get_le(h + 100, 4));
+    d.fill = static_cast<uint32_t>(get_le(h + 104, 4));
+    std::memcpy(d.len, h + 256, 256);
+    unsigned longest = 0, coded = 0;
+    uint64_t kraft = 0;
+    for (int s = 0; s < 256; ++s) {
+        if (d.len[s] > AFX_MAX_CODE_LEN) return AFX_E_FORMAT;
+        if (d.len[s]) {
+            ++coded;
+            kraft += uint64_t{1} << (AFX_MAX_CODE_LEN - d.len[s]);
+        }
+        longest = std::max<unsigned>(longest, d.len[s]);
+    }
+    if (d.max_len != longest) return AFX_E_FORMAT;
+    if (d.nsym >= 2) {
+        if (coded != d.nsym || kraft != (uint64_t{1} << AFX_MAX_CODE_LEN) || d.fill != 0) return AFX_E_FORMAT;
+        if (total_bits < n || total_bits == 0) return AFX_E_FORMAT;
+        unsigned min_len = 255;
+        for (int s = 0; s < 256; ++s)
+            if (d.len[s]) min_len = std::min<unsigned>(min_len, d.len[s]);
+        if (8ull * T * C > static_cast<uint64_t>(AFX_BLOCK_CAPACITY) * min_len) return AFX_E_FORMAT;
+    } else {
+        if (coded != 0 || total_bits != 0 || d.fill > 255) return AFX_E_FORMAT;
+        if (d.nsym == 0 && (n != 0 || d.fill != 0)) return AFX_E_FORMAT;
+        if (d.nsym == 1 && n == 0) return AFX_E_FORMAT;
+    }
+    *out = d;
+    return AFX_OK;
+}
+
+afx_status afx_check_desc(const afx_desc* d) {
+    if (!d) return AFX_E_ARG;
+    if (!geometry_ok(d->chunk_bytes, d->block_chunks)) return AFX_E_FORMAT;
+    if (d->n > (uint64_t{1} << 48) || d->total_bits > 24 * d->n) return AFX_E_FORMAT;
+    afx_desc L;
+    layout(d->n, d->total_bits, d->chunk_bytes, d->block_chunks, &L);
+    if (L.n_chunks != d->n_chunks || L.n_blocks != d->n_blocks || L.off_exp != d->off_exp ||
+        L.exp_bytes != d->exp_bytes || L.off_sm != d->off_sm || L.off_chunk != d->off_chunk ||
+        L.off_block != d->off_block || L.container_bytes != d->container_bytes)
+        return AFX_E_FORMAT;
+    unsigned longest = 0, coded = 0, min_len = 255;
+    uint64_t kraft = 0;
+    for (int s = 0; s < 256; ++s) {
+        if (d->len[s] > AFX_MAX_CODE_LEN) return AFX_E_FORMAT;
+        if (d->len[s]) {
+            ++coded;
+            kraft += uint64_t{1} << (AFX_MAX_CODE_LEN - d->len[s]);
+            min_len = std::min<unsigned>(min_len, d->len[s]);
+        }
+        longest = std::max<unsigned>(longest, d->len[s]);
+    }
+    if (d->max_len != longest) return AFX_E_FORMAT;
+    if (d->nsym >= 2) {
+        if (coded != d->nsym || kraft != (uint64_t{1} << AFX_MAX_CODE_LEN)) return AFX_E_FORMAT;
+        if (d->total_bits < d->n) return AFX_E_FORMAT;
+        if (8ull * d->chunk_bytes * d->block_chunks > static_cast<uint64_t>(AFX_BLOCK_CAPACITY) * min_len)
+            return AFX_E_FORMAT;
+    } else {
+        if (coded != 0 || d->total_bits != 0 || d->fill > 255) return AFX_E_FORMAT;
+        if (d->nsym == 1 && d->n == 0) return AFX_E_FORMAT;
+        if (d->nsym == 0 && d->n != 0) return AFX_E_FORMAT;
+    }
+    return AFX_OK;
+}
+
+afx_status afx_decode_gemv_workspace(const afx_desc* d, uint32_t batch, uint64_t* bytes) {
+    if (!d || !bytes || batch < 1 || batch > 4) return AFX_E_ARG;
+    *bytes = afx_gemv_workspace_bytes(d->n_blocks, batch);
+    return AFX_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,114 @@
+// Layer streaming: compressed layers move from pinned host memory to the GPU
+// on a copy stream while the previous layer's ops run on a compute stream.
+//
+// "Why Weight Offloading Slows Inference", section "Loading during
+// computation" and Figure 2: while the GPU computes one layer the next is
+// already loading, and a load costs nothing only if it finishes before the
+// GPU needs the weights.  "Memory requirements of language model inference
+// on a consumer GPU", section "Loading one part of the model at a time":
+// load a layer, use it, release its memory, go on to the next.  Here the
+// copy carries the compressed container, so the link moves fewer bytes and
+// the unpack runs on the GPU after the copy.
+//
+// Ordering uses CUDA events only: buffer l % n_bufs is refilled after the
+// ops that read it have finished, and a layer's ops start after its copy.
+// The host never waits.
+#include <cuda_runtime.h>
+
+#include <vector>
+
+#include "afx_internal.h"
+
+namespace {
+
+struct EventSet {
+    std::vector<cudaEvent_t> ev;
+    ~EventSet() {
+        for (cudaEvent_t e : ev)
+            if (e) cudaEventDestroy(e);
+    }
+    bool create(size_t n) {
+        ev.assign(n, nullptr);
+        for (auto& e : ev)
+            if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return false;
+        return true;
+    }
+};
+
+#define AFX_STREAM_TRY(call, what)                                        \
+    do {                                                                  \
+        const cudaError_t e_ = (call);                                    \
+        if (e_ != cudaSuccess) return afx_fail(AFX_E_CUDA, (what), e_);   \
+    } while (0)
+
+bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+afx_status check_layer(const afx_layer& L, uint64_t buf_bytes) {
+    if ((!L.host_blob && L.blob_bytes) || (!L.ops && L.n_ops)) return AFX_E_ARG;
+    if (L.blob_bytes > buf_bytes) return AFX_E_NOSPACE;
+    for (uint32_t i = 0; i < L.n_ops; ++i) {
+        const afx_op& op = L.ops[i];
+        afx_status st = afx_check_desc(&op.desc);
+        if (st != AFX_OK) return st;
+        if (op.offset % 256 != 0 || op.offset > L.blob_bytes || op.desc.container_bytes > L.blob_bytes - op.offset)
+            return AFX_E_ARG;
+        if (op.kind == AFX_OP_DECODE) {
+            if (op.desc.n && !op.out_dev) return AFX_E_ARG;
+        } else if (op.kind == AFX_OP_GEMV) {
+            if (!op.x_dev || !op.out_dev || op.batch < 1 || op.batch > 4) return AFX_E_ARG;
+            if (static_cast<uint64_t>(op.rows) * op.cols != op.desc.n) return AFX_E_ARG;
+        } else {
+            return AFX_E_ARG;
+        }
+    }
+    return AFX_OK;
+}
+
+}  // namespace
+
+extern "C" afx_status afx_stream_run(const afx_layer* layers, uint32_t n_layers, void* const* dev_bufs,
+                                     uint32_t n_bufs, uint64_t buf_bytes, afx_stream_t compute_stream,
+                                     afx_stream_t copy_stream, int32_t* status_dev) {
+    if ((!layers && n_layers) || !dev_bufs || n_bufs < 2) return AFX_E_ARG;
+    for (uint32_t k = 0; k < n_bufs; ++k)
+        if (!dev_bufs[k] || !aligned256(dev_bufs[k])) return AFX_E_ARG;
+    for (uint32_t l = 0; l < n_layers; ++l) {
+        afx_status st = check_layer(layers[l], buf_bytes);
+        if (st != AFX_OK) return st;
+    }
+    cudaStream_t compute = reinterpret_cast<cudaStream_t>(compute_stream);
+    cudaStream_t copy = reinterpret_cast<cudaStream_t>(copy_stream);
+    EventSet copied, consumed, entry;
+    if (!copied.create(n_bufs) || !consumed.create(n_bufs) || !entry.create(1))
+        return afx_fail(AFX_E_CUDA, "cudaEventCreateWithFlags", static_cast<int>(cudaGetLastError()));
+    // The buffers may still be read by work an earlier call queued on the
+    // compute stream: the first copy of this call waits for all of it.
+    AFX_STREAM_TRY(cudaEventRecord(entry.ev[0], compute), "cudaEventRecord");
+    AFX_STREAM_TRY(cudaStreamWaitEvent(copy, entry.ev[0], 0), "cudaStreamWaitEvent");
+
+    for (uint32_t l = 0; l < n_layers; ++l) {
+        const afx_layer& L = layers[l];
+        const uint32_t k = l % n_bufs;
+        uint8_t* buf = static_cast<uint8_t*>(dev_bufs[k]);
+        if (l >= n_bufs) AFX_STREAM_TRY(cudaStreamWaitEvent(copy, consumed.ev[k], 0), "cudaStreamWaitEvent");
+        if (L.blob_bytes)
+            AFX_STREAM_TRY(cudaMemcpyAsync(buf, L.host_blob, L.blob_bytes, cudaMemcpyHostToDevice, copy),
+                           "cudaMemcpyAsync");
+        AFX_STREAM_TRY(cudaEventRecord(copied.ev[k], copy), "cudaEventRecord");
+        AFX_STREAM_TRY(cudaStreamWaitEvent(compute, copied.ev[k], 0), "cudaStreamWaitEvent");
+        for (uint32_t i = 0; i < L.n_ops; ++i) {
+            const afx_op& op = L.ops[i];
+            const void* container = buf + op.offset;
+            afx_status st;
+            if (op.kind == AFX_OP_DECODE)
+                st = afx_decode(&op.desc, container, static_cast<uint16_t*>(op.out_dev), compute_stream, status_dev);
+            else
+                st = afx_decode_gemv(&op.desc, container, op.rows, op.cols, op.x_dev, op.batch,
+                                     static_cast<float*>(op.out_dev), op.workspace_dev, op.workspace_bytes,
+                                     compute_stream, status_dev);
+            if (st != AFX_OK) return st;
+        }
+        AFX_STREAM_TRY(cudaEventRecord(consumed.ev[k], compute), "cudaEventRecord");
+    }
+    return AFX_OK;
+}
