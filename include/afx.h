@@ -152,6 +152,17 @@ afx_status afx_parse_header(const uint8_t* header_host, uint64_t bytes, afx_desc
 afx_status afx_decode(const afx_desc* desc, const void* container_dev, uint16_t* out_dev,
                       afx_stream_t stream, int32_t* status_dev);
 
+/* Restores several containers in one launch: outs_dev[i] gets the weights
+ * of containers_dev[i] described by descs[i], for i < count.  The tiles of
+ * all containers are shared out over one persistent grid, so small tensors
+ * do not leave the GPU idle and the per-launch cost is paid once.  Same
+ * arguments, alignment, ownership and errors as afx_decode, per container.
+ * Cites: as afx_decode; and "Memory requirements of language model
+ * inference on a consumer GPU", section "Loading one part of the model at a
+ * time" -- a layer's weights are needed together. */
+afx_status afx_decode_batch(const afx_desc* descs, const void* const* containers_dev, uint16_t* const* outs_dev,
+                            uint32_t count, afx_stream_t stream, int32_t* status_dev);
+
 /* Device workspace (bytes) that afx_decode_gemv needs for this container
  * and batch: one float per batch row for the two partial output rows of
  * every block. */
@@ -172,6 +183,17 @@ afx_status afx_decode_gemv_workspace(const afx_desc* desc, uint32_t batch, uint6
 afx_status afx_decode_gemv(const afx_desc* desc, const void* container_dev, uint32_t rows, uint32_t cols,
                            const uint16_t* x_dev, uint32_t batch, float* y_dev, void* workspace_dev,
                            uint64_t workspace_bytes, afx_stream_t stream, int32_t* status_dev);
+
+/* Several fused restore + GEMV products in one launch, all with the same
+ * batch (1..4): for i < count, ys_dev[i] = W_i x_i with W_i the weights of
+ * containers_dev[i] viewed as [rows[i]][cols[i]] and x_i = xs_dev[i]
+ * ([batch][cols[i]]).  workspaces_dev[i] holds workspace_bytes[i] >=
+ * afx_decode_gemv_workspace(descs[i], batch).  Same rules and errors as
+ * afx_decode_gemv, per product. */
+afx_status afx_decode_gemv_batch(const afx_desc* descs, const void* const* containers_dev, const uint32_t* rows,
+                                 const uint32_t* cols, const uint16_t* const* xs_dev, uint32_t batch,
+                                 float* const* ys_dev, void* const* workspaces_dev, const uint64_t* workspace_bytes,
+                                 uint32_t count, afx_stream_t stream, int32_t* status_dev);
 
 /* One tensor of a streamed layer. */
 typedef enum afx_op_kind { AFX_OP_DECODE = 0, AFX_OP_GEMV = 1 } afx_op_kind;
@@ -204,7 +226,8 @@ typedef struct afx_layer {
  * (>= every blob_bytes), 256-byte aligned; they may be passed again to a
  * later call, whose first copy waits for all work already queued on
  * compute_stream.  Enqueues everything and returns; synchronise
- * compute_stream to wait for the results.
+ * compute_stream to wait for the results.  Consecutive ops of one kind
+ * (and, for GEMV, one batch size) run as one batch launch.
  * Cites: "Why Weight Offloading Slows Inference", section "Loading during
  * computation" and Figure 2 (load layer l+1 while layer l computes; a load
  * is free only if it finishes before the GPU needs it), and "Memory

@@ -168,3 +168,52 @@ def test_host_side_argument_errors(afx):
     d32 = afx.afx_parse_header(c32)
     with pytest.raises(afx.AfxError):  # the decoder runs 256 chunks per block
         afx.afx_decode(d32, torch.from_numpy(c32).cuda(), out)
+
+
+# ---- several containers in one launch ------------------------------------------
+
+def test_batch_of_mixed_tensors_in_one_launch(afx):
+    import torch
+    tensors = [synth.normal(1_000_003, seed=1), synth.layer_tensor("input_layernorm", seed=2),
+               np.full(4099, 0x3F80, np.uint16), synth.adversarial(300_001, seed=3), synth.normal(7, seed=4),
+               np.zeros(0, np.uint16), synth.normal(2_000_000, 1.0, 0.05, seed=5)]
+    encoded = [afx.encode(w) for w in tensors]
+    devs = [torch.from_numpy(c).cuda() for c, _ in encoded]
+    outs = [torch.full((max(1, w.size),), 0x5A5A, dtype=torch.int16, device="cuda") for w in tensors]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    afx.afx_decode_batch([d for _, d in encoded], devs, outs, status_dev=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    for w, o in zip(tensors, outs):
+        got = o.cpu().numpy().view(np.uint16)
+        assert np.array_equal(got[:w.size], w)
+
+
+def test_batch_longer_than_one_launch(afx):
+    import torch
+    tensors = [synth.normal(50_000 + 37 * i, seed=100 + i) for i in range(37)]  # more than 16 per launch
+    encoded = [afx.encode(w) for w in tensors]
+    devs = [torch.from_numpy(c).cuda() for c, _ in encoded]
+    outs = [torch.empty(w.size, dtype=torch.int16, device="cuda") for w in tensors]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    afx.afx_decode_batch([d for _, d in encoded], devs, outs, status_dev=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    for w, o in zip(tensors, outs):
+        assert np.array_equal(o.cpu().numpy().view(np.uint16), w)
+
+
+@pytest.mark.slow
+def test_qwen3_layer_in_one_launch(afx):
+    import torch
+    layer = synth.layer(seed=0)
+    encoded = [afx.encode(t.reshape(-1)) for t in layer.values()]
+    devs = [torch.from_numpy(c).cuda() for c, _ in encoded]
+    outs = [torch.empty(d.n, dtype=torch.int16, device="cuda") for _, d in encoded]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    afx.afx_decode_batch([d for _, d in encoded], devs, outs, status_dev=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    for (c, _), o in zip(encoded, outs):
+        ref, st = oracle.decode(c)
+        assert st == oracle.OK and np.array_equal(o.cpu().numpy().view(np.uint16), ref)

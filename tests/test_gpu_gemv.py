@@ -102,3 +102,27 @@ def test_qwen3_layer_matrices(afx, B):
         W = synth.layer_tensor(name, seed=0)
         x = synth.activations(B, shape[1], seed=10 + B)
         _check(afx, W, x)
+
+
+def test_gemv_batch_of_products_in_one_launch(afx):
+    import torch
+    shapes = [(96, 640), (640, 1024), (33, 5120), (1024, 72), (3, 200_000)]
+    B = 3
+    items = []
+    for i, (r, c) in enumerate(shapes):
+        W = synth.normal(r * c, seed=200 + i).reshape(r, c)
+        x = synth.activations(B, c, seed=300 + i)
+        cont, d = afx.encode(W.reshape(-1))
+        items.append((W, x, cont, d))
+    devs = [torch.from_numpy(cont).cuda() for _, _, cont, _ in items]
+    xs = [torch.from_numpy(x.view(np.int16)).cuda() for _, x, _, _ in items]
+    ys = [torch.full((B, r), float("nan"), dtype=torch.float32, device="cuda") for r, _ in shapes]
+    wss = [torch.empty(afx.afx_decode_gemv_workspace(d, B) // 4 + 4, dtype=torch.float32, device="cuda")
+           for _, _, _, d in items]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    afx.afx_decode_gemv_batch([d for *_, d in items], devs, shapes, xs, ys, wss, status_dev=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    for (W, x, _, _), y in zip(items, ys):
+        y_ref, A = oracle.gemv(W, x)
+        assert within_gemv_tolerance(y.cpu().numpy(), y_ref, A)

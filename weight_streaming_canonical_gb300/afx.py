@@ -98,6 +98,11 @@ _lib.afx_parse_header.argtypes = [_vp, _u64, ctypes.POINTER(afx_desc)]
 _lib.afx_decode.argtypes = [ctypes.POINTER(afx_desc), _vp, _vp, _vp, _i32p]
 _lib.afx_decode_gemv_workspace.argtypes = [ctypes.POINTER(afx_desc), _u32, ctypes.POINTER(ctypes.c_uint64)]
 _lib.afx_decode_gemv.argtypes = [ctypes.POINTER(afx_desc), _vp, _u32, _u32, _vp, _u32, _vp, _vp, _u64, _vp, _i32p]
+_PP = ctypes.POINTER(ctypes.c_void_p)
+_lib.afx_decode_batch.argtypes = [ctypes.POINTER(afx_desc), _PP, _PP, _u32, _vp, _i32p]
+_lib.afx_decode_gemv_batch.argtypes = [ctypes.POINTER(afx_desc), _PP, ctypes.POINTER(ctypes.c_uint32),
+                                       ctypes.POINTER(ctypes.c_uint32), _PP, _u32, _PP, _PP,
+                                       ctypes.POINTER(ctypes.c_uint64), _u32, _vp, _i32p]
 _lib.afx_stream_run.argtypes = [ctypes.POINTER(afx_layer), _u32, ctypes.POINTER(ctypes.c_void_p), _u32, _u64, _vp,
                                 _vp, _i32p]
 _lib.afx_last_error.argtypes = []
@@ -105,7 +110,8 @@ _lib.afx_last_error.restype = ctypes.c_char_p
 _lib.afx_status_string.argtypes = [ctypes.c_int]
 _lib.afx_status_string.restype = ctypes.c_char_p
 for _f in (_lib.afx_build_code, _lib.afx_encode_bound, _lib.afx_encode, _lib.afx_parse_header, _lib.afx_decode,
-           _lib.afx_decode_gemv_workspace, _lib.afx_decode_gemv, _lib.afx_stream_run):
+           _lib.afx_decode_batch, _lib.afx_decode_gemv_workspace, _lib.afx_decode_gemv, _lib.afx_decode_gemv_batch,
+           _lib.afx_stream_run):
     _f.restype = ctypes.c_int
 
 
@@ -189,6 +195,39 @@ def afx_decode(desc: afx_desc, container_dev, out_dev, stream=None, status_dev=N
         raise ValueError("out_dev must hold n 16-bit elements")
     _check("afx_decode", _lib.afx_decode(ctypes.byref(desc), _dev_ptr(container_dev), _dev_ptr(out_dev),
                                           _stream_handle(stream), _dev_ptr(status_dev)))
+
+
+def _ptrs(tensors) -> ctypes.Array:
+    return (ctypes.c_void_p * len(tensors))(*[_dev_ptr(t) for t in tensors])
+
+
+def afx_decode_batch(descs, containers_dev, outs_dev, stream=None, status_dev=None) -> None:
+    """Restore several containers in one launch (lists of equal length)."""
+    if not (len(descs) == len(containers_dev) == len(outs_dev)):
+        raise ValueError("descs, containers_dev and outs_dev must have the same length")
+    for d, o in zip(descs, outs_dev):
+        if o.numel() < d.n or o.element_size() != 2:
+            raise ValueError("every output must hold n 16-bit elements")
+    arr = (afx_desc * len(descs))(*descs)
+    _check("afx_decode_batch", _lib.afx_decode_batch(arr, _ptrs(containers_dev), _ptrs(outs_dev), len(descs),
+                                                      _stream_handle(stream), _dev_ptr(status_dev)))
+
+
+def afx_decode_gemv_batch(descs, containers_dev, shapes, xs_dev, ys_dev, workspaces_dev, stream=None,
+                          status_dev=None) -> None:
+    """Several fused restore+GEMV products in one launch; shapes = [(rows, cols)], one batch size for all."""
+    count = len(descs)
+    batch = xs_dev[0].shape[0] if xs_dev and xs_dev[0].dim() == 2 else 1
+    for x, y, (r, c) in zip(xs_dev, ys_dev, shapes):
+        if (x.shape[0] if x.dim() == 2 else 1) != batch or y.numel() < batch * r:
+            raise ValueError("every x must have the same batch and every y must hold batch * rows floats")
+    arr = (afx_desc * count)(*descs)
+    rows = (ctypes.c_uint32 * count)(*[r for r, _ in shapes])
+    cols = (ctypes.c_uint32 * count)(*[c for _, c in shapes])
+    wsb = (ctypes.c_uint64 * count)(*[w.numel() * w.element_size() for w in workspaces_dev])
+    _check("afx_decode_gemv_batch", _lib.afx_decode_gemv_batch(
+        arr, _ptrs(containers_dev), rows, cols, _ptrs(xs_dev), batch, _ptrs(ys_dev), _ptrs(workspaces_dev), wsb,
+        count, _stream_handle(stream), _dev_ptr(status_dev)))
 
 
 def afx_decode_gemv_workspace(desc: afx_desc, batch: int) -> int:

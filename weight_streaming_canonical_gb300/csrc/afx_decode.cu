@@ -1,6 +1,6 @@
 // sm_103a kernels of afx: restore BF16 weights from the exponent-coded
-// container, alone (afx_decode) or fused into a batch-1..4 GEMV
-// (afx_decode_gemv).
+// container, alone (afx_decode, afx_decode_batch) or fused into a batch-1..4
+// GEMV (afx_decode_gemv, afx_decode_gemv_batch).
 //
 // The operation: "Why Weight Offloading Slows Inference", section
 // "Lossless compression: fewer bytes to read, more work to unpack" -- every
@@ -8,28 +8,35 @@
 // sign and mantissa raw; the released bits are restored before compute.
 // This is the t_unpack term of that page's Eq. (1).
 //
-// Work decomposition (one CTA tile = one block of the container = 256
-// chunks of 8*T stream bits, persistent CTAs loop over tiles):
-//   1. stage the tile's stream words and chunk-index entries in shared
-//      memory;
+// Work decomposition.  One launch restores a list of tensors.  A tile is
+// one block of a container (256 chunks of 8*T stream bits); the tiles of
+// all tensors form one list, and each persistent CTA takes a contiguous
+// run of it, so it meets at most a few tensors.  For each tile:
+//   1. the tile's stream words, chunk entries and block-index pair arrive in
+//      shared memory by cp.async, issued one tile ahead (double buffer); the
+//      tile's sign|mantissa bytes are prefetched into L2 in one bulk request;
 //   2. each thread takes one chunk: the index gives the bit offset of its
 //      first codeword and how many codewords start in it; a warp-shuffle
 //      plus block prefix scan of those counts places every thread's run of
-//      outputs inside the tile;
-//   3. each thread decodes its codewords through a two-level table in
-//      shared memory (a 4096-entry table resolves every code of at most 12
-//      bits from a 12-bit peek; longer codes, up to 24 bits, fall back to a
-//      per-length canonical search) into a shared exponent buffer;
-//   4. the whole CTA joins exponents with the sign|mantissa bytes in
-//      aligned groups of 8 weights: 8-byte coalesced loads of
-//      sign|mantissa and 16-byte coalesced BF16 stores (or, fused, 8
-//      products per batch row with no store of the weights at all).
-// Every index read from the container is checked before it is used to
-// address shared or global memory; a bad value sets a status bit and the
-// tile is skipped.  No kernel waits on anything but __syncthreads.
+//      exponents inside the tile;
+//   3. each thread decodes its run from a 64-bit window of stream words
+//      through two tables rebuilt in shared memory whenever the tensor
+//      changes: a 4096-entry table that, from a 12-bit peek, yields up to
+//      three whole codes (their exponents and total length), and a
+//      4096-entry table of the first code's length for single steps; codes
+//      longer than 12 bits fall back to a per-length canonical search.
+//      Exponents are packed four to a word and stored as aligned words;
+//   4. the whole CTA joins exponents with sign|mantissa bytes in aligned
+//      groups of 8 weights: 8-byte coalesced loads and 16-byte coalesced
+//      BF16 stores (or, fused, 8 products per batch row, and the weights
+//      never reach global memory).
+// Every value read from the container is checked before it addresses
+// memory; a bad one sets a status bit and the tile is skipped.  The kernels
+// wait only on __syncthreads and cp.async groups.
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstddef>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -63,97 +70,241 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kLutBits = 12;
 constexpr int kLutSize = 1 << kLutBits;
 constexpr int kStageBytes = AFX_BLOCK_CAPACITY + 16;
-constexpr int kMaxBatch = 4;
+constexpr int kMaxBatch = 4;       // GEMV activation rows
+constexpr int kMaxTensors = 16;    // tensors per launch
+constexpr int kStreamPad = 32;     // stream bytes staged past a tile's own chunks
+constexpr int kChunkStage = kThreads + 8;  // chunk entries staged per tile (the next tile's first included)
 
 // Canonical decode tables, built on the host from the 256 code lengths.
-// In 24-bit left-aligned code space, all codes of length <= L lie in
-// [0, limit[L]); a 24-bit peek v therefore has the length L = the smallest L
-// with v < limit[L], and its exponent is sorted[base[L] + (v >> (24 - L))].
+// In 24-bit left-aligned code space all codes of length <= L lie in
+// [0, limit[L]); a 24-bit peek v has the length L = the smallest L with
+// v < limit[L], and its exponent is sorted[base[L] + (v >> (24 - L))].
 struct CodeTables {
     uint32_t limit[AFX_MAX_CODE_LEN + 1];
     int32_t base[AFX_MAX_CODE_LEN + 1];
     uint8_t sorted[256];
 };
 
-struct TileShared {
-    uint16_t lut[kLutSize];  // (length << 8) | exponent for codes <= 12 bits; 0 = longer code
+// One tensor of a launch.
+struct TensorArgs {
+    const uint32_t* exp_words;
+    const uint8_t* sm;
+    const uint16_t* chunk_index;
+    const uint64_t* block_index;
+    uint64_t n, n_chunks, n_blocks, exp_bytes;
+    uint64_t tile_begin;       // first tile of this tensor in the launch's tile list
+    uint32_t chunk_bytes;      // T
+    uint32_t rows_per_warp;    // GEMV: capacity of the per-warp partial table
+    uint16_t* out;             // restore: n BF16
+    const uint16_t* x;         // GEMV: [B][cols]
+    float* y;                  // GEMV: [B][rows]
+    float* ws;                 // GEMV: [n_blocks][2][B]
+    uint32_t rows, cols;
+    CodeTables tab;
+};
+
+struct LaunchArgs {
+    uint32_t count;
+    uint32_t max_chunk_bytes;
+    uint32_t max_rows_per_warp;
+    uint32_t pad;
+    uint64_t total_tiles;
+    int32_t* status;
+    TensorArgs t[kMaxTensors];
+};
+
+struct Shared {
+    uint32_t lut[kLutSize];   // up to 3 codes per 12-bit peek: bits 0-3 total length, 4-5 count, 8-31 exponents
+    uint8_t len0[kLutSize];   // length of the first code of a 12-bit peek (0: longer than 12 bits)
     uint32_t limit[AFX_MAX_CODE_LEN + 1];
     int32_t base[AFX_MAX_CODE_LEN + 1];
     uint8_t sorted[256];
-    uint16_t chunk[kThreads + 1];  // this tile's chunk entries plus the next tile's first
+    alignas(16) uint16_t chunk[2][kChunkStage];  // cp.async destinations: 16-byte aligned rows
+    alignas(16) uint64_t block_pair[2][2];
     uint32_t warp_total[kWarps];
     int32_t tile_ok;
-    uint8_t stage[kStageBytes];  // exponents of the tile, at (o - o0 + (o0 & 7))
-    // followed by the staged stream words (dynamic size)
+    alignas(16) uint8_t stage[kStageBytes];  // exponent of weight (o0 & ~7) + i at stage[i]
+    // dynamic part: stream[2][kThreads * max_T + kStreamPad], then GEMV partials
 };
 
-struct DecodeArgs {
-    const uint32_t* exp_words;   // exp section
-    const uint8_t* sm;           // sign|mantissa section
-    const uint16_t* chunk_index;
-    const uint64_t* block_index;
-    uint64_t n;
-    uint64_t n_chunks;
-    uint64_t n_blocks;
-    uint64_t exp_bytes;
-    uint32_t chunk_bytes;        // T
-    int32_t* status;
-};
+constexpr size_t shared_fixed_bytes() { return (sizeof(Shared) + 15) & ~size_t(15); }
+static_assert(offsetof(Shared, chunk) % 16 == 0 && (kChunkStage * 2) % 16 == 0, "cp.async rows must be 16-byte aligned");
+static_assert(offsetof(Shared, stage) % 16 == 0, "stage must be 16-byte aligned");
+
+// ---- small device helpers ------------------------------------------------------
 
 __device__ __forceinline__ void raise_status(int32_t* status, int32_t bits) {
     if (status) atomicOr(status, bits);
 }
 
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(s), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// One request that pulls [p, p + bytes) into L2 (p and bytes multiples of 16).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // BF16 from exponent and sign|mantissa: sign to bit 15, exponent to bits
-// 7..14, mantissa to bits 0..6.  Four weights per call: e4 and s4 hold four
-// exponent and four sign|mantissa bytes; the result is two u32 of packed
-// BF16 pairs.  byte_perm interleaves to (e << 8) | s per 16-bit lane; then
-// s bits 0..6 stay, e moves down one bit to 7..14, s bit 7 moves to 15.
+// 7..14, mantissa to bits 0..6.  byte_perm interleaves four sign|mantissa
+// bytes s and four exponents e into (e << 8) | s per 16-bit lane; then s
+// bits 0..6 stay, e moves down one bit, s bit 7 moves up to bit 15.
 __device__ __forceinline__ uint32_t join_pair(uint32_t x) {
     return (x & 0x007F007Fu) | ((x >> 1) & 0x7F807F80u) | ((x << 8) & 0x80008000u);
 }
 
-__device__ __forceinline__ uint2 join4(uint32_t e4, uint32_t s4) {
-    uint2 r;
-    r.x = join_pair(__byte_perm(s4, e4, 0x5140));
-    r.y = join_pair(__byte_perm(s4, e4, 0x7362));
-    return r;
+__device__ __forceinline__ uint4 join8(uint2 e8, uint2 s8) {
+    uint4 v;
+    v.x = join_pair(__byte_perm(s8.x, e8.x, 0x5140));
+    v.y = join_pair(__byte_perm(s8.x, e8.x, 0x7362));
+    v.z = join_pair(__byte_perm(s8.y, e8.y, 0x5140));
+    v.w = join_pair(__byte_perm(s8.y, e8.y, 0x7362));
+    return v;
 }
 
 __device__ __forceinline__ uint16_t join1(uint32_t e, uint32_t s) {
     return static_cast<uint16_t>(((s & 0x80u) << 8) | (e << 7) | (s & 0x7Fu));
 }
 
-__device__ void build_tables(TileShared& sh, const CodeTables& tab) {
+// ---- decode tables ---------------------------------------------------------------
+//
+// Rebuilt whenever a CTA moves to another tensor.  Step 1 gives every 12-bit
+// peek its first code (exponent, length) using the canonical limits; a
+// thread's 16 consecutive peeks have non-decreasing lengths, so one search
+// plus short advances suffices.  The (length << 8 | exponent) pairs go to a
+// scratch table in the stage buffer (free between tiles).  Step 2 chains up
+// to three first codes per peek: after the first code of length L1, the
+// remaining 12 - L1 peek bits start the second code, which counts only if
+// it ends within the 12 bits, and likewise for the third.
+
+__device__ void build_tables(Shared& sh, const CodeTables& tab) {
     const int tid = threadIdx.x;
     for (int i = tid; i <= AFX_MAX_CODE_LEN; i += kThreads) {
         sh.limit[i] = tab.limit[i];
         sh.base[i] = tab.base[i];
     }
     for (int i = tid; i < 256; i += kThreads) sh.sorted[i] = tab.sorted[i];
-    for (int p = tid; p < kLutSize; p += kThreads) {
-        const uint32_t v = static_cast<uint32_t>(p) << (24 - kLutBits);
-        int len = 0;  // smallest L <= 12 with v < limit[L]; 0 = the code is longer
-#pragma unroll
-        for (int L = kLutBits; L >= 1; --L)
-            if (v < tab.limit[L]) len = L;
-        uint16_t entry = 0;
-        if (len) {
-            const uint32_t sym = tab.sorted[tab.base[len] + static_cast<int32_t>(v >> (24 - len))];
-            entry = static_cast<uint16_t>((len << 8) | sym);
+    uint16_t* first = reinterpret_cast<uint16_t*>(sh.stage);  // scratch: 8 KB
+    constexpr int kPer = kLutSize / kThreads;
+    {
+        const int p0 = tid * kPer;
+        int L = 1;
+        while (L <= kLutBits && (static_cast<uint32_t>(p0) << (24 - kLutBits)) >= tab.limit[L]) ++L;
+        for (int j = 0; j < kPer; ++j) {
+            const uint32_t p = static_cast<uint32_t>(p0 + j);
+            const uint32_t v = p << (24 - kLutBits);
+            while (L <= kLutBits && v >= tab.limit[L]) ++L;
+            uint16_t e = 0;
+            if (L <= kLutBits)
+                e = static_cast<uint16_t>((L << 8) | tab.sorted[tab.base[L] + static_cast<int32_t>(v >> (24 - L))]);
+            first[p] = e;
+            sh.len0[p] = static_cast<uint8_t>(e >> 8);
+        }
+    }
+    __syncthreads();
+    for (int j = 0; j < kPer; ++j) {
+        const uint32_t p = static_cast<uint32_t>(tid * kPer + j);
+        const uint32_t f1 = first[p];
+        const uint32_t l1 = f1 >> 8;
+        uint32_t entry = 0;
+        if (l1) {
+            uint32_t bits = l1, count = 1, syms = f1 & 0xFFu;
+            const uint32_t f2 = first[(p << l1) & (kLutSize - 1)];
+            const uint32_t l2 = f2 >> 8;
+            if (l2 && bits + l2 <= kLutBits) {
+                bits += l2;
+                syms |= (f2 & 0xFFu) << 8;
+                count = 2;
+                const uint32_t f3 = first[(p << bits) & (kLutSize - 1)];
+                const uint32_t l3 = f3 >> 8;
+                if (l3 && bits + l3 <= kLutBits) {
+                    bits += l3;
+                    syms |= (f3 & 0xFFu) << 16;
+                    count = 3;
+                }
+            }
+            entry = bits | (count << 4) | (syms << 8);
         }
         sh.lut[p] = entry;
     }
+    __syncthreads();
 }
 
-// Exclusive block-wide scan of one count per thread; returns this thread's
-// offset and writes the total into *total.
-__device__ __forceinline__ uint32_t block_exclusive_scan(TileShared& sh, uint32_t v, uint32_t* total) {
+// One code from a 32-bit window: exponent, length in len (0 on a bad code).
+__device__ __forceinline__ uint32_t decode_one(const Shared& sh, uint32_t win, uint32_t& len) {
+    const uint32_t p = win >> (32 - kLutBits);
+    uint32_t L = sh.len0[p];
+    if (L) {
+        len = L;
+        return (sh.lut[p] >> 8) & 0xFFu;
+    }
+    const uint32_t v = win >> 8;
+    L = kLutBits + 1;
+    while (L <= AFX_MAX_CODE_LEN && v >= sh.limit[L]) ++L;
+    if (L > AFX_MAX_CODE_LEN) {
+        len = 0;
+        return 0;
+    }
+    len = L;
+    return sh.sorted[sh.base[L] + static_cast<int32_t>(v >> (24 - L))];
+}
+
+// ---- tile staging ----------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t stream_stage_bytes(const TensorArgs& t, uint64_t b) {
+    const uint64_t byte0 = b * static_cast<uint64_t>(kThreads) * t.chunk_bytes;
+    const uint64_t want = static_cast<uint64_t>(kThreads) * t.chunk_bytes + kStreamPad;
+    const uint64_t avail = t.exp_bytes > byte0 ? t.exp_bytes - byte0 : 0;
+    return static_cast<uint32_t>(want < avail ? want : avail);
+}
+
+// Issues the cp.async copies of tile b of tensor t into buffer slot `buf`
+// and commits them as one group (every thread commits, possibly empty).
+__device__ void issue_tile(Shared& sh, uint8_t* stream_base, uint32_t stream_stride, const TensorArgs& t, uint64_t b,
+                           int buf) {
+    const int tid = threadIdx.x;
+    uint8_t* dst = stream_base + static_cast<size_t>(buf) * stream_stride;
+    const uint8_t* src =
+        reinterpret_cast<const uint8_t*>(t.exp_words) + b * static_cast<uint64_t>(kThreads) * t.chunk_bytes;
+    const uint32_t bytes = stream_stage_bytes(t, b);
+    for (uint32_t i = tid * 16u; i < bytes; i += kThreads * 16u) cp_async16(dst + i, src + i);
+    // chunk entries of this tile and the next tile's first eight, inside the
+    // chunk section and its zero padding (rounded up to 16 bytes)
+    const uint64_t cb0 = b * static_cast<uint64_t>(kThreads) * 2;
+    const uint64_t csec = (t.n_chunks * 2 + 15) & ~uint64_t(15);
+    const uint64_t cavail = csec > cb0 ? csec - cb0 : 0;
+    const uint32_t cbytes = static_cast<uint32_t>(cavail < kChunkStage * 2 ? cavail : kChunkStage * 2);
+    const uint8_t* csrc = reinterpret_cast<const uint8_t*>(t.chunk_index) + cb0;
+    uint8_t* cdst = reinterpret_cast<uint8_t*>(sh.chunk[buf]);
+    for (uint32_t i = tid * 16u; i < cbytes; i += kThreads * 16u) cp_async16(cdst + i, csrc + i);
+    if (tid == 0) {
+        cp_async8(&sh.block_pair[buf][0], t.block_index + b);
+        cp_async8(&sh.block_pair[buf][1], t.block_index + b + 1);
+    }
+    cp_async_commit();
+}
+
+// Exclusive block-wide scan of one count per thread.
+__device__ __forceinline__ uint32_t block_exclusive_scan(Shared& sh, uint32_t v, uint32_t* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t inc = v;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-        uint32_t o = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+        const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, inc, d);
         if (lane >= d) inc += o;
     }
     if (lane == 31) sh.warp_total[warp] = inc;
@@ -169,190 +320,173 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(TileShared& sh, uint32_
     return warp_off + inc - v;
 }
 
-// Stages tile b, scans, decodes the tile's exponents into sh.stage.
-// Returns false (uniformly) when the tile must be skipped.
-__device__ bool decode_tile(TileShared& sh, uint32_t* stream, const DecodeArgs& a, uint64_t b, uint64_t& o0,
-                            uint64_t& o1) {
-    const int tid = threadIdx.x;
-    const uint32_t T = a.chunk_bytes;
-    const uint32_t words_per_chunk = T >> 2;
-    const uint64_t tile_byte0 = b * static_cast<uint64_t>(kThreads) * T;
-    const uint64_t want = static_cast<uint64_t>(kThreads) * T + 16;
-    const uint64_t avail_bytes = a.exp_bytes > tile_byte0 ? a.exp_bytes - tile_byte0 : 0;
-    const uint32_t stage_bytes = static_cast<uint32_t>(want < avail_bytes ? want : avail_bytes);
-    const uint32_t staged_words = stage_bytes >> 2;
-
-    // 1. stage stream words (16-byte vectors) and chunk entries
-    {
-        const uint4* src = reinterpret_cast<const uint4*>(a.exp_words + (tile_byte0 >> 2));
-        uint4* dst = reinterpret_cast<uint4*>(stream);
-        for (uint32_t i = tid; i < (stage_bytes >> 4); i += kThreads) dst[i] = __ldg(src + i);
-        const uint64_t c0 = b * kThreads;
-        for (int i = tid; i <= kThreads; i += kThreads) {
-            const uint64_t c = c0 + i;
-            sh.chunk[i] = c < a.n_chunks ? __ldg(a.chunk_index + c) : uint16_t(0);
-        }
-        if (tid == 0) sh.tile_ok = 1;
+// Appends n8 / 8 exponents (low bytes of `bytes`) to the word accumulator
+// and stores every completed word.
+__device__ __forceinline__ void append(uint32_t bytes, uint32_t n8, uint32_t& acc, uint32_t& fill_bits,
+                                       uint32_t*& wout) {
+    const uint32_t word = acc | (bytes << fill_bits);
+    const uint32_t carry = __funnelshift_l(bytes, 0u, fill_bits);  // bytes >> (32 - fill), 0 when fill is 0
+    fill_bits += n8;
+    if (fill_bits >= 32) {
+        *wout++ = word;
+        acc = carry;
+        fill_bits -= 32;
+    } else {
+        acc = word;
     }
-    o0 = __ldg(a.block_index + b);
-    o1 = __ldg(a.block_index + b + 1);
-    __syncthreads();
+}
 
-    // 2. counts and placement
-    const uint32_t entry = sh.chunk[tid];
+// Decodes tile b of tensor t (staged in slot buf) into sh.stage.  Returns
+// false, uniformly, when the tile must be skipped.
+__device__ bool decode_tile(Shared& sh, const uint32_t* stream, const TensorArgs& t, uint64_t b, int buf,
+                            int32_t* status, uint64_t& o0, uint64_t& o1) {
+    const int tid = threadIdx.x;
+    const uint32_t T = t.chunk_bytes;
+    const uint32_t chunk_bits = 8u * T;
+    const uint32_t staged_words = stream_stage_bytes(t, b) >> 2;
+    const uint64_t c0 = b * kThreads;
+    o0 = sh.block_pair[buf][0];
+    o1 = sh.block_pair[buf][1];
+    if (tid == 0) {
+        sh.tile_ok = 1;
+        // the tile's sign|mantissa bytes are needed after the decode
+        if (o0 < o1 && o1 <= t.n) {
+            const uint64_t a0 = o0 & ~uint64_t(15), a1 = (o1 + 15) & ~uint64_t(15);
+            prefetch_l2(t.sm + a0, static_cast<uint32_t>(a1 - a0));
+        }
+    }
+
+    const uint32_t entry = (c0 + tid < t.n_chunks) ? sh.chunk[buf][tid] : 0u;
     const uint32_t gap = entry & 31u;
     uint32_t cnt = entry >> 5;
-    const uint32_t chunk_bits = 8u * T;
-    if (cnt > chunk_bits - gap || gap > 23u) {
-        raise_status(a.status, AFX_DEV_BAD_CHUNK);
-        sh.tile_ok = 0;
+    bool bad = false;
+    if (gap > 23u || cnt > chunk_bits - gap) {
+        bad = true;
         cnt = 0;
     }
     uint32_t total = 0;
-    const uint32_t off = block_exclusive_scan(sh, cnt, &total);
-    const bool last_ok = b + 1 != a.n_blocks || o1 == a.n;  // the block index ends at n
-    if (o1 < o0 || o1 - o0 != total || total > AFX_BLOCK_CAPACITY || o1 > a.n || !last_ok) {
-        if (tid == 0) raise_status(a.status, AFX_DEV_BAD_BLOCK);
-        return false;  // uniform: every thread sees the same o0, o1, total
+    const uint32_t off = block_exclusive_scan(sh, cnt, &total);  // contains a __syncthreads
+    const bool last_ok = b + 1 != t.n_blocks || o1 == t.n;       // the block index ends at n
+    if (o1 < o0 || o1 - o0 != total || total > AFX_BLOCK_CAPACITY || o1 > t.n || !last_ok) {
+        if (tid == 0) raise_status(status, AFX_DEV_BAD_BLOCK);
+        return false;
     }
 
-    // 3. decode this thread's codewords
     if (cnt) {
-        uint32_t widx = tid * words_per_chunk;
-        uint64_t buf = (static_cast<uint64_t>(stream[widx]) << 32) | stream[widx + 1];
-        buf <<= gap;
-        int avail = 64 - static_cast<int>(gap);
-        widx += 2;
-        uint8_t* out = sh.stage + (o0 & 7u) + off;
-        bool bad = false;
-        for (uint32_t i = 0; i < cnt; ++i) {
-            if (avail < 32) {
-                if (widx >= staged_words) {
-                    bad = true;
-                    break;
-                }
-                buf |= static_cast<uint64_t>(stream[widx++]) << (32 - avail);
-                avail += 32;
+        const uint32_t s0 = static_cast<uint32_t>(o0 & 7u) + off;  // stage index of this run
+        uint32_t k = tid * (T >> 2);
+        uint32_t w0 = stream[k], w1 = stream[k + 1];
+        k += 2;
+        uint32_t pos = gap;  // bit of w0 where the next code starts (0..31)
+        uint32_t i = 0;
+        // head: single codes until the stage index is word aligned
+        const uint32_t head = min(cnt, (0u - s0) & 3u);
+        for (; i < head; ++i) {
+            uint32_t len;
+            const uint32_t sym = decode_one(sh, __funnelshift_l(w1, w0, pos), len);
+            if (!len) {
+                bad = true;
+                break;
             }
-            const uint32_t e = sh.lut[static_cast<uint32_t>(buf >> (64 - kLutBits))];
-            uint32_t len = e >> 8;
-            uint32_t sym = e & 0xFFu;
-            if (len == 0) {
-                const uint32_t v = static_cast<uint32_t>(buf >> 40);
-                len = kLutBits + 1;
-                while (len <= AFX_MAX_CODE_LEN && v >= sh.limit[len]) ++len;
-                if (len > AFX_MAX_CODE_LEN) {
-                    bad = true;
-                    break;
-                }
-                sym = sh.sorted[sh.base[len] + static_cast<int32_t>(v >> (24 - len))];
+            sh.stage[s0 + i] = static_cast<uint8_t>(sym);
+            pos += len;
+            if (pos >= 32) {
+                pos -= 32;
+                w0 = w1;
+                w1 = k < staged_words ? stream[k] : 0u;
+                ++k;
             }
-            buf <<= len;
-            avail -= static_cast<int>(len);
-            out[i] = static_cast<uint8_t>(sym);
         }
-        // the codewords must end exactly where the next chunk's first begins
-        const uint32_t next = sh.chunk[tid + 1];
-        const uint32_t end = widx * 32u - static_cast<uint32_t>(avail);
-        const uint32_t chunk_end = (tid + 1) * chunk_bits;
+        uint32_t* wout = reinterpret_cast<uint32_t*>(sh.stage + s0 + i);
+        uint32_t acc = 0, fill = 0;
+        // body: up to three codes per table lookup, never past cnt
+        while (!bad && i + 3 <= cnt) {
+            const uint32_t win = __funnelshift_l(w1, w0, pos);
+            const uint32_t e = sh.lut[win >> (32 - kLutBits)];
+            uint32_t n = (e >> 4) & 3u;
+            uint32_t bytes;
+            if (n) {
+                pos += e & 15u;
+                bytes = e >> 8;
+            } else {  // the first code is longer than 12 bits
+                uint32_t len;
+                bytes = decode_one(sh, win, len);
+                if (!len) {
+                    bad = true;
+                    break;
+                }
+                pos += len;
+                n = 1;
+            }
+            append(bytes, n * 8, acc, fill, wout);
+            i += n;
+            if (pos >= 32) {
+                pos -= 32;
+                w0 = w1;
+                w1 = k < staged_words ? stream[k] : 0u;
+                ++k;
+            }
+        }
+        // tail: single codes up to exactly cnt
+        while (!bad && i < cnt) {
+            uint32_t len;
+            const uint32_t sym = decode_one(sh, __funnelshift_l(w1, w0, pos), len);
+            if (!len) {
+                bad = true;
+                break;
+            }
+            append(sym, 8, acc, fill, wout);
+            ++i;
+            pos += len;
+            if (pos >= 32) {
+                pos -= 32;
+                w0 = w1;
+                w1 = k < staged_words ? stream[k] : 0u;
+                ++k;
+            }
+        }
+        // pending exponents (at most three) go out as bytes
+        uint8_t* tail = reinterpret_cast<uint8_t*>(wout);
+        for (uint32_t j = 0; j * 8 < fill; ++j) tail[j] = static_cast<uint8_t>(acc >> (8 * j));
+        // the codes must end exactly where the next chunk's first code begins
         if (!bad) {
+            const uint32_t end = (k - 2) * 32u + pos;  // bit offset inside the staged stream
+            const uint32_t next = (c0 + tid + 1 < t.n_chunks) ? sh.chunk[buf][tid + 1] : 0u;
+            const uint32_t chunk_end = (tid + 1) * chunk_bits;
             if ((next >> 5) != 0)
                 bad = end != chunk_end + (next & 31u);
             else
                 bad = end > chunk_end + AFX_MAX_CODE_LEN;
         }
-        if (bad) {
-            raise_status(a.status, AFX_DEV_BAD_CHUNK);
-            sh.tile_ok = 0;
-        }
+    }
+    if (bad) {
+        raise_status(status, AFX_DEV_BAD_CHUNK);
+        sh.tile_ok = 0;
     }
     __syncthreads();
     return sh.tile_ok != 0;
 }
 
-struct StoreArgs {
-    uint16_t* out;
-};
+// ---- epilogues ---------------------------------------------------------------------
 
-__global__ void __launch_bounds__(kThreads) decode_store_kernel(const DecodeArgs a, const CodeTables tab,
-                                                                 const StoreArgs st) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    TileShared& sh = *reinterpret_cast<TileShared*>(smem);
-    uint32_t* stream = reinterpret_cast<uint32_t*>(smem + ((sizeof(TileShared) + 15) & ~size_t(15)));
-    build_tables(sh, tab);
-    __syncthreads();
-    for (uint64_t b = blockIdx.x; b < a.n_blocks; b += gridDim.x) {
-        uint64_t o0, o1;
-        if (decode_tile(sh, stream, a, b, o0, o1)) {
-            const uint64_t ob0 = o0 & ~uint64_t(7);  // stage[i] holds weight ob0 + i
-            const uint64_t g0 = o0 >> 3, g1 = (o1 + 7) >> 3;
-            for (uint64_t g = g0 + threadIdx.x; g < g1; g += kThreads) {
-                const uint64_t ob = g << 3;
-                const uint32_t si = static_cast<uint32_t>(ob - ob0);  // multiple of 8
-                if (ob >= o0 && ob + 8 <= o1) {
-                    const uint2 e8 = *reinterpret_cast<const uint2*>(sh.stage + si);
-                    const uint2 s8 = __ldg(reinterpret_cast<const uint2*>(a.sm + ob));
-                    const uint2 lo = join4(e8.x, s8.x);
-                    const uint2 hi = join4(e8.y, s8.y);
-                    uint4 v;
-                    v.x = lo.x;
-                    v.y = lo.y;
-                    v.z = hi.x;
-                    v.w = hi.y;
-                    __stcs(reinterpret_cast<uint4*>(st.out + ob), v);
-                } else {
-                    for (uint32_t k = 0; k < 8; ++k) {
-                        const uint64_t o = ob + k;
-                        if (o >= o0 && o < o1) st.out[o] = join1(sh.stage[si + k], a.sm[o]);
-                    }
-                }
+__device__ __forceinline__ void store_tile(const Shared& sh, const TensorArgs& t, uint64_t o0, uint64_t o1) {
+    const uint64_t ob0 = o0 & ~uint64_t(7);
+    const uint64_t g0 = o0 >> 3, g1 = (o1 + 7) >> 3;
+    for (uint64_t g = g0 + threadIdx.x; g < g1; g += kThreads) {
+        const uint64_t ob = g << 3;
+        const uint32_t si = static_cast<uint32_t>(ob - ob0);  // multiple of 8
+        if (ob >= o0 && ob + 8 <= o1) {
+            const uint2 e8 = *reinterpret_cast<const uint2*>(sh.stage + si);
+            const uint2 s8 = __ldg(reinterpret_cast<const uint2*>(t.sm + ob));
+            __stcs(reinterpret_cast<uint4*>(t.out + ob), join8(e8, s8));
+        } else {
+            for (uint32_t q = 0; q < 8; ++q) {
+                const uint64_t o = ob + q;
+                if (o >= o0 && o < o1) t.out[o] = join1(sh.stage[si + q], t.sm[o]);
             }
         }
-        __syncthreads();
     }
 }
-
-// One exponent for every weight: out[i] = join(fill, sm[i]).  The block
-// index holds the single entry n.
-__global__ void fill_store_kernel(const uint8_t* __restrict__ sm, const uint64_t* __restrict__ block_index,
-                                  uint32_t fill, uint64_t n, uint16_t* __restrict__ out, int32_t* status) {
-    if (blockIdx.x == 0 && threadIdx.x == 0 && block_index[0] != n) raise_status(status, AFX_DEV_BAD_BLOCK);
-    const uint64_t groups = (n + 7) >> 3;
-    const uint32_t f4 = fill * 0x01010101u;
-    for (uint64_t g = blockIdx.x * static_cast<uint64_t>(blockDim.x) + threadIdx.x; g < groups;
-         g += static_cast<uint64_t>(gridDim.x) * blockDim.x) {
-        const uint64_t ob = g << 3;
-        if (ob + 8 <= n) {
-            const uint2 s8 = __ldg(reinterpret_cast<const uint2*>(sm + ob));
-            const uint2 lo = join4(f4, s8.x);
-            const uint2 hi = join4(f4, s8.y);
-            __stcs(reinterpret_cast<uint4*>(out + ob), make_uint4(lo.x, lo.y, hi.x, hi.y));
-        } else {
-            for (uint64_t o = ob; o < n; ++o) out[o] = join1(fill, sm[o]);
-        }
-    }
-}
-
-// ---- fused GEMV ------------------------------------------------------------
-//
-// y[b][r] = sum_c W[r][c] x[b][c].  Within a tile, warp w takes a contiguous
-// slice of 8-weight groups, so it meets the rows of its slice in order.
-// Each lane keeps float32 sums for the warp's current row; when the row
-// changes the warp reduces them with a fixed butterfly and stores one
-// partial per (warp, row) in shared memory.  Then every row of the tile is
-// summed over warps in warp order: rows that lie wholly in the tile go to
-// y, the tile's first and last (partial) rows go to the workspace, and
-// gemv_fixup_kernel adds those across tiles in tile order.  Every sum has a
-// fixed order, so y is reproducible bit for bit.
-
-struct GemvArgs {
-    const uint16_t* x;
-    float* y;
-    float* ws;          // [n_blocks][2][batch]
-    uint32_t rows, cols;
-    uint32_t batch;
-    uint32_t rows_per_warp;  // capacity of the per-warp partial table
-};
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
@@ -369,209 +503,268 @@ __device__ __forceinline__ void warp_flush(float (&acc)[kMaxBatch], float* part,
     }
 }
 
+// y[b][r] = sum_c W[r][c] x[b][c] for the rows this tile meets.  Warp w
+// takes a contiguous slice of 8-weight groups, keeps float32 sums for its
+// current row and, when the row changes, reduces them with a fixed
+// butterfly into one partial per (warp, row).  Rows are then summed over
+// warps in warp order: rows wholly inside the tile go to y, the first and
+// last (partial) rows to the workspace, which gemv_fixup_kernel adds across
+// tiles in tile order.  Every sum has a fixed order: y is reproducible.
 template <int B>
-__global__ void __launch_bounds__(kThreads) decode_gemv_kernel(const DecodeArgs a, const CodeTables tab,
-                                                                const GemvArgs g) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    TileShared& sh = *reinterpret_cast<TileShared*>(smem);
-    uint8_t* after = smem + ((sizeof(TileShared) + 15) & ~size_t(15));
-    uint32_t* stream = reinterpret_cast<uint32_t*>(after);
-    const uint32_t stream_bytes = kThreads * a.chunk_bytes + 16;
-    float* part = reinterpret_cast<float*>(after + stream_bytes);   // [kWarps][rows_per_warp][B]
-    uint64_t* warp_row0 = reinterpret_cast<uint64_t*>(part + kWarps * g.rows_per_warp * B);  // [kWarps]
-    uint32_t* warp_nrows = reinterpret_cast<uint32_t*>(warp_row0 + kWarps);                   // [kWarps]
-
-    build_tables(sh, tab);
-    __syncthreads();
+__device__ void gemv_tile(const Shared& sh, const TensorArgs& t, uint64_t tile, uint64_t o0, uint64_t o1,
+                          float* part, uint64_t* warp_row0, uint32_t* warp_nrows) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint64_t cols = g.cols;
+    const uint64_t cols = t.cols;
     const bool vec_x = (cols & 7u) == 0;
+    const uint64_t ob0 = o0 & ~uint64_t(7);
+    const uint64_t g0 = o0 >> 3, g1 = (o1 + 7) >> 3;
+    const uint64_t ng = g1 - g0;
+    const uint64_t s_begin = g0 + ng * warp / kWarps, s_end = g0 + ng * (warp + 1) / kWarps;
+    float* wpart = part + static_cast<size_t>(warp) * t.rows_per_warp * B;
 
-    for (uint64_t tb = blockIdx.x; tb < a.n_blocks; tb += gridDim.x) {
-        uint64_t o0, o1;
-        if (!decode_tile(sh, stream, a, tb, o0, o1) || o0 == o1) {
-            __syncthreads();
-            continue;
-        }
-        const uint64_t ob0 = o0 & ~uint64_t(7);  // stage[i] holds weight ob0 + i
-        const uint64_t g0 = o0 >> 3, g1 = (o1 + 7) >> 3;
-        const uint64_t ng = g1 - g0;
-        const uint64_t s_begin = g0 + ng * warp / kWarps, s_end = g0 + ng * (warp + 1) / kWarps;
+    uint64_t cur = 0, row0 = 0;
+    uint32_t nrows = 0;
+    if (s_begin < s_end) {
+        const uint64_t first_o = (s_begin << 3) > o0 ? (s_begin << 3) : o0;
+        row0 = first_o / cols;
+        cur = row0;
+    }
+    float acc[kMaxBatch] = {0.f, 0.f, 0.f, 0.f};
+    for (uint64_t base = s_begin; base < s_end; base += 32) {
+        const uint64_t gi = base + lane;
+        const bool active = gi < s_end;
+        const uint64_t step_first = (base << 3) > o0 ? (base << 3) : o0;
+        const uint64_t last_g = (base + 32 < s_end ? base + 32 : s_end) - 1;
+        const uint64_t step_last = ((last_g << 3) + 7) < o1 - 1 ? ((last_g << 3) + 7) : o1 - 1;
+        const uint64_t r_lo = step_first / cols, r_hi = step_last / cols;
 
-        uint64_t cur = ~uint64_t(0), row0 = 0;
-        uint32_t nrows = 0;
-        if (s_begin < s_end) {
-            const uint64_t first_o = (s_begin << 3) > o0 ? (s_begin << 3) : o0;
-            row0 = first_o / cols;
-            cur = row0;
-        }
-        float acc[kMaxBatch] = {0.f, 0.f, 0.f, 0.f};
-        for (uint64_t base = s_begin; base < s_end; base += 32) {
-            const uint64_t gi = base + lane;
-            const bool active = gi < s_end;
-            // rows met by this step: from the first element of the step to its last
-            const uint64_t step_first = (base << 3) > o0 ? (base << 3) : o0;
-            const uint64_t last_g = (base + 32 < s_end ? base + 32 : s_end) - 1;
-            const uint64_t step_last = ((last_g << 3) + 7) < o1 - 1 ? ((last_g << 3) + 7) : o1 - 1;
-            const uint64_t r_lo = step_first / cols, r_hi = step_last / cols;
-
-            // this lane's products, split by row (a group meets at most two rows as cols >= 64)
-            float ca[kMaxBatch] = {0.f, 0.f, 0.f, 0.f}, cb[kMaxBatch] = {0.f, 0.f, 0.f, 0.f};
-            uint64_t ra = ~uint64_t(0), rb = ~uint64_t(0);
-            if (active) {
-                const uint64_t ob = gi << 3;
-                const uint32_t si = static_cast<uint32_t>(ob - ob0);
-                const bool full = ob >= o0 && ob + 8 <= o1;
-                ra = (ob >= o0 ? ob : o0) / cols;
-                const uint64_t c0 = ob - ra * cols;
-                if (full && vec_x && c0 + 8 <= cols) {
-                    const uint2 e8 = *reinterpret_cast<const uint2*>(sh.stage + si);
-                    const uint2 s8 = __ldg(reinterpret_cast<const uint2*>(a.sm + ob));
-                    const uint2 lo = join4(e8.x, s8.x);
-                    const uint2 hi = join4(e8.y, s8.y);
-                    float wv[8];
-                    wv[0] = bf16_lo(lo.x); wv[1] = bf16_hi(lo.x);
-                    wv[2] = bf16_lo(lo.y); wv[3] = bf16_hi(lo.y);
-                    wv[4] = bf16_lo(hi.x); wv[5] = bf16_hi(hi.x);
-                    wv[6] = bf16_lo(hi.y); wv[7] = bf16_hi(hi.y);
-#pragma unroll
-                    for (int b = 0; b < B; ++b) {
-                        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(g.x + b * cols + c0));
-                        float s = wv[0] * bf16_lo(xv.x);
-                        s = fmaf(wv[1], bf16_hi(xv.x), s);
-                        s = fmaf(wv[2], bf16_lo(xv.y), s);
-                        s = fmaf(wv[3], bf16_hi(xv.y), s);
-                        s = fmaf(wv[4], bf16_lo(xv.z), s);
-                        s = fmaf(wv[5], bf16_hi(xv.z), s);
-                        s = fmaf(wv[6], bf16_lo(xv.w), s);
-                        s = fmaf(wv[7], bf16_hi(xv.w), s);
-                        ca[b] = s;
-                    }
-                } else {
-                    for (uint32_t k = 0; k < 8; ++k) {
-                        const uint64_t o = ob + k;
-                        if (o < o0 || o >= o1) continue;
-                        const uint64_t r = o / cols;
-                        const uint64_t c = o - r * cols;
-                        const float wf = __uint_as_float(static_cast<uint32_t>(join1(sh.stage[si + k], a.sm[o])) << 16);
-#pragma unroll
-                        for (int b = 0; b < B; ++b) {
-                            const float xf = __uint_as_float(static_cast<uint32_t>(g.x[b * cols + c]) << 16);
-                            if (r == ra)
-                                ca[b] = fmaf(wf, xf, ca[b]);
-                            else {
-                                cb[b] = fmaf(wf, xf, cb[b]);
-                            }
-                        }
-                        if (r != ra) rb = r;
-                    }
-                }
-            }
-            for (uint64_t rr = r_lo; rr <= r_hi; ++rr) {
-                if (rr != cur) {
-                    warp_flush<B>(acc, part + static_cast<size_t>(warp) * g.rows_per_warp * B,
-                                  static_cast<uint32_t>(cur - row0), lane);
-                    cur = rr;
-                }
+        // this lane's products, split by row (a group meets at most two rows as cols >= 64)
+        float ca[kMaxBatch] = {0.f, 0.f, 0.f, 0.f}, cb[kMaxBatch] = {0.f, 0.f, 0.f, 0.f};
+        uint64_t ra = ~uint64_t(0), rb = ~uint64_t(0);
+        if (active) {
+            const uint64_t ob = gi << 3;
+            const uint32_t si = static_cast<uint32_t>(ob - ob0);
+            const bool full = ob >= o0 && ob + 8 <= o1;
+            ra = (ob >= o0 ? ob : o0) / cols;
+            const uint64_t c0 = ob - ra * cols;
+            if (full && vec_x && c0 + 8 <= cols) {
+                const uint2 e8 = *reinterpret_cast<const uint2*>(sh.stage + si);
+                const uint2 s8 = __ldg(reinterpret_cast<const uint2*>(t.sm + ob));
+                const uint4 wv4 = join8(e8, s8);
+                float wv[8];
+                wv[0] = bf16_lo(wv4.x);
+                wv[1] = bf16_hi(wv4.x);
+                wv[2] = bf16_lo(wv4.y);
+                wv[3] = bf16_hi(wv4.y);
+                wv[4] = bf16_lo(wv4.z);
+                wv[5] = bf16_hi(wv4.z);
+                wv[6] = bf16_lo(wv4.w);
+                wv[7] = bf16_hi(wv4.w);
 #pragma unroll
                 for (int b = 0; b < B; ++b) {
-                    if (ra == rr) acc[b] += ca[b];
-                    if (rb == rr) acc[b] += cb[b];
+                    const uint4 xv = __ldg(reinterpret_cast<const uint4*>(t.x + b * cols + c0));
+                    float s = wv[0] * bf16_lo(xv.x);
+                    s = fmaf(wv[1], bf16_hi(xv.x), s);
+                    s = fmaf(wv[2], bf16_lo(xv.y), s);
+                    s = fmaf(wv[3], bf16_hi(xv.y), s);
+                    s = fmaf(wv[4], bf16_lo(xv.z), s);
+                    s = fmaf(wv[5], bf16_hi(xv.z), s);
+                    s = fmaf(wv[6], bf16_lo(xv.w), s);
+                    s = fmaf(wv[7], bf16_hi(xv.w), s);
+                    ca[b] = s;
+                }
+            } else {
+                for (uint32_t q = 0; q < 8; ++q) {
+                    const uint64_t o = ob + q;
+                    if (o < o0 || o >= o1) continue;
+                    const uint64_t r = o / cols;
+                    const uint64_t c = o - r * cols;
+                    const float wf = __uint_as_float(static_cast<uint32_t>(join1(sh.stage[si + q], t.sm[o])) << 16);
+#pragma unroll
+                    for (int b = 0; b < B; ++b) {
+                        const float xf = __uint_as_float(static_cast<uint32_t>(t.x[b * cols + c]) << 16);
+                        if (r == ra)
+                            ca[b] = fmaf(wf, xf, ca[b]);
+                        else
+                            cb[b] = fmaf(wf, xf, cb[b]);
+                    }
+                    if (r != ra) rb = r;
                 }
             }
         }
-        if (s_begin < s_end) {
-            warp_flush<B>(acc, part + static_cast<size_t>(warp) * g.rows_per_warp * B,
-                          static_cast<uint32_t>(cur - row0), lane);
-            nrows = static_cast<uint32_t>(cur - row0 + 1);
+        for (uint64_t rr = r_lo; rr <= r_hi; ++rr) {
+            if (rr != cur) {
+                warp_flush<B>(acc, wpart, static_cast<uint32_t>(cur - row0), lane);
+                cur = rr;
+            }
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                if (ra == rr) acc[b] += ca[b];
+                if (rb == rr) acc[b] += cb[b];
+            }
         }
-        if (lane == 0) {
-            warp_row0[warp] = row0;
-            warp_nrows[warp] = nrows;
-        }
-        __syncthreads();
+    }
+    if (s_begin < s_end) {
+        warp_flush<B>(acc, wpart, static_cast<uint32_t>(cur - row0), lane);
+        nrows = static_cast<uint32_t>(cur - row0 + 1);
+    }
+    if (lane == 0) {
+        warp_row0[warp] = row0;
+        warp_nrows[warp] = nrows;
+    }
+    __syncthreads();
 
-        // combine warps in order; whole rows to y, partial rows to the workspace
-        const uint64_t r_first = o0 / cols, r_last = (o1 - 1) / cols;
-        const uint64_t nr = r_last - r_first + 1;
-        for (uint64_t i = threadIdx.x; i < nr * B; i += kThreads) {
-            const uint64_t r = r_first + i / B;
-            const int b = static_cast<int>(i % B);
-            float s = 0.f;
-            for (int w = 0; w < kWarps; ++w) {
-                if (warp_nrows[w] && r >= warp_row0[w] && r < warp_row0[w] + warp_nrows[w])
-                    s += part[(static_cast<size_t>(w) * g.rows_per_warp + (r - warp_row0[w])) * B + b];
-            }
-            const bool whole = r * cols >= o0 && (r + 1) * cols <= o1;
-            if (whole)
-                g.y[static_cast<uint64_t>(b) * g.rows + r] = s;
-            else {
-                const int slot = (r == r_first) ? 0 : 1;
-                g.ws[(tb * 2 + slot) * B + b] = s;
-            }
+    const uint64_t r_first = o0 / cols, r_last = (o1 - 1) / cols;
+    const uint64_t nr = r_last - r_first + 1;
+    for (uint64_t i = threadIdx.x; i < nr * B; i += kThreads) {
+        const uint64_t r = r_first + i / B;
+        const int b = static_cast<int>(i % B);
+        float s = 0.f;
+        for (int w = 0; w < kWarps; ++w) {
+            if (warp_nrows[w] && r >= warp_row0[w] && r < warp_row0[w] + warp_nrows[w])
+                s += part[(static_cast<size_t>(w) * t.rows_per_warp + (r - warp_row0[w])) * B + b];
         }
-        __syncthreads();
+        const bool whole = r * cols >= o0 && (r + 1) * cols <= o1;
+        if (whole)
+            t.y[static_cast<uint64_t>(b) * t.rows + r] = s;
+        else
+            t.ws[(tile * 2 + (r == r_first ? 0 : 1)) * B + b] = s;
+    }
+}
+
+// ---- the restore kernel ------------------------------------------------------------
+//
+// B == 0: store the BF16 weights; B in 1..4: fused GEMV with B activation rows.
+template <int B>
+__global__ void __launch_bounds__(kThreads) restore_kernel(const __grid_constant__ LaunchArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    Shared& sh = *reinterpret_cast<Shared*>(smem);
+    uint8_t* stream_base = smem + shared_fixed_bytes();
+    const uint32_t stream_stride = kThreads * a.max_chunk_bytes + kStreamPad;
+    float* part = reinterpret_cast<float*>(stream_base + 2 * static_cast<size_t>(stream_stride));
+    uint64_t* warp_row0 = reinterpret_cast<uint64_t*>(part + (B ? kWarps * a.max_rows_per_warp * B : 0));
+    uint32_t* warp_nrows = reinterpret_cast<uint32_t*>(warp_row0 + kWarps);
+
+    const uint64_t g_begin = a.total_tiles * blockIdx.x / gridDim.x;
+    const uint64_t g_end = a.total_tiles * (blockIdx.x + 1) / gridDim.x;
+    if (g_begin >= g_end) return;
+
+    uint32_t k = 0;  // tensor of the current tile
+    while (k + 1 < a.count && g_begin >= a.t[k + 1].tile_begin) ++k;
+    uint32_t kn = k;  // tensor of the next tile to issue
+    int built = -1;
+    issue_tile(sh, stream_base, stream_stride, a.t[k], g_begin - a.t[k].tile_begin, 0);
+    int buf = 0;
+    for (uint64_t g = g_begin; g < g_end; ++g) {
+        if (g + 1 < g_end) {
+            while (kn + 1 < a.count && g + 1 >= a.t[kn + 1].tile_begin) ++kn;
+            issue_tile(sh, stream_base, stream_stride, a.t[kn], g + 1 - a.t[kn].tile_begin, buf ^ 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        while (k + 1 < a.count && g >= a.t[k + 1].tile_begin) ++k;
+        const TensorArgs& t = a.t[k];
+        __syncthreads();  // the staged tile is visible; the previous tile is done
+        if (built != static_cast<int>(k)) {
+            build_tables(sh, t.tab);
+            built = static_cast<int>(k);
+        }
+        const uint64_t b = g - t.tile_begin;
+        uint64_t o0, o1;
+        const uint32_t* stream =
+            reinterpret_cast<const uint32_t*>(stream_base + static_cast<size_t>(buf) * stream_stride);
+        if (decode_tile(sh, stream, t, b, buf, a.status, o0, o1) && o0 < o1) {
+            if constexpr (B == 0)
+                store_tile(sh, t, o0, o1);
+            else
+                gemv_tile<B>(sh, t, b, o0, o1, part, warp_row0, warp_nrows);
+        }
+        buf ^= 1;
     }
 }
 
 // Rows split across tiles: the tile in which a row starts adds its own tail
 // partial and the head partials of the following tiles, in tile order.
 template <int B>
-__global__ void gemv_fixup_kernel(const uint64_t* __restrict__ block_index, uint64_t n_blocks, GemvArgs g) {
-    const uint64_t t = blockIdx.x * static_cast<uint64_t>(blockDim.x) + threadIdx.x;
-    if (t >= n_blocks) return;
-    const uint64_t cols = g.cols;
-    const uint64_t n = static_cast<uint64_t>(g.rows) * cols;
-    const uint64_t o0 = block_index[t], o1 = block_index[t + 1];
+__global__ void gemv_fixup_kernel(const __grid_constant__ LaunchArgs a) {
+    const uint64_t g = blockIdx.x * static_cast<uint64_t>(blockDim.x) + threadIdx.x;
+    if (g >= a.total_tiles) return;
+    uint32_t k = 0;
+    while (k + 1 < a.count && g >= a.t[k + 1].tile_begin) ++k;
+    const TensorArgs& t = a.t[k];
+    const uint64_t tile = g - t.tile_begin;
+    const uint64_t cols = t.cols;
+    const uint64_t n = static_cast<uint64_t>(t.rows) * cols;
+    const uint64_t o0 = t.block_index[tile], o1 = t.block_index[tile + 1];
     if (o1 <= o0 || o1 > n) return;  // empty, or a corrupt index the main kernel already flagged
     const uint64_t r_first = o0 / cols, r_last = (o1 - 1) / cols;
     const uint64_t row_start = r_last * cols, row_end = row_start + cols;
-    if (row_start < o0 || row_end <= o1) return;  // not started here, or wholly inside
+    if (row_start < o0 || row_end <= o1) return;  // the row did not start here, or ends here
     float s[kMaxBatch];
     const int slot = (r_last == r_first) ? 0 : 1;
 #pragma unroll
-    for (int b = 0; b < B; ++b) s[b] = g.ws[(t * 2 + slot) * B + b];
-    for (uint64_t u = t + 1; u < n_blocks; ++u) {
-        const uint64_t p0 = block_index[u], p1 = block_index[u + 1];
+    for (int b = 0; b < B; ++b) s[b] = t.ws[(tile * 2 + slot) * B + b];
+    for (uint64_t u = tile + 1; u < t.n_blocks; ++u) {
+        const uint64_t p0 = t.block_index[u], p1 = t.block_index[u + 1];
         if (p1 < p0 || p1 > n) break;
         if (p1 == p0) continue;
 #pragma unroll
-        for (int b = 0; b < B; ++b) s[b] += g.ws[(u * 2 + 0) * B + b];
+        for (int b = 0; b < B; ++b) s[b] += t.ws[(u * 2) * B + b];
         if (p1 >= row_end) break;
     }
 #pragma unroll
-    for (int b = 0; b < B; ++b) g.y[static_cast<uint64_t>(b) * g.rows + r_last] = s[b];
+    for (int b = 0; b < B; ++b) t.y[static_cast<uint64_t>(b) * t.rows + r_last] = s[b];
+}
+
+// One exponent for every weight: out[i] = join(fill, sm[i]).  The block
+// index holds the single entry n.
+__global__ void fill_store_kernel(const uint8_t* __restrict__ sm, const uint64_t* __restrict__ block_index,
+                                  uint32_t fill, uint64_t n, uint16_t* __restrict__ out, int32_t* status) {
+    if (blockIdx.x == 0 && threadIdx.x == 0 && block_index[0] != n) raise_status(status, AFX_DEV_BAD_BLOCK);
+    const uint64_t groups = (n + 7) >> 3;
+    const uint32_t f4 = fill * 0x01010101u;
+    for (uint64_t g = blockIdx.x * static_cast<uint64_t>(blockDim.x) + threadIdx.x; g < groups;
+         g += static_cast<uint64_t>(gridDim.x) * blockDim.x) {
+        const uint64_t ob = g << 3;
+        if (ob + 8 <= n) {
+            const uint2 s8 = __ldg(reinterpret_cast<const uint2*>(sm + ob));
+            __stcs(reinterpret_cast<uint4*>(out + ob), join8(make_uint2(f4, f4), s8));
+        } else {
+            for (uint64_t o = ob; o < n; ++o) out[o] = join1(fill, sm[o]);
+        }
+    }
 }
 
 // All weights share one exponent: one warp per row, fixed-order reduction.
 template <int B>
 __global__ void fill_gemv_kernel(const uint8_t* __restrict__ sm, const uint64_t* __restrict__ block_index,
-                                 uint32_t fill, GemvArgs g, int32_t* status) {
+                                 uint32_t fill, const uint16_t* __restrict__ x, float* __restrict__ y, uint32_t rows,
+                                 uint32_t cols, int32_t* status) {
     const int lane = threadIdx.x & 31;
-    if (blockIdx.x == 0 && threadIdx.x == 0 && block_index[0] != static_cast<uint64_t>(g.rows) * g.cols)
+    if (blockIdx.x == 0 && threadIdx.x == 0 && block_index[0] != static_cast<uint64_t>(rows) * cols)
         raise_status(status, AFX_DEV_BAD_BLOCK);
     const uint64_t warps = static_cast<uint64_t>(gridDim.x) * (blockDim.x >> 5);
-    for (uint64_t r = blockIdx.x * static_cast<uint64_t>(blockDim.x >> 5) + (threadIdx.x >> 5); r < g.rows;
+    for (uint64_t r = blockIdx.x * static_cast<uint64_t>(blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
          r += warps) {
         float acc[kMaxBatch] = {0.f, 0.f, 0.f, 0.f};
-        for (uint64_t c = lane; c < g.cols; c += 32) {
-            const uint64_t o = r * g.cols + c;
-            const float wf = __uint_as_float(static_cast<uint32_t>(join1(fill, sm[o])) << 16);
+        for (uint64_t c = lane; c < cols; c += 32) {
+            const float wf = __uint_as_float(static_cast<uint32_t>(join1(fill, sm[r * cols + c])) << 16);
 #pragma unroll
             for (int b = 0; b < B; ++b)
-                acc[b] = fmaf(wf, __uint_as_float(static_cast<uint32_t>(g.x[b * g.cols + c]) << 16), acc[b]);
+                acc[b] = fmaf(wf, __uint_as_float(static_cast<uint32_t>(x[b * cols + c]) << 16), acc[b]);
         }
 #pragma unroll
         for (int b = 0; b < B; ++b) {
             float v = acc[b];
 #pragma unroll
             for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, d);
-            if (lane == 0) g.y[static_cast<uint64_t>(b) * g.rows + r] = v;
+            if (lane == 0) y[static_cast<uint64_t>(b) * rows + r] = v;
         }
     }
 }
 
-// ---- host launch helpers -----------------------------------------------------
+// ---- host side ------------------------------------------------------------------------
 
 void make_tables(const afx_desc& d, CodeTables& t) {
     std::memset(&t, 0, sizeof t);
@@ -582,7 +775,6 @@ void make_tables(const afx_desc& d, CodeTables& t) {
     uint32_t first = 0;
     for (int L = 1; L <= AFX_MAX_CODE_LEN; ++L) {
         if (L > 1) first = (first + count[L - 1]) << 1;
-        // symbols of length L in value order
         const unsigned first_pos = pos;
         for (int s = 0; s < 256; ++s)
             if (d.len[s] == L) t.sorted[pos++] = static_cast<uint8_t>(s);
@@ -590,9 +782,6 @@ void make_tables(const afx_desc& d, CodeTables& t) {
         t.base[L] = static_cast<int32_t>(first_pos) - static_cast<int32_t>(first);
     }
 }
-
-size_t stream_stage_bytes(uint32_t T) { return static_cast<size_t>(kThreads) * T + 16; }
-size_t tile_shared_bytes() { return (sizeof(TileShared) + 15) & ~size_t(15); }
 
 std::mutex g_mutex;
 
@@ -665,128 +854,199 @@ int sm_count() {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-afx_status make_decode_args(const afx_desc& d, const void* container, int32_t* status, DecodeArgs& a) {
+void fill_tensor(const afx_desc& d, const void* container, TensorArgs& t) {
+    std::memset(&t, 0, sizeof t);
     const uint8_t* base = static_cast<const uint8_t*>(container);
-    a.exp_words = reinterpret_cast<const uint32_t*>(base + d.off_exp);
-    a.sm = base + d.off_sm;
-    a.chunk_index = reinterpret_cast<const uint16_t*>(base + d.off_chunk);
-    a.block_index = reinterpret_cast<const uint64_t*>(base + d.off_block);
-    a.n = d.n;
-    a.n_chunks = d.n_chunks;
-    a.n_blocks = d.n_blocks;
-    a.exp_bytes = d.exp_bytes;
-    a.chunk_bytes = d.chunk_bytes;
-    a.status = status;
+    t.exp_words = reinterpret_cast<const uint32_t*>(base + d.off_exp);
+    t.sm = base + d.off_sm;
+    t.chunk_index = reinterpret_cast<const uint16_t*>(base + d.off_chunk);
+    t.block_index = reinterpret_cast<const uint64_t*>(base + d.off_block);
+    t.n = d.n;
+    t.n_chunks = d.n_chunks;
+    t.n_blocks = d.n_blocks;
+    t.exp_bytes = d.exp_bytes;
+    t.chunk_bytes = d.chunk_bytes;
+    make_tables(d, t.tab);
+}
+
+// Rows a GEMV warp slice can meet: a slice is at most
+// (capacity + 16) / 8 / warps + 2 groups of 8 weights.
+uint32_t gemv_rows_per_warp(uint32_t cols) {
+    const uint64_t slice = ((AFX_BLOCK_CAPACITY + 16) / 8 / kWarps + 2) * 8;
+    return static_cast<uint32_t>(slice / cols + 2);
+}
+
+template <int B>
+afx_status launch_restore(LaunchArgs& la, cudaStream_t s) {
+    if (la.count == 0 || la.total_tiles == 0) return AFX_OK;
+    const int sms = sm_count();
+    if (sms <= 0) return afx_fail(AFX_E_CUDA, "cannot query the SM count", 0);
+    size_t smem = shared_fixed_bytes() + 2 * (static_cast<size_t>(kThreads) * la.max_chunk_bytes + kStreamPad);
+    if (B)
+        smem += static_cast<size_t>(kWarps) * la.max_rows_per_warp * B * sizeof(float) +
+                kWarps * (sizeof(uint64_t) + sizeof(uint32_t));
+    if (smem > 227 * 1024) return afx_fail(AFX_E_ARG, "launch needs too much shared memory", 0);
+    int per_sm = 0;
+    const afx_status st = prepare_kernel(reinterpret_cast<const void*>(restore_kernel<B>), smem, &per_sm);
+    if (st != AFX_OK) return st;
+    const uint64_t grid = std::min<uint64_t>(la.total_tiles, static_cast<uint64_t>(sms) * per_sm);
+    restore_kernel<B><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(la);
+    AFX_CUDA_TRY(cudaGetLastError(), "restore_kernel launch");
+    if (B) {
+        const unsigned fix_blocks = static_cast<unsigned>((la.total_tiles + 127) / 128);
+        gemv_fixup_kernel<B><<<fix_blocks, 128, 0, s>>>(la);
+        AFX_CUDA_TRY(cudaGetLastError(), "gemv_fixup_kernel launch");
+    }
     return AFX_OK;
+}
+
+void reset_launch(LaunchArgs& la) {
+    la.count = 0;
+    la.total_tiles = 0;
+    la.max_chunk_bytes = 0;
+    la.max_rows_per_warp = 0;
 }
 
 }  // namespace afx
 
 using namespace afx;
 
+extern "C" afx_status afx_decode_batch(const afx_desc* descs, const void* const* containers, uint16_t* const* outs,
+                                       uint32_t count, afx_stream_t stream, int32_t* status) {
+    if (count && (!descs || !containers || !outs)) return afx_fail(AFX_E_ARG, "null array", 0);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    for (uint32_t i = 0; i < count; ++i) {
+        const afx_desc& d = descs[i];
+        const afx_status st = afx_check_desc(&d);
+        if (st != AFX_OK) return afx_fail(st, "invalid container description", 0);
+        if (d.n == 0) continue;
+        if (!containers[i] || !outs[i] || !aligned(containers[i], 16) || !aligned(outs[i], 16))
+            return afx_fail(AFX_E_ARG, "container and output must be 16-byte aligned device pointers", 0);
+        if (d.nsym >= 2 && d.block_chunks != static_cast<uint32_t>(kThreads))
+            return afx_fail(AFX_E_ARG, "the decoder runs 256 chunks per block", 0);
+    }
+    LaunchArgs la;
+    std::memset(&la, 0, sizeof la);
+    la.status = status;
+    for (uint32_t i = 0; i < count; ++i) {
+        const afx_desc& d = descs[i];
+        if (d.n == 0) continue;
+        const uint8_t* base = static_cast<const uint8_t*>(containers[i]);
+        if (d.nsym == 1) {
+            const int sms = sm_count();
+            if (sms <= 0) return afx_fail(AFX_E_CUDA, "cannot query the SM count", 0);
+            const uint64_t groups = (d.n + 7) / 8;
+            const uint64_t blocks = std::min<uint64_t>((groups + 255) / 256, static_cast<uint64_t>(sms) * 8);
+            fill_store_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+                base + d.off_sm, reinterpret_cast<const uint64_t*>(base + d.off_block), d.fill, d.n, outs[i], status);
+            AFX_CUDA_TRY(cudaGetLastError(), "fill_store_kernel launch");
+            continue;
+        }
+        if (la.count == static_cast<uint32_t>(kMaxTensors)) {
+            const afx_status st = launch_restore<0>(la, s);
+            if (st != AFX_OK) return st;
+            reset_launch(la);
+        }
+        TensorArgs& t = la.t[la.count++];
+        fill_tensor(d, containers[i], t);
+        t.out = outs[i];
+        t.tile_begin = la.total_tiles;
+        la.total_tiles += d.n_blocks;
+        la.max_chunk_bytes = std::max(la.max_chunk_bytes, d.chunk_bytes);
+    }
+    return launch_restore<0>(la, s);
+}
+
 extern "C" afx_status afx_decode(const afx_desc* desc, const void* container, uint16_t* out, afx_stream_t stream,
                                  int32_t* status) {
-    if (!desc || (!container && desc->n) || (!out && desc->n)) return AFX_E_ARG;
-    afx_status st = afx_check_desc(desc);
-    if (st != AFX_OK) return st;
-    if (desc->n == 0) return AFX_OK;
-    if (!aligned(container, 16) || !aligned(out, 16)) return AFX_E_ARG;
-    if (desc->nsym >= 2 && desc->block_chunks != static_cast<uint32_t>(kThreads)) return AFX_E_ARG;
-    const int sms = sm_count();
-    if (sms <= 0) return afx_fail(AFX_E_CUDA, "cannot query the SM count", 0);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const uint8_t* base = static_cast<const uint8_t*>(container);
-
-    if (desc->nsym == 1) {
-        const uint64_t groups = (desc->n + 7) / 8;
-        const uint64_t blocks = std::min<uint64_t>((groups + 255) / 256, static_cast<uint64_t>(sms) * 8);
-        fill_store_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-            base + desc->off_sm, reinterpret_cast<const uint64_t*>(base + desc->off_block), desc->fill, desc->n, out,
-            status);
-        AFX_CUDA_TRY(cudaGetLastError(), "fill_store_kernel launch");
-        return AFX_OK;
-    }
-    DecodeArgs a;
-    make_decode_args(*desc, container, status, a);
-    CodeTables tab;
-    make_tables(*desc, tab);
-    const size_t smem = tile_shared_bytes() + stream_stage_bytes(desc->chunk_bytes);
-    int per_sm = 0;
-    st = prepare_kernel(reinterpret_cast<const void*>(decode_store_kernel), smem, &per_sm);
-    if (st != AFX_OK) return st;
-    const uint64_t grid = std::min<uint64_t>(desc->n_blocks, static_cast<uint64_t>(sms) * per_sm);
-    StoreArgs sa{out};
-    decode_store_kernel<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(a, tab, sa);
-    AFX_CUDA_TRY(cudaGetLastError(), "decode_store_kernel launch");
-    return AFX_OK;
+    if (!desc) return afx_fail(AFX_E_ARG, "null description", 0);
+    if (desc->n && (!container || !out)) return afx_fail(AFX_E_ARG, "null pointer", 0);
+    return afx_decode_batch(desc, &container, &out, 1, stream, status);
 }
 
 namespace {
 
 template <int B>
-afx_status launch_gemv(const afx_desc& d, const void* container, const GemvArgs& g, cudaStream_t s,
-                       int32_t* status, int sms) {
-    const uint8_t* base = static_cast<const uint8_t*>(container);
-    if (d.nsym == 1) {
-        const uint64_t blocks = std::min<uint64_t>((g.rows + 7) / 8, static_cast<uint64_t>(sms) * 8);
-        fill_gemv_kernel<B><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-            base + d.off_sm, reinterpret_cast<const uint64_t*>(base + d.off_block), d.fill, g, status);
-        AFX_CUDA_TRY(cudaGetLastError(), "fill_gemv_kernel launch");
-        return AFX_OK;
+afx_status gemv_batch(const afx_desc* descs, const void* const* containers, const uint32_t* rows,
+                      const uint32_t* cols, const uint16_t* const* xs, float* const* ys, void* const* workspaces,
+                      uint32_t count, cudaStream_t s, int32_t* status) {
+    LaunchArgs la;
+    std::memset(&la, 0, sizeof la);
+    la.status = status;
+    for (uint32_t i = 0; i < count; ++i) {
+        const afx_desc& d = descs[i];
+        const uint8_t* base = static_cast<const uint8_t*>(containers[i]);
+        if (d.nsym == 1) {
+            const int sms = sm_count();
+            if (sms <= 0) return afx_fail(AFX_E_CUDA, "cannot query the SM count", 0);
+            const uint64_t blocks = std::min<uint64_t>((rows[i] + 7) / 8, static_cast<uint64_t>(sms) * 8);
+            fill_gemv_kernel<B><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+                base + d.off_sm, reinterpret_cast<const uint64_t*>(base + d.off_block), d.fill, xs[i], ys[i], rows[i],
+                cols[i], status);
+            AFX_CUDA_TRY(cudaGetLastError(), "fill_gemv_kernel launch");
+            continue;
+        }
+        if (la.count == static_cast<uint32_t>(kMaxTensors)) {
+            const afx_status st = launch_restore<B>(la, s);
+            if (st != AFX_OK) return st;
+            reset_launch(la);
+        }
+        TensorArgs& t = la.t[la.count++];
+        fill_tensor(d, containers[i], t);
+        t.x = xs[i];
+        t.y = ys[i];
+        t.ws = static_cast<float*>(workspaces[i]);
+        t.rows = rows[i];
+        t.cols = cols[i];
+        t.rows_per_warp = gemv_rows_per_warp(cols[i]);
+        t.tile_begin = la.total_tiles;
+        la.total_tiles += d.n_blocks;
+        la.max_chunk_bytes = std::max(la.max_chunk_bytes, d.chunk_bytes);
+        la.max_rows_per_warp = std::max(la.max_rows_per_warp, t.rows_per_warp);
     }
-    DecodeArgs a;
-    make_decode_args(d, container, status, a);
-    CodeTables tab;
-    make_tables(d, tab);
-    const size_t part_bytes = static_cast<size_t>(kWarps) * g.rows_per_warp * B * sizeof(float);
-    const size_t smem = tile_shared_bytes() + stream_stage_bytes(d.chunk_bytes) + part_bytes +
-                        kWarps * (sizeof(uint64_t) + sizeof(uint32_t));
-    if (smem > 227 * 1024) return afx_fail(AFX_E_ARG, "GEMV shape needs too much shared memory", 0);
-    int per_sm = 0;
-    const afx_status st = prepare_kernel(reinterpret_cast<const void*>(decode_gemv_kernel<B>), smem, &per_sm);
-    if (st != AFX_OK) return st;
-    const uint64_t grid = std::min<uint64_t>(d.n_blocks, static_cast<uint64_t>(sms) * per_sm);
-    decode_gemv_kernel<B><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(a, tab, g);
-    AFX_CUDA_TRY(cudaGetLastError(), "decode_gemv_kernel launch");
-    const unsigned fix_blocks = static_cast<unsigned>((d.n_blocks + 127) / 128);
-    gemv_fixup_kernel<B><<<fix_blocks, 128, 0, s>>>(a.block_index, d.n_blocks, g);
-    AFX_CUDA_TRY(cudaGetLastError(), "gemv_fixup_kernel launch");
-    return AFX_OK;
+    return launch_restore<B>(la, s);
 }
 
 }  // namespace
 
+extern "C" afx_status afx_decode_gemv_batch(const afx_desc* descs, const void* const* containers,
+                                            const uint32_t* rows, const uint32_t* cols, const uint16_t* const* xs,
+                                            uint32_t batch, float* const* ys, void* const* workspaces,
+                                            const uint64_t* workspace_bytes, uint32_t count, afx_stream_t stream,
+                                            int32_t* status) {
+    if (count && (!descs || !containers || !rows || !cols || !xs || !ys || !workspaces || !workspace_bytes))
+        return afx_fail(AFX_E_ARG, "null array", 0);
+    if (batch < 1 || batch > static_cast<uint32_t>(kMaxBatch)) return afx_fail(AFX_E_ARG, "batch must be 1..4", 0);
+    for (uint32_t i = 0; i < count; ++i) {
+        const afx_desc& d = descs[i];
+        const afx_status st = afx_check_desc(&d);
+        if (st != AFX_OK) return afx_fail(st, "invalid container description", 0);
+        if (!containers[i] || !xs[i] || !ys[i]) return afx_fail(AFX_E_ARG, "null pointer", 0);
+        if (rows[i] == 0 || cols[i] < 64 || static_cast<uint64_t>(rows[i]) * cols[i] != d.n)
+            return afx_fail(AFX_E_ARG, "rows * cols must equal n, with cols >= 64", 0);
+        if (!aligned(containers[i], 16) || !aligned(xs[i], 16))
+            return afx_fail(AFX_E_ARG, "container and x must be 16-byte aligned", 0);
+        if (d.nsym >= 2) {
+            if (d.block_chunks != static_cast<uint32_t>(kThreads))
+                return afx_fail(AFX_E_ARG, "the decoder runs 256 chunks per block", 0);
+            if (!workspaces[i] || !aligned(workspaces[i], 16)) return afx_fail(AFX_E_ARG, "bad workspace", 0);
+            if (workspace_bytes[i] < afx_gemv_workspace_bytes(d.n_blocks, batch))
+                return afx_fail(AFX_E_NOSPACE, "workspace too small", 0);
+        }
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    switch (batch) {
+        case 1: return gemv_batch<1>(descs, containers, rows, cols, xs, ys, workspaces, count, s, status);
+        case 2: return gemv_batch<2>(descs, containers, rows, cols, xs, ys, workspaces, count, s, status);
+        case 3: return gemv_batch<3>(descs, containers, rows, cols, xs, ys, workspaces, count, s, status);
+        default: return gemv_batch<4>(descs, containers, rows, cols, xs, ys, workspaces, count, s, status);
+    }
+}
+
 extern "C" afx_status afx_decode_gemv(const afx_desc* desc, const void* container, uint32_t rows, uint32_t cols,
                                       const uint16_t* x, uint32_t batch, float* y, void* workspace,
                                       uint64_t workspace_bytes, afx_stream_t stream, int32_t* status) {
-    if (!desc || !container || !x || !y) return AFX_E_ARG;
-    afx_status st = afx_check_desc(desc);
-    if (st != AFX_OK) return st;
-    if (batch < 1 || batch > static_cast<uint32_t>(kMaxBatch)) return AFX_E_ARG;
-    if (rows == 0 || cols < 64 || static_cast<uint64_t>(rows) * cols != desc->n) return AFX_E_ARG;
-    if (!aligned(container, 16) || !aligned(x, 16)) return AFX_E_ARG;
-    if (desc->nsym >= 2 && desc->block_chunks != static_cast<uint32_t>(kThreads)) return AFX_E_ARG;
-    if (desc->nsym >= 2) {
-        if (!workspace || !aligned(workspace, 16)) return AFX_E_ARG;
-        if (workspace_bytes < afx_gemv_workspace_bytes(desc->n_blocks, batch)) return AFX_E_NOSPACE;
-    }
-    const int sms = sm_count();
-    if (sms <= 0) return afx_fail(AFX_E_CUDA, "cannot query the SM count", 0);
-    GemvArgs g;
-    g.x = x;
-    g.y = y;
-    g.ws = static_cast<float*>(workspace);
-    g.rows = rows;
-    g.cols = cols;
-    g.batch = batch;
-    // rows a warp slice can meet: slice <= (capacity + 16) / 8 / warps + 1 groups
-    const uint64_t slice_elems = ((AFX_BLOCK_CAPACITY + 16) / 8 / kWarps + 2) * 8;
-    g.rows_per_warp = static_cast<uint32_t>(slice_elems / cols + 2);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    switch (batch) {
-        case 1: return launch_gemv<1>(*desc, container, g, s, status, sms);
-        case 2: return launch_gemv<2>(*desc, container, g, s, status, sms);
-        case 3: return launch_gemv<3>(*desc, container, g, s, status, sms);
-        default: return launch_gemv<4>(*desc, container, g, s, status, sms);
-    }
+    if (!desc) return afx_fail(AFX_E_ARG, "null description", 0);
+    return afx_decode_gemv_batch(desc, &container, &rows, &cols, &x, batch, &y, &workspace, &workspace_bytes, 1,
+                                 stream, status);
 }

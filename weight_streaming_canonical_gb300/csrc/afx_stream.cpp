@@ -64,6 +64,36 @@ afx_status check_layer(const afx_layer& L, uint64_t buf_bytes) {
     return AFX_OK;
 }
 
+// Runs ops[0..count), all of one kind (and one batch size), as one batch call.
+afx_status run_group(const afx_op* ops, uint32_t count, uint8_t* buf, afx_stream_t stream, int32_t* status_dev) {
+    std::vector<afx_desc> descs(count);
+    std::vector<const void*> containers(count);
+    for (uint32_t i = 0; i < count; ++i) {
+        descs[i] = ops[i].desc;
+        containers[i] = buf + ops[i].offset;
+    }
+    if (ops[0].kind == AFX_OP_DECODE) {
+        std::vector<uint16_t*> outs(count);
+        for (uint32_t i = 0; i < count; ++i) outs[i] = static_cast<uint16_t*>(ops[i].out_dev);
+        return afx_decode_batch(descs.data(), containers.data(), outs.data(), count, stream, status_dev);
+    }
+    std::vector<uint32_t> rows(count), cols(count);
+    std::vector<const uint16_t*> xs(count);
+    std::vector<float*> ys(count);
+    std::vector<void*> ws(count);
+    std::vector<uint64_t> ws_bytes(count);
+    for (uint32_t i = 0; i < count; ++i) {
+        rows[i] = ops[i].rows;
+        cols[i] = ops[i].cols;
+        xs[i] = ops[i].x_dev;
+        ys[i] = static_cast<float*>(ops[i].out_dev);
+        ws[i] = ops[i].workspace_dev;
+        ws_bytes[i] = ops[i].workspace_bytes;
+    }
+    return afx_decode_gemv_batch(descs.data(), containers.data(), rows.data(), cols.data(), xs.data(), ops[0].batch,
+                                 ys.data(), ws.data(), ws_bytes.data(), count, stream, status_dev);
+}
+
 }  // namespace
 
 extern "C" afx_status afx_stream_run(const afx_layer* layers, uint32_t n_layers, void* const* dev_bufs,
@@ -96,17 +126,15 @@ extern "C" afx_status afx_stream_run(const afx_layer* layers, uint32_t n_layers,
                            "cudaMemcpyAsync");
         AFX_STREAM_TRY(cudaEventRecord(copied.ev[k], copy), "cudaEventRecord");
         AFX_STREAM_TRY(cudaStreamWaitEvent(compute, copied.ev[k], 0), "cudaStreamWaitEvent");
-        for (uint32_t i = 0; i < L.n_ops; ++i) {
-            const afx_op& op = L.ops[i];
-            const void* container = buf + op.offset;
-            afx_status st;
-            if (op.kind == AFX_OP_DECODE)
-                st = afx_decode(&op.desc, container, static_cast<uint16_t*>(op.out_dev), compute_stream, status_dev);
-            else
-                st = afx_decode_gemv(&op.desc, container, op.rows, op.cols, op.x_dev, op.batch,
-                                     static_cast<float*>(op.out_dev), op.workspace_dev, op.workspace_bytes,
-                                     compute_stream, status_dev);
+        // consecutive ops of one kind (and one GEMV batch size) share a launch
+        for (uint32_t i = 0; i < L.n_ops;) {
+            uint32_t j = i + 1;
+            while (j < L.n_ops && L.ops[j].kind == L.ops[i].kind &&
+                   (L.ops[i].kind == AFX_OP_DECODE || L.ops[j].batch == L.ops[i].batch))
+                ++j;
+            const afx_status st = run_group(L.ops + i, j - i, buf, compute_stream, status_dev);
             if (st != AFX_OK) return st;
+            i = j;
         }
         AFX_STREAM_TRY(cudaEventRecord(consumed.ev[k], compute), "cudaEventRecord");
     }
