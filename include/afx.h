@@ -92,7 +92,7 @@ typedef struct afx_desc {
     uint64_t n;               /* weights */
     uint64_t total_bits;      /* sum of all code lengths */
     uint32_t chunk_bytes;     /* T: stream bytes per chunk, 4..64, power of two */
-    uint32_t block_chunks;    /* C: chunks per block (the decoder runs C = 256) */
+    uint32_t block_chunks;    /* C: chunks per block (the GPU decoder runs C = 512) */
     uint64_t n_chunks;        /* ceil(total_bits / (8 T)) */
     uint64_t n_blocks;        /* ceil(n_chunks / C) */
     uint64_t off_exp, exp_bytes;
@@ -115,9 +115,10 @@ typedef struct afx_desc {
 afx_status afx_build_code(const uint16_t* w_host, uint64_t n, uint32_t max_len, afx_code* out);
 
 /* Plans the container for n weights coded with `code`: fills *out with the
- * geometry, section offsets and total size.  chunk_bytes = 0 picks T (32,
- * or 16 when some code is 1 bit long, so a block never exceeds
- * AFX_BLOCK_CAPACITY codewords); block_chunks = 0 picks C = 256.
+ * geometry, section offsets and total size.  block_chunks = 0 picks C =
+ * 512, the geometry the GPU decoder runs; chunk_bytes = 0 picks the largest
+ * T of 32, 16, 8, 4 for which a block can never hold more than
+ * AFX_BLOCK_CAPACITY codewords (T = 16, or 8 when some code is 1 bit long).
  * Host only.  Errors: AFX_E_ARG on a bad geometry or a T that could
  * overflow the block capacity. */
 afx_status afx_encode_bound(uint64_t n, const afx_code* code, uint32_t chunk_bytes,

@@ -81,15 +81,18 @@ def test_container_is_byte_identical_to_the_oracle(afx, case, T):
 def test_geometry_choice_respects_block_capacity(afx):
     w = synth.normal(100_000, seed=4)
     d = afx.afx_encode_bound(w.size, afx.afx_build_code(w))
-    assert d.chunk_bytes == 32 and d.block_chunks == 256
-    # a dominant exponent gets a 1-bit code: 32-byte chunks could hold 65536 codewords per block
+    # shortest code 2 bits: 512 chunks of 16 bytes hold at most 32768 codewords
+    assert d.chunk_bytes == 16 and d.block_chunks == 512
+    # a dominant exponent gets a 1-bit code: the chunks shrink to 8 bytes
     v = np.where(np.arange(50_000) % 3 == 0, 0x4000, 0x3F80).astype(np.uint16)
     code = afx.afx_build_code(v)
     assert min(l for l in code.len if l) == 1
     d = afx.afx_encode_bound(v.size, code)
-    assert d.chunk_bytes == 16
+    assert d.chunk_bytes == 8
     with pytest.raises(afx.AfxError):
-        afx.afx_encode_bound(v.size, code, 32, 256)
+        afx.afx_encode_bound(v.size, code, 16, 512)
+    d = afx.afx_encode_bound(w.size, afx.afx_build_code(w), 0, 256)
+    assert d.chunk_bytes == 32 and d.block_chunks == 256
 
 
 def test_parse_header_roundtrip_and_rejections(afx):

@@ -9,7 +9,7 @@
 // This is the t_unpack term of that page's Eq. (1).
 //
 // Work decomposition.  One launch restores a list of tensors.  A tile is
-// one block of a container (256 chunks of 8*T stream bits); the tiles of
+// one block of a container (512 chunks of 8*T stream bits); the tiles of
 // all tensors form one list, and each persistent CTA takes a contiguous
 // run of it, so it meets at most a few tensors.  For each tile:
 //   1. the tile's stream words, chunk entries and block-index pair arrive in
@@ -191,7 +191,7 @@ __device__ __forceinline__ uint16_t join1(uint32_t e, uint32_t s) {
 // remaining 12 - L1 peek bits start the second code, which counts only if
 // it ends within the 12 bits, and likewise for the third.
 
-__device__ void build_tables(Shared& sh, const CodeTables& tab) {
+__device__ __forceinline__ void build_tables(Shared& sh, const CodeTables& tab) {
     const int tid = threadIdx.x;
     for (int i = tid; i <= AFX_MAX_CODE_LEN; i += kThreads) {
         sh.limit[i] = tab.limit[i];
@@ -274,7 +274,7 @@ __device__ __forceinline__ uint32_t stream_stage_bytes(const TensorArgs& t, uint
 
 // Issues the cp.async copies of tile b of tensor t into buffer slot `buf`
 // and commits them as one group (every thread commits, possibly empty).
-__device__ void issue_tile(Shared& sh, uint8_t* stream_base, uint32_t stream_stride, const TensorArgs& t, uint64_t b,
+__device__ __forceinline__ void issue_tile(Shared& sh, uint8_t* stream_base, uint32_t stream_stride, const TensorArgs& t, uint64_t b,
                            int buf) {
     const int tid = threadIdx.x;
     uint8_t* dst = stream_base + static_cast<size_t>(buf) * stream_stride;
@@ -338,7 +338,7 @@ __device__ __forceinline__ void append(uint32_t bytes, uint32_t n8, uint32_t& ac
 
 // Decodes tile b of tensor t (staged in slot buf) into sh.stage.  Returns
 // false, uniformly, when the tile must be skipped.
-__device__ bool decode_tile(Shared& sh, const uint32_t* stream, const TensorArgs& t, uint64_t b, int buf,
+__device__ __forceinline__ bool decode_tile(Shared& sh, const uint32_t* stream, const TensorArgs& t, uint64_t b, int buf,
                             int32_t* status, uint64_t& o0, uint64_t& o1) {
     const int tid = threadIdx.x;
     const uint32_t T = t.chunk_bytes;
@@ -469,20 +469,46 @@ __device__ bool decode_tile(Shared& sh, const uint32_t* stream, const TensorArgs
 
 // ---- epilogues ---------------------------------------------------------------------
 
+// Joins and stores the tile's weights.  The first and last group of 8 may
+// be shared with the neighbouring tiles and go out weight by weight; the
+// full groups in between are handled kUnroll per thread at a time so that
+// their sign|mantissa loads are in flight together.
 __device__ __forceinline__ void store_tile(const Shared& sh, const TensorArgs& t, uint64_t o0, uint64_t o1) {
+    constexpr int kUnroll = 4;
     const uint64_t ob0 = o0 & ~uint64_t(7);
-    const uint64_t g0 = o0 >> 3, g1 = (o1 + 7) >> 3;
-    for (uint64_t g = g0 + threadIdx.x; g < g1; g += kThreads) {
-        const uint64_t ob = g << 3;
-        const uint32_t si = static_cast<uint32_t>(ob - ob0);  // multiple of 8
-        if (ob >= o0 && ob + 8 <= o1) {
-            const uint2 e8 = *reinterpret_cast<const uint2*>(sh.stage + si);
-            const uint2 s8 = __ldg(reinterpret_cast<const uint2*>(t.sm + ob));
-            __stcs(reinterpret_cast<uint4*>(t.out + ob), join8(e8, s8));
-        } else {
-            for (uint32_t q = 0; q < 8; ++q) {
-                const uint64_t o = ob + q;
-                if (o >= o0 && o < o1) t.out[o] = join1(sh.stage[si + q], t.sm[o]);
+    const uint64_t f0 = (o0 + 7) >> 3, f1 = o1 >> 3;  // full groups [f0, f1)
+    const int tid = threadIdx.x;
+    const uint64_t gh = o0 >> 3, gt = o1 >> 3;
+    const bool head_partial = (o0 & 7) != 0, tail_partial = (o1 & 7) != 0;
+    // thread 0: the partial head group; thread 1: the partial tail group,
+    // unless it is the same group as the head
+    const bool mine = (tid == 0 && head_partial) || (tid == 1 && tail_partial && !(head_partial && gt == gh));
+    if (mine) {
+        const uint64_t ob = (tid == 0 ? gh : gt) << 3;
+        for (uint32_t q = 0; q < 8; ++q) {
+            const uint64_t o = ob + q;
+            if (o >= o0 && o < o1) t.out[o] = join1(sh.stage[static_cast<uint32_t>(o - ob0)], t.sm[o]);
+        }
+    }
+    if (f1 <= f0) return;
+    // full groups, indexed from the first one in 32-bit arithmetic
+    const uint32_t nfull = static_cast<uint32_t>(f1 - f0);
+    const uint2* smp = reinterpret_cast<const uint2*>(t.sm + (f0 << 3));
+    uint4* outp = reinterpret_cast<uint4*>(t.out + (f0 << 3));
+    const uint8_t* stp = sh.stage + static_cast<uint32_t>((f0 << 3) - ob0);
+    for (uint32_t j = tid; j < nfull; j += kThreads * kUnroll) {
+        uint2 s8[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const uint32_t jj = j + u * kThreads;
+            if (jj < nfull) s8[u] = __ldg(smp + jj);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const uint32_t jj = j + u * kThreads;
+            if (jj < nfull) {
+                const uint2 e8 = *reinterpret_cast<const uint2*>(stp + 8 * jj);
+                __stcs(outp + jj, join8(e8, s8[u]));
             }
         }
     }
@@ -511,7 +537,7 @@ __device__ __forceinline__ void warp_flush(float (&acc)[kMaxBatch], float* part,
 // last (partial) rows to the workspace, which gemv_fixup_kernel adds across
 // tiles in tile order.  Every sum has a fixed order: y is reproducible.
 template <int B>
-__device__ void gemv_tile(const Shared& sh, const TensorArgs& t, uint64_t tile, uint64_t o0, uint64_t o1,
+__device__ __forceinline__ void gemv_tile(const Shared& sh, const TensorArgs& t, uint64_t tile, uint64_t o0, uint64_t o1,
                           float* part, uint64_t* warp_row0, uint32_t* warp_nrows) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint64_t cols = t.cols;
@@ -636,7 +662,7 @@ __device__ void gemv_tile(const Shared& sh, const TensorArgs& t, uint64_t tile, 
 //
 // B == 0: store the BF16 weights; B in 1..4: fused GEMV with B activation rows.
 template <int B>
-__global__ void __launch_bounds__(kThreads) restore_kernel(const __grid_constant__ LaunchArgs a) {
+__global__ void __launch_bounds__(kThreads, B == 0 ? 3 : 2) restore_kernel(const __grid_constant__ LaunchArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     Shared& sh = *reinterpret_cast<Shared*>(smem);
     uint8_t* stream_base = smem + shared_fixed_bytes();
@@ -923,7 +949,7 @@ extern "C" afx_status afx_decode_batch(const afx_desc* descs, const void* const*
         if (!containers[i] || !outs[i] || !aligned(containers[i], 16) || !aligned(outs[i], 16))
             return afx_fail(AFX_E_ARG, "container and output must be 16-byte aligned device pointers", 0);
         if (d.nsym >= 2 && d.block_chunks != static_cast<uint32_t>(kThreads))
-            return afx_fail(AFX_E_ARG, "the decoder runs 256 chunks per block", 0);
+            return afx_fail(AFX_E_ARG, "the decoder runs 512 chunks per block", 0);
     }
     LaunchArgs la;
     std::memset(&la, 0, sizeof la);
@@ -1028,7 +1054,7 @@ extern "C" afx_status afx_decode_gemv_batch(const afx_desc* descs, const void* c
             return afx_fail(AFX_E_ARG, "container and x must be 16-byte aligned", 0);
         if (d.nsym >= 2) {
             if (d.block_chunks != static_cast<uint32_t>(kThreads))
-                return afx_fail(AFX_E_ARG, "the decoder runs 256 chunks per block", 0);
+                return afx_fail(AFX_E_ARG, "the decoder runs 512 chunks per block", 0);
             if (!workspaces[i] || !aligned(workspaces[i], 16)) return afx_fail(AFX_E_ARG, "bad workspace", 0);
             if (workspace_bytes[i] < afx_gemv_workspace_bytes(d.n_blocks, batch))
                 return afx_fail(AFX_E_NOSPACE, "workspace too small", 0);

@@ -188,7 +188,7 @@ afx_status afx_build_code(const uint16_t* w, uint64_t n, uint32_t max_len, afx_c
 
 afx_status afx_encode_bound(uint64_t n, const afx_code* code, uint32_t T, uint32_t C, afx_desc* out) {
     if (!code || !out) return AFX_E_ARG;
-    if (C == 0) C = 256;
+    if (C == 0) C = AFX_DECODE_THREADS;
     uint64_t total_bits = 0, present = 0;
     unsigned min_len = 255;
     for (int s = 0; s < 256; ++s) {

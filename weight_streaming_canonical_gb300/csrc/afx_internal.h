@@ -8,7 +8,7 @@
 #define AFX_MAGIC 0x31584641u
 
 // Decoder geometry: one CTA thread per chunk, so a block is one CTA tile.
-#define AFX_DECODE_THREADS 256
+#define AFX_DECODE_THREADS 512
 
 #ifdef __cplusplus
 inline uint64_t afx_gemv_workspace_bytes(uint64_t n_blocks, uint32_t batch) {
