@@ -114,7 +114,7 @@ struct LaunchArgs {
 };
 
 struct Shared {
-    uint32_t lut[kLutSize];   // up to 3 codes per 12-bit peek: bits 0-3 total length, 4-5 count, 8-31 exponents
+    uint32_t lut[kLutSize];   // up to 3 codes per 12-bit peek: bits 0-3 total length, 4-5 count, 8-31 rotated exponents
     uint8_t len0[kLutSize];   // length of the first code of a 12-bit peek (0: longer than 12 bits)
     uint32_t limit[AFX_MAX_CODE_LEN + 1];
     int32_t base[AFX_MAX_CODE_LEN + 1];
@@ -123,7 +123,7 @@ struct Shared {
     alignas(16) uint64_t block_pair[2][2];
     uint32_t warp_total[kWarps];
     int32_t tile_ok;
-    alignas(16) uint8_t stage[kStageBytes];  // exponent of weight (o0 & ~7) + i at stage[i]
+    alignas(16) uint8_t stage[kStageBytes];  // rotated exponent of weight (o0 & ~7) + i at stage[i]
     // dynamic part: stream[2][kThreads * max_T + kStreamPad], then GEMV partials
 };
 
@@ -159,25 +159,27 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
 }
 
-// BF16 from exponent and sign|mantissa: sign to bit 15, exponent to bits
-// 7..14, mantissa to bits 0..6.  byte_perm interleaves four sign|mantissa
-// bytes s and four exponents e into (e << 8) | s per 16-bit lane; then s
-// bits 0..6 stay, e moves down one bit, s bit 7 moves up to bit 15.
-__device__ __forceinline__ uint32_t join_pair(uint32_t x) {
-    return (x & 0x007F007Fu) | ((x >> 1) & 0x7F807F80u) | ((x << 8) & 0x80008000u);
+// Exponents are kept rotated right by one bit, R = (e >> 1) | (e << 7), in
+// the decode tables and the stage buffer.  A BF16 weight's high byte is
+// sign | e >> 1 = (R & 0x7F) | (s & 0x80) and its low byte is
+// e << 7 | mantissa = (R & 0x80) | (s & 0x7F), with s the sign|mantissa
+// byte; so four weights take two bit selects and two byte interleaves.
+__host__ __device__ __forceinline__ uint32_t ror8(uint32_t e) { return ((e >> 1) | (e << 7)) & 0xFFu; }
+
+__device__ __forceinline__ uint2 join4(uint32_t r4, uint32_t s4) {
+    const uint32_t hi = (r4 & 0x7F7F7F7Fu) | (s4 & 0x80808080u);
+    const uint32_t lo = (s4 & 0x7F7F7F7Fu) | (r4 & 0x80808080u);
+    return make_uint2(__byte_perm(lo, hi, 0x5140), __byte_perm(lo, hi, 0x7362));
 }
 
-__device__ __forceinline__ uint4 join8(uint2 e8, uint2 s8) {
-    uint4 v;
-    v.x = join_pair(__byte_perm(s8.x, e8.x, 0x5140));
-    v.y = join_pair(__byte_perm(s8.x, e8.x, 0x7362));
-    v.z = join_pair(__byte_perm(s8.y, e8.y, 0x5140));
-    v.w = join_pair(__byte_perm(s8.y, e8.y, 0x7362));
-    return v;
+__device__ __forceinline__ uint4 join8(uint2 r8, uint2 s8) {
+    const uint2 a = join4(r8.x, s8.x), b = join4(r8.y, s8.y);
+    return make_uint4(a.x, a.y, b.x, b.y);
 }
 
-__device__ __forceinline__ uint16_t join1(uint32_t e, uint32_t s) {
-    return static_cast<uint16_t>(((s & 0x80u) << 8) | (e << 7) | (s & 0x7Fu));
+// One weight from a rotated exponent r and its sign|mantissa byte s.
+__device__ __forceinline__ uint16_t join1(uint32_t r, uint32_t s) {
+    return static_cast<uint16_t>((((r & 0x7Fu) | (s & 0x80u)) << 8) | (s & 0x7Fu) | (r & 0x80u));
 }
 
 // ---- decode tables ---------------------------------------------------------------
@@ -210,7 +212,7 @@ __device__ __forceinline__ void build_tables(Shared& sh, const CodeTables& tab) 
             while (L <= kLutBits && v >= tab.limit[L]) ++L;
             uint16_t e = 0;
             if (L <= kLutBits)
-                e = static_cast<uint16_t>((L << 8) | tab.sorted[tab.base[L] + static_cast<int32_t>(v >> (24 - L))]);
+                e = static_cast<uint16_t>((L << 8) | ror8(tab.sorted[tab.base[L] + static_cast<int32_t>(v >> (24 - L))]));
             first[p] = e;
             sh.len0[p] = static_cast<uint8_t>(e >> 8);
         }
@@ -244,7 +246,7 @@ __device__ __forceinline__ void build_tables(Shared& sh, const CodeTables& tab) 
     __syncthreads();
 }
 
-// One code from a 32-bit window: exponent, length in len (0 on a bad code).
+// One code from a 32-bit window: rotated exponent, length in len (0 on a bad code).
 __device__ __forceinline__ uint32_t decode_one(const Shared& sh, uint32_t win, uint32_t& len) {
     const uint32_t p = win >> (32 - kLutBits);
     uint32_t L = sh.len0[p];
@@ -260,7 +262,7 @@ __device__ __forceinline__ uint32_t decode_one(const Shared& sh, uint32_t win, u
         return 0;
     }
     len = L;
-    return sh.sorted[sh.base[L] + static_cast<int32_t>(v >> (24 - L))];
+    return ror8(sh.sorted[sh.base[L] + static_cast<int32_t>(v >> (24 - L))]);
 }
 
 // ---- tile staging ----------------------------------------------------------------
@@ -298,8 +300,10 @@ __device__ __forceinline__ void issue_tile(Shared& sh, uint8_t* stream_base, uin
     cp_async_commit();
 }
 
-// Exclusive block-wide scan of one count per thread.
+// Exclusive block-wide scan of one count per thread: warp-shuffle scans of
+// the counts and then of the warp totals.
 __device__ __forceinline__ uint32_t block_exclusive_scan(Shared& sh, uint32_t v, uint32_t* total) {
+    static_assert(kWarps <= 32, "one warp scans the warp totals");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     uint32_t inc = v;
 #pragma unroll
@@ -309,15 +313,15 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(Shared& sh, uint32_t v,
     }
     if (lane == 31) sh.warp_total[warp] = inc;
     __syncthreads();
-    uint32_t warp_off = 0, all = 0;
+    uint32_t wt = lane < kWarps ? sh.warp_total[lane] : 0u;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        const uint32_t t = sh.warp_total[w];
-        if (w < warp) warp_off += t;
-        all += t;
+    for (int d = 1; d < kWarps; d <<= 1) {
+        const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, wt, d);
+        if (lane >= d) wt += o;
     }
-    *total = all;
-    return warp_off + inc - v;
+    const uint32_t before = __shfl_sync(0xFFFFFFFFu, wt, (warp + 31) & 31);
+    *total = __shfl_sync(0xFFFFFFFFu, wt, kWarps - 1);
+    return (warp ? before : 0u) + inc - v;
 }
 
 // Appends n8 / 8 exponents (low bytes of `bytes`) to the word accumulator
@@ -379,8 +383,34 @@ __device__ __forceinline__ bool decode_tile(Shared& sh, const uint32_t* stream, 
         k += 2;
         uint32_t pos = gap;  // bit of w0 where the next code starts (0..31)
         uint32_t i = 0;
-        // head: single codes until the stage index is word aligned
+        // head: codes until the stage index is word aligned, from one lookup
+        // when it holds them all (their exact length from the first-code
+        // lengths), else one code at a time
         const uint32_t head = min(cnt, (0u - s0) & 3u);
+        if (head) {
+            const uint32_t win = __funnelshift_l(w1, w0, pos);
+            const uint32_t e = sh.lut[win >> (32 - kLutBits)];
+            if (((e >> 4) & 3u) >= head) {
+                uint32_t bits = sh.len0[win >> (32 - kLutBits)];
+                sh.stage[s0] = static_cast<uint8_t>(e >> 8);
+                if (head > 1) {
+                    bits += sh.len0[(win << bits) >> (32 - kLutBits)];
+                    sh.stage[s0 + 1] = static_cast<uint8_t>(e >> 16);
+                }
+                if (head > 2) {
+                    bits += sh.len0[(win << bits) >> (32 - kLutBits)];
+                    sh.stage[s0 + 2] = static_cast<uint8_t>(e >> 24);
+                }
+                pos += bits;
+                i = head;
+                if (pos >= 32) {
+                    pos -= 32;
+                    w0 = w1;
+                    w1 = k < staged_words ? stream[k] : 0u;
+                    ++k;
+                }
+            }
+        }
         for (; i < head; ++i) {
             uint32_t len;
             const uint32_t sym = decode_one(sh, __funnelshift_l(w1, w0, pos), len);
@@ -427,7 +457,25 @@ __device__ __forceinline__ bool decode_tile(Shared& sh, const uint32_t* stream, 
                 ++k;
             }
         }
-        // tail: single codes up to exactly cnt
+        // tail: the last one or two codes, from one lookup when it holds them
+        if (!bad && i < cnt) {
+            const uint32_t r = cnt - i;  // 1 or 2
+            const uint32_t win = __funnelshift_l(w1, w0, pos);
+            const uint32_t e = sh.lut[win >> (32 - kLutBits)];
+            if (((e >> 4) & 3u) >= r) {
+                uint32_t bits = sh.len0[win >> (32 - kLutBits)];
+                if (r > 1) bits += sh.len0[(win << bits) >> (32 - kLutBits)];
+                append((e >> 8) & (r > 1 ? 0xFFFFu : 0xFFu), 8 * r, acc, fill, wout);
+                i = cnt;
+                pos += bits;
+                if (pos >= 32) {
+                    pos -= 32;
+                    w0 = w1;
+                    w1 = k < staged_words ? stream[k] : 0u;
+                    ++k;
+                }
+            }
+        }
         while (!bad && i < cnt) {
             uint32_t len;
             const uint32_t sym = decode_one(sh, __funnelshift_l(w1, w0, pos), len);
@@ -749,7 +797,7 @@ __global__ void fill_store_kernel(const uint8_t* __restrict__ sm, const uint64_t
                                   uint32_t fill, uint64_t n, uint16_t* __restrict__ out, int32_t* status) {
     if (blockIdx.x == 0 && threadIdx.x == 0 && block_index[0] != n) raise_status(status, AFX_DEV_BAD_BLOCK);
     const uint64_t groups = (n + 7) >> 3;
-    const uint32_t f4 = fill * 0x01010101u;
+    const uint32_t f4 = ror8(fill) * 0x01010101u;
     for (uint64_t g = blockIdx.x * static_cast<uint64_t>(blockDim.x) + threadIdx.x; g < groups;
          g += static_cast<uint64_t>(gridDim.x) * blockDim.x) {
         const uint64_t ob = g << 3;
@@ -757,7 +805,7 @@ __global__ void fill_store_kernel(const uint8_t* __restrict__ sm, const uint64_t
             const uint2 s8 = __ldg(reinterpret_cast<const uint2*>(sm + ob));
             __stcs(reinterpret_cast<uint4*>(out + ob), join8(make_uint2(f4, f4), s8));
         } else {
-            for (uint64_t o = ob; o < n; ++o) out[o] = join1(fill, sm[o]);
+            for (uint64_t o = ob; o < n; ++o) out[o] = join1(ror8(fill), sm[o]);
         }
     }
 }
@@ -775,7 +823,7 @@ __global__ void fill_gemv_kernel(const uint8_t* __restrict__ sm, const uint64_t*
          r += warps) {
         float acc[kMaxBatch] = {0.f, 0.f, 0.f, 0.f};
         for (uint64_t c = lane; c < cols; c += 32) {
-            const float wf = __uint_as_float(static_cast<uint32_t>(join1(fill, sm[r * cols + c])) << 16);
+            const float wf = __uint_as_float(static_cast<uint32_t>(join1(ror8(fill), sm[r * cols + c])) << 16);
 #pragma unroll
             for (int b = 0; b < B; ++b)
                 acc[b] = fmaf(wf, __uint_as_float(static_cast<uint32_t>(x[b * cols + c]) << 16), acc[b]);
