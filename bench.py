@@ -357,7 +357,7 @@ def run_ours(args):
     peak, peak_kind = measured_hbm_peak()
     achieved = alg_total / (kernel_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": None, "kernel": "restore_kernel<0>", "peak_kind": peak_kind,
+                "traffic": None, "kernel": "restore_store_kernel", "peak_kind": peak_kind,
                 "launches_per_step": 1, "algorithmic_bytes_per_step": alg_total,
                 "kernel_ms_per_step": kernel_ms}
 

@@ -217,3 +217,9 @@ def test_qwen3_layer_in_one_launch(afx):
     for (c, _), o in zip(encoded, outs):
         ref, st = oracle.decode(c)
         assert st == oracle.OK and np.array_equal(o.cpu().numpy().view(np.uint16), ref)
+
+
+@pytest.mark.parametrize("n", [3_000_017, 9_000_001])
+def test_sizes_where_a_cta_owns_several_blocks(afx, n):
+    # more blocks than resident CTAs: every warp restores several sub-tiles in a row
+    _check(afx, synth.normal(n, seed=n))

@@ -188,19 +188,19 @@ __device__ __forceinline__ uint16_t join1(uint32_t r, uint32_t s) {
 // peek its first code (exponent, length) using the canonical limits; a
 // thread's 16 consecutive peeks have non-decreasing lengths, so one search
 // plus short advances suffices.  The (length << 8 | exponent) pairs go to a
-// scratch table in the stage buffer (free between tiles).  Step 2 chains up
+// scratch table (free shared memory between tiles).  Step 2 chains up
 // to three first codes per peek: after the first code of length L1, the
 // remaining 12 - L1 peek bits start the second code, which counts only if
 // it ends within the 12 bits, and likewise for the third.
 
-__device__ __forceinline__ void build_tables(Shared& sh, const CodeTables& tab) {
+template <class S>
+__device__ __forceinline__ void build_tables(S& sh, uint16_t* first /* 8 KB scratch */, const CodeTables& tab) {
     const int tid = threadIdx.x;
     for (int i = tid; i <= AFX_MAX_CODE_LEN; i += kThreads) {
         sh.limit[i] = tab.limit[i];
         sh.base[i] = tab.base[i];
     }
     for (int i = tid; i < 256; i += kThreads) sh.sorted[i] = tab.sorted[i];
-    uint16_t* first = reinterpret_cast<uint16_t*>(sh.stage);  // scratch: 8 KB
     constexpr int kPer = kLutSize / kThreads;
     {
         const int p0 = tid * kPer;
@@ -247,7 +247,8 @@ __device__ __forceinline__ void build_tables(Shared& sh, const CodeTables& tab) 
 }
 
 // One code from a 32-bit window: rotated exponent, length in len (0 on a bad code).
-__device__ __forceinline__ uint32_t decode_one(const Shared& sh, uint32_t win, uint32_t& len) {
+template <class S>
+__device__ __forceinline__ uint32_t decode_one(const S& sh, uint32_t win, uint32_t& len) {
     const uint32_t p = win >> (32 - kLutBits);
     uint32_t L = sh.len0[p];
     if (L) {
@@ -340,45 +341,18 @@ __device__ __forceinline__ void append(uint32_t bytes, uint32_t n8, uint32_t& ac
     }
 }
 
-// Decodes tile b of tensor t (staged in slot buf) into sh.stage.  Returns
-// false, uniformly, when the tile must be skipped.
-__device__ __forceinline__ bool decode_tile(Shared& sh, const uint32_t* stream, const TensorArgs& t, uint64_t b, int buf,
-                            int32_t* status, uint64_t& o0, uint64_t& o1) {
-    const int tid = threadIdx.x;
-    const uint32_t T = t.chunk_bytes;
-    const uint32_t chunk_bits = 8u * T;
-    const uint32_t staged_words = stream_stage_bytes(t, b) >> 2;
-    const uint64_t c0 = b * kThreads;
-    o0 = sh.block_pair[buf][0];
-    o1 = sh.block_pair[buf][1];
-    if (tid == 0) {
-        sh.tile_ok = 1;
-        // the tile's sign|mantissa bytes are needed after the decode
-        if (o0 < o1 && o1 <= t.n) {
-            const uint64_t a0 = o0 & ~uint64_t(15), a1 = (o1 + 15) & ~uint64_t(15);
-            prefetch_l2(t.sm + a0, static_cast<uint32_t>(a1 - a0));
-        }
-    }
-
-    const uint32_t entry = (c0 + tid < t.n_chunks) ? sh.chunk[buf][tid] : 0u;
-    const uint32_t gap = entry & 31u;
-    uint32_t cnt = entry >> 5;
+// Decodes the cnt codes of one chunk into stage[s0 .. s0 + cnt): the chunk
+// starts at stream word k0 and its first code at bit `gap` of that word;
+// staged_words words are valid.  `next` is the following chunk's index
+// entry (0 if none) and chunk_end the bit offset of this chunk's end in the
+// staged stream.  Returns true when the stream is not valid.
+template <class S>
+__device__ __forceinline__ bool decode_run(const S& sh, const uint32_t* stream, uint32_t staged_words, uint32_t k0,
+                                           uint32_t gap, uint32_t cnt, uint8_t* stage, uint32_t s0, uint32_t next,
+                                           uint32_t chunk_end) {
     bool bad = false;
-    if (gap > 23u || cnt > chunk_bits - gap) {
-        bad = true;
-        cnt = 0;
-    }
-    uint32_t total = 0;
-    const uint32_t off = block_exclusive_scan(sh, cnt, &total);  // contains a __syncthreads
-    const bool last_ok = b + 1 != t.n_blocks || o1 == t.n;       // the block index ends at n
-    if (o1 < o0 || o1 - o0 != total || total > AFX_BLOCK_CAPACITY || o1 > t.n || !last_ok) {
-        if (tid == 0) raise_status(status, AFX_DEV_BAD_BLOCK);
-        return false;
-    }
-
-    if (cnt) {
-        const uint32_t s0 = static_cast<uint32_t>(o0 & 7u) + off;  // stage index of this run
-        uint32_t k = tid * (T >> 2);
+    {
+        uint32_t k = k0;
         uint32_t w0 = stream[k], w1 = stream[k + 1];
         k += 2;
         uint32_t pos = gap;  // bit of w0 where the next code starts (0..31)
@@ -392,14 +366,14 @@ __device__ __forceinline__ bool decode_tile(Shared& sh, const uint32_t* stream, 
             const uint32_t e = sh.lut[win >> (32 - kLutBits)];
             if (((e >> 4) & 3u) >= head) {
                 uint32_t bits = sh.len0[win >> (32 - kLutBits)];
-                sh.stage[s0] = static_cast<uint8_t>(e >> 8);
+                stage[s0] = static_cast<uint8_t>(e >> 8);
                 if (head > 1) {
                     bits += sh.len0[(win << bits) >> (32 - kLutBits)];
-                    sh.stage[s0 + 1] = static_cast<uint8_t>(e >> 16);
+                    stage[s0 + 1] = static_cast<uint8_t>(e >> 16);
                 }
                 if (head > 2) {
                     bits += sh.len0[(win << bits) >> (32 - kLutBits)];
-                    sh.stage[s0 + 2] = static_cast<uint8_t>(e >> 24);
+                    stage[s0 + 2] = static_cast<uint8_t>(e >> 24);
                 }
                 pos += bits;
                 i = head;
@@ -418,7 +392,7 @@ __device__ __forceinline__ bool decode_tile(Shared& sh, const uint32_t* stream, 
                 bad = true;
                 break;
             }
-            sh.stage[s0 + i] = static_cast<uint8_t>(sym);
+            stage[s0 + i] = static_cast<uint8_t>(sym);
             pos += len;
             if (pos >= 32) {
                 pos -= 32;
@@ -427,7 +401,7 @@ __device__ __forceinline__ bool decode_tile(Shared& sh, const uint32_t* stream, 
                 ++k;
             }
         }
-        uint32_t* wout = reinterpret_cast<uint32_t*>(sh.stage + s0 + i);
+        uint32_t* wout = reinterpret_cast<uint32_t*>(stage + s0 + i);
         uint32_t acc = 0, fill = 0;
         // body: up to three codes per table lookup, never past cnt
         while (!bad && i + 3 <= cnt) {
@@ -498,14 +472,55 @@ __device__ __forceinline__ bool decode_tile(Shared& sh, const uint32_t* stream, 
         for (uint32_t j = 0; j * 8 < fill; ++j) tail[j] = static_cast<uint8_t>(acc >> (8 * j));
         // the codes must end exactly where the next chunk's first code begins
         if (!bad) {
-            const uint32_t end = (k - 2) * 32u + pos;  // bit offset inside the staged stream
-            const uint32_t next = (c0 + tid + 1 < t.n_chunks) ? sh.chunk[buf][tid + 1] : 0u;
-            const uint32_t chunk_end = (tid + 1) * chunk_bits;
+            const uint32_t end_bit = (k - 2) * 32u + pos;  // bit offset inside the staged stream
             if ((next >> 5) != 0)
-                bad = end != chunk_end + (next & 31u);
+                bad = end_bit != chunk_end + (next & 31u);
             else
-                bad = end > chunk_end + AFX_MAX_CODE_LEN;
+                bad = end_bit > chunk_end + AFX_MAX_CODE_LEN;
         }
+    }
+    return bad;
+}
+
+// Decodes tile b of tensor t (staged in slot buf) into sh.stage.  Returns
+// false, uniformly, when the tile must be skipped.
+__device__ __forceinline__ bool decode_tile(Shared& sh, const uint32_t* stream, const TensorArgs& t, uint64_t b, int buf,
+                            int32_t* status, uint64_t& o0, uint64_t& o1) {
+    const int tid = threadIdx.x;
+    const uint32_t T = t.chunk_bytes;
+    const uint32_t chunk_bits = 8u * T;
+    const uint64_t c0 = b * kThreads;
+    o0 = sh.block_pair[buf][0];
+    o1 = sh.block_pair[buf][1];
+    if (tid == 0) {
+        sh.tile_ok = 1;
+        // the tile's sign|mantissa bytes are needed after the decode
+        if (o0 < o1 && o1 <= t.n) {
+            const uint64_t a0 = o0 & ~uint64_t(15), a1 = (o1 + 15) & ~uint64_t(15);
+            prefetch_l2(t.sm + a0, static_cast<uint32_t>(a1 - a0));
+        }
+    }
+
+    const uint32_t entry = (c0 + tid < t.n_chunks) ? sh.chunk[buf][tid] : 0u;
+    const uint32_t gap = entry & 31u;
+    uint32_t cnt = entry >> 5;
+    bool bad = false;
+    if (gap > 23u || cnt > chunk_bits - gap) {
+        bad = true;
+        cnt = 0;
+    }
+    uint32_t total = 0;
+    const uint32_t off = block_exclusive_scan(sh, cnt, &total);  // contains a __syncthreads
+    const bool last_ok = b + 1 != t.n_blocks || o1 == t.n;       // the block index ends at n
+    if (o1 < o0 || o1 - o0 != total || total > AFX_BLOCK_CAPACITY || o1 > t.n || !last_ok) {
+        if (tid == 0) raise_status(status, AFX_DEV_BAD_BLOCK);
+        return false;
+    }
+
+    if (cnt) {
+        const uint32_t next = (c0 + tid + 1 < t.n_chunks) ? sh.chunk[buf][tid + 1] : 0u;
+        bad = decode_run(sh, stream, stream_stage_bytes(t, b) >> 2, tid * (T >> 2), gap, cnt, sh.stage,
+                         static_cast<uint32_t>(o0 & 7u) + off, next, (tid + 1) * chunk_bits);
     }
     if (bad) {
         raise_status(status, AFX_DEV_BAD_CHUNK);
@@ -517,43 +532,42 @@ __device__ __forceinline__ bool decode_tile(Shared& sh, const uint32_t* stream, 
 
 // ---- epilogues ---------------------------------------------------------------------
 
-// Joins and stores the tile's weights.  The first and last group of 8 may
-// be shared with the neighbouring tiles and go out weight by weight; the
-// full groups in between are handled kUnroll per thread at a time so that
-// their sign|mantissa loads are in flight together.
-__device__ __forceinline__ void store_tile(const Shared& sh, const TensorArgs& t, uint64_t o0, uint64_t o1) {
+// Joins and stores weights [o0, o1) whose rotated exponents are at
+// stage[o - (o0 & ~7)], with NT threads (thread index tid).  The first and
+// last group of 8 may be shared with neighbouring ranges and go out weight
+// by weight; the full groups in between are handled kUnroll per thread at a
+// time so that their sign|mantissa loads are in flight together.
+template <int NT>
+__device__ __forceinline__ void store_range(const uint8_t* stage, const TensorArgs& t, uint64_t o0, uint64_t o1,
+                                            int tid) {
     constexpr int kUnroll = 4;
     const uint64_t ob0 = o0 & ~uint64_t(7);
     const uint64_t f0 = (o0 + 7) >> 3, f1 = o1 >> 3;  // full groups [f0, f1)
-    const int tid = threadIdx.x;
-    const uint64_t gh = o0 >> 3, gt = o1 >> 3;
-    const bool head_partial = (o0 & 7) != 0, tail_partial = (o1 & 7) != 0;
-    // thread 0: the partial head group; thread 1: the partial tail group,
-    // unless it is the same group as the head
-    const bool mine = (tid == 0 && head_partial) || (tid == 1 && tail_partial && !(head_partial && gt == gh));
-    if (mine) {
-        const uint64_t ob = (tid == 0 ? gh : gt) << 3;
-        for (uint32_t q = 0; q < 8; ++q) {
-            const uint64_t o = ob + q;
-            if (o >= o0 && o < o1) t.out[o] = join1(sh.stage[static_cast<uint32_t>(o - ob0)], t.sm[o]);
-        }
+    // weights outside the full groups (at most 7 at each end): threads 0-7
+    // take the first group's, threads 8-15 the last group's, one weight each
+    if (tid < 16) {
+        const uint64_t o = (tid < 8 ? (o0 & ~uint64_t(7)) : (o1 & ~uint64_t(7))) + (tid & 7);
+        const bool outside_full = o < (f0 << 3) || o >= (f1 << 3);
+        const bool twice = tid >= 8 && (o0 >> 3) == (o1 >> 3);  // one group holds both ends
+        if (o >= o0 && o < o1 && outside_full && !twice)
+            t.out[o] = join1(stage[static_cast<uint32_t>(o - ob0)], t.sm[o]);
     }
     if (f1 <= f0) return;
     // full groups, indexed from the first one in 32-bit arithmetic
     const uint32_t nfull = static_cast<uint32_t>(f1 - f0);
     const uint2* smp = reinterpret_cast<const uint2*>(t.sm + (f0 << 3));
     uint4* outp = reinterpret_cast<uint4*>(t.out + (f0 << 3));
-    const uint8_t* stp = sh.stage + static_cast<uint32_t>((f0 << 3) - ob0);
-    for (uint32_t j = tid; j < nfull; j += kThreads * kUnroll) {
+    const uint8_t* stp = stage + static_cast<uint32_t>((f0 << 3) - ob0);
+    for (uint32_t j = tid; j < nfull; j += NT * kUnroll) {
         uint2 s8[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-            const uint32_t jj = j + u * kThreads;
+            const uint32_t jj = j + u * NT;
             if (jj < nfull) s8[u] = __ldg(smp + jj);
         }
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
-            const uint32_t jj = j + u * kThreads;
+            const uint32_t jj = j + u * NT;
             if (jj < nfull) {
                 const uint2 e8 = *reinterpret_cast<const uint2*>(stp + 8 * jj);
                 __stcs(outp + jj, join8(e8, s8[u]));
@@ -706,11 +720,12 @@ __device__ __forceinline__ void gemv_tile(const Shared& sh, const TensorArgs& t,
     }
 }
 
-// ---- the restore kernel ------------------------------------------------------------
+// ---- the fused GEMV kernel ---------------------------------------------------------
 //
-// B == 0: store the BF16 weights; B in 1..4: fused GEMV with B activation rows.
+// B in 1..4 activation rows; whole blocks per CTA tile.
 template <int B>
-__global__ void __launch_bounds__(kThreads, B == 0 ? 3 : 2) restore_kernel(const __grid_constant__ LaunchArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) restore_kernel(const __grid_constant__ LaunchArgs a) {
+    static_assert(B >= 1 && B <= kMaxBatch, "restore_kernel is the fused GEMV path");
     extern __shared__ __align__(16) uint8_t smem[];
     Shared& sh = *reinterpret_cast<Shared*>(smem);
     uint8_t* stream_base = smem + shared_fixed_bytes();
@@ -741,7 +756,7 @@ __global__ void __launch_bounds__(kThreads, B == 0 ? 3 : 2) restore_kernel(const
         const TensorArgs& t = a.t[k];
         __syncthreads();  // the staged tile is visible; the previous tile is done
         if (built != static_cast<int>(k)) {
-            build_tables(sh, t.tab);
+            build_tables(sh, reinterpret_cast<uint16_t*>(sh.stage), t.tab);
             built = static_cast<int>(k);
         }
         const uint64_t b = g - t.tile_begin;
@@ -749,12 +764,188 @@ __global__ void __launch_bounds__(kThreads, B == 0 ? 3 : 2) restore_kernel(const
         const uint32_t* stream =
             reinterpret_cast<const uint32_t*>(stream_base + static_cast<size_t>(buf) * stream_stride);
         if (decode_tile(sh, stream, t, b, buf, a.status, o0, o1) && o0 < o1) {
-            if constexpr (B == 0)
-                store_tile(sh, t, o0, o1);
-            else
-                gemv_tile<B>(sh, t, b, o0, o1, part, warp_row0, warp_nrows);
+            gemv_tile<B>(sh, t, b, o0, o1, part, warp_row0, warp_nrows);
         }
         buf ^= 1;
+    }
+}
+
+// ---- warp-independent restore ------------------------------------------------------
+//
+// The restore (store) path splits every block further into sub-tiles of 32
+// chunks, one warp each.  A CTA still owns a contiguous run of blocks and
+// one copy of the decode tables, but its warps run on their own: each takes
+// a contiguous run of sub-tiles of the current tensor, stages them with
+// cp.async one sub-tile ahead, places its lanes' codes with a warp-shuffle
+// scan, and carries the output index of the next sub-tile forward as a
+// running sum.  The first sub-tile of a run starts at the block index entry
+// of its block plus the counts of that block's earlier chunks.  The running
+// sum is checked against the block index at every block boundary that a run
+// crosses or ends on, so every entry of the block index is verified.  The
+// only CTA barriers are those around a rebuild of the tables.
+
+constexpr int kWarpChunks = 32;                                  // chunks per sub-tile
+constexpr int kSubtilesPerBlock = kThreads / kWarpChunks;        // 16
+constexpr int kMaxChunkCodes = AFX_BLOCK_CAPACITY / kThreads;    // codes one chunk may hold
+constexpr int kWarpStage = kWarpChunks * kMaxChunkCodes + 16;    // exponents of one sub-tile
+constexpr int kWarpChunkStage = 40;                              // 33 entries staged (80 bytes)
+
+struct WarpSlot {
+    alignas(16) uint16_t chunk[2][kWarpChunkStage];
+    alignas(16) uint8_t stage[kWarpStage];
+};
+
+struct SharedW {
+    uint32_t lut[kLutSize];
+    uint8_t len0[kLutSize];
+    uint32_t limit[AFX_MAX_CODE_LEN + 1];
+    int32_t base[AFX_MAX_CODE_LEN + 1];
+    uint8_t sorted[256];
+    alignas(16) WarpSlot w[kWarps];
+    // dynamic part: per warp two stream buffers of kWarpChunks * max_T + kStreamPad bytes
+};
+
+constexpr size_t sharedw_fixed_bytes() { return (sizeof(SharedW) + 15) & ~size_t(15); }
+static_assert(sizeof(WarpSlot) % 16 == 0 && offsetof(WarpSlot, stage) % 16 == 0, "warp slots stay 16-byte aligned");
+
+__device__ __forceinline__ uint32_t warp_stream_bytes(const TensorArgs& t, uint64_t s) {
+    const uint64_t byte0 = s * kWarpChunks * t.chunk_bytes;
+    const uint64_t want = static_cast<uint64_t>(kWarpChunks) * t.chunk_bytes + kStreamPad;
+    const uint64_t avail = t.exp_bytes > byte0 ? t.exp_bytes - byte0 : 0;
+    return static_cast<uint32_t>(want < avail ? want : avail);
+}
+
+// cp.async of sub-tile s (its stream words and 33 chunk entries) into slot buf.
+__device__ __forceinline__ void warp_issue(WarpSlot& ws, uint8_t* wstream, uint32_t wstride, const TensorArgs& t,
+                                           uint64_t s, int buf, int lane) {
+    uint8_t* dst = wstream + static_cast<size_t>(buf) * wstride;
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(t.exp_words) + s * kWarpChunks * t.chunk_bytes;
+    const uint32_t bytes = warp_stream_bytes(t, s);
+    for (uint32_t i = lane * 16u; i < bytes; i += 32 * 16u) cp_async16(dst + i, src + i);
+    const uint64_t cb0 = s * kWarpChunks * 2;
+    const uint64_t csec = (t.n_chunks * 2 + 15) & ~uint64_t(15);
+    const uint64_t cavail = csec > cb0 ? csec - cb0 : 0;
+    const uint32_t cbytes = static_cast<uint32_t>(cavail < kWarpChunkStage * 2 ? cavail : kWarpChunkStage * 2);
+    if (lane * 16u < cbytes)
+        cp_async16(reinterpret_cast<uint8_t*>(ws.chunk[buf]) + lane * 16,
+                   reinterpret_cast<const uint8_t*>(t.chunk_index) + cb0 + lane * 16);
+    cp_async_commit();
+}
+
+__device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, d);
+    return v;
+}
+
+// Restores sub-tiles [s0, s1) of tensor t with one warp.
+__device__ __forceinline__ void warp_run(const SharedW& sh, WarpSlot& ws, uint8_t* wstream, uint32_t wstride,
+                                         const TensorArgs& t, uint64_t s0, uint64_t s1, int lane, int32_t* status) {
+    const uint32_t T = t.chunk_bytes;
+    const uint32_t chunk_bits = 8u * T;
+    const uint64_t n_sub = (t.n_chunks + kWarpChunks - 1) / kWarpChunks;
+    // the output index of sub-tile s0's first code
+    const uint64_t blk = s0 / kSubtilesPerBlock;
+    uint32_t pre = 0;
+    for (uint64_t c = blk * kThreads + lane; c < s0 * kWarpChunks; c += 32) pre += __ldg(t.chunk_index + c) >> 5;
+    pre = warp_sum(pre);
+    uint64_t start = __ldg(t.block_index + blk) + pre;
+    if (s0 == 0 && start != 0 && lane == 0) raise_status(status, AFX_DEV_BAD_BLOCK);
+    warp_issue(ws, wstream, wstride, t, s0, 0, lane);
+    int buf = 0;
+    for (uint64_t s = s0; s < s1; ++s) {
+        if (s + 1 < s1) {
+            warp_issue(ws, wstream, wstride, t, s + 1, buf ^ 1, lane);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncwarp();
+        if (s != s0 && s % kSubtilesPerBlock == 0) {  // a block boundary inside the run
+            const uint64_t bo = __ldg(t.block_index + s / kSubtilesPerBlock);
+            if (bo != start) {
+                if (lane == 0) raise_status(status, AFX_DEV_BAD_BLOCK);
+                start = bo;
+            }
+        }
+        const uint64_t c = s * kWarpChunks + lane;
+        const uint32_t entry = c < t.n_chunks ? ws.chunk[buf][lane] : 0u;
+        const uint32_t gap = entry & 31u;
+        uint32_t cnt = entry >> 5;
+        bool bad = false;
+        if (gap > 23u || cnt > chunk_bits - gap || cnt > static_cast<uint32_t>(kMaxChunkCodes)) {
+            bad = true;
+            cnt = 0;
+        }
+        uint32_t inc = cnt;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+            if (lane >= d) inc += o;
+        }
+        const uint32_t total = __shfl_sync(0xFFFFFFFFu, inc, 31);
+        const uint64_t o0 = start, o1 = start + total;
+        const bool in_range = o1 <= t.n;
+        if (lane == 0) {
+            if (!in_range)
+                raise_status(status, AFX_DEV_BAD_BLOCK);
+            else if (o0 < o1) {  // the sign|mantissa bytes are needed after the decode
+                const uint64_t a0 = o0 & ~uint64_t(15), a1 = (o1 + 15) & ~uint64_t(15);
+                prefetch_l2(t.sm + a0, static_cast<uint32_t>(a1 - a0));
+            }
+        }
+        if (cnt && in_range) {
+            const uint32_t next = (c + 1 < t.n_chunks) ? ws.chunk[buf][lane + 1] : 0u;
+            const uint32_t* stream = reinterpret_cast<const uint32_t*>(wstream + static_cast<size_t>(buf) * wstride);
+            bad = decode_run(sh, stream, warp_stream_bytes(t, s) >> 2, lane * (T >> 2), gap, cnt, ws.stage,
+                             static_cast<uint32_t>(o0 & 7u) + (inc - cnt), next, (lane + 1) * chunk_bits);
+        }
+        if (bad) raise_status(status, AFX_DEV_BAD_CHUNK);
+        const bool any_bad = __any_sync(0xFFFFFFFFu, bad);
+        __syncwarp();
+        if (!any_bad && in_range && o0 < o1) store_range<32>(ws.stage, t, o0, o1, lane);
+        start = o1;
+        buf ^= 1;
+        __syncwarp();
+    }
+    // a run that ends on a block boundary checks the block index there; the
+    // last run checks that the codes and the block index both end at n
+    if (lane == 0) {
+        if (s1 < n_sub && s1 % kSubtilesPerBlock == 0) {
+            if (__ldg(t.block_index + s1 / kSubtilesPerBlock) != start) raise_status(status, AFX_DEV_BAD_BLOCK);
+        }
+        if (s1 == n_sub && (start != t.n || __ldg(t.block_index + t.n_blocks) != t.n))
+            raise_status(status, AFX_DEV_BAD_BLOCK);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 3) restore_store_kernel(const __grid_constant__ LaunchArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    SharedW& sh = *reinterpret_cast<SharedW*>(smem);
+    uint8_t* stream_all = smem + sharedw_fixed_bytes();
+    const uint32_t wstride = kWarpChunks * a.max_chunk_bytes + kStreamPad;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    WarpSlot& ws = sh.w[warp];
+    uint8_t* wstream = stream_all + static_cast<size_t>(warp) * 2 * wstride;
+
+    const uint64_t g_begin = a.total_tiles * blockIdx.x / gridDim.x;
+    const uint64_t g_end = a.total_tiles * (blockIdx.x + 1) / gridDim.x;
+    if (g_begin >= g_end) return;
+    for (uint32_t k = 0; k < a.count; ++k) {
+        const TensorArgs& t = a.t[k];
+        const uint64_t t0 = t.tile_begin, t1 = t.tile_begin + t.n_blocks;
+        if (t1 <= g_begin) continue;
+        if (t0 >= g_end) break;
+        // this tensor's blocks in the CTA's run, as sub-tiles
+        const uint64_t b0 = (g_begin > t0 ? g_begin : t0) - t0, b1 = (g_end < t1 ? g_end : t1) - t0;
+        const uint64_t n_sub = (t.n_chunks + kWarpChunks - 1) / kWarpChunks;
+        const uint64_t sb = b0 * kSubtilesPerBlock;
+        const uint64_t se = b1 * kSubtilesPerBlock < n_sub ? b1 * kSubtilesPerBlock : n_sub;
+        __syncthreads();  // every warp is done with the previous tensor's tables and buffers
+        build_tables(sh, reinterpret_cast<uint16_t*>(stream_all), t.tab);  // ends with __syncthreads
+        const uint64_t span = se - sb;
+        const uint64_t s0 = sb + span * warp / kWarps, s1 = sb + span * (warp + 1) / kWarps;
+        if (s0 < s1) warp_run(sh, ws, wstream, wstride, t, s0, s1, lane, a.status);
     }
 }
 
@@ -955,23 +1146,33 @@ afx_status launch_restore(LaunchArgs& la, cudaStream_t s) {
     if (la.count == 0 || la.total_tiles == 0) return AFX_OK;
     const int sms = sm_count();
     if (sms <= 0) return afx_fail(AFX_E_CUDA, "cannot query the SM count", 0);
-    size_t smem = shared_fixed_bytes() + 2 * (static_cast<size_t>(kThreads) * la.max_chunk_bytes + kStreamPad);
-    if (B)
+    if constexpr (B == 0) {
+        const size_t streams = static_cast<size_t>(kWarps) * 2 * (kWarpChunks * la.max_chunk_bytes + kStreamPad);
+        const size_t smem = sharedw_fixed_bytes() + (streams > 8192 ? streams : 8192);  // 8 KB: table-build scratch
+        if (smem > 227 * 1024) return afx_fail(AFX_E_ARG, "launch needs too much shared memory", 0);
+        int per_sm = 0;
+        const afx_status st = prepare_kernel(reinterpret_cast<const void*>(restore_store_kernel), smem, &per_sm);
+        if (st != AFX_OK) return st;
+        const uint64_t grid = std::min<uint64_t>(la.total_tiles, static_cast<uint64_t>(sms) * per_sm);
+        restore_store_kernel<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(la);
+        AFX_CUDA_TRY(cudaGetLastError(), "restore_store_kernel launch");
+        return AFX_OK;
+    } else {
+        size_t smem = shared_fixed_bytes() + 2 * (static_cast<size_t>(kThreads) * la.max_chunk_bytes + kStreamPad);
         smem += static_cast<size_t>(kWarps) * la.max_rows_per_warp * B * sizeof(float) +
                 kWarps * (sizeof(uint64_t) + sizeof(uint32_t));
-    if (smem > 227 * 1024) return afx_fail(AFX_E_ARG, "launch needs too much shared memory", 0);
-    int per_sm = 0;
-    const afx_status st = prepare_kernel(reinterpret_cast<const void*>(restore_kernel<B>), smem, &per_sm);
-    if (st != AFX_OK) return st;
-    const uint64_t grid = std::min<uint64_t>(la.total_tiles, static_cast<uint64_t>(sms) * per_sm);
-    restore_kernel<B><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(la);
-    AFX_CUDA_TRY(cudaGetLastError(), "restore_kernel launch");
-    if (B) {
+        if (smem > 227 * 1024) return afx_fail(AFX_E_ARG, "launch needs too much shared memory", 0);
+        int per_sm = 0;
+        const afx_status st = prepare_kernel(reinterpret_cast<const void*>(restore_kernel<B>), smem, &per_sm);
+        if (st != AFX_OK) return st;
+        const uint64_t grid = std::min<uint64_t>(la.total_tiles, static_cast<uint64_t>(sms) * per_sm);
+        restore_kernel<B><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(la);
+        AFX_CUDA_TRY(cudaGetLastError(), "restore_kernel launch");
         const unsigned fix_blocks = static_cast<unsigned>((la.total_tiles + 127) / 128);
         gemv_fixup_kernel<B><<<fix_blocks, 128, 0, s>>>(la);
         AFX_CUDA_TRY(cudaGetLastError(), "gemv_fixup_kernel launch");
+        return AFX_OK;
     }
-    return AFX_OK;
 }
 
 void reset_launch(LaunchArgs& la) {
