@@ -196,6 +196,32 @@ afx_status afx_decode_gemv_batch(const afx_desc* descs, const void* const* conta
                                  float* const* ys_dev, void* const* workspaces_dev, const uint64_t* workspace_bytes,
                                  uint32_t count, afx_stream_t stream, int32_t* status_dev);
 
+/* Size of the device workspace that afx_decode_gemv_static owns: 1 MiB,
+ * enough for a batch-4 product over a container of up to 32,768 blocks
+ * (about 800M weights of N(0, 0.02) BF16). */
+#define AFX_STATIC_WORKSPACE_BYTES (1u << 20)
+
+/* afx_decode_gemv without the workspace argument, for callers that cannot
+ * allocate device memory: for example a plugin called from inside another
+ * runtime's enqueue step, where that runtime owns every device allocation,
+ * or code that must not pay for cudaMalloc synchronising the device.  The
+ * workspace is a file-scope device array of AFX_STATIC_WORKSPACE_BYTES in
+ * this library, held by every GPU that loads it until the process exits;
+ * the call itself allocates nothing.  The first call on a device looks up
+ * that array's device address (cudaGetSymbolAddress) with the device
+ * current, so make that first call before any stream capture.  Every call
+ * shares the one array and it keeps the last call's contents (nothing in
+ * it needs to start at zero: each value read is written earlier in the same
+ * call), so calls that overlap on the GPU, on any streams, race; run them
+ * one after another.  Arguments, results and errors as afx_decode_gemv;
+ * AFX_E_NOSPACE (with a message in afx_last_error) when the container needs
+ * more workspace than AFX_STATIC_WORKSPACE_BYTES.
+ * No counterpart on the pages: this is a deployment convenience of the
+ * library, not part of the method. */
+afx_status afx_decode_gemv_static(const afx_desc* desc, const void* container_dev, uint32_t rows, uint32_t cols,
+                                  const uint16_t* x_dev, uint32_t batch, float* y_dev, afx_stream_t stream,
+                                  int32_t* status_dev);
+
 /* One tensor of a streamed layer. */
 typedef enum afx_op_kind { AFX_OP_DECODE = 0, AFX_OP_GEMV = 1 } afx_op_kind;
 

@@ -28,6 +28,7 @@ AFX_DEV_BAD_BLOCK, AFX_DEV_BAD_CHUNK, AFX_DEV_BAD_CODE, AFX_DEV_BAD_SHAPE = 0x1,
 AFX_MAX_CODE_LEN = 24
 AFX_BLOCK_CAPACITY = 32768
 AFX_HEADER_BYTES = 512
+AFX_STATIC_WORKSPACE_BYTES = 1 << 20
 AFX_OP_DECODE, AFX_OP_GEMV = 0, 1
 
 
@@ -103,6 +104,7 @@ _lib.afx_decode_batch.argtypes = [ctypes.POINTER(afx_desc), _PP, _PP, _u32, _vp,
 _lib.afx_decode_gemv_batch.argtypes = [ctypes.POINTER(afx_desc), _PP, ctypes.POINTER(ctypes.c_uint32),
                                        ctypes.POINTER(ctypes.c_uint32), _PP, _u32, _PP, _PP,
                                        ctypes.POINTER(ctypes.c_uint64), _u32, _vp, _i32p]
+_lib.afx_decode_gemv_static.argtypes = [ctypes.POINTER(afx_desc), _vp, _u32, _u32, _vp, _u32, _vp, _vp, _i32p]
 _lib.afx_stream_run.argtypes = [ctypes.POINTER(afx_layer), _u32, ctypes.POINTER(ctypes.c_void_p), _u32, _u64, _vp,
                                 _vp, _i32p]
 _lib.afx_last_error.argtypes = []
@@ -111,7 +113,7 @@ _lib.afx_status_string.argtypes = [ctypes.c_int]
 _lib.afx_status_string.restype = ctypes.c_char_p
 for _f in (_lib.afx_build_code, _lib.afx_encode_bound, _lib.afx_encode, _lib.afx_parse_header, _lib.afx_decode,
            _lib.afx_decode_batch, _lib.afx_decode_gemv_workspace, _lib.afx_decode_gemv, _lib.afx_decode_gemv_batch,
-           _lib.afx_stream_run):
+           _lib.afx_decode_gemv_static, _lib.afx_stream_run):
     _f.restype = ctypes.c_int
 
 
@@ -131,7 +133,7 @@ def afx_status_string(status: int) -> str:
 
 def _check(fn: str, st: int) -> None:
     if st != AFX_OK:
-        raise AfxError(fn, st, afx_last_error() if st == AFX_E_CUDA else "")
+        raise AfxError(fn, st, afx_last_error() if st in (AFX_E_CUDA, AFX_E_NOSPACE) else "")
 
 
 def _host_u16(w) -> np.ndarray:
@@ -246,6 +248,17 @@ def afx_decode_gemv(desc: afx_desc, container_dev, rows: int, cols: int, x_dev, 
     _check("afx_decode_gemv", _lib.afx_decode_gemv(
         ctypes.byref(desc), _dev_ptr(container_dev), rows, cols, _dev_ptr(x_dev), batch, _dev_ptr(y_dev),
         _dev_ptr(workspace_dev), ws_bytes, _stream_handle(stream), _dev_ptr(status_dev)))
+
+
+def afx_decode_gemv_static(desc: afx_desc, container_dev, rows: int, cols: int, x_dev, y_dev, stream=None,
+                           status_dev=None) -> None:
+    """afx_decode_gemv with the library's own fixed device workspace (no allocation by the call)."""
+    batch = x_dev.shape[0] if x_dev.dim() == 2 else 1
+    if y_dev.numel() < batch * rows:
+        raise ValueError("y_dev too small")
+    _check("afx_decode_gemv_static", _lib.afx_decode_gemv_static(
+        ctypes.byref(desc), _dev_ptr(container_dev), rows, cols, _dev_ptr(x_dev), batch, _dev_ptr(y_dev),
+        _stream_handle(stream), _dev_ptr(status_dev)))
 
 
 def afx_stream_run(layers, dev_bufs, buf_bytes: int, compute_stream=None, copy_stream=None, status_dev=None) -> None:

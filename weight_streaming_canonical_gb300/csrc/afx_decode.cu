@@ -1325,3 +1325,59 @@ extern "C" afx_status afx_decode_gemv(const afx_desc* desc, const void* containe
     return afx_decode_gemv_batch(desc, &container, &rows, &cols, &x, batch, &y, &workspace, &workspace_bytes, 1,
                                  stream, status);
 }
+
+// ---- fused restore + GEMV with a fixed, library-owned workspace -------------------
+//
+// For callers that must not allocate device memory themselves: the
+// workspace of the fused GEMV lives in one file-scope device array of
+// AFX_STATIC_WORKSPACE_BYTES that every GPU loading the library holds until
+// the process exits.  The array's name in host code is only a stand-in, so
+// its device address is looked up once per device with
+// cudaGetSymbolAddress, with that device current, on the first call made
+// on that device.
+
+static __device__ __align__(256) float g_static_workspace[AFX_STATIC_WORKSPACE_BYTES / sizeof(float)];
+
+namespace {
+
+std::mutex g_static_mutex;
+void* g_static_workspace_ptr[afx::kMaxDevices] = {};
+
+afx_status static_workspace(void** ptr) {
+    int dev = -1;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return afx_fail(AFX_E_CUDA, "cudaGetDevice", e);
+    if (dev < 0 || dev >= afx::kMaxDevices) return afx_fail(AFX_E_CUDA, "device ordinal out of range", 0);
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    if (!g_static_workspace_ptr[dev]) {
+        void* p = nullptr;
+        const cudaError_t r = cudaGetSymbolAddress(&p, g_static_workspace);
+        if (r != cudaSuccess) return afx_fail(AFX_E_CUDA, "cudaGetSymbolAddress", r);
+        g_static_workspace_ptr[dev] = p;
+    }
+    *ptr = g_static_workspace_ptr[dev];
+    return AFX_OK;
+}
+
+}  // namespace
+
+extern "C" afx_status afx_decode_gemv_static(const afx_desc* desc, const void* container, uint32_t rows,
+                                             uint32_t cols, const uint16_t* x, uint32_t batch, float* y,
+                                             afx_stream_t stream, int32_t* status) {
+    if (!desc) return afx_fail(AFX_E_ARG, "null description", 0);
+    if (batch < 1 || batch > static_cast<uint32_t>(afx::kMaxBatch)) return afx_fail(AFX_E_ARG, "batch must be 1..4", 0);
+    const afx_status st = afx_check_desc(desc);
+    if (st != AFX_OK) return afx_fail(st, "invalid container description", 0);
+    const uint64_t need = afx_gemv_workspace_bytes(desc->n_blocks, batch);
+    if (desc->nsym >= 2 && need > AFX_STATIC_WORKSPACE_BYTES) {
+        char msg[160];
+        snprintf(msg, sizeof msg,
+                 "this container needs %llu bytes of GEMV workspace; the static workspace holds %u bytes",
+                 static_cast<unsigned long long>(need), static_cast<unsigned>(AFX_STATIC_WORKSPACE_BYTES));
+        return afx_fail(AFX_E_NOSPACE, msg, 0);
+    }
+    void* ws = nullptr;
+    const afx_status ws_st = static_workspace(&ws);
+    if (ws_st != AFX_OK) return ws_st;
+    return afx_decode_gemv(desc, container, rows, cols, x, batch, y, ws, AFX_STATIC_WORKSPACE_BYTES, stream, status);
+}
