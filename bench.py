@@ -177,6 +177,24 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu capture of `kernel`, or
+    None when that capture was of another workload or the kernel source has
+    changed since (the sha256 of the source is stored with the counters)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"{kernel}.traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+    except (OSError, KeyError, ValueError):
+        return None
+    if sha != rec.get("source_sha256") or workload != "layer":
+        return None
+    return int(rec["dram_bytes_per_launch"])
+
+
 def measured_hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -357,7 +375,8 @@ def run_ours(args):
     peak, peak_kind = measured_hbm_peak()
     achieved = alg_total / (kernel_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": None, "kernel": "restore_store_kernel", "peak_kind": peak_kind,
+                "traffic": profiled_traffic("restore_store_kernel", args.workload),
+                "kernel": "restore_store_kernel", "peak_kind": peak_kind,
                 "launches_per_step": 1, "algorithmic_bytes_per_step": alg_total,
                 "kernel_ms_per_step": kernel_ms}
 
