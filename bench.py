@@ -405,6 +405,16 @@ def run_ours(args):
     if not args.no_extras and rank == 0:
         line["e2e"] = run_e2e(afx, parts, views, dev, args)
         line["cpu_baseline"] = run_cpu_baseline(parts)
+        if args.workload == "layer":
+            line["fused_gemv"] = run_gemv_bench(afx, parts, dev_blob, offs, dev, args)
+            line["streamed_40_layers"] = run_stream_bench(afx, parts, dev, args)
+            # "Why Weight Offloading Slows Inference", Eq. (2): compression pays
+            # when (S - S_disk) / b > t_unpack; here b is the measured link
+            S, S_disk = 2 * n_total, comp_total
+            b = line["streamed_40_layers"]["batch1"]["h2d_gbs"] * 1e9
+            line["eq2_break_even"] = {"S_bytes": S, "S_disk_bytes": S_disk, "b_link_gbs": b / 1e9,
+                                      "read_time_saved_ms": (S - S_disk) / b * 1e3, "t_unpack_ms": ms,
+                                      "pays": (S - S_disk) / b > ms * 1e-3}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -460,6 +470,165 @@ def run_e2e(afx, parts, views, dev, args):
     return {"value": 2 * n / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
             "h2d_bytes_per_step": int(sum(b.numel() for b in blobs)), "d2h_bytes_per_step": 2 * n,
             "bit_exact": bool(ok), "path": "afx_stream_run (pinned host containers) + D2H of the BF16 layer"}
+
+
+def _layer_ops(afx, parts, B, dev, keep):
+    """Ops for one streamed layer (its containers back to back in one blob):
+    the two norms restored, the seven matrices through the fused GEMV with B
+    activation rows."""
+    import torch
+    from weight_streaming_canonical_gb300 import synth
+    shapes = {name: shape for name, shape, _ in synth.LAYER_TENSORS}
+    kinds = {name: kind for name, _, kind in synth.LAYER_TENSORS}
+    offs = np.cumsum([0] + [c.size for _, _, c, _ in parts])[:-1]
+    ops = []
+    for (name, w, c, d), off in zip(parts, offs):
+        op = afx.afx_op()
+        op.desc = d
+        op.offset = int(off)
+        if kinds.get(name) == "norm":
+            out = torch.empty(d.n, dtype=torch.int16, device=dev)
+            op.kind = afx.AFX_OP_DECODE
+            op.out_dev = out.data_ptr()
+            keep.append(out)
+        else:
+            rows, cols = shapes[name]
+            x = torch.from_numpy(synth.activations(B, cols, seed=11).view(np.int16)).to(dev)
+            y = torch.empty((B, rows), dtype=torch.float32, device=dev)
+            ws = torch.empty(afx.afx_decode_gemv_workspace(d, B) // 4 + 4, dtype=torch.float32, device=dev)
+            op.kind = afx.AFX_OP_GEMV
+            op.rows, op.cols, op.batch = rows, cols, B
+            op.x_dev, op.out_dev, op.workspace_dev = x.data_ptr(), y.data_ptr(), ws.data_ptr()
+            op.workspace_bytes = ws.numel() * 4
+            keep.extend([x, y, ws])
+        ops.append(op)
+    return ops
+
+
+def run_gemv_bench(afx, parts, dev_blob, offs, dev, args):
+    """Fused restore + GEMV over the layer's seven matrices in one launch,
+    batch 1 and 4, containers resident in HBM."""
+    import torch
+    from weight_streaming_canonical_gb300 import synth
+    shapes = {name: shape for name, shape, _ in synth.LAYER_TENSORS}
+    res = {}
+    mats = [(name, d, off) for (name, _, _, d), off in zip(parts, offs) if name in shapes and len(shapes[name]) == 2]
+    n = sum(d.n for _, d, _ in mats)
+    comp = sum((d.total_bits + 7) // 8 + d.n + 2 * d.n_chunks + 8 * (d.n_blocks + 1) for _, d, _ in mats)
+    for B in (1, 4):
+        xs, ys, wss = [], [], []
+        for name, d, off in mats:
+            rows, cols = shapes[name]
+            xs.append(torch.from_numpy(synth.activations(B, cols, seed=5).view(np.int16)).to(dev))
+            ys.append(torch.empty((B, rows), dtype=torch.float32, device=dev))
+            wss.append(torch.empty(afx.afx_decode_gemv_workspace(d, B) // 4 + 4, dtype=torch.float32, device=dev))
+        descs = [d for _, d, _ in mats]
+        conts = [dev_blob[off:off + d.container_bytes] for _, d, off in mats]
+        shp = [shapes[name] for name, _, _ in mats]
+        stream = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(stream):
+            for _ in range(max(3, args.warmup)):
+                afx.afx_decode_gemv_batch(descs, conts, shp, xs, ys, wss)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                afx.afx_decode_gemv_batch(descs, conts, shp, xs, ys, wss)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        res[f"batch{B}"] = {"ms": ms, "weights_per_s": n / (ms * 1e-3), "compressed_read_gbs": comp / (ms * 1e-3) / 1e9,
+                            "launches": "one restore_kernel<B> and one fix-up per product batch"}
+    res["weights"] = n
+    return res
+
+
+def run_stream_bench(afx, parts, dev, args, layers=40):
+    """40 streamed layer steps: compressed layers in pinned host memory, the
+    copy of layer l+1 overlapped with layer l's restore (norms) and fused
+    GEMVs (matrices), against the same copies alone and the same ops alone."""
+    import torch
+    blob_host = []
+    for seed_shift in (0, 1):
+        ps = parts if seed_shift == 0 else build_layer(args.seed + 1)
+        size = sum(c.size for _, _, c, _ in ps)
+        b = torch.empty(size, dtype=torch.uint8).pin_memory()
+        o = 0
+        for _, _, c, _ in ps:
+            b.numpy()[o:o + c.size] = c
+            o += c.size
+        blob_host.append((b, ps))
+    buf_bytes = max(b.numel() for b, _ in blob_host)
+    bufs = [torch.empty(buf_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    compute, copy = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    out = {"layers": layers, "distinct_pinned_layers": len(blob_host),
+           "layer_compressed_bytes": int(blob_host[0][0].numel())}
+    for B in (1, 4):
+        keep = []
+        ops_per_blob = [_layer_ops(afx, ps, B, dev, keep) for _, ps in blob_host]
+        seq = [(blob_host[l % 2][0], ops_per_blob[l % 2]) for l in range(layers)]
+        copies_only = [(blob_host[l % 2][0], []) for l in range(layers)]
+
+        def timed(layer_list):
+            for _ in range(2):
+                afx.afx_stream_run(layer_list, bufs, buf_bytes, compute, copy)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = 3
+            e0.record(compute)
+            for _ in range(reps):
+                afx.afx_stream_run(layer_list, bufs, buf_bytes, compute, copy)
+            e1.record(compute)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / reps
+
+        step_ms = timed(seq)
+        copy_ms = timed(copies_only)
+        # the same ops with every layer already on the device: no copies at all
+        dev_blobs = [b.to(dev) for b, _ in blob_host]
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(compute):
+            e0.record(compute)
+            for l in range(layers):
+                ops = ops_per_blob[l % 2]
+                i = 0
+                while i < len(ops):
+                    j = i + 1
+                    while j < len(ops) and ops[j].kind == ops[i].kind:
+                        j += 1
+                    grp = ops[i:j]
+                    conts = [dev_blobs[l % 2][op.offset:op.offset + op.desc.container_bytes] for op in grp]
+                    if grp[0].kind == afx.AFX_OP_DECODE:
+                        outs = [torch.empty(op.desc.n, dtype=torch.int16, device=dev) for op in grp]
+                        afx.afx_decode_batch([op.desc for op in grp], conts, outs)
+                    else:
+                        import ctypes
+                        arr = (afx.afx_desc * len(grp))(*[op.desc for op in grp])
+                        ptrs = lambda xs: (ctypes.c_void_p * len(xs))(*xs)
+                        st = afx._lib.afx_decode_gemv_batch(
+                            arr, ptrs([c.data_ptr() for c in conts]), (ctypes.c_uint32 * len(grp))(*[op.rows for op in grp]),
+                            (ctypes.c_uint32 * len(grp))(*[op.cols for op in grp]), ptrs([op.x_dev for op in grp]), B,
+                            ptrs([op.out_dev for op in grp]), ptrs([op.workspace_dev for op in grp]),
+                            (ctypes.c_uint64 * len(grp))(*[op.workspace_bytes for op in grp]), len(grp),
+                            compute.cuda_stream, None)
+                        assert st == 0
+                    i = j
+            e1.record(compute)
+        torch.cuda.synchronize()
+        compute_ms = e0.elapsed_time(e1)
+        per_layer_copy = copy_ms / layers
+        out[f"batch{B}"] = {"step_ms": step_ms, "copy_only_ms": copy_ms, "compute_only_ms": compute_ms,
+                            "step_over_copy": step_ms / copy_ms,
+                            "hidden": step_ms <= 1.05 * copy_ms + compute_ms / layers,
+                            "h2d_gbs": layers * blob_host[0][0].numel() / (copy_ms * 1e-3) / 1e9,
+                            "per_layer_copy_ms": per_layer_copy, "per_layer_compute_ms": compute_ms / layers}
+        del keep
+    return out
 
 
 def run_cpu_baseline(parts):
