@@ -223,3 +223,28 @@ def test_qwen3_layer_in_one_launch(afx):
 def test_sizes_where_a_cta_owns_several_blocks(afx, n):
     # more blocks than resident CTAs: every warp restores several sub-tiles in a row
     _check(afx, synth.normal(n, seed=n))
+
+
+@pytest.mark.slow
+def test_full_model_resident_bit_exact(afx):
+    """All 362 tensors of the Qwen3-14B-shaped model (14.77B weights) resident
+    on one GPU and restored by batched launches; every restored tensor equals
+    its original bit for bit (compared on the device); the oracle decodes one
+    sampled tensor of every kind as well."""
+    import torch
+    import bench
+    parts = bench.build_layer(0, 0, "model")
+    assert sum(d.n for _, _, _, d in parts) == synth.model_weight_count()
+    conts = [torch.from_numpy(c).cuda() for _, _, c, _ in parts]
+    outs = [torch.empty(d.n, dtype=torch.int16, device="cuda") for _, _, _, d in parts]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    afx.afx_decode_batch([d for *_, d in parts], conts, outs, status_dev=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    for (name, w, _, _), o in zip(parts, outs):
+        assert torch.equal(o, torch.from_numpy(w.reshape(-1).view(np.int16)).cuda()), name
+    sampled = {"embed_tokens", "layers.17.q_proj", "layers.39.input_layernorm", "lm_head"}
+    for (name, w, c, _), o in zip(parts, outs):
+        if name in sampled:
+            ref, st = oracle.decode(c)
+            assert st == oracle.OK and np.array_equal(o.cpu().numpy().view(np.uint16), ref), name

@@ -73,12 +73,18 @@ def model_weight_count() -> int:
 
 def bf16_round(f: np.ndarray) -> np.ndarray:
     """float32 -> BF16 bit patterns (uint16), round to nearest even; NaN stays NaN."""
-    u = np.ascontiguousarray(f, dtype=np.float32).view(np.uint32)
-    r = ((u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)).astype(np.uint16)
-    nan = (u & np.uint32(0x7FFFFFFF)) > np.uint32(0x7F800000)
+    f = np.ascontiguousarray(f, dtype=np.float32)
+    u = f.view(np.uint32)
+    r = u >> np.uint32(16)
+    r &= np.uint32(1)
+    r += np.uint32(0x7FFF)
+    r += u
+    r >>= np.uint32(16)
+    out = r.astype(np.uint16)
+    nan = np.isnan(f)
     if nan.any():
-        r[nan] = ((u[nan] >> np.uint32(16)) | np.uint32(0x40)).astype(np.uint16)
-    return r
+        out[nan] = ((u[nan] >> np.uint32(16)) | np.uint32(0x40)).astype(np.uint16)
+    return out
 
 
 def _rng(seed: int, stream: int, block: int) -> np.random.Generator:
