@@ -36,6 +36,33 @@ def test_every_bf16_pattern_every_chunk_size(afx, T):
     _check(afx, np.concatenate([w, rng.permutation(w), w[::-1]]), chunk_bytes=T)
 
 
+@pytest.mark.parametrize("T", [4, 8, 16])
+def test_byte_steps_every_chunk_size(afx, T):
+    c, d = _check(afx, synth.normal(700_001, seed=T), chunk_bytes=T, out_pad=16)
+    assert d.chunk_bytes == T
+
+
+def test_byte_steps_with_32_byte_chunks(afx):
+    # 16 nearly equally likely exponents: every code is 4 bits, so T = 32 is allowed
+    c, d = _check(afx, synth.exponent_mix(600_011, 16, ratio=0.97, seed=2), out_pad=16)
+    assert d.chunk_bytes == 32 and min(l for l in d.len if l) == 4
+
+
+@pytest.mark.parametrize("nsym", [57, 58])
+def test_largest_state_table_and_the_first_tree_past_it(afx, nsym):
+    # 57 exponents: 56 internal nodes, the largest state table; 58: the 12-bit table
+    c, d = _check(afx, synth.exponent_mix(3_000_017, nsym, ratio=0.85, seed=nsym), out_pad=16)
+    assert d.nsym == nsym and min(l for l in d.len if l) >= 2
+
+
+def test_gaps_that_skip_zero_one_and_two_bytes(afx):
+    # a chunk's first code may begin 0..23 bits in; 16 or more skips two bytes
+    c, d = _check(afx, synth.exponent_mix(2_000_003, 50, ratio=0.75, seed=6))
+    chunk = np.frombuffer(c[d.off_chunk: d.off_chunk + 2 * d.n_chunks].tobytes(), dtype="<u2")
+    gaps = set(int(g) for g in np.unique(chunk & 31))
+    assert gaps >= set(range(0, 17)) and min(l for l in d.len if l) == 2
+
+
 @pytest.mark.parametrize("offset", [0, 8, 16, 24])
 def test_output_offsets_keep_guards(afx, offset):
     _check(afx, synth.normal(123_457, seed=3), out_offset=offset, out_pad=16)

@@ -79,10 +79,23 @@ constexpr int kChunkStage = kThreads + 8;  // chunk entries staged per tile (the
 // In 24-bit left-aligned code space all codes of length <= L lie in
 // [0, limit[L]); a 24-bit peek v has the length L = the smallest L with
 // v < limit[L], and its exponent is sorted[base[L] + (v >> (24 - L))].
+//
+// The internal nodes of the code tree (the prefixes that are not codes yet)
+// are numbered for the byte-step decoder: depth by depth, prefix value
+// ascending, the root first.  A prefix of depth d is internal when it lies
+// at or past limit[d] in d-bit space, so depth d holds the prefixes
+// [limit[d] >> (24 - d), 2^d) and node (d, p) is number
+// state_base[d] + p - (limit[d] >> (24 - d)).  A complete code of nsym
+// symbols has nsym - 1 of them.
+constexpr int kMaxStates = 56;
 struct CodeTables {
     uint32_t limit[AFX_MAX_CODE_LEN + 1];
     int32_t base[AFX_MAX_CODE_LEN + 1];
+    uint32_t state_base[AFX_MAX_CODE_LEN + 1];
     uint8_t sorted[256];
+    uint8_t state_depth[kMaxStates];
+    uint32_t n_states;  // internal nodes (nsym - 1)
+    uint32_t fsm;       // 1: the restore path decodes this tensor a byte at a time
 };
 
 // One tensor of a launch.
@@ -92,6 +105,7 @@ struct TensorArgs {
     const uint16_t* chunk_index;
     const uint64_t* block_index;
     uint64_t n, n_chunks, n_blocks, exp_bytes;
+    uint64_t total_bits;       // coded bits in the stream
     uint64_t tile_begin;       // first tile of this tensor in the launch's tile list
     uint32_t chunk_bytes;      // T
     uint32_t rows_per_warp;    // GEMV: capacity of the per-warp partial table
@@ -107,7 +121,7 @@ struct LaunchArgs {
     uint32_t count;
     uint32_t max_chunk_bytes;
     uint32_t max_rows_per_warp;
-    uint32_t pad;
+    uint32_t tab_bytes;        // restore path: size of the shared decode-table region
     uint64_t total_tiles;
     int32_t* status;
     TensorArgs t[kMaxTensors];
@@ -783,30 +797,331 @@ __global__ void __launch_bounds__(kThreads, 2) restore_kernel(const __grid_const
 // sum is checked against the block index at every block boundary that a run
 // crosses or ends on, so every entry of the block index is verified.  The
 // only CTA barriers are those around a rebuild of the tables.
+//
+// Byte-step decoding.  When no code is 1 bit long and the tree has at most
+// kMaxStates internal nodes, a lane decodes its chunk eight stream bits at a
+// time through a state machine whose state is the internal node reached by
+// the bits of the code in progress: entry (state, byte) holds the rotated
+// exponents of the (at most four) codes that end within the byte, their
+// count, and the next state.  Every lane steps through all T bytes of its
+// chunk from the chunk's first word, so the lanes of a warp run the same
+// loop with aligned word loads.  The gap (the tail of the previous chunk's
+// last code) is dropped by starting in one of seven skip rows (the first
+// 1..7 bits of the byte end an earlier code) and, for gaps of 8 or more, by
+// not stepping through the first one or two bytes.  After the last byte the
+// state's depth says where the code that crosses the chunk end began; that
+// one code is decoded on its own.  The partial last chunk of a stream and
+// tensors with 1-bit codes or larger trees use the 12-bit multi-code table.
 
 constexpr int kWarpChunks = 32;                                  // chunks per sub-tile
 constexpr int kSubtilesPerBlock = kThreads / kWarpChunks;        // 16
 constexpr int kMaxChunkCodes = AFX_BLOCK_CAPACITY / kThreads;    // codes one chunk may hold
 constexpr int kWarpStage = kWarpChunks * kMaxChunkCodes + 16;    // exponents of one sub-tile
 constexpr int kWarpChunkStage = 40;                              // 33 entries staged (80 bytes)
+constexpr int kRestoreMaxWarps = 32;
+constexpr uint32_t kLutTabBytes = kLutSize * 4 + kLutSize;       // 12-bit table + first-code lengths
+constexpr uint32_t kFsmRowBytes = 256 * 8;                       // one state: 256 entries of 8 bytes
+constexpr uint32_t kSkipRows = 7;                                // rows that first drop 1..7 bits of a byte
 
 struct WarpSlot {
     alignas(16) uint16_t chunk[2][kWarpChunkStage];
     alignas(16) uint8_t stage[kWarpStage];
 };
 
+// Fixed part of the restore kernel's shared memory.  It is followed by the
+// decode-table region (LaunchArgs::tab_bytes: the 12-bit table and the
+// first-code lengths, or the state table), one WarpSlot per warp and two
+// stream buffers per warp.
 struct SharedW {
-    uint32_t lut[kLutSize];
-    uint8_t len0[kLutSize];
     uint32_t limit[AFX_MAX_CODE_LEN + 1];
     int32_t base[AFX_MAX_CODE_LEN + 1];
     uint8_t sorted[256];
-    alignas(16) WarpSlot w[kWarps];
-    // dynamic part: per warp two stream buffers of kWarpChunks * max_T + kStreamPad bytes
+    uint8_t depth[64];               // depth of each state's node
+    alignas(16) uint16_t first[kLutSize];  // first code of a 12-bit peek: length << 8 | rotated exponent
+    alignas(16) uint8_t tab[16];     // start of the table region
 };
 
-constexpr size_t sharedw_fixed_bytes() { return (sizeof(SharedW) + 15) & ~size_t(15); }
 static_assert(sizeof(WarpSlot) % 16 == 0 && offsetof(WarpSlot, stage) % 16 == 0, "warp slots stay 16-byte aligned");
+static_assert(offsetof(SharedW, tab) % 16 == 0, "table region must be 16-byte aligned");
+
+constexpr size_t sharedw_table_offset() { return offsetof(SharedW, tab); }
+
+// The tables as the decoders see them (pointers into shared memory).
+struct TabView {
+    const uint32_t* lut;
+    const uint8_t* len0;
+    const uint32_t* limit;
+    const int32_t* base;
+    const uint8_t* sorted;
+    const uint16_t* first;
+    const char* fsm;
+    const uint8_t* depth;
+};
+
+// One code from a 32-bit window through the first-code table (exact
+// length in len), falling back to the canonical limits past 12 bits.  The
+// code is complete (the host checks Kraft equality), so every window holds
+// a code of at most 24 bits.
+__device__ __forceinline__ uint32_t decode_first(const TabView& tv, uint32_t win, uint32_t& len) {
+    const uint32_t f = tv.first[win >> (32 - kLutBits)];
+    if (f >> 8) {
+        len = f >> 8;
+        return f & 0xFFu;
+    }
+    const uint32_t v = win >> 8;
+    uint32_t L = kLutBits + 1;
+    while (L < AFX_MAX_CODE_LEN && v >= tv.limit[L]) ++L;
+    len = L;
+    return ror8(tv.sorted[tv.base[L] + static_cast<int32_t>(v >> (24 - L))]);
+}
+
+__device__ __forceinline__ uint32_t stream_window(const uint32_t* stream, uint32_t bit) {
+    return __funnelshift_l(stream[(bit >> 5) + 1], stream[bit >> 5], bit & 31u);
+}
+
+// Builds the tables of tensor tab with all nthreads threads of the CTA.
+// First pass: the first code of every 12-bit peek (a thread's consecutive
+// peeks have non-decreasing lengths, so one search plus short advances).
+// Second pass, state-machine tensors: entry (s, b) decodes node s's prefix
+// followed by byte b from the start of the code in progress, keeps every
+// code that ends within those bits, and names the node of the bits left
+// over.  Other tensors: up to three first codes chained per 12-bit peek.
+__device__ void build_tables_w(SharedW& sh, uint8_t* tabr, const CodeTables& tab, int tid, int nthreads) {
+    for (int i = tid; i <= AFX_MAX_CODE_LEN; i += nthreads) {
+        sh.limit[i] = tab.limit[i];
+        sh.base[i] = tab.base[i];
+    }
+    for (int i = tid; i < 256; i += nthreads) sh.sorted[i] = tab.sorted[i];
+    for (int i = tid; i < kMaxStates; i += nthreads) sh.depth[i] = tab.state_depth[i];
+    for (int p0 = tid * 4; p0 < kLutSize; p0 += nthreads * 4) {
+        int L = 1;
+        while (L <= kLutBits && (static_cast<uint32_t>(p0) << (24 - kLutBits)) >= tab.limit[L]) ++L;
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t p = static_cast<uint32_t>(p0 + j);
+            const uint32_t v = p << (24 - kLutBits);
+            while (L <= kLutBits && v >= tab.limit[L]) ++L;
+            uint16_t e = 0;
+            if (L <= kLutBits)
+                e = static_cast<uint16_t>((L << 8) | ror8(tab.sorted[tab.base[L] + static_cast<int32_t>(v >> (24 - L))]));
+            sh.first[p] = e;
+        }
+    }
+    __syncthreads();
+    if (tab.fsm) {
+        TabView tv{};
+        tv.limit = sh.limit;
+        tv.base = sh.base;
+        tv.sorted = sh.sorted;
+        tv.first = sh.first;
+        uint2* fsm = reinterpret_cast<uint2*>(tabr);
+        const uint32_t entries = (tab.n_states + kSkipRows) * 256u;
+        for (uint32_t i = tid; i < entries; i += nthreads) {
+            const uint32_t s = i >> 8, b = i & 255u;
+            uint32_t avail, V;
+            if (s < tab.n_states) {  // node s: its prefix, then the byte
+                const uint32_t d = tab.state_depth[s];
+                const uint32_t lo_d = d ? tab.limit[d] >> (24 - d) : 0u;
+                const uint32_t p = lo_d + s - tab.state_base[d];
+                avail = d + 8;  // at most 31 bits
+                V = (d ? p << (32 - d) : 0u) | (b << (24 - d));
+            } else {  // skip row h: the byte's first h bits end an earlier code
+                const uint32_t h = s - tab.n_states + 1;
+                avail = 8 - h;
+                V = b << (24 + h);
+            }
+            uint32_t pos = 0, out = 0, cnt = 0;
+            while (cnt < 4) {
+                uint32_t len;
+                const uint32_t sym = decode_first(tv, V << pos, len);
+                if (len > avail - pos) break;
+                out |= sym << (8 * cnt);
+                ++cnt;
+                pos += len;
+            }
+            const uint32_t r = avail - pos;
+            const uint32_t q = r ? (V << pos) >> (32 - r) : 0u;
+            const uint32_t lo_r = r ? tab.limit[r] >> (24 - r) : 0u;
+            const uint32_t next = tab.state_base[r] + q - lo_r;
+            fsm[i] = make_uint2(out, (next * kFsmRowBytes) | ((cnt * 8u) << 26));
+        }
+    } else {
+        uint32_t* lut = reinterpret_cast<uint32_t*>(tabr);
+        uint8_t* len0 = tabr + kLutSize * 4;
+        for (int p = tid; p < kLutSize; p += nthreads) {
+            const uint32_t f1 = sh.first[p];
+            const uint32_t l1 = f1 >> 8;
+            uint32_t entry = 0;
+            if (l1) {
+                uint32_t bits = l1, count = 1, syms = f1 & 0xFFu;
+                const uint32_t f2 = sh.first[(static_cast<uint32_t>(p) << l1) & (kLutSize - 1)];
+                const uint32_t l2 = f2 >> 8;
+                if (l2 && bits + l2 <= kLutBits) {
+                    bits += l2;
+                    syms |= (f2 & 0xFFu) << 8;
+                    count = 2;
+                    const uint32_t f3 = sh.first[(static_cast<uint32_t>(p) << bits) & (kLutSize - 1)];
+                    const uint32_t l3 = f3 >> 8;
+                    if (l3 && bits + l3 <= kLutBits) {
+                        bits += l3;
+                        syms |= (f3 & 0xFFu) << 16;
+                        count = 3;
+                    }
+                }
+                entry = bits | (count << 4) | (syms << 8);
+            }
+            lut[p] = entry;
+            len0[p] = static_cast<uint8_t>(l1);
+        }
+    }
+    __syncthreads();
+}
+
+// One step of the state machine: the byte b read in state st (the byte
+// offset of its row).
+__device__ __forceinline__ void fsm_step(const char* fsm, uint32_t& st, uint32_t b, uint32_t& acc, uint32_t& fill,
+                                         uint32_t*& wout) {
+    const uint2 e = *reinterpret_cast<const uint2*>(fsm + st + (b << 3));
+    append(e.x, e.y >> 26, acc, fill, wout);
+    st = e.y & 0x3FFFFFFu;
+}
+
+// Byte-step counterpart of decode_run (same contract).  stream_end is the
+// bit offset in the staged stream where the coded bits end: the padding
+// after it decodes as codes, so no step reads past it.
+__device__ __forceinline__ bool decode_run_fsm(const TabView& tv, const uint32_t* stream, uint32_t k0, uint32_t gap,
+                                               uint32_t cnt, uint8_t* stage, uint32_t s0, uint32_t next,
+                                               uint32_t chunk_end, uint32_t stream_end) {
+    uint32_t P = k0 * 32u + gap;  // bit of the next code in the staged stream
+    uint32_t i = 0;
+    // head: codes until the stage index is word aligned, one at a time
+    const uint32_t head = min(cnt, (0u - s0) & 3u);
+    for (; i < head; ++i) {
+        uint32_t len;
+        stage[s0 + i] = static_cast<uint8_t>(decode_first(tv, stream_window(stream, P), len));
+        P += len;
+    }
+    uint32_t* wout = reinterpret_cast<uint32_t*>(stage + s0 + i);
+    const uint32_t* const w_begin = wout;
+    uint32_t acc = 0, fill = 0;
+    bool bad = false;
+    if (i < cnt) {
+        // whole bytes of the chunk's bits from the code at P
+        const uint32_t lim = min(chunk_end, stream_end);
+        const uint32_t steps = lim > P ? (lim - P) >> 3 : 0u;
+        uint32_t k = P >> 5;
+        const uint32_t sh = P & 31u;
+        uint32_t w0 = stream[k], w1 = stream[k + 1];
+        uint32_t st = 0;  // the root
+        for (uint32_t q = steps >> 2; q; --q) {
+            const uint32_t X = __funnelshift_l(w1, w0, sh);
+            w0 = w1;
+            w1 = stream[k + 2];
+            ++k;
+            fsm_step(tv.fsm, st, X >> 24, acc, fill, wout);
+            fsm_step(tv.fsm, st, __byte_perm(X, 0u, 0x4442), acc, fill, wout);
+            fsm_step(tv.fsm, st, __byte_perm(X, 0u, 0x4441), acc, fill, wout);
+            fsm_step(tv.fsm, st, X & 0xFFu, acc, fill, wout);
+        }
+        const uint32_t rem = steps & 3u;
+        if (rem) {
+            const uint32_t X = __funnelshift_l(w1, w0, sh);
+            fsm_step(tv.fsm, st, X >> 24, acc, fill, wout);
+            if (rem > 1) fsm_step(tv.fsm, st, __byte_perm(X, 0u, 0x4442), acc, fill, wout);
+            if (rem > 2) fsm_step(tv.fsm, st, __byte_perm(X, 0u, 0x4441), acc, fill, wout);
+        }
+        // the code in progress began depth(st) bits before the last step's end
+        P += 8 * steps - tv.depth[st / kFsmRowBytes];
+        i += 4 * static_cast<uint32_t>(wout - w_begin) + (fill >> 3);
+        bad = i > cnt;
+    }
+    // tail: the codes that start in the last bits of the chunk
+    while (!bad && i < cnt) {
+        if (P >= chunk_end) {
+            bad = true;
+            break;
+        }
+        uint32_t len;
+        const uint32_t sym = decode_first(tv, stream_window(stream, P), len);
+        append(sym, 8, acc, fill, wout);
+        P += len;
+        ++i;
+    }
+    uint8_t* tail = reinterpret_cast<uint8_t*>(wout);
+    for (uint32_t j = 0; j * 8 < fill; ++j) tail[j] = static_cast<uint8_t>(acc >> (8 * j));
+    if (!bad) {
+        if ((next >> 5) != 0)
+            bad = P != chunk_end + (next & 31u);
+        else
+            bad = P > chunk_end + AFX_MAX_CODE_LEN;
+    }
+    return bad;
+}
+
+// What a lane's byte steps leave for after the warp barrier: the
+// exponents not yet stored (acc, fill bits), the word they go to, the byte
+// of that word where this lane's own bytes begin, the count of codes
+// emitted and the final state.
+struct FsmLane {
+    uint32_t* wout;
+    uint32_t acc, fill, first, emitted, st;
+};
+
+// All T bytes of a full chunk whose first word is words[0] (byte-step
+// decoding).  Completed stage words are stored whole, including a first
+// word shared with the previous lane: that lane stores its bytes of the
+// word only after the warp barrier.
+__device__ __forceinline__ void fsm_chunk_steps(const TabView& tv, const uint32_t* words, uint32_t nwords, uint32_t gap,
+                                                uint32_t skip_row0, uint8_t* stage, uint32_t s_run, FsmLane& fl) {
+    uint32_t* wout = reinterpret_cast<uint32_t*>(stage + (s_run & ~3u));
+    const uint32_t* const w_begin = wout;
+    uint32_t acc = 0, fill = 8 * (s_run & 3u);
+    const uint32_t h = gap & 7u;
+    uint32_t st = h ? skip_row0 + (h - 1) * kFsmRowBytes : 0u;
+    const uint32_t X0 = words[0];
+    if (gap < 8) fsm_step(tv.fsm, st, X0 >> 24, acc, fill, wout);
+    if (gap < 16) fsm_step(tv.fsm, st, __byte_perm(X0, 0u, 0x4442), acc, fill, wout);
+    fsm_step(tv.fsm, st, __byte_perm(X0, 0u, 0x4441), acc, fill, wout);
+    fsm_step(tv.fsm, st, X0 & 0xFFu, acc, fill, wout);
+    for (uint32_t w = 1; w < nwords; ++w) {
+        const uint32_t X = words[w];
+        fsm_step(tv.fsm, st, X >> 24, acc, fill, wout);
+        fsm_step(tv.fsm, st, __byte_perm(X, 0u, 0x4442), acc, fill, wout);
+        fsm_step(tv.fsm, st, __byte_perm(X, 0u, 0x4441), acc, fill, wout);
+        fsm_step(tv.fsm, st, X & 0xFFu, acc, fill, wout);
+    }
+    fl.wout = wout;
+    fl.acc = acc;
+    fl.fill = fill;
+    fl.first = wout == w_begin ? (s_run & 3u) : 0u;
+    fl.emitted = 4 * static_cast<uint32_t>(wout - w_begin) + (fill >> 3) - (s_run & 3u);
+    fl.st = st;
+}
+
+// After the warp barrier: the code that crosses the chunk end (if the final
+// state is not the root), the lane's pending bytes, and the checks of the
+// count and of where the next chunk's first code begins.  Returns true when
+// the stream is not valid.
+__device__ __forceinline__ bool fsm_chunk_finish(const TabView& tv, const uint32_t* stream, const FsmLane& fl,
+                                                 uint32_t cnt, uint32_t chunk_end, uint32_t next) {
+    const uint32_t d = tv.depth[fl.st / kFsmRowBytes];
+    uint32_t end = chunk_end, emitted = fl.emitted, acc = fl.acc, fill = fl.fill;
+    if (d) {
+        uint32_t len;
+        const uint32_t sym = decode_first(tv, stream_window(stream, chunk_end - d), len);
+        end = chunk_end - d + len;
+        acc |= sym << fill;  // fill <= 24 here
+        fill += 8;
+        ++emitted;
+    }
+    uint8_t* p = reinterpret_cast<uint8_t*>(fl.wout);
+    for (uint32_t j = fl.first; j * 8 < fill; ++j) p[j] = static_cast<uint8_t>(acc >> (8 * j));
+    bool bad = emitted != cnt;
+    if ((next >> 5) != 0)
+        bad = bad || end != chunk_end + (next & 31u);
+    else
+        bad = bad || end > chunk_end + AFX_MAX_CODE_LEN;
+    return bad;
+}
 
 __device__ __forceinline__ uint32_t warp_stream_bytes(const TensorArgs& t, uint64_t s) {
     const uint64_t byte0 = s * kWarpChunks * t.chunk_bytes;
@@ -839,10 +1154,13 @@ __device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
 }
 
 // Restores sub-tiles [s0, s1) of tensor t with one warp.
-__device__ __forceinline__ void warp_run(const SharedW& sh, WarpSlot& ws, uint8_t* wstream, uint32_t wstride,
+__device__ __forceinline__ void warp_run(const TabView& tv, WarpSlot& ws, uint8_t* wstream, uint32_t wstride,
                                          const TensorArgs& t, uint64_t s0, uint64_t s1, int lane, int32_t* status) {
     const uint32_t T = t.chunk_bytes;
     const uint32_t chunk_bits = 8u * T;
+    const uint32_t sub_bits = kWarpChunks * chunk_bits;
+    const bool fsm = t.tab.fsm != 0;
+    const uint32_t skip_row0 = t.tab.n_states * kFsmRowBytes;
     const uint64_t n_sub = (t.n_chunks + kWarpChunks - 1) / kWarpChunks;
     // the output index of sub-tile s0's first code
     const uint64_t blk = s0 / kSubtilesPerBlock;
@@ -894,12 +1212,31 @@ __device__ __forceinline__ void warp_run(const SharedW& sh, WarpSlot& ws, uint8_
                 prefetch_l2(t.sm + a0, static_cast<uint32_t>(a1 - a0));
             }
         }
+        const uint32_t next = (c + 1 < t.n_chunks) ? ws.chunk[buf][lane + 1] : 0u;
+        const uint32_t* stream = reinterpret_cast<const uint32_t*>(wstream + static_cast<size_t>(buf) * wstride);
+        const uint32_t chunk_end = (lane + 1) * chunk_bits;
+        bool stepped = false;  // byte steps done, finish after the barrier
+        FsmLane fl;
         if (cnt && in_range) {
-            const uint32_t next = (c + 1 < t.n_chunks) ? ws.chunk[buf][lane + 1] : 0u;
-            const uint32_t* stream = reinterpret_cast<const uint32_t*>(wstream + static_cast<size_t>(buf) * wstride);
-            bad = decode_run(sh, stream, warp_stream_bytes(t, s) >> 2, lane * (T >> 2), gap, cnt, ws.stage,
-                             static_cast<uint32_t>(o0 & 7u) + (inc - cnt), next, (lane + 1) * chunk_bits);
+            const uint32_t s_run = static_cast<uint32_t>(o0 & 7u) + (inc - cnt);
+            if (fsm) {
+                const uint64_t bit0 = s * static_cast<uint64_t>(sub_bits);
+                const uint64_t left = t.total_bits > bit0 ? t.total_bits - bit0 : 0;
+                const uint32_t stream_end = left < sub_bits ? static_cast<uint32_t>(left) : sub_bits;
+                if (chunk_end <= stream_end) {
+                    fsm_chunk_steps(tv, stream + lane * (T >> 2), T >> 2, gap, skip_row0, ws.stage, s_run, fl);
+                    stepped = true;
+                } else {  // the stream's partial last chunk
+                    bad = decode_run_fsm(tv, stream, lane * (T >> 2), gap, cnt, ws.stage, s_run, next, chunk_end,
+                                         stream_end);
+                }
+            } else {
+                bad = decode_run(tv, stream, warp_stream_bytes(t, s) >> 2, lane * (T >> 2), gap, cnt, ws.stage, s_run,
+                                 next, chunk_end);
+            }
         }
+        __syncwarp();
+        if (stepped) bad = fsm_chunk_finish(tv, stream, fl, cnt, chunk_end, next);
         if (bad) raise_status(status, AFX_DEV_BAD_CHUNK);
         const bool any_bad = __any_sync(0xFFFFFFFFu, bad);
         __syncwarp();
@@ -919,14 +1256,27 @@ __device__ __forceinline__ void warp_run(const SharedW& sh, WarpSlot& ws, uint8_
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 3) restore_store_kernel(const __grid_constant__ LaunchArgs a) {
+// One CTA per SM (up to 32 warps) sharing one copy of the decode tables.
+__global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1) restore_store_kernel(const __grid_constant__ LaunchArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     SharedW& sh = *reinterpret_cast<SharedW*>(smem);
-    uint8_t* stream_all = smem + sharedw_fixed_bytes();
-    const uint32_t wstride = kWarpChunks * a.max_chunk_bytes + kStreamPad;
+    uint8_t* tabr = smem + sharedw_table_offset();
+    const int nthreads = blockDim.x, nwarps = nthreads >> 5;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    WarpSlot& ws = sh.w[warp];
+    WarpSlot* slots = reinterpret_cast<WarpSlot*>(tabr + a.tab_bytes);
+    uint8_t* stream_all = reinterpret_cast<uint8_t*>(slots + nwarps);
+    const uint32_t wstride = kWarpChunks * a.max_chunk_bytes + kStreamPad;
+    WarpSlot& ws = slots[warp];
     uint8_t* wstream = stream_all + static_cast<size_t>(warp) * 2 * wstride;
+    TabView tv;
+    tv.lut = reinterpret_cast<const uint32_t*>(tabr);
+    tv.len0 = tabr + kLutSize * 4;
+    tv.limit = sh.limit;
+    tv.base = sh.base;
+    tv.sorted = sh.sorted;
+    tv.first = sh.first;
+    tv.fsm = reinterpret_cast<const char*>(tabr);
+    tv.depth = sh.depth;
 
     const uint64_t g_begin = a.total_tiles * blockIdx.x / gridDim.x;
     const uint64_t g_end = a.total_tiles * (blockIdx.x + 1) / gridDim.x;
@@ -941,11 +1291,11 @@ __global__ void __launch_bounds__(kThreads, 3) restore_store_kernel(const __grid
         const uint64_t n_sub = (t.n_chunks + kWarpChunks - 1) / kWarpChunks;
         const uint64_t sb = b0 * kSubtilesPerBlock;
         const uint64_t se = b1 * kSubtilesPerBlock < n_sub ? b1 * kSubtilesPerBlock : n_sub;
-        __syncthreads();  // every warp is done with the previous tensor's tables and buffers
-        build_tables(sh, reinterpret_cast<uint16_t*>(stream_all), t.tab);  // ends with __syncthreads
+        __syncthreads();  // every warp is done with the previous tensor's tables
+        build_tables_w(sh, tabr, t.tab, threadIdx.x, nthreads);  // ends with __syncthreads
         const uint64_t span = se - sb;
-        const uint64_t s0 = sb + span * warp / kWarps, s1 = sb + span * (warp + 1) / kWarps;
-        if (s0 < s1) warp_run(sh, ws, wstream, wstride, t, s0, s1, lane, a.status);
+        const uint64_t s0 = sb + span * warp / nwarps, s1 = sb + span * (warp + 1) / nwarps;
+        if (s0 < s1) warp_run(tv, ws, wstream, wstride, t, s0, s1, lane, a.status);
     }
 }
 
@@ -1046,6 +1396,22 @@ void make_tables(const afx_desc& d, CodeTables& t) {
         t.limit[L] = (first + count[L]) << (AFX_MAX_CODE_LEN - L);
         t.base[L] = static_cast<int32_t>(first_pos) - static_cast<int32_t>(first);
     }
+    // internal nodes of the code tree, depth by depth (the root is node 0)
+    unsigned min_len = AFX_MAX_CODE_LEN;
+    for (int s = 0; s < 256; ++s)
+        if (d.len[s]) min_len = std::min<unsigned>(min_len, d.len[s]);
+    uint64_t states = 0;
+    for (uint32_t depth = 0; depth <= AFX_MAX_CODE_LEN; ++depth) {
+        t.state_base[depth] = static_cast<uint32_t>(std::min<uint64_t>(states, 0xFFFFFFFFu));
+        if (depth >= d.max_len) continue;
+        const uint64_t lo = depth ? (t.limit[depth] >> (AFX_MAX_CODE_LEN - depth)) : 0;
+        const uint64_t here = (uint64_t{1} << depth) - lo;
+        for (uint64_t k = 0; k < here && states + k < static_cast<uint64_t>(kMaxStates); ++k)
+            t.state_depth[states + k] = static_cast<uint8_t>(depth);
+        states += here;
+    }
+    t.n_states = static_cast<uint32_t>(std::min<uint64_t>(states, 0xFFFFFFFFu));
+    t.fsm = d.nsym >= 2 && min_len >= 2 && states <= static_cast<uint64_t>(kMaxStates) ? 1u : 0u;
 }
 
 std::mutex g_mutex;
@@ -1060,6 +1426,7 @@ constexpr int kCacheSlots = 64;
 constexpr int kFuncSlots = 16;
 struct OccupancySlot {
     const void* func;
+    int threads;
     size_t smem;
     int per_sm;
 };
@@ -1078,13 +1445,13 @@ int current_device() {
     return dev;
 }
 
-afx_status prepare_kernel(const void* func, size_t smem, int* blocks_per_sm) {
+afx_status prepare_kernel(const void* func, int threads, size_t smem, int* blocks_per_sm) {
     const int dev = current_device();
     if (dev < 0) return afx_fail(AFX_E_CUDA, "no current CUDA device", 0);
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceCache& dc = g_devices[dev];
     for (int i = 0; i < dc.used; ++i)
-        if (dc.slot[i].func == func && dc.slot[i].smem == smem) {
+        if (dc.slot[i].func == func && dc.slot[i].smem == smem && dc.slot[i].threads == threads) {
             *blocks_per_sm = dc.slot[i].per_sm;
             return AFX_OK;
         }
@@ -1098,10 +1465,10 @@ afx_status prepare_kernel(const void* func, size_t smem, int* blocks_per_sm) {
                      "cudaFuncSetAttribute");
         if (dc.n_funcs < kFuncSlots) dc.funcs[dc.n_funcs++] = func;
     }
-    AFX_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, func, kThreads, smem),
+    AFX_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, func, threads, smem),
                  "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
     if (*blocks_per_sm < 1) return afx_fail(AFX_E_CUDA, "kernel does not fit on an SM", 0);
-    if (dc.used < kCacheSlots) dc.slot[dc.used++] = {func, smem, *blocks_per_sm};
+    if (dc.used < kCacheSlots) dc.slot[dc.used++] = {func, threads, smem, *blocks_per_sm};
     return AFX_OK;
 }
 
@@ -1130,6 +1497,7 @@ void fill_tensor(const afx_desc& d, const void* container, TensorArgs& t) {
     t.n_chunks = d.n_chunks;
     t.n_blocks = d.n_blocks;
     t.exp_bytes = d.exp_bytes;
+    t.total_bits = d.total_bits;
     t.chunk_bytes = d.chunk_bytes;
     make_tables(d, t.tab);
 }
@@ -1147,14 +1515,42 @@ afx_status launch_restore(LaunchArgs& la, cudaStream_t s) {
     const int sms = sm_count();
     if (sms <= 0) return afx_fail(AFX_E_CUDA, "cannot query the SM count", 0);
     if constexpr (B == 0) {
-        const size_t streams = static_cast<size_t>(kWarps) * 2 * (kWarpChunks * la.max_chunk_bytes + kStreamPad);
-        const size_t smem = sharedw_fixed_bytes() + (streams > 8192 ? streams : 8192);  // 8 KB: table-build scratch
-        if (smem > 227 * 1024) return afx_fail(AFX_E_ARG, "launch needs too much shared memory", 0);
+        // Up to 32 warps per CTA, one CTA per SM: the warp slots and stream
+        // buffers are fixed by the warp count and the largest T, the rest of
+        // the opt-in shared memory holds the tables.  A tensor whose state
+        // table does not fit falls back to the 12-bit table.
+        int optin = 0;
+        const int dev = current_device();
+        if (dev < 0) return afx_fail(AFX_E_CUDA, "no current CUDA device", 0);
+        AFX_CUDA_TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev),
+                     "cudaDeviceGetAttribute");
+        int warps = kRestoreMaxWarps;
+        size_t fixed = 0;
+        for (; warps >= 1; warps /= 2) {
+            fixed = sharedw_table_offset() + static_cast<size_t>(warps) * sizeof(WarpSlot) +
+                    static_cast<size_t>(warps) * 2 * (kWarpChunks * la.max_chunk_bytes + kStreamPad);
+            if (fixed + kLutTabBytes <= static_cast<size_t>(optin)) break;
+        }
+        if (warps < 1) return afx_fail(AFX_E_ARG, "launch needs too much shared memory", 0);
+        const size_t budget = static_cast<size_t>(optin) - fixed;
+        uint32_t tab_bytes = kLutTabBytes;
+        for (uint32_t i = 0; i < la.count; ++i) {
+            CodeTables& tab = la.t[i].tab;
+            if (!tab.fsm) continue;
+            const size_t need = static_cast<size_t>(tab.n_states + kSkipRows) * kFsmRowBytes;
+            if (need > budget)
+                tab.fsm = 0;
+            else
+                tab_bytes = std::max<uint32_t>(tab_bytes, static_cast<uint32_t>(need));
+        }
+        la.tab_bytes = tab_bytes;
+        const size_t smem = fixed + tab_bytes;
         int per_sm = 0;
-        const afx_status st = prepare_kernel(reinterpret_cast<const void*>(restore_store_kernel), smem, &per_sm);
+        const afx_status st =
+            prepare_kernel(reinterpret_cast<const void*>(restore_store_kernel), warps * 32, smem, &per_sm);
         if (st != AFX_OK) return st;
         const uint64_t grid = std::min<uint64_t>(la.total_tiles, static_cast<uint64_t>(sms) * per_sm);
-        restore_store_kernel<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(la);
+        restore_store_kernel<<<static_cast<unsigned>(grid), warps * 32, smem, s>>>(la);
         AFX_CUDA_TRY(cudaGetLastError(), "restore_store_kernel launch");
         return AFX_OK;
     } else {
@@ -1163,7 +1559,7 @@ afx_status launch_restore(LaunchArgs& la, cudaStream_t s) {
                 kWarps * (sizeof(uint64_t) + sizeof(uint32_t));
         if (smem > 227 * 1024) return afx_fail(AFX_E_ARG, "launch needs too much shared memory", 0);
         int per_sm = 0;
-        const afx_status st = prepare_kernel(reinterpret_cast<const void*>(restore_kernel<B>), smem, &per_sm);
+        const afx_status st = prepare_kernel(reinterpret_cast<const void*>(restore_kernel<B>), kThreads, smem, &per_sm);
         if (st != AFX_OK) return st;
         const uint64_t grid = std::min<uint64_t>(la.total_tiles, static_cast<uint64_t>(sms) * per_sm);
         restore_kernel<B><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(la);

@@ -187,6 +187,19 @@ def activations(batch: int, width: int, seed: int = 1, stream: int = _ACT_ID) ->
     return normal(batch * width, 0.0, 1.0, seed, stream).reshape(batch, width)
 
 
+def exponent_mix(n: int, n_exponents: int, ratio: float = 0.85, first: int = 100, seed: int = 0) -> np.ndarray:
+    """n BF16 patterns whose exponents are first .. first + n_exponents - 1,
+    exponent first + k drawn with probability proportional to ratio**k;
+    sign and mantissa uniform.  Sets the size and shape of the code tree
+    directly (every exponent is present once n is large enough)."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([int(seed), 105, int(n_exponents)])))
+    p = ratio ** np.arange(n_exponents, dtype=np.float64)
+    p /= p.sum()
+    e = (first + rng.choice(n_exponents, size=int(n), p=p)).astype(np.uint16)
+    low = rng.integers(0, 1 << 16, size=int(n), dtype=np.uint32).astype(np.uint16)
+    return (low & np.uint16(0x807F)) | (e << np.uint16(7))
+
+
 def all_bf16_patterns() -> np.ndarray:
     """Every one of the 65,536 BF16 bit patterns, in order."""
     return np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
