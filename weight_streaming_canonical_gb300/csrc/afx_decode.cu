@@ -106,6 +106,7 @@ struct TensorArgs {
     const uint64_t* block_index;
     uint64_t n, n_chunks, n_blocks, exp_bytes;
     uint64_t total_bits;       // coded bits in the stream
+    uint64_t n_sub_full;       // leading sub-tiles whose chunks, next entry and stream pad all exist
     uint64_t tile_begin;       // first tile of this tensor in the launch's tile list
     uint32_t chunk_bytes;      // T
     uint32_t rows_per_warp;    // GEMV: capacity of the per-warp partial table
@@ -546,50 +547,6 @@ __device__ __forceinline__ bool decode_tile(Shared& sh, const uint32_t* stream, 
 
 // ---- epilogues ---------------------------------------------------------------------
 
-// Joins and stores weights [o0, o1) whose rotated exponents are at
-// stage[o - (o0 & ~7)], with NT threads (thread index tid).  The first and
-// last group of 8 may be shared with neighbouring ranges and go out weight
-// by weight; the full groups in between are handled kUnroll per thread at a
-// time so that their sign|mantissa loads are in flight together.
-template <int NT>
-__device__ __forceinline__ void store_range(const uint8_t* stage, const TensorArgs& t, uint64_t o0, uint64_t o1,
-                                            int tid) {
-    constexpr int kUnroll = 4;
-    const uint64_t ob0 = o0 & ~uint64_t(7);
-    const uint64_t f0 = (o0 + 7) >> 3, f1 = o1 >> 3;  // full groups [f0, f1)
-    // weights outside the full groups (at most 7 at each end): threads 0-7
-    // take the first group's, threads 8-15 the last group's, one weight each
-    if (tid < 16) {
-        const uint64_t o = (tid < 8 ? (o0 & ~uint64_t(7)) : (o1 & ~uint64_t(7))) + (tid & 7);
-        const bool outside_full = o < (f0 << 3) || o >= (f1 << 3);
-        const bool twice = tid >= 8 && (o0 >> 3) == (o1 >> 3);  // one group holds both ends
-        if (o >= o0 && o < o1 && outside_full && !twice)
-            t.out[o] = join1(stage[static_cast<uint32_t>(o - ob0)], t.sm[o]);
-    }
-    if (f1 <= f0) return;
-    // full groups, indexed from the first one in 32-bit arithmetic
-    const uint32_t nfull = static_cast<uint32_t>(f1 - f0);
-    const uint2* smp = reinterpret_cast<const uint2*>(t.sm + (f0 << 3));
-    uint4* outp = reinterpret_cast<uint4*>(t.out + (f0 << 3));
-    const uint8_t* stp = stage + static_cast<uint32_t>((f0 << 3) - ob0);
-    for (uint32_t j = tid; j < nfull; j += NT * kUnroll) {
-        uint2 s8[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const uint32_t jj = j + u * NT;
-            if (jj < nfull) s8[u] = __ldg(smp + jj);
-        }
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const uint32_t jj = j + u * NT;
-            if (jj < nfull) {
-                const uint2 e8 = *reinterpret_cast<const uint2*>(stp + 8 * jj);
-                __stcs(outp + jj, join8(e8, s8[u]));
-            }
-        }
-    }
-}
-
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
@@ -914,21 +871,12 @@ __device__ void build_tables_w(SharedW& sh, uint8_t* tabr, const CodeTables& tab
         tv.sorted = sh.sorted;
         tv.first = sh.first;
         uint2* fsm = reinterpret_cast<uint2*>(tabr);
-        const uint32_t entries = (tab.n_states + kSkipRows) * 256u;
-        for (uint32_t i = tid; i < entries; i += nthreads) {
-            const uint32_t s = i >> 8, b = i & 255u;
-            uint32_t avail, V;
-            if (s < tab.n_states) {  // node s: its prefix, then the byte
-                const uint32_t d = tab.state_depth[s];
-                const uint32_t lo_d = d ? tab.limit[d] >> (24 - d) : 0u;
-                const uint32_t p = lo_d + s - tab.state_base[d];
-                avail = d + 8;  // at most 31 bits
-                V = (d ? p << (32 - d) : 0u) | (b << (24 - d));
-            } else {  // skip row h: the byte's first h bits end an earlier code
-                const uint32_t h = s - tab.n_states + 1;
-                avail = 8 - h;
-                V = b << (24 + h);
-            }
+        const uint32_t nodes = tab.n_states;
+        // the root row and the skip rows, code by code
+        for (uint32_t i = tid; i < (1 + kSkipRows) * 256u; i += nthreads) {
+            const uint32_t h = i >> 8, b = i & 255u;  // h: bits of the byte that end an earlier code
+            const uint32_t avail = 8 - h;
+            const uint32_t V = b << (24 + h);
             uint32_t pos = 0, out = 0, cnt = 0;
             while (cnt < 4) {
                 uint32_t len;
@@ -942,7 +890,31 @@ __device__ void build_tables_w(SharedW& sh, uint8_t* tabr, const CodeTables& tab
             const uint32_t q = r ? (V << pos) >> (32 - r) : 0u;
             const uint32_t lo_r = r ? tab.limit[r] >> (24 - r) : 0u;
             const uint32_t next = tab.state_base[r] + q - lo_r;
-            fsm[i] = make_uint2(out, (next * kFsmRowBytes) | ((cnt * 8u) << 26));
+            fsm[(h ? nodes + h - 1 : 0u) * 256u + b] = make_uint2(out, (next * kFsmRowBytes) | ((cnt * 8u) << 26));
+        }
+        __syncthreads();
+        // node rows: the code in progress ends h bits into the byte (or does
+        // not end in it); the rest of the byte is skip row h
+        for (uint32_t i = 256u + tid; i < nodes * 256u; i += nthreads) {
+            const uint32_t s = i >> 8, b = i & 255u;
+            const uint32_t d = tab.state_depth[s];
+            const uint32_t lo_d = tab.limit[d] >> (24 - d);
+            const uint32_t p = lo_d + s - tab.state_base[d];
+            uint32_t len;
+            const uint32_t sym = decode_first(tv, (p << (32 - d)) | (b << (24 - d)), len);
+            const uint32_t h = len - d;
+            uint2 e;
+            if (h > 8) {  // still inside the code: the node of its first d + 8 bits
+                const uint32_t d8 = d + 8;
+                const uint32_t next = tab.state_base[d8] + ((p << 8) | b) - (tab.limit[d8] >> (24 - d8));
+                e = make_uint2(0u, next * kFsmRowBytes);
+            } else if (h == 8) {
+                e = make_uint2(sym, 8u << 26);
+            } else {
+                const uint2 rest = fsm[(nodes + h - 1) * 256u + b];
+                e = make_uint2(sym | (rest.x << 8), rest.y + (8u << 26));
+            }
+            fsm[i] = e;
         }
     } else {
         uint32_t* lut = reinterpret_cast<uint32_t*>(tabr);
@@ -1153,15 +1125,56 @@ __device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
     return v;
 }
 
+// cp.async of a full sub-tile (see TensorArgs::n_sub_full): its stream
+// bytes plus the pad and 40 chunk entries, from sources that are known to
+// hold them.
+__device__ __forceinline__ void warp_issue_full(uint16_t* chunk_dst, uint8_t* stream_dst, const uint8_t* exp_src,
+                                                const uint16_t* chunk_src, uint32_t sub_bytes, int lane) {
+    for (uint32_t i = lane * 16u; i < sub_bytes + kStreamPad; i += 32 * 16u) cp_async16(stream_dst + i, exp_src + i);
+    if (lane < kWarpChunkStage * 2 / 16)
+        cp_async16(reinterpret_cast<uint8_t*>(chunk_dst) + lane * 16, reinterpret_cast<const uint8_t*>(chunk_src) + lane * 16);
+    cp_async_commit();
+}
+
+// Joins and stores `count` weights from o0 with the 32 lanes of a warp; the
+// rotated exponent of weight o is at stage[o - (o0 & ~7)].  The first and
+// last group of 8 may be shared with neighbouring ranges and go out weight
+// by weight (lanes 0-7 and 8-15); the full groups between go out as 16-byte
+// stores, one group per lane at a time.
+__device__ __forceinline__ void warp_store(const uint8_t* stage, const uint8_t* sm, uint16_t* out, uint64_t o0,
+                                           uint32_t count, int lane) {
+    const uint64_t ob0 = o0 & ~uint64_t(7);
+    const uint8_t* smb = sm + ob0;
+    uint16_t* outb = out + ob0;
+    const uint32_t a = static_cast<uint32_t>(o0) & 7u, b = a + count;  // the range, relative to ob0
+    const uint32_t f0 = (a + 7) & ~7u, f1 = b & ~7u;                  // full groups [f0, f1)
+    if (lane < 16) {
+        const uint32_t r = lane < 8 ? lane : f1 + (lane & 7);
+        const bool same_group = lane >= 8 && f1 == 0;  // the last group is the first one
+        if (r >= a && r < b && (r < f0 || r >= f1) && !same_group) outb[r] = join1(stage[r], smb[r]);
+    }
+    if (f1 > f0) {
+        const uint32_t nfull = (f1 - f0) >> 3;
+        const uint2* smp = reinterpret_cast<const uint2*>(smb + f0);
+        const uint2* stp = reinterpret_cast<const uint2*>(stage + f0);
+        uint4* outp = reinterpret_cast<uint4*>(outb + f0);
+        for (uint32_t j = lane; j < nfull; j += 32) __stcs(outp + j, join8(stp[j], __ldg(smp + j)));
+    }
+}
+
 // Restores sub-tiles [s0, s1) of tensor t with one warp.
 __device__ __forceinline__ void warp_run(const TabView& tv, WarpSlot& ws, uint8_t* wstream, uint32_t wstride,
                                          const TensorArgs& t, uint64_t s0, uint64_t s1, int lane, int32_t* status) {
     const uint32_t T = t.chunk_bytes;
     const uint32_t chunk_bits = 8u * T;
-    const uint32_t sub_bits = kWarpChunks * chunk_bits;
+    const uint32_t sub_bytes = kWarpChunks * T, sub_bits = 8u * sub_bytes;
     const bool fsm = t.tab.fsm != 0;
     const uint32_t skip_row0 = t.tab.n_states * kFsmRowBytes;
     const uint64_t n_sub = (t.n_chunks + kWarpChunks - 1) / kWarpChunks;
+    const uint64_t n_full = t.n_sub_full;
+    const uint8_t* const sm = t.sm;
+    uint16_t* const out = t.out;
+    const uint64_t n = t.n;
     // the output index of sub-tile s0's first code
     const uint64_t blk = s0 / kSubtilesPerBlock;
     uint32_t pre = 0;
@@ -1169,25 +1182,42 @@ __device__ __forceinline__ void warp_run(const TabView& tv, WarpSlot& ws, uint8_
     pre = warp_sum(pre);
     uint64_t start = __ldg(t.block_index + blk) + pre;
     if (s0 == 0 && start != 0 && lane == 0) raise_status(status, AFX_DEV_BAD_BLOCK);
-    warp_issue(ws, wstream, wstride, t, s0, 0, lane);
+    // sources of the next sub-tile to stage
+    const uint8_t* exp_src = reinterpret_cast<const uint8_t*>(t.exp_words) + s0 * sub_bytes;
+    const uint16_t* chunk_src = t.chunk_index + s0 * kWarpChunks;
+    if (s0 < n_full)
+        warp_issue_full(ws.chunk[0], wstream, exp_src, chunk_src, sub_bytes, lane);
+    else
+        warp_issue(ws, wstream, wstride, t, s0, 0, lane);
+    const uint32_t nrun = static_cast<uint32_t>(s1 - s0);
+    uint32_t sub_in_block = static_cast<uint32_t>(s0 % kSubtilesPerBlock);
     int buf = 0;
-    for (uint64_t s = s0; s < s1; ++s) {
-        if (s + 1 < s1) {
-            warp_issue(ws, wstream, wstride, t, s + 1, buf ^ 1, lane);
+    for (uint32_t r = 0; r < nrun; ++r) {
+        const uint64_t s = s0 + r;
+        if (r + 1 < nrun) {
+            exp_src += sub_bytes;
+            chunk_src += kWarpChunks;
+            if (s + 1 < n_full)
+                warp_issue_full(ws.chunk[buf ^ 1], wstream + (buf ^ 1) * wstride, exp_src, chunk_src, sub_bytes, lane);
+            else
+                warp_issue(ws, wstream, wstride, t, s + 1, buf ^ 1, lane);
             cp_async_wait<1>();
         } else {
             cp_async_wait<0>();
         }
         __syncwarp();
-        if (s != s0 && s % kSubtilesPerBlock == 0) {  // a block boundary inside the run
+        if (r != 0 && sub_in_block == 0) {  // a block boundary inside the run
             const uint64_t bo = __ldg(t.block_index + s / kSubtilesPerBlock);
             if (bo != start) {
                 if (lane == 0) raise_status(status, AFX_DEV_BAD_BLOCK);
                 start = bo;
             }
         }
-        const uint64_t c = s * kWarpChunks + lane;
-        const uint32_t entry = c < t.n_chunks ? ws.chunk[buf][lane] : 0u;
+        // chunk entries that exist from this sub-tile's first (33 read at most)
+        const bool full = s < n_full;
+        const uint32_t nexist =
+            full ? 64u : static_cast<uint32_t>(min(t.n_chunks - min(t.n_chunks, s * kWarpChunks), uint64_t{64}));
+        const uint32_t entry = static_cast<uint32_t>(lane) < nexist ? ws.chunk[buf][lane] : 0u;
         const uint32_t gap = entry & 31u;
         uint32_t cnt = entry >> 5;
         bool bad = false;
@@ -1203,16 +1233,16 @@ __device__ __forceinline__ void warp_run(const TabView& tv, WarpSlot& ws, uint8_
         }
         const uint32_t total = __shfl_sync(0xFFFFFFFFu, inc, 31);
         const uint64_t o0 = start, o1 = start + total;
-        const bool in_range = o1 <= t.n;
+        const bool in_range = o1 <= n;
         if (lane == 0) {
             if (!in_range)
                 raise_status(status, AFX_DEV_BAD_BLOCK);
             else if (o0 < o1) {  // the sign|mantissa bytes are needed after the decode
                 const uint64_t a0 = o0 & ~uint64_t(15), a1 = (o1 + 15) & ~uint64_t(15);
-                prefetch_l2(t.sm + a0, static_cast<uint32_t>(a1 - a0));
+                prefetch_l2(sm + a0, static_cast<uint32_t>(a1 - a0));
             }
         }
-        const uint32_t next = (c + 1 < t.n_chunks) ? ws.chunk[buf][lane + 1] : 0u;
+        const uint32_t next = static_cast<uint32_t>(lane) + 1 < nexist ? ws.chunk[buf][lane + 1] : 0u;
         const uint32_t* stream = reinterpret_cast<const uint32_t*>(wstream + static_cast<size_t>(buf) * wstride);
         const uint32_t chunk_end = (lane + 1) * chunk_bits;
         bool stepped = false;  // byte steps done, finish after the barrier
@@ -1220,9 +1250,12 @@ __device__ __forceinline__ void warp_run(const TabView& tv, WarpSlot& ws, uint8_
         if (cnt && in_range) {
             const uint32_t s_run = static_cast<uint32_t>(o0 & 7u) + (inc - cnt);
             if (fsm) {
-                const uint64_t bit0 = s * static_cast<uint64_t>(sub_bits);
-                const uint64_t left = t.total_bits > bit0 ? t.total_bits - bit0 : 0;
-                const uint32_t stream_end = left < sub_bits ? static_cast<uint32_t>(left) : sub_bits;
+                uint32_t stream_end = sub_bits;
+                if (!full) {
+                    const uint64_t bit0 = s * static_cast<uint64_t>(sub_bits);
+                    const uint64_t left = t.total_bits > bit0 ? t.total_bits - bit0 : 0;
+                    stream_end = left < sub_bits ? static_cast<uint32_t>(left) : sub_bits;
+                }
                 if (chunk_end <= stream_end) {
                     fsm_chunk_steps(tv, stream + lane * (T >> 2), T >> 2, gap, skip_row0, ws.stage, s_run, fl);
                     stepped = true;
@@ -1240,9 +1273,10 @@ __device__ __forceinline__ void warp_run(const TabView& tv, WarpSlot& ws, uint8_
         if (bad) raise_status(status, AFX_DEV_BAD_CHUNK);
         const bool any_bad = __any_sync(0xFFFFFFFFu, bad);
         __syncwarp();
-        if (!any_bad && in_range && o0 < o1) store_range<32>(ws.stage, t, o0, o1, lane);
+        if (!any_bad && in_range && total) warp_store(ws.stage, sm, out, o0, total, lane);
         start = o1;
         buf ^= 1;
+        sub_in_block = (sub_in_block + 1) & (kSubtilesPerBlock - 1);
         __syncwarp();
     }
     // a run that ends on a block boundary checks the block index there; the
@@ -1251,7 +1285,7 @@ __device__ __forceinline__ void warp_run(const TabView& tv, WarpSlot& ws, uint8_
         if (s1 < n_sub && s1 % kSubtilesPerBlock == 0) {
             if (__ldg(t.block_index + s1 / kSubtilesPerBlock) != start) raise_status(status, AFX_DEV_BAD_BLOCK);
         }
-        if (s1 == n_sub && (start != t.n || __ldg(t.block_index + t.n_blocks) != t.n))
+        if (s1 == n_sub && (start != n || __ldg(t.block_index + t.n_blocks) != n))
             raise_status(status, AFX_DEV_BAD_BLOCK);
     }
 }
@@ -1499,6 +1533,14 @@ void fill_tensor(const afx_desc& d, const void* container, TensorArgs& t) {
     t.exp_bytes = d.exp_bytes;
     t.total_bits = d.total_bits;
     t.chunk_bytes = d.chunk_bytes;
+    {
+        // sub-tile s is full when chunks s*32 .. s*32+39 exist (the staged
+        // entries) and its stream bytes plus the pad lie inside the section
+        const uint64_t sub_bytes = static_cast<uint64_t>(kWarpChunks) * d.chunk_bytes;
+        const uint64_t by_chunks = d.n_chunks >= kWarpChunkStage ? (d.n_chunks - kWarpChunkStage) / kWarpChunks + 1 : 0;
+        const uint64_t by_bytes = d.exp_bytes >= sub_bytes + kStreamPad ? (d.exp_bytes - kStreamPad) / sub_bytes : 0;
+        t.n_sub_full = std::min(by_chunks, by_bytes);
+    }
     make_tables(d, t.tab);
 }
 
