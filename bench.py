@@ -556,7 +556,7 @@ def run_gemv_bench(afx, parts, dev_blob, offs, dev, args):
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / args.steps
         res[f"batch{B}"] = {"ms": ms, "weights_per_s": n / (ms * 1e-3), "compressed_read_gbs": comp / (ms * 1e-3) / 1e9,
-                            "launches": "one restore_kernel<B> and one fix-up per product batch"}
+                            "launches": "one restore_gemv_kernel<B> and one row fix-up per product batch"}
     res["weights"] = n
     return res
 

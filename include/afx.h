@@ -165,8 +165,9 @@ afx_status afx_decode_batch(const afx_desc* descs, const void* const* containers
                             uint32_t count, afx_stream_t stream, int32_t* status_dev);
 
 /* Device workspace (bytes) that afx_decode_gemv needs for this container
- * and batch: one float per batch row for the two partial output rows of
- * every block. */
+ * and batch: for every run of 32 chunks (16 per block) its first weight
+ * index (8 bytes) and one float per batch row for each of the two output
+ * rows the run can meet. */
 afx_status afx_decode_gemv_workspace(const afx_desc* desc, uint32_t batch, uint64_t* bytes);
 
 /* Fused restore + GEMV: y_dev[b][r] = sum_c W[r][c] * x_dev[b][c] for
@@ -196,10 +197,10 @@ afx_status afx_decode_gemv_batch(const afx_desc* descs, const void* const* conta
                                  float* const* ys_dev, void* const* workspaces_dev, const uint64_t* workspace_bytes,
                                  uint32_t count, afx_stream_t stream, int32_t* status_dev);
 
-/* Size of the device workspace that afx_decode_gemv_static owns: 1 MiB,
- * enough for a batch-4 product over a container of up to 32,768 blocks
- * (about 800M weights of N(0, 0.02) BF16). */
-#define AFX_STATIC_WORKSPACE_BYTES (1u << 20)
+/* Size of the device workspace that afx_decode_gemv_static owns: 4 MiB,
+ * enough for a batch-4 product over a container of up to 6,553 blocks
+ * (about 165M weights of N(0, 0.02) BF16), or batch 1 over 16,384 blocks. */
+#define AFX_STATIC_WORKSPACE_BYTES (4u << 20)
 
 /* afx_decode_gemv without the workspace argument, for callers that cannot
  * allocate device memory: for example a plugin called from inside another

@@ -36,6 +36,27 @@ def test_shapes_and_batches(afx, shape, B):
     _check(afx, W, x)
 
 
+@pytest.mark.parametrize("cols", [2056, 2064, 2072])
+def test_rows_at_the_warp_path_boundary(afx, cols):
+    # 2064 columns and more (a multiple of 8): one warp's run of 32 chunks meets at most two rows
+    W = synth.normal(500 * cols, seed=cols).reshape(500, cols)
+    x = synth.activations(4, cols, seed=cols)
+    _check(afx, W, x)
+
+
+def test_corrupt_stream_is_flagged_by_the_gemv(afx):
+    import torch
+    rows, cols = 200, 5120
+    W = synth.normal(rows * cols, seed=21).reshape(rows, cols)
+    c, d = afx.encode(W.reshape(-1))
+    bad = c.copy()
+    rng = np.random.default_rng(2)
+    bad[d.off_exp: d.off_exp + d.n_chunks * d.chunk_bytes] = rng.integers(
+        0, 256, size=d.n_chunks * d.chunk_bytes, dtype=np.uint8)
+    y, status = gpu_gemv(afx, bad, d, rows, cols, synth.activations(2, cols, seed=5))
+    assert status != 0
+
+
 def test_unit_vector_gives_a_column_exactly(afx):
     rows, cols = 300, 5120
     W = synth.normal(rows * cols, seed=1).reshape(rows, cols)

@@ -53,7 +53,7 @@ def test_static_workspace_rejects_containers_that_need_more(afx):
     import torch
     w = synth.normal(5120 * 16, seed=1)
     code = afx.afx_build_code(w)
-    factor = 1 << 16  # the same exponent mix at 5.4G weights: far more blocks than 1 MiB of partials covers
+    factor = 1 << 16  # the same exponent mix at 5.4G weights: far more blocks than the static workspace covers
     for s in range(256):
         code.count[s] = code.count[s] * factor
     n = w.size * factor

@@ -28,7 +28,7 @@ AFX_DEV_BAD_BLOCK, AFX_DEV_BAD_CHUNK, AFX_DEV_BAD_CODE, AFX_DEV_BAD_SHAPE = 0x1,
 AFX_MAX_CODE_LEN = 24
 AFX_BLOCK_CAPACITY = 32768
 AFX_HEADER_BYTES = 512
-AFX_STATIC_WORKSPACE_BYTES = 1 << 20
+AFX_STATIC_WORKSPACE_BYTES = 4 << 20
 AFX_OP_DECODE, AFX_OP_GEMV = 0, 1
 
 

@@ -108,6 +108,7 @@ struct TensorArgs {
     uint64_t total_bits;       // coded bits in the stream
     uint64_t n_sub_full;       // leading sub-tiles whose chunks, next entry and stream pad all exist
     uint64_t tile_begin;       // first tile of this tensor in the launch's tile list
+    uint64_t sub_begin;        // warp GEMV: first sub-tile of this tensor in the launch's sub-tile list
     uint32_t chunk_bytes;      // T
     uint32_t rows_per_warp;    // GEMV: capacity of the per-warp partial table
     uint16_t* out;             // restore: n BF16
@@ -124,6 +125,7 @@ struct LaunchArgs {
     uint32_t max_rows_per_warp;
     uint32_t tab_bytes;        // restore path: size of the shared decode-table region
     uint64_t total_tiles;
+    uint64_t total_subs;       // warp GEMV: sub-tiles of all tensors
     int32_t* status;
     TensorArgs t[kMaxTensors];
 };
@@ -1162,9 +1164,115 @@ __device__ __forceinline__ void warp_store(const uint8_t* stage, const uint8_t* 
     }
 }
 
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, d);
+    return v;
+}
+
+// y[b][r] += sum over the weights [o0, o0 + count) of row r of W[r][c] x[b][c],
+// for a matrix whose rows are at least kWarpStage weights long and a
+// multiple of 8: a sub-tile meets at most two rows (r_a and r_a + 1) and no
+// group of 8 straddles two rows.  Each lane keeps float32 sums for the two
+// rows; a fixed butterfly reduces them, and lane 0 stores the sub-tile's
+// start and its two row partials in the workspace (zeros when the sub-tile
+// is not valid).  gemv_fixup_warp_kernel adds each row's partials in
+// sub-tile order, so y does not depend on how the grid split the work.
+template <int B>
+__device__ __forceinline__ void warp_gemv(const uint8_t* stage, const TensorArgs& t, uint64_t s, uint64_t o0,
+                                          uint32_t count, bool ok, int lane) {
+    float acc_a[B], acc_b[B];
+#pragma unroll
+    for (int b = 0; b < B; ++b) acc_a[b] = acc_b[b] = 0.f;
+    if (ok && count) {
+        const uint64_t cols = t.cols;
+        const uint64_t ra = o0 / cols;
+        const uint64_t ob0 = o0 & ~uint64_t(7);
+        const uint32_t a = static_cast<uint32_t>(o0) & 7u, e = a + count;  // the range, relative to ob0
+        const uint64_t next_row = (ra + 1) * cols;
+        const uint32_t split = next_row - ob0 < e ? static_cast<uint32_t>(next_row - ob0) : e;  // row r_a + 1 from here
+        const uint32_t cbase = static_cast<uint32_t>(ob0 - ra * cols);  // column of relative index 0 in row r_a
+        const uint8_t* smb = t.sm + ob0;
+        const uint16_t* x = t.x;
+        const uint32_t f0 = (a + 7) & ~7u, f1 = e & ~7u;  // full groups [f0, f1)
+        if (lane < 16) {  // weights outside the full groups, one per lane
+            const uint32_t r = lane < 8 ? lane : f1 + (lane & 7);
+            const bool same_group = lane >= 8 && f1 == 0;
+            if (r >= a && r < e && (r < f0 || r >= f1) && !same_group) {
+                const float w = __uint_as_float(static_cast<uint32_t>(join1(stage[r], smb[r])) << 16);
+                const bool in_b = r >= split;
+                const uint32_t c = in_b ? r - split : cbase + r;
+#pragma unroll
+                for (int b = 0; b < B; ++b) {
+                    const float xf = __uint_as_float(static_cast<uint32_t>(__ldg(x + b * cols + c)) << 16);
+                    if (in_b)
+                        acc_b[b] = fmaf(w, xf, acc_b[b]);
+                    else
+                        acc_a[b] = fmaf(w, xf, acc_a[b]);
+                }
+            }
+        }
+        for (uint32_t r = f0 + 8 * lane; r < f1; r += 8 * 32) {
+            const uint4 wv4 = join8(*reinterpret_cast<const uint2*>(stage + r), __ldg(reinterpret_cast<const uint2*>(smb + r)));
+            const bool in_b = r >= split;
+            const uint32_t c = in_b ? r - split : cbase + r;
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + b * cols + c));
+                float d = bf16_lo(wv4.x) * bf16_lo(xv.x);
+                d = fmaf(bf16_hi(wv4.x), bf16_hi(xv.x), d);
+                d = fmaf(bf16_lo(wv4.y), bf16_lo(xv.y), d);
+                d = fmaf(bf16_hi(wv4.y), bf16_hi(xv.y), d);
+                d = fmaf(bf16_lo(wv4.z), bf16_lo(xv.z), d);
+                d = fmaf(bf16_hi(wv4.z), bf16_hi(xv.z), d);
+                d = fmaf(bf16_lo(wv4.w), bf16_lo(xv.w), d);
+                d = fmaf(bf16_hi(wv4.w), bf16_hi(xv.w), d);
+                if (in_b)
+                    acc_b[b] += d;
+                else
+                    acc_a[b] += d;
+            }
+        }
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+        acc_a[b] = warp_sum_f(acc_a[b]);
+        acc_b[b] = warp_sum_f(acc_b[b]);
+    }
+    if (lane == 0) {
+        uint64_t* ws_o0 = reinterpret_cast<uint64_t*>(t.ws);
+        float* part = reinterpret_cast<float*>(ws_o0 + t.n_blocks * kSubtilesPerBlock);
+        ws_o0[s] = o0;
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+            part[(s * 2) * B + b] = acc_a[b];
+            part[(s * 2 + 1) * B + b] = acc_b[b];
+        }
+    }
+}
+
+// What warp_run does with a decoded sub-tile: store the BF16 weights, or
+// the fused GEMV above.
+struct StoreEpilogue {
+    __device__ __forceinline__ void operator()(const uint8_t* stage, const TensorArgs& t, uint64_t, uint64_t o0,
+                                               uint32_t count, bool ok, int lane) const {
+        if (ok && count) warp_store(stage, t.sm, t.out, o0, count, lane);
+    }
+};
+
+template <int B>
+struct GemvEpilogue {
+    __device__ __forceinline__ void operator()(const uint8_t* stage, const TensorArgs& t, uint64_t s, uint64_t o0,
+                                               uint32_t count, bool ok, int lane) const {
+        warp_gemv<B>(stage, t, s, o0, count, ok, lane);
+    }
+};
+
 // Restores sub-tiles [s0, s1) of tensor t with one warp.
+template <class Epi>
 __device__ __forceinline__ void warp_run(const TabView& tv, WarpSlot& ws, uint8_t* wstream, uint32_t wstride,
-                                         const TensorArgs& t, uint64_t s0, uint64_t s1, int lane, int32_t* status) {
+                                         const TensorArgs& t, uint64_t s0, uint64_t s1, int lane, int32_t* status,
+                                         const Epi& epi) {
     const uint32_t T = t.chunk_bytes;
     const uint32_t chunk_bits = 8u * T;
     const uint32_t sub_bytes = kWarpChunks * T, sub_bits = 8u * sub_bytes;
@@ -1173,7 +1281,6 @@ __device__ __forceinline__ void warp_run(const TabView& tv, WarpSlot& ws, uint8_
     const uint64_t n_sub = (t.n_chunks + kWarpChunks - 1) / kWarpChunks;
     const uint64_t n_full = t.n_sub_full;
     const uint8_t* const sm = t.sm;
-    uint16_t* const out = t.out;
     const uint64_t n = t.n;
     // the output index of sub-tile s0's first code
     const uint64_t blk = s0 / kSubtilesPerBlock;
@@ -1273,7 +1380,7 @@ __device__ __forceinline__ void warp_run(const TabView& tv, WarpSlot& ws, uint8_
         if (bad) raise_status(status, AFX_DEV_BAD_CHUNK);
         const bool any_bad = __any_sync(0xFFFFFFFFu, bad);
         __syncwarp();
-        if (!any_bad && in_range && total) warp_store(ws.stage, sm, out, o0, total, lane);
+        epi(ws.stage, t, s, o0, total, !any_bad && in_range, lane);
         start = o1;
         buf ^= 1;
         sub_in_block = (sub_in_block + 1) & (kSubtilesPerBlock - 1);
@@ -1291,7 +1398,8 @@ __device__ __forceinline__ void warp_run(const TabView& tv, WarpSlot& ws, uint8_
 }
 
 // One CTA per SM (up to 32 warps) sharing one copy of the decode tables.
-__global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1) restore_store_kernel(const __grid_constant__ LaunchArgs a) {
+template <class Epi>
+__device__ __forceinline__ void restore_warps(const LaunchArgs& a, const Epi& epi) {
     extern __shared__ __align__(16) uint8_t smem[];
     SharedW& sh = *reinterpret_cast<SharedW*>(smem);
     uint8_t* tabr = smem + sharedw_table_offset();
@@ -1329,8 +1437,51 @@ __global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1) restore_store_kernel
         build_tables_w(sh, tabr, t.tab, threadIdx.x, nthreads);  // ends with __syncthreads
         const uint64_t span = se - sb;
         const uint64_t s0 = sb + span * warp / nwarps, s1 = sb + span * (warp + 1) / nwarps;
-        if (s0 < s1) warp_run(tv, ws, wstream, wstride, t, s0, s1, lane, a.status);
+        if (s0 < s1) warp_run(tv, ws, wstream, wstride, t, s0, s1, lane, a.status, epi);
     }
+}
+
+__global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1) restore_store_kernel(const __grid_constant__ LaunchArgs a) {
+    restore_warps(a, StoreEpilogue{});
+}
+
+template <int B>
+__global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1) restore_gemv_kernel(const __grid_constant__ LaunchArgs a) {
+    restore_warps(a, GemvEpilogue<B>{});
+}
+
+// Rows of the warp GEMV: the sub-tile in which a row starts adds its own
+// partial of the row and the first-row partials of the following sub-tiles
+// that still lie in the row, in sub-tile order.  One thread per sub-tile.
+template <int B>
+__global__ void gemv_fixup_warp_kernel(const __grid_constant__ LaunchArgs a) {
+    const uint64_t g = blockIdx.x * static_cast<uint64_t>(blockDim.x) + threadIdx.x;
+    if (g >= a.total_subs) return;
+    uint32_t k = 0;
+    while (k + 1 < a.count && g >= a.t[k + 1].sub_begin) ++k;
+    const TensorArgs& t = a.t[k];
+    const uint64_t s = g - t.sub_begin;
+    const uint64_t n_sub = (t.n_chunks + kWarpChunks - 1) / kWarpChunks;
+    if (s >= n_sub) return;
+    const uint64_t* ws_o0 = reinterpret_cast<const uint64_t*>(t.ws);
+    const float* part = reinterpret_cast<const float*>(ws_o0 + t.n_blocks * kSubtilesPerBlock);
+    const uint64_t cols = t.cols, n = t.n;
+    const uint64_t o0 = ws_o0[s], o1 = s + 1 < n_sub ? ws_o0[s + 1] : n;
+    if (o1 <= o0 || o1 > n) return;  // empty, or a corrupt stream the main kernel already flagged
+    const uint64_t ra = o0 / cols, r = (o1 - 1) / cols;
+    const uint64_t row_start = r * cols, row_end = row_start + cols;
+    if (row_start < o0 || r >= t.rows) return;  // the row began in an earlier sub-tile
+    const int slot = r == ra ? 0 : 1;
+    float sum[kMaxBatch];
+#pragma unroll
+    for (int b = 0; b < B; ++b) sum[b] = part[(s * 2 + slot) * B + b];
+    for (uint64_t u = s + 1; u < n_sub; ++u) {
+        if (ws_o0[u] >= row_end) break;
+#pragma unroll
+        for (int b = 0; b < B; ++b) sum[b] += part[(u * 2) * B + b];
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b) t.y[static_cast<uint64_t>(b) * t.rows + r] = sum[b];
 }
 
 // Rows split across tiles: the tile in which a row starts adds its own tail
@@ -1551,46 +1702,77 @@ uint32_t gemv_rows_per_warp(uint32_t cols) {
     return static_cast<uint32_t>(slice / cols + 2);
 }
 
+// Up to 32 warps per CTA, one CTA per SM: the warp slots and stream
+// buffers are fixed by the warp count and the largest T, the rest of the
+// opt-in shared memory holds the tables.  A tensor whose state table does
+// not fit falls back to the 12-bit table.
+afx_status warp_launch_config(LaunchArgs& la, int* warps_out, size_t* smem_out) {
+    int optin = 0;
+    const int dev = current_device();
+    if (dev < 0) return afx_fail(AFX_E_CUDA, "no current CUDA device", 0);
+    AFX_CUDA_TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev), "cudaDeviceGetAttribute");
+    int warps = kRestoreMaxWarps;
+    size_t fixed = 0;
+    for (; warps >= 1; warps /= 2) {
+        fixed = sharedw_table_offset() + static_cast<size_t>(warps) * sizeof(WarpSlot) +
+                static_cast<size_t>(warps) * 2 * (kWarpChunks * la.max_chunk_bytes + kStreamPad);
+        if (fixed + kLutTabBytes <= static_cast<size_t>(optin)) break;
+    }
+    if (warps < 1) return afx_fail(AFX_E_ARG, "launch needs too much shared memory", 0);
+    const size_t budget = static_cast<size_t>(optin) - fixed;
+    uint32_t tab_bytes = kLutTabBytes;
+    for (uint32_t i = 0; i < la.count; ++i) {
+        CodeTables& tab = la.t[i].tab;
+        if (!tab.fsm) continue;
+        const size_t need = static_cast<size_t>(tab.n_states + kSkipRows) * kFsmRowBytes;
+        if (need > budget)
+            tab.fsm = 0;
+        else
+            tab_bytes = std::max<uint32_t>(tab_bytes, static_cast<uint32_t>(need));
+    }
+    la.tab_bytes = tab_bytes;
+    *warps_out = warps;
+    *smem_out = fixed + tab_bytes;
+    return AFX_OK;
+}
+
+// The warp GEMV (matrices whose rows hold at least kWarpStage weights, a
+// multiple of 8) and its row fix-up.
+template <int B>
+afx_status launch_gemv_warp(LaunchArgs& la, cudaStream_t s) {
+    if (la.count == 0 || la.total_tiles == 0) return AFX_OK;
+    const int sms = sm_count();
+    if (sms <= 0) return afx_fail(AFX_E_CUDA, "cannot query the SM count", 0);
+    int warps = 0;
+    size_t smem = 0;
+    const afx_status st = warp_launch_config(la, &warps, &smem);
+    if (st != AFX_OK) return st;
+    int per_sm = 0;
+    const afx_status pst = prepare_kernel(reinterpret_cast<const void*>(restore_gemv_kernel<B>), warps * 32, smem, &per_sm);
+    if (pst != AFX_OK) return pst;
+    const uint64_t grid = std::min<uint64_t>(la.total_tiles, static_cast<uint64_t>(sms) * per_sm);
+    restore_gemv_kernel<B><<<static_cast<unsigned>(grid), warps * 32, smem, s>>>(la);
+    AFX_CUDA_TRY(cudaGetLastError(), "restore_gemv_kernel launch");
+    const unsigned fix_blocks = static_cast<unsigned>((la.total_subs + 255) / 256);
+    gemv_fixup_warp_kernel<B><<<fix_blocks, 256, 0, s>>>(la);
+    AFX_CUDA_TRY(cudaGetLastError(), "gemv_fixup_warp_kernel launch");
+    return AFX_OK;
+}
+
 template <int B>
 afx_status launch_restore(LaunchArgs& la, cudaStream_t s) {
     if (la.count == 0 || la.total_tiles == 0) return AFX_OK;
     const int sms = sm_count();
     if (sms <= 0) return afx_fail(AFX_E_CUDA, "cannot query the SM count", 0);
     if constexpr (B == 0) {
-        // Up to 32 warps per CTA, one CTA per SM: the warp slots and stream
-        // buffers are fixed by the warp count and the largest T, the rest of
-        // the opt-in shared memory holds the tables.  A tensor whose state
-        // table does not fit falls back to the 12-bit table.
-        int optin = 0;
-        const int dev = current_device();
-        if (dev < 0) return afx_fail(AFX_E_CUDA, "no current CUDA device", 0);
-        AFX_CUDA_TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev),
-                     "cudaDeviceGetAttribute");
-        int warps = kRestoreMaxWarps;
-        size_t fixed = 0;
-        for (; warps >= 1; warps /= 2) {
-            fixed = sharedw_table_offset() + static_cast<size_t>(warps) * sizeof(WarpSlot) +
-                    static_cast<size_t>(warps) * 2 * (kWarpChunks * la.max_chunk_bytes + kStreamPad);
-            if (fixed + kLutTabBytes <= static_cast<size_t>(optin)) break;
-        }
-        if (warps < 1) return afx_fail(AFX_E_ARG, "launch needs too much shared memory", 0);
-        const size_t budget = static_cast<size_t>(optin) - fixed;
-        uint32_t tab_bytes = kLutTabBytes;
-        for (uint32_t i = 0; i < la.count; ++i) {
-            CodeTables& tab = la.t[i].tab;
-            if (!tab.fsm) continue;
-            const size_t need = static_cast<size_t>(tab.n_states + kSkipRows) * kFsmRowBytes;
-            if (need > budget)
-                tab.fsm = 0;
-            else
-                tab_bytes = std::max<uint32_t>(tab_bytes, static_cast<uint32_t>(need));
-        }
-        la.tab_bytes = tab_bytes;
-        const size_t smem = fixed + tab_bytes;
-        int per_sm = 0;
-        const afx_status st =
-            prepare_kernel(reinterpret_cast<const void*>(restore_store_kernel), warps * 32, smem, &per_sm);
+        int warps = 0;
+        size_t smem = 0;
+        const afx_status st = warp_launch_config(la, &warps, &smem);
         if (st != AFX_OK) return st;
+        int per_sm = 0;
+        const afx_status pst =
+            prepare_kernel(reinterpret_cast<const void*>(restore_store_kernel), warps * 32, smem, &per_sm);
+        if (pst != AFX_OK) return pst;
         const uint64_t grid = std::min<uint64_t>(la.total_tiles, static_cast<uint64_t>(sms) * per_sm);
         restore_store_kernel<<<static_cast<unsigned>(grid), warps * 32, smem, s>>>(la);
         AFX_CUDA_TRY(cudaGetLastError(), "restore_store_kernel launch");
@@ -1616,6 +1798,7 @@ afx_status launch_restore(LaunchArgs& la, cudaStream_t s) {
 void reset_launch(LaunchArgs& la) {
     la.count = 0;
     la.total_tiles = 0;
+    la.total_subs = 0;
     la.max_chunk_bytes = 0;
     la.max_rows_per_warp = 0;
 }
@@ -1679,13 +1862,19 @@ extern "C" afx_status afx_decode(const afx_desc* desc, const void* container, ui
 
 namespace {
 
+// Rows long enough for the warp GEMV: a sub-tile (at most kWarpStage - 16
+// weights) then meets at most two rows, and rows start on groups of 8.
+bool warp_gemv_shape(uint32_t cols) { return cols >= static_cast<uint32_t>(kWarpStage) && cols % 8 == 0; }
+
 template <int B>
 afx_status gemv_batch(const afx_desc* descs, const void* const* containers, const uint32_t* rows,
                       const uint32_t* cols, const uint16_t* const* xs, float* const* ys, void* const* workspaces,
                       uint32_t count, cudaStream_t s, int32_t* status) {
-    LaunchArgs la;
+    LaunchArgs la, lw;  // CTA-tile GEMV, warp GEMV
     std::memset(&la, 0, sizeof la);
+    std::memset(&lw, 0, sizeof lw);
     la.status = status;
+    lw.status = status;
     for (uint32_t i = 0; i < count; ++i) {
         const afx_desc& d = descs[i];
         const uint8_t* base = static_cast<const uint8_t*>(containers[i]);
@@ -1699,12 +1888,14 @@ afx_status gemv_batch(const afx_desc* descs, const void* const* containers, cons
             AFX_CUDA_TRY(cudaGetLastError(), "fill_gemv_kernel launch");
             continue;
         }
-        if (la.count == static_cast<uint32_t>(kMaxTensors)) {
-            const afx_status st = launch_restore<B>(la, s);
+        const bool warp = warp_gemv_shape(cols[i]);
+        LaunchArgs& L = warp ? lw : la;
+        if (L.count == static_cast<uint32_t>(kMaxTensors)) {
+            const afx_status st = warp ? launch_gemv_warp<B>(L, s) : launch_restore<B>(L, s);
             if (st != AFX_OK) return st;
-            reset_launch(la);
+            reset_launch(L);
         }
-        TensorArgs& t = la.t[la.count++];
+        TensorArgs& t = L.t[L.count++];
         fill_tensor(d, containers[i], t);
         t.x = xs[i];
         t.y = ys[i];
@@ -1712,11 +1903,15 @@ afx_status gemv_batch(const afx_desc* descs, const void* const* containers, cons
         t.rows = rows[i];
         t.cols = cols[i];
         t.rows_per_warp = gemv_rows_per_warp(cols[i]);
-        t.tile_begin = la.total_tiles;
-        la.total_tiles += d.n_blocks;
-        la.max_chunk_bytes = std::max(la.max_chunk_bytes, d.chunk_bytes);
-        la.max_rows_per_warp = std::max(la.max_rows_per_warp, t.rows_per_warp);
+        t.tile_begin = L.total_tiles;
+        t.sub_begin = L.total_subs;
+        L.total_tiles += d.n_blocks;
+        L.total_subs += (d.n_chunks + kWarpChunks - 1) / kWarpChunks;
+        L.max_chunk_bytes = std::max(L.max_chunk_bytes, d.chunk_bytes);
+        L.max_rows_per_warp = std::max(L.max_rows_per_warp, t.rows_per_warp);
     }
+    const afx_status st = launch_gemv_warp<B>(lw, s);
+    if (st != AFX_OK) return st;
     return launch_restore<B>(la, s);
 }
 

@@ -11,8 +11,10 @@
 #define AFX_DECODE_THREADS 512
 
 #ifdef __cplusplus
+// GEMV workspace: per sub-tile of 32 chunks (16 per block), its first
+// weight index and two row partials per batch row.
 inline uint64_t afx_gemv_workspace_bytes(uint64_t n_blocks, uint32_t batch) {
-    uint64_t b = n_blocks * 2ull * batch * sizeof(float);
+    uint64_t b = n_blocks * 16ull * (sizeof(uint64_t) + 2ull * batch * sizeof(float));
     return b < 16 ? 16 : (b + 15) / 16 * 16;
 }
 #endif
