@@ -236,6 +236,7 @@ typedef struct afx_op {
     void* out_dev;          /* AFX_OP_DECODE: uint16[n];  AFX_OP_GEMV: float[batch][rows] */
     void* workspace_dev;    /* AFX_OP_GEMV */
     uint64_t workspace_bytes;
+    void* out_host;         /* AFX_OP_DECODE, optional: pinned host uint16[n] that receives out_dev */
 } afx_op;
 
 typedef struct afx_layer {
@@ -254,8 +255,12 @@ typedef struct afx_layer {
  * (>= every blob_bytes), 256-byte aligned; they may be passed again to a
  * later call, whose first copy waits for all work already queued on
  * compute_stream.  Enqueues everything and returns; synchronise
- * compute_stream to wait for the results.  Consecutive ops of one kind
- * (and, for GEMV, one batch size) run as one batch launch.
+ * compute_stream and d2h_stream to wait for the results.  Consecutive ops
+ * of one kind (and, for GEMV, one batch size) run as one batch launch.
+ * A decode op with out_host set also copies its restored weights to that
+ * pinned host buffer, on d2h_stream (copy_stream when NULL) after the op,
+ * so that copy overlaps the next layer's load and ops; give layers one
+ * tensor each to overlap tensor by tensor.
  * Cites: "Why Weight Offloading Slows Inference", section "Loading during
  * computation" and Figure 2 (load layer l+1 while layer l computes; a load
  * is free only if it finishes before the GPU needs it), and "Memory
@@ -266,7 +271,7 @@ typedef struct afx_layer {
  * AFX_E_FORMAT, AFX_E_CUDA. */
 afx_status afx_stream_run(const afx_layer* layers, uint32_t n_layers, void* const* dev_bufs, uint32_t n_bufs,
                           uint64_t buf_bytes, afx_stream_t compute_stream, afx_stream_t copy_stream,
-                          int32_t* status_dev);
+                          afx_stream_t d2h_stream, int32_t* status_dev);
 
 /* Static text for a status code. */
 const char* afx_status_string(afx_status status);

@@ -79,6 +79,36 @@ def test_streamed_layers_match_the_oracle(afx, n_bufs):
             assert within_gemv_tolerance(out.cpu().numpy(), y_ref, A)
 
 
+@pytest.mark.parametrize("own_stream", [False, True])
+def test_restored_tensors_copied_back_to_host(afx, own_stream):
+    # one tensor per layer, each restored on the GPU and copied back to pinned host memory
+    import torch
+    layers, refs, hosts = [], [], []
+    for l in range(6):
+        w = synth.normal(50_000 + 9_999 * l, seed=40 + l)
+        c, d = afx.encode(w)
+        blob = torch.empty(c.size, dtype=torch.uint8).pin_memory()
+        blob.numpy()[:] = c
+        out = torch.empty(d.n, dtype=torch.int16, device="cuda")
+        host = torch.full((d.n,), -1, dtype=torch.int16).pin_memory()
+        op = afx.afx_op()
+        op.desc, op.offset, op.kind = d, 0, afx.AFX_OP_DECODE
+        op.out_dev, op.out_host = out.data_ptr(), host.data_ptr()
+        layers.append((blob, [op]))
+        refs.append((w, out))
+        hosts.append(host)
+    buf_bytes = max(b.numel() for b, _ in layers)
+    bufs = [torch.empty(buf_bytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    copy = torch.cuda.Stream()
+    d2h = torch.cuda.Stream() if own_stream else None
+    afx.afx_stream_run(layers, bufs, buf_bytes, torch.cuda.current_stream(), copy, status_dev=status, d2h_stream=d2h)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    for (w, out), host in zip(refs, hosts):
+        assert np.array_equal(host.numpy().view(np.uint16), w)
+
+
 def test_blob_larger_than_buffer_is_rejected(afx):
     import torch
     blob, metas = _layer(afx, 7, [("decode", (64, 640))])

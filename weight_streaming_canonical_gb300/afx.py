@@ -78,6 +78,7 @@ class afx_op(ctypes.Structure):
         ("out_dev", ctypes.c_void_p),
         ("workspace_dev", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_uint64),
+        ("out_host", ctypes.c_void_p),
     ]
 
 
@@ -106,7 +107,7 @@ _lib.afx_decode_gemv_batch.argtypes = [ctypes.POINTER(afx_desc), _PP, ctypes.POI
                                        ctypes.POINTER(ctypes.c_uint64), _u32, _vp, _i32p]
 _lib.afx_decode_gemv_static.argtypes = [ctypes.POINTER(afx_desc), _vp, _u32, _u32, _vp, _u32, _vp, _vp, _i32p]
 _lib.afx_stream_run.argtypes = [ctypes.POINTER(afx_layer), _u32, ctypes.POINTER(ctypes.c_void_p), _u32, _u64, _vp,
-                                _vp, _i32p]
+                                _vp, _vp, _i32p]
 _lib.afx_last_error.argtypes = []
 _lib.afx_last_error.restype = ctypes.c_char_p
 _lib.afx_status_string.argtypes = [ctypes.c_int]
@@ -261,7 +262,8 @@ def afx_decode_gemv_static(desc: afx_desc, container_dev, rows: int, cols: int, 
         _stream_handle(stream), _dev_ptr(status_dev)))
 
 
-def afx_stream_run(layers, dev_bufs, buf_bytes: int, compute_stream=None, copy_stream=None, status_dev=None) -> None:
+def afx_stream_run(layers, dev_bufs, buf_bytes: int, compute_stream=None, copy_stream=None, status_dev=None,
+                   d2h_stream=None) -> None:
     """layers: list of (pinned host uint8 tensor, [afx_op, ...]); dev_bufs: list of CUDA uint8 tensors."""
     arr = (afx_layer * len(layers))()
     keep = []
@@ -275,6 +277,7 @@ def afx_stream_run(layers, dev_bufs, buf_bytes: int, compute_stream=None, copy_s
     bufs = (ctypes.c_void_p * len(dev_bufs))(*[_dev_ptr(b) for b in dev_bufs])
     _check("afx_stream_run", _lib.afx_stream_run(arr, len(layers), bufs, len(dev_bufs), buf_bytes,
                                                   _stream_handle(compute_stream), _stream_handle(copy_stream),
+                                                  _stream_handle(d2h_stream) if d2h_stream is not None else None,
                                                   _dev_ptr(status_dev)))
 
 

@@ -12,7 +12,9 @@
 //
 // Ordering uses CUDA events only: buffer l % n_bufs is refilled after the
 // ops that read it have finished, and a layer's ops start after its copy.
-// The host never waits.
+// Restored tensors that go back to host memory are copied on a third
+// stream after their layer's ops, so that with a full-duplex link the copy
+// back overlaps the next layer's load.  The host never waits.
 #include <cuda_runtime.h>
 
 #include <vector>
@@ -98,7 +100,7 @@ afx_status run_group(const afx_op* ops, uint32_t count, uint8_t* buf, afx_stream
 
 extern "C" afx_status afx_stream_run(const afx_layer* layers, uint32_t n_layers, void* const* dev_bufs,
                                      uint32_t n_bufs, uint64_t buf_bytes, afx_stream_t compute_stream,
-                                     afx_stream_t copy_stream, int32_t* status_dev) {
+                                     afx_stream_t copy_stream, afx_stream_t d2h_stream, int32_t* status_dev) {
     if ((!layers && n_layers) || !dev_bufs || n_bufs < 2) return AFX_E_ARG;
     for (uint32_t k = 0; k < n_bufs; ++k)
         if (!dev_bufs[k] || !aligned256(dev_bufs[k])) return AFX_E_ARG;
@@ -108,6 +110,7 @@ extern "C" afx_status afx_stream_run(const afx_layer* layers, uint32_t n_layers,
     }
     cudaStream_t compute = reinterpret_cast<cudaStream_t>(compute_stream);
     cudaStream_t copy = reinterpret_cast<cudaStream_t>(copy_stream);
+    cudaStream_t d2h = d2h_stream ? reinterpret_cast<cudaStream_t>(d2h_stream) : copy;
     EventSet copied, consumed, entry;
     if (!copied.create(n_bufs) || !consumed.create(n_bufs) || !entry.create(1))
         return afx_fail(AFX_E_CUDA, "cudaEventCreateWithFlags", static_cast<int>(cudaGetLastError()));
@@ -137,6 +140,18 @@ extern "C" afx_status afx_stream_run(const afx_layer* layers, uint32_t n_layers,
             i = j;
         }
         AFX_STREAM_TRY(cudaEventRecord(consumed.ev[k], compute), "cudaEventRecord");
+        bool to_host = false;
+        for (uint32_t i = 0; i < L.n_ops; ++i) to_host = to_host || (L.ops[i].kind == AFX_OP_DECODE && L.ops[i].out_host);
+        if (to_host) {
+            AFX_STREAM_TRY(cudaStreamWaitEvent(d2h, consumed.ev[k], 0), "cudaStreamWaitEvent");
+            for (uint32_t i = 0; i < L.n_ops; ++i) {
+                const afx_op& op = L.ops[i];
+                if (op.kind != AFX_OP_DECODE || !op.out_host || op.desc.n == 0) continue;
+                AFX_STREAM_TRY(cudaMemcpyAsync(op.out_host, op.out_dev, op.desc.n * sizeof(uint16_t),
+                                               cudaMemcpyDeviceToHost, d2h),
+                               "cudaMemcpyAsync");
+            }
+        }
     }
     return AFX_OK;
 }
