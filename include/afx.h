@@ -68,6 +68,7 @@ typedef enum afx_status {
 #define AFX_DEV_BAD_CHUNK 0x2 /* a chunk's codewords do not end where the next chunk begins */
 #define AFX_DEV_BAD_CODE 0x4  /* a bit pattern that is no codeword */
 #define AFX_DEV_BAD_SHAPE 0x8 /* GEMV rows x cols disagree with the block index */
+#define AFX_DEV_TIMEOUT 0x10  /* a staging copy did not arrive within the kernel's wait limit; work skipped */
 
 #define AFX_MAX_CODE_LEN 24
 /* At most this many codewords start in one block (the decoder's per-block

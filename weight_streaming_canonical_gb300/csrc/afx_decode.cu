@@ -176,6 +176,57 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// mbarrier-tracked bulk copies (the TMA engine's non-tensor form): one
+// thread arms the barrier with the bytes to expect and issues the copies;
+// every waiting thread polls the barrier's phase.
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// [src, src + bytes) to shared dst, completing on bar; both addresses and
+// bytes multiples of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Waits for the phase of bar with the given parity to complete, giving up
+// after kWaitLimit polls (a copy of a few hundred bytes takes microseconds;
+// the limit is far beyond that).  Returns false on timeout.
+constexpr uint32_t kWaitLimit = 1u << 22;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kWaitLimit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// Orders this thread's earlier shared-memory reads before later writes of
+// the async proxy (a bulk copy refilling the same buffer).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
 // Exponents are kept rotated right by one bit, R = (e >> 1) | (e << 7), in
 // the decode tables and the stage buffer.  A BF16 weight's high byte is
 // sign | e >> 1 = (R & 0x7F) | (s & 0x80) and its low byte is
@@ -785,6 +836,7 @@ constexpr uint32_t kSkipRows = 7;                                // rows that fi
 struct WarpSlot {
     alignas(16) uint16_t chunk[2][kWarpChunkStage];
     alignas(16) uint8_t stage[kWarpStage];
+    uint64_t bar[2];    // completion of the bulk copies into stream buffer / chunk row 0 and 1
 };
 
 // Fixed part of the restore kernel's shared memory.  It is followed by the
@@ -794,6 +846,7 @@ struct WarpSlot {
 struct SharedW {
     uint32_t limit[AFX_MAX_CODE_LEN + 1];
     int32_t base[AFX_MAX_CODE_LEN + 1];
+    uint32_t state_base[AFX_MAX_CODE_LEN + 1];
     uint8_t sorted[256];
     uint8_t depth[64];               // depth of each state's node
     alignas(16) uint16_t first[kLutSize];  // first code of a 12-bit peek: length << 8 | rotated exponent
@@ -849,19 +902,21 @@ __device__ void build_tables_w(SharedW& sh, uint8_t* tabr, const CodeTables& tab
     for (int i = tid; i <= AFX_MAX_CODE_LEN; i += nthreads) {
         sh.limit[i] = tab.limit[i];
         sh.base[i] = tab.base[i];
+        sh.state_base[i] = tab.state_base[i];
     }
     for (int i = tid; i < 256; i += nthreads) sh.sorted[i] = tab.sorted[i];
     for (int i = tid; i < kMaxStates; i += nthreads) sh.depth[i] = tab.state_depth[i];
+    __syncthreads();
     for (int p0 = tid * 4; p0 < kLutSize; p0 += nthreads * 4) {
         int L = 1;
-        while (L <= kLutBits && (static_cast<uint32_t>(p0) << (24 - kLutBits)) >= tab.limit[L]) ++L;
+        while (L <= kLutBits && (static_cast<uint32_t>(p0) << (24 - kLutBits)) >= sh.limit[L]) ++L;
         for (int j = 0; j < 4; ++j) {
             const uint32_t p = static_cast<uint32_t>(p0 + j);
             const uint32_t v = p << (24 - kLutBits);
-            while (L <= kLutBits && v >= tab.limit[L]) ++L;
+            while (L <= kLutBits && v >= sh.limit[L]) ++L;
             uint16_t e = 0;
             if (L <= kLutBits)
-                e = static_cast<uint16_t>((L << 8) | ror8(tab.sorted[tab.base[L] + static_cast<int32_t>(v >> (24 - L))]));
+                e = static_cast<uint16_t>((L << 8) | ror8(sh.sorted[sh.base[L] + static_cast<int32_t>(v >> (24 - L))]));
             sh.first[p] = e;
         }
     }
@@ -890,8 +945,8 @@ __device__ void build_tables_w(SharedW& sh, uint8_t* tabr, const CodeTables& tab
             }
             const uint32_t r = avail - pos;
             const uint32_t q = r ? (V << pos) >> (32 - r) : 0u;
-            const uint32_t lo_r = r ? tab.limit[r] >> (24 - r) : 0u;
-            const uint32_t next = tab.state_base[r] + q - lo_r;
+            const uint32_t lo_r = r ? sh.limit[r] >> (24 - r) : 0u;
+            const uint32_t next = sh.state_base[r] + q - lo_r;
             fsm[(h ? nodes + h - 1 : 0u) * 256u + b] = make_uint2(out, (next * kFsmRowBytes) | ((cnt * 8u) << 26));
         }
         __syncthreads();
@@ -899,16 +954,16 @@ __device__ void build_tables_w(SharedW& sh, uint8_t* tabr, const CodeTables& tab
         // not end in it); the rest of the byte is skip row h
         for (uint32_t i = 256u + tid; i < nodes * 256u; i += nthreads) {
             const uint32_t s = i >> 8, b = i & 255u;
-            const uint32_t d = tab.state_depth[s];
-            const uint32_t lo_d = tab.limit[d] >> (24 - d);
-            const uint32_t p = lo_d + s - tab.state_base[d];
+            const uint32_t d = sh.depth[s];
+            const uint32_t lo_d = sh.limit[d] >> (24 - d);
+            const uint32_t p = lo_d + s - sh.state_base[d];
             uint32_t len;
             const uint32_t sym = decode_first(tv, (p << (32 - d)) | (b << (24 - d)), len);
             const uint32_t h = len - d;
             uint2 e;
             if (h > 8) {  // still inside the code: the node of its first d + 8 bits
                 const uint32_t d8 = d + 8;
-                const uint32_t next = tab.state_base[d8] + ((p << 8) | b) - (tab.limit[d8] >> (24 - d8));
+                const uint32_t next = sh.state_base[d8] + ((p << 8) | b) - (sh.limit[d8] >> (24 - d8));
                 e = make_uint2(0u, next * kFsmRowBytes);
             } else if (h == 8) {
                 e = make_uint2(sym, 8u << 26);
@@ -1088,7 +1143,10 @@ __device__ __forceinline__ bool fsm_chunk_finish(const TabView& tv, const uint32
         ++emitted;
     }
     uint8_t* p = reinterpret_cast<uint8_t*>(fl.wout);
-    for (uint32_t j = fl.first; j * 8 < fill; ++j) p[j] = static_cast<uint8_t>(acc >> (8 * j));
+    const uint32_t pending = fill >> 3;  // 0..4 bytes
+#pragma unroll
+    for (uint32_t j = 0; j < 4; ++j)
+        if (j >= fl.first && j < pending) p[j] = static_cast<uint8_t>(acc >> (8 * j));
     bool bad = emitted != cnt;
     if ((next >> 5) != 0)
         bad = bad || end != chunk_end + (next & 31u);
@@ -1104,38 +1162,31 @@ __device__ __forceinline__ uint32_t warp_stream_bytes(const TensorArgs& t, uint6
     return static_cast<uint32_t>(want < avail ? want : avail);
 }
 
-// cp.async of sub-tile s (its stream words and 33 chunk entries) into slot buf.
-__device__ __forceinline__ void warp_issue(WarpSlot& ws, uint8_t* wstream, uint32_t wstride, const TensorArgs& t,
-                                           uint64_t s, int buf, int lane) {
-    uint8_t* dst = wstream + static_cast<size_t>(buf) * wstride;
-    const uint8_t* src = reinterpret_cast<const uint8_t*>(t.exp_words) + s * kWarpChunks * t.chunk_bytes;
-    const uint32_t bytes = warp_stream_bytes(t, s);
-    for (uint32_t i = lane * 16u; i < bytes; i += 32 * 16u) cp_async16(dst + i, src + i);
-    const uint64_t cb0 = s * kWarpChunks * 2;
-    const uint64_t csec = (t.n_chunks * 2 + 15) & ~uint64_t(15);
-    const uint64_t cavail = csec > cb0 ? csec - cb0 : 0;
-    const uint32_t cbytes = static_cast<uint32_t>(cavail < kWarpChunkStage * 2 ? cavail : kWarpChunkStage * 2);
-    if (lane * 16u < cbytes)
-        cp_async16(reinterpret_cast<uint8_t*>(ws.chunk[buf]) + lane * 16,
-                   reinterpret_cast<const uint8_t*>(t.chunk_index) + cb0 + lane * 16);
-    cp_async_commit();
-}
-
 __device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
 #pragma unroll
     for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, d);
     return v;
 }
 
-// cp.async of a full sub-tile (see TensorArgs::n_sub_full): its stream
-// bytes plus the pad and 40 chunk entries, from sources that are known to
-// hold them.
-__device__ __forceinline__ void warp_issue_full(uint16_t* chunk_dst, uint8_t* stream_dst, const uint8_t* exp_src,
-                                                const uint16_t* chunk_src, uint32_t sub_bytes, int lane) {
-    for (uint32_t i = lane * 16u; i < sub_bytes + kStreamPad; i += 32 * 16u) cp_async16(stream_dst + i, exp_src + i);
-    if (lane < kWarpChunkStage * 2 / 16)
-        cp_async16(reinterpret_cast<uint8_t*>(chunk_dst) + lane * 16, reinterpret_cast<const uint8_t*>(chunk_src) + lane * 16);
-    cp_async_commit();
+// Stages sub-tile s in buffer b with two bulk copies on ws.bar[b], issued
+// by lane 0: the stream bytes of its 32 chunks plus the pad, and its 40
+// chunk entries (the next sub-tile's first included).  A full sub-tile
+// (TensorArgs::n_sub_full) has all of them; the last ones take what the
+// sections hold.  Every size and address is a multiple of 16.
+__device__ __forceinline__ void warp_issue_bulk(WarpSlot& ws, uint8_t* stream_dst, const TensorArgs& t, uint64_t s,
+                                                bool full, const uint8_t* exp_src, const uint16_t* chunk_src,
+                                                uint32_t sub_bytes, int b) {
+    uint32_t sbytes = sub_bytes + kStreamPad, cbytes = kWarpChunkStage * 2;
+    if (!full) {
+        sbytes = warp_stream_bytes(t, s);
+        const uint64_t cb0 = s * kWarpChunks * 2;
+        const uint64_t csec = (t.n_chunks * 2 + 15) & ~uint64_t(15);
+        const uint64_t cavail = csec > cb0 ? csec - cb0 : 0;
+        cbytes = static_cast<uint32_t>(cavail < kWarpChunkStage * 2 ? cavail : kWarpChunkStage * 2);
+    }
+    mbar_expect_tx(&ws.bar[b], sbytes + cbytes);
+    if (sbytes) bulk_copy_g2s(stream_dst, exp_src, sbytes, &ws.bar[b]);
+    if (cbytes) bulk_copy_g2s(ws.chunk[b], chunk_src, cbytes, &ws.bar[b]);
 }
 
 // Joins and stores `count` weights from o0 with the 32 lanes of a warp; the
@@ -1268,11 +1319,13 @@ struct GemvEpilogue {
     }
 };
 
-// Restores sub-tiles [s0, s1) of tensor t with one warp.
+// Restores sub-tiles [s0, s1) of tensor t with one warp.  phases holds the
+// parity each of the warp's two copy barriers waits for next.  Returns false
+// when a staging copy timed out (the run is abandoned and flagged).
 template <class Epi>
-__device__ __forceinline__ void warp_run(const TabView& tv, WarpSlot& ws, uint8_t* wstream, uint32_t wstride,
+__device__ __forceinline__ bool warp_run(const TabView& tv, WarpSlot& ws, uint8_t* wstream, uint32_t wstride,
                                          const TensorArgs& t, uint64_t s0, uint64_t s1, int lane, int32_t* status,
-                                         const Epi& epi) {
+                                         uint32_t& phases, const Epi& epi) {
     const uint32_t T = t.chunk_bytes;
     const uint32_t chunk_bits = 8u * T;
     const uint32_t sub_bytes = kWarpChunks * T, sub_bits = 8u * sub_bytes;
@@ -1292,10 +1345,7 @@ __device__ __forceinline__ void warp_run(const TabView& tv, WarpSlot& ws, uint8_
     // sources of the next sub-tile to stage
     const uint8_t* exp_src = reinterpret_cast<const uint8_t*>(t.exp_words) + s0 * sub_bytes;
     const uint16_t* chunk_src = t.chunk_index + s0 * kWarpChunks;
-    if (s0 < n_full)
-        warp_issue_full(ws.chunk[0], wstream, exp_src, chunk_src, sub_bytes, lane);
-    else
-        warp_issue(ws, wstream, wstride, t, s0, 0, lane);
+    if (lane == 0) warp_issue_bulk(ws, wstream, t, s0, s0 < n_full, exp_src, chunk_src, sub_bytes, 0);
     const uint32_t nrun = static_cast<uint32_t>(s1 - s0);
     uint32_t sub_in_block = static_cast<uint32_t>(s0 % kSubtilesPerBlock);
     int buf = 0;
@@ -1304,15 +1354,21 @@ __device__ __forceinline__ void warp_run(const TabView& tv, WarpSlot& ws, uint8_
         if (r + 1 < nrun) {
             exp_src += sub_bytes;
             chunk_src += kWarpChunks;
-            if (s + 1 < n_full)
-                warp_issue_full(ws.chunk[buf ^ 1], wstream + (buf ^ 1) * wstride, exp_src, chunk_src, sub_bytes, lane);
-            else
-                warp_issue(ws, wstream, wstride, t, s + 1, buf ^ 1, lane);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
+            if (lane == 0)
+                warp_issue_bulk(ws, wstream + (buf ^ 1) * wstride, t, s + 1, s + 1 < n_full, exp_src, chunk_src,
+                                sub_bytes, buf ^ 1);
         }
-        __syncwarp();
+        const bool arrived = mbar_wait(&ws.bar[buf], (phases >> buf) & 1u);
+        phases ^= 1u << buf;
+        if (!__all_sync(0xFFFFFFFFu, arrived)) {
+            // give up on this run: flag it and let the copy still in flight land
+            if (lane == 0) raise_status(status, AFX_DEV_TIMEOUT);
+            if (r + 1 < nrun) {
+                mbar_wait(&ws.bar[buf ^ 1], (phases >> (buf ^ 1)) & 1u);
+                phases ^= 1u << (buf ^ 1);
+            }
+            return false;
+        }
         if (r != 0 && sub_in_block == 0) {  // a block boundary inside the run
             const uint64_t bo = __ldg(t.block_index + s / kSubtilesPerBlock);
             if (bo != start) {
@@ -1384,6 +1440,7 @@ __device__ __forceinline__ void warp_run(const TabView& tv, WarpSlot& ws, uint8_
         start = o1;
         buf ^= 1;
         sub_in_block = (sub_in_block + 1) & (kSubtilesPerBlock - 1);
+        fence_proxy_async_smem();  // this buffer's reads come before the bulk copy that refills it
         __syncwarp();
     }
     // a run that ends on a block boundary checks the block index there; the
@@ -1395,6 +1452,7 @@ __device__ __forceinline__ void warp_run(const TabView& tv, WarpSlot& ws, uint8_
         if (s1 == n_sub && (start != n || __ldg(t.block_index + t.n_blocks) != n))
             raise_status(status, AFX_DEV_BAD_BLOCK);
     }
+    return true;
 }
 
 // One CTA per SM (up to 32 warps) sharing one copy of the decode tables.
@@ -1423,6 +1481,13 @@ __device__ __forceinline__ void restore_warps(const LaunchArgs& a, const Epi& ep
     const uint64_t g_begin = a.total_tiles * blockIdx.x / gridDim.x;
     const uint64_t g_end = a.total_tiles * (blockIdx.x + 1) / gridDim.x;
     if (g_begin >= g_end) return;
+    if (lane == 0) {
+        mbar_init(&ws.bar[0]);
+        mbar_init(&ws.bar[1]);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    uint32_t phases = 0;  // parity each copy barrier of this warp waits for next
+    bool alive = true;    // false after a staging copy timed out
     for (uint32_t k = 0; k < a.count; ++k) {
         const TensorArgs& t = a.t[k];
         const uint64_t t0 = t.tile_begin, t1 = t.tile_begin + t.n_blocks;
@@ -1437,7 +1502,7 @@ __device__ __forceinline__ void restore_warps(const LaunchArgs& a, const Epi& ep
         build_tables_w(sh, tabr, t.tab, threadIdx.x, nthreads);  // ends with __syncthreads
         const uint64_t span = se - sb;
         const uint64_t s0 = sb + span * warp / nwarps, s1 = sb + span * (warp + 1) / nwarps;
-        if (s0 < s1) warp_run(tv, ws, wstream, wstride, t, s0, s1, lane, a.status, epi);
+        if (alive && s0 < s1) alive = warp_run(tv, ws, wstream, wstride, t, s0, s1, lane, a.status, phases, epi);
     }
 }
 
