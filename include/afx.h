@@ -274,6 +274,19 @@ afx_status afx_stream_run(const afx_layer* layers, uint32_t n_layers, void* cons
                           uint64_t buf_bytes, afx_stream_t compute_stream, afx_stream_t copy_stream,
                           afx_stream_t d2h_stream, int32_t* status_dev);
 
+/* Failure injection for tests of the staging timeout: restores a coded
+ * tensor (two or more exponents) as afx_decode, except that every staging
+ * barrier is armed with the bytes it expects and no copy is issued.  Each
+ * warp's first wait therefore gives up after wait_polls polls (1..2^22);
+ * the kernel ORs AFX_DEV_TIMEOUT into *status_dev (required) and returns
+ * without touching out_dev.  Nothing is left in flight, so the context stays
+ * usable.  The production entry points wait up to 2^22 polls.
+ * No counterpart on the pages: this exists to test the library's own
+ * bounded waits.
+ * Errors: AFX_E_ARG, AFX_E_FORMAT, AFX_E_CUDA. */
+afx_status afx_test_restore_stalled(const afx_desc* desc, const void* container_dev, uint16_t* out_dev,
+                                    uint32_t wait_polls, afx_stream_t stream, int32_t* status_dev);
+
 /* Static text for a status code. */
 const char* afx_status_string(afx_status status);
 

@@ -177,6 +177,36 @@ def test_garbage_stream_never_hangs(afx):
     assert status != 0
 
 
+@pytest.mark.parametrize("n", [200_003, 3_000_017])
+def test_staging_wait_that_runs_out_is_flagged_and_the_gpu_stays_usable(afx, n):
+    # failure injection: the staging barriers are armed and no copy is issued,
+    # so every warp's first wait gives up; nothing is left in flight
+    import torch
+    w = synth.normal(n, seed=31)
+    c, d = afx.encode(w)
+    dev = torch.from_numpy(c).cuda()
+    out = torch.full((n,), 0x5A5A, dtype=torch.int16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    afx.afx_test_restore_stalled(d, dev, out, 2000, status)
+    torch.cuda.synchronize()
+    assert status.item() & afx.AFX_DEV_TIMEOUT
+    assert bool((out == 0x5A5A).all())
+    # the same context restores the tensor correctly afterwards
+    got, st, _ = gpu_decode(afx, c, d)
+    assert st == 0 and np.array_equal(got, w)
+
+
+def test_stalled_restore_rejects_bad_arguments(afx):
+    import torch
+    c, d = afx.encode(synth.normal(10_000, seed=2))
+    dev = torch.from_numpy(c).cuda()
+    out = torch.empty(d.n, dtype=torch.int16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for polls in (0, (1 << 22) + 1):
+        with pytest.raises(afx.AfxError):
+            afx.afx_test_restore_stalled(d, dev, out, polls, status)
+
+
 def test_host_side_argument_errors(afx):
     import torch
     w = synth.normal(10_000, seed=15)

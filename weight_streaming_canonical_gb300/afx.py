@@ -25,6 +25,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 AFX_OK, AFX_E_ARG, AFX_E_FORMAT, AFX_E_CORRUPT, AFX_E_CUDA, AFX_E_NOSPACE, AFX_E_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
 AFX_DEV_BAD_BLOCK, AFX_DEV_BAD_CHUNK, AFX_DEV_BAD_CODE, AFX_DEV_BAD_SHAPE = 0x1, 0x2, 0x4, 0x8
+AFX_DEV_TIMEOUT = 0x10
 AFX_MAX_CODE_LEN = 24
 AFX_BLOCK_CAPACITY = 32768
 AFX_HEADER_BYTES = 512
@@ -108,13 +109,14 @@ _lib.afx_decode_gemv_batch.argtypes = [ctypes.POINTER(afx_desc), _PP, ctypes.POI
 _lib.afx_decode_gemv_static.argtypes = [ctypes.POINTER(afx_desc), _vp, _u32, _u32, _vp, _u32, _vp, _vp, _i32p]
 _lib.afx_stream_run.argtypes = [ctypes.POINTER(afx_layer), _u32, ctypes.POINTER(ctypes.c_void_p), _u32, _u64, _vp,
                                 _vp, _vp, _i32p]
+_lib.afx_test_restore_stalled.argtypes = [ctypes.POINTER(afx_desc), _vp, _vp, _u32, _vp, _i32p]
 _lib.afx_last_error.argtypes = []
 _lib.afx_last_error.restype = ctypes.c_char_p
 _lib.afx_status_string.argtypes = [ctypes.c_int]
 _lib.afx_status_string.restype = ctypes.c_char_p
 for _f in (_lib.afx_build_code, _lib.afx_encode_bound, _lib.afx_encode, _lib.afx_parse_header, _lib.afx_decode,
            _lib.afx_decode_batch, _lib.afx_decode_gemv_workspace, _lib.afx_decode_gemv, _lib.afx_decode_gemv_batch,
-           _lib.afx_decode_gemv_static, _lib.afx_stream_run):
+           _lib.afx_decode_gemv_static, _lib.afx_stream_run, _lib.afx_test_restore_stalled):
     _f.restype = ctypes.c_int
 
 
@@ -198,6 +200,14 @@ def afx_decode(desc: afx_desc, container_dev, out_dev, stream=None, status_dev=N
         raise ValueError("out_dev must hold n 16-bit elements")
     _check("afx_decode", _lib.afx_decode(ctypes.byref(desc), _dev_ptr(container_dev), _dev_ptr(out_dev),
                                           _stream_handle(stream), _dev_ptr(status_dev)))
+
+
+def afx_test_restore_stalled(desc: afx_desc, container_dev, out_dev, wait_polls: int, status_dev,
+                             stream=None) -> None:
+    """Failure injection: a restore whose staging copies never come (see afx.h)."""
+    _check("afx_test_restore_stalled",
+           _lib.afx_test_restore_stalled(ctypes.byref(desc), _dev_ptr(container_dev), _dev_ptr(out_dev), wait_polls,
+                                         _stream_handle(stream), _dev_ptr(status_dev)))
 
 
 def _ptrs(tensors) -> ctypes.Array:

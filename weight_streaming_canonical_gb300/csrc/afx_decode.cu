@@ -126,6 +126,8 @@ struct LaunchArgs {
     uint32_t tab_bytes;        // restore path: size of the shared decode-table region
     uint64_t total_tiles;
     uint64_t total_subs;       // warp GEMV: sub-tiles of all tensors
+    uint32_t wait_limit;       // polls of a staging wait before it gives up (0: kWaitLimit)
+    uint32_t stall;            // failure injection for tests: arm the staging barriers, issue no copies
     int32_t* status;
     TensorArgs t[kMaxTensors];
 };
@@ -215,8 +217,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // after kWaitLimit polls (a copy of a few hundred bytes takes microseconds;
 // the limit is far beyond that).  Returns false on timeout.
 constexpr uint32_t kWaitLimit = 1u << 22;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
 }
@@ -1175,7 +1177,7 @@ __device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
 // sections hold.  Every size and address is a multiple of 16.
 __device__ __forceinline__ void warp_issue_bulk(WarpSlot& ws, uint8_t* stream_dst, const TensorArgs& t, uint64_t s,
                                                 bool full, const uint8_t* exp_src, const uint16_t* chunk_src,
-                                                uint32_t sub_bytes, int b) {
+                                                uint32_t sub_bytes, int b, bool stall) {
     uint32_t sbytes = sub_bytes + kStreamPad, cbytes = kWarpChunkStage * 2;
     if (!full) {
         sbytes = warp_stream_bytes(t, s);
@@ -1185,6 +1187,7 @@ __device__ __forceinline__ void warp_issue_bulk(WarpSlot& ws, uint8_t* stream_ds
         cbytes = static_cast<uint32_t>(cavail < kWarpChunkStage * 2 ? cavail : kWarpChunkStage * 2);
     }
     mbar_expect_tx(&ws.bar[b], sbytes + cbytes);
+    if (stall) return;  // failure injection: the bytes never come
     if (sbytes) bulk_copy_g2s(stream_dst, exp_src, sbytes, &ws.bar[b]);
     if (cbytes) bulk_copy_g2s(ws.chunk[b], chunk_src, cbytes, &ws.bar[b]);
 }
@@ -1325,7 +1328,7 @@ struct GemvEpilogue {
 template <class Epi>
 __device__ __forceinline__ bool warp_run(const TabView& tv, WarpSlot& ws, uint8_t* wstream, uint32_t wstride,
                                          const TensorArgs& t, uint64_t s0, uint64_t s1, int lane, int32_t* status,
-                                         uint32_t& phases, const Epi& epi) {
+                                         uint32_t wait_limit, bool stall, uint32_t& phases, const Epi& epi) {
     const uint32_t T = t.chunk_bytes;
     const uint32_t chunk_bits = 8u * T;
     const uint32_t sub_bytes = kWarpChunks * T, sub_bits = 8u * sub_bytes;
@@ -1345,7 +1348,7 @@ __device__ __forceinline__ bool warp_run(const TabView& tv, WarpSlot& ws, uint8_
     // sources of the next sub-tile to stage
     const uint8_t* exp_src = reinterpret_cast<const uint8_t*>(t.exp_words) + s0 * sub_bytes;
     const uint16_t* chunk_src = t.chunk_index + s0 * kWarpChunks;
-    if (lane == 0) warp_issue_bulk(ws, wstream, t, s0, s0 < n_full, exp_src, chunk_src, sub_bytes, 0);
+    if (lane == 0) warp_issue_bulk(ws, wstream, t, s0, s0 < n_full, exp_src, chunk_src, sub_bytes, 0, stall);
     const uint32_t nrun = static_cast<uint32_t>(s1 - s0);
     uint32_t sub_in_block = static_cast<uint32_t>(s0 % kSubtilesPerBlock);
     int buf = 0;
@@ -1356,15 +1359,15 @@ __device__ __forceinline__ bool warp_run(const TabView& tv, WarpSlot& ws, uint8_
             chunk_src += kWarpChunks;
             if (lane == 0)
                 warp_issue_bulk(ws, wstream + (buf ^ 1) * wstride, t, s + 1, s + 1 < n_full, exp_src, chunk_src,
-                                sub_bytes, buf ^ 1);
+                                sub_bytes, buf ^ 1, stall);
         }
-        const bool arrived = mbar_wait(&ws.bar[buf], (phases >> buf) & 1u);
+        const bool arrived = mbar_wait(&ws.bar[buf], (phases >> buf) & 1u, wait_limit);
         phases ^= 1u << buf;
         if (!__all_sync(0xFFFFFFFFu, arrived)) {
             // give up on this run: flag it and let the copy still in flight land
             if (lane == 0) raise_status(status, AFX_DEV_TIMEOUT);
             if (r + 1 < nrun) {
-                mbar_wait(&ws.bar[buf ^ 1], (phases >> (buf ^ 1)) & 1u);
+                mbar_wait(&ws.bar[buf ^ 1], (phases >> (buf ^ 1)) & 1u, wait_limit);
                 phases ^= 1u << (buf ^ 1);
             }
             return false;
@@ -1487,6 +1490,7 @@ __device__ __forceinline__ void restore_warps(const LaunchArgs& a, const Epi& ep
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     uint32_t phases = 0;  // parity each copy barrier of this warp waits for next
+    const uint32_t wait_limit = a.wait_limit ? a.wait_limit : kWaitLimit;
     bool alive = true;    // false after a staging copy timed out
     for (uint32_t k = 0; k < a.count; ++k) {
         const TensorArgs& t = a.t[k];
@@ -1502,7 +1506,8 @@ __device__ __forceinline__ void restore_warps(const LaunchArgs& a, const Epi& ep
         build_tables_w(sh, tabr, t.tab, threadIdx.x, nthreads);  // ends with __syncthreads
         const uint64_t span = se - sb;
         const uint64_t s0 = sb + span * warp / nwarps, s1 = sb + span * (warp + 1) / nwarps;
-        if (alive && s0 < s1) alive = warp_run(tv, ws, wstream, wstride, t, s0, s1, lane, a.status, phases, epi);
+        if (alive && s0 < s1)
+            alive = warp_run(tv, ws, wstream, wstride, t, s0, s1, lane, a.status, wait_limit, a.stall != 0, phases, epi);
     }
 }
 
@@ -1872,8 +1877,12 @@ void reset_launch(LaunchArgs& la) {
 
 using namespace afx;
 
-extern "C" afx_status afx_decode_batch(const afx_desc* descs, const void* const* containers, uint16_t* const* outs,
-                                       uint32_t count, afx_stream_t stream, int32_t* status) {
+namespace {
+
+// afx_decode_batch; stall_polls != 0 is the failure injection of
+// afx_test_restore_stalled.
+afx_status decode_batch(const afx_desc* descs, const void* const* containers, uint16_t* const* outs, uint32_t count,
+                        afx_stream_t stream, int32_t* status, uint32_t stall_polls) {
     if (count && (!descs || !containers || !outs)) return afx_fail(AFX_E_ARG, "null array", 0);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     for (uint32_t i = 0; i < count; ++i) {
@@ -1889,6 +1898,8 @@ extern "C" afx_status afx_decode_batch(const afx_desc* descs, const void* const*
     LaunchArgs la;
     std::memset(&la, 0, sizeof la);
     la.status = status;
+    la.wait_limit = stall_polls;
+    la.stall = stall_polls != 0;
     for (uint32_t i = 0; i < count; ++i) {
         const afx_desc& d = descs[i];
         if (d.n == 0) continue;
@@ -1916,6 +1927,22 @@ extern "C" afx_status afx_decode_batch(const afx_desc* descs, const void* const*
         la.max_chunk_bytes = std::max(la.max_chunk_bytes, d.chunk_bytes);
     }
     return launch_restore<0>(la, s);
+}
+
+}  // namespace
+
+extern "C" afx_status afx_decode_batch(const afx_desc* descs, const void* const* containers, uint16_t* const* outs,
+                                       uint32_t count, afx_stream_t stream, int32_t* status) {
+    return decode_batch(descs, containers, outs, count, stream, status, 0);
+}
+
+extern "C" afx_status afx_test_restore_stalled(const afx_desc* desc, const void* container, uint16_t* out,
+                                               uint32_t wait_polls, afx_stream_t stream, int32_t* status) {
+    if (!desc) return afx_fail(AFX_E_ARG, "null description", 0);
+    if (desc->nsym < 2 || desc->n == 0) return afx_fail(AFX_E_ARG, "needs a coded tensor (two or more exponents)", 0);
+    if (!container || !out || !status) return afx_fail(AFX_E_ARG, "null pointer", 0);
+    if (wait_polls == 0 || wait_polls > kWaitLimit) return afx_fail(AFX_E_ARG, "wait_polls must be 1..2^22", 0);
+    return decode_batch(desc, &container, &out, 1, stream, status, wait_polls);
 }
 
 extern "C" afx_status afx_decode(const afx_desc* desc, const void* container, uint16_t* out, afx_stream_t stream,
