@@ -426,6 +426,7 @@ def run_ours(args):
 
     if not args.no_extras and rank == 0:
         line["e2e"] = run_e2e(afx, parts, views, dev, args)
+        line["zero_copy"] = run_zero_copy(afx, parts, dev, args)
         line["cpu_baseline"] = run_cpu_baseline(parts)
         if args.workload == "layer":
             line["fused_gemv"] = run_gemv_bench(afx, parts, dev_blob, offs, dev, args)
@@ -496,6 +497,50 @@ def run_e2e(afx, parts, views, dev, args):
             "bit_exact": bool(ok),
             "path": "afx_stream_run, one tensor per streamed layer: pinned host containers in, BF16 back to pinned "
                     "host on a third stream"}
+
+
+def run_zero_copy(afx, parts, dev, args):
+    """The layer's containers stay in pinned host memory and one
+    afx_decode_batch call reads them over the host link (no staging copy):
+    into device memory, and back into pinned host memory (host to host in
+    one launch).  Compared with the copy pipeline in e2e."""
+    import torch
+    n = sum(d.n for _, _, _, d in parts)
+    host_c = []
+    for (_, _, c, _) in parts:
+        t = torch.empty(c.size, dtype=torch.uint8).pin_memory()
+        t.numpy()[:] = c
+        host_c.append(t)
+    descs = [d for *_, d in parts]
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    res = {}
+    for where in ("device", "host"):
+        if where == "device":
+            outs = [torch.empty(d.n, dtype=torch.int16, device=dev) for d in descs]
+        else:
+            outs = [torch.empty(d.n, dtype=torch.int16).pin_memory() for d in descs]
+        stream = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(stream):
+            for _ in range(max(3, args.warmup)):
+                afx.afx_decode_batch(descs, host_c, outs, stream=stream, status_dev=status)
+            torch.cuda.synchronize()
+            steps = max(3, args.steps // 2)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                afx.afx_decode_batch(descs, host_c, outs, stream=stream, status_dev=status)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        ok = status.item() == 0 and all(np.array_equal(o.cpu().numpy().view(np.uint16), w)
+                                        for o, (_, w, _, _) in zip(outs, parts))
+        res["to_" + where] = {"value": 2 * n / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+                              "link_read_bytes": int(sum(c.numel() for c in host_c)),
+                              "link_write_bytes": 2 * n if where == "host" else 0, "bit_exact": bool(ok)}
+    res["path"] = ("afx_decode_batch of the layer with its containers in pinned host memory, read by "
+                   "restore_store_host_kernel over the host link; to_host also writes the BF16 weights to "
+                   "pinned host memory")
+    return res
 
 
 def _layer_ops(afx, parts, B, dev, keep):

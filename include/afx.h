@@ -140,17 +140,20 @@ afx_status afx_encode(const uint16_t* w_host, uint64_t n, const afx_code* code, 
 afx_status afx_parse_header(const uint8_t* header_host, uint64_t bytes, afx_desc* out);
 
 /* Restores all n BF16 weights of one container: out_dev[i] = the i-th
- * weight, bit for bit.  container_dev: the whole container in device
- * memory, 16-byte aligned.  out_dev: n uint16 in device memory, 16-byte
- * aligned.  desc: host copy of the container's description.  Runs
- * asynchronously on `stream`; never reads outside the container or writes
- * outside out_dev[0..n).  A corrupt stream or index sets AFX_DEV_* bits in
- * *status_dev (the output is then unspecified).
+ * weight, bit for bit.  container_dev: the whole container, 16-byte
+ * aligned, in device memory or in pinned (or managed) host memory; a
+ * host-resident container is read by the kernel over the host link with no
+ * staging copy ("zero copy").  out_dev: n uint16, 16-byte aligned, in
+ * device memory or pinned host memory.  desc: host copy of the container's
+ * description.  Runs asynchronously on `stream`; never reads outside the
+ * container or writes outside out_dev[0..n).  A corrupt stream or index
+ * sets AFX_DEV_* bits in *status_dev (the output is then unspecified).
  * Cites: "Why Weight Offloading Slows Inference", section "Lossless
  * compression: fewer bytes to read, more work to unpack" (restore the
- * released bits before computation; t_unpack of Eq. (1)).
- * Errors: AFX_E_ARG (null or misaligned pointers), AFX_E_FORMAT (desc),
- * AFX_E_CUDA (launch). */
+ * released bits before computation; t_unpack of Eq. (1)); the zero-copy
+ * read is that page's load path over the link without the staging copy.
+ * Errors: AFX_E_ARG (null or misaligned pointers, pageable host memory),
+ * AFX_E_FORMAT (desc), AFX_E_CUDA (launch). */
 afx_status afx_decode(const afx_desc* desc, const void* container_dev, uint16_t* out_dev,
                       afx_stream_t stream, int32_t* status_dev);
 
@@ -178,7 +181,8 @@ afx_status afx_decode_gemv_workspace(const afx_desc* desc, uint32_t batch, uint6
  * to global memory.  Products and sums are float32; y_dev is float32
  * [batch][rows], overwritten, and bitwise reproducible run to run.
  * workspace_dev: afx_decode_gemv_workspace bytes of device memory, 16-byte
- * aligned, contents ignored.  Requires cols >= 64, x_dev 16-byte aligned.
+ * aligned, contents ignored.  Requires cols >= 64, x_dev 16-byte aligned,
+ * and the container in device memory.
  * Cites: same passage as afx_decode -- the restored weights feed the
  * computation directly.
  * Errors: AFX_E_ARG (shape, batch, alignment), AFX_E_NOSPACE (workspace),

@@ -305,3 +305,70 @@ def test_full_model_resident_bit_exact(afx):
         if name in sampled:
             ref, st = oracle.decode(c)
             assert st == oracle.OK and np.array_equal(o.cpu().numpy().view(np.uint16), ref), name
+
+
+# ---- containers in pinned host memory (read by the kernel over the host link) ----
+
+def _pinned(a: np.ndarray):
+    import torch
+    t = torch.empty(a.nbytes, dtype=torch.uint8).pin_memory()
+    t.numpy()[:] = a.view(np.uint8).reshape(-1)
+    return t
+
+
+@pytest.mark.parametrize("n", [1, 1000, 65_537, 3_000_017])
+@pytest.mark.parametrize("out_on_host", [False, True])
+def test_restore_from_pinned_host_container(afx, n, out_on_host):
+    import torch
+    w = synth.normal(n, seed=50 + n)
+    c, d = afx.encode(w)
+    host_c = _pinned(c)
+    if out_on_host:
+        out = torch.full((n,), 0x5A5A, dtype=torch.int16).pin_memory()
+    else:
+        out = torch.full((n,), 0x5A5A, dtype=torch.int16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    afx.afx_decode(d, host_c, out, status_dev=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), w)
+
+
+def test_batch_mixing_host_and_device_containers(afx):
+    import torch
+    ws = [synth.normal(200_000 + 7 * i, seed=60 + i) for i in range(4)] + [synth.adversarial(300_001, seed=3)]
+    enc = [afx.encode(w) for w in ws]
+    conts = [(_pinned(c) if i % 2 else torch.from_numpy(c).cuda()) for i, (c, _) in enumerate(enc)]
+    outs = [torch.empty(w.size, dtype=torch.int16, device="cuda") for w in ws]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    afx.afx_decode_batch([d for _, d in enc], conts, outs, status_dev=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    for w, o in zip(ws, outs):
+        assert np.array_equal(o.cpu().numpy().view(np.uint16), w)
+
+
+def test_corrupt_host_container_is_flagged(afx):
+    import torch
+    w = synth.normal(500_000, seed=70)
+    c, d = afx.encode(w)
+    bad = c.copy()
+    rng = np.random.default_rng(3)
+    bad[d.off_exp: d.off_exp + d.n_chunks * d.chunk_bytes] = rng.integers(
+        0, 256, size=d.n_chunks * d.chunk_bytes, dtype=np.uint8)
+    out = torch.empty(d.n, dtype=torch.int16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    afx.afx_decode(d, _pinned(bad), out, status_dev=status)
+    torch.cuda.synchronize()
+    assert status.item() != 0
+
+
+def test_gemv_refuses_a_host_container(afx):
+    import torch
+    rows, cols = 64, 5120
+    c, d = afx.encode(synth.normal(rows * cols, seed=71))
+    x = torch.zeros((1, cols), dtype=torch.int16, device="cuda")
+    y = torch.zeros((1, rows), dtype=torch.float32, device="cuda")
+    ws = torch.empty(afx.afx_decode_gemv_workspace(d, 1) // 4 + 4, dtype=torch.float32, device="cuda")
+    with pytest.raises((afx.AfxError, ValueError)):
+        afx.afx_decode_gemv(d, _pinned(c), rows, cols, x, y, ws)

@@ -154,6 +154,15 @@ def _dev_ptr(t) -> int:
     return t.data_ptr()
 
 
+def _buf_ptr(t) -> int:
+    """A CUDA tensor, or a pinned host tensor (read or written by the kernel over the host link)."""
+    if t.is_cuda:
+        return _dev_ptr(t)
+    if not t.is_pinned() or not t.is_contiguous():
+        raise ValueError("expected a contiguous CUDA tensor or a contiguous pinned host tensor")
+    return t.data_ptr()
+
+
 def _stream_handle(stream) -> int:
     if stream is None:
         import torch
@@ -198,7 +207,7 @@ def afx_decode(desc: afx_desc, container_dev, out_dev, stream=None, status_dev=N
     """out_dev: CUDA tensor of n 16-bit elements (uint16/int16/bfloat16)."""
     if out_dev.numel() < desc.n or out_dev.element_size() != 2:
         raise ValueError("out_dev must hold n 16-bit elements")
-    _check("afx_decode", _lib.afx_decode(ctypes.byref(desc), _dev_ptr(container_dev), _dev_ptr(out_dev),
+    _check("afx_decode", _lib.afx_decode(ctypes.byref(desc), _buf_ptr(container_dev), _buf_ptr(out_dev),
                                           _stream_handle(stream), _dev_ptr(status_dev)))
 
 
@@ -222,7 +231,9 @@ def afx_decode_batch(descs, containers_dev, outs_dev, stream=None, status_dev=No
         if o.numel() < d.n or o.element_size() != 2:
             raise ValueError("every output must hold n 16-bit elements")
     arr = (afx_desc * len(descs))(*descs)
-    _check("afx_decode_batch", _lib.afx_decode_batch(arr, _ptrs(containers_dev), _ptrs(outs_dev), len(descs),
+    bufs_in = (ctypes.c_void_p * len(containers_dev))(*[_buf_ptr(t) for t in containers_dev])
+    bufs_out = (ctypes.c_void_p * len(outs_dev))(*[_buf_ptr(t) for t in outs_dev])
+    _check("afx_decode_batch", _lib.afx_decode_batch(arr, bufs_in, bufs_out, len(descs),
                                                       _stream_handle(stream), _dev_ptr(status_dev)))
 
 

@@ -128,6 +128,8 @@ struct LaunchArgs {
     uint64_t total_subs;       // warp GEMV: sub-tiles of all tensors
     uint32_t wait_limit;       // polls of a staging wait before it gives up (0: kWaitLimit)
     uint32_t stall;            // failure injection for tests: arm the staging barriers, issue no copies
+    uint32_t host_src;         // restore: the containers are in pinned host memory (restore_store_host_kernel)
+    uint32_t pad;
     int32_t* status;
     TensorArgs t[kMaxTensors];
 };
@@ -1170,26 +1172,43 @@ __device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
     return v;
 }
 
+// Bytes staged for sub-tile s: the stream bytes of its 32 chunks plus the
+// pad, and its 40 chunk entries (the next sub-tile's first included).  A
+// full sub-tile (TensorArgs::n_sub_full) has all of them; the last ones take
+// what the sections hold.  Both are multiples of 16.
+__device__ __forceinline__ uint2 sub_tile_bytes(const TensorArgs& t, uint64_t s, bool full, uint32_t sub_bytes) {
+    if (full) return make_uint2(sub_bytes + kStreamPad, kWarpChunkStage * 2);
+    const uint64_t cb0 = s * kWarpChunks * 2;
+    const uint64_t csec = (t.n_chunks * 2 + 15) & ~uint64_t(15);
+    const uint64_t cavail = csec > cb0 ? csec - cb0 : 0;
+    return make_uint2(warp_stream_bytes(t, s),
+                      static_cast<uint32_t>(cavail < kWarpChunkStage * 2 ? cavail : kWarpChunkStage * 2));
+}
+
 // Stages sub-tile s in buffer b with two bulk copies on ws.bar[b], issued
-// by lane 0: the stream bytes of its 32 chunks plus the pad, and its 40
-// chunk entries (the next sub-tile's first included).  A full sub-tile
-// (TensorArgs::n_sub_full) has all of them; the last ones take what the
-// sections hold.  Every size and address is a multiple of 16.
+// by lane 0 (device-resident containers).  Every size and address is a
+// multiple of 16.
 __device__ __forceinline__ void warp_issue_bulk(WarpSlot& ws, uint8_t* stream_dst, const TensorArgs& t, uint64_t s,
                                                 bool full, const uint8_t* exp_src, const uint16_t* chunk_src,
                                                 uint32_t sub_bytes, int b, bool stall) {
-    uint32_t sbytes = sub_bytes + kStreamPad, cbytes = kWarpChunkStage * 2;
-    if (!full) {
-        sbytes = warp_stream_bytes(t, s);
-        const uint64_t cb0 = s * kWarpChunks * 2;
-        const uint64_t csec = (t.n_chunks * 2 + 15) & ~uint64_t(15);
-        const uint64_t cavail = csec > cb0 ? csec - cb0 : 0;
-        cbytes = static_cast<uint32_t>(cavail < kWarpChunkStage * 2 ? cavail : kWarpChunkStage * 2);
-    }
-    mbar_expect_tx(&ws.bar[b], sbytes + cbytes);
+    const uint2 nb = sub_tile_bytes(t, s, full, sub_bytes);
+    mbar_expect_tx(&ws.bar[b], nb.x + nb.y);
     if (stall) return;  // failure injection: the bytes never come
-    if (sbytes) bulk_copy_g2s(stream_dst, exp_src, sbytes, &ws.bar[b]);
-    if (cbytes) bulk_copy_g2s(ws.chunk[b], chunk_src, cbytes, &ws.bar[b]);
+    if (nb.x) bulk_copy_g2s(stream_dst, exp_src, nb.x, &ws.bar[b]);
+    if (nb.y) bulk_copy_g2s(ws.chunk[b], chunk_src, nb.y, &ws.bar[b]);
+}
+
+// The same staging from a container in pinned host memory, read over the
+// host link with plain 16-byte loads by all lanes (no bulk copies).
+__device__ __forceinline__ void warp_stage_host(WarpSlot& ws, uint8_t* stream_dst, const TensorArgs& t, uint64_t s,
+                                                bool full, const uint8_t* exp_src, const uint16_t* chunk_src,
+                                                uint32_t sub_bytes, int b, int lane) {
+    const uint2 nb = sub_tile_bytes(t, s, full, sub_bytes);
+    for (uint32_t i = lane * 16u; i < nb.x; i += 32 * 16u)
+        *reinterpret_cast<uint4*>(stream_dst + i) = *reinterpret_cast<const uint4*>(exp_src + i);
+    if (lane * 16u < nb.y)
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(ws.chunk[b]) + lane * 16) =
+            *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(chunk_src) + lane * 16);
 }
 
 // Joins and stores `count` weights from o0 with the 32 lanes of a warp; the
@@ -1325,7 +1344,7 @@ struct GemvEpilogue {
 // Restores sub-tiles [s0, s1) of tensor t with one warp.  phases holds the
 // parity each of the warp's two copy barriers waits for next.  Returns false
 // when a staging copy timed out (the run is abandoned and flagged).
-template <class Epi>
+template <bool host_src, class Epi>
 __device__ __forceinline__ bool warp_run(const TabView& tv, WarpSlot& ws, uint8_t* wstream, uint32_t wstride,
                                          const TensorArgs& t, uint64_t s0, uint64_t s1, int lane, int32_t* status,
                                          uint32_t wait_limit, bool stall, uint32_t& phases, const Epi& epi) {
@@ -1348,21 +1367,29 @@ __device__ __forceinline__ bool warp_run(const TabView& tv, WarpSlot& ws, uint8_
     // sources of the next sub-tile to stage
     const uint8_t* exp_src = reinterpret_cast<const uint8_t*>(t.exp_words) + s0 * sub_bytes;
     const uint16_t* chunk_src = t.chunk_index + s0 * kWarpChunks;
-    if (lane == 0) warp_issue_bulk(ws, wstream, t, s0, s0 < n_full, exp_src, chunk_src, sub_bytes, 0, stall);
+    if (!host_src && lane == 0) warp_issue_bulk(ws, wstream, t, s0, s0 < n_full, exp_src, chunk_src, sub_bytes, 0, stall);
     const uint32_t nrun = static_cast<uint32_t>(s1 - s0);
     uint32_t sub_in_block = static_cast<uint32_t>(s0 % kSubtilesPerBlock);
     int buf = 0;
     for (uint32_t r = 0; r < nrun; ++r) {
         const uint64_t s = s0 + r;
-        if (r + 1 < nrun) {
+        if constexpr (host_src) {  // the link is the bound: stage this sub-tile now, synchronously
+            warp_stage_host(ws, wstream + buf * wstride, t, s, s < n_full, exp_src, chunk_src, sub_bytes, buf, lane);
+            exp_src += sub_bytes;
+            chunk_src += kWarpChunks;
+            __syncwarp();
+        } else if (r + 1 < nrun) {
             exp_src += sub_bytes;
             chunk_src += kWarpChunks;
             if (lane == 0)
                 warp_issue_bulk(ws, wstream + (buf ^ 1) * wstride, t, s + 1, s + 1 < n_full, exp_src, chunk_src,
                                 sub_bytes, buf ^ 1, stall);
         }
-        const bool arrived = mbar_wait(&ws.bar[buf], (phases >> buf) & 1u, wait_limit);
-        phases ^= 1u << buf;
+        bool arrived = true;
+        if constexpr (!host_src) {
+            arrived = mbar_wait(&ws.bar[buf], (phases >> buf) & 1u, wait_limit);
+            phases ^= 1u << buf;
+        }
         if (!__all_sync(0xFFFFFFFFu, arrived)) {
             // give up on this run: flag it and let the copy still in flight land
             if (lane == 0) raise_status(status, AFX_DEV_TIMEOUT);
@@ -1403,7 +1430,7 @@ __device__ __forceinline__ bool warp_run(const TabView& tv, WarpSlot& ws, uint8_
         if (lane == 0) {
             if (!in_range)
                 raise_status(status, AFX_DEV_BAD_BLOCK);
-            else if (o0 < o1) {  // the sign|mantissa bytes are needed after the decode
+            else if (o0 < o1 && !host_src) {  // the sign|mantissa bytes are needed after the decode
                 const uint64_t a0 = o0 & ~uint64_t(15), a1 = (o1 + 15) & ~uint64_t(15);
                 prefetch_l2(sm + a0, static_cast<uint32_t>(a1 - a0));
             }
@@ -1459,7 +1486,8 @@ __device__ __forceinline__ bool warp_run(const TabView& tv, WarpSlot& ws, uint8_
 }
 
 // One CTA per SM (up to 32 warps) sharing one copy of the decode tables.
-template <class Epi>
+// host_src: the containers are in pinned host memory.
+template <bool host_src, class Epi>
 __device__ __forceinline__ void restore_warps(const LaunchArgs& a, const Epi& epi) {
     extern __shared__ __align__(16) uint8_t smem[];
     SharedW& sh = *reinterpret_cast<SharedW*>(smem);
@@ -1507,17 +1535,24 @@ __device__ __forceinline__ void restore_warps(const LaunchArgs& a, const Epi& ep
         const uint64_t span = se - sb;
         const uint64_t s0 = sb + span * warp / nwarps, s1 = sb + span * (warp + 1) / nwarps;
         if (alive && s0 < s1)
-            alive = warp_run(tv, ws, wstream, wstride, t, s0, s1, lane, a.status, wait_limit, a.stall != 0, phases, epi);
+            alive = warp_run<host_src>(tv, ws, wstream, wstride, t, s0, s1, lane, a.status, wait_limit, a.stall != 0,
+                                       phases, epi);
     }
 }
 
 __global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1) restore_store_kernel(const __grid_constant__ LaunchArgs a) {
-    restore_warps(a, StoreEpilogue{});
+    restore_warps<false>(a, StoreEpilogue{});
+}
+
+// The restore from containers in pinned host memory, read over the host link.
+__global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
+    restore_store_host_kernel(const __grid_constant__ LaunchArgs a) {
+    restore_warps<true>(a, StoreEpilogue{});
 }
 
 template <int B>
 __global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1) restore_gemv_kernel(const __grid_constant__ LaunchArgs a) {
-    restore_warps(a, GemvEpilogue<B>{});
+    restore_warps<false>(a, GemvEpilogue<B>{});
 }
 
 // Rows of the warp GEMV: the sub-tile in which a row starts adds its own
@@ -1840,11 +1875,15 @@ afx_status launch_restore(LaunchArgs& la, cudaStream_t s) {
         const afx_status st = warp_launch_config(la, &warps, &smem);
         if (st != AFX_OK) return st;
         int per_sm = 0;
-        const afx_status pst =
-            prepare_kernel(reinterpret_cast<const void*>(restore_store_kernel), warps * 32, smem, &per_sm);
+        const void* func = la.host_src ? reinterpret_cast<const void*>(restore_store_host_kernel)
+                                       : reinterpret_cast<const void*>(restore_store_kernel);
+        const afx_status pst = prepare_kernel(func, warps * 32, smem, &per_sm);
         if (pst != AFX_OK) return pst;
         const uint64_t grid = std::min<uint64_t>(la.total_tiles, static_cast<uint64_t>(sms) * per_sm);
-        restore_store_kernel<<<static_cast<unsigned>(grid), warps * 32, smem, s>>>(la);
+        if (la.host_src)
+            restore_store_host_kernel<<<static_cast<unsigned>(grid), warps * 32, smem, s>>>(la);
+        else
+            restore_store_kernel<<<static_cast<unsigned>(grid), warps * 32, smem, s>>>(la);
         AFX_CUDA_TRY(cudaGetLastError(), "restore_store_kernel launch");
         return AFX_OK;
     } else {
@@ -1863,6 +1902,24 @@ afx_status launch_restore(LaunchArgs& la, cudaStream_t s) {
         AFX_CUDA_TRY(cudaGetLastError(), "gemv_fixup_kernel launch");
         return AFX_OK;
     }
+}
+
+// Where a buffer lives.  Device memory is staged with bulk copies; pinned
+// (or managed) host memory is read with plain loads; pageable host memory
+// that the GPU cannot address is refused.
+enum class Where { device, host, unusable };
+
+Where where(const void* p) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return Where::unusable;
+    }
+    if (at.type == cudaMemoryTypeDevice) return Where::device;
+    // host memory the kernel can address with the same pointer
+    if ((at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeManaged) && at.devicePointer == p)
+        return Where::host;
+    return Where::unusable;
 }
 
 void reset_launch(LaunchArgs& la) {
@@ -1891,19 +1948,29 @@ afx_status decode_batch(const afx_desc* descs, const void* const* containers, ui
         if (st != AFX_OK) return afx_fail(st, "invalid container description", 0);
         if (d.n == 0) continue;
         if (!containers[i] || !outs[i] || !aligned(containers[i], 16) || !aligned(outs[i], 16))
-            return afx_fail(AFX_E_ARG, "container and output must be 16-byte aligned device pointers", 0);
+            return afx_fail(AFX_E_ARG, "container and output must be 16-byte aligned", 0);
         if (d.nsym >= 2 && d.block_chunks != static_cast<uint32_t>(kThreads))
             return afx_fail(AFX_E_ARG, "the decoder runs 512 chunks per block", 0);
     }
-    LaunchArgs la;
-    std::memset(&la, 0, sizeof la);
-    la.status = status;
-    la.wait_limit = stall_polls;
-    la.stall = stall_polls != 0;
+    LaunchArgs lists[2];  // device-resident containers, host-resident containers
+    for (int h = 0; h < 2; ++h) {
+        LaunchArgs& la = lists[h];
+        std::memset(&la, 0, sizeof la);
+        la.status = status;
+        la.wait_limit = stall_polls;
+        la.stall = stall_polls != 0;
+        la.host_src = static_cast<uint32_t>(h);
+    }
     for (uint32_t i = 0; i < count; ++i) {
         const afx_desc& d = descs[i];
         if (d.n == 0) continue;
         const uint8_t* base = static_cast<const uint8_t*>(containers[i]);
+        const Where wc = where(containers[i]), wo = where(outs[i]);
+        if (wc == Where::unusable || wo == Where::unusable)
+            return afx_fail(AFX_E_ARG, "container and output must be device memory or pinned host memory", 0);
+        if (stall_polls && wc != Where::device)
+            return afx_fail(AFX_E_ARG, "the stalled test restore needs a device-resident container", 0);
+        LaunchArgs& la = lists[wc == Where::host ? 1 : 0];
         if (d.nsym == 1) {
             const int sms = sm_count();
             if (sms <= 0) return afx_fail(AFX_E_CUDA, "cannot query the SM count", 0);
@@ -1926,7 +1993,9 @@ afx_status decode_batch(const afx_desc* descs, const void* const* containers, ui
         la.total_tiles += d.n_blocks;
         la.max_chunk_bytes = std::max(la.max_chunk_bytes, d.chunk_bytes);
     }
-    return launch_restore<0>(la, s);
+    const afx_status st = launch_restore<0>(lists[0], s);
+    if (st != AFX_OK) return st;
+    return launch_restore<0>(lists[1], s);
 }
 
 }  // namespace
@@ -2026,6 +2095,10 @@ extern "C" afx_status afx_decode_gemv_batch(const afx_desc* descs, const void* c
             return afx_fail(AFX_E_ARG, "rows * cols must equal n, with cols >= 64", 0);
         if (!aligned(containers[i], 16) || !aligned(xs[i], 16))
             return afx_fail(AFX_E_ARG, "container and x must be 16-byte aligned", 0);
+        if (where(containers[i]) != Where::device)
+            return afx_fail(AFX_E_ARG, "the fused GEMV needs a device-resident container", 0);
+        if (where(xs[i]) == Where::unusable || where(ys[i]) == Where::unusable)
+            return afx_fail(AFX_E_ARG, "x and y must be device memory or pinned host memory", 0);
         if (d.nsym >= 2) {
             if (d.block_chunks != static_cast<uint32_t>(kThreads))
                 return afx_fail(AFX_E_ARG, "the decoder runs 512 chunks per block", 0);
