@@ -438,6 +438,7 @@ def run_ours(args):
             line["eq2_break_even"] = {"S_bytes": S, "S_disk_bytes": S_disk, "b_link_gbs": b / 1e9,
                                       "read_time_saved_ms": (S - S_disk) / b * 1e3, "t_unpack_ms": ms,
                                       "pays": (S - S_disk) / b > ms * 1e-3}
+            line["residency_plan"] = run_residency_plan(afx, parts, b / 1e9, value)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -541,6 +542,30 @@ def run_zero_copy(afx, parts, dev, args):
                    "restore_store_host_kernel over the host link; to_host also writes the BF16 weights to "
                    "pinned host memory")
     return res
+
+
+def run_residency_plan(afx, parts, link_gbs, restore_gbs):
+    """afx_plan_residency for the whole Qwen3-14B-shaped model (40 layers
+    with this layer's container sizes, embedding and head at the matrices'
+    bits per weight) with the link and restore rates measured in this run,
+    at device budgets from the pages' 8 GB laptop GPU upwards."""
+    from weight_streaming_canonical_gb300 import synth
+    tensors = [(2 * d.n, d.container_bytes) for _ in range(synth.LAYERS) for _, _, _, d in parts]
+    mats = [d for name, _, _, d in parts if name == "gate_proj"]
+    bpw = mats[0].container_bytes / mats[0].n if mats else 1.37
+    for shape in (synth.EMBED_SHAPE, synth.HEAD_SHAPE):
+        n = synth.numel(shape)
+        tensors.append((2 * n, int(n * bpw)))
+    names = {afx.AFX_RESIDENT_DECODED: "resident_decoded", afx.AFX_RESIDENT_COMPRESSED: "resident_compressed",
+             afx.AFX_STREAM_COMPRESSED: "stream_compressed", afx.AFX_STREAM_RAW: "stream_raw"}
+    out = {"link_gbs": link_gbs, "restore_gbs": restore_gbs, "tensors": len(tensors),
+           "model_bf16_bytes": sum(S for S, _ in tensors), "model_compressed_bytes": sum(C for _, C in tensors),
+           "plans": []}
+    for gb in (8, 16, 24, 32):
+        place, ms, resident = afx.afx_plan_residency(tensors, gb * 10**9, link_gbs, restore_gbs, overlapped=True)
+        counts = {v: place.count(k) for k, v in names.items()}
+        out["plans"].append({"budget_gb": gb, "step_ms": ms, "resident_bytes": resident, **counts})
+    return out
 
 
 def _layer_ops(afx, parts, B, dev, keep):

@@ -291,6 +291,50 @@ afx_status afx_stream_run(const afx_layer* layers, uint32_t n_layers, void* cons
 afx_status afx_test_restore_stalled(const afx_desc* desc, const void* container_dev, uint16_t* out_dev,
                                     uint32_t wait_polls, afx_stream_t stream, int32_t* status_dev);
 
+/* ---- residency planning ------------------------------------------------
+ *
+ * Where each tensor of a model lives during inference on one GPU with a
+ * device-memory budget.  "Why Weight Offloading Slows Inference", section
+ * "Lossless compression: fewer bytes to read, more work to unpack", Eq. (1)
+ * (a step costs the reads plus t_unpack) and Eq. (2) (streaming compressed
+ * weights pays when (S - S_disk) / b > t_unpack); "Memory requirements of
+ * language model inference on a consumer GPU", section "Loading one part of
+ * the model at a time" (what does not fit is loaded as needed). */
+typedef enum afx_placement {
+    AFX_RESIDENT_DECODED = 0,    /* BF16 in device memory: S bytes, no per-step cost */
+    AFX_RESIDENT_COMPRESSED = 1, /* container in device memory: C bytes, restored each step */
+    AFX_STREAM_COMPRESSED = 2,   /* container copied over the link each step, then restored */
+    AFX_STREAM_RAW = 3           /* BF16 copied over the link each step */
+} afx_placement;
+
+typedef struct afx_plan_tensor {
+    uint64_t decoded_bytes;    /* S: 2 bytes per weight */
+    uint64_t compressed_bytes; /* C: the container */
+} afx_plan_tensor;
+
+typedef struct afx_plan_rates {
+    double link_gbs;      /* b: host-to-device copy rate, GB/s (1e9 bytes/s) */
+    double restore_gbs;   /* restore rate in decoded BF16 GB/s: t_unpack = S / restore_gbs */
+    uint32_t overlapped;  /* 1: a streamed tensor's copy overlaps the previous one's restore, costing
+                             max(C/b, t_unpack); 0: the two add, C/b + t_unpack (Eq. (2) as written) */
+    uint32_t reserved;
+} afx_plan_rates;
+
+/* Chooses a placement for each of n tensors that minimises the modelled
+ * per-step time (the sum of the tensors' costs) with the resident bytes at
+ * most device_budget_bytes.  Costs per step: resident decoded 0; resident
+ * compressed t_unpack; streamed compressed C/b + t_unpack (or the max when
+ * overlapped); streamed raw S/b.  Exact dynamic programming over memory in
+ * units of device_budget_bytes / 65536, every size rounded up to whole
+ * units (so the plan always fits; it may leave part of a unit unused).
+ * placement_out: n afx_placement values.  step_ms_out, resident_bytes_out:
+ * the plan's modelled time and exact resident bytes (either may be NULL).
+ * Host only.  Errors: AFX_E_ARG (null arrays, n == 0, rates not positive,
+ * n above 65536). */
+afx_status afx_plan_residency(const afx_plan_tensor* tensors, uint32_t n, uint64_t device_budget_bytes,
+                              const afx_plan_rates* rates, uint32_t* placement_out, double* step_ms_out,
+                              uint64_t* resident_bytes_out);
+
 /* Static text for a status code. */
 const char* afx_status_string(afx_status status);
 

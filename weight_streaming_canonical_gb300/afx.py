@@ -110,13 +110,27 @@ _lib.afx_decode_gemv_static.argtypes = [ctypes.POINTER(afx_desc), _vp, _u32, _u3
 _lib.afx_stream_run.argtypes = [ctypes.POINTER(afx_layer), _u32, ctypes.POINTER(ctypes.c_void_p), _u32, _u64, _vp,
                                 _vp, _vp, _i32p]
 _lib.afx_test_restore_stalled.argtypes = [ctypes.POINTER(afx_desc), _vp, _vp, _u32, _vp, _i32p]
+class afx_plan_tensor(ctypes.Structure):
+    _fields_ = [("decoded_bytes", ctypes.c_uint64), ("compressed_bytes", ctypes.c_uint64)]
+
+
+class afx_plan_rates(ctypes.Structure):
+    _fields_ = [("link_gbs", ctypes.c_double), ("restore_gbs", ctypes.c_double), ("overlapped", ctypes.c_uint32),
+                ("reserved", ctypes.c_uint32)]
+
+
+AFX_RESIDENT_DECODED, AFX_RESIDENT_COMPRESSED, AFX_STREAM_COMPRESSED, AFX_STREAM_RAW = 0, 1, 2, 3
+_lib.afx_plan_residency.argtypes = [ctypes.POINTER(afx_plan_tensor), _u32, _u64, ctypes.POINTER(afx_plan_rates),
+                                    ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_double),
+                                    ctypes.POINTER(ctypes.c_uint64)]
 _lib.afx_last_error.argtypes = []
 _lib.afx_last_error.restype = ctypes.c_char_p
 _lib.afx_status_string.argtypes = [ctypes.c_int]
 _lib.afx_status_string.restype = ctypes.c_char_p
 for _f in (_lib.afx_build_code, _lib.afx_encode_bound, _lib.afx_encode, _lib.afx_parse_header, _lib.afx_decode,
            _lib.afx_decode_batch, _lib.afx_decode_gemv_workspace, _lib.afx_decode_gemv, _lib.afx_decode_gemv_batch,
-           _lib.afx_decode_gemv_static, _lib.afx_stream_run, _lib.afx_test_restore_stalled):
+           _lib.afx_decode_gemv_static, _lib.afx_stream_run, _lib.afx_test_restore_stalled,
+           _lib.afx_plan_residency):
     _f.restype = ctypes.c_int
 
 
@@ -300,6 +314,19 @@ def afx_stream_run(layers, dev_bufs, buf_bytes: int, compute_stream=None, copy_s
                                                   _stream_handle(compute_stream), _stream_handle(copy_stream),
                                                   _stream_handle(d2h_stream) if d2h_stream is not None else None,
                                                   _dev_ptr(status_dev)))
+
+
+def afx_plan_residency(tensors, device_budget_bytes: int, link_gbs: float, restore_gbs: float,
+                       overlapped: bool = True) -> tuple[list[int], float, int]:
+    """tensors: [(decoded_bytes, compressed_bytes)].  Returns (placements, step_ms, resident_bytes)."""
+    n = len(tensors)
+    arr = (afx_plan_tensor * max(n, 1))(*[afx_plan_tensor(int(S), int(C)) for S, C in tensors])
+    rates = afx_plan_rates(float(link_gbs), float(restore_gbs), 1 if overlapped else 0, 0)
+    out = (ctypes.c_uint32 * max(n, 1))()
+    ms, res = ctypes.c_double(), ctypes.c_uint64()
+    _check("afx_plan_residency", _lib.afx_plan_residency(arr, n, int(device_budget_bytes), ctypes.byref(rates), out,
+                                                          ctypes.byref(ms), ctypes.byref(res)))
+    return [int(v) for v in out[:n]], ms.value, res.value
 
 
 # ---- conveniences over the entry points ---------------------------------------
