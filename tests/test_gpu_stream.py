@@ -117,3 +117,61 @@ def test_blob_larger_than_buffer_is_rejected(afx):
     bufs = [torch.empty(256, dtype=torch.uint8, device="cuda") for _ in range(2)]
     with pytest.raises(afx.AfxError):
         afx.afx_stream_run([(blob, ops)], bufs, 256)
+
+
+def _bf16_to_f64(a: np.ndarray) -> np.ndarray:
+    return (a.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("B", [1, 4])
+def test_forty_streamed_full_size_layers_sampled_rows(afx, B):
+    # the bench's streaming configuration: two distinct Qwen3-14B-shaped
+    # layers in pinned host memory alternate over 40 streamed layers, norms
+    # restored and the seven matrices through the fused GEMV; every layer's
+    # norms are checked bit for bit and 16 sampled rows of every product
+    # against float64 dot products of the original weights
+    import torch
+    import bench
+    blobs = []
+    for seed in (0, 1):
+        parts = bench.build_layer(seed)
+        size = sum(c.size for _, _, c, _ in parts)
+        blob = torch.empty(size, dtype=torch.uint8).pin_memory()
+        o = 0
+        for _, _, c, _ in parts:
+            blob.numpy()[o:o + c.size] = c
+            o += c.size
+        blobs.append((blob, parts))
+    keep, layers, outs = [], [], []
+    for l in range(40):
+        blob, parts = blobs[l % 2]
+        first = len(keep)
+        ops = bench._layer_ops(afx, parts, B, torch.device("cuda"), keep)
+        layers.append((blob, ops))
+        outs.append(keep[first:])
+    buf_bytes = max(b.numel() for b, _ in blobs)
+    bufs = [torch.empty(buf_bytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    afx.afx_stream_run(layers, bufs, buf_bytes, torch.cuda.current_stream(), torch.cuda.Stream(), status_dev=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    shapes = {name: shape for name, shape, _ in synth.LAYER_TENSORS}
+    rng = np.random.default_rng(B)
+    for l in range(40):
+        _, parts = blobs[l % 2]
+        it = iter(outs[l])
+        for name, w, _, _ in parts:
+            if len(shapes[name]) == 1:  # a norm vector, restored
+                assert np.array_equal(next(it).cpu().numpy().view(np.uint16), w.reshape(-1))
+                continue
+            x_t, y_t, _ = next(it), next(it), next(it)
+            rows, cols = shapes[name]
+            x = _bf16_to_f64(x_t.cpu().numpy().view(np.uint16).reshape(B, cols))
+            y = y_t.cpu().numpy()
+            pick = rng.choice(rows, size=16, replace=False)
+            W = _bf16_to_f64(w.reshape(rows, cols)[pick])
+            ref = W @ x.T  # [16][B]
+            A = np.abs(W) @ np.abs(x).T
+            err = np.abs(y[:, pick].T.astype(np.float64) - ref)
+            assert np.all(err <= 2e-3 * A + np.abs(ref) * 2.0 ** -23), (l, name)
