@@ -143,6 +143,19 @@ def workload_text(workload: str) -> str:
     return WORKLOADS[workload]
 
 
+def exponent_entropy_bits(parts) -> float:
+    """Empirical entropy of the BF16 exponents per weight, weighted over the
+    tensors (each tensor has its own code): the least any exponent code can
+    spend, before the chunk and block index."""
+    total, n_all = 0.0, 0
+    for _, w, _, _ in parts:
+        counts = np.bincount(((w.reshape(-1) >> 7) & 0xFF).astype(np.intp), minlength=256).astype(np.float64)
+        p = counts[counts > 0] / w.size
+        total += float(-(p * np.log2(p)).sum()) * w.size
+        n_all += w.size
+    return total / max(n_all, 1)
+
+
 def algorithmic_bytes(d) -> int:
     """Bytes a restore must move: coded exponent bits, sign|mantissa bytes,
     chunk and block index entries read; 2 bytes per weight written."""
@@ -411,6 +424,8 @@ def run_ours(args):
         "data": "synthetic: seeded N(0,0.02) BF16 matrices, N(1,0.05) norms, Qwen3-14B layer shapes",
         "config": {"workload": workload_text(args.workload), "weights": n_total, "compressed_bytes": comp_total,
                    "bits_per_weight": 8 * comp_total / n_total,
+                   "coded_exponent_bits_per_weight": sum(d.total_bits for *_, d in parts) / n_total,
+                   "exponent_entropy_bits_per_weight": exponent_entropy_bits(parts),
                    "l2": "inputs larger than L2: %.0f MB compressed read and %.0f MB written per step"
                          % (comp_total / 1e6, 2 * n_total / 1e6),
                    "launch": f"one afx_decode_batch call of {len(views)} tensors ({launches_per_step} kernel launches) "
@@ -419,6 +434,7 @@ def run_ours(args):
         "weights_per_s": weights_per_s,
         "hbm_gbs": alg_total * world / sec / 1e9,
         "hbm_frac": alg_total / sec / 1e9 / peak,
+        "hbm_frac_of_nominal_7900_gbs": alg_total / sec / 1e9 / 7900.0,
         "roofline": roofline,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,

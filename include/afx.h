@@ -335,6 +335,17 @@ afx_status afx_plan_residency(const afx_plan_tensor* tensors, uint32_t n, uint64
                               const afx_plan_rates* rates, uint32_t* placement_out, double* step_ms_out,
                               uint64_t* resident_bytes_out);
 
+/* Bounds report of the restore kernels since the last call (the report is
+ * cleared).  In a library built with AFX_DEBUG_BOUNDS=1 (the build's
+ * --debug-bounds variant, libafx_debug.so) every range the restore path is
+ * about to read or write is checked against its buffer first -- the warp's
+ * exponent stage, the stream buffer, the state table, the output -- and a
+ * failed check sets one bit of *bits (see BoundsCheck in the kernel
+ * source); *checked is 1 in such a build and 0 in a regular one, whose
+ * report stays 0.  A stand-in for a memory checker; no counterpart on the
+ * pages.  Synchronises the device.  Errors: AFX_E_ARG, AFX_E_CUDA. */
+afx_status afx_debug_bounds_report(uint32_t* bits, uint32_t* checked);
+
 /* Static text for a status code. */
 const char* afx_status_string(afx_status status);
 

@@ -1,0 +1,95 @@
+"""The bounds-checked build (AFX_DEBUG_BOUNDS=1, libafx_debug.so) on the
+restore path: across ragged sizes, the 12-bit-table path, long codes, host
+containers, the fused GEMV and corrupt containers, no range a kernel
+touches ever leaves its buffer.  The check runs in a child process that
+loads the debug library; compute-sanitizer is not available here."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+CHILD = r"""
+import json, sys
+import numpy as np, torch
+from weight_streaming_canonical_gb300 import build
+build.build(debug_bounds=True)
+from weight_streaming_canonical_gb300 import afx, synth
+assert afx.DEBUG_BOUNDS
+statuses = []
+
+def restore(c, d, host=False):
+    cont = torch.from_numpy(c).cuda() if not host else torch.from_numpy(c).pin_memory()
+    out = torch.empty(max(d.n, 1), dtype=torch.int16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    afx.afx_decode(d, cont, out[:d.n] if d.n else out, status_dev=st)
+    torch.cuda.synchronize()
+    return out[:d.n].cpu().numpy().view(np.uint16), int(st.item())
+
+for n in (1, 1000, 65_537, 3_000_017):
+    w = synth.normal(n, seed=n)
+    got, st = restore(*afx.encode(w))
+    statuses.append(("normal", n, st, bool(np.array_equal(got, w))))
+w = synth.adversarial(1 << 20, seed=2)
+got, st = restore(*afx.encode(w))
+statuses.append(("adversarial", w.size, st, bool(np.array_equal(got, w))))
+w = synth.all_bf16_patterns()
+for T in (4, 32):
+    got, st = restore(*afx.encode(w, chunk_bytes=T))
+    statuses.append(("patterns", T, st, bool(np.array_equal(got, w))))
+w = synth.normal(500_000, seed=5)
+got, st = restore(*afx.encode(w), host=True)
+statuses.append(("host", w.size, st, bool(np.array_equal(got, w))))
+# corrupt containers: must be flagged, never read or write out of range
+rng = np.random.default_rng(9)
+w = synth.normal(400_000, seed=6)
+c, d = afx.encode(w)
+bad = c.copy()
+bad[d.off_exp: d.off_exp + d.n_chunks * d.chunk_bytes] = rng.integers(0, 256, size=d.n_chunks * d.chunk_bytes,
+                                                                        dtype=np.uint8)
+statuses.append(("garbage stream", 0, restore(bad, d)[1], None))
+bad = c.copy()
+idx = d.off_chunk + 2 * rng.integers(0, d.n_chunks, size=64)
+bad[idx] ^= np.uint8(0xA5)
+statuses.append(("chunk index", 0, restore(bad, d)[1], None))
+bad = c.copy()
+bad[d.off_block + 8: d.off_block + 16] = 0xFF
+statuses.append(("block index", 0, restore(bad, d)[1], None))
+# the fused GEMV on the warp path
+rows, cols = 96, 5120
+W = synth.normal(rows * cols, seed=7)
+c, d = afx.encode(W)
+x = torch.from_numpy(synth.activations(2, cols, seed=1).view(np.int16)).cuda()
+y = torch.empty((2, rows), dtype=torch.float32, device="cuda")
+ws = torch.empty(afx.afx_decode_gemv_workspace(d, 2) // 4 + 4, dtype=torch.float32, device="cuda")
+st = torch.zeros(1, dtype=torch.int32, device="cuda")
+afx.afx_decode_gemv(d, torch.from_numpy(c).cuda(), rows, cols, x, y, ws, status_dev=st)
+torch.cuda.synchronize()
+statuses.append(("gemv", rows * cols, int(st.item()), None))
+bits, checked = afx.afx_debug_bounds_report()
+print(json.dumps({"bits": bits, "checked": checked, "cases": statuses}))
+"""
+
+
+def test_bounds_checked_build_reports_no_violation():
+    env = dict(os.environ, AFX_DEBUG_BOUNDS="1")
+    r = subprocess.run([sys.executable, "-c", CHILD], cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-3000:]
+    rep = json.loads(r.stdout.strip().splitlines()[-1])
+    assert rep["checked"]
+    for kind, size, status, exact in rep["cases"]:
+        if kind in ("garbage stream", "chunk index", "block index"):
+            assert status != 0, kind
+        else:
+            assert status == 0 and exact in (True, None), (kind, size)
+    assert rep["bits"] == 0, f"bounds checks failed: {rep['bits']:#x}"
+
+
+def test_regular_build_reports_nothing(afx):
+    bits, checked = afx.afx_debug_bounds_report()
+    assert bits == 0 and not checked

@@ -14,11 +14,15 @@ import os
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libafx.so")
+# AFX_DEBUG_BOUNDS=1 in the environment loads the bounds-checked build
+# (`python -m weight_streaming_canonical_gb300.build --debug-bounds`)
+DEBUG_BOUNDS = os.environ.get("AFX_DEBUG_BOUNDS", "0") == "1"
+LIB_PATH = (os.path.join(_HERE, "_build_debug", "libafx_debug.so") if DEBUG_BOUNDS
+            else os.path.join(_HERE, "_build", "libafx.so"))
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
-        f"libafx.so is not built ({LIB_PATH} missing); run "
+        f"{os.path.basename(LIB_PATH)} is not built ({LIB_PATH} missing); run "
         "`python -m weight_streaming_canonical_gb300.build` (needs nvcc)")
 
 _lib = ctypes.CDLL(LIB_PATH)
@@ -123,6 +127,7 @@ AFX_RESIDENT_DECODED, AFX_RESIDENT_COMPRESSED, AFX_STREAM_COMPRESSED, AFX_STREAM
 _lib.afx_plan_residency.argtypes = [ctypes.POINTER(afx_plan_tensor), _u32, _u64, ctypes.POINTER(afx_plan_rates),
                                     ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_double),
                                     ctypes.POINTER(ctypes.c_uint64)]
+_lib.afx_debug_bounds_report.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint32)]
 _lib.afx_last_error.argtypes = []
 _lib.afx_last_error.restype = ctypes.c_char_p
 _lib.afx_status_string.argtypes = [ctypes.c_int]
@@ -130,7 +135,7 @@ _lib.afx_status_string.restype = ctypes.c_char_p
 for _f in (_lib.afx_build_code, _lib.afx_encode_bound, _lib.afx_encode, _lib.afx_parse_header, _lib.afx_decode,
            _lib.afx_decode_batch, _lib.afx_decode_gemv_workspace, _lib.afx_decode_gemv, _lib.afx_decode_gemv_batch,
            _lib.afx_decode_gemv_static, _lib.afx_stream_run, _lib.afx_test_restore_stalled,
-           _lib.afx_plan_residency):
+           _lib.afx_plan_residency, _lib.afx_debug_bounds_report):
     _f.restype = ctypes.c_int
 
 
@@ -327,6 +332,13 @@ def afx_plan_residency(tensors, device_budget_bytes: int, link_gbs: float, resto
     _check("afx_plan_residency", _lib.afx_plan_residency(arr, n, int(device_budget_bytes), ctypes.byref(rates), out,
                                                           ctypes.byref(ms), ctypes.byref(res)))
     return [int(v) for v in out[:n]], ms.value, res.value
+
+
+def afx_debug_bounds_report() -> tuple[int, bool]:
+    """(bits of the failed bounds checks since the last call, whether this build checks)."""
+    bits, checked = ctypes.c_uint32(), ctypes.c_uint32()
+    _check("afx_debug_bounds_report", _lib.afx_debug_bounds_report(ctypes.byref(bits), ctypes.byref(checked)))
+    return bits.value, bool(checked.value)
 
 
 # ---- conveniences over the entry points ---------------------------------------

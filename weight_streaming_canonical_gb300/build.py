@@ -16,6 +16,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libafx.so")
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(BUILD_DEBUG, "libafx_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O3,-pthread", "--expt-relaxed-constexpr"]
@@ -44,8 +46,12 @@ def _stale(out: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, debug_bounds: bool = False) -> str:
+    """Builds libafx.so; debug_bounds builds libafx_debug.so instead, with
+    every buffer bound checked in the kernels (AFX_DEBUG_BOUNDS=1)."""
+    build_dir = BUILD_DEBUG if debug_bounds else BUILD
+    lib = LIB_DEBUG if debug_bounds else LIB
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".h")]
     headers.append(os.path.join(os.path.dirname(HERE), "include", "afx.h"))
@@ -53,15 +59,16 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     objs = []
     jobs = []
     for src in srcs:
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + headers):
+            defs = ["-DAFX_DEBUG_BOUNDS=1"] if debug_bounds else []
             if src.endswith(".cu"):
-                cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+                cmd = [nvcc, *ARCH, *NVCC_FLAGS, *defs, "-c", src, "-o", obj]
                 if ptxas_info:
                     cmd.insert(1, "-Xptxas=-v")
             else:
-                cmd = ["g++", *CXX_FLAGS, "-I", _cuda_include(nvcc), "-c", src, "-o", obj]
+                cmd = ["g++", *CXX_FLAGS, *defs, "-I", _cuda_include(nvcc), "-c", src, "-o", obj]
             jobs.append(cmd)
 
     def run(cmd):
@@ -75,13 +82,14 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     with cf.ThreadPoolExecutor(max(1, len(jobs))) as ex:
         list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-Xcompiler", "-pthread"])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    path = build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas-info" in sys.argv)
+    path = build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas-info" in sys.argv,
+                 debug_bounds="--debug-bounds" in sys.argv)
     print(path)

@@ -158,6 +158,32 @@ __device__ __forceinline__ void raise_status(int32_t* status, int32_t bits) {
     if (status) atomicOr(status, bits);
 }
 
+// Bounds-checked builds.  Compute-sanitizer is not available, so a build
+// with AFX_DEBUG_BOUNDS=1 checks, on the restore path, every range a kernel
+// is about to read or write against its buffer (stage, stream buffer,
+// decode tables, output); a failed check ORs its bit into g_bounds_report,
+// which afx_debug_bounds_report reads.  In regular builds the checks
+// compile to nothing.
+#ifndef AFX_DEBUG_BOUNDS
+#define AFX_DEBUG_BOUNDS 0
+#endif
+__device__ unsigned int g_bounds_report;
+enum BoundsCheck : unsigned {
+    kChkTableState = 0,   // a byte step's state offset inside the state table
+    kChkStageSteps,       // the byte steps' stage words inside the warp's stage
+    kChkStreamWords,      // a chunk's words inside the stream buffer
+    kChkStagePending,     // pending bytes inside the stage
+    kChkStageRun,         // a 12-bit-table or partial-chunk run inside the stage
+    kChkMergeStage,       // the merged range inside the stage
+    kChkMergeOutput,      // the merged range inside the output
+    kChkStagingBytes,     // staged bytes inside the stream buffer and chunk rows
+    kChkTableBuild,       // a built entry's next state inside the table
+};
+#define AFX_CHECK(cond, bit)                                                      \
+    do {                                                                          \
+        if (AFX_DEBUG_BOUNDS && !(cond)) atomicOr(&g_bounds_report, 1u << (bit)); \
+    } while (0)
+
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
     const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(dst));
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(src) : "memory");
@@ -872,6 +898,7 @@ struct TabView {
     const uint16_t* first;
     const char* fsm;
     const uint8_t* depth;
+    uint32_t fsm_bytes;  // size of the state table (bounds-checked builds)
 };
 
 // One code from a 32-bit window through the first-code table (exact
@@ -951,6 +978,7 @@ __device__ void build_tables_w(SharedW& sh, uint8_t* tabr, const CodeTables& tab
             const uint32_t q = r ? (V << pos) >> (32 - r) : 0u;
             const uint32_t lo_r = r ? sh.limit[r] >> (24 - r) : 0u;
             const uint32_t next = sh.state_base[r] + q - lo_r;
+            AFX_CHECK(next < nodes, kChkTableBuild);
             fsm[(h ? nodes + h - 1 : 0u) * 256u + b] = make_uint2(out, (next * kFsmRowBytes) | ((cnt * 8u) << 26));
         }
         __syncthreads();
@@ -968,6 +996,7 @@ __device__ void build_tables_w(SharedW& sh, uint8_t* tabr, const CodeTables& tab
             if (h > 8) {  // still inside the code: the node of its first d + 8 bits
                 const uint32_t d8 = d + 8;
                 const uint32_t next = sh.state_base[d8] + ((p << 8) | b) - (sh.limit[d8] >> (24 - d8));
+                AFX_CHECK(next < nodes, kChkTableBuild);
                 e = make_uint2(0u, next * kFsmRowBytes);
             } else if (h == 8) {
                 e = make_uint2(sym, 8u << 26);
@@ -1016,6 +1045,13 @@ __device__ __forceinline__ void fsm_step(const char* fsm, uint32_t& st, uint32_t
     const uint2 e = *reinterpret_cast<const uint2*>(fsm + st + (b << 3));
     append(e.x, e.y >> 26, acc, fill, wout);
     st = e.y & 0x3FFFFFFu;
+}
+
+// The same step with the state offset checked in bounds-checked builds.
+__device__ __forceinline__ void fsm_step_checked(const TabView& tv, uint32_t& st, uint32_t b, uint32_t& acc,
+                                                 uint32_t& fill, uint32_t*& wout) {
+    AFX_CHECK(st + (b << 3) + 8 <= tv.fsm_bytes, kChkTableState);
+    fsm_step(tv.fsm, st, b, acc, fill, wout);
 }
 
 // Byte-step counterpart of decode_run (same contract).  stream_end is the
@@ -1111,17 +1147,18 @@ __device__ __forceinline__ void fsm_chunk_steps(const TabView& tv, const uint32_
     const uint32_t h = gap & 7u;
     uint32_t st = h ? skip_row0 + (h - 1) * kFsmRowBytes : 0u;
     const uint32_t X0 = words[0];
-    if (gap < 8) fsm_step(tv.fsm, st, X0 >> 24, acc, fill, wout);
-    if (gap < 16) fsm_step(tv.fsm, st, __byte_perm(X0, 0u, 0x4442), acc, fill, wout);
-    fsm_step(tv.fsm, st, __byte_perm(X0, 0u, 0x4441), acc, fill, wout);
-    fsm_step(tv.fsm, st, X0 & 0xFFu, acc, fill, wout);
+    if (gap < 8) fsm_step_checked(tv, st, X0 >> 24, acc, fill, wout);
+    if (gap < 16) fsm_step_checked(tv, st, __byte_perm(X0, 0u, 0x4442), acc, fill, wout);
+    fsm_step_checked(tv, st, __byte_perm(X0, 0u, 0x4441), acc, fill, wout);
+    fsm_step_checked(tv, st, X0 & 0xFFu, acc, fill, wout);
     for (uint32_t w = 1; w < nwords; ++w) {
         const uint32_t X = words[w];
-        fsm_step(tv.fsm, st, X >> 24, acc, fill, wout);
-        fsm_step(tv.fsm, st, __byte_perm(X, 0u, 0x4442), acc, fill, wout);
-        fsm_step(tv.fsm, st, __byte_perm(X, 0u, 0x4441), acc, fill, wout);
-        fsm_step(tv.fsm, st, X & 0xFFu, acc, fill, wout);
+        fsm_step_checked(tv, st, X >> 24, acc, fill, wout);
+        fsm_step_checked(tv, st, __byte_perm(X, 0u, 0x4442), acc, fill, wout);
+        fsm_step_checked(tv, st, __byte_perm(X, 0u, 0x4441), acc, fill, wout);
+        fsm_step_checked(tv, st, X & 0xFFu, acc, fill, wout);
     }
+    AFX_CHECK(reinterpret_cast<uint8_t*>(wout) <= stage + kWarpStage, kChkStageSteps);
     fl.wout = wout;
     fl.acc = acc;
     fl.fill = fill;
@@ -1192,6 +1229,7 @@ __device__ __forceinline__ void warp_issue_bulk(WarpSlot& ws, uint8_t* stream_ds
                                                 bool full, const uint8_t* exp_src, const uint16_t* chunk_src,
                                                 uint32_t sub_bytes, int b, bool stall) {
     const uint2 nb = sub_tile_bytes(t, s, full, sub_bytes);
+    AFX_CHECK(nb.x <= sub_bytes + kStreamPad && nb.y <= kWarpChunkStage * 2, kChkStagingBytes);
     mbar_expect_tx(&ws.bar[b], nb.x + nb.y);
     if (stall) return;  // failure injection: the bytes never come
     if (nb.x) bulk_copy_g2s(stream_dst, exp_src, nb.x, &ws.bar[b]);
@@ -1204,6 +1242,7 @@ __device__ __forceinline__ void warp_stage_host(WarpSlot& ws, uint8_t* stream_ds
                                                 bool full, const uint8_t* exp_src, const uint16_t* chunk_src,
                                                 uint32_t sub_bytes, int b, int lane) {
     const uint2 nb = sub_tile_bytes(t, s, full, sub_bytes);
+    AFX_CHECK(nb.x <= sub_bytes + kStreamPad && nb.y <= kWarpChunkStage * 2, kChkStagingBytes);
     for (uint32_t i = lane * 16u; i < nb.x; i += 32 * 16u)
         *reinterpret_cast<uint4*>(stream_dst + i) = *reinterpret_cast<const uint4*>(exp_src + i);
     if (lane * 16u < nb.y)
@@ -1449,23 +1488,33 @@ __device__ __forceinline__ bool warp_run(const TabView& tv, WarpSlot& ws, uint8_
                     const uint64_t left = t.total_bits > bit0 ? t.total_bits - bit0 : 0;
                     stream_end = left < sub_bits ? static_cast<uint32_t>(left) : sub_bits;
                 }
+                AFX_CHECK((lane + 1) * (T >> 2) <= wstride >> 2, kChkStreamWords);
                 if (chunk_end <= stream_end) {
                     fsm_chunk_steps(tv, stream + lane * (T >> 2), T >> 2, gap, skip_row0, ws.stage, s_run, fl);
                     stepped = true;
                 } else {  // the stream's partial last chunk
+                    AFX_CHECK(s_run + cnt <= static_cast<uint32_t>(kWarpStage), kChkStageRun);
                     bad = decode_run_fsm(tv, stream, lane * (T >> 2), gap, cnt, ws.stage, s_run, next, chunk_end,
                                          stream_end);
                 }
             } else {
+                AFX_CHECK(s_run + cnt <= static_cast<uint32_t>(kWarpStage), kChkStageRun);
                 bad = decode_run(tv, stream, warp_stream_bytes(t, s) >> 2, lane * (T >> 2), gap, cnt, ws.stage, s_run,
                                  next, chunk_end);
             }
         }
         __syncwarp();
-        if (stepped) bad = fsm_chunk_finish(tv, stream, fl, cnt, chunk_end, next);
+        if (stepped) {
+            AFX_CHECK(reinterpret_cast<uint8_t*>(fl.wout) + 4 <= ws.stage + kWarpStage, kChkStagePending);
+            bad = fsm_chunk_finish(tv, stream, fl, cnt, chunk_end, next);
+        }
         if (bad) raise_status(status, AFX_DEV_BAD_CHUNK);
         const bool any_bad = __any_sync(0xFFFFFFFFu, bad);
         __syncwarp();
+        if (!any_bad && in_range) {
+            AFX_CHECK((o0 & 7u) + total <= static_cast<uint64_t>(kWarpStage), kChkMergeStage);
+            AFX_CHECK(o0 + total <= n, kChkMergeOutput);
+        }
         epi(ws.stage, t, s, o0, total, !any_bad && in_range, lane);
         start = o1;
         buf ^= 1;
@@ -1508,6 +1557,7 @@ __device__ __forceinline__ void restore_warps(const LaunchArgs& a, const Epi& ep
     tv.first = sh.first;
     tv.fsm = reinterpret_cast<const char*>(tabr);
     tv.depth = sh.depth;
+    tv.fsm_bytes = a.tab_bytes;
 
     const uint64_t g_begin = a.total_tiles * blockIdx.x / gridDim.x;
     const uint64_t g_end = a.total_tiles * (blockIdx.x + 1) / gridDim.x;
@@ -2012,6 +2062,17 @@ extern "C" afx_status afx_test_restore_stalled(const afx_desc* desc, const void*
     if (!container || !out || !status) return afx_fail(AFX_E_ARG, "null pointer", 0);
     if (wait_polls == 0 || wait_polls > kWaitLimit) return afx_fail(AFX_E_ARG, "wait_polls must be 1..2^22", 0);
     return decode_batch(desc, &container, &out, 1, stream, status, wait_polls);
+}
+
+extern "C" afx_status afx_debug_bounds_report(uint32_t* bits, uint32_t* checked) {
+    if (!bits) return afx_fail(AFX_E_ARG, "null pointer", 0);
+    unsigned int v = 0;
+    AFX_CUDA_TRY(cudaMemcpyFromSymbol(&v, g_bounds_report, sizeof v), "cudaMemcpyFromSymbol");
+    const unsigned int zero = 0;
+    AFX_CUDA_TRY(cudaMemcpyToSymbol(g_bounds_report, &zero, sizeof zero), "cudaMemcpyToSymbol");
+    *bits = v;
+    if (checked) *checked = AFX_DEBUG_BOUNDS ? 1u : 0u;
+    return AFX_OK;
 }
 
 extern "C" afx_status afx_decode(const afx_desc* desc, const void* container, uint16_t* out, afx_stream_t stream,

@@ -16,7 +16,9 @@
 // stream after their layer's ops, so that with a full-duplex link the copy
 // back overlaps the next layer's load.  The host never waits.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
+#include <cstdio>
 #include <vector>
 
 #include "afx_internal.h"
@@ -65,6 +67,14 @@ afx_status check_layer(const afx_layer& L, uint64_t buf_bytes) {
     }
     return AFX_OK;
 }
+
+// An NVTX range for as long as the object lives (a profiler's timeline shows
+// where each layer's copy and ops were enqueued; without a tool attached the
+// calls do nothing).
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
 
 // Runs ops[0..count), all of one kind (and one batch size), as one batch call.
 afx_status run_group(const afx_op* ops, uint32_t count, uint8_t* buf, afx_stream_t stream, int32_t* status_dev) {
@@ -119,9 +129,13 @@ extern "C" afx_status afx_stream_run(const afx_layer* layers, uint32_t n_layers,
     AFX_STREAM_TRY(cudaEventRecord(entry.ev[0], compute), "cudaEventRecord");
     AFX_STREAM_TRY(cudaStreamWaitEvent(copy, entry.ev[0], 0), "cudaStreamWaitEvent");
 
+    NvtxRange run_range("afx_stream_run");
     for (uint32_t l = 0; l < n_layers; ++l) {
         const afx_layer& L = layers[l];
         const uint32_t k = l % n_bufs;
+        char name[48];
+        snprintf(name, sizeof name, "afx layer %u: copy and ops", l);
+        NvtxRange layer_range(name);
         uint8_t* buf = static_cast<uint8_t*>(dev_bufs[k]);
         if (l >= n_bufs) AFX_STREAM_TRY(cudaStreamWaitEvent(copy, consumed.ev[k], 0), "cudaStreamWaitEvent");
         if (L.blob_bytes)
