@@ -455,6 +455,7 @@ def run_ours(args):
                                       "read_time_saved_ms": (S - S_disk) / b * 1e3, "t_unpack_ms": ms,
                                       "pays": (S - S_disk) / b > ms * 1e-3}
             line["residency_plan"] = run_residency_plan(afx, parts, b / 1e9, value)
+            line["prefill"] = run_prefill_bench(afx, parts, dev_blob, offs, dev, args)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -558,6 +559,84 @@ def run_zero_copy(afx, parts, dev, args):
                    "restore_store_host_kernel over the host link; to_host also writes the BF16 weights to "
                    "pinned host memory")
     return res
+
+
+def run_prefill_bench(afx, parts, dev_blob, offs, dev, args):
+    """The layer's seven matrices times N token vectors (prefill), containers
+    resident in HBM: restore then tensor-core product per matrix on one
+    stream, the same with restores overlapped with products on two streams
+    (afx_prefill_batch), and the restores alone."""
+    import torch
+    from weight_streaming_canonical_gb300 import synth
+    shapes = {name: shape for name, shape, _ in synth.LAYER_TENSORS}
+    mats = [(name, d, int(off)) for (name, _, _, d), off in zip(parts, offs) if len(shapes.get(name, ())) == 2]
+    n_w = sum(d.n for _, d, _ in mats)
+    biggest = max(d.n for _, d, _ in mats)
+    scratch = [torch.empty(biggest, dtype=torch.int16, device=dev) for _ in range(2)]
+    ws = torch.empty(afx.AFX_PREFILL_GEMM_WORKSPACE_BYTES, dtype=torch.uint8, device=dev)
+    conts = [dev_blob[off:off + d.container_bytes] for _, d, off in mats]
+    descs = [d for _, d, _ in mats]
+    mshapes = [shapes[name] for name, _, _ in mats]
+    peak = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"] if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else 1900.0
+    rs, gs = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    out = {"matrices": len(mats), "weights": n_w, "bf16_peak_tflops": peak, "runs": []}
+
+    def timed(fn, stream, reps=5):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    padded = [(d.n * 2 + 255) // 256 * 128 for d in descs]
+    whole = torch.empty(sum(padded), dtype=torch.int16, device=dev)
+    whole_views = [whole[o:o + d.n] for o, d in zip(np.cumsum([0] + padded[:-1]), descs)]
+    with torch.cuda.stream(gs):
+        def restores():
+            for (_, d, _), c in zip(mats, conts):
+                afx.afx_decode(d, c, scratch[0][:d.n], stream=gs)
+        restore_ms = timed(restores, gs)
+        restore_one_launch_ms = timed(lambda: afx.afx_decode_batch(descs, conts, whole_views, stream=gs), gs)
+    out["restore_ms_per_matrix_launches"] = restore_ms
+    out["restore_ms_one_launch"] = restore_one_launch_ms
+    for n_tok in (128, 512, 2048):
+        xs = [torch.from_numpy(synth.activations(n_tok, cl, seed=21).view(np.int16)).to(dev) for _, cl in mshapes]
+        ys = [torch.empty((n_tok, r), dtype=torch.float32, device=dev) for r, _ in mshapes]
+
+        def sequential():
+            for i, (d, c) in enumerate(zip(descs, conts)):
+                r, cl = mshapes[i]
+                afx.afx_prefill(d, c, r, cl, xs[i], ys[i], scratch[0], ws, stream=gs)
+
+        def overlapped():
+            afx.afx_prefill_batch(descs, conts, mshapes, xs, ys, scratch, ws, restore_stream=rs, gemm_stream=gs)
+
+        def one_launch():
+            afx.afx_prefill_batch(descs, conts, mshapes, xs, ys, [whole, None], ws, gemm_stream=gs)
+
+        seq_ms = timed(sequential, gs)
+        ovl_ms = timed(overlapped, gs)
+        one_ms = timed(one_launch, gs)
+        gemm_ms = max(seq_ms - restore_ms, 1e-9)
+        best = min(seq_ms, ovl_ms, one_ms)
+        flop = 2.0 * n_w * n_tok
+        out["runs"].append({"tokens": n_tok, "sequential_ms": seq_ms, "overlapped_ms": ovl_ms,
+                            "one_restore_launch_ms": one_ms, "gemm_ms_from_difference": gemm_ms,
+                            "tokens_per_s": n_tok / (best * 1e-3), "tflops": flop / (best * 1e-3) / 1e12,
+                            "gemm_tflops": flop / (gemm_ms * 1e-3) / 1e12,
+                            "gemm_frac_of_bf16_peak": flop / (gemm_ms * 1e-3) / 1e12 / peak,
+                            "best_over_sum_of_parts": best / (restore_one_launch_ms + gemm_ms)})
+    out["path"] = ("afx_prefill / afx_prefill_batch: restore_store_kernel into scratch, cuBLAS BF16 GEMM with "
+                   "float32 accumulation; sequential: restore then product per matrix on one stream; overlapped: "
+                   "restore of matrix i+1 on a second stream; one restore launch: all seven restored by one "
+                   "afx_decode_batch launch, then the products; tokens_per_s and tflops from the fastest")
+    return out
 
 
 def run_residency_plan(afx, parts, link_gbs, restore_gbs):

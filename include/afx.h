@@ -291,6 +291,55 @@ afx_status afx_stream_run(const afx_layer* layers, uint32_t n_layers, void* cons
 afx_status afx_test_restore_stalled(const afx_desc* desc, const void* container_dev, uint16_t* out_dev,
                                     uint32_t wait_polls, afx_stream_t stream, int32_t* status_dev);
 
+/* ---- prefill -------------------------------------------------------------
+ *
+ * The prompt of a request multiplies every weight matrix by many token
+ * vectors at once ("Memory requirements of language model inference on a
+ * consumer GPU", section "Loading one part of the model at a time": the
+ * prefill stage processes the whole prompt, then decoding produces one
+ * token at a time).  That product is a dense contraction
+ * for the tensor cores, and the restore (not HBM) bounds the weights' side:
+ * the matrix is restored into scratch memory by the restore kernel, then
+ * multiplied by cuBLAS (BF16 inputs, float32 accumulation), and across
+ * matrices the restore of the next overlaps the product of the current. */
+
+/* cuBLAS workspace these calls hand to cuBLAS (caller-owned device memory). */
+#define AFX_PREFILL_GEMM_WORKSPACE_BYTES (32u << 20)
+
+/* y_dev[t][r] = sum_c W[r][c] * x_dev[t][c] for t < n_tokens: W the
+ * container's weights as [rows][cols] (rows * cols == n, row-major, as
+ * afx_decode_gemv), x_dev BF16 [n_tokens][cols], y_dev float32
+ * [n_tokens][rows] (overwritten).  w_scratch_dev: rows * cols BF16 of
+ * device memory that receives the restored W (16-byte aligned).
+ * gemm_workspace_dev: AFX_PREFILL_GEMM_WORKSPACE_BYTES of device memory.
+ * Enqueues the restore and the product on `stream`.  The first call on a
+ * host thread creates that thread's cuBLAS handle for the device (cuBLAS
+ * allocates its own small state then); calls allocate nothing else.
+ * Status bits of the restore land in *status_dev as for afx_decode.
+ * Errors: AFX_E_ARG, AFX_E_FORMAT, AFX_E_CUDA (a failed cuBLAS call too). */
+afx_status afx_prefill(const afx_desc* desc, const void* container_dev, uint32_t rows, uint32_t cols,
+                       const uint16_t* x_dev, uint32_t n_tokens, float* y_dev, uint16_t* w_scratch_dev,
+                       void* gemm_workspace_dev, afx_stream_t stream, int32_t* status_dev);
+
+/* afx_prefill over count matrices, in one of two forms.
+ * w_scratch_dev[1] != NULL: pipelined on two streams -- the restore of
+ * matrix i (restore_stream, into w_scratch_dev[i % 2]) may overlap the
+ * product of matrix i-1 (gemm_stream); each product waits for its restore
+ * and each scratch buffer is refilled only after the product that read it
+ * (CUDA events, no host waits); both buffers hold the largest rows * cols
+ * BF16.  w_scratch_dev[1] == NULL: all matrices are restored in one launch
+ * into w_scratch_dev[0], back to back, each starting at a 256-byte
+ * boundary (sum of round_up(2 * rows * cols, 256) bytes), then multiplied
+ * in order, all on gemm_stream.  On a GPU where both kernels fill every SM
+ * they run one after the other either way, and the one-launch form saves
+ * the restore launches' ramps.  Synchronise gemm_stream for the results.
+ * Same rules and errors as afx_prefill, per matrix. */
+afx_status afx_prefill_batch(const afx_desc* descs, const void* const* containers_dev, const uint32_t* rows,
+                             const uint32_t* cols, const uint16_t* const* xs_dev, uint32_t n_tokens,
+                             float* const* ys_dev, uint32_t count, uint16_t* const* w_scratch_dev,
+                             void* gemm_workspace_dev, afx_stream_t restore_stream, afx_stream_t gemm_stream,
+                             int32_t* status_dev);
+
 /* ---- residency planning ------------------------------------------------
  *
  * Where each tensor of a model lives during inference on one GPU with a

@@ -128,6 +128,12 @@ _lib.afx_plan_residency.argtypes = [ctypes.POINTER(afx_plan_tensor), _u32, _u64,
                                     ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_double),
                                     ctypes.POINTER(ctypes.c_uint64)]
 _lib.afx_debug_bounds_report.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint32)]
+_lib.afx_prefill.argtypes = [ctypes.POINTER(afx_desc), _vp, _u32, _u32, _vp, _u32, _vp, _vp, _vp, _vp, _i32p]
+_lib.afx_prefill_batch.argtypes = [ctypes.POINTER(afx_desc), ctypes.POINTER(ctypes.c_void_p),
+                                   ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint32),
+                                   ctypes.POINTER(ctypes.c_void_p), _u32, ctypes.POINTER(ctypes.c_void_p), _u32,
+                                   ctypes.POINTER(ctypes.c_void_p), _vp, _vp, _vp, _i32p]
+AFX_PREFILL_GEMM_WORKSPACE_BYTES = 32 << 20
 _lib.afx_last_error.argtypes = []
 _lib.afx_last_error.restype = ctypes.c_char_p
 _lib.afx_status_string.argtypes = [ctypes.c_int]
@@ -135,7 +141,7 @@ _lib.afx_status_string.restype = ctypes.c_char_p
 for _f in (_lib.afx_build_code, _lib.afx_encode_bound, _lib.afx_encode, _lib.afx_parse_header, _lib.afx_decode,
            _lib.afx_decode_batch, _lib.afx_decode_gemv_workspace, _lib.afx_decode_gemv, _lib.afx_decode_gemv_batch,
            _lib.afx_decode_gemv_static, _lib.afx_stream_run, _lib.afx_test_restore_stalled,
-           _lib.afx_plan_residency, _lib.afx_debug_bounds_report):
+           _lib.afx_plan_residency, _lib.afx_debug_bounds_report, _lib.afx_prefill, _lib.afx_prefill_batch):
     _f.restype = ctypes.c_int
 
 
@@ -319,6 +325,36 @@ def afx_stream_run(layers, dev_bufs, buf_bytes: int, compute_stream=None, copy_s
                                                   _stream_handle(compute_stream), _stream_handle(copy_stream),
                                                   _stream_handle(d2h_stream) if d2h_stream is not None else None,
                                                   _dev_ptr(status_dev)))
+
+
+def afx_prefill(desc: afx_desc, container_dev, rows: int, cols: int, x_dev, y_dev, w_scratch_dev, gemm_workspace_dev,
+                stream=None, status_dev=None) -> None:
+    """y_dev[t] = W x_dev[t] for every token t: x_dev BF16 [n_tokens][cols], y_dev float32 [n_tokens][rows]."""
+    n_tokens = x_dev.shape[0]
+    if x_dev.numel() != n_tokens * cols or y_dev.numel() != n_tokens * rows:
+        raise ValueError("x_dev must be [n_tokens][cols] and y_dev [n_tokens][rows]")
+    if w_scratch_dev.numel() * w_scratch_dev.element_size() < 2 * rows * cols:
+        raise ValueError("w_scratch_dev must hold rows * cols BF16")
+    _check("afx_prefill", _lib.afx_prefill(ctypes.byref(desc), _dev_ptr(container_dev), rows, cols, _dev_ptr(x_dev),
+                                            n_tokens, _dev_ptr(y_dev), _dev_ptr(w_scratch_dev),
+                                            _dev_ptr(gemm_workspace_dev), _stream_handle(stream), _dev_ptr(status_dev)))
+
+
+def afx_prefill_batch(descs, containers_dev, shapes, xs_dev, ys_dev, w_scratch_dev, gemm_workspace_dev,
+                      restore_stream=None, gemm_stream=None, status_dev=None) -> None:
+    """afx_prefill over several matrices (shapes = [(rows, cols)]).  w_scratch_dev: two buffers of the
+    largest rows * cols BF16 (restores pipelined with products), or [one buffer of all matrices, None]
+    (one restore launch, then the products)."""
+    n = len(descs)
+    n_tokens = xs_dev[0].shape[0]
+    arr = (afx_desc * n)(*descs)
+    rows = (ctypes.c_uint32 * n)(*[r for r, _ in shapes])
+    cols = (ctypes.c_uint32 * n)(*[c for _, c in shapes])
+    scratch = (ctypes.c_void_p * 2)(*[(_dev_ptr(t) if t is not None else None) for t in w_scratch_dev])
+    _check("afx_prefill_batch", _lib.afx_prefill_batch(arr, _ptrs(containers_dev), rows, cols, _ptrs(xs_dev), n_tokens,
+                                                        _ptrs(ys_dev), n, scratch, _dev_ptr(gemm_workspace_dev),
+                                                        _stream_handle(restore_stream), _stream_handle(gemm_stream),
+                                                        _dev_ptr(status_dev)))
 
 
 def afx_plan_residency(tensors, device_budget_bytes: int, link_gbs: float, restore_gbs: float,

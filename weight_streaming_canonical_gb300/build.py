@@ -84,7 +84,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, 
         list(ex.map(run, jobs))
     if force or jobs or _stale(lib, objs):
         tmp = lib + f".tmp{os.getpid()}"
-        run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-Xcompiler", "-pthread"])
+        run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-Xcompiler", "-pthread", "-lcublas"])
         os.replace(tmp, lib)
     return lib
 
