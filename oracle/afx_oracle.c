@@ -35,6 +35,20 @@
  *    float64 sums (every bf16 x bf16 product is exact in float64), rounded
  *    to float32 once at the end; A[b][r] = sum_c |W[r][c] * x[b][c]|.
  *
+ * Element formats.  The pages treat BF16 only; the same container also
+ * holds two other formats (this library's extension, its own reading).
+ * Each element splits into an 8-bit-or-smaller symbol, which is coded, and
+ * raw bits, which are stored as they are:
+ *   0 BF16 (16 bits: sign, 8 exponent, 7 mantissa): symbol = exponent;
+ *     raw byte = sign << 7 | mantissa.
+ *   1 FP16 (IEEE 754 binary16: sign, 5 exponent, 10 fraction): symbol =
+ *     exponent << 3 | the 3 leading fraction bits; raw byte = sign << 7 |
+ *     the 7 trailing fraction bits.  The symbol takes three fraction bits
+ *     so that the raw part stays one byte per element.
+ *   2 E4M3 (OCP 8-bit floating point, E4M3: sign, 4 exponent, 3 mantissa):
+ *     symbol = exponent; raw nibble = sign << 3 | mantissa, two per byte,
+ *     element 2k in the low nibble of byte k.
+ *
  * Container (all integers little-endian):
  *   header, 512 bytes:
  *     0  u32 magic 0x31584641      4  u16 version 1     6  u16 header bytes 512
@@ -46,10 +60,12 @@
  *    80  u64 block index offset   88  u64 container bytes
  *    96  u32 longest code length 100  u32 number of present exponents
  *   104  u32 fill exponent (when exactly one exponent is present)
- *   108..255 zero;   256..511 code length of each exponent value 0..255
+ *   108  u32 element format (0 BF16, 1 FP16, 2 E4M3)
+ *   112..255 zero;   256..511 code length of each symbol value 0..255
  *   exp section: u32 words; stream bit i is bit (31 - i mod 32) of word
  *     floor(i / 32); size = (chunks * T rounded up to 16) + 16 zero bytes.
- *   sm section: one byte per weight, (sign << 7) | mantissa.
+ *   sm section: the raw bits, one byte per element ((sign << 7) | mantissa
+ *     for BF16), or one nibble per element for E4M3 (ceil(n / 2) bytes).
  *   chunk index: one u16 per chunk of 8*T stream bits:
  *     bits 0..4  = offset of the first codeword that starts in the chunk,
  *     bits 5..15 = number of codewords that start in the chunk.
@@ -88,6 +104,83 @@ static uint16_t orc_join(unsigned exponent, unsigned sign_mantissa) {
     return (uint16_t)((sign << 15) | (exponent << 7) | mantissa);
 }
 
+#define ORC_FMT_BF16 0u
+#define ORC_FMT_FP16 1u
+#define ORC_FMT_E4M3 2u
+
+static int orc_valid_format(unsigned fmt) { return fmt <= ORC_FMT_E4M3; }
+
+static unsigned orc_elem_bytes(unsigned fmt) { return fmt == ORC_FMT_E4M3 ? 1u : 2u; }
+
+static uint64_t orc_raw_bytes(unsigned fmt, uint64_t n) { return fmt == ORC_FMT_E4M3 ? (n + 1) / 2 : n; }
+
+static unsigned orc_symbols_of_format(unsigned fmt) { return fmt == ORC_FMT_E4M3 ? 16u : 256u; }
+
+static unsigned orc_read_elem(const void* elems, unsigned fmt, uint64_t i) {
+    if (orc_elem_bytes(fmt) == 1) return ((const uint8_t*)elems)[i];
+    return ((const uint16_t*)elems)[i];
+}
+
+static void orc_write_elem(void* elems, unsigned fmt, uint64_t i, unsigned v) {
+    if (orc_elem_bytes(fmt) == 1)
+        ((uint8_t*)elems)[i] = (uint8_t)v;
+    else
+        ((uint16_t*)elems)[i] = (uint16_t)v;
+}
+
+static unsigned orc_symbol_of(unsigned fmt, unsigned v) {
+    if (fmt == ORC_FMT_FP16) {
+        unsigned exponent = (v >> 10) & 0x1Fu;
+        unsigned fraction = v & 0x3FFu;
+        return (exponent << 3) | (fraction >> 7);
+    }
+    if (fmt == ORC_FMT_E4M3) return (v >> 3) & 0xFu;
+    return orc_exponent_of((uint16_t)v);
+}
+
+static unsigned orc_raw_of(unsigned fmt, unsigned v) {
+    if (fmt == ORC_FMT_FP16) {
+        unsigned sign = (v >> 15) & 1u;
+        unsigned fraction = v & 0x3FFu;
+        return (sign << 7) | (fraction & 0x7Fu);
+    }
+    if (fmt == ORC_FMT_E4M3) {
+        unsigned sign = (v >> 7) & 1u;
+        unsigned mantissa = v & 0x7u;
+        return (sign << 3) | mantissa;
+    }
+    return orc_sign_mantissa_of((uint16_t)v);
+}
+
+static unsigned orc_join_of(unsigned fmt, unsigned symbol, unsigned raw) {
+    if (fmt == ORC_FMT_FP16) {
+        unsigned sign = (raw >> 7) & 1u;
+        unsigned exponent = symbol >> 3;
+        unsigned fraction = ((symbol & 0x7u) << 7) | (raw & 0x7Fu);
+        return (sign << 15) | (exponent << 10) | fraction;
+    }
+    if (fmt == ORC_FMT_E4M3) {
+        unsigned sign = (raw >> 3) & 1u;
+        unsigned mantissa = raw & 0x7u;
+        return (sign << 7) | (symbol << 3) | mantissa;
+    }
+    return orc_join(symbol, raw);
+}
+
+/* raw bits of element i in the sm section */
+static unsigned orc_get_raw(const uint8_t* sm, unsigned fmt, uint64_t i) {
+    if (fmt == ORC_FMT_E4M3) return (sm[i / 2] >> (4 * (i % 2))) & 0xFu;
+    return sm[i];
+}
+
+/* the section starts zeroed; element i's raw bits are OR-ed in */
+static void orc_put_raw(uint8_t* sm, unsigned fmt, uint64_t i, unsigned raw) {
+    if (fmt == ORC_FMT_E4M3)
+        sm[i / 2] = (uint8_t)(sm[i / 2] | (raw << (4 * (i % 2))));
+    else
+        sm[i] = (uint8_t)raw;
+}
+
 /* ---- little-endian field access ------------------------------------------- */
 
 static uint64_t orc_get(const uint8_t* p, unsigned bytes) {
@@ -104,10 +197,15 @@ static uint64_t orc_round_up(uint64_t v, uint64_t m) { return (v + m - 1) / m * 
 
 /* ---- histogram ------------------------------------------------------------ */
 
-int orc_histogram(const uint16_t* w, uint64_t n, uint64_t hist[256]) {
+int orc_histogram_fmt(const void* elems, uint64_t n, unsigned fmt, uint64_t hist[256]) {
+    if (!orc_valid_format(fmt)) return ORC_E_ARG;
     for (int s = 0; s < 256; s++) hist[s] = 0;
-    for (uint64_t i = 0; i < n; i++) hist[orc_exponent_of(w[i])]++;
+    for (uint64_t i = 0; i < n; i++) hist[orc_symbol_of(fmt, orc_read_elem(elems, fmt, i))]++;
     return ORC_OK;
+}
+
+int orc_histogram(const uint16_t* w, uint64_t n, uint64_t hist[256]) {
+    return orc_histogram_fmt(w, n, ORC_FMT_BF16, hist);
 }
 
 /* ---- package-merge ---------------------------------------------------------
@@ -227,7 +325,8 @@ static int orc_valid_geometry(uint32_t T, uint32_t C) {
     return 1;
 }
 
-static void orc_make_layout(uint64_t n, uint64_t total_bits, uint32_t T, uint32_t C, orc_layout* L) {
+static void orc_make_layout(uint64_t n, unsigned fmt, uint64_t total_bits, uint32_t T, uint32_t C,
+                            orc_layout* L) {
     L->n = n;
     L->total_bits = total_bits;
     L->T = T;
@@ -238,18 +337,23 @@ static void orc_make_layout(uint64_t n, uint64_t total_bits, uint32_t T, uint32_
     L->off_exp = ORC_HEADER_BYTES;
     L->exp_bytes = orc_round_up(L->n_chunks * T, 16) + 16;
     L->off_sm = orc_round_up(L->off_exp + L->exp_bytes, 256);
-    L->off_chunk = orc_round_up(L->off_sm + n, 256);
+    L->off_chunk = orc_round_up(L->off_sm + orc_raw_bytes(fmt, n), 256);
     L->off_block = orc_round_up(L->off_chunk + 2 * L->n_chunks, 256);
     L->container_bytes = orc_round_up(L->off_block + 8 * (L->n_blocks + 1), 256);
 }
 
-/* Size of the container for n weights whose codes total total_bits bits. */
-int orc_container_bytes(uint64_t n, uint64_t total_bits, uint32_t T, uint32_t C, uint64_t* bytes) {
-    if (!orc_valid_geometry(T, C)) return ORC_E_ARG;
+/* Size of the container for n elements whose codes total total_bits bits. */
+int orc_container_bytes_fmt(uint64_t n, unsigned fmt, uint64_t total_bits, uint32_t T, uint32_t C,
+                            uint64_t* bytes) {
+    if (!orc_valid_geometry(T, C) || !orc_valid_format(fmt)) return ORC_E_ARG;
     orc_layout L;
-    orc_make_layout(n, total_bits, T, C, &L);
+    orc_make_layout(n, fmt, total_bits, T, C, &L);
     *bytes = L.container_bytes;
     return ORC_OK;
+}
+
+int orc_container_bytes(uint64_t n, uint64_t total_bits, uint32_t T, uint32_t C, uint64_t* bytes) {
+    return orc_container_bytes_fmt(n, ORC_FMT_BF16, total_bits, T, C, bytes);
 }
 
 /* ---- stream bits -------------------------------------------------------------- */
@@ -271,15 +375,19 @@ static unsigned orc_get_bit(const uint8_t* exp_section, uint64_t i) {
 }
 
 /* ---- encode ------------------------------------------------------------------
- * Writes the whole container for w[0..n) with the given code lengths.  The
- * lengths must give every present exponent a code (or, with exactly one
- * present exponent, be all zero).  dst must hold orc_container_bytes().
+ * Writes the whole container for the elements elems[0..n) of format fmt
+ * with the given code lengths.  The lengths must give every present symbol
+ * a code (or, with exactly one present symbol, be all zero), and no length
+ * to a value the format's symbols cannot take.  dst must hold
+ * orc_container_bytes_fmt().
  */
-int orc_encode(const uint16_t* w, uint64_t n, const uint8_t len[256], uint32_t T, uint32_t C,
-               uint8_t* dst, uint64_t dst_bytes) {
-    if (!orc_valid_geometry(T, C)) return ORC_E_ARG;
+int orc_encode_fmt(const void* elems, uint64_t n, unsigned fmt, const uint8_t len[256], uint32_t T, uint32_t C,
+                   uint8_t* dst, uint64_t dst_bytes) {
+    if (!orc_valid_geometry(T, C) || !orc_valid_format(fmt)) return ORC_E_ARG;
+    for (unsigned s = orc_symbols_of_format(fmt); s < 256; s++)
+        if (len[s] != 0) return ORC_E_ARG;
     uint64_t hist[256];
-    orc_histogram(w, n, hist);
+    orc_histogram_fmt(elems, n, fmt, hist);
     unsigned nsym = 0, fill = 0, longest = 0;
     for (int s = 0; s < 256; s++) {
         if (hist[s] > 0) { nsym++; fill = (unsigned)s; }
@@ -301,7 +409,7 @@ int orc_encode(const uint16_t* w, uint64_t n, const uint8_t len[256], uint32_t T
     if (orc_canonical_codes(len, code) != ORC_OK) return ORC_E_ARG;
 
     orc_layout L;
-    orc_make_layout(n, total_bits, T, C, &L);
+    orc_make_layout(n, fmt, total_bits, T, C, &L);
     if (dst_bytes < L.container_bytes) return ORC_E_ARG;
     memset(dst, 0, L.container_bytes);
 
@@ -324,6 +432,7 @@ int orc_encode(const uint16_t* w, uint64_t n, const uint8_t len[256], uint32_t T
     orc_put(dst + 96, 4, nsym >= 2 ? longest : 0);
     orc_put(dst + 100, 4, nsym);
     orc_put(dst + 104, 4, nsym == 1 ? fill : 0);
+    orc_put(dst + 108, 4, fmt);
     for (int s = 0; s < 256; s++) dst[256 + s] = len[s];
 
     /* exponent codes, one bit at a time, most significant code bit first;
@@ -337,7 +446,7 @@ int orc_encode(const uint16_t* w, uint64_t n, const uint8_t len[256], uint32_t T
     uint64_t pos = 0;
     if (nsym >= 2) {
         for (uint64_t i = 0; i < n; i++) {
-            unsigned e = orc_exponent_of(w[i]);
+            unsigned e = orc_symbol_of(fmt, orc_read_elem(elems, fmt, i));
             uint64_t chunk = pos / chunk_bits;
             if (first[chunk] < 0) first[chunk] = (int64_t)(pos - chunk * chunk_bits);
             starts[chunk]++;
@@ -348,8 +457,8 @@ int orc_encode(const uint16_t* w, uint64_t n, const uint8_t len[256], uint32_t T
         }
     }
 
-    /* sign|mantissa bytes */
-    for (uint64_t i = 0; i < n; i++) dst[L.off_sm + i] = (uint8_t)orc_sign_mantissa_of(w[i]);
+    /* raw bits (sign|mantissa bytes for BF16) */
+    for (uint64_t i = 0; i < n; i++) orc_put_raw(dst + L.off_sm, fmt, i, orc_raw_of(fmt, orc_read_elem(elems, fmt, i)));
 
     /* chunk index */
     for (uint64_t c = 0; c < L.n_chunks; c++) {
@@ -371,14 +480,20 @@ int orc_encode(const uint16_t* w, uint64_t n, const uint8_t len[256], uint32_t T
     return ORC_OK;
 }
 
+int orc_encode(const uint16_t* w, uint64_t n, const uint8_t len[256], uint32_t T, uint32_t C,
+               uint8_t* dst, uint64_t dst_bytes) {
+    return orc_encode_fmt(w, n, ORC_FMT_BF16, len, T, C, dst, dst_bytes);
+}
+
 /* ---- decode ------------------------------------------------------------------
  * Parses the header, rebuilds the canonical code from the 256 lengths alone,
- * reads the exponent stream one bit at a time, and joins each exponent with
- * its sign|mantissa byte.  The chunk and block indices are not used to
- * decode; they are checked afterwards against the codeword start positions
- * seen while decoding (ORC_E_INDEX on any difference).
+ * reads the symbol stream one bit at a time, and joins each symbol with its
+ * raw bits.  out receives out_n elements of the header's format (uint16 for
+ * BF16 and FP16, uint8 for E4M3).  The chunk and block indices are not used
+ * to decode; they are checked afterwards against the codeword start
+ * positions seen while decoding (ORC_E_INDEX on any difference).
  */
-int orc_decode(const uint8_t* src, uint64_t src_bytes, uint16_t* out, uint64_t out_n) {
+int orc_decode(const uint8_t* src, uint64_t src_bytes, void* out, uint64_t out_n) {
     if (src_bytes < ORC_HEADER_BYTES) return ORC_E_FORMAT;
     if (orc_get(src + 0, 4) != ORC_MAGIC) return ORC_E_FORMAT;
     if (orc_get(src + 4, 2) != 1 || orc_get(src + 6, 2) != ORC_HEADER_BYTES) return ORC_E_FORMAT;
@@ -387,8 +502,10 @@ int orc_decode(const uint8_t* src, uint64_t src_bytes, uint16_t* out, uint64_t o
     uint32_t T = (uint32_t)orc_get(src + 24, 4);
     uint32_t C = (uint32_t)orc_get(src + 28, 4);
     if (!orc_valid_geometry(T, C)) return ORC_E_FORMAT;
+    unsigned fmt = (unsigned)orc_get(src + 108, 4);
+    if (!orc_valid_format(fmt)) return ORC_E_FORMAT;
     orc_layout L;
-    orc_make_layout(n, total_bits, T, C, &L);
+    orc_make_layout(n, fmt, total_bits, T, C, &L);
     if (orc_get(src + 32, 8) != L.n_chunks || orc_get(src + 40, 8) != L.n_blocks ||
         orc_get(src + 48, 8) != L.off_exp || orc_get(src + 56, 8) != L.exp_bytes ||
         orc_get(src + 64, 8) != L.off_sm || orc_get(src + 72, 8) != L.off_chunk ||
@@ -396,13 +513,14 @@ int orc_decode(const uint8_t* src, uint64_t src_bytes, uint16_t* out, uint64_t o
         return ORC_E_FORMAT;
     if (src_bytes < L.container_bytes) return ORC_E_FORMAT;
     if (out_n != n) return ORC_E_ARG;
-    for (unsigned i = 108; i < 256; i++)
+    for (unsigned i = 112; i < 256; i++)
         if (src[i] != 0) return ORC_E_FORMAT;
 
     const uint8_t* len = src + 256;
     unsigned longest = 0, coded = 0;
     for (int s = 0; s < 256; s++) {
         if (len[s] > 24) return ORC_E_FORMAT;
+        if (len[s] > 0 && (unsigned)s >= orc_symbols_of_format(fmt)) return ORC_E_FORMAT;
         if (len[s] > longest) longest = len[s];
         if (len[s] > 0) coded++;
     }
@@ -439,7 +557,7 @@ int orc_decode(const uint8_t* src, uint64_t src_bytes, uint16_t* out, uint64_t o
     } else {
         if (coded != 0 || total_bits != 0) return ORC_E_FORMAT;
         if (nsym == 0 && (n != 0 || fill != 0)) return ORC_E_FORMAT;
-        if (nsym == 1 && (n == 0 || fill > 255)) return ORC_E_FORMAT;
+        if (nsym == 1 && (n == 0 || fill >= orc_symbols_of_format(fmt))) return ORC_E_FORMAT;
     }
 
     const uint8_t* exp_section = src + L.off_exp;
@@ -475,10 +593,12 @@ int orc_decode(const uint8_t* src, uint64_t src_bytes, uint16_t* out, uint64_t o
             if (found < 0) { status = ORC_E_CORRUPT; break; }
             e = (unsigned)found;
         }
-        out[i] = orc_join(e, sm[i]);
+        orc_write_elem(out, fmt, i, orc_join_of(fmt, e, orc_get_raw(sm, fmt, i)));
     }
     if (status == ORC_OK && pos != total_bits) status = ORC_E_CORRUPT;
 
+    if (status == ORC_OK && fmt == ORC_FMT_E4M3 && n % 2 == 1 && (sm[n / 2] >> 4) != 0)
+        status = ORC_E_FORMAT; /* the unused nibble after an odd count is zero */
     if (status == ORC_OK) {
         /* the stream's padding bits are zero */
         for (uint64_t b = total_bits; b < 8 * L.exp_bytes; b++)

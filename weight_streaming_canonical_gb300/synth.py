@@ -1,7 +1,8 @@
 """Seeded synthetic inputs shared by the tests, the benchmark and the oracle.
 
-This module draws random BF16 bit patterns with the shapes and value
-distributions of the workloads.  It holds none of the codec's arithmetic:
+This module draws random BF16 bit patterns (and FP16 or E4M3 ones for the
+other element formats) with the shapes and value distributions of the
+workloads.  It holds none of the codec's arithmetic:
 no exponent split, no code construction, no packing.
 
 Shapes follow "Memory requirements of language model inference on a
@@ -95,8 +96,46 @@ def _threads() -> int:
     return max(1, min(16, os.cpu_count() or 1))
 
 
-def _blocked(n: int, fill, seed: int, stream: int) -> np.ndarray:
-    out = np.empty(n, np.uint16)
+def fp16_round(f: np.ndarray) -> np.ndarray:
+    """float32 -> IEEE binary16 bit patterns (uint16), round to nearest even
+    (numpy's conversion); magnitudes past 65504 become infinities."""
+    with np.errstate(over="ignore"):
+        return np.ascontiguousarray(f, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+E4M3_MAX = 448.0  # largest finite OCP E4M3 value, 1.75 * 2**8
+
+
+def e4m3_round(f: np.ndarray) -> np.ndarray:
+    """float32 -> OCP 8-bit float E4M3 bit patterns (uint8): 1 sign, 4 exponent
+    bits with bias 7, 3 mantissa bits; round to nearest even, magnitudes past
+    448 saturate to 448 (the format has no infinities).  NaN is not produced."""
+    x = np.ascontiguousarray(f, dtype=np.float32).astype(np.float64)
+    sign = np.signbit(x).astype(np.uint8) << np.uint8(7)
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    out = np.zeros(a.shape, np.uint8)
+    normal = a >= 2.0 ** -6
+    # subnormals: multiples of 2**-9 below 2**-6 (a result of 8 is the smallest normal)
+    q = np.rint(a[~normal] / 2.0 ** -9).astype(np.int64)
+    out[~normal] = np.where(q >= 8, np.uint8(1 << 3), q.astype(np.uint8))
+    an = a[normal]
+    e = np.floor(np.log2(an)).astype(np.int64)
+    # log2 of a value just below a power of two can round up: fix the exponent exactly
+    e = np.where(np.ldexp(1.0, e) > an, e - 1, e)
+    e = np.where(np.ldexp(1.0, e + 1) <= an, e + 1, e)
+    m = np.rint((an / np.ldexp(1.0, e) - 1.0) * 8.0).astype(np.int64)
+    carry = m == 8
+    e = np.where(carry, e + 1, e)
+    m = np.where(carry, 0, m)
+    big = (e > 8) | ((e == 8) & (m > 6))
+    e = np.where(big, 8, e)
+    m = np.where(big, 6, m)
+    out[normal] = (((e + 7) << 3) | m).astype(np.uint8)
+    return out | sign
+
+
+def _blocked(n: int, fill, seed: int, stream: int, dtype=np.uint16) -> np.ndarray:
+    out = np.empty(n, dtype)
     starts = list(range(0, n, BLOCK))
 
     def work(start: int) -> None:
@@ -122,6 +161,31 @@ def normal(n: int, mean: float = 0.0, std: float = 0.02, seed: int = 0, stream: 
         return bf16_round(v)
 
     return _blocked(int(n), fill, seed, stream)
+
+
+def normal_fp16(n: int, mean: float = 0.0, std: float = 0.02, seed: int = 0, stream: int = _MATRIX_ID) -> np.ndarray:
+    """n FP16 patterns of N(mean, std) drawn in float32 and rounded to nearest even."""
+
+    def fill(rng, k):
+        v = rng.standard_normal(k, dtype=np.float32)
+        v *= np.float32(std)
+        v += np.float32(mean)
+        return fp16_round(v)
+
+    return _blocked(int(n), fill, seed, stream)
+
+
+def normal_e4m3(n: int, mean: float = 0.0, std: float = 1.0, seed: int = 0, stream: int = _MATRIX_ID) -> np.ndarray:
+    """n E4M3 patterns of N(mean, std) * 448 / (6 std): a per-tensor scale that puts
+    six standard deviations at the format's largest value, the usual way FP8
+    weights are stored (the scale is kept beside the tensor, not in it)."""
+    scale = E4M3_MAX / (6.0 * std)
+
+    def fill(rng, k):
+        v = rng.standard_normal(k, dtype=np.float32).astype(np.float64) * std + mean
+        return e4m3_round((v * scale).astype(np.float32))
+
+    return _blocked(int(n), fill, seed, stream, np.uint8)
 
 
 def adversarial(n: int = 1 << 28, seed: int = 0, stream: int = _ADVERSARIAL_ID) -> np.ndarray:
@@ -169,6 +233,29 @@ def layer_tensor(name: str, seed: int = 0, layer: int = 0) -> np.ndarray:
     raise KeyError(name)
 
 
+def layer_tensor_fp16(name: str, seed: int = 0, layer: int = 0) -> np.ndarray:
+    """The layer tensor `name` with the same value distribution, stored as FP16."""
+    for nm, shape, kind in LAYER_TENSORS:
+        if nm == name:
+            stream = 2000 + 16 * int(layer) + _TENSOR_IDS[nm]
+            if kind == "norm":
+                return normal_fp16(numel(shape), 1.0, 0.05, seed, stream).reshape(shape)
+            return normal_fp16(numel(shape), 0.0, 0.02, seed, stream).reshape(shape)
+    raise KeyError(name)
+
+
+def layer_matrix_e4m3(name: str, seed: int = 0, layer: int = 0) -> np.ndarray:
+    """The layer matrix `name` stored as E4M3 with a per-tensor scale (matrices
+    only: the norm vectors stay in a wider format)."""
+    for nm, shape, kind in LAYER_TENSORS:
+        if nm == name:
+            if kind != "matrix":
+                raise KeyError(f"{name} is not a matrix")
+            stream = 3000 + 16 * int(layer) + _TENSOR_IDS[nm]
+            return normal_e4m3(numel(shape), 0.0, 0.02, seed, stream).reshape(shape)
+    raise KeyError(name)
+
+
 def layer(seed: int = 0, layer_index: int = 0) -> dict[str, np.ndarray]:
     """All tensors of one Qwen3-14B-shaped decoder layer (~330M weights)."""
     return {name: layer_tensor(name, seed, layer_index) for name, _, _ in LAYER_TENSORS}
@@ -203,3 +290,8 @@ def exponent_mix(n: int, n_exponents: int, ratio: float = 0.85, first: int = 100
 def all_bf16_patterns() -> np.ndarray:
     """Every one of the 65,536 BF16 bit patterns, in order."""
     return np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+
+
+def all_e4m3_patterns() -> np.ndarray:
+    """Every one of the 256 E4M3 bit patterns, in order (0x7F and 0xFF are NaN)."""
+    return np.arange(256, dtype=np.uint16).astype(np.uint8)
