@@ -157,9 +157,12 @@ def exponent_entropy_bits(parts) -> float:
 
 
 def algorithmic_bytes(d) -> int:
-    """Bytes a restore must move: coded exponent bits, sign|mantissa bytes,
-    chunk and block index entries read; 2 bytes per weight written."""
-    return (d.total_bits + 7) // 8 + d.n + 2 * d.n_chunks + 8 * (d.n_blocks + 1) + 2 * d.n
+    """Bytes a restore must move: coded symbol bits, the raw bits (a sign|mantissa
+    byte per element; a nibble for E4M3), chunk and block index entries read;
+    the elements written (2 bytes each; 1 for E4M3)."""
+    e4m3 = getattr(d, "format", 0) == 2
+    raw, out = ((d.n + 1) // 2, d.n) if e4m3 else (d.n, 2 * d.n)
+    return (d.total_bits + 7) // 8 + raw + 2 * d.n_chunks + 8 * (d.n_blocks + 1) + out
 
 
 class ClockSampler:
@@ -456,6 +459,7 @@ def run_ours(args):
                                       "pays": (S - S_disk) / b > ms * 1e-3}
             line["residency_plan"] = run_residency_plan(afx, parts, b / 1e9, value)
             line["prefill"] = run_prefill_bench(afx, parts, dev_blob, offs, dev, args)
+            line["formats"] = run_formats_bench(afx, dev, args)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -636,6 +640,77 @@ def run_prefill_bench(afx, parts, dev_blob, offs, dev, args):
                    "float32 accumulation; sequential: restore then product per matrix on one stream; overlapped: "
                    "restore of matrix i+1 on a second stream; one restore launch: all seven restored by one "
                    "afx_decode_batch launch, then the products; tokens_per_s and tflops from the fastest")
+    return out
+
+
+def run_formats_bench(afx, dev, args):
+    """The other element formats on the same layer shapes, containers resident
+    in HBM, one afx_decode_batch launch per step: FP16 (all nine tensors, the
+    BF16 distributions rounded to FP16) and E4M3 (the seven matrices with a
+    per-tensor scale).  Bit-exact check first, then the median of per-launch
+    CUDA-event times."""
+    import torch
+    from weight_streaming_canonical_gb300 import synth
+    out = {}
+    for fmt, label in ((afx.AFX_FMT_FP16, "fp16"), (afx.AFX_FMT_E4M3, "e4m3")):
+        if fmt == afx.AFX_FMT_FP16:
+            gens = [(nm, (lambda nm=nm: synth.layer_tensor_fp16(nm, seed=args.seed))) for nm, _, _ in synth.LAYER_TENSORS]
+        else:
+            gens = [(nm, (lambda nm=nm: synth.layer_matrix_e4m3(nm, seed=args.seed)))
+                    for nm, _, kind in synth.LAYER_TENSORS if kind == "matrix"]
+
+        def one(item, fmt=fmt):
+            nm, gen = item
+            w = np.ascontiguousarray(gen()).reshape(-1)
+            c, d = afx.encode(w, fmt=fmt)
+            return nm, w, c, d
+
+        with cf.ThreadPoolExecutor(min(len(gens), 16)) as ex:
+            parts = list(ex.map(one, gens))
+        elem = afx.element_bytes(fmt)
+        descs = [d for *_, d in parts]
+        conts = [torch.from_numpy(c).to(dev) for _, _, c, _ in parts]
+        outs = [torch.empty(w.size, dtype=torch.uint8 if elem == 1 else torch.int16, device=dev) for _, w, _, _ in parts]
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        stream = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(stream):
+            afx.afx_decode_batch(descs, conts, outs, stream=stream, status_dev=status)
+        torch.cuda.synchronize()
+        exact = status.item() == 0 and all(
+            torch.equal(o, torch.from_numpy(w.view(np.uint8 if elem == 1 else np.int16)).to(dev))
+            for (_, w, _, _), o in zip(parts, outs))
+        reps = max(10, args.steps)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                afx.afx_decode_batch(descs, conts, outs, stream=stream, status_dev=status)
+            for e0, e1 in ev:
+                e0.record(stream)
+                afx.afx_decode_batch(descs, conts, outs, stream=stream, status_dev=status)
+                e1.record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
+        n = sum(d.n for d in descs)
+        alg = sum(algorithmic_bytes(d) for d in descs)
+        comp = sum(d.container_bytes for d in descs)
+        peak, peak_kind = measured_hbm_peak()
+        sym_bits = 0.0
+        for _, w, _, d in parts:
+            sym = (w >> 3) & 0xF if elem == 1 else (w >> 7) & 0xFF
+            cnt = np.bincount(sym.astype(np.intp), minlength=256).astype(np.float64)
+            p = cnt[cnt > 0] / w.size
+            sym_bits += float(-(p * np.log2(p)).sum()) * w.size
+        out[label] = {
+            "tensors": len(parts), "elements": n, "bit_exact": bool(exact), "ms": ms,
+            "decoded_gbs": elem * n / (ms * 1e-3) / 1e9, "elements_per_s": n / (ms * 1e-3),
+            "hbm_gbs": alg / (ms * 1e-3) / 1e9, "hbm_frac": alg / (ms * 1e-3) / 1e9 / peak, "peak_kind": peak_kind,
+            "bits_per_element": 8 * comp / n, "raw_bits_per_element": 8 * elem,
+            "coded_symbol_bits_per_element": sum(d.total_bits for d in descs) / n,
+            "symbol_entropy_bits_per_element": sym_bits / n,
+            "algorithmic_bytes_per_step": alg,
+        }
+    out["path"] = ("afx_decode_batch of the whole set per step: restore_store_kernel (FP16: the same bit split as "
+                   "BF16) and restore_store_e4m3_kernel (raw nibbles, byte outputs)")
     return out
 
 

@@ -70,21 +70,38 @@ typedef enum afx_status {
 #define AFX_DEV_BAD_SHAPE 0x8 /* GEMV rows x cols disagree with the block index */
 #define AFX_DEV_TIMEOUT 0x10  /* a staging copy did not arrive within the kernel's wait limit; work skipped */
 
+/* Element formats a container can hold (header field at byte 108).  The
+ * pages treat BF16 only; FP16 and E4M3 are this library's extension under
+ * the same container:
+ *   AFX_FMT_BF16  16-bit elements; coded symbol = the 8-bit exponent, raw
+ *                 byte = sign << 7 | 7-bit mantissa.
+ *   AFX_FMT_FP16  IEEE 754 binary16; coded symbol = the 5-bit exponent and
+ *                 the 3 leading fraction bits (bits 14..7), raw byte = sign
+ *                 << 7 | the 7 trailing fraction bits.  The same bit split
+ *                 as BF16, so the raw part stays one byte per element.
+ *   AFX_FMT_E4M3  OCP 8-bit float E4M3 (bias 7, largest 448); coded symbol =
+ *                 the 4-bit exponent, raw nibble = sign << 3 | 3-bit
+ *                 mantissa, two per byte, element 2k in the low nibble of
+ *                 byte k. */
+#define AFX_FMT_BF16 0u
+#define AFX_FMT_FP16 1u
+#define AFX_FMT_E4M3 2u
+
 #define AFX_MAX_CODE_LEN 24
 /* At most this many codewords start in one block (the decoder's per-block
    staging capacity); the encoder picks T so that this always holds. */
 #define AFX_BLOCK_CAPACITY 32768
 #define AFX_HEADER_BYTES 512
 
-/* A code over the 256 exponent values. */
+/* A code over the 256 symbol values (the exponents, for BF16). */
 typedef struct afx_code {
-    uint64_t count[256]; /* how many weights have each exponent */
+    uint64_t count[256]; /* how many elements have each symbol */
     uint32_t code[256];  /* canonical code, right-aligned in len bits */
-    uint8_t len[256];    /* code length; 0 = exponent absent (or the only one) */
-    uint32_t nsym;       /* number of exponents present */
+    uint8_t len[256];    /* code length; 0 = symbol absent (or the only one) */
+    uint32_t nsym;       /* number of symbols present */
     uint32_t max_len;    /* longest code length (0 when nsym <= 1) */
-    uint32_t fill;       /* the exponent when nsym == 1, else 0 */
-    uint32_t reserved;
+    uint32_t fill;       /* the symbol when nsym == 1, else 0 */
+    uint32_t format;     /* AFX_FMT_*: the element format the code was built for */
 } afx_code;
 
 /* Host-side description of one container: its geometry and section
@@ -101,7 +118,8 @@ typedef struct afx_desc {
     uint64_t off_chunk;
     uint64_t off_block;
     uint64_t container_bytes; /* whole container, a multiple of 256 */
-    uint32_t max_len, nsym, fill, reserved;
+    uint32_t max_len, nsym, fill;
+    uint32_t format;          /* AFX_FMT_*; elements are 2 bytes (BF16, FP16) or 1 byte (E4M3) */
     uint8_t len[256];
 } afx_desc;
 
@@ -115,7 +133,15 @@ typedef struct afx_desc {
  * number of present exponents. */
 afx_status afx_build_code(const uint16_t* w_host, uint64_t n, uint32_t max_len, afx_code* out);
 
-/* Plans the container for n weights coded with `code`: fills *out with the
+/* afx_build_code for elements of any format: elems_host holds n elements of
+ * `format` (uint16 for AFX_FMT_BF16 and AFX_FMT_FP16, uint8 for
+ * AFX_FMT_E4M3) and the histogram is over that format's coded symbol.
+ * out->format records the format; afx_encode_bound and afx_encode take it
+ * from there.  Errors: as afx_build_code, and AFX_E_ARG on an unknown
+ * format. */
+afx_status afx_build_code_fmt(const void* elems_host, uint64_t n, uint32_t format, uint32_t max_len, afx_code* out);
+
+/* Plans the container for n elements coded with `code` (in code->format): fills *out with the
  * geometry, section offsets and total size.  block_chunks = 0 picks C =
  * 512, the geometry the GPU decoder runs; chunk_bytes = 0 picks the largest
  * T of 32, 16, 8, 4 for which a block can never hold more than
@@ -125,12 +151,13 @@ afx_status afx_build_code(const uint16_t* w_host, uint64_t n, uint32_t max_len, 
 afx_status afx_encode_bound(uint64_t n, const afx_code* code, uint32_t chunk_bytes,
                             uint32_t block_chunks, afx_desc* out);
 
-/* Writes the container for w_host[0..n) into dst_host (dst_bytes >=
+/* Writes the container for elems_host[0..n) into dst_host (dst_bytes >=
  * desc->container_bytes), using the code and the plan from
- * afx_encode_bound.  Host only.  Errors: AFX_E_ARG when w holds an exponent
- * that the code does not cover or n differs from the plan; AFX_E_NOSPACE
- * when dst is too small. */
-afx_status afx_encode(const uint16_t* w_host, uint64_t n, const afx_code* code, const afx_desc* desc,
+ * afx_encode_bound.  elems_host holds elements of desc->format (uint16 BF16
+ * or FP16 patterns, or uint8 E4M3 patterns).  Host only.  Errors: AFX_E_ARG
+ * when an element has a symbol that the code does not cover, or n or the
+ * format differs from the plan; AFX_E_NOSPACE when dst is too small. */
+afx_status afx_encode(const void* elems_host, uint64_t n, const afx_code* code, const afx_desc* desc,
                       uint8_t* dst_host, uint64_t dst_bytes);
 
 /* Validates the header of a container held in host memory (magic, version,
@@ -139,11 +166,12 @@ afx_status afx_encode(const uint16_t* w_host, uint64_t n, const afx_code* code, 
  * caller holds (at least the header).  Errors: AFX_E_FORMAT. */
 afx_status afx_parse_header(const uint8_t* header_host, uint64_t bytes, afx_desc* out);
 
-/* Restores all n BF16 weights of one container: out_dev[i] = the i-th
- * weight, bit for bit.  container_dev: the whole container, 16-byte
+/* Restores all n elements of one container: out_dev[i] = the i-th
+ * element, bit for bit.  container_dev: the whole container, 16-byte
  * aligned, in device memory or in pinned (or managed) host memory; a
  * host-resident container is read by the kernel over the host link with no
- * staging copy ("zero copy").  out_dev: n uint16, 16-byte aligned, in
+ * staging copy ("zero copy").  out_dev: n elements of the container's
+ * format (uint16 for BF16 and FP16, uint8 for E4M3), 16-byte aligned, in
  * device memory or pinned host memory.  desc: host copy of the container's
  * description.  Runs asynchronously on `stream`; never reads outside the
  * container or writes outside out_dev[0..n).  A corrupt stream or index
@@ -154,7 +182,7 @@ afx_status afx_parse_header(const uint8_t* header_host, uint64_t bytes, afx_desc
  * read is that page's load path over the link without the staging copy.
  * Errors: AFX_E_ARG (null or misaligned pointers, pageable host memory),
  * AFX_E_FORMAT (desc), AFX_E_CUDA (launch). */
-afx_status afx_decode(const afx_desc* desc, const void* container_dev, uint16_t* out_dev,
+afx_status afx_decode(const afx_desc* desc, const void* container_dev, void* out_dev,
                       afx_stream_t stream, int32_t* status_dev);
 
 /* Restores several containers in one launch: outs_dev[i] gets the weights
@@ -165,7 +193,7 @@ afx_status afx_decode(const afx_desc* desc, const void* container_dev, uint16_t*
  * Cites: as afx_decode; and "Memory requirements of language model
  * inference on a consumer GPU", section "Loading one part of the model at a
  * time" -- a layer's weights are needed together. */
-afx_status afx_decode_batch(const afx_desc* descs, const void* const* containers_dev, uint16_t* const* outs_dev,
+afx_status afx_decode_batch(const afx_desc* descs, const void* const* containers_dev, void* const* outs_dev,
                             uint32_t count, afx_stream_t stream, int32_t* status_dev);
 
 /* Device workspace (bytes) that afx_decode_gemv needs for this container
@@ -181,8 +209,8 @@ afx_status afx_decode_gemv_workspace(const afx_desc* desc, uint32_t batch, uint6
  * to global memory.  Products and sums are float32; y_dev is float32
  * [batch][rows], overwritten, and bitwise reproducible run to run.
  * workspace_dev: afx_decode_gemv_workspace bytes of device memory, 16-byte
- * aligned, contents ignored.  Requires cols >= 64, x_dev 16-byte aligned,
- * and the container in device memory.
+ * aligned, contents ignored.  Requires a BF16 container in device memory,
+ * cols >= 64 and x_dev 16-byte aligned.
  * Cites: same passage as afx_decode -- the restored weights feed the
  * computation directly.
  * Errors: AFX_E_ARG (shape, batch, alignment), AFX_E_NOSPACE (workspace),
@@ -234,14 +262,14 @@ typedef enum afx_op_kind { AFX_OP_DECODE = 0, AFX_OP_GEMV = 1 } afx_op_kind;
 typedef struct afx_op {
     afx_desc desc;          /* the tensor's container description */
     uint64_t offset;        /* byte offset of its container inside the layer blob (multiple of 256) */
-    uint32_t kind;          /* afx_op_kind */
+    uint32_t kind;          /* afx_op_kind (AFX_OP_GEMV needs a BF16 container) */
     uint32_t rows, cols;    /* AFX_OP_GEMV: weight shape */
     uint32_t batch;         /* AFX_OP_GEMV: 1..4 */
     const uint16_t* x_dev;  /* AFX_OP_GEMV: [batch][cols] BF16 */
-    void* out_dev;          /* AFX_OP_DECODE: uint16[n];  AFX_OP_GEMV: float[batch][rows] */
+    void* out_dev;          /* AFX_OP_DECODE: n elements of desc.format;  AFX_OP_GEMV: float[batch][rows] */
     void* workspace_dev;    /* AFX_OP_GEMV */
     uint64_t workspace_bytes;
-    void* out_host;         /* AFX_OP_DECODE, optional: pinned host uint16[n] that receives out_dev */
+    void* out_host;         /* AFX_OP_DECODE, optional: pinned host buffer of n elements that receives out_dev */
 } afx_op;
 
 typedef struct afx_layer {
@@ -288,7 +316,7 @@ afx_status afx_stream_run(const afx_layer* layers, uint32_t n_layers, void* cons
  * No counterpart on the pages: this exists to test the library's own
  * bounded waits.
  * Errors: AFX_E_ARG, AFX_E_FORMAT, AFX_E_CUDA. */
-afx_status afx_test_restore_stalled(const afx_desc* desc, const void* container_dev, uint16_t* out_dev,
+afx_status afx_test_restore_stalled(const afx_desc* desc, const void* container_dev, void* out_dev,
                                     uint32_t wait_polls, afx_stream_t stream, int32_t* status_dev);
 
 /* ---- prefill -------------------------------------------------------------
@@ -300,17 +328,19 @@ afx_status afx_test_restore_stalled(const afx_desc* desc, const void* container_
  * token at a time).  That product is a dense contraction
  * for the tensor cores, and the restore (not HBM) bounds the weights' side:
  * the matrix is restored into scratch memory by the restore kernel, then
- * multiplied by cuBLAS (BF16 inputs, float32 accumulation), and across
- * matrices the restore of the next overlaps the product of the current. */
+ * multiplied by cuBLAS (16-bit inputs, float32 accumulation).  BF16 and
+ * FP16 containers are accepted, with activations of the same format;
+ * E4M3 containers are refused (AFX_E_ARG). */
 
 /* cuBLAS workspace these calls hand to cuBLAS (caller-owned device memory). */
 #define AFX_PREFILL_GEMM_WORKSPACE_BYTES (32u << 20)
 
 /* y_dev[t][r] = sum_c W[r][c] * x_dev[t][c] for t < n_tokens: W the
  * container's weights as [rows][cols] (rows * cols == n, row-major, as
- * afx_decode_gemv), x_dev BF16 [n_tokens][cols], y_dev float32
- * [n_tokens][rows] (overwritten).  w_scratch_dev: rows * cols BF16 of
- * device memory that receives the restored W (16-byte aligned).
+ * afx_decode_gemv), x_dev [n_tokens][cols] in the container's format (BF16
+ * or FP16), y_dev float32 [n_tokens][rows] (overwritten).  w_scratch_dev:
+ * rows * cols 16-bit elements of device memory that receives the restored
+ * W (16-byte aligned).
  * gemm_workspace_dev: AFX_PREFILL_GEMM_WORKSPACE_BYTES of device memory.
  * Enqueues the restore and the product on `stream`.  The first call on a
  * host thread creates that thread's cuBLAS handle for the device (cuBLAS

@@ -51,3 +51,25 @@ def within_gemv_tolerance(y: np.ndarray, y_ref: np.ndarray, A: np.ndarray, rel: 
     err = np.abs(y.astype(np.float64) - y_ref.astype(np.float64))
     bound = rel * A + np.abs(y_ref.astype(np.float64)) * 2.0 ** -23
     return bool(np.all(err <= bound))
+
+
+def gpu_decode_any(afx, container: np.ndarray, desc, out_pad: int = 0, out_offset: int = 0, host: bool = False):
+    """gpu_decode for any element format (uint16 out for BF16 / FP16, uint8 for
+    E4M3); host=True keeps the container in pinned host memory (zero copy)."""
+    import torch
+    e4m3 = desc.format == afx.AFX_FMT_E4M3
+    src = torch.from_numpy(np.ascontiguousarray(container))
+    src = src.pin_memory() if host else src.cuda()
+    total = desc.n + out_offset + out_pad
+    guard = 0x5A if e4m3 else 0x5A5A
+    out = torch.full((max(total, 1),), guard, dtype=torch.uint8 if e4m3 else torch.int16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    view = out[out_offset:out_offset + desc.n]
+    afx.afx_decode(desc, src, view if desc.n else out, status_dev=status)
+    torch.cuda.synchronize()
+    host_out = out.cpu().numpy()
+    if not e4m3:
+        host_out = host_out.view(np.uint16)
+    guards = np.concatenate([host_out[:out_offset], host_out[out_offset + desc.n:total]])
+    intact = bool((guards == guard).all())
+    return host_out[out_offset:out_offset + desc.n].copy(), int(status.item()), intact

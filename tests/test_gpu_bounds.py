@@ -1,6 +1,6 @@
 """The bounds-checked build (AFX_DEBUG_BOUNDS=1, libafx_debug.so) on the
 restore path: across ragged sizes, the 12-bit-table path, long codes, host
-containers, the fused GEMV and corrupt containers, no range a kernel
+containers, E4M3 and FP16 elements, the fused GEMV and corrupt containers, no range a kernel
 touches ever leaves its buffer.  The check runs in a child process that
 loads the debug library; compute-sanitizer is not available here."""
 import json
@@ -25,11 +25,13 @@ statuses = []
 
 def restore(c, d, host=False):
     cont = torch.from_numpy(c).cuda() if not host else torch.from_numpy(c).pin_memory()
-    out = torch.empty(max(d.n, 1), dtype=torch.int16, device="cuda")
+    e4m3 = d.format == afx.AFX_FMT_E4M3
+    out = torch.empty(max(d.n, 1), dtype=torch.uint8 if e4m3 else torch.int16, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     afx.afx_decode(d, cont, out[:d.n] if d.n else out, status_dev=st)
     torch.cuda.synchronize()
-    return out[:d.n].cpu().numpy().view(np.uint16), int(st.item())
+    got = out[:d.n].cpu().numpy()
+    return (got if e4m3 else got.view(np.uint16)), int(st.item())
 
 for n in (1, 1000, 65_537, 3_000_017):
     w = synth.normal(n, seed=n)
@@ -45,6 +47,16 @@ for T in (4, 32):
 w = synth.normal(500_000, seed=5)
 got, st = restore(*afx.encode(w), host=True)
 statuses.append(("host", w.size, st, bool(np.array_equal(got, w))))
+for n in (1, 17, 999_999):  # E4M3: raw nibbles, byte outputs
+    w = synth.normal_e4m3(n, seed=n)
+    got, st = restore(*afx.encode(w, fmt=afx.AFX_FMT_E4M3))
+    statuses.append(("e4m3", n, st, bool(np.array_equal(got, w))))
+w = synth.normal_e4m3(300_001, seed=8)
+got, st = restore(*afx.encode(w, fmt=afx.AFX_FMT_E4M3), host=True)
+statuses.append(("e4m3 host", w.size, st, bool(np.array_equal(got, w))))
+w = synth.normal_fp16(300_001, seed=8)
+got, st = restore(*afx.encode(w, fmt=afx.AFX_FMT_FP16))
+statuses.append(("fp16", w.size, st, bool(np.array_equal(got, w))))
 # corrupt containers: must be flagged, never read or write out of range
 rng = np.random.default_rng(9)
 w = synth.normal(400_000, seed=6)

@@ -134,3 +134,76 @@ def test_gemv_workspace_size(afx):
         assert afx.afx_decode_gemv_workspace(d, b) >= d.n_blocks * 2 * b * 4
     with pytest.raises(afx.AfxError):
         afx.afx_decode_gemv_workspace(d, 5)
+
+
+# ---- other element formats -------------------------------------------------------
+
+FMT_CASES = {
+    "fp16_normal": (1, lambda: synth.normal_fp16(300_001, seed=11)),
+    "fp16_all_patterns": (1, synth.all_bf16_patterns),
+    "fp16_norm_vector": (1, lambda: synth.normal_fp16(5120, 1.0, 0.05, seed=12)),
+    "fp16_single": (1, lambda: np.full(333, 0x3C00, np.uint16)),
+    "e4m3_normal": (2, lambda: synth.normal_e4m3(300_001, seed=13)),
+    "e4m3_all_patterns": (2, lambda: np.resize(synth.all_e4m3_patterns(), 1027)),
+    "e4m3_single": (2, lambda: np.resize(np.array([0x38, 0xB9, 0x3F], np.uint8), 501)),
+    "e4m3_tiny_odd": (2, lambda: np.array([0x38, 0xC1, 0x3C, 0x30, 0x3E], np.uint8)),
+    "e4m3_empty": (2, lambda: np.zeros(0, np.uint8)),
+}
+
+
+@pytest.mark.parametrize("case", sorted(FMT_CASES))
+@pytest.mark.parametrize("T", [0, 4, 16])
+def test_format_container_is_byte_identical_to_the_oracle(afx, case, T):
+    fmt, gen = FMT_CASES[case]
+    w = gen()
+    code = afx.afx_build_code_fmt(w, fmt)
+    assert code.format == fmt
+    hist = oracle.histogram(w, fmt)
+    assert np.array_equal(np.array(code.count[:], np.uint64), hist)
+    lens = np.array(code.len[:], np.uint8)
+    assert _cost(hist, lens) == _cost(hist, oracle.code_lengths(hist, 24))
+    desc = afx.afx_encode_bound(w.size, code, T, 256)
+    assert desc.format == fmt
+    c = afx.afx_encode(w, code, desc)
+    ref = oracle.encode(w, lens, desc.chunk_bytes, 256, fmt=fmt)
+    assert np.array_equal(c, ref)
+    out, st = oracle.decode(c)
+    assert st == oracle.OK and np.array_equal(out, w)
+    assert afx.desc_dict(afx.afx_parse_header(c)) == afx.desc_dict(desc)
+
+
+def test_format_rejections(afx):
+    w = synth.normal_e4m3(10_000, seed=14)
+    c, d = afx.encode(w, fmt=afx.AFX_FMT_E4M3)
+    # a code length for a symbol E4M3 cannot produce, an out-of-range fill, an unknown format
+    for off, val in ((256 + 16, 3), (108, 3)):
+        bad = c.copy()
+        bad[off] = val
+        with pytest.raises(afx.AfxError):
+            afx.afx_parse_header(bad)
+    one = np.full(64, 0x38, np.uint8)
+    c1, d1 = afx.encode(one, fmt=afx.AFX_FMT_E4M3)
+    assert d1.nsym == 1 and d1.fill == 7
+    bad = c1.copy()
+    bad[104] = 16
+    with pytest.raises(afx.AfxError):
+        afx.afx_parse_header(bad)
+    # the code and the plan must agree on the format
+    code16 = afx.afx_build_code_fmt(synth.normal_fp16(1000, seed=1), afx.AFX_FMT_FP16)
+    desc16 = afx.afx_encode_bound(1000, code16)
+    desc16.format = afx.AFX_FMT_BF16
+    with pytest.raises(afx.AfxError):
+        afx.afx_encode(synth.normal_fp16(1000, seed=1), code16, desc16)
+    with pytest.raises(afx.AfxError):
+        afx.afx_build_code_fmt(np.zeros(4, np.uint16), 7)
+    # an E4M3 container's raw section is one nibble per element
+    assert d.off_chunk - d.off_sm >= (w.size + 1) // 2 and d.off_chunk - d.off_sm < (w.size + 1) // 2 + 256
+
+
+def test_bf16_containers_are_unchanged_by_the_format_field(afx):
+    # format 0 leaves header byte 108 zero: a BF16 container is the same bytes as before the field
+    w = synth.normal(20_000, seed=15)
+    c, d = afx.encode(w)
+    assert d.format == afx.AFX_FMT_BF16 and not c[108:112].any()
+    c2, d2 = afx.encode(w, fmt=afx.AFX_FMT_BF16)
+    assert np.array_equal(c, c2)

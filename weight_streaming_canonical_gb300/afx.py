@@ -35,6 +35,7 @@ AFX_BLOCK_CAPACITY = 32768
 AFX_HEADER_BYTES = 512
 AFX_STATIC_WORKSPACE_BYTES = 4 << 20
 AFX_OP_DECODE, AFX_OP_GEMV = 0, 1
+AFX_FMT_BF16, AFX_FMT_FP16, AFX_FMT_E4M3 = 0, 1, 2
 
 
 class afx_code(ctypes.Structure):
@@ -45,7 +46,7 @@ class afx_code(ctypes.Structure):
         ("nsym", ctypes.c_uint32),
         ("max_len", ctypes.c_uint32),
         ("fill", ctypes.c_uint32),
-        ("reserved", ctypes.c_uint32),
+        ("format", ctypes.c_uint32),
     ]
 
 
@@ -66,7 +67,7 @@ class afx_desc(ctypes.Structure):
         ("max_len", ctypes.c_uint32),
         ("nsym", ctypes.c_uint32),
         ("fill", ctypes.c_uint32),
-        ("reserved", ctypes.c_uint32),
+        ("format", ctypes.c_uint32),
         ("len", ctypes.c_uint8 * 256),
     ]
 
@@ -99,6 +100,7 @@ class afx_layer(ctypes.Structure):
 
 _vp, _u32, _u64, _i32p = ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_void_p
 _lib.afx_build_code.argtypes = [_vp, _u64, _u32, ctypes.POINTER(afx_code)]
+_lib.afx_build_code_fmt.argtypes = [_vp, _u64, _u32, _u32, ctypes.POINTER(afx_code)]
 _lib.afx_encode_bound.argtypes = [_u64, ctypes.POINTER(afx_code), _u32, _u32, ctypes.POINTER(afx_desc)]
 _lib.afx_encode.argtypes = [_vp, _u64, ctypes.POINTER(afx_code), ctypes.POINTER(afx_desc), _vp, _u64]
 _lib.afx_parse_header.argtypes = [_vp, _u64, ctypes.POINTER(afx_desc)]
@@ -138,7 +140,7 @@ _lib.afx_last_error.argtypes = []
 _lib.afx_last_error.restype = ctypes.c_char_p
 _lib.afx_status_string.argtypes = [ctypes.c_int]
 _lib.afx_status_string.restype = ctypes.c_char_p
-for _f in (_lib.afx_build_code, _lib.afx_encode_bound, _lib.afx_encode, _lib.afx_parse_header, _lib.afx_decode,
+for _f in (_lib.afx_build_code, _lib.afx_build_code_fmt, _lib.afx_encode_bound, _lib.afx_encode, _lib.afx_parse_header, _lib.afx_decode,
            _lib.afx_decode_batch, _lib.afx_decode_gemv_workspace, _lib.afx_decode_gemv, _lib.afx_decode_gemv_batch,
            _lib.afx_decode_gemv_static, _lib.afx_stream_run, _lib.afx_test_restore_stalled,
            _lib.afx_plan_residency, _lib.afx_debug_bounds_report, _lib.afx_prefill, _lib.afx_prefill_batch):
@@ -169,6 +171,25 @@ def _host_u16(w) -> np.ndarray:
     if a.dtype != np.uint16:
         raise TypeError(f"expected BF16 bit patterns as uint16, got {a.dtype}")
     return a
+
+
+def element_bytes(fmt: int) -> int:
+    """Bytes per element of a format: 2 for BF16 and FP16, 1 for E4M3."""
+    return 1 if fmt == AFX_FMT_E4M3 else 2
+
+
+def _host_elems(w, fmt: int) -> np.ndarray:
+    a = np.ascontiguousarray(w).reshape(-1)
+    want = np.uint8 if fmt == AFX_FMT_E4M3 else np.uint16
+    if a.dtype != want:
+        raise TypeError(f"expected {np.dtype(want).name} bit patterns for format {fmt}, got {a.dtype}")
+    return a
+
+
+def _check_out(desc: afx_desc, out) -> None:
+    if out.numel() * out.element_size() < desc.n * element_bytes(desc.format) or \
+            out.element_size() != element_bytes(desc.format):
+        raise ValueError(f"the output must hold n elements of {element_bytes(desc.format)} bytes")
 
 
 def _dev_ptr(t) -> int:
@@ -204,6 +225,13 @@ def afx_build_code(w, max_len: int = AFX_MAX_CODE_LEN) -> afx_code:
     return code
 
 
+def afx_build_code_fmt(w, fmt: int, max_len: int = AFX_MAX_CODE_LEN) -> afx_code:
+    a = _host_elems(w, fmt)
+    code = afx_code()
+    _check("afx_build_code_fmt", _lib.afx_build_code_fmt(a.ctypes.data, a.size, fmt, max_len, ctypes.byref(code)))
+    return code
+
+
 def afx_encode_bound(n: int, code: afx_code, chunk_bytes: int = 0, block_chunks: int = 0) -> afx_desc:
     d = afx_desc()
     _check("afx_encode_bound", _lib.afx_encode_bound(n, ctypes.byref(code), chunk_bytes, block_chunks, ctypes.byref(d)))
@@ -211,7 +239,7 @@ def afx_encode_bound(n: int, code: afx_code, chunk_bytes: int = 0, block_chunks:
 
 
 def afx_encode(w, code: afx_code, desc: afx_desc, out: np.ndarray | None = None) -> np.ndarray:
-    a = _host_u16(w)
+    a = _host_elems(w, desc.format)
     if out is None:
         out = np.empty(desc.container_bytes, np.uint8)
     if out.dtype != np.uint8 or not out.flags["C_CONTIGUOUS"]:
@@ -229,9 +257,9 @@ def afx_parse_header(container) -> afx_desc:
 
 
 def afx_decode(desc: afx_desc, container_dev, out_dev, stream=None, status_dev=None) -> None:
-    """out_dev: CUDA tensor of n 16-bit elements (uint16/int16/bfloat16)."""
-    if out_dev.numel() < desc.n or out_dev.element_size() != 2:
-        raise ValueError("out_dev must hold n 16-bit elements")
+    """out_dev: CUDA (or pinned host) tensor of n elements of the container's format:
+    16-bit (uint16/int16/bfloat16/float16) for BF16 and FP16, 8-bit (uint8) for E4M3."""
+    _check_out(desc, out_dev)
     _check("afx_decode", _lib.afx_decode(ctypes.byref(desc), _buf_ptr(container_dev), _buf_ptr(out_dev),
                                           _stream_handle(stream), _dev_ptr(status_dev)))
 
@@ -253,8 +281,7 @@ def afx_decode_batch(descs, containers_dev, outs_dev, stream=None, status_dev=No
     if not (len(descs) == len(containers_dev) == len(outs_dev)):
         raise ValueError("descs, containers_dev and outs_dev must have the same length")
     for d, o in zip(descs, outs_dev):
-        if o.numel() < d.n or o.element_size() != 2:
-            raise ValueError("every output must hold n 16-bit elements")
+        _check_out(d, o)
     arr = (afx_desc * len(descs))(*descs)
     bufs_in = (ctypes.c_void_p * len(containers_dev))(*[_buf_ptr(t) for t in containers_dev])
     bufs_out = (ctypes.c_void_p * len(outs_dev))(*[_buf_ptr(t) for t in outs_dev])
@@ -329,12 +356,13 @@ def afx_stream_run(layers, dev_bufs, buf_bytes: int, compute_stream=None, copy_s
 
 def afx_prefill(desc: afx_desc, container_dev, rows: int, cols: int, x_dev, y_dev, w_scratch_dev, gemm_workspace_dev,
                 stream=None, status_dev=None) -> None:
-    """y_dev[t] = W x_dev[t] for every token t: x_dev BF16 [n_tokens][cols], y_dev float32 [n_tokens][rows]."""
+    """y_dev[t] = W x_dev[t] for every token t: x_dev [n_tokens][cols] in the container's format (BF16 or
+    FP16), y_dev float32 [n_tokens][rows]."""
     n_tokens = x_dev.shape[0]
     if x_dev.numel() != n_tokens * cols or y_dev.numel() != n_tokens * rows:
         raise ValueError("x_dev must be [n_tokens][cols] and y_dev [n_tokens][rows]")
     if w_scratch_dev.numel() * w_scratch_dev.element_size() < 2 * rows * cols:
-        raise ValueError("w_scratch_dev must hold rows * cols BF16")
+        raise ValueError("w_scratch_dev must hold rows * cols 16-bit elements")
     _check("afx_prefill", _lib.afx_prefill(ctypes.byref(desc), _dev_ptr(container_dev), rows, cols, _dev_ptr(x_dev),
                                             n_tokens, _dev_ptr(y_dev), _dev_ptr(w_scratch_dev),
                                             _dev_ptr(gemm_workspace_dev), _stream_handle(stream), _dev_ptr(status_dev)))
@@ -379,10 +407,11 @@ def afx_debug_bounds_report() -> tuple[int, bool]:
 
 # ---- conveniences over the entry points ---------------------------------------
 
-def encode(w, chunk_bytes: int = 0, max_len: int = AFX_MAX_CODE_LEN) -> tuple[np.ndarray, afx_desc]:
-    """Container (uint8 numpy) and its description for the BF16 patterns w."""
-    a = _host_u16(w)
-    code = afx_build_code(a, max_len)
+def encode(w, chunk_bytes: int = 0, max_len: int = AFX_MAX_CODE_LEN, fmt: int = AFX_FMT_BF16) -> tuple[np.ndarray, afx_desc]:
+    """Container (uint8 numpy) and its description for the element patterns w
+    (uint16 for BF16 and FP16, uint8 for E4M3)."""
+    a = _host_elems(w, fmt)
+    code = afx_build_code_fmt(a, fmt, max_len)
     desc = afx_encode_bound(a.size, code, chunk_bytes, 0)
     return afx_encode(a, code, desc), desc
 

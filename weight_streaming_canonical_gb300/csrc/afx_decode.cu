@@ -111,7 +111,7 @@ struct TensorArgs {
     uint64_t sub_begin;        // warp GEMV: first sub-tile of this tensor in the launch's sub-tile list
     uint32_t chunk_bytes;      // T
     uint32_t rows_per_warp;    // GEMV: capacity of the per-warp partial table
-    uint16_t* out;             // restore: n BF16
+    void* out;                 // restore: n elements (uint16 BF16 / FP16, uint8 E4M3)
     const uint16_t* x;         // GEMV: [B][cols]
     float* y;                  // GEMV: [B][rows]
     float* ws;                 // GEMV: [n_blocks][2][B]
@@ -129,7 +129,7 @@ struct LaunchArgs {
     uint32_t wait_limit;       // polls of a staging wait before it gives up (0: kWaitLimit)
     uint32_t stall;            // failure injection for tests: arm the staging barriers, issue no copies
     uint32_t host_src;         // restore: the containers are in pinned host memory (restore_store_host_kernel)
-    uint32_t pad;
+    uint32_t e4m3;             // restore: E4M3 containers (raw nibbles, byte outputs)
     int32_t* status;
     TensorArgs t[kMaxTensors];
 };
@@ -278,6 +278,28 @@ __device__ __forceinline__ uint4 join8(uint2 r8, uint2 s8) {
 // One weight from a rotated exponent r and its sign|mantissa byte s.
 __device__ __forceinline__ uint16_t join1(uint32_t r, uint32_t s) {
     return static_cast<uint16_t>((((r & 0x7Fu) | (s & 0x80u)) << 8) | (s & 0x7Fu) | (r & 0x80u));
+}
+
+// E4M3 elements: byte = sign << 7 | e << 3 | mantissa, from the rotated
+// exponent R (e = R rotated back left by one; e < 16, so e << 3 stays in its
+// byte) and the raw nibble sign << 3 | mantissa.  Four at a time: r4 holds
+// four R bytes, n4 four nibbles (one per byte).
+__device__ __forceinline__ uint32_t e4m3_join4(uint32_t r4, uint32_t n4) {
+    const uint32_t e4 = ((r4 << 1) & 0xFEFEFEFEu) | ((r4 >> 7) & 0x01010101u);
+    return ((n4 & 0x08080808u) << 4) | (e4 << 3) | (n4 & 0x07070707u);
+}
+
+// Sixteen E4M3 elements from their 16 rotated exponents (two uint2) and
+// their 8 raw bytes (element 2k in the low nibble of byte k).
+__device__ __forceinline__ uint4 e4m3_join16(uint2 ra, uint2 rb, uint2 raw) {
+    const uint32_t lo0 = raw.x & 0x0F0F0F0Fu, hi0 = (raw.x >> 4) & 0x0F0F0F0Fu;
+    const uint32_t lo1 = raw.y & 0x0F0F0F0Fu, hi1 = (raw.y >> 4) & 0x0F0F0F0Fu;
+    return make_uint4(e4m3_join4(ra.x, __byte_perm(lo0, hi0, 0x5140)), e4m3_join4(ra.y, __byte_perm(lo0, hi0, 0x7362)),
+                      e4m3_join4(rb.x, __byte_perm(lo1, hi1, 0x5140)), e4m3_join4(rb.y, __byte_perm(lo1, hi1, 0x7362)));
+}
+
+__device__ __forceinline__ uint8_t e4m3_join1(uint32_t r, uint32_t nib) {
+    return static_cast<uint8_t>(e4m3_join4(r & 0xFFu, nib & 0xFu) & 0xFFu);
 }
 
 // ---- decode tables ---------------------------------------------------------------
@@ -1363,17 +1385,52 @@ __device__ __forceinline__ void warp_gemv(const uint8_t* stage, const TensorArgs
     }
 }
 
-// What warp_run does with a decoded sub-tile: store the BF16 weights, or
-// the fused GEMV above.
+// Joins and stores `count` E4M3 elements from o0 with the 32 lanes of a
+// warp; the rotated exponent of element o is at stage[o - (o0 & ~7)] and its
+// raw nibble in byte o / 2 of raw.  Groups of 16 elements (one 16-byte
+// store, 8 raw bytes) start at multiples of 16; the first and last group may
+// be shared with neighbouring ranges and go out byte by byte (lanes 0-15
+// and 16-31), the full groups between one per lane at a time.
+__device__ __forceinline__ void warp_store_e4m3(const uint8_t* stage, const uint8_t* raw, uint8_t* out, uint64_t o0,
+                                                uint32_t count, int lane) {
+    const uint64_t g0 = o0 & ~uint64_t(15);
+    const uint32_t d = static_cast<uint32_t>((o0 & ~uint64_t(7)) - g0);  // stage index of g0 + i is i - d
+    const uint8_t* rawg = raw + g0 / 2;
+    uint8_t* outg = out + g0;
+    const uint32_t a = static_cast<uint32_t>(o0 - g0), b = a + count;  // the range, relative to g0
+    const uint32_t f0 = (a + 15) & ~15u, f1 = b & ~15u;              // full groups [f0, f1)
+    const uint32_t r = lane < 16 ? static_cast<uint32_t>(lane) : f1 + static_cast<uint32_t>(lane - 16);
+    const bool mine = lane < 16 ? (r >= a && r < b && r < f0) : (r >= f0 && r < b);
+    if (mine) outg[r] = e4m3_join1(stage[r - d], rawg[r >> 1] >> ((r & 1u) * 4));
+    for (uint32_t q = f0 + 16 * lane; q < f1; q += 16 * 32) {
+        const uint2 ra = *reinterpret_cast<const uint2*>(stage + q - d);
+        const uint2 rb = *reinterpret_cast<const uint2*>(stage + q - d + 8);
+        __stcs(reinterpret_cast<uint4*>(outg + q), e4m3_join16(ra, rb, __ldg(reinterpret_cast<const uint2*>(rawg + q / 2))));
+    }
+}
+
+// What warp_run does with a decoded sub-tile: store the 16-bit elements
+// (BF16 or FP16: the same bit split), store E4M3 elements, or the fused
+// GEMV above.  kNibbles: the raw section holds a nibble per element.
 struct StoreEpilogue {
+    static constexpr bool kNibbles = false;
     __device__ __forceinline__ void operator()(const uint8_t* stage, const TensorArgs& t, uint64_t, uint64_t o0,
                                                uint32_t count, bool ok, int lane) const {
-        if (ok && count) warp_store(stage, t.sm, t.out, o0, count, lane);
+        if (ok && count) warp_store(stage, t.sm, static_cast<uint16_t*>(t.out), o0, count, lane);
+    }
+};
+
+struct StoreE4M3Epilogue {
+    static constexpr bool kNibbles = true;
+    __device__ __forceinline__ void operator()(const uint8_t* stage, const TensorArgs& t, uint64_t, uint64_t o0,
+                                               uint32_t count, bool ok, int lane) const {
+        if (ok && count) warp_store_e4m3(stage, t.sm, static_cast<uint8_t*>(t.out), o0, count, lane);
     }
 };
 
 template <int B>
 struct GemvEpilogue {
+    static constexpr bool kNibbles = false;
     __device__ __forceinline__ void operator()(const uint8_t* stage, const TensorArgs& t, uint64_t s, uint64_t o0,
                                                uint32_t count, bool ok, int lane) const {
         warp_gemv<B>(stage, t, s, o0, count, ok, lane);
@@ -1469,9 +1526,14 @@ __device__ __forceinline__ bool warp_run(const TabView& tv, WarpSlot& ws, uint8_
         if (lane == 0) {
             if (!in_range)
                 raise_status(status, AFX_DEV_BAD_BLOCK);
-            else if (o0 < o1 && !host_src) {  // the sign|mantissa bytes are needed after the decode
-                const uint64_t a0 = o0 & ~uint64_t(15), a1 = (o1 + 15) & ~uint64_t(15);
-                prefetch_l2(sm + a0, static_cast<uint32_t>(a1 - a0));
+            else if (o0 < o1 && !host_src) {  // the raw bytes are needed after the decode
+                if constexpr (Epi::kNibbles) {
+                    const uint64_t a0 = (o0 >> 1) & ~uint64_t(15), a1 = (((o1 + 1) >> 1) + 15) & ~uint64_t(15);
+                    prefetch_l2(sm + a0, static_cast<uint32_t>(a1 - a0));
+                } else {
+                    const uint64_t a0 = o0 & ~uint64_t(15), a1 = (o1 + 15) & ~uint64_t(15);
+                    prefetch_l2(sm + a0, static_cast<uint32_t>(a1 - a0));
+                }
             }
         }
         const uint32_t next = static_cast<uint32_t>(lane) + 1 < nexist ? ws.chunk[buf][lane + 1] : 0u;
@@ -1600,6 +1662,18 @@ __global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
     restore_warps<true>(a, StoreEpilogue{});
 }
 
+// The restore of E4M3 containers (raw nibbles, one byte per element), from
+// device memory and from pinned host memory.
+__global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
+    restore_store_e4m3_kernel(const __grid_constant__ LaunchArgs a) {
+    restore_warps<false>(a, StoreE4M3Epilogue{});
+}
+
+__global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
+    restore_store_e4m3_host_kernel(const __grid_constant__ LaunchArgs a) {
+    restore_warps<true>(a, StoreE4M3Epilogue{});
+}
+
 template <int B>
 __global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1) restore_gemv_kernel(const __grid_constant__ LaunchArgs a) {
     restore_warps<false>(a, GemvEpilogue<B>{});
@@ -1687,6 +1761,25 @@ __global__ void fill_store_kernel(const uint8_t* __restrict__ sm, const uint64_t
             __stcs(reinterpret_cast<uint4*>(out + ob), join8(make_uint2(f4, f4), s8));
         } else {
             for (uint64_t o = ob; o < n; ++o) out[o] = join1(ror8(fill), sm[o]);
+        }
+    }
+}
+
+// E4M3 with one exponent for every element: 16 elements (8 raw bytes) per
+// group; the ragged last group goes out element by element.
+__global__ void fill_store_e4m3_kernel(const uint8_t* __restrict__ raw, const uint64_t* __restrict__ block_index,
+                                       uint32_t fill, uint64_t n, uint8_t* __restrict__ out, int32_t* status) {
+    if (blockIdx.x == 0 && threadIdx.x == 0 && block_index[0] != n) raise_status(status, AFX_DEV_BAD_BLOCK);
+    const uint64_t groups = (n + 15) >> 4;
+    const uint32_t f4 = ror8(fill) * 0x01010101u;
+    for (uint64_t g = blockIdx.x * static_cast<uint64_t>(blockDim.x) + threadIdx.x; g < groups;
+         g += static_cast<uint64_t>(gridDim.x) * blockDim.x) {
+        const uint64_t ob = g << 4;
+        if (ob + 16 <= n) {
+            const uint2 r8 = __ldg(reinterpret_cast<const uint2*>(raw + (ob >> 1)));
+            __stcs(reinterpret_cast<uint4*>(out + ob), e4m3_join16(make_uint2(f4, f4), make_uint2(f4, f4), r8));
+        } else {
+            for (uint64_t o = ob; o < n; ++o) out[o] = e4m3_join1(ror8(fill), raw[o >> 1] >> ((o & 1u) * 4));
         }
     }
 }
@@ -1925,15 +2018,13 @@ afx_status launch_restore(LaunchArgs& la, cudaStream_t s) {
         const afx_status st = warp_launch_config(la, &warps, &smem);
         if (st != AFX_OK) return st;
         int per_sm = 0;
-        const void* func = la.host_src ? reinterpret_cast<const void*>(restore_store_host_kernel)
-                                       : reinterpret_cast<const void*>(restore_store_kernel);
-        const afx_status pst = prepare_kernel(func, warps * 32, smem, &per_sm);
+        void (*const kernels[2][2])(LaunchArgs) = {{restore_store_kernel, restore_store_host_kernel},
+                                                    {restore_store_e4m3_kernel, restore_store_e4m3_host_kernel}};
+        void (*const kernel)(LaunchArgs) = kernels[la.e4m3 ? 1 : 0][la.host_src ? 1 : 0];
+        const afx_status pst = prepare_kernel(reinterpret_cast<const void*>(kernel), warps * 32, smem, &per_sm);
         if (pst != AFX_OK) return pst;
         const uint64_t grid = std::min<uint64_t>(la.total_tiles, static_cast<uint64_t>(sms) * per_sm);
-        if (la.host_src)
-            restore_store_host_kernel<<<static_cast<unsigned>(grid), warps * 32, smem, s>>>(la);
-        else
-            restore_store_kernel<<<static_cast<unsigned>(grid), warps * 32, smem, s>>>(la);
+        kernel<<<static_cast<unsigned>(grid), warps * 32, smem, s>>>(la);
         AFX_CUDA_TRY(cudaGetLastError(), "restore_store_kernel launch");
         return AFX_OK;
     } else {
@@ -1988,7 +2079,7 @@ namespace {
 
 // afx_decode_batch; stall_polls != 0 is the failure injection of
 // afx_test_restore_stalled.
-afx_status decode_batch(const afx_desc* descs, const void* const* containers, uint16_t* const* outs, uint32_t count,
+afx_status decode_batch(const afx_desc* descs, const void* const* containers, void* const* outs, uint32_t count,
                         afx_stream_t stream, int32_t* status, uint32_t stall_polls) {
     if (count && (!descs || !containers || !outs)) return afx_fail(AFX_E_ARG, "null array", 0);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -2002,15 +2093,18 @@ afx_status decode_batch(const afx_desc* descs, const void* const* containers, ui
         if (d.nsym >= 2 && d.block_chunks != static_cast<uint32_t>(kThreads))
             return afx_fail(AFX_E_ARG, "the decoder runs 512 chunks per block", 0);
     }
-    LaunchArgs lists[2];  // device-resident containers, host-resident containers
-    for (int h = 0; h < 2; ++h) {
-        LaunchArgs& la = lists[h];
-        std::memset(&la, 0, sizeof la);
-        la.status = status;
-        la.wait_limit = stall_polls;
-        la.stall = stall_polls != 0;
-        la.host_src = static_cast<uint32_t>(h);
-    }
+    // [16-bit elements, E4M3][device-resident containers, host-resident containers]
+    LaunchArgs lists[2][2];
+    for (int f = 0; f < 2; ++f)
+        for (int h = 0; h < 2; ++h) {
+            LaunchArgs& la = lists[f][h];
+            std::memset(&la, 0, sizeof la);
+            la.status = status;
+            la.wait_limit = stall_polls;
+            la.stall = stall_polls != 0;
+            la.host_src = static_cast<uint32_t>(h);
+            la.e4m3 = static_cast<uint32_t>(f);
+        }
     for (uint32_t i = 0; i < count; ++i) {
         const afx_desc& d = descs[i];
         if (d.n == 0) continue;
@@ -2020,14 +2114,21 @@ afx_status decode_batch(const afx_desc* descs, const void* const* containers, ui
             return afx_fail(AFX_E_ARG, "container and output must be device memory or pinned host memory", 0);
         if (stall_polls && wc != Where::device)
             return afx_fail(AFX_E_ARG, "the stalled test restore needs a device-resident container", 0);
-        LaunchArgs& la = lists[wc == Where::host ? 1 : 0];
+        const bool e4m3 = d.format == AFX_FMT_E4M3;
+        LaunchArgs& la = lists[e4m3 ? 1 : 0][wc == Where::host ? 1 : 0];
         if (d.nsym == 1) {
             const int sms = sm_count();
             if (sms <= 0) return afx_fail(AFX_E_CUDA, "cannot query the SM count", 0);
-            const uint64_t groups = (d.n + 7) / 8;
+            const uint64_t groups = e4m3 ? (d.n + 15) / 16 : (d.n + 7) / 8;
             const uint64_t blocks = std::min<uint64_t>((groups + 255) / 256, static_cast<uint64_t>(sms) * 8);
-            fill_store_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-                base + d.off_sm, reinterpret_cast<const uint64_t*>(base + d.off_block), d.fill, d.n, outs[i], status);
+            if (e4m3)
+                fill_store_e4m3_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+                    base + d.off_sm, reinterpret_cast<const uint64_t*>(base + d.off_block), d.fill, d.n,
+                    static_cast<uint8_t*>(outs[i]), status);
+            else
+                fill_store_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+                    base + d.off_sm, reinterpret_cast<const uint64_t*>(base + d.off_block), d.fill, d.n,
+                    static_cast<uint16_t*>(outs[i]), status);
             AFX_CUDA_TRY(cudaGetLastError(), "fill_store_kernel launch");
             continue;
         }
@@ -2043,19 +2144,22 @@ afx_status decode_batch(const afx_desc* descs, const void* const* containers, ui
         la.total_tiles += d.n_blocks;
         la.max_chunk_bytes = std::max(la.max_chunk_bytes, d.chunk_bytes);
     }
-    const afx_status st = launch_restore<0>(lists[0], s);
-    if (st != AFX_OK) return st;
-    return launch_restore<0>(lists[1], s);
+    for (int f = 0; f < 2; ++f)
+        for (int h = 0; h < 2; ++h) {
+            const afx_status st = launch_restore<0>(lists[f][h], s);
+            if (st != AFX_OK) return st;
+        }
+    return AFX_OK;
 }
 
 }  // namespace
 
-extern "C" afx_status afx_decode_batch(const afx_desc* descs, const void* const* containers, uint16_t* const* outs,
+extern "C" afx_status afx_decode_batch(const afx_desc* descs, const void* const* containers, void* const* outs,
                                        uint32_t count, afx_stream_t stream, int32_t* status) {
     return decode_batch(descs, containers, outs, count, stream, status, 0);
 }
 
-extern "C" afx_status afx_test_restore_stalled(const afx_desc* desc, const void* container, uint16_t* out,
+extern "C" afx_status afx_test_restore_stalled(const afx_desc* desc, const void* container, void* out,
                                                uint32_t wait_polls, afx_stream_t stream, int32_t* status) {
     if (!desc) return afx_fail(AFX_E_ARG, "null description", 0);
     if (desc->nsym < 2 || desc->n == 0) return afx_fail(AFX_E_ARG, "needs a coded tensor (two or more exponents)", 0);
@@ -2075,7 +2179,7 @@ extern "C" afx_status afx_debug_bounds_report(uint32_t* bits, uint32_t* checked)
     return AFX_OK;
 }
 
-extern "C" afx_status afx_decode(const afx_desc* desc, const void* container, uint16_t* out, afx_stream_t stream,
+extern "C" afx_status afx_decode(const afx_desc* desc, const void* container, void* out, afx_stream_t stream,
                                  int32_t* status) {
     if (!desc) return afx_fail(AFX_E_ARG, "null description", 0);
     if (desc->n && (!container || !out)) return afx_fail(AFX_E_ARG, "null pointer", 0);
@@ -2152,6 +2256,7 @@ extern "C" afx_status afx_decode_gemv_batch(const afx_desc* descs, const void* c
         const afx_status st = afx_check_desc(&d);
         if (st != AFX_OK) return afx_fail(st, "invalid container description", 0);
         if (!containers[i] || !xs[i] || !ys[i]) return afx_fail(AFX_E_ARG, "null pointer", 0);
+        if (d.format != AFX_FMT_BF16) return afx_fail(AFX_E_ARG, "the fused GEMV takes BF16 containers", 0);
         if (rows[i] == 0 || cols[i] < 64 || static_cast<uint64_t>(rows[i]) * cols[i] != d.n)
             return afx_fail(AFX_E_ARG, "rows * cols must equal n, with cols >= 64", 0);
         if (!aligned(containers[i], 16) || !aligned(xs[i], 16))

@@ -1,5 +1,7 @@
-// Host side of afx: exponent histogram, length-limited canonical code,
-// container planning, bit packing and header validation.
+// Host side of afx: symbol histogram, length-limited canonical code,
+// container planning, bit packing and header validation.  BF16 is the
+// pages' format; FP16 and E4M3 share the container (the element format
+// fixes which bits are coded and which are stored raw; see afx.h).
 //
 // The operation: "Why Weight Offloading Slows Inference", section
 // "Lossless compression: fewer bytes to read, more work to unpack" --
@@ -116,12 +118,34 @@ void canonical_codes(const uint8_t len[256], uint32_t code[256]) {
     }
 }
 
+bool format_ok(uint32_t fmt) { return fmt == AFX_FMT_BF16 || fmt == AFX_FMT_FP16 || fmt == AFX_FMT_E4M3; }
+
+// Symbols a format's elements can produce: 256 for the 16-bit formats, 16
+// for E4M3 (its 4-bit exponent).
+unsigned symbol_range(uint32_t fmt) { return fmt == AFX_FMT_E4M3 ? 16u : 256u; }
+
+uint64_t raw_bytes(uint32_t fmt, uint64_t n) { return fmt == AFX_FMT_E4M3 ? (n + 1) / 2 : n; }
+
+// BF16 and FP16 share one bit split: bits 14..7 are coded (BF16's exponent;
+// FP16's exponent and its 3 leading fraction bits), the sign and bits 6..0
+// are the raw byte.  E4M3: bits 6..3 (the exponent) are coded, the sign and
+// bits 2..0 are the raw nibble.
+inline unsigned symbol_of(uint32_t fmt, unsigned v) { return fmt == AFX_FMT_E4M3 ? (v >> 3) & 0xFu : (v >> 7) & 0xFFu; }
+
+inline unsigned raw_of(uint32_t fmt, unsigned v) {
+    return fmt == AFX_FMT_E4M3 ? ((v >> 4) & 0x8u) | (v & 0x7u) : ((v >> 8) & 0x80u) | (v & 0x7Fu);
+}
+
+inline unsigned element(const void* elems, uint32_t fmt, uint64_t i) {
+    return fmt == AFX_FMT_E4M3 ? static_cast<const uint8_t*>(elems)[i] : static_cast<const uint16_t*>(elems)[i];
+}
+
 bool geometry_ok(uint32_t T, uint32_t C) {
     bool t_ok = T == 4 || T == 8 || T == 16 || T == 32 || T == 64;
     return t_ok && C >= 32 && C <= 1024 && C % 32 == 0;
 }
 
-void layout(uint64_t n, uint64_t total_bits, uint32_t T, uint32_t C, afx_desc* d) {
+void layout(uint64_t n, uint32_t fmt, uint64_t total_bits, uint32_t T, uint32_t C, afx_desc* d) {
     d->n = n;
     d->total_bits = total_bits;
     d->chunk_bytes = T;
@@ -132,7 +156,8 @@ void layout(uint64_t n, uint64_t total_bits, uint32_t T, uint32_t C, afx_desc* d
     d->off_exp = AFX_HEADER_BYTES;
     d->exp_bytes = round_up(d->n_chunks * T, 16) + 16;
     d->off_sm = round_up(d->off_exp + d->exp_bytes, 256);
-    d->off_chunk = round_up(d->off_sm + n, 256);
+    d->off_chunk = round_up(d->off_sm + raw_bytes(fmt, n), 256);
+    d->format = fmt;
     d->off_block = round_up(d->off_chunk + 2 * d->n_chunks, 256);
     d->container_bytes = round_up(d->off_block + 8 * (d->n_blocks + 1), 256);
 }
@@ -155,14 +180,25 @@ const char* afx_status_string(afx_status s) {
 }
 
 afx_status afx_build_code(const uint16_t* w, uint64_t n, uint32_t max_len, afx_code* out) {
-    if (!out || (n && !w)) return AFX_E_ARG;
+    return afx_build_code_fmt(w, n, AFX_FMT_BF16, max_len, out);
+}
+
+afx_status afx_build_code_fmt(const void* w, uint64_t n, uint32_t fmt, uint32_t max_len, afx_code* out) {
+    if (!out || (n && !w) || !format_ok(fmt)) return AFX_E_ARG;
     std::memset(out, 0, sizeof(*out));
+    out->format = fmt;
     const unsigned workers = worker_count(n);
     std::vector<std::vector<uint64_t>> part(workers, std::vector<uint64_t>(256, 0));
     auto count_range = [&](unsigned k) {
         uint64_t lo = n * k / workers, hi = n * (k + 1) / workers;
         uint64_t* h = part[k].data();
-        for (uint64_t i = lo; i < hi; ++i) ++h[(w[i] >> 7) & 0xFFu];
+        if (fmt == AFX_FMT_E4M3) {
+            const uint8_t* e = static_cast<const uint8_t*>(w);
+            for (uint64_t i = lo; i < hi; ++i) ++h[(e[i] >> 3) & 0xFu];
+        } else {
+            const uint16_t* e = static_cast<const uint16_t*>(w);
+            for (uint64_t i = lo; i < hi; ++i) ++h[(e[i] >> 7) & 0xFFu];
+        }
     };
     if (workers == 1) {
         count_range(0);
@@ -187,7 +223,9 @@ afx_status afx_build_code(const uint16_t* w, uint64_t n, uint32_t max_len, afx_c
 }
 
 afx_status afx_encode_bound(uint64_t n, const afx_code* code, uint32_t T, uint32_t C, afx_desc* out) {
-    if (!code || !out) return AFX_E_ARG;
+    if (!code || !out || !format_ok(code->format)) return AFX_E_ARG;
+    for (unsigned s = symbol_range(code->format); s < 256; ++s)
+        if (code->len[s] || code->count[s]) return AFX_E_ARG;
     if (C == 0) C = AFX_DECODE_THREADS;
     uint64_t total_bits = 0, present = 0;
     unsigned min_len = 255;
@@ -210,7 +248,7 @@ afx_status afx_encode_bound(uint64_t n, const afx_code* code, uint32_t T, uint32
     if (!geometry_ok(T, C)) return AFX_E_ARG;
     if (8ull * T * C > static_cast<uint64_t>(AFX_BLOCK_CAPACITY) * min_len) return AFX_E_ARG;
     std::memset(out, 0, sizeof(*out));
-    layout(n, total_bits, T, C, out);
+    layout(n, code->format, total_bits, T, C, out);
     out->nsym = code->nsym;
     out->fill = code->nsym == 1 ? code->fill : 0;
     out->max_len = code->nsym >= 2 ? code->max_len : 0;
@@ -218,13 +256,15 @@ afx_status afx_encode_bound(uint64_t n, const afx_code* code, uint32_t T, uint32
     return AFX_OK;
 }
 
-afx_status afx_encode(const uint16_t* w, uint64_t n, const afx_code* code, const afx_desc* d, uint8_t* dst,
+afx_status afx_encode(const void* w, uint64_t n, const afx_code* code, const afx_desc* d, uint8_t* dst,
                       uint64_t dst_bytes) {
     if (!code || !d || !dst || (n && !w)) return AFX_E_ARG;
     if (d->n != n || !geometry_ok(d->chunk_bytes, d->block_chunks)) return AFX_E_ARG;
+    const uint32_t fmt = d->format;
+    if (!format_ok(fmt) || code->format != fmt) return AFX_E_ARG;
     if (dst_bytes < d->container_bytes) return AFX_E_NOSPACE;
     afx_desc check;
-    layout(n, d->total_bits, d->chunk_bytes, d->block_chunks, &check);
+    layout(n, fmt, d->total_bits, d->chunk_bytes, d->block_chunks, &check);
     if (check.container_bytes != d->container_bytes || check.off_block != d->off_block) return AFX_E_ARG;
     if (std::memcmp(d->len, code->len, 256) != 0) return AFX_E_ARG;
     std::memset(dst, 0, d->container_bytes);
@@ -248,14 +288,19 @@ afx_status afx_encode(const uint16_t* w, uint64_t n, const afx_code* code, const
     put_le(h + 96, 4, d->max_len);
     put_le(h + 100, 4, d->nsym);
     put_le(h + 104, 4, d->fill);
+    put_le(h + 108, 4, fmt);
     std::memcpy(h + 256, code->len, 256);
 
     uint8_t* sm = dst + d->off_sm;
-    for (uint64_t i = 0; i < n; ++i) sm[i] = static_cast<uint8_t>(((w[i] >> 8) & 0x80u) | (w[i] & 0x7Fu));
+    if (fmt == AFX_FMT_E4M3) {
+        for (uint64_t i = 0; i < n; ++i) sm[i / 2] |= static_cast<uint8_t>(raw_of(fmt, element(w, fmt, i)) << (4 * (i & 1)));
+    } else {
+        for (uint64_t i = 0; i < n; ++i) sm[i] = static_cast<uint8_t>(raw_of(fmt, element(w, fmt, i)));
+    }
 
     if (d->nsym <= 1) {
         for (uint64_t i = 0; i < n; ++i)
-            if (((w[i] >> 7) & 0xFFu) != d->fill) return AFX_E_ARG;
+            if (symbol_of(fmt, element(w, fmt, i)) != d->fill) return AFX_E_ARG;
         if (d->total_bits != 0) return AFX_E_ARG;
         put_le(dst + d->off_block, 8, n);
         return AFX_OK;
@@ -275,7 +320,7 @@ afx_status afx_encode(const uint16_t* w, uint64_t n, const afx_code* code, const
         if (cur_chunk != ~uint64_t{0}) put_le(chunk_index + 2 * cur_chunk, 2, cur_gap | (cur_count << 5));
     };
     for (uint64_t i = 0; i < n; ++i) {
-        const unsigned e = (w[i] >> 7) & 0xFFu;
+        const unsigned e = symbol_of(fmt, element(w, fmt, i));
         const unsigned l = code->len[e];
         if (l == 0) return AFX_E_ARG;
         const uint64_t chunk = pos >> chunk_shift;
@@ -321,12 +366,14 @@ afx_status afx_parse_header(const uint8_t* h, uint64_t bytes, afx_desc* out) {
     const uint32_t T = static_cast<uint32_t>(get_le(h + 24, 4)), C = static_cast<uint32_t>(get_le(h + 28, 4));
     if (!geometry_ok(T, C)) return AFX_E_FORMAT;
     if (n > (uint64_t{1} << 48) || total_bits > 24 * n) return AFX_E_FORMAT;
-    layout(n, total_bits, T, C, &d);
+    const uint32_t fmt = static_cast<uint32_t>(get_le(h + 108, 4));
+    if (!format_ok(fmt)) return AFX_E_FORMAT;
+    layout(n, fmt, total_bits, T, C, &d);
     if (get_le(h + 32, 8) != d.n_chunks || get_le(h + 40, 8) != d.n_blocks || get_le(h + 48, 8) != d.off_exp ||
         get_le(h + 56, 8) != d.exp_bytes || get_le(h + 64, 8) != d.off_sm || get_le(h + 72, 8) != d.off_chunk ||
         get_le(h + 80, 8) != d.off_block || get_le(h + 88, 8) != d.container_bytes)
         return AFX_E_FORMAT;
-    for (unsigned i = 108; i < 256; ++i)
+    for (unsigned i = 112; i < 256; ++i)
         if (h[i]) return AFX_E_FORMAT;
     d.max_len = static_cast<uint32_t>(get_le(h + 96, 4));
     d.nsym = static_cast<uint32_t>(get_le(h + 100, 4));
@@ -336,6 +383,7 @@ afx_status afx_parse_header(const uint8_t* h, uint64_t bytes, afx_desc* out) {
     uint64_t kraft = 0;
     for (int s = 0; s < 256; ++s) {
         if (d.len[s] > AFX_MAX_CODE_LEN) return AFX_E_FORMAT;
+        if (d.len[s] && static_cast<unsigned>(s) >= symbol_range(fmt)) return AFX_E_FORMAT;
         if (d.len[s]) {
             ++coded;
             kraft += uint64_t{1} << (AFX_MAX_CODE_LEN - d.len[s]);
@@ -351,7 +399,7 @@ afx_status afx_parse_header(const uint8_t* h, uint64_t bytes, afx_desc* out) {
             if (d.len[s]) min_len = std::min<unsigned>(min_len, d.len[s]);
         if (8ull * T * C > static_cast<uint64_t>(AFX_BLOCK_CAPACITY) * min_len) return AFX_E_FORMAT;
     } else {
-        if (coded != 0 || total_bits != 0 || d.fill > 255) return AFX_E_FORMAT;
+        if (coded != 0 || total_bits != 0 || d.fill >= symbol_range(fmt)) return AFX_E_FORMAT;
         if (d.nsym == 0 && (n != 0 || d.fill != 0)) return AFX_E_FORMAT;
         if (d.nsym == 1 && n == 0) return AFX_E_FORMAT;
     }
@@ -363,8 +411,9 @@ afx_status afx_check_desc(const afx_desc* d) {
     if (!d) return AFX_E_ARG;
     if (!geometry_ok(d->chunk_bytes, d->block_chunks)) return AFX_E_FORMAT;
     if (d->n > (uint64_t{1} << 48) || d->total_bits > 24 * d->n) return AFX_E_FORMAT;
+    if (!format_ok(d->format)) return AFX_E_FORMAT;
     afx_desc L;
-    layout(d->n, d->total_bits, d->chunk_bytes, d->block_chunks, &L);
+    layout(d->n, d->format, d->total_bits, d->chunk_bytes, d->block_chunks, &L);
     if (L.n_chunks != d->n_chunks || L.n_blocks != d->n_blocks || L.off_exp != d->off_exp ||
         L.exp_bytes != d->exp_bytes || L.off_sm != d->off_sm || L.off_chunk != d->off_chunk ||
         L.off_block != d->off_block || L.container_bytes != d->container_bytes)
@@ -373,6 +422,7 @@ afx_status afx_check_desc(const afx_desc* d) {
     uint64_t kraft = 0;
     for (int s = 0; s < 256; ++s) {
         if (d->len[s] > AFX_MAX_CODE_LEN) return AFX_E_FORMAT;
+        if (d->len[s] && static_cast<unsigned>(s) >= symbol_range(d->format)) return AFX_E_FORMAT;
         if (d->len[s]) {
             ++coded;
             kraft += uint64_t{1} << (AFX_MAX_CODE_LEN - d->len[s]);
@@ -387,7 +437,7 @@ afx_status afx_check_desc(const afx_desc* d) {
         if (8ull * d->chunk_bytes * d->block_chunks > static_cast<uint64_t>(AFX_BLOCK_CAPACITY) * min_len)
             return AFX_E_FORMAT;
     } else {
-        if (coded != 0 || d->total_bits != 0 || d->fill > 255) return AFX_E_FORMAT;
+        if (coded != 0 || d->total_bits != 0 || d->fill >= symbol_range(d->format)) return AFX_E_FORMAT;
         if (d->nsym == 1 && d->n == 0) return AFX_E_FORMAT;
         if (d->nsym == 0 && d->n != 0) return AFX_E_FORMAT;
     }

@@ -7,7 +7,7 @@
 // tensor cores, while the weights' side is bounded by the restore, which is
 // limited by its instruction rate rather than by HBM.  So the matrix is
 // restored into scratch memory by the restore kernel and multiplied by
-// cuBLAS (BF16 inputs, float32 accumulation).  A list of matrices is either
+// cuBLAS (BF16 or FP16 inputs, float32 accumulation).  A list of matrices is either
 // pipelined (the restore of the next on its own stream while the current one
 // is multiplied, ordered by CUDA events only) or restored in one launch and
 // then multiplied: the restore kernel holds a whole SM per CTA, so where it
@@ -56,6 +56,8 @@ afx_status check_product(const afx_desc& d, const void* container, uint32_t rows
                          const uint16_t* x, uint32_t n_tokens, const float* y) {
     const afx_status st = afx_check_desc(&d);
     if (st != AFX_OK) return afx_fail(st, "invalid container description", 0);
+    if (d.format != AFX_FMT_BF16 && d.format != AFX_FMT_FP16)
+        return afx_fail(AFX_E_ARG, "prefill takes BF16 or FP16 containers", 0);
     if (!container || !x || !y) return afx_fail(AFX_E_ARG, "null pointer", 0);
     if (rows == 0 || cols == 0 || n_tokens == 0 || static_cast<uint64_t>(rows) * cols != d.n)
         return afx_fail(AFX_E_ARG, "rows * cols must equal n and n_tokens must be positive", 0);
@@ -66,15 +68,17 @@ afx_status check_product(const afx_desc& d, const void* container, uint32_t rows
 }
 
 // y[t][r] = sum_c w[r][c] x[t][c]: in cuBLAS's column-major terms
-// y^T (rows x n) = (w as cols x rows)^T * (x as cols x n).
+// y^T (rows x n) = (w as cols x rows)^T * (x as cols x n).  w and x are
+// both BF16 or both FP16 (the container's format).
 afx_status product(cublasHandle_t h, const uint16_t* w, const uint16_t* x, float* y, uint32_t rows, uint32_t cols,
-                   uint32_t n_tokens, void* workspace, cudaStream_t s) {
+                   uint32_t n_tokens, uint32_t format, void* workspace, cudaStream_t s) {
+    const cudaDataType_t type = format == AFX_FMT_FP16 ? CUDA_R_16F : CUDA_R_16BF;
     AFX_PF_CUBLAS(cublasSetStream(h, s), "cublasSetStream");
     AFX_PF_CUBLAS(cublasSetWorkspace(h, workspace, AFX_PREFILL_GEMM_WORKSPACE_BYTES), "cublasSetWorkspace");
     const float alpha = 1.0f, beta = 0.0f;
     AFX_PF_CUBLAS(cublasGemmEx(h, CUBLAS_OP_T, CUBLAS_OP_N, static_cast<int>(rows), static_cast<int>(n_tokens),
-                               static_cast<int>(cols), &alpha, w, CUDA_R_16BF, static_cast<int>(cols), x,
-                               CUDA_R_16BF, static_cast<int>(cols), &beta, y, CUDA_R_32F, static_cast<int>(rows),
+                               static_cast<int>(cols), &alpha, w, type, static_cast<int>(cols), x, type,
+                               static_cast<int>(cols), &beta, y, CUDA_R_32F, static_cast<int>(rows),
                                CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT),
                   "cublasGemmEx");
     return AFX_OK;
@@ -109,7 +113,7 @@ extern "C" afx_status afx_prefill(const afx_desc* desc, const void* container_de
     if (st != AFX_OK) return st;
     st = afx_decode(desc, container_dev, w_scratch_dev, stream, status_dev);
     if (st != AFX_OK) return st;
-    return product(h, w_scratch_dev, x_dev, y_dev, rows, cols, n_tokens, gemm_workspace_dev,
+    return product(h, w_scratch_dev, x_dev, y_dev, rows, cols, n_tokens, desc->format, gemm_workspace_dev,
                    reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -135,7 +139,7 @@ extern "C" afx_status afx_prefill_batch(const afx_desc* descs, const void* const
     if (!w_scratch_dev[1]) {
         // every matrix restored in one launch into w_scratch_dev[0] (back to
         // back, each at a 256-byte boundary), then the products in order
-        std::vector<uint16_t*> outs(count);
+        std::vector<void*> outs(count);
         uint64_t off = 0;
         for (uint32_t i = 0; i < count; ++i) {
             outs[i] = w_scratch_dev[0] + off / 2;
@@ -144,7 +148,8 @@ extern "C" afx_status afx_prefill_batch(const afx_desc* descs, const void* const
         st = afx_decode_batch(descs, containers_dev, outs.data(), count, gemm_stream, status_dev);
         if (st != AFX_OK) return st;
         for (uint32_t i = 0; i < count; ++i) {
-            st = product(h, outs[i], xs_dev[i], ys_dev[i], rows[i], cols[i], n_tokens, gemm_workspace_dev, gs);
+            st = product(h, static_cast<const uint16_t*>(outs[i]), xs_dev[i], ys_dev[i], rows[i], cols[i], n_tokens,
+                         descs[i].format, gemm_workspace_dev, gs);
             if (st != AFX_OK) return st;
         }
         return AFX_OK;
@@ -162,7 +167,8 @@ extern "C" afx_status afx_prefill_batch(const afx_desc* descs, const void* const
         if (st != AFX_OK) return st;
         AFX_PF_CUDA(cudaEventRecord(restored.ev[i], rs), "cudaEventRecord");
         AFX_PF_CUDA(cudaStreamWaitEvent(gs, restored.ev[i], 0), "cudaStreamWaitEvent");
-        st = product(h, w_scratch_dev[k], xs_dev[i], ys_dev[i], rows[i], cols[i], n_tokens, gemm_workspace_dev, gs);
+        st = product(h, w_scratch_dev[k], xs_dev[i], ys_dev[i], rows[i], cols[i], n_tokens, descs[i].format,
+                     gemm_workspace_dev, gs);
         if (st != AFX_OK) return st;
         AFX_PF_CUDA(cudaEventRecord(consumed.ev[k], gs), "cudaEventRecord");
     }

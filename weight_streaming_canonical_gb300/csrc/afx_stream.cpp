@@ -60,6 +60,7 @@ afx_status check_layer(const afx_layer& L, uint64_t buf_bytes) {
             if (op.desc.n && !op.out_dev) return AFX_E_ARG;
         } else if (op.kind == AFX_OP_GEMV) {
             if (!op.x_dev || !op.out_dev || op.batch < 1 || op.batch > 4) return AFX_E_ARG;
+            if (op.desc.format != AFX_FMT_BF16) return AFX_E_ARG;
             if (static_cast<uint64_t>(op.rows) * op.cols != op.desc.n) return AFX_E_ARG;
         } else {
             return AFX_E_ARG;
@@ -85,8 +86,8 @@ afx_status run_group(const afx_op* ops, uint32_t count, uint8_t* buf, afx_stream
         containers[i] = buf + ops[i].offset;
     }
     if (ops[0].kind == AFX_OP_DECODE) {
-        std::vector<uint16_t*> outs(count);
-        for (uint32_t i = 0; i < count; ++i) outs[i] = static_cast<uint16_t*>(ops[i].out_dev);
+        std::vector<void*> outs(count);
+        for (uint32_t i = 0; i < count; ++i) outs[i] = ops[i].out_dev;
         return afx_decode_batch(descs.data(), containers.data(), outs.data(), count, stream, status_dev);
     }
     std::vector<uint32_t> rows(count), cols(count);
@@ -161,7 +162,8 @@ extern "C" afx_status afx_stream_run(const afx_layer* layers, uint32_t n_layers,
             for (uint32_t i = 0; i < L.n_ops; ++i) {
                 const afx_op& op = L.ops[i];
                 if (op.kind != AFX_OP_DECODE || !op.out_host || op.desc.n == 0) continue;
-                AFX_STREAM_TRY(cudaMemcpyAsync(op.out_host, op.out_dev, op.desc.n * sizeof(uint16_t),
+                const uint64_t bytes = op.desc.format == AFX_FMT_E4M3 ? op.desc.n : op.desc.n * sizeof(uint16_t);
+                AFX_STREAM_TRY(cudaMemcpyAsync(op.out_host, op.out_dev, bytes,
                                                cudaMemcpyDeviceToHost, d2h),
                                "cudaMemcpyAsync");
             }
