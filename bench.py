@@ -50,7 +50,8 @@ def parse_args(argv=None):
     p.add_argument("--no-extras", action="store_true", help="skip e2e and cpu_baseline legs")
     p.add_argument("--workload", default="layer",
                    help="layer (default: one Qwen3-14B-shaped decoder layer), matrix4096, adversarial "
-                        "(2^28 heavy-tailed), or tensor:<name> (one tensor of the layer)")
+                        "(2^28 heavy-tailed), tensor:<name> (one tensor of the layer), layer-fp16 or layer-e4m3 "
+                        "(the layer in the other element formats)")
     return p.parse_args(argv)
 
 
@@ -85,12 +86,12 @@ def max_over_ranks(v: float, world: int) -> float:
     return float(t.item())
 
 
-def job_throughput(weights_per_rank: int, world: int, ms_max: float) -> tuple[float, float]:
+def job_throughput(weights_per_rank: int, world: int, ms_max: float, elem_bytes: int = 2) -> tuple[float, float]:
     """Whole-job decoded GB/s and weights/s: every rank restores its own
     copy of the workload (weak scaling); the slowest rank's time counts."""
     total = weights_per_rank * world
     sec = ms_max * 1e-3
-    return 2 * total / sec / 1e9, total / sec
+    return elem_bytes * total / sec / 1e9, total / sec
 
 
 # ---- workload ------------------------------------------------------------------------
@@ -100,7 +101,28 @@ WORKLOADS = {
     "model": "full qwen3-14b-shaped model: 40 layers + embedding and untied LM head 151936x5120, 14.77B BF16 weights",
     "matrix4096": "single 4096x4096 BF16 matrix, N(0,0.02)",
     "adversarial": "2^28 BF16: Student-t(3)*0.01, 1% x100, 5% zeros, subnormals, +-inf, NaN payloads",
+    "layer-fp16": "the qwen3-14b-shaped decoder layer stored as FP16 (same shapes and distributions)",
+    "layer-e4m3": "the qwen3-14b-shaped decoder layer's seven matrices stored as E4M3 with a per-tensor scale",
 }
+
+FMT_OF_WORKLOAD = {"layer-fp16": 1, "layer-e4m3": 2}
+
+
+def fmt_of(parts) -> int:
+    return int(parts[0][3].format) if parts else 0
+
+
+def elem_bytes(fmt: int) -> int:
+    return 1 if fmt == 2 else 2
+
+
+def torch_elem_dtype(fmt: int):
+    import torch
+    return torch.uint8 if fmt == 2 else torch.int16
+
+
+def np_elem_dtype(fmt: int):
+    return np.uint8 if fmt == 2 else np.uint16
 
 
 def build_layer(seed: int, rank: int = 0, workload: str = "layer"):
@@ -117,6 +139,12 @@ def build_layer(seed: int, rank: int = 0, workload: str = "layer"):
     elif workload == "layer":
         gens = {name: (lambda nm=name: synth.layer_tensor(nm, seed=seed, layer=rank))
                 for name, _, _ in synth.LAYER_TENSORS}
+    elif workload == "layer-fp16":
+        gens = {name: (lambda nm=name: synth.layer_tensor_fp16(nm, seed=seed, layer=rank))
+                for name, _, _ in synth.LAYER_TENSORS}
+    elif workload == "layer-e4m3":
+        gens = {name: (lambda nm=name: synth.layer_matrix_e4m3(nm, seed=seed, layer=rank))
+                for name, _, kind in synth.LAYER_TENSORS if kind == "matrix"}
     elif workload == "model":
         gens = {"embed_tokens": lambda: synth.embedding(seed=seed + rank)}
         for layer_index in range(synth.LAYERS):
@@ -127,10 +155,12 @@ def build_layer(seed: int, rank: int = 0, workload: str = "layer"):
     else:
         raise SystemExit(f"unknown workload {workload}")
 
+    fmt = FMT_OF_WORKLOAD.get(workload, 0)
+
     def one(item):
         name, gen = item
         w = np.ascontiguousarray(gen()).reshape(-1)
-        c, d = afx.encode(w)
+        c, d = afx.encode(w, fmt=fmt)
         return name, w, c, d
 
     with cf.ThreadPoolExecutor(min(len(gens), 16)) as ex:
@@ -148,8 +178,9 @@ def exponent_entropy_bits(parts) -> float:
     tensors (each tensor has its own code): the least any exponent code can
     spend, before the chunk and block index."""
     total, n_all = 0.0, 0
-    for _, w, _, _ in parts:
-        counts = np.bincount(((w.reshape(-1) >> 7) & 0xFF).astype(np.intp), minlength=256).astype(np.float64)
+    for _, w, _, d in parts:
+        sym = (w.reshape(-1) >> 3) & 0xF if d.format == 2 else (w.reshape(-1) >> 7) & 0xFF
+        counts = np.bincount(sym.astype(np.intp), minlength=256).astype(np.float64)
         p = counts[counts > 0] / w.size
         total += float(-(p * np.log2(p)).sum()) * w.size
         n_all += w.size
@@ -223,7 +254,7 @@ def profiled_traffic(kernel: str, workload: str):
             sha = hashlib.sha256(f.read()).hexdigest()
     except (OSError, KeyError, ValueError):
         return None
-    if sha != rec.get("source_sha256") or workload != "layer":
+    if sha != rec.get("source_sha256") or workload != rec.get("bench_workload", "layer"):
         return None
     return int(rec["dram_bytes_per_launch"])
 
@@ -247,9 +278,9 @@ def oracle_sample(parts, slice_elems: int = 1 << 24):
     work = []
     for name, w, c, d in parts:
         for s in range(0, w.size, slice_elems):
-            work.append(w[s:s + slice_elems])
+            work.append((w[s:s + slice_elems], int(d.format)))
     with cf.ThreadPoolExecutor(16) as ex:
-        return list(ex.map(lambda a: afx.encode(a)[0], work))
+        return list(ex.map(lambda a: afx.encode(a[0], fmt=a[1])[0], work))
 
 
 def time_oracle(containers, threads: int) -> tuple[float, int]:
@@ -295,7 +326,7 @@ def run_reference(args):
         times.append(dt)
         weights = nw
     sec = sum(times) / len(times)
-    value = 2 * weights / sec / 1e9
+    value = elem_bytes(fmt_of(parts)) * weights / sec / 1e9
     sample = f"{len(per_step)} oracle containers of <= 2^24 weights ({weights} weights) per step, from the layer's {n_total} weights"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
@@ -339,7 +370,8 @@ def run_ours(args):
     for _, _, _, d in parts:
         out_offs.append(oo)
         oo += d.n
-    out = torch.empty(oo, dtype=torch.int16, device=dev)
+    fmt = fmt_of(parts)
+    out = torch.empty(oo, dtype=torch_elem_dtype(fmt), device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     views = [(d, dev_blob[off:off + d.container_bytes], out[oo_:oo_ + d.n])
              for (_, _, _, d), off, oo_ in zip(parts, offs, out_offs)]
@@ -370,7 +402,7 @@ def run_ours(args):
         graph.replay()
     torch.cuda.synchronize()
     for (name, w, _, _), oo_ in zip(parts, out_offs):  # compared on the device, one tensor at a time
-        ref = torch.from_numpy(w.view(np.int16)).to(dev)
+        ref = torch.from_numpy(w.view(np.uint8 if fmt == 2 else np.int16)).to(dev)
         if not torch.equal(out[oo_:oo_ + w.size], ref):
             raise SystemExit(f"restore of {name} is not bit-exact")
         del ref
@@ -412,25 +444,28 @@ def run_ours(args):
     kernel_ms = statistics.median(launch_ms)
     peak, peak_kind = measured_hbm_peak()
     achieved = alg_total / (kernel_ms * 1e-3) / 1e9
+    kernel_name = "restore_store_e4m3_kernel" if fmt == 2 else "restore_store_kernel"
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": profiled_traffic("restore_store_kernel", args.workload),
-                "kernel": "restore_store_kernel", "peak_kind": peak_kind,
+                "traffic": profiled_traffic(kernel_name, args.workload),
+                "kernel": kernel_name, "peak_kind": peak_kind,
                 "launches_per_step": launches_per_step, "algorithmic_bytes_per_step": alg_total,
                 "kernel_ms_per_step": kernel_ms}
 
     sec = ms * 1e-3
-    value, weights_per_s = job_throughput(n_total, world, ms)
+    value, weights_per_s = job_throughput(n_total, world, ms, elem_bytes(fmt))
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "u32",
-        "data": "synthetic: seeded N(0,0.02) BF16 matrices, N(1,0.05) norms, Qwen3-14B layer shapes",
+        "data": {0: "synthetic: seeded N(0,0.02) BF16 matrices, N(1,0.05) norms, Qwen3-14B layer shapes",
+                 1: "synthetic: seeded N(0,0.02) matrices, N(1,0.05) norms rounded to FP16, Qwen3-14B layer shapes",
+                 2: "synthetic: seeded N(0,1) x 448/6 matrices rounded to E4M3, Qwen3-14B layer matrix shapes"}[fmt],
         "config": {"workload": workload_text(args.workload), "weights": n_total, "compressed_bytes": comp_total,
                    "bits_per_weight": 8 * comp_total / n_total,
                    "coded_exponent_bits_per_weight": sum(d.total_bits for *_, d in parts) / n_total,
                    "exponent_entropy_bits_per_weight": exponent_entropy_bits(parts),
                    "l2": "inputs larger than L2: %.0f MB compressed read and %.0f MB written per step"
-                         % (comp_total / 1e6, 2 * n_total / 1e6),
+                         % (comp_total / 1e6, elem_bytes(fmt) * n_total / 1e6),
                    "launch": f"one afx_decode_batch call of {len(views)} tensors ({launches_per_step} kernel launches) "
                              "per step, replayed from a CUDA graph",
                    "parallelism": f"replicas x{world}"},
@@ -473,13 +508,14 @@ def run_e2e(afx, parts, views, dev, args):
     i+1 overlaps the restore of tensor i, and the copy back of tensor i
     (on its own stream) overlaps both."""
     import torch
-    host_out = torch.empty(sum(d.n for _, _, _, d in parts), dtype=torch.int16).pin_memory()
+    fmt = fmt_of(parts)
+    host_out = torch.empty(sum(d.n for _, _, _, d in parts), dtype=torch_elem_dtype(fmt)).pin_memory()
     blobs, ops_all, outs = [], [], []
     o = 0
     for (_, w, c, d) in parts:
         blob = torch.empty(c.size, dtype=torch.uint8).pin_memory()
         blob.numpy()[:] = c
-        out = torch.empty(d.n, dtype=torch.int16, device=dev)
+        out = torch.empty(d.n, dtype=torch_elem_dtype(fmt), device=dev)
         op = afx.afx_op()
         op.desc = d
         op.offset = 0
@@ -512,10 +548,11 @@ def run_e2e(afx, parts, views, dev, args):
     torch.cuda.synchronize()
     ms = start.elapsed_time(end) / steps
     n = sum(d.n for _, _, _, d in parts)
-    ok = all(np.array_equal(host_out.numpy().view(np.uint16)[s:s + w.size], w)
+    eb = elem_bytes(fmt)
+    ok = all(np.array_equal(host_out.numpy().view(np_elem_dtype(fmt))[s:s + w.size], w)
              for s, w in zip(np.cumsum([0] + [w.size for _, w, _, _ in parts])[:-1], [w for _, w, _, _ in parts]))
-    return {"value": 2 * n / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": int(sum(b.numel() for b in blobs)), "d2h_bytes_per_step": 2 * n,
+    return {"value": eb * n / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": int(sum(b.numel() for b in blobs)), "d2h_bytes_per_step": eb * n,
             "bit_exact": bool(ok),
             "path": "afx_stream_run, one tensor per streamed layer: pinned host containers in, BF16 back to pinned "
                     "host on a third stream"}
@@ -528,6 +565,8 @@ def run_zero_copy(afx, parts, dev, args):
     one launch).  Compared with the copy pipeline in e2e."""
     import torch
     n = sum(d.n for _, _, _, d in parts)
+    fmt = fmt_of(parts)
+    eb = elem_bytes(fmt)
     host_c = []
     for (_, _, c, _) in parts:
         t = torch.empty(c.size, dtype=torch.uint8).pin_memory()
@@ -538,9 +577,9 @@ def run_zero_copy(afx, parts, dev, args):
     res = {}
     for where in ("device", "host"):
         if where == "device":
-            outs = [torch.empty(d.n, dtype=torch.int16, device=dev) for d in descs]
+            outs = [torch.empty(d.n, dtype=torch_elem_dtype(fmt), device=dev) for d in descs]
         else:
-            outs = [torch.empty(d.n, dtype=torch.int16).pin_memory() for d in descs]
+            outs = [torch.empty(d.n, dtype=torch_elem_dtype(fmt)).pin_memory() for d in descs]
         stream = torch.cuda.Stream(device=dev)
         with torch.cuda.stream(stream):
             for _ in range(max(3, args.warmup)):
@@ -554,11 +593,11 @@ def run_zero_copy(afx, parts, dev, args):
             e1.record(stream)
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / steps
-        ok = status.item() == 0 and all(np.array_equal(o.cpu().numpy().view(np.uint16), w)
+        ok = status.item() == 0 and all(np.array_equal(o.cpu().numpy().view(np_elem_dtype(fmt)), w)
                                         for o, (_, w, _, _) in zip(outs, parts))
-        res["to_" + where] = {"value": 2 * n / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+        res["to_" + where] = {"value": eb * n / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
                               "link_read_bytes": int(sum(c.numel() for c in host_c)),
-                              "link_write_bytes": 2 * n if where == "host" else 0, "bit_exact": bool(ok)}
+                              "link_write_bytes": eb * n if where == "host" else 0, "bit_exact": bool(ok)}
     res["path"] = ("afx_decode_batch of the layer with its containers in pinned host memory, read by "
                    "restore_store_host_kernel over the host link; to_host also writes the BF16 weights to "
                    "pinned host memory")
@@ -903,7 +942,7 @@ def run_cpu_baseline(parts):
     threads = os.cpu_count() or 1
     dt, nw = time_oracle(sample, threads)
     dt1, nw1 = time_oracle(sample[:1], 1)
-    return {"value": 2 * nw / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+    return {"value": elem_bytes(fmt_of(parts)) * nw / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"{len(sample)} containers of <= 2^24 weights ({nw} weights) from the layer, one per thread",
             "weights_per_s": nw / dt, "one_core_weights_per_s": nw1 / dt1, "cpu": cpu_model()}
 
