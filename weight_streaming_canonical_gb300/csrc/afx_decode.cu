@@ -78,7 +78,10 @@ constexpr int kChunkStage = kThreads + 8;  // chunk entries staged per tile (the
 // Canonical decode tables, built on the host from the 256 code lengths.
 // In 24-bit left-aligned code space all codes of length <= L lie in
 // [0, limit[L]); a 24-bit peek v has the length L = the smallest L with
-// v < limit[L], and its exponent is sorted[base[L] + (v >> (24 - L))].
+// v < limit[L], and its symbol's stage byte is sorted[base[L] + (v >> (24 - L))].
+// Stage bytes are what the merge of the tensor's element format wants: the
+// exponent rotated right by one bit for the 16-bit formats (see ror8), the
+// exponent shifted left by three (its place in the element) for E4M3.
 //
 // The internal nodes of the code tree (the prefixes that are not codes yet)
 // are numbered for the byte-step decoder: depth by depth, prefix value
@@ -280,17 +283,15 @@ __device__ __forceinline__ uint16_t join1(uint32_t r, uint32_t s) {
     return static_cast<uint16_t>((((r & 0x7Fu) | (s & 0x80u)) << 8) | (s & 0x7Fu) | (r & 0x80u));
 }
 
-// E4M3 elements: byte = sign << 7 | e << 3 | mantissa, from the rotated
-// exponent R (e = R rotated back left by one; e < 16, so e << 3 stays in its
-// byte) and the raw nibble sign << 3 | mantissa.  Four at a time: r4 holds
-// four R bytes, n4 four nibbles (one per byte).
-__device__ __forceinline__ uint32_t e4m3_join4(uint32_t r4, uint32_t n4) {
-    const uint32_t e4 = ((r4 << 1) & 0xFEFEFEFEu) | ((r4 >> 7) & 0x01010101u);
-    return ((n4 & 0x08080808u) << 4) | (e4 << 3) | (n4 & 0x07070707u);
+// E4M3 elements: byte = sign << 7 | e << 3 | mantissa, from the stage byte
+// e << 3 and the raw nibble sign << 3 | mantissa.  Four at a time: s4 holds
+// four stage bytes, n4 four nibbles (one per byte).
+__device__ __forceinline__ uint32_t e4m3_join4(uint32_t s4, uint32_t n4) {
+    return ((n4 & 0x08080808u) << 4) | s4 | (n4 & 0x07070707u);
 }
 
-// Sixteen E4M3 elements from their 16 rotated exponents (two uint2) and
-// their 8 raw bytes (element 2k in the low nibble of byte k).
+// Sixteen E4M3 elements from their 16 stage bytes (two uint2) and their 8
+// raw bytes (element 2k in the low nibble of byte k).
 __device__ __forceinline__ uint4 e4m3_join16(uint2 ra, uint2 rb, uint2 raw) {
     const uint32_t lo0 = raw.x & 0x0F0F0F0Fu, hi0 = (raw.x >> 4) & 0x0F0F0F0Fu;
     const uint32_t lo1 = raw.y & 0x0F0F0F0Fu, hi1 = (raw.y >> 4) & 0x0F0F0F0Fu;
@@ -332,7 +333,7 @@ __device__ __forceinline__ void build_tables(S& sh, uint16_t* first /* 8 KB scra
             while (L <= kLutBits && v >= tab.limit[L]) ++L;
             uint16_t e = 0;
             if (L <= kLutBits)
-                e = static_cast<uint16_t>((L << 8) | ror8(tab.sorted[tab.base[L] + static_cast<int32_t>(v >> (24 - L))]));
+                e = static_cast<uint16_t>((L << 8) | tab.sorted[tab.base[L] + static_cast<int32_t>(v >> (24 - L))]);
             first[p] = e;
             sh.len0[p] = static_cast<uint8_t>(e >> 8);
         }
@@ -366,7 +367,7 @@ __device__ __forceinline__ void build_tables(S& sh, uint16_t* first /* 8 KB scra
     __syncthreads();
 }
 
-// One code from a 32-bit window: rotated exponent, length in len (0 on a bad code).
+// One code from a 32-bit window: its stage byte, length in len (0 on a bad code).
 template <class S>
 __device__ __forceinline__ uint32_t decode_one(const S& sh, uint32_t win, uint32_t& len) {
     const uint32_t p = win >> (32 - kLutBits);
@@ -383,7 +384,7 @@ __device__ __forceinline__ uint32_t decode_one(const S& sh, uint32_t win, uint32
         return 0;
     }
     len = L;
-    return ror8(sh.sorted[sh.base[L] + static_cast<int32_t>(v >> (24 - L))]);
+    return sh.sorted[sh.base[L] + static_cast<int32_t>(v >> (24 - L))];
 }
 
 // ---- tile staging ----------------------------------------------------------------
@@ -901,7 +902,7 @@ struct SharedW {
     uint32_t state_base[AFX_MAX_CODE_LEN + 1];
     uint8_t sorted[256];
     uint8_t depth[64];               // depth of each state's node
-    alignas(16) uint16_t first[kLutSize];  // first code of a 12-bit peek: length << 8 | rotated exponent
+    alignas(16) uint16_t first[kLutSize];  // first code of a 12-bit peek: length << 8 | stage byte
     alignas(16) uint8_t tab[16];     // start of the table region
 };
 
@@ -937,7 +938,7 @@ __device__ __forceinline__ uint32_t decode_first(const TabView& tv, uint32_t win
     uint32_t L = kLutBits + 1;
     while (L < AFX_MAX_CODE_LEN && v >= tv.limit[L]) ++L;
     len = L;
-    return ror8(tv.sorted[tv.base[L] + static_cast<int32_t>(v >> (24 - L))]);
+    return tv.sorted[tv.base[L] + static_cast<int32_t>(v >> (24 - L))];
 }
 
 __device__ __forceinline__ uint32_t stream_window(const uint32_t* stream, uint32_t bit) {
@@ -969,7 +970,7 @@ __device__ void build_tables_w(SharedW& sh, uint8_t* tabr, const CodeTables& tab
             while (L <= kLutBits && v >= sh.limit[L]) ++L;
             uint16_t e = 0;
             if (L <= kLutBits)
-                e = static_cast<uint16_t>((L << 8) | ror8(sh.sorted[sh.base[L] + static_cast<int32_t>(v >> (24 - L))]));
+                e = static_cast<uint16_t>((L << 8) | sh.sorted[sh.base[L] + static_cast<int32_t>(v >> (24 - L))]);
             sh.first[p] = e;
         }
     }
@@ -1386,7 +1387,7 @@ __device__ __forceinline__ void warp_gemv(const uint8_t* stage, const TensorArgs
 }
 
 // Joins and stores `count` E4M3 elements from o0 with the 32 lanes of a
-// warp; the rotated exponent of element o is at stage[o - (o0 & ~7)] and its
+// warp; the stage byte of element o is at stage[o - (o0 & ~7)] and its
 // raw nibble in byte o / 2 of raw.  Groups of 16 elements (one 16-byte
 // store, 8 raw bytes) start at multiples of 16; the first and last group may
 // be shared with neighbouring ranges and go out byte by byte (lanes 0-15
@@ -1771,7 +1772,7 @@ __global__ void fill_store_e4m3_kernel(const uint8_t* __restrict__ raw, const ui
                                        uint32_t fill, uint64_t n, uint8_t* __restrict__ out, int32_t* status) {
     if (blockIdx.x == 0 && threadIdx.x == 0 && block_index[0] != n) raise_status(status, AFX_DEV_BAD_BLOCK);
     const uint64_t groups = (n + 15) >> 4;
-    const uint32_t f4 = ror8(fill) * 0x01010101u;
+    const uint32_t f4 = ((fill << 3) & 0xFFu) * 0x01010101u;
     for (uint64_t g = blockIdx.x * static_cast<uint64_t>(blockDim.x) + threadIdx.x; g < groups;
          g += static_cast<uint64_t>(gridDim.x) * blockDim.x) {
         const uint64_t ob = g << 4;
@@ -1779,7 +1780,7 @@ __global__ void fill_store_e4m3_kernel(const uint8_t* __restrict__ raw, const ui
             const uint2 r8 = __ldg(reinterpret_cast<const uint2*>(raw + (ob >> 1)));
             __stcs(reinterpret_cast<uint4*>(out + ob), e4m3_join16(make_uint2(f4, f4), make_uint2(f4, f4), r8));
         } else {
-            for (uint64_t o = ob; o < n; ++o) out[o] = e4m3_join1(ror8(fill), raw[o >> 1] >> ((o & 1u) * 4));
+            for (uint64_t o = ob; o < n; ++o) out[o] = e4m3_join1((fill << 3) & 0xFFu, raw[o >> 1] >> ((o & 1u) * 4));
         }
     }
 }
@@ -1814,6 +1815,9 @@ __global__ void fill_gemv_kernel(const uint8_t* __restrict__ sm, const uint64_t*
 
 // ---- host side ------------------------------------------------------------------------
 
+// The stage byte of symbol s for the merge of format fmt.
+uint32_t stage_byte(uint32_t fmt, uint32_t s) { return fmt == AFX_FMT_E4M3 ? (s << 3) & 0xFFu : ror8(s); }
+
 void make_tables(const afx_desc& d, CodeTables& t) {
     std::memset(&t, 0, sizeof t);
     unsigned count[AFX_MAX_CODE_LEN + 1] = {0};
@@ -1825,7 +1829,7 @@ void make_tables(const afx_desc& d, CodeTables& t) {
         if (L > 1) first = (first + count[L - 1]) << 1;
         const unsigned first_pos = pos;
         for (int s = 0; s < 256; ++s)
-            if (d.len[s] == L) t.sorted[pos++] = static_cast<uint8_t>(s);
+            if (d.len[s] == L) t.sorted[pos++] = static_cast<uint8_t>(stage_byte(d.format, static_cast<uint32_t>(s)));
         t.limit[L] = (first + count[L]) << (AFX_MAX_CODE_LEN - L);
         t.base[L] = static_cast<int32_t>(first_pos) - static_cast<int32_t>(first);
     }
