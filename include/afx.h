@@ -306,6 +306,21 @@ afx_status afx_stream_run(const afx_layer* layers, uint32_t n_layers, void* cons
                           uint64_t buf_bytes, afx_stream_t compute_stream, afx_stream_t copy_stream,
                           afx_stream_t d2h_stream, int32_t* status_dev);
 
+/* Waits on the host until all work queued so far on `stream` has finished,
+ * for at most timeout_ms milliseconds (0: no limit), by recording an event
+ * and polling it; the host thread never blocks inside a CUDA call.  Then,
+ * when status_dev is not NULL (the status word passed to the calls, in
+ * device or pinned host memory), it reads that word behind the queued work
+ * and stores it in *status_out (when not NULL; 0 otherwise).
+ * Returns AFX_OK; AFX_E_CORRUPT when the status word has any AFX_DEV_* bit
+ * set (the outputs of the flagged calls are unspecified); AFX_E_TIMEOUT
+ * when the limit passed first -- nothing is cancelled, the work keeps
+ * running and a later afx_sync can wait for it; AFX_E_CUDA when a CUDA call
+ * failed (afx_last_error names it).
+ * No counterpart on the pages: this is the library's failure detection
+ * (a stream that never finishes becomes an error, not a hung host). */
+afx_status afx_sync(afx_stream_t stream, uint32_t timeout_ms, const int32_t* status_dev, int32_t* status_out);
+
 /* Failure injection for tests of the staging timeout: restores a coded
  * tensor (two or more exponents) as afx_decode, except that every staging
  * barrier is armed with the bytes it expects and no copy is issued.  Each

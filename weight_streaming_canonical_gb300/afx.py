@@ -116,6 +116,8 @@ _lib.afx_decode_gemv_static.argtypes = [ctypes.POINTER(afx_desc), _vp, _u32, _u3
 _lib.afx_stream_run.argtypes = [ctypes.POINTER(afx_layer), _u32, ctypes.POINTER(ctypes.c_void_p), _u32, _u64, _vp,
                                 _vp, _vp, _i32p]
 _lib.afx_test_restore_stalled.argtypes = [ctypes.POINTER(afx_desc), _vp, _vp, _u32, _vp, _i32p]
+_lib.afx_sync.argtypes = [_vp, _u32, _vp, ctypes.POINTER(ctypes.c_int32)]
+_lib.afx_sync.restype = ctypes.c_int
 class afx_plan_tensor(ctypes.Structure):
     _fields_ = [("decoded_bytes", ctypes.c_uint64), ("compressed_bytes", ctypes.c_uint64)]
 
@@ -396,6 +398,17 @@ def afx_plan_residency(tensors, device_budget_bytes: int, link_gbs: float, resto
     _check("afx_plan_residency", _lib.afx_plan_residency(arr, n, int(device_budget_bytes), ctypes.byref(rates), out,
                                                           ctypes.byref(ms), ctypes.byref(res)))
     return [int(v) for v in out[:n]], ms.value, res.value
+
+
+def afx_sync(stream=None, timeout_ms: int = 0, status_dev=None) -> tuple[int, int]:
+    """Bounded host wait for the work queued on `stream`, then the status word.
+    Returns (AFX_OK, 0), (AFX_E_CORRUPT, bits) or (AFX_E_TIMEOUT, 0); raises on a CUDA error."""
+    word = ctypes.c_int32(0)
+    st = _lib.afx_sync(_stream_handle(stream), int(timeout_ms), _buf_ptr(status_dev) if status_dev is not None else None,
+                       ctypes.byref(word))
+    if st not in (AFX_OK, AFX_E_CORRUPT, AFX_E_TIMEOUT):
+        _check("afx_sync", st)
+    return int(st), int(word.value)
 
 
 def afx_debug_bounds_report() -> tuple[int, bool]:
