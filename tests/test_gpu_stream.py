@@ -109,6 +109,45 @@ def test_restored_tensors_copied_back_to_host(afx, own_stream):
         assert np.array_equal(host.numpy().view(np.uint16), w)
 
 
+def test_streamed_mixed_formats_copied_back_to_host(afx):
+    # layers of BF16, FP16 and E4M3 tensors (several per layer, one batch
+    # launch per format), each restored and copied back to pinned host memory
+    import torch
+    gens = [(0, lambda n, s: synth.normal(n, seed=s)), (1, lambda n, s: synth.normal_fp16(n, seed=s)),
+            (2, lambda n, s: synth.normal_e4m3(n, seed=s))]
+    layers, refs = [], []
+    for l in range(4):
+        parts, ops, off = [], [], 0
+        for k, (fmt, gen) in enumerate(gens):
+            w = gen(30_001 + 7_777 * l + 1_111 * k, 60 + 3 * l + k)
+            c, d = afx.encode(w, fmt=fmt)
+            dt = torch.uint8 if fmt == 2 else torch.int16
+            out = torch.empty(d.n, dtype=dt, device="cuda")
+            host = torch.full((d.n,), 0x5A if fmt == 2 else -1, dtype=dt).pin_memory()
+            op = afx.afx_op()
+            op.desc, op.offset, op.kind = d, off, afx.AFX_OP_DECODE
+            op.out_dev, op.out_host = out.data_ptr(), host.data_ptr()
+            parts.append(c)
+            ops.append(op)
+            refs.append((fmt, w, out, host))
+            off += c.size
+        blob = torch.empty(off, dtype=torch.uint8).pin_memory()
+        blob.numpy()[:] = np.concatenate(parts)
+        layers.append((blob, ops))
+    buf_bytes = max(b.numel() for b, _ in layers)
+    bufs = [torch.empty(buf_bytes, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    copy, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    compute = torch.cuda.current_stream()
+    afx.afx_stream_run(layers, bufs, buf_bytes, compute, copy, status_dev=status, d2h_stream=d2h)
+    st, word = afx.afx_sync(d2h, 30_000, status)
+    torch.cuda.synchronize()
+    assert (st, word) == (afx.AFX_OK, 0)
+    for fmt, w, out, host in refs:
+        got = host.numpy()
+        assert np.array_equal(got if fmt == 2 else got.view(np.uint16), w), fmt
+
+
 def test_blob_larger_than_buffer_is_rejected(afx):
     import torch
     blob, metas = _layer(afx, 7, [("decode", (64, 640))])
