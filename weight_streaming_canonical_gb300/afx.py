@@ -412,7 +412,7 @@ def afx_sync(stream=None, timeout_ms: int = 0, status_dev=None) -> tuple[int, in
 
 
 def afx_debug_bounds_report() -> tuple[int, bool]:
-    """(bits of the failed bounds checks since the last call, whether this build checks)."""
+    """(bits of the failed bounds checks since the last call, whether the loaded library checks)."""
     bits, checked = ctypes.c_uint32(), ctypes.c_uint32()
     _check("afx_debug_bounds_report", _lib.afx_debug_bounds_report(ctypes.byref(bits), ctypes.byref(checked)))
     return bits.value, bool(checked.value)
