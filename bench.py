@@ -48,6 +48,9 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-extras", action="store_true", help="skip e2e and cpu_baseline legs")
+    p.add_argument("--legs", default="all",
+                   help="extra legs to run after the headline (comma list of e2e, zero_copy, cpu_baseline, gemv, "
+                        "stream, prefill, formats; default all)")
     p.add_argument("--workload", default="layer",
                    help="layer (default: one Qwen3-14B-shaped decoder layer), matrix4096, adversarial "
                         "(2^28 heavy-tailed), tensor:<name> (one tensor of the layer), layer-fp16 or layer-e4m3 "
@@ -478,23 +481,32 @@ def run_ours(args):
         "clocks": clocks,
     }
 
+    legs = set(args.legs.split(",")) if args.legs != "all" else {
+        "e2e", "zero_copy", "cpu_baseline", "gemv", "stream", "prefill", "formats"}
     if not args.no_extras and rank == 0:
-        line["e2e"] = run_e2e(afx, parts, views, dev, args)
-        line["zero_copy"] = run_zero_copy(afx, parts, dev, args)
-        line["cpu_baseline"] = run_cpu_baseline(parts)
+        if "e2e" in legs:
+            line["e2e"] = run_e2e(afx, parts, views, dev, args)
+        if "zero_copy" in legs:
+            line["zero_copy"] = run_zero_copy(afx, parts, dev, args)
+        if "cpu_baseline" in legs:
+            line["cpu_baseline"] = run_cpu_baseline(parts)
         if args.workload == "layer":
-            line["fused_gemv"] = run_gemv_bench(afx, parts, dev_blob, offs, dev, args)
-            line["streamed_40_layers"] = run_stream_bench(afx, parts, dev, args)
-            # "Why Weight Offloading Slows Inference", Eq. (2): compression pays
-            # when (S - S_disk) / b > t_unpack; here b is the measured link
-            S, S_disk = 2 * n_total, comp_total
-            b = line["streamed_40_layers"]["batch1"]["h2d_gbs"] * 1e9
-            line["eq2_break_even"] = {"S_bytes": S, "S_disk_bytes": S_disk, "b_link_gbs": b / 1e9,
-                                      "read_time_saved_ms": (S - S_disk) / b * 1e3, "t_unpack_ms": ms,
-                                      "pays": (S - S_disk) / b > ms * 1e-3}
-            line["residency_plan"] = run_residency_plan(afx, parts, b / 1e9, value)
-            line["prefill"] = run_prefill_bench(afx, parts, dev_blob, offs, dev, args)
-            line["formats"] = run_formats_bench(afx, dev, args)
+            if "gemv" in legs:
+                line["fused_gemv"] = run_gemv_bench(afx, parts, dev_blob, offs, dev, args, weights_per_s)
+            if "stream" in legs:
+                line["streamed_40_layers"] = run_stream_bench(afx, parts, dev, args)
+                # "Why Weight Offloading Slows Inference", Eq. (2): compression pays
+                # when (S - S_disk) / b > t_unpack; here b is the measured link
+                S, S_disk = 2 * n_total, comp_total
+                b = line["streamed_40_layers"]["batch1"]["h2d_gbs"] * 1e9
+                line["eq2_break_even"] = {"S_bytes": S, "S_disk_bytes": S_disk, "b_link_gbs": b / 1e9,
+                                          "read_time_saved_ms": (S - S_disk) / b * 1e3, "t_unpack_ms": ms,
+                                          "pays": (S - S_disk) / b > ms * 1e-3}
+                line["residency_plan"] = run_residency_plan(afx, parts, b / 1e9, value)
+            if "prefill" in legs:
+                line["prefill"] = run_prefill_bench(afx, parts, dev_blob, offs, dev, args)
+            if "formats" in legs:
+                line["formats"] = run_formats_bench(afx, dev, args)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -810,7 +822,7 @@ def _layer_ops(afx, parts, B, dev, keep):
     return ops
 
 
-def run_gemv_bench(afx, parts, dev_blob, offs, dev, args):
+def run_gemv_bench(afx, parts, dev_blob, offs, dev, args, restore_weights_per_s=None):
     """Fused restore + GEMV over the layer's seven matrices in one launch,
     batch 1 and 4, containers resident in HBM."""
     import torch
@@ -846,9 +858,19 @@ def run_gemv_bench(afx, parts, dev_blob, offs, dev, args):
             e1.record(stream)
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / args.steps
+        # bytes the product must move: the containers' coded bits, sign|mantissa
+        # bytes and indices, x read once, y written once
+        io = comp + sum(2 * B * c + 4 * B * r for r, c in shp)
+        peak, peak_kind = measured_hbm_peak()
         res[f"batch{B}"] = {"ms": ms, "weights_per_s": n / (ms * 1e-3), "compressed_read_gbs": comp / (ms * 1e-3) / 1e9,
+                            "hbm_gbs": io / (ms * 1e-3) / 1e9, "hbm_frac": io / (ms * 1e-3) / 1e9 / peak,
+                            "peak_kind": peak_kind,
+                            "frac_of_restore_rate": (n / (ms * 1e-3)) / restore_weights_per_s
+                            if restore_weights_per_s else None,
                             "launches": "one restore_gemv_kernel<B> and one row fix-up per product batch"}
     res["weights"] = n
+    res["bound"] = ("the decode's instruction rate (the same byte-step decoder as the restore), not HBM: "
+                    "frac_of_restore_rate compares the product's weights/s with the restore's")
     return res
 
 
