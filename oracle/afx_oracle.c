@@ -42,9 +42,10 @@
  *   0 BF16 (16 bits: sign, 8 exponent, 7 mantissa): symbol = exponent;
  *     raw byte = sign << 7 | mantissa.
  *   1 FP16 (IEEE 754 binary16: sign, 5 exponent, 10 fraction): symbol =
- *     exponent << 3 | the 3 leading fraction bits; raw byte = sign << 7 |
- *     the 7 trailing fraction bits.  The symbol takes three fraction bits
- *     so that the raw part stays one byte per element.
+ *     exponent; raw byte = sign << 7 | the 7 trailing fraction bits; the 3
+ *     leading fraction bits go to a second raw section, the "hi" section,
+ *     3 bits per element: element i's bits are section bits 3i .. 3i + 2
+ *     (bit 0 the lowest), and section bit b is bit b % 8 of byte b / 8.
  *   2 E4M3 (OCP 8-bit floating point, E4M3: sign, 4 exponent, 3 mantissa):
  *     symbol = exponent; raw nibble = sign << 3 | mantissa, two per byte,
  *     element 2k in the low nibble of byte k.
@@ -61,11 +62,13 @@
  *    96  u32 longest code length 100  u32 number of present exponents
  *   104  u32 fill exponent (when exactly one exponent is present)
  *   108  u32 element format (0 BF16, 1 FP16, 2 E4M3)
- *   112..255 zero;   256..511 code length of each symbol value 0..255
+ *   112  u64 hi section offset (FP16; 0 for the other formats)
+ *   120..255 zero;   256..511 code length of each symbol value 0..255
  *   exp section: u32 words; stream bit i is bit (31 - i mod 32) of word
  *     floor(i / 32); size = (chunks * T rounded up to 16) + 16 zero bytes.
  *   sm section: the raw bits, one byte per element ((sign << 7) | mantissa
  *     for BF16), or one nibble per element for E4M3 (ceil(n / 2) bytes).
+ *   hi section (FP16 only, after the sm section): ceil(3n / 8) bytes.
  *   chunk index: one u16 per chunk of 8*T stream bits:
  *     bits 0..4  = offset of the first codeword that starts in the chunk,
  *     bits 5..15 = number of codewords that start in the chunk.
@@ -114,7 +117,11 @@ static unsigned orc_elem_bytes(unsigned fmt) { return fmt == ORC_FMT_E4M3 ? 1u :
 
 static uint64_t orc_raw_bytes(unsigned fmt, uint64_t n) { return fmt == ORC_FMT_E4M3 ? (n + 1) / 2 : n; }
 
-static unsigned orc_symbols_of_format(unsigned fmt) { return fmt == ORC_FMT_E4M3 ? 16u : 256u; }
+static unsigned orc_symbols_of_format(unsigned fmt) {
+    return fmt == ORC_FMT_E4M3 ? 16u : fmt == ORC_FMT_FP16 ? 32u : 256u;
+}
+
+static uint64_t orc_hi_bytes(unsigned fmt, uint64_t n) { return fmt == ORC_FMT_FP16 ? (3 * n + 7) / 8 : 0; }
 
 static unsigned orc_read_elem(const void* elems, unsigned fmt, uint64_t i) {
     if (orc_elem_bytes(fmt) == 1) return ((const uint8_t*)elems)[i];
@@ -129,11 +136,7 @@ static void orc_write_elem(void* elems, unsigned fmt, uint64_t i, unsigned v) {
 }
 
 static unsigned orc_symbol_of(unsigned fmt, unsigned v) {
-    if (fmt == ORC_FMT_FP16) {
-        unsigned exponent = (v >> 10) & 0x1Fu;
-        unsigned fraction = v & 0x3FFu;
-        return (exponent << 3) | (fraction >> 7);
-    }
+    if (fmt == ORC_FMT_FP16) return (v >> 10) & 0x1Fu; /* the exponent */
     if (fmt == ORC_FMT_E4M3) return (v >> 3) & 0xFu;
     return orc_exponent_of((uint16_t)v);
 }
@@ -152,11 +155,17 @@ static unsigned orc_raw_of(unsigned fmt, unsigned v) {
     return orc_sign_mantissa_of((uint16_t)v);
 }
 
-static unsigned orc_join_of(unsigned fmt, unsigned symbol, unsigned raw) {
+/* the 3 leading fraction bits of an FP16 element (0 for the other formats) */
+static unsigned orc_hi_of(unsigned fmt, unsigned v) {
+    if (fmt == ORC_FMT_FP16) return ((v & 0x3FFu) >> 7) & 0x7u;
+    return 0;
+}
+
+static unsigned orc_join_of(unsigned fmt, unsigned symbol, unsigned raw, unsigned hi) {
     if (fmt == ORC_FMT_FP16) {
         unsigned sign = (raw >> 7) & 1u;
-        unsigned exponent = symbol >> 3;
-        unsigned fraction = ((symbol & 0x7u) << 7) | (raw & 0x7Fu);
+        unsigned exponent = symbol;
+        unsigned fraction = (hi << 7) | (raw & 0x7Fu);
         return (sign << 15) | (exponent << 10) | fraction;
     }
     if (fmt == ORC_FMT_E4M3) {
@@ -171,6 +180,23 @@ static unsigned orc_join_of(unsigned fmt, unsigned symbol, unsigned raw) {
 static unsigned orc_get_raw(const uint8_t* sm, unsigned fmt, uint64_t i) {
     if (fmt == ORC_FMT_E4M3) return (sm[i / 2] >> (4 * (i % 2))) & 0xFu;
     return sm[i];
+}
+
+/* hi-section bits of element i, one bit at a time */
+static unsigned orc_get_hi(const uint8_t* hi, uint64_t i) {
+    unsigned v = 0;
+    for (unsigned b = 0; b < 3; b++) {
+        uint64_t bit = 3 * i + b;
+        v |= ((hi[bit / 8] >> (bit % 8)) & 1u) << b;
+    }
+    return v;
+}
+
+static void orc_put_hi(uint8_t* hi, uint64_t i, unsigned v) {
+    for (unsigned b = 0; b < 3; b++) {
+        uint64_t bit = 3 * i + b;
+        if ((v >> b) & 1u) hi[bit / 8] = (uint8_t)(hi[bit / 8] | (1u << (bit % 8)));
+    }
 }
 
 /* the section starts zeroed; element i's raw bits are OR-ed in */
@@ -315,7 +341,7 @@ int orc_canonical_codes(const uint8_t len[256], uint32_t code[256]) {
 
 typedef struct {
     uint64_t n, total_bits, n_chunks, n_blocks;
-    uint64_t off_exp, exp_bytes, off_sm, off_chunk, off_block, container_bytes;
+    uint64_t off_exp, exp_bytes, off_sm, off_hi, off_chunk, off_block, container_bytes;
     uint32_t T, C;
 } orc_layout;
 
@@ -337,7 +363,13 @@ static void orc_make_layout(uint64_t n, unsigned fmt, uint64_t total_bits, uint3
     L->off_exp = ORC_HEADER_BYTES;
     L->exp_bytes = orc_round_up(L->n_chunks * T, 16) + 16;
     L->off_sm = orc_round_up(L->off_exp + L->exp_bytes, 256);
-    L->off_chunk = orc_round_up(L->off_sm + orc_raw_bytes(fmt, n), 256);
+    if (fmt == ORC_FMT_FP16) {
+        L->off_hi = orc_round_up(L->off_sm + orc_raw_bytes(fmt, n), 256);
+        L->off_chunk = orc_round_up(L->off_hi + orc_hi_bytes(fmt, n), 256);
+    } else {
+        L->off_hi = 0;
+        L->off_chunk = orc_round_up(L->off_sm + orc_raw_bytes(fmt, n), 256);
+    }
     L->off_block = orc_round_up(L->off_chunk + 2 * L->n_chunks, 256);
     L->container_bytes = orc_round_up(L->off_block + 8 * (L->n_blocks + 1), 256);
 }
@@ -433,6 +465,7 @@ int orc_encode_fmt(const void* elems, uint64_t n, unsigned fmt, const uint8_t le
     orc_put(dst + 100, 4, nsym);
     orc_put(dst + 104, 4, nsym == 1 ? fill : 0);
     orc_put(dst + 108, 4, fmt);
+    orc_put(dst + 112, 8, L.off_hi);
     for (int s = 0; s < 256; s++) dst[256 + s] = len[s];
 
     /* exponent codes, one bit at a time, most significant code bit first;
@@ -459,6 +492,8 @@ int orc_encode_fmt(const void* elems, uint64_t n, unsigned fmt, const uint8_t le
 
     /* raw bits (sign|mantissa bytes for BF16) */
     for (uint64_t i = 0; i < n; i++) orc_put_raw(dst + L.off_sm, fmt, i, orc_raw_of(fmt, orc_read_elem(elems, fmt, i)));
+    if (fmt == ORC_FMT_FP16)
+        for (uint64_t i = 0; i < n; i++) orc_put_hi(dst + L.off_hi, i, orc_hi_of(fmt, orc_read_elem(elems, fmt, i)));
 
     /* chunk index */
     for (uint64_t c = 0; c < L.n_chunks; c++) {
@@ -513,7 +548,8 @@ int orc_decode(const uint8_t* src, uint64_t src_bytes, void* out, uint64_t out_n
         return ORC_E_FORMAT;
     if (src_bytes < L.container_bytes) return ORC_E_FORMAT;
     if (out_n != n) return ORC_E_ARG;
-    for (unsigned i = 112; i < 256; i++)
+    if (orc_get(src + 112, 8) != L.off_hi) return ORC_E_FORMAT;
+    for (unsigned i = 120; i < 256; i++)
         if (src[i] != 0) return ORC_E_FORMAT;
 
     const uint8_t* len = src + 256;
@@ -593,12 +629,18 @@ int orc_decode(const uint8_t* src, uint64_t src_bytes, void* out, uint64_t out_n
             if (found < 0) { status = ORC_E_CORRUPT; break; }
             e = (unsigned)found;
         }
-        orc_write_elem(out, fmt, i, orc_join_of(fmt, e, orc_get_raw(sm, fmt, i)));
+        unsigned hi = fmt == ORC_FMT_FP16 ? orc_get_hi(src + L.off_hi, i) : 0u;
+        orc_write_elem(out, fmt, i, orc_join_of(fmt, e, orc_get_raw(sm, fmt, i), hi));
     }
     if (status == ORC_OK && pos != total_bits) status = ORC_E_CORRUPT;
 
     if (status == ORC_OK && fmt == ORC_FMT_E4M3 && n % 2 == 1 && (sm[n / 2] >> 4) != 0)
         status = ORC_E_FORMAT; /* the unused nibble after an odd count is zero */
+    if (status == ORC_OK && fmt == ORC_FMT_FP16) {
+        /* the hi section's bits past element n - 1 are zero */
+        for (uint64_t bit = 3 * n; bit < 8 * orc_hi_bytes(fmt, n); bit++)
+            if ((src[L.off_hi + bit / 8] >> (bit % 8)) & 1u) { status = ORC_E_FORMAT; break; }
+    }
     if (status == ORC_OK) {
         /* the stream's padding bits are zero */
         for (uint64_t b = total_bits; b < 8 * L.exp_bytes; b++)

@@ -31,7 +31,7 @@ HEADER_FIELDS = {
     "n": (8, 8), "total_bits": (16, 8), "T": (24, 4), "C": (28, 4), "n_chunks": (32, 8),
     "n_blocks": (40, 8), "off_exp": (48, 8), "exp_bytes": (56, 8), "off_sm": (64, 8),
     "off_chunk": (72, 8), "off_block": (80, 8), "container_bytes": (88, 8), "longest": (96, 4),
-    "nsym": (100, 4), "fill": (104, 4), "format": (108, 4),
+    "nsym": (100, 4), "fill": (104, 4), "format": (108, 4), "off_hi": (112, 8),
 }
 
 
@@ -55,13 +55,20 @@ def test_golden_format_containers(golden_dir, name, dtype):
     for k, v in g["header"].items():
         off, nb = HEADER_FIELDS[k]
         assert _le(c, off, nb) == v, k
-    assert not c[112:256].any()
+    assert not c[120:256].any()
+    assert _le(c, 112, 8) == g["header"].get("off_hi", 0)
     off_exp = g["header"]["off_exp"]
     words = [_le(c, off_exp + 4 * i, 4) for i in range(len(g["stream_words_hex"]))]
     assert words == [int(x, 16) for x in g["stream_words_hex"]]
     raw = c[g["header"]["off_sm"]: g["header"]["off_sm"] + len(g["raw_hex"])]
     assert raw.tolist() == [int(x, 16) for x in g["raw_hex"]]
-    assert not c[g["header"]["off_sm"] + len(g["raw_hex"]): g["header"]["off_chunk"]].any()
+    raw_end = g["header"].get("off_hi") or g["header"]["off_chunk"]
+    assert not c[g["header"]["off_sm"] + len(g["raw_hex"]): raw_end].any()
+    if "hi_hex" in g:
+        off_hi = g["header"]["off_hi"]
+        hi = c[off_hi: off_hi + len(g["hi_hex"])]
+        assert hi.tolist() == [int(x, 16) for x in g["hi_hex"]]
+        assert not c[off_hi + len(g["hi_hex"]): g["header"]["off_chunk"]].any()
     entries = [_le(c, g["header"]["off_chunk"] + 2 * i, 2) for i in range(g["header"]["n_chunks"])]
     assert entries == g["chunk_entries"]
     blocks = [_le(c, g["header"]["off_block"] + 8 * i, 8) for i in range(g["header"]["n_blocks"] + 1)]
@@ -70,45 +77,48 @@ def test_golden_format_containers(golden_dir, name, dtype):
     assert st == oracle.OK and out.dtype == dtype and out.tolist() == w.tolist()
 
 
-# ---- FP16: the symbol from the value ------------------------------------------------
+# ---- FP16: the fields from the value ------------------------------------------------
 
-def _fp16_expected_symbols(bits):
-    """exponent << 3 | 3 leading fraction bits, computed from the float16 values."""
-    x = np.abs(bits.view(np.float16).astype(np.float64))
-    sym = np.zeros(x.size, np.int64)
-    normal = x >= 2.0 ** -14
-    m, ex = np.frexp(x[normal])          # x = m 2^ex, m in [0.5, 1)
-    k = ex - 1                           # floor(log2 x)
-    frac = np.rint((x[normal] / np.ldexp(1.0, k) - 1.0) * 1024).astype(np.int64)
-    sym[normal] = ((k + 15) << 3) | (frac >> 7)
-    sub = ~normal                        # exponent field 0: x = fraction * 2^-24
-    sym[sub] = np.rint(x[sub] / 2.0 ** -24).astype(np.int64) >> 7
-    return sym, normal
+def _fp16_fields(bits):
+    """(biased exponent, 10-bit fraction, sign) of float16 values, from the numbers themselves."""
+    x = bits.view(np.float16).astype(np.float64)
+    a = np.abs(x)
+    exp = np.zeros(a.size, np.int64)
+    frac = np.zeros(a.size, np.int64)
+    normal = a >= 2.0 ** -14
+    m, ex = np.frexp(a[normal])          # a = m 2^ex, m in [0.5, 1)
+    k = ex - 1                           # floor(log2 a)
+    exp[normal] = k + 15
+    frac[normal] = np.rint((a[normal] / np.ldexp(1.0, k) - 1.0) * 1024).astype(np.int64)
+    sub = ~normal                        # exponent field 0: a = fraction * 2^-24
+    frac[sub] = np.rint(a[sub] / 2.0 ** -24).astype(np.int64)
+    return exp, frac, np.signbit(x).astype(np.int64), normal
 
 
-def test_fp16_symbol_is_exponent_and_leading_fraction_bits_by_value():
+def test_fp16_symbol_is_the_exponent_by_value():
     bits = synth.normal_fp16(200_000, 0.0, 0.02, seed=3)
     bits = np.concatenate([bits, synth.normal_fp16(50_000, 0.0, 3e-5, seed=4)])  # many subnormals
     finite = np.isfinite(bits.view(np.float16))
     bits = bits[finite]
-    sym, normal = _fp16_expected_symbols(bits)
+    exp, _, _, normal = _fp16_fields(bits)
     assert (~normal).sum() > 1000
-    assert np.array_equal(oracle.histogram(bits, FP16), np.bincount(sym, minlength=256))
+    assert np.array_equal(oracle.histogram(bits, FP16), np.bincount(exp, minlength=256))
 
 
-def test_fp16_raw_byte_is_sign_and_trailing_fraction_bits_by_value():
-    bits = synth.normal_fp16(4096, 0.0, 0.5, seed=5)
-    x = bits.view(np.float16).astype(np.float64)
-    a = np.abs(x)
-    m, ex = np.frexp(a)
-    k = ex - 1
-    frac = np.where(a >= 2.0 ** -14, np.rint((a / np.ldexp(1.0, k) - 1.0) * 1024),
-                    np.rint(a / 2.0 ** -24)).astype(np.int64)
-    expect = (np.signbit(x).astype(np.int64) << 7) | (frac & 0x7F)
+def test_fp16_raw_byte_and_hi_section_by_value():
+    bits = synth.normal_fp16(4097, 0.0, 0.5, seed=5)
+    exp, frac, sign, _ = _fp16_fields(bits)
     lens = oracle.code_lengths(oracle.histogram(bits, FP16))
     c = oracle.encode(bits, lens, fmt=FP16)
-    off_sm = _le(c, 64, 8)
-    assert c[off_sm: off_sm + bits.size].tolist() == expect.tolist()
+    off_sm, off_hi, off_chunk = _le(c, 64, 8), _le(c, 112, 8), _le(c, 72, 8)
+    assert off_hi >= off_sm + bits.size and off_chunk >= off_hi + (3 * bits.size + 7) // 8
+    # sign and the 7 trailing fraction bits, one byte per element
+    assert c[off_sm: off_sm + bits.size].tolist() == ((sign << 7) | (frac & 0x7F)).tolist()
+    # the 3 leading fraction bits: element i at section bits 3i .. 3i + 2, lowest bit first
+    sec = np.unpackbits(c[off_hi: off_hi + (3 * bits.size + 7) // 8], bitorder="little")
+    got = sec[0: 3 * bits.size: 3] | (sec[1: 3 * bits.size: 3] << 1) | (sec[2: 3 * bits.size: 3] << 2)
+    assert got.astype(np.int64).tolist() == (frac >> 7).tolist()
+    assert not sec[3 * bits.size:].any()
 
 
 @pytest.mark.parametrize("T", [4, 32])
@@ -260,3 +270,16 @@ def test_e4m3_single_symbol_fill_in_range():
     c2 = c.copy()
     c2[104] = 16
     assert oracle.decode(c2)[1] == oracle.E_FORMAT
+
+
+def test_fp16_rejects_a_used_hi_padding_bit():
+    w = np.array([0x3C00, 0xBE00, 0x3780, 0x3C01, 0x4000], np.uint16)  # 15 hi bits in 2 bytes
+    lens = oracle.code_lengths(oracle.histogram(w, FP16))
+    c = oracle.encode(w, lens, 4, 32, fmt=FP16)
+    assert oracle.decode(c)[1] == oracle.OK
+    c2 = c.copy()
+    c2[_le(c, 112, 8) + 1] |= 0x80  # bit 15: past element 4
+    assert oracle.decode(c2)[1] == oracle.E_FORMAT
+    c3 = c.copy()
+    c3[112] ^= 0x01  # the hi section's offset no longer matches the layout
+    assert oracle.decode(c3)[1] == oracle.E_FORMAT
