@@ -182,7 +182,8 @@ def exponent_entropy_bits(parts) -> float:
     spend, before the chunk and block index."""
     total, n_all = 0.0, 0
     for _, w, _, d in parts:
-        sym = (w.reshape(-1) >> 3) & 0xF if d.format == 2 else (w.reshape(-1) >> 7) & 0xFF
+        sym = ((w.reshape(-1) >> 3) & 0xF if d.format == 2 else (w.reshape(-1) >> 10) & 0x1F if d.format == 1
+               else (w.reshape(-1) >> 7) & 0xFF)
         counts = np.bincount(sym.astype(np.intp), minlength=256).astype(np.float64)
         p = counts[counts > 0] / w.size
         total += float(-(p * np.log2(p)).sum()) * w.size
@@ -192,10 +193,12 @@ def exponent_entropy_bits(parts) -> float:
 
 def algorithmic_bytes(d) -> int:
     """Bytes a restore must move: coded symbol bits, the raw bits (a sign|mantissa
-    byte per element; a nibble for E4M3), chunk and block index entries read;
-    the elements written (2 bytes each; 1 for E4M3)."""
-    e4m3 = getattr(d, "format", 0) == 2
-    raw, out = ((d.n + 1) // 2, d.n) if e4m3 else (d.n, 2 * d.n)
+    byte per element, plus FP16's 3 hi-section bits; a nibble for E4M3), chunk
+    and block index entries read; the elements written (2 bytes each; 1 for E4M3)."""
+    fmt = getattr(d, "format", 0)
+    raw, out = ((d.n + 1) // 2, d.n) if fmt == 2 else (d.n, 2 * d.n)
+    if fmt == 1:
+        raw += (3 * d.n + 7) // 8  # FP16's hi section
     return (d.total_bits + 7) // 8 + raw + 2 * d.n_chunks + 8 * (d.n_blocks + 1) + out
 
 
@@ -447,7 +450,7 @@ def run_ours(args):
     kernel_ms = statistics.median(launch_ms)
     peak, peak_kind = measured_hbm_peak()
     achieved = alg_total / (kernel_ms * 1e-3) / 1e9
-    kernel_name = "restore_store_e4m3_kernel" if fmt == 2 else "restore_store_kernel"
+    kernel_name = {1: "restore_store_fp16_kernel", 2: "restore_store_e4m3_kernel"}.get(fmt, "restore_store_kernel")
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": profiled_traffic(kernel_name, args.workload),
                 "kernel": kernel_name, "peak_kind": peak_kind,
@@ -747,7 +750,7 @@ def run_formats_bench(afx, dev, args):
         peak, peak_kind = measured_hbm_peak()
         sym_bits = 0.0
         for _, w, _, d in parts:
-            sym = (w >> 3) & 0xF if elem == 1 else (w >> 7) & 0xFF
+            sym = (w >> 3) & 0xF if elem == 1 else (w >> 10) & 0x1F if fmt == afx.AFX_FMT_FP16 else (w >> 7) & 0xFF
             cnt = np.bincount(sym.astype(np.intp), minlength=256).astype(np.float64)
             p = cnt[cnt > 0] / w.size
             sym_bits += float(-(p * np.log2(p)).sum()) * w.size
@@ -760,8 +763,8 @@ def run_formats_bench(afx, dev, args):
             "symbol_entropy_bits_per_element": sym_bits / n,
             "algorithmic_bytes_per_step": alg,
         }
-    out["path"] = ("afx_decode_batch of the whole set per step: restore_store_kernel (FP16: the same bit split as "
-                   "BF16) and restore_store_e4m3_kernel (raw nibbles, byte outputs)")
+    out["path"] = ("afx_decode_batch of the whole set per step: restore_store_fp16_kernel (raw bytes plus the hi "
+                   "section) and restore_store_e4m3_kernel (raw nibbles, byte outputs)")
     return out
 
 

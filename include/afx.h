@@ -70,15 +70,18 @@ typedef enum afx_status {
 #define AFX_DEV_BAD_SHAPE 0x8 /* GEMV rows x cols disagree with the block index */
 #define AFX_DEV_TIMEOUT 0x10  /* a staging copy did not arrive within the kernel's wait limit; work skipped */
 
-/* Element formats a container can hold (header field at byte 108).  The
+/* Element formats a container can hold (header field at byte 108; the hi
+ * section's offset is the u64 at byte 112, 0 unless FP16).  The
  * pages treat BF16 only; FP16 and E4M3 are this library's extension under
  * the same container:
  *   AFX_FMT_BF16  16-bit elements; coded symbol = the 8-bit exponent, raw
  *                 byte = sign << 7 | 7-bit mantissa.
- *   AFX_FMT_FP16  IEEE 754 binary16; coded symbol = the 5-bit exponent and
- *                 the 3 leading fraction bits (bits 14..7), raw byte = sign
- *                 << 7 | the 7 trailing fraction bits.  The same bit split
- *                 as BF16, so the raw part stays one byte per element.
+ *   AFX_FMT_FP16  IEEE 754 binary16; coded symbol = the 5-bit exponent, raw
+ *                 byte = sign << 7 | the 7 trailing fraction bits, and the 3
+ *                 leading fraction bits in a second raw section (the hi
+ *                 section, afx_desc::off_hi): element i at section bits
+ *                 3i .. 3i + 2, bit b of the section in bit b % 8 of byte
+ *                 b / 8.
  *   AFX_FMT_E4M3  OCP 8-bit float E4M3 (bias 7, largest 448); coded symbol =
  *                 the 4-bit exponent, raw nibble = sign << 3 | 3-bit
  *                 mantissa, two per byte, element 2k in the low nibble of
@@ -115,6 +118,7 @@ typedef struct afx_desc {
     uint64_t n_blocks;        /* ceil(n_chunks / C) */
     uint64_t off_exp, exp_bytes;
     uint64_t off_sm;
+    uint64_t off_hi;          /* FP16: the hi section (3 bits per element); 0 for the other formats */
     uint64_t off_chunk;
     uint64_t off_block;
     uint64_t container_bytes; /* whole container, a multiple of 256 */

@@ -31,7 +31,7 @@ def test_every_declared_entry_point_is_exported(afx):
 def test_struct_sizes_match_the_c_layout(afx):
     # afx_code: 256 u64 + 256 u32 + 256 u8 + 4 u32; afx_desc: fixed fields + 256 lengths
     assert ctypes.sizeof(afx.afx_code) == 2048 + 1024 + 256 + 16
-    assert ctypes.sizeof(afx.afx_desc) == 8 * 2 + 4 * 2 + 8 * 2 + 8 * 6 + 4 * 4 + 256
+    assert ctypes.sizeof(afx.afx_desc) == 8 * 2 + 4 * 2 + 8 * 2 + 8 * 7 + 4 * 4 + 256
 
 
 CASES = {

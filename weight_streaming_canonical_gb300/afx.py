@@ -61,6 +61,7 @@ class afx_desc(ctypes.Structure):
         ("off_exp", ctypes.c_uint64),
         ("exp_bytes", ctypes.c_uint64),
         ("off_sm", ctypes.c_uint64),
+        ("off_hi", ctypes.c_uint64),
         ("off_chunk", ctypes.c_uint64),
         ("off_block", ctypes.c_uint64),
         ("container_bytes", ctypes.c_uint64),

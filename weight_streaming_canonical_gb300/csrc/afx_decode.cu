@@ -80,8 +80,8 @@ constexpr int kChunkStage = kThreads + 8;  // chunk entries staged per tile (the
 // [0, limit[L]); a 24-bit peek v has the length L = the smallest L with
 // v < limit[L], and its symbol's stage byte is sorted[base[L] + (v >> (24 - L))].
 // Stage bytes are what the merge of the tensor's element format wants: the
-// exponent rotated right by one bit for the 16-bit formats (see ror8), the
-// exponent shifted left by three (its place in the element) for E4M3.
+// exponent rotated right by one bit for BF16 (see ror8), and the exponent at
+// its place in the element's high byte for FP16 (<< 2) and E4M3 (<< 3).
 //
 // The internal nodes of the code tree (the prefixes that are not codes yet)
 // are numbered for the byte-step decoder: depth by depth, prefix value
@@ -105,6 +105,7 @@ struct CodeTables {
 struct TensorArgs {
     const uint32_t* exp_words;
     const uint8_t* sm;
+    const uint8_t* hi;         // FP16: the 3 leading fraction bits per element (nullptr otherwise)
     const uint16_t* chunk_index;
     const uint64_t* block_index;
     uint64_t n, n_chunks, n_blocks, exp_bytes;
@@ -132,7 +133,7 @@ struct LaunchArgs {
     uint32_t wait_limit;       // polls of a staging wait before it gives up (0: kWaitLimit)
     uint32_t stall;            // failure injection for tests: arm the staging barriers, issue no copies
     uint32_t host_src;         // restore: the containers are in pinned host memory (restore_store_host_kernel)
-    uint32_t e4m3;             // restore: E4M3 containers (raw nibbles, byte outputs)
+    uint32_t kind;             // restore: element kind, kKindBF16 / kKindFP16 / kKindE4M3
     int32_t* status;
     TensorArgs t[kMaxTensors];
 };
@@ -297,6 +298,43 @@ __device__ __forceinline__ uint4 e4m3_join16(uint2 ra, uint2 rb, uint2 raw) {
     const uint32_t lo1 = raw.y & 0x0F0F0F0Fu, hi1 = (raw.y >> 4) & 0x0F0F0F0Fu;
     return make_uint4(e4m3_join4(ra.x, __byte_perm(lo0, hi0, 0x5140)), e4m3_join4(ra.y, __byte_perm(lo0, hi0, 0x7362)),
                       e4m3_join4(rb.x, __byte_perm(lo1, hi1, 0x5140)), e4m3_join4(rb.y, __byte_perm(lo1, hi1, 0x7362)));
+}
+
+// FP16 elements: high byte = sign << 7 | e << 2 | h >> 1, low byte = (h & 1)
+// << 7 | the 7 trailing fraction bits, from the stage byte e << 2, the raw
+// byte (sign << 7 | trailing bits) and h, the 3 leading fraction bits.  Four
+// at a time: s4, r4 and f4 hold one value per byte.
+__device__ __forceinline__ uint2 fp16_join4(uint32_t s4, uint32_t r4, uint32_t f4) {
+    const uint32_t hi = (r4 & 0x80808080u) | s4 | ((f4 >> 1) & 0x03030303u);
+    const uint32_t lo = ((f4 << 7) & 0x80808080u) | (r4 & 0x7F7F7F7Fu);
+    return make_uint2(__byte_perm(lo, hi, 0x5140), __byte_perm(lo, hi, 0x7362));
+}
+
+// The 3-bit fields of four consecutive elements (12 bits, lowest first), one per byte.
+__device__ __forceinline__ uint32_t spread3x4(uint32_t t) {
+    return (t & 0x7u) | ((t & 0x38u) << 5) | ((t & 0x1C0u) << 10) | ((t & 0xE00u) << 15);
+}
+
+// Eight FP16 elements from their stage bytes, raw bytes and the 24 hi-section
+// bits of their group (element j at bits 3j .. 3j + 2).
+__device__ __forceinline__ uint4 fp16_join8(uint2 s8, uint2 r8, uint32_t h24) {
+    const uint2 a = fp16_join4(s8.x, r8.x, spread3x4(h24 & 0xFFFu));
+    const uint2 b = fp16_join4(s8.y, r8.y, spread3x4(h24 >> 12));
+    return make_uint4(a.x, a.y, b.x, b.y);
+}
+
+// The 3 leading fraction bits of FP16 element o (two bytes read: the field
+// may straddle them; the byte after the section's last is still inside the
+// container).
+__device__ __forceinline__ uint32_t fp16_hi3(const uint8_t* hi, uint64_t o) {
+    const uint64_t bit = 3 * o;
+    const uint32_t w = static_cast<uint32_t>(hi[bit >> 3]) | (static_cast<uint32_t>(hi[(bit >> 3) + 1]) << 8);
+    return (w >> (bit & 7u)) & 0x7u;
+}
+
+__device__ __forceinline__ uint16_t fp16_join1(uint32_t s, uint32_t r, uint32_t h) {
+    const uint2 v = fp16_join4(s & 0xFFu, r & 0xFFu, h & 0x7u);
+    return static_cast<uint16_t>(v.x & 0xFFFFu);
 }
 
 __device__ __forceinline__ uint8_t e4m3_join1(uint32_t r, uint32_t nib) {
@@ -1410,19 +1448,62 @@ __device__ __forceinline__ void warp_store_e4m3(const uint8_t* stage, const uint
     }
 }
 
-// What warp_run does with a decoded sub-tile: store the 16-bit elements
-// (BF16 or FP16: the same bit split), store E4M3 elements, or the fused
-// GEMV above.  kNibbles: the raw section holds a nibble per element.
+// Joins and stores `count` FP16 elements from o0 with the 32 lanes of a
+// warp, as warp_store does for BF16, with each group of 8 also taking its
+// 24 hi-section bits (3 bytes from byte 3g / 8 for the group at element g).
+__device__ __forceinline__ void warp_store_fp16(const uint8_t* stage, const uint8_t* sm, const uint8_t* hi,
+                                                uint16_t* out, uint64_t o0, uint32_t count, int lane) {
+    const uint64_t ob0 = o0 & ~uint64_t(7);
+    const uint8_t* smb = sm + ob0;
+    uint16_t* outb = out + ob0;
+    const uint32_t a = static_cast<uint32_t>(o0) & 7u, b = a + count;  // the range, relative to ob0
+    const uint32_t f0 = (a + 7) & ~7u, f1 = b & ~7u;                  // full groups [f0, f1)
+    if (lane < 16) {
+        const uint32_t r = lane < 8 ? lane : f1 + (lane & 7);
+        const bool same_group = lane >= 8 && f1 == 0;  // the last group is the first one
+        if (r >= a && r < b && (r < f0 || r >= f1) && !same_group)
+            outb[r] = fp16_join1(stage[r], smb[r], fp16_hi3(hi, ob0 + r));
+    }
+    if (f1 > f0) {
+        const uint32_t nfull = (f1 - f0) >> 3;
+        const uint2* smp = reinterpret_cast<const uint2*>(smb + f0);
+        const uint2* stp = reinterpret_cast<const uint2*>(stage + f0);
+        uint4* outp = reinterpret_cast<uint4*>(outb + f0);
+        const uint8_t* hg = hi + 3 * ((ob0 + f0) >> 3);  // the first full group's 3 bytes
+        for (uint32_t j = lane; j < nfull; j += 32) {
+            const uint8_t* h = hg + 3 * j;
+            const uint32_t h24 = static_cast<uint32_t>(__ldg(h)) | (static_cast<uint32_t>(__ldg(h + 1)) << 8) |
+                                 (static_cast<uint32_t>(__ldg(h + 2)) << 16);
+            __stcs(outp + j, fp16_join8(stp[j], __ldg(smp + j), h24));
+        }
+    }
+}
+
+// What warp_run does with a decoded sub-tile: store BF16, FP16 or E4M3
+// elements, or the fused GEMV above.  kRaw: what the raw sections hold --
+// a byte per element (BF16), a byte and 3 hi-section bits (FP16), or a
+// nibble (E4M3).
+constexpr int kRawBytes = 0, kRawBytesHi = 1, kRawNibbles = 2;
+constexpr uint32_t kKindBF16 = 0, kKindFP16 = 1, kKindE4M3 = 2;
+
 struct StoreEpilogue {
-    static constexpr bool kNibbles = false;
+    static constexpr int kRaw = kRawBytes;
     __device__ __forceinline__ void operator()(const uint8_t* stage, const TensorArgs& t, uint64_t, uint64_t o0,
                                                uint32_t count, bool ok, int lane) const {
         if (ok && count) warp_store(stage, t.sm, static_cast<uint16_t*>(t.out), o0, count, lane);
     }
 };
 
+struct StoreFP16Epilogue {
+    static constexpr int kRaw = kRawBytesHi;
+    __device__ __forceinline__ void operator()(const uint8_t* stage, const TensorArgs& t, uint64_t, uint64_t o0,
+                                               uint32_t count, bool ok, int lane) const {
+        if (ok && count) warp_store_fp16(stage, t.sm, t.hi, static_cast<uint16_t*>(t.out), o0, count, lane);
+    }
+};
+
 struct StoreE4M3Epilogue {
-    static constexpr bool kNibbles = true;
+    static constexpr int kRaw = kRawNibbles;
     __device__ __forceinline__ void operator()(const uint8_t* stage, const TensorArgs& t, uint64_t, uint64_t o0,
                                                uint32_t count, bool ok, int lane) const {
         if (ok && count) warp_store_e4m3(stage, t.sm, static_cast<uint8_t*>(t.out), o0, count, lane);
@@ -1431,7 +1512,7 @@ struct StoreE4M3Epilogue {
 
 template <int B>
 struct GemvEpilogue {
-    static constexpr bool kNibbles = false;
+    static constexpr int kRaw = kRawBytes;
     __device__ __forceinline__ void operator()(const uint8_t* stage, const TensorArgs& t, uint64_t s, uint64_t o0,
                                                uint32_t count, bool ok, int lane) const {
         warp_gemv<B>(stage, t, s, o0, count, ok, lane);
@@ -1528,12 +1609,16 @@ __device__ __forceinline__ bool warp_run(const TabView& tv, WarpSlot& ws, uint8_
             if (!in_range)
                 raise_status(status, AFX_DEV_BAD_BLOCK);
             else if (o0 < o1 && !host_src) {  // the raw bytes are needed after the decode
-                if constexpr (Epi::kNibbles) {
+                if constexpr (Epi::kRaw == kRawNibbles) {
                     const uint64_t a0 = (o0 >> 1) & ~uint64_t(15), a1 = (((o1 + 1) >> 1) + 15) & ~uint64_t(15);
                     prefetch_l2(sm + a0, static_cast<uint32_t>(a1 - a0));
                 } else {
                     const uint64_t a0 = o0 & ~uint64_t(15), a1 = (o1 + 15) & ~uint64_t(15);
                     prefetch_l2(sm + a0, static_cast<uint32_t>(a1 - a0));
+                    if constexpr (Epi::kRaw == kRawBytesHi) {  // and the hi section's bits of the range
+                        const uint64_t h0 = ((3 * o0) >> 3) & ~uint64_t(15), h1 = (((3 * o1 + 7) >> 3) + 15) & ~uint64_t(15);
+                        prefetch_l2(t.hi + h0, static_cast<uint32_t>(h1 - h0));
+                    }
                 }
             }
         }
@@ -1675,6 +1760,18 @@ __global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
     restore_warps<true>(a, StoreE4M3Epilogue{});
 }
 
+// The restore of FP16 containers (raw bytes plus the hi section's 3 bits per
+// element), from device memory and from pinned host memory.
+__global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
+    restore_store_fp16_kernel(const __grid_constant__ LaunchArgs a) {
+    restore_warps<false>(a, StoreFP16Epilogue{});
+}
+
+__global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
+    restore_store_fp16_host_kernel(const __grid_constant__ LaunchArgs a) {
+    restore_warps<true>(a, StoreFP16Epilogue{});
+}
+
 template <int B>
 __global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1) restore_gemv_kernel(const __grid_constant__ LaunchArgs a) {
     restore_warps<false>(a, GemvEpilogue<B>{});
@@ -1768,6 +1865,29 @@ __global__ void fill_store_kernel(const uint8_t* __restrict__ sm, const uint64_t
 
 // E4M3 with one exponent for every element: 16 elements (8 raw bytes) per
 // group; the ragged last group goes out element by element.
+// FP16 with one exponent for every element: 8 elements (8 raw bytes, 3 hi
+// bytes) per group; the ragged last group goes out element by element.
+__global__ void fill_store_fp16_kernel(const uint8_t* __restrict__ raw, const uint8_t* __restrict__ hi,
+                                       const uint64_t* __restrict__ block_index, uint32_t fill, uint64_t n,
+                                       uint16_t* __restrict__ out, int32_t* status) {
+    if (blockIdx.x == 0 && threadIdx.x == 0 && block_index[0] != n) raise_status(status, AFX_DEV_BAD_BLOCK);
+    const uint64_t groups = (n + 7) >> 3;
+    const uint32_t s1 = (fill << 2) & 0xFFu, s4 = s1 * 0x01010101u;
+    for (uint64_t g = blockIdx.x * static_cast<uint64_t>(blockDim.x) + threadIdx.x; g < groups;
+         g += static_cast<uint64_t>(gridDim.x) * blockDim.x) {
+        const uint64_t ob = g << 3;
+        if (ob + 8 <= n) {
+            const uint8_t* h = hi + 3 * g;
+            const uint32_t h24 = static_cast<uint32_t>(h[0]) | (static_cast<uint32_t>(h[1]) << 8) |
+                                 (static_cast<uint32_t>(h[2]) << 16);
+            const uint2 r8 = __ldg(reinterpret_cast<const uint2*>(raw + ob));
+            __stcs(reinterpret_cast<uint4*>(out + ob), fp16_join8(make_uint2(s4, s4), r8, h24));
+        } else {
+            for (uint64_t o = ob; o < n; ++o) out[o] = fp16_join1(s1, raw[o], fp16_hi3(hi, o));
+        }
+    }
+}
+
 __global__ void fill_store_e4m3_kernel(const uint8_t* __restrict__ raw, const uint64_t* __restrict__ block_index,
                                        uint32_t fill, uint64_t n, uint8_t* __restrict__ out, int32_t* status) {
     if (blockIdx.x == 0 && threadIdx.x == 0 && block_index[0] != n) raise_status(status, AFX_DEV_BAD_BLOCK);
@@ -1816,7 +1936,9 @@ __global__ void fill_gemv_kernel(const uint8_t* __restrict__ sm, const uint64_t*
 // ---- host side ------------------------------------------------------------------------
 
 // The stage byte of symbol s for the merge of format fmt.
-uint32_t stage_byte(uint32_t fmt, uint32_t s) { return fmt == AFX_FMT_E4M3 ? (s << 3) & 0xFFu : ror8(s); }
+uint32_t stage_byte(uint32_t fmt, uint32_t s) {
+    return fmt == AFX_FMT_E4M3 ? (s << 3) & 0xFFu : fmt == AFX_FMT_FP16 ? (s << 2) & 0xFFu : ror8(s);
+}
 
 void make_tables(const afx_desc& d, CodeTables& t) {
     std::memset(&t, 0, sizeof t);
@@ -1928,6 +2050,7 @@ void fill_tensor(const afx_desc& d, const void* container, TensorArgs& t) {
     const uint8_t* base = static_cast<const uint8_t*>(container);
     t.exp_words = reinterpret_cast<const uint32_t*>(base + d.off_exp);
     t.sm = base + d.off_sm;
+    t.hi = d.format == AFX_FMT_FP16 ? base + d.off_hi : nullptr;
     t.chunk_index = reinterpret_cast<const uint16_t*>(base + d.off_chunk);
     t.block_index = reinterpret_cast<const uint64_t*>(base + d.off_block);
     t.n = d.n;
@@ -2031,9 +2154,10 @@ afx_status launch_restore(LaunchArgs& la, cudaStream_t s) {
         const afx_status st = warp_launch_config(la, &warps, &smem);
         if (st != AFX_OK) return st;
         int per_sm = 0;
-        void (*const kernels[2][2])(LaunchArgs) = {{restore_store_kernel, restore_store_host_kernel},
+        void (*const kernels[3][2])(LaunchArgs) = {{restore_store_kernel, restore_store_host_kernel},
+                                                    {restore_store_fp16_kernel, restore_store_fp16_host_kernel},
                                                     {restore_store_e4m3_kernel, restore_store_e4m3_host_kernel}};
-        void (*const kernel)(LaunchArgs) = kernels[la.e4m3 ? 1 : 0][la.host_src ? 1 : 0];
+        void (*const kernel)(LaunchArgs) = kernels[la.kind < 3 ? la.kind : 0][la.host_src ? 1 : 0];
         const afx_status pst = prepare_kernel(reinterpret_cast<const void*>(kernel), warps * 32, smem, &per_sm);
         if (pst != AFX_OK) return pst;
         const uint64_t grid = std::min<uint64_t>(la.total_tiles, static_cast<uint64_t>(sms) * per_sm);
@@ -2106,9 +2230,9 @@ afx_status decode_batch(const afx_desc* descs, const void* const* containers, vo
         if (d.nsym >= 2 && d.block_chunks != static_cast<uint32_t>(kThreads))
             return afx_fail(AFX_E_ARG, "the decoder runs 512 chunks per block", 0);
     }
-    // [16-bit elements, E4M3][device-resident containers, host-resident containers]
-    LaunchArgs lists[2][2];
-    for (int f = 0; f < 2; ++f)
+    // [BF16, FP16, E4M3][device-resident containers, host-resident containers]
+    LaunchArgs lists[3][2];
+    for (int f = 0; f < 3; ++f)
         for (int h = 0; h < 2; ++h) {
             LaunchArgs& la = lists[f][h];
             std::memset(&la, 0, sizeof la);
@@ -2116,7 +2240,7 @@ afx_status decode_batch(const afx_desc* descs, const void* const* containers, vo
             la.wait_limit = stall_polls;
             la.stall = stall_polls != 0;
             la.host_src = static_cast<uint32_t>(h);
-            la.e4m3 = static_cast<uint32_t>(f);
+            la.kind = static_cast<uint32_t>(f);
         }
     for (uint32_t i = 0; i < count; ++i) {
         const afx_desc& d = descs[i];
@@ -2127,8 +2251,8 @@ afx_status decode_batch(const afx_desc* descs, const void* const* containers, vo
             return afx_fail(AFX_E_ARG, "container and output must be device memory or pinned host memory", 0);
         if (stall_polls && wc != Where::device)
             return afx_fail(AFX_E_ARG, "the stalled test restore needs a device-resident container", 0);
-        const bool e4m3 = d.format == AFX_FMT_E4M3;
-        LaunchArgs& la = lists[e4m3 ? 1 : 0][wc == Where::host ? 1 : 0];
+        const bool e4m3 = d.format == AFX_FMT_E4M3, fp16 = d.format == AFX_FMT_FP16;
+        LaunchArgs& la = lists[e4m3 ? kKindE4M3 : fp16 ? kKindFP16 : kKindBF16][wc == Where::host ? 1 : 0];
         if (d.nsym == 1) {
             const int sms = sm_count();
             if (sms <= 0) return afx_fail(AFX_E_CUDA, "cannot query the SM count", 0);
@@ -2138,6 +2262,10 @@ afx_status decode_batch(const afx_desc* descs, const void* const* containers, vo
                 fill_store_e4m3_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
                     base + d.off_sm, reinterpret_cast<const uint64_t*>(base + d.off_block), d.fill, d.n,
                     static_cast<uint8_t*>(outs[i]), status);
+            else if (fp16)
+                fill_store_fp16_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+                    base + d.off_sm, base + d.off_hi, reinterpret_cast<const uint64_t*>(base + d.off_block), d.fill,
+                    d.n, static_cast<uint16_t*>(outs[i]), status);
             else
                 fill_store_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
                     base + d.off_sm, reinterpret_cast<const uint64_t*>(base + d.off_block), d.fill, d.n,
@@ -2158,7 +2286,7 @@ afx_status decode_batch(const afx_desc* descs, const void* const* containers, vo
         la.total_tiles += d.n_blocks;
         la.max_chunk_bytes = std::max(la.max_chunk_bytes, d.chunk_bytes);
     }
-    for (int f = 0; f < 2; ++f)
+    for (int f = 0; f < 3; ++f)
         for (int h = 0; h < 2; ++h) {
             const afx_status st = launch_restore<0>(lists[f][h], s);
             if (st != AFX_OK) return st;

@@ -120,17 +120,22 @@ void canonical_codes(const uint8_t len[256], uint32_t code[256]) {
 
 bool format_ok(uint32_t fmt) { return fmt == AFX_FMT_BF16 || fmt == AFX_FMT_FP16 || fmt == AFX_FMT_E4M3; }
 
-// Symbols a format's elements can produce: 256 for the 16-bit formats, 16
-// for E4M3 (its 4-bit exponent).
-unsigned symbol_range(uint32_t fmt) { return fmt == AFX_FMT_E4M3 ? 16u : 256u; }
+// Symbols a format's elements can produce: 256 for BF16 (its 8-bit
+// exponent), 32 for FP16, 16 for E4M3.
+unsigned symbol_range(uint32_t fmt) { return fmt == AFX_FMT_E4M3 ? 16u : fmt == AFX_FMT_FP16 ? 32u : 256u; }
 
 uint64_t raw_bytes(uint32_t fmt, uint64_t n) { return fmt == AFX_FMT_E4M3 ? (n + 1) / 2 : n; }
 
-// BF16 and FP16 share one bit split: bits 14..7 are coded (BF16's exponent;
-// FP16's exponent and its 3 leading fraction bits), the sign and bits 6..0
-// are the raw byte.  E4M3: bits 6..3 (the exponent) are coded, the sign and
-// bits 2..0 are the raw nibble.
-inline unsigned symbol_of(uint32_t fmt, unsigned v) { return fmt == AFX_FMT_E4M3 ? (v >> 3) & 0xFu : (v >> 7) & 0xFFu; }
+// FP16's hi section: 3 bits per element.
+uint64_t hi_bytes(uint32_t fmt, uint64_t n) { return fmt == AFX_FMT_FP16 ? (3 * n + 7) / 8 : 0; }
+
+// The coded symbol is the exponent: BF16 bits 14..7, FP16 bits 14..10,
+// E4M3 bits 6..3.  The raw byte of the 16-bit formats is the sign and bits
+// 6..0; FP16's bits 9..7 go to the hi section.  E4M3's raw nibble is the
+// sign and bits 2..0.
+inline unsigned symbol_of(uint32_t fmt, unsigned v) {
+    return fmt == AFX_FMT_E4M3 ? (v >> 3) & 0xFu : fmt == AFX_FMT_FP16 ? (v >> 10) & 0x1Fu : (v >> 7) & 0xFFu;
+}
 
 inline unsigned raw_of(uint32_t fmt, unsigned v) {
     return fmt == AFX_FMT_E4M3 ? ((v >> 4) & 0x8u) | (v & 0x7u) : ((v >> 8) & 0x80u) | (v & 0x7Fu);
@@ -156,7 +161,13 @@ void layout(uint64_t n, uint32_t fmt, uint64_t total_bits, uint32_t T, uint32_t 
     d->off_exp = AFX_HEADER_BYTES;
     d->exp_bytes = round_up(d->n_chunks * T, 16) + 16;
     d->off_sm = round_up(d->off_exp + d->exp_bytes, 256);
-    d->off_chunk = round_up(d->off_sm + raw_bytes(fmt, n), 256);
+    if (fmt == AFX_FMT_FP16) {
+        d->off_hi = round_up(d->off_sm + raw_bytes(fmt, n), 256);
+        d->off_chunk = round_up(d->off_hi + hi_bytes(fmt, n), 256);
+    } else {
+        d->off_hi = 0;
+        d->off_chunk = round_up(d->off_sm + raw_bytes(fmt, n), 256);
+    }
     d->format = fmt;
     d->off_block = round_up(d->off_chunk + 2 * d->n_chunks, 256);
     d->container_bytes = round_up(d->off_block + 8 * (d->n_blocks + 1), 256);
@@ -197,7 +208,8 @@ afx_status afx_build_code_fmt(const void* w, uint64_t n, uint32_t fmt, uint32_t 
             for (uint64_t i = lo; i < hi; ++i) ++h[(e[i] >> 3) & 0xFu];
         } else {
             const uint16_t* e = static_cast<const uint16_t*>(w);
-            for (uint64_t i = lo; i < hi; ++i) ++h[(e[i] >> 7) & 0xFFu];
+            const unsigned shift = fmt == AFX_FMT_FP16 ? 10u : 7u, mask = fmt == AFX_FMT_FP16 ? 0x1Fu : 0xFFu;
+        for (uint64_t i = lo; i < hi; ++i) ++h[(e[i] >> shift) & mask];
         }
     };
     if (workers == 1) {
@@ -289,6 +301,7 @@ afx_status afx_encode(const void* w, uint64_t n, const afx_code* code, const afx
     put_le(h + 100, 4, d->nsym);
     put_le(h + 104, 4, d->fill);
     put_le(h + 108, 4, fmt);
+    put_le(h + 112, 8, d->off_hi);
     std::memcpy(h + 256, code->len, 256);
 
     uint8_t* sm = dst + d->off_sm;
@@ -296,6 +309,15 @@ afx_status afx_encode(const void* w, uint64_t n, const afx_code* code, const afx
         for (uint64_t i = 0; i < n; ++i) sm[i / 2] |= static_cast<uint8_t>(raw_of(fmt, element(w, fmt, i)) << (4 * (i & 1)));
     } else {
         for (uint64_t i = 0; i < n; ++i) sm[i] = static_cast<uint8_t>(raw_of(fmt, element(w, fmt, i)));
+    }
+    if (fmt == AFX_FMT_FP16) {  // the 3 leading fraction bits, packed lowest bit first
+        uint8_t* hs = dst + d->off_hi;
+        for (uint64_t i = 0; i < n; ++i) {
+            const uint32_t h3 = (element(w, fmt, i) >> 7) & 0x7u;
+            const uint64_t bit = 3 * i;
+            hs[bit >> 3] |= static_cast<uint8_t>(h3 << (bit & 7));
+            if ((bit & 7) > 5) hs[(bit >> 3) + 1] |= static_cast<uint8_t>(h3 >> (8 - (bit & 7)));
+        }
     }
 
     if (d->nsym <= 1) {
@@ -371,9 +393,9 @@ afx_status afx_parse_header(const uint8_t* h, uint64_t bytes, afx_desc* out) {
     layout(n, fmt, total_bits, T, C, &d);
     if (get_le(h + 32, 8) != d.n_chunks || get_le(h + 40, 8) != d.n_blocks || get_le(h + 48, 8) != d.off_exp ||
         get_le(h + 56, 8) != d.exp_bytes || get_le(h + 64, 8) != d.off_sm || get_le(h + 72, 8) != d.off_chunk ||
-        get_le(h + 80, 8) != d.off_block || get_le(h + 88, 8) != d.container_bytes)
+        get_le(h + 80, 8) != d.off_block || get_le(h + 88, 8) != d.container_bytes || get_le(h + 112, 8) != d.off_hi)
         return AFX_E_FORMAT;
-    for (unsigned i = 112; i < 256; ++i)
+    for (unsigned i = 120; i < 256; ++i)
         if (h[i]) return AFX_E_FORMAT;
     d.max_len = static_cast<uint32_t>(get_le(h + 96, 4));
     d.nsym = static_cast<uint32_t>(get_le(h + 100, 4));
@@ -416,7 +438,7 @@ afx_status afx_check_desc(const afx_desc* d) {
     layout(d->n, d->format, d->total_bits, d->chunk_bytes, d->block_chunks, &L);
     if (L.n_chunks != d->n_chunks || L.n_blocks != d->n_blocks || L.off_exp != d->off_exp ||
         L.exp_bytes != d->exp_bytes || L.off_sm != d->off_sm || L.off_chunk != d->off_chunk ||
-        L.off_block != d->off_block || L.container_bytes != d->container_bytes)
+        L.off_block != d->off_block || L.container_bytes != d->container_bytes || L.off_hi != d->off_hi)
         return AFX_E_FORMAT;
     unsigned longest = 0, coded = 0, min_len = 255;
     uint64_t kraft = 0;
