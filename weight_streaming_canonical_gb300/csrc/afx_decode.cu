@@ -2208,6 +2208,11 @@ void reset_launch(LaunchArgs& la) {
     la.max_rows_per_warp = 0;
 }
 
+// Zeroes the fields in front of the tensor slots.  Slot k is written in full
+// (fill_tensor) before count passes it and the kernels read no slot at or
+// past count, so the 13 KB of slots need no clearing on every call.
+void clear_launch(LaunchArgs& la) { std::memset(&la, 0, offsetof(LaunchArgs, t)); }
+
 }  // namespace afx
 
 using namespace afx;
@@ -2235,7 +2240,7 @@ afx_status decode_batch(const afx_desc* descs, const void* const* containers, vo
     for (int f = 0; f < 3; ++f)
         for (int h = 0; h < 2; ++h) {
             LaunchArgs& la = lists[f][h];
-            std::memset(&la, 0, sizeof la);
+            clear_launch(la);
             la.status = status;
             la.wait_limit = stall_polls;
             la.stall = stall_polls != 0;
@@ -2339,8 +2344,8 @@ afx_status gemv_batch(const afx_desc* descs, const void* const* containers, cons
                       const uint32_t* cols, const uint16_t* const* xs, float* const* ys, void* const* workspaces,
                       uint32_t count, cudaStream_t s, int32_t* status) {
     LaunchArgs la, lw;  // CTA-tile GEMV, warp GEMV
-    std::memset(&la, 0, sizeof la);
-    std::memset(&lw, 0, sizeof lw);
+    clear_launch(la);
+    clear_launch(lw);
     la.status = status;
     lw.status = status;
     for (uint32_t i = 0; i < count; ++i) {
