@@ -83,6 +83,34 @@ st = torch.zeros(1, dtype=torch.int32, device="cuda")
 afx.afx_decode_gemv(d, torch.from_numpy(c).cuda(), rows, cols, x, y, ws, status_dev=st)
 torch.cuda.synchronize()
 statuses.append(("gemv", rows * cols, int(st.item()), None))
+# randomized corruption: bytes of every section replaced, flipped or zeroed,
+# in all three formats; the kernels must flag or restore, never leave a buffer
+rng = np.random.default_rng(2026)
+fuzz_flagged = fuzz_exact = 0
+bases = [afx.encode(synth.normal(300_001, seed=21)), afx.encode(synth.normal_fp16(200_003, seed=22), fmt=1),
+         afx.encode(synth.normal_e4m3(300_007, seed=23), fmt=2), afx.encode(synth.adversarial(1 << 18, seed=24))]
+for trial in range(120):
+    c0, d = bases[trial % len(bases)]
+    bad = c0.copy()
+    section = trial % 4
+    lo, hi = [(d.off_exp, d.off_exp + d.exp_bytes), (d.off_sm, d.off_chunk),
+              (d.off_chunk, d.off_block), (d.off_block, d.container_bytes)][section]
+    k = int(rng.integers(1, 64))
+    idx = rng.integers(lo, hi, size=k)
+    mode = trial % 3
+    if mode == 0:
+        bad[idx] = rng.integers(0, 256, size=k, dtype=np.uint8)
+    elif mode == 1:
+        bad[idx] ^= np.uint8(1) << rng.integers(0, 8, size=k).astype(np.uint8)
+    else:
+        bad[idx] = 0
+    got, st = restore(bad, d)
+    if st != 0:
+        fuzz_flagged += 1
+    else:
+        fuzz_exact += 1
+statuses.append(("fuzz", fuzz_flagged, 0, None))
+statuses.append(("fuzz_clean", fuzz_exact, 0, None))
 bits, checked = afx.afx_debug_bounds_report()
 print(json.dumps({"bits": bits, "checked": checked, "cases": statuses}))
 """
@@ -97,6 +125,8 @@ def test_bounds_checked_build_reports_no_violation():
     for kind, size, status, exact in rep["cases"]:
         if kind in ("garbage stream", "chunk index", "block index"):
             assert status != 0, kind
+        elif kind == "fuzz":
+            assert size > 0  # corruptions the kernels flagged
         else:
             assert status == 0 and exact in (True, None), (kind, size)
     assert rep["bits"] == 0, f"bounds checks failed: {rep['bits']:#x}"

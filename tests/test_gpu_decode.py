@@ -372,3 +372,18 @@ def test_gemv_refuses_a_host_container(afx):
     ws = torch.empty(afx.afx_decode_gemv_workspace(d, 1) // 4 + 4, dtype=torch.float32, device="cuda")
     with pytest.raises((afx.AfxError, ValueError)):
         afx.afx_decode_gemv(d, _pinned(c), rows, cols, x, y, ws)
+
+
+def test_block_index_entries_near_2_64_write_nothing_outside(afx):
+    # a block-index entry of 2^64 - 1 makes start + count wrap back below n;
+    # the restore must flag it and write nothing outside the output (the
+    # guard elements on both sides stay as they were)
+    w = synth.normal(400_003, seed=77)
+    c, d = afx.encode(w)
+    assert d.n_blocks > 4
+    bad = c.copy()
+    for b in range(1, int(d.n_blocks)):
+        bad[d.off_block + 8 * b: d.off_block + 8 * b + 8] = 0xFF
+    out, status, intact = gpu_decode(afx, bad, d, out_pad=64, out_offset=64)
+    assert status & afx.AFX_DEV_BAD_BLOCK
+    assert intact, "wrote outside the output range"

@@ -1603,8 +1603,10 @@ __device__ __forceinline__ bool warp_run(const TabView& tv, WarpSlot& ws, uint8_
             if (lane >= d) inc += o;
         }
         const uint32_t total = __shfl_sync(0xFFFFFFFFu, inc, 31);
+        // a corrupt block index can put start anywhere: o0 <= n keeps o1 from
+        // wrapping past 2^64 back into [0, n]
         const uint64_t o0 = start, o1 = start + total;
-        const bool in_range = o1 <= n;
+        const bool in_range = o0 <= n && o1 <= n;
         if (lane == 0) {
             if (!in_range)
                 raise_status(status, AFX_DEV_BAD_BLOCK);
