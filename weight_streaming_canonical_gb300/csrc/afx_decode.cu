@@ -691,8 +691,26 @@ __device__ __forceinline__ bool decode_tile(Shared& sh, const uint32_t* stream, 
 
 // ---- epilogues ---------------------------------------------------------------------
 
-__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+// c + a * b with BF16 multiplicands and a float32 accumulator, rounded once
+// (the BF16 values convert to float32 exactly, so this equals fmaf on the
+// converted values): the multiply-adds take the BF16 bit patterns as they
+// are, with no conversion instructions.  fma_bf16: a and b in the low 16
+// bits; fma_bf16x2: the two halves of a and b, low half first.
+__device__ __forceinline__ float fma_bf16(uint32_t a, uint32_t b, float c) {
+    asm("{\n .reg .b16 al, ah, bl, bh;\n mov.b32 {al, ah}, %1;\n mov.b32 {bl, bh}, %2;\n"
+        " fma.rn.f32.bf16 %0, al, bl, %0;\n}\n"
+        : "+f"(c)
+        : "r"(a), "r"(b));
+    return c;
+}
+
+__device__ __forceinline__ float fma_bf16x2(uint32_t a, uint32_t b, float c) {
+    asm("{\n .reg .b16 al, ah, bl, bh;\n mov.b32 {al, ah}, %1;\n mov.b32 {bl, bh}, %2;\n"
+        " fma.rn.f32.bf16 %0, al, bl, %0;\n fma.rn.f32.bf16 %0, ah, bh, %0;\n}\n"
+        : "+f"(c)
+        : "r"(a), "r"(b));
+    return c;
+}
 
 template <int B>
 __device__ __forceinline__ void warp_flush(float (&acc)[kMaxBatch], float* part, uint32_t slot, int lane) {
@@ -754,26 +772,13 @@ __device__ __forceinline__ void gemv_tile(const Shared& sh, const TensorArgs& t,
                 const uint2 e8 = *reinterpret_cast<const uint2*>(sh.stage + si);
                 const uint2 s8 = __ldg(reinterpret_cast<const uint2*>(t.sm + ob));
                 const uint4 wv4 = join8(e8, s8);
-                float wv[8];
-                wv[0] = bf16_lo(wv4.x);
-                wv[1] = bf16_hi(wv4.x);
-                wv[2] = bf16_lo(wv4.y);
-                wv[3] = bf16_hi(wv4.y);
-                wv[4] = bf16_lo(wv4.z);
-                wv[5] = bf16_hi(wv4.z);
-                wv[6] = bf16_lo(wv4.w);
-                wv[7] = bf16_hi(wv4.w);
 #pragma unroll
                 for (int b = 0; b < B; ++b) {
                     const uint4 xv = __ldg(reinterpret_cast<const uint4*>(t.x + b * cols + c0));
-                    float s = wv[0] * bf16_lo(xv.x);
-                    s = fmaf(wv[1], bf16_hi(xv.x), s);
-                    s = fmaf(wv[2], bf16_lo(xv.y), s);
-                    s = fmaf(wv[3], bf16_hi(xv.y), s);
-                    s = fmaf(wv[4], bf16_lo(xv.z), s);
-                    s = fmaf(wv[5], bf16_hi(xv.z), s);
-                    s = fmaf(wv[6], bf16_lo(xv.w), s);
-                    s = fmaf(wv[7], bf16_hi(xv.w), s);
+                    float s = fma_bf16x2(wv4.x, xv.x, 0.f);
+                    s = fma_bf16x2(wv4.y, xv.y, s);
+                    s = fma_bf16x2(wv4.z, xv.z, s);
+                    s = fma_bf16x2(wv4.w, xv.w, s);
                     ca[b] = s;
                 }
             } else {
@@ -782,14 +787,14 @@ __device__ __forceinline__ void gemv_tile(const Shared& sh, const TensorArgs& t,
                     if (o < o0 || o >= o1) continue;
                     const uint64_t r = o / cols;
                     const uint64_t c = o - r * cols;
-                    const float wf = __uint_as_float(static_cast<uint32_t>(join1(sh.stage[si + q], t.sm[o])) << 16);
+                    const uint32_t wb = join1(sh.stage[si + q], t.sm[o]);
 #pragma unroll
                     for (int b = 0; b < B; ++b) {
-                        const float xf = __uint_as_float(static_cast<uint32_t>(t.x[b * cols + c]) << 16);
+                        const uint32_t xb = t.x[b * cols + c];
                         if (r == ra)
-                            ca[b] = fmaf(wf, xf, ca[b]);
+                            ca[b] = fma_bf16(wb, xb, ca[b]);
                         else
-                            cb[b] = fmaf(wf, xf, cb[b]);
+                            cb[b] = fma_bf16(wb, xb, cb[b]);
                     }
                     if (r != ra) rb = r;
                 }
@@ -1372,16 +1377,16 @@ __device__ __forceinline__ void warp_gemv(const uint8_t* stage, const TensorArgs
             const uint32_t r = lane < 8 ? lane : f1 + (lane & 7);
             const bool same_group = lane >= 8 && f1 == 0;
             if (r >= a && r < e && (r < f0 || r >= f1) && !same_group) {
-                const float w = __uint_as_float(static_cast<uint32_t>(join1(stage[r], smb[r])) << 16);
+                const uint32_t w = join1(stage[r], smb[r]);
                 const bool in_b = r >= split;
                 const uint32_t c = in_b ? r - split : cbase + r;
 #pragma unroll
                 for (int b = 0; b < B; ++b) {
-                    const float xf = __uint_as_float(static_cast<uint32_t>(__ldg(x + b * cols + c)) << 16);
+                    const uint32_t xb = __ldg(x + b * cols + c);
                     if (in_b)
-                        acc_b[b] = fmaf(w, xf, acc_b[b]);
+                        acc_b[b] = fma_bf16(w, xb, acc_b[b]);
                     else
-                        acc_a[b] = fmaf(w, xf, acc_a[b]);
+                        acc_a[b] = fma_bf16(w, xb, acc_a[b]);
                 }
             }
         }
@@ -1392,14 +1397,10 @@ __device__ __forceinline__ void warp_gemv(const uint8_t* stage, const TensorArgs
 #pragma unroll
             for (int b = 0; b < B; ++b) {
                 const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + b * cols + c));
-                float d = bf16_lo(wv4.x) * bf16_lo(xv.x);
-                d = fmaf(bf16_hi(wv4.x), bf16_hi(xv.x), d);
-                d = fmaf(bf16_lo(wv4.y), bf16_lo(xv.y), d);
-                d = fmaf(bf16_hi(wv4.y), bf16_hi(xv.y), d);
-                d = fmaf(bf16_lo(wv4.z), bf16_lo(xv.z), d);
-                d = fmaf(bf16_hi(wv4.z), bf16_hi(xv.z), d);
-                d = fmaf(bf16_lo(wv4.w), bf16_lo(xv.w), d);
-                d = fmaf(bf16_hi(wv4.w), bf16_hi(xv.w), d);
+                float d = fma_bf16x2(wv4.x, xv.x, 0.f);
+                d = fma_bf16x2(wv4.y, xv.y, d);
+                d = fma_bf16x2(wv4.z, xv.z, d);
+                d = fma_bf16x2(wv4.w, xv.w, d);
                 if (in_b)
                     acc_b[b] += d;
                 else
@@ -1920,10 +1921,9 @@ __global__ void fill_gemv_kernel(const uint8_t* __restrict__ sm, const uint64_t*
          r += warps) {
         float acc[kMaxBatch] = {0.f, 0.f, 0.f, 0.f};
         for (uint64_t c = lane; c < cols; c += 32) {
-            const float wf = __uint_as_float(static_cast<uint32_t>(join1(ror8(fill), sm[r * cols + c])) << 16);
+            const uint32_t wb = join1(ror8(fill), sm[r * cols + c]);
 #pragma unroll
-            for (int b = 0; b < B; ++b)
-                acc[b] = fmaf(wf, __uint_as_float(static_cast<uint32_t>(x[b * cols + c]) << 16), acc[b]);
+            for (int b = 0; b < B; ++b) acc[b] = fma_bf16(wb, x[b * cols + c], acc[b]);
         }
 #pragma unroll
         for (int b = 0; b < B; ++b) {
