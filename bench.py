@@ -38,6 +38,7 @@ if ROOT not in sys.path:
 METRIC = "decoded BF16 GB/s (and weights/s) per GB300; % of HBM roofline"
 WORKLOAD = "qwen3-14b-shaped decoder layer: q,o 5120x5120; k,v 1024x5120; gate,up 17408x5120; down 5120x17408; 2 norms 5120"
 FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2 ** 20  # GB300 L2
 
 
 def parse_args(argv=None):
@@ -415,7 +416,11 @@ def run_ours(args):
     if status.item() != 0:
         raise SystemExit(f"device status {status.item()}")
 
-    # timed region: K graph replays
+    # timed region: K graph replays.  A workload whose bytes would stay in L2
+    # (129 MB) between replays is timed launch by launch instead, with L2
+    # flushed before each (a 512 MB write, outside the events).
+    small = comp_total + elem_bytes(fmt) * n_total < 2 * L2_BYTES
+    flush = torch.empty(4 * L2_BYTES, dtype=torch.uint8, device=dev) if small else None
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             graph.replay()
@@ -423,17 +428,28 @@ def run_ours(args):
     barrier(world)
     sampler = ClockSampler(local)
     time.sleep(0.3)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for _ in range(args.steps):
-            graph.replay()
-        end.record(stream)
-    torch.cuda.synchronize()
+    if small:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        with torch.cuda.stream(stream):
+            for e0, e1 in evs:
+                flush.fill_(1)
+                e0.record(stream)
+                graph.replay()
+                e1.record(stream)
+        torch.cuda.synchronize()
+        ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / args.steps
+    else:
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            end.record(stream)
+        torch.cuda.synchronize()
+        ms = start.elapsed_time(end) / args.steps
     clocks = sampler.stop()
     barrier(world)
-    ms = start.elapsed_time(end) / args.steps
     ms = max_over_ranks(ms, world)
 
     # duration of the restore kernel itself: events on its stream around each
@@ -442,6 +458,8 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         graph.replay()
         for e0, e1 in ev:
+            if small:
+                flush.fill_(1)
             e0.record(stream)
             step()
             e1.record(stream)
@@ -470,7 +488,9 @@ def run_ours(args):
                    "bits_per_weight": 8 * comp_total / n_total,
                    "coded_exponent_bits_per_weight": sum(d.total_bits for *_, d in parts) / n_total,
                    "exponent_entropy_bits_per_weight": exponent_entropy_bits(parts),
-                   "l2": "inputs larger than L2: %.0f MB compressed read and %.0f MB written per step"
+                   "l2": ("L2 flushed before each timed launch (a 512 MB write outside the events): "
+                          if small else "inputs larger than L2: ")
+                         + "%.0f MB compressed read and %.0f MB written per step"
                          % (comp_total / 1e6, elem_bytes(fmt) * n_total / 1e6),
                    "launch": f"one afx_decode_batch call of {len(views)} tensors ({launches_per_step} kernel launches) "
                              "per step, replayed from a CUDA graph",
