@@ -192,3 +192,33 @@ def test_e4m3_and_fp16_layer_matrices_full_size(afx):
         for w, o in zip(ws, outs):
             got = o.cpu().numpy()
             assert np.array_equal(got if fmt == E4M3 else got.view(np.uint16), w)
+
+
+@pytest.mark.parametrize("n", [1, 7, 8, 9, 15, 16, 17, 1001])
+def test_fp16_single_exponent_fill_with_hi_bits(afx, n):
+    # every element in [1, 2): one exponent (15), all fraction bits in use
+    rng = np.random.default_rng(n)
+    w = (np.uint16(0x3C00) | rng.integers(0, 1024, size=n).astype(np.uint16)) ^ (
+        rng.integers(0, 2, size=n).astype(np.uint16) << np.uint16(15))
+    c, d = _check(afx, w, FP16, out_pad=16, out_offset=8)
+    assert d.nsym == 1 and d.fill == 15
+
+
+@pytest.mark.parametrize("T", [4, 8])
+def test_fp16_small_chunks_ragged(afx, T):
+    _check(afx, synth.normal_fp16(300_007, seed=T), FP16, chunk_bytes=T, out_pad=24)
+
+
+def test_fp16_host_resident_container(afx):
+    w = synth.normal_fp16(500_003, seed=29)
+    c, d = afx.encode(w, fmt=FP16)
+    out, status, intact = gpu_decode_any(afx, c, d, out_pad=16, host=True)
+    assert status == 0 and intact and np.array_equal(out, w)
+
+
+def test_fp16_every_hi_pattern_at_every_phase(afx):
+    # the 3-bit hi fields start at every bit phase (3i mod 8) with every value
+    vals = np.array([(e << 10) | (h << 7) | m for e in (13, 14, 15, 16) for h in range(8) for m in (0, 5, 127)],
+                    np.uint16)
+    w = np.resize(np.random.default_rng(3).permutation(vals), 8 * 97 + 5)
+    _check(afx, w, FP16, out_pad=16)
