@@ -49,6 +49,9 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-extras", action="store_true", help="skip e2e and cpu_baseline legs")
+    p.add_argument("--config", type=int, choices=[1, 2, 3, 4, 5], default=None,
+                   help="the five workloads by number: 1 the 4096x4096 matrix, 2 the layer, 3 the whole model, "
+                        "4 the 2^28 adversarial tensor, 5 the layer with the 40-layer streaming leg")
     p.add_argument("--legs", default="all",
                    help="extra legs to run after the headline (comma list of e2e, zero_copy, cpu_baseline, gemv, "
                         "stream, prefill, formats; default all)")
@@ -56,7 +59,12 @@ def parse_args(argv=None):
                    help="layer (default: one Qwen3-14B-shaped decoder layer), matrix4096, adversarial "
                         "(2^28 heavy-tailed), tensor:<name> (one tensor of the layer), layer-fp16 or layer-e4m3 "
                         "(the layer in the other element formats)")
-    return p.parse_args(argv)
+    args = p.parse_args(argv)
+    if args.config is not None:
+        args.workload = {1: "matrix4096", 2: "layer", 3: "model", 4: "adversarial", 5: "layer"}[args.config]
+        if args.config == 5:
+            args.legs = "stream"
+    return args
 
 
 # ---- distributed plumbing (barrier and max over ranks only) ----------------------

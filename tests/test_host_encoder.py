@@ -207,3 +207,17 @@ def test_bf16_containers_are_unchanged_by_the_format_field(afx):
     assert d.format == afx.AFX_FMT_BF16 and not c[108:112].any()
     c2, d2 = afx.encode(w, fmt=afx.AFX_FMT_BF16)
     assert np.array_equal(c, c2)
+
+
+def test_container_survives_a_file_round_trip(afx, tmp_path):
+    # the container is the persistence format: bytes written to a file and
+    # read back parse to the same description and decode to the same weights
+    w = synth.normal(123_457, seed=19)
+    c, d = afx.encode(w)
+    path = tmp_path / "tensor.afx"
+    c.tofile(path)
+    back = np.fromfile(path, dtype=np.uint8)
+    assert np.array_equal(back, c)
+    assert afx.desc_dict(afx.afx_parse_header(back)) == afx.desc_dict(d)
+    out, st = oracle.decode(back)
+    assert st == oracle.OK and np.array_equal(out, w)
