@@ -221,3 +221,34 @@ def test_container_survives_a_file_round_trip(afx, tmp_path):
     assert afx.desc_dict(afx.afx_parse_header(back)) == afx.desc_dict(d)
     out, st = oracle.decode(back)
     assert st == oracle.OK and np.array_equal(out, w)
+
+
+@pytest.mark.parametrize("fmt,n,T", [(0, 6_000_011, 0), (0, 5_000_000, 4), (1, 4_000_003, 16), (2, 3_000_017, 8),
+                                     (0, 2_097_152, 4)])
+def test_parallel_encoder_is_byte_identical_to_the_oracle(afx, fmt, n, T):
+    # large enough for several encoder threads (one per million elements):
+    # the segment edges, shared stream words and shared chunk entries merge
+    # to the oracle's single-pass container
+    w = (synth.normal(n, seed=n) if fmt == 0 else synth.normal_fp16(n, seed=n) if fmt == 1
+         else synth.normal_e4m3(n, seed=n))
+    code = afx.afx_build_code_fmt(w, fmt)
+    desc = afx.afx_encode_bound(w.size, code, T, 256 if T == 4 else 0)
+    c = afx.afx_encode(w, code, desc)
+    ref = oracle.encode(w, np.array(code.len[:], np.uint8), desc.chunk_bytes, desc.block_chunks, fmt=fmt)
+    assert np.array_equal(c, ref)
+
+
+def test_encode_refuses_elements_that_do_not_match_the_plan(afx):
+    # the code and plan of one tensor, the elements of another whose codes
+    # are longer: refused before any stream byte is written
+    w1 = synth.normal(2_000_000, seed=1)
+    code = afx.afx_build_code(w1)
+    desc = afx.afx_encode_bound(w1.size, code)
+    w2 = synth.normal(2_000_000, 0.0, 0.0002, seed=2)  # exponents from the code's rare, long end
+    lens = np.array(code.len[:], np.uint8)
+    w2 = np.where(lens[(w2 >> 7) & 0xFF] > 0, w2, w1).astype(np.uint16)  # keep every symbol coded
+    assert int(lens[(w2 >> 7) & 0xFF].astype(np.int64).sum()) > desc.total_bits
+    out = np.zeros(desc.container_bytes, np.uint8)
+    with pytest.raises(afx.AfxError):
+        afx.afx_encode(w2, code, desc, out=out)
+    assert not out[desc.off_exp: desc.off_sm].any()  # nothing of the stream was written

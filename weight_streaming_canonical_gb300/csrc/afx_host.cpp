@@ -304,67 +304,180 @@ afx_status afx_encode(const void* w, uint64_t n, const afx_code* code, const afx
     put_le(h + 112, 8, d->off_hi);
     std::memcpy(h + 256, code->len, 256);
 
-    uint8_t* sm = dst + d->off_sm;
-    if (fmt == AFX_FMT_E4M3) {
-        for (uint64_t i = 0; i < n; ++i) sm[i / 2] |= static_cast<uint8_t>(raw_of(fmt, element(w, fmt, i)) << (4 * (i & 1)));
-    } else {
-        for (uint64_t i = 0; i < n; ++i) sm[i] = static_cast<uint8_t>(raw_of(fmt, element(w, fmt, i)));
-    }
-    if (fmt == AFX_FMT_FP16) {  // the 3 leading fraction bits, packed lowest bit first
-        uint8_t* hs = dst + d->off_hi;
-        for (uint64_t i = 0; i < n; ++i) {
-            const uint32_t h3 = (element(w, fmt, i) >> 7) & 0x7u;
-            const uint64_t bit = 3 * i;
-            hs[bit >> 3] |= static_cast<uint8_t>(h3 << (bit & 7));
-            if ((bit & 7) > 5) hs[(bit >> 3) + 1] |= static_cast<uint8_t>(h3 >> (8 - (bit & 7)));
+    // The work is split into segments of whole groups of 8 elements (so every
+    // raw byte, nibble pair and hi-section byte has one writer), run on
+    // worker threads.
+    const unsigned workers = worker_count(n);
+    std::vector<uint64_t> seg(workers + 1);
+    for (unsigned k = 0; k <= workers; ++k) seg[k] = std::min<uint64_t>(n, (n * k / workers + 7) & ~uint64_t{7});
+    seg[workers] = n;
+    auto parallel = [&](auto&& fn) {
+        if (workers == 1) {
+            fn(0u);
+            return;
         }
-    }
+        std::vector<std::thread> pool;
+        for (unsigned k = 0; k < workers; ++k) pool.emplace_back(fn, k);
+        for (auto& t : pool) t.join();
+    };
+
+    uint8_t* sm = dst + d->off_sm;
+    uint8_t* hs = fmt == AFX_FMT_FP16 ? dst + d->off_hi : nullptr;
+    std::vector<char> off_fill(workers, 0);  // single-symbol tensors: an element with another symbol
+    parallel([&](unsigned k) {
+        for (uint64_t i = seg[k]; i < seg[k + 1]; ++i) {
+            const unsigned v = element(w, fmt, i);
+            if (d->nsym <= 1 && symbol_of(fmt, v) != d->fill) off_fill[k] = 1;
+            if (fmt == AFX_FMT_E4M3) {
+                sm[i / 2] |= static_cast<uint8_t>(raw_of(fmt, v) << (4 * (i & 1)));
+            } else {
+                sm[i] = static_cast<uint8_t>(raw_of(fmt, v));
+            }
+            if (fmt == AFX_FMT_FP16) {  // the 3 leading fraction bits, packed lowest bit first
+                const uint32_t h3 = (v >> 7) & 0x7u;
+                const uint64_t bit = 3 * i;
+                hs[bit >> 3] |= static_cast<uint8_t>(h3 << (bit & 7));
+                if ((bit & 7) > 5) hs[(bit >> 3) + 1] |= static_cast<uint8_t>(h3 >> (8 - (bit & 7)));
+            }
+        }
+    });
 
     if (d->nsym <= 1) {
-        for (uint64_t i = 0; i < n; ++i)
-            if (symbol_of(fmt, element(w, fmt, i)) != d->fill) return AFX_E_ARG;
+        for (unsigned k = 0; k < workers; ++k)
+            if (off_fill[k]) return AFX_E_ARG;
         if (d->total_bits != 0) return AFX_E_ARG;
         put_le(dst + d->off_block, 8, n);
         return AFX_OK;
     }
 
-    // Bit packing into u32 words, most significant bit first, with the
-    // chunk index updated as each codeword starts.
+    // Pass 1: each segment's coded bits.  The stream is written only when
+    // they add up to the plan's total, so elements that do not match the code
+    // cannot write past the stream section.
+    std::vector<uint64_t> seg_bits(workers, 0);
+    std::vector<char> seg_bad(workers, 0);
+    parallel([&](unsigned k) {
+        uint64_t bits = 0;
+        for (uint64_t i = seg[k]; i < seg[k + 1]; ++i) {
+            const unsigned l = code->len[symbol_of(fmt, element(w, fmt, i))];
+            if (l == 0) seg_bad[k] = 1;
+            bits += l;
+        }
+        seg_bits[k] = bits;
+    });
+    std::vector<uint64_t> seg_start(workers + 1, 0);
+    for (unsigned k = 0; k < workers; ++k) {
+        if (seg_bad[k]) return AFX_E_ARG;
+        seg_start[k + 1] = seg_start[k] + seg_bits[k];
+    }
+    if (seg_start[workers] != d->total_bits) return AFX_E_ARG;
+
+    // Pass 2: bit packing into u32 words, most significant bit first, with
+    // the chunk index updated as each codeword starts.  A segment's first
+    // and last word, and its first and last chunk entry, may be shared with
+    // its neighbours: those are kept aside and merged after the workers.
     uint8_t* words = dst + d->off_exp;
     uint8_t* chunk_index = dst + d->off_chunk;
     const unsigned chunk_shift = static_cast<unsigned>(__builtin_ctz(8u * d->chunk_bytes));
-    uint64_t acc = 0;
-    unsigned acc_bits = 0;
-    uint64_t pos = 0, word_i = 0;
-    uint64_t cur_chunk = ~uint64_t{0};
-    uint32_t cur_count = 0, cur_gap = 0;
-    auto flush_chunk = [&]() {
-        if (cur_chunk != ~uint64_t{0}) put_le(chunk_index + 2 * cur_chunk, 2, cur_gap | (cur_count << 5));
+    struct Edge {
+        uint64_t word_i = ~uint64_t{0};
+        uint32_t word = 0;
+        uint64_t chunk = ~uint64_t{0};
+        uint32_t gap = 0, count = 0;
     };
-    for (uint64_t i = 0; i < n; ++i) {
-        const unsigned e = symbol_of(fmt, element(w, fmt, i));
-        const unsigned l = code->len[e];
-        if (l == 0) return AFX_E_ARG;
-        const uint64_t chunk = pos >> chunk_shift;
-        if (chunk != cur_chunk) {
-            flush_chunk();
-            cur_chunk = chunk;
-            cur_count = 0;
-            cur_gap = static_cast<uint32_t>(pos - (chunk << chunk_shift));
+    std::vector<Edge> head(workers), tail(workers);
+    parallel([&](unsigned k) {
+        if (seg[k] == seg[k + 1]) return;
+        uint64_t pos = seg_start[k];
+        uint64_t word_i = pos >> 5;
+        unsigned acc_bits = static_cast<unsigned>(pos & 31);  // bits of the word before this segment's (zeros)
+        uint64_t acc = 0;
+        bool first_word = true, first_chunk = true;
+        uint64_t cur_chunk = ~uint64_t{0};
+        uint32_t cur_count = 0, cur_gap = 0;
+        auto flush_chunk = [&]() {
+            if (cur_chunk == ~uint64_t{0}) return;
+            if (first_chunk) {
+                head[k].chunk = cur_chunk;
+                head[k].gap = cur_gap;
+                head[k].count = cur_count;
+                first_chunk = false;
+            } else {
+                put_le(chunk_index + 2 * cur_chunk, 2, cur_gap | (cur_count << 5));
+            }
+        };
+        for (uint64_t i = seg[k]; i < seg[k + 1]; ++i) {
+            const unsigned e = symbol_of(fmt, element(w, fmt, i));
+            const unsigned l = code->len[e];
+            const uint64_t chunk = pos >> chunk_shift;
+            if (chunk != cur_chunk) {
+                flush_chunk();
+                cur_chunk = chunk;
+                cur_count = 0;
+                cur_gap = static_cast<uint32_t>(pos - (chunk << chunk_shift));
+            }
+            ++cur_count;
+            acc = (acc << l) | code->code[e];
+            acc_bits += l;
+            pos += l;
+            if (acc_bits >= 32) {
+                acc_bits -= 32;
+                const uint32_t out = static_cast<uint32_t>(acc >> acc_bits);
+                if (first_word) {
+                    head[k].word_i = word_i;
+                    head[k].word = out;
+                    first_word = false;
+                } else {
+                    put_le(words + 4 * word_i, 4, out);
+                }
+                ++word_i;
+                acc &= (uint64_t{1} << acc_bits) - 1;
+            }
         }
-        ++cur_count;
-        acc = (acc << l) | code->code[e];
-        acc_bits += l;
-        pos += l;
-        if (acc_bits >= 32) {
-            acc_bits -= 32;
-            put_le(words + 4 * word_i++, 4, static_cast<uint32_t>(acc >> acc_bits));
-            acc &= (uint64_t{1} << acc_bits) - 1;
+        // the last chunk entry and the partial last word go to the merge
+        tail[k].chunk = cur_chunk;
+        tail[k].gap = cur_gap;
+        tail[k].count = cur_count;
+        if (first_chunk) {  // the segment's codes all started in one chunk: that entry is its head
+            head[k].chunk = ~uint64_t{0};
         }
+        if (acc_bits) {
+            tail[k].word_i = word_i;
+            tail[k].word = static_cast<uint32_t>(acc << (32 - acc_bits));
+        }
+    });
+    // merge the edges in segment order: words by OR (each side's bits of a
+    // shared word are zero in the other's), chunk entries by adding counts
+    // (the gap is that of the first code starting in the chunk)
+    uint64_t open_chunk = ~uint64_t{0};
+    uint32_t open_gap = 0, open_count = 0;
+    auto emit = [&](uint64_t chunk, uint32_t gap, uint32_t count) {
+        if (chunk == ~uint64_t{0}) return;
+        if (chunk == open_chunk) {
+            open_count += count;
+            return;
+        }
+        if (open_chunk != ~uint64_t{0}) put_le(chunk_index + 2 * open_chunk, 2, open_gap | (open_count << 5));
+        open_chunk = chunk;
+        open_gap = gap;
+        open_count = count;
+    };
+    for (unsigned k = 0; k < workers; ++k) {
+        for (const Edge* e : {&head[k], &tail[k]})
+            if (e->word_i != ~uint64_t{0}) {
+                const uint32_t v = static_cast<uint32_t>(get_le(words + 4 * e->word_i, 4)) | e->word;
+                put_le(words + 4 * e->word_i, 4, v);
+            }
+        if (seg[k] == seg[k + 1]) continue;
+        emit(head[k].chunk, head[k].gap, head[k].count);
+        // chunks the segment wrote itself lie between its head and tail: the
+        // open entry (the head's) closes before them
+        if (tail[k].chunk != head[k].chunk && head[k].chunk != ~uint64_t{0} && open_chunk == head[k].chunk) {
+            put_le(chunk_index + 2 * open_chunk, 2, open_gap | (open_count << 5));
+            open_chunk = ~uint64_t{0};
+        }
+        emit(tail[k].chunk, tail[k].gap, tail[k].count);
     }
-    flush_chunk();
-    if (acc_bits) put_le(words + 4 * word_i, 4, static_cast<uint32_t>(acc << (32 - acc_bits)));
-    if (pos != d->total_bits) return AFX_E_ARG;
+    if (open_chunk != ~uint64_t{0}) put_le(chunk_index + 2 * open_chunk, 2, open_gap | (open_count << 5));
 
     // Block index: weights before each block's first chunk.
     uint8_t* block_index = dst + d->off_block;
