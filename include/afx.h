@@ -210,7 +210,8 @@ afx_status afx_decode_gemv_workspace(const afx_desc* desc, uint32_t batch, uint6
  * b < batch (1..4), where W is the container's weights viewed row-major as
  * [rows][cols] (rows * cols == n; a row is one output, PyTorch nn.Linear
  * layout) and x_dev is BF16 [batch][cols].  The restored weights never go
- * to global memory.  Products and sums are float32; y_dev is float32
+ * to global memory.  Each BF16 product is added into a float32 sum with
+ * one rounding (fma.rn.f32.bf16); y_dev is float32
  * [batch][rows], overwritten, and bitwise reproducible run to run.
  * workspace_dev: afx_decode_gemv_workspace bytes of device memory, 16-byte
  * aligned, contents ignored.  Requires a BF16 container in device memory,
