@@ -39,6 +39,14 @@ METRIC = "decoded BF16 GB/s (and weights/s) per GB300; % of HBM roofline"
 WORKLOAD = "qwen3-14b-shaped decoder layer: q,o 5120x5120; k,v 1024x5120; gate,up 17408x5120; down 5120x17408; 2 norms 5120"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20  # GB300 L2
+BUSY_PAD_S = 0.5  # seconds of untimed identical steps on each side of the timed ones
+
+
+def busy_pad_steps(step_ms: float) -> int:
+    """Steps that fill about BUSY_PAD_S of GPU time (at least 1, at most 20000)."""
+    if not step_ms > 0:
+        return 1
+    return max(1, min(20000, int(BUSY_PAD_S * 1e3 / step_ms + 0.5)))
 
 
 def parse_args(argv=None):
@@ -212,22 +220,68 @@ def algorithmic_bytes(d) -> int:
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms with the
+    sample's wall-clock time.  stop(window) keeps the samples taken inside the
+    host-time window (t0, t1) during which the GPU was kept busy around the
+    timed steps."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.proc = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
 
-    def stop(self):
+    @staticmethod
+    def _wall(stamp: str):
+        import datetime
+        try:
+            return datetime.datetime.strptime(stamp, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
+    @classmethod
+    def summarize(cls, lines, window=None):
+        """Median SM clock, highest max clock, median power and the throttle
+        reasons seen, over the samples inside window (all samples when none
+        falls inside it or no window is given)."""
+        rows = []
+        for line in lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm, mx = float(f[1]), float(f[2])
+            except ValueError:
+                continue
+            try:
+                watts = float(f[3])
+            except ValueError:
+                watts = None
+            active = {name for name, val in zip(cls.REASONS, f[5:9]) if val.lower() == "active"}
+            rows.append((cls._wall(f[0]), sm, mx, watts, active))
+        if not rows:
+            return None
+        inside = rows
+        if window is not None:
+            t0, t1 = window
+            inside = [r for r in rows if r[0] is not None and t0 <= r[0] <= t1]
+        scope = "samples taken while the GPU ran the timed steps and the same work around them"
+        if not inside:
+            inside, scope = rows, "no sample fell inside the busy window: all samples of the run"
+        watts = [r[3] for r in inside if r[3] is not None]
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": sorted(set().union(*(r[4] for r in inside))), "samples": len(inside),
+                "power_w": statistics.median(watts) if watts else None, "scope": scope}
+
+    def stop(self, window=None):
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -236,24 +290,7 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 8:
-                continue
-            try:
-                sm.append(float(f[0]))
-                mx.append(float(f[1]))
-            except ValueError:
-                continue
-            for name, val in zip(names, f[4:8]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return self.summarize(out.splitlines(), window)
 
 
 def profiled_traffic(kernel: str, workload: str):
@@ -429,14 +466,35 @@ def run_ours(args):
     # flushed before each (a 512 MB write, outside the events).
     small = comp_total + elem_bytes(fmt) * n_total < 2 * L2_BYTES
     flush = torch.empty(4 * L2_BYTES, dtype=torch.uint8, device=dev) if small else None
+
+    def one_step():
+        if small:
+            flush.fill_(1)
+        graph.replay()
+
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             graph.replay()
     torch.cuda.synchronize()
+    # the timed steps sit inside a busy window of the same work (about
+    # BUSY_PAD_S of it on each side, outside the events), so that the clock
+    # samples, 100 ms apart, are taken under this load
+    est0, est1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        est0.record(stream)
+        for _ in range(3):
+            one_step()
+        est1.record(stream)
+    torch.cuda.synchronize()
+    pad = busy_pad_steps(est0.elapsed_time(est1) / 3)
     barrier(world)
     sampler = ClockSampler(local)
     time.sleep(0.3)
     torch.cuda.synchronize()
+    busy_t0 = time.time()
+    with torch.cuda.stream(stream):
+        for _ in range(pad):
+            one_step()
     if small:
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
         with torch.cuda.stream(stream):
@@ -445,6 +503,8 @@ def run_ours(args):
                 e0.record(stream)
                 graph.replay()
                 e1.record(stream)
+            for _ in range(pad):
+                one_step()
         torch.cuda.synchronize()
         ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / args.steps
     else:
@@ -454,9 +514,14 @@ def run_ours(args):
             for _ in range(args.steps):
                 graph.replay()
             end.record(stream)
+            for _ in range(pad):
+                one_step()
         torch.cuda.synchronize()
         ms = start.elapsed_time(end) / args.steps
-    clocks = sampler.stop()
+    busy_t1 = time.time()
+    clocks = sampler.stop((busy_t0, busy_t1))
+    if clocks is not None:
+        clocks["busy_pad_steps_each_side"] = pad
     barrier(world)
     ms = max_over_ranks(ms, world)
 
