@@ -611,6 +611,8 @@ def run_ours(args):
                 line["residency_plan"] = run_residency_plan(afx, parts, b / 1e9, value)
             if "prefill" in legs:
                 line["prefill"] = run_prefill_bench(afx, parts, dev_blob, offs, dev, args)
+            if "gemv" in legs and "prefill" in legs:
+                line["fused_gemv"]["vs_restore_then_gemm"] = fused_vs_unfused(line["fused_gemv"], line["prefill"])
             if "formats" in legs:
                 line["formats"] = run_formats_bench(afx, dev, args)
     if rank == 0:
@@ -766,7 +768,8 @@ def run_prefill_bench(afx, parts, dev_blob, offs, dev, args):
         restore_one_launch_ms = timed(lambda: afx.afx_decode_batch(descs, conts, whole_views, stream=gs), gs)
     out["restore_ms_per_matrix_launches"] = restore_ms
     out["restore_ms_one_launch"] = restore_one_launch_ms
-    for n_tok in (128, 512, 2048):
+    for n_tok in (1, 4, 128, 512, 2048):
+        reps = 20 if n_tok <= 4 else 5
         xs = [torch.from_numpy(synth.activations(n_tok, cl, seed=21).view(np.int16)).to(dev) for _, cl in mshapes]
         ys = [torch.empty((n_tok, r), dtype=torch.float32, device=dev) for r, _ in mshapes]
 
@@ -781,9 +784,9 @@ def run_prefill_bench(afx, parts, dev_blob, offs, dev, args):
         def one_launch():
             afx.afx_prefill_batch(descs, conts, mshapes, xs, ys, [whole, None], ws, gemm_stream=gs)
 
-        seq_ms = timed(sequential, gs)
-        ovl_ms = timed(overlapped, gs)
-        one_ms = timed(one_launch, gs)
+        seq_ms = timed(sequential, gs, reps)
+        ovl_ms = timed(overlapped, gs, reps)
+        one_ms = timed(one_launch, gs, reps)
         gemm_ms = max(seq_ms - restore_ms, 1e-9)
         best = min(seq_ms, ovl_ms, one_ms)
         flop = 2.0 * n_w * n_tok
@@ -797,6 +800,24 @@ def run_prefill_bench(afx, parts, dev_blob, offs, dev, args):
                    "float32 accumulation; sequential: restore then product per matrix on one stream; overlapped: "
                    "restore of matrix i+1 on a second stream; one restore launch: all seven restored by one "
                    "afx_decode_batch launch, then the products; tokens_per_s and tflops from the fastest")
+    return out
+
+
+def fused_vs_unfused(fused: dict, prefill: dict) -> dict:
+    """The fused product against the unfused path at the same batch: all
+    seven matrices restored to BF16 in HBM scratch, then cuBLAS products
+    (afx_prefill_batch, fastest of its three forms).  ratio > 1: the fused
+    product is faster."""
+    runs = {r["tokens"]: r for r in prefill.get("runs", [])}
+    out = {}
+    for B in (1, 4):
+        f, r = fused.get(f"batch{B}"), runs.get(B)
+        if not f or not r:
+            continue
+        form, unfused = min((("sequential", r["sequential_ms"]), ("overlapped", r["overlapped_ms"]),
+                             ("one_restore_launch", r["one_restore_launch_ms"])), key=lambda kv: kv[1])
+        out[f"batch{B}"] = {"fused_ms": f["ms"], "restore_then_gemm_ms": unfused, "unfused_form": form,
+                            "unfused_over_fused": unfused / f["ms"]}
     return out
 
 

@@ -1342,20 +1342,55 @@ __device__ __forceinline__ void warp_store(const uint8_t* stage, const uint8_t* 
     }
 }
 
-__device__ __forceinline__ float warp_sum_f(float v) {
+// The 8 weights of group w times x[b][c .. c + 8) added into acc[b], for
+// every b (x[b][c] at x + b * cols + c; B * cols < 2^31 on this path).
+template <int B>
+__device__ __forceinline__ void gemv_group(const uint4& w, const uint16_t* x, uint32_t cols, uint32_t c,
+                                           float (&acc)[B]) {
 #pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, d);
-    return v;
+    for (int b = 0; b < B; ++b) {
+        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + (b * cols + c)));
+        float d = fma_bf16x2(w.x, xv.x, acc[b]);
+        d = fma_bf16x2(w.y, xv.y, d);
+        d = fma_bf16x2(w.z, xv.z, d);
+        acc[b] = fma_bf16x2(w.w, xv.w, d);
+    }
+}
+
+// Sums the V values v[0 .. V) (V a power of two, at most 32) over the 32
+// lanes with one transposed butterfly: in each of the first log2(V) steps a
+// lane keeps one half of its values and adds the half its partner sends
+// for them, so that afterwards lane L holds a partial of value
+// L >> (5 - log2 V) only; the remaining steps complete that sum.  Returns
+// it; every lane gets the sum of its value.
+template <int V>
+__device__ __forceinline__ float warp_sum_transposed(float (&v)[V], int lane) {
+    int m = 16;
+#pragma unroll
+    for (int c = V; c > 1; c >>= 1, m >>= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int k = 0; k < c / 2; ++k) {
+            const float send = upper ? v[k] : v[k + c / 2];
+            const float keep = upper ? v[k + c / 2] : v[k];
+            v[k] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, m);
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (; m >= 1; m >>= 1) r += __shfl_xor_sync(0xFFFFFFFFu, r, m);
+    return r;
 }
 
 // y[b][r] += sum over the weights [o0, o0 + count) of row r of W[r][c] x[b][c],
 // for a matrix whose rows are at least kWarpStage weights long and a
 // multiple of 8: a sub-tile meets at most two rows (r_a and r_a + 1) and no
 // group of 8 straddles two rows.  Each lane keeps float32 sums for the two
-// rows; a fixed butterfly reduces them, and lane 0 stores the sub-tile's
-// start and its two row partials in the workspace (zeros when the sub-tile
-// is not valid).  gemv_fixup_warp_kernel adds each row's partials in
-// sub-tile order, so y does not depend on how the grid split the work.
+// rows (the full groups of row r_a first, then those of row r_a + 1); one
+// transposed butterfly reduces all 2B of them, and the workspace gets the
+// sub-tile's start and its two row partials (zeros when the sub-tile is not
+// valid).  gemv_fixup_warp_kernel adds each row's partials in sub-tile
+// order, so y does not depend on how the grid split the work.
 template <int B>
 __device__ __forceinline__ void warp_gemv(const uint8_t* stage, const TensorArgs& t, uint64_t s, uint64_t o0,
                                           uint32_t count, bool ok, int lane) {
@@ -1372,6 +1407,7 @@ __device__ __forceinline__ void warp_gemv(const uint8_t* stage, const TensorArgs
         const uint32_t cbase = static_cast<uint32_t>(ob0 - ra * cols);  // column of relative index 0 in row r_a
         const uint8_t* smb = t.sm + ob0;
         const uint16_t* x = t.x;
+        const uint32_t cols32 = static_cast<uint32_t>(cols);
         const uint32_t f0 = (a + 7) & ~7u, f1 = e & ~7u;  // full groups [f0, f1)
         if (lane < 16) {  // weights outside the full groups, one per lane
             const uint32_t r = lane < 8 ? lane : f1 + (lane & 7);
@@ -1382,7 +1418,7 @@ __device__ __forceinline__ void warp_gemv(const uint8_t* stage, const TensorArgs
                 const uint32_t c = in_b ? r - split : cbase + r;
 #pragma unroll
                 for (int b = 0; b < B; ++b) {
-                    const uint32_t xb = __ldg(x + b * cols + c);
+                    const uint32_t xb = __ldg(x + (b * cols32 + c));
                     if (in_b)
                         acc_b[b] = fma_bf16(w, xb, acc_b[b]);
                     else
@@ -1390,39 +1426,28 @@ __device__ __forceinline__ void warp_gemv(const uint8_t* stage, const TensorArgs
                 }
             }
         }
-        for (uint32_t r = f0 + 8 * lane; r < f1; r += 8 * 32) {
-            const uint4 wv4 = join8(*reinterpret_cast<const uint2*>(stage + r), __ldg(reinterpret_cast<const uint2*>(smb + r)));
-            const bool in_b = r >= split;
-            const uint32_t c = in_b ? r - split : cbase + r;
-#pragma unroll
-            for (int b = 0; b < B; ++b) {
-                const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + b * cols + c));
-                float d = fma_bf16x2(wv4.x, xv.x, 0.f);
-                d = fma_bf16x2(wv4.y, xv.y, d);
-                d = fma_bf16x2(wv4.z, xv.z, d);
-                d = fma_bf16x2(wv4.w, xv.w, d);
-                if (in_b)
-                    acc_b[b] += d;
-                else
-                    acc_a[b] += d;
-            }
-        }
+        // full groups of row r_a: [f0, mid); of row r_a + 1: [mid, f1)
+        const uint32_t mid = split < f1 ? (split > f0 ? split : f0) : f1;
+        for (uint32_t r = f0 + 8 * lane; r < mid; r += 8 * 32)
+            gemv_group<B>(join8(*reinterpret_cast<const uint2*>(stage + r), __ldg(reinterpret_cast<const uint2*>(smb + r))),
+                          x, cols32, cbase + r, acc_a);
+        for (uint32_t r = mid + 8 * lane; r < f1; r += 8 * 32)
+            gemv_group<B>(join8(*reinterpret_cast<const uint2*>(stage + r), __ldg(reinterpret_cast<const uint2*>(smb + r))),
+                          x, cols32, r - split, acc_b);
     }
+    constexpr int V = B == 1 ? 2 : B == 2 ? 4 : 8;  // 2B values, padded to a power of two
+    float v[V];
 #pragma unroll
-    for (int b = 0; b < B; ++b) {
-        acc_a[b] = warp_sum_f(acc_a[b]);
-        acc_b[b] = warp_sum_f(acc_b[b]);
-    }
-    if (lane == 0) {
-        uint64_t* ws_o0 = reinterpret_cast<uint64_t*>(t.ws);
-        float* part = reinterpret_cast<float*>(ws_o0 + t.n_blocks * kSubtilesPerBlock);
-        ws_o0[s] = o0;
-#pragma unroll
-        for (int b = 0; b < B; ++b) {
-            part[(s * 2) * B + b] = acc_a[b];
-            part[(s * 2 + 1) * B + b] = acc_b[b];
-        }
-    }
+    for (int j = 0; j < V; ++j) v[j] = j < B ? acc_a[j] : j < 2 * B ? acc_b[j - B] : 0.f;
+    const float sum = warp_sum_transposed<V>(v, lane);
+    // lane L holds value j = L / (32 / V): row r_a's batch j for j < B, row
+    // r_a + 1's batch j - B for B <= j < 2B; part[s][2B] is laid out the same way
+    constexpr int kLanesPerValue = 32 / V;
+    const int j = lane / kLanesPerValue;
+    uint64_t* ws_o0 = reinterpret_cast<uint64_t*>(t.ws);
+    float* part = reinterpret_cast<float*>(ws_o0 + t.n_blocks * kSubtilesPerBlock);
+    if (lane % kLanesPerValue == 0 && j < 2 * B) part[s * 2 * B + j] = sum;
+    if (lane == 0) ws_o0[s] = o0;
 }
 
 // Joins and stores `count` E4M3 elements from o0 with the 32 lanes of a
@@ -2339,7 +2364,11 @@ namespace {
 
 // Rows long enough for the warp GEMV: a sub-tile (at most kWarpStage - 16
 // weights) then meets at most two rows, and rows start on groups of 8.
-bool warp_gemv_shape(uint32_t cols) { return cols >= static_cast<uint32_t>(kWarpStage) && cols % 8 == 0; }
+// Rows of at least kWarpStage weights, a multiple of 8, and short enough
+// that kMaxBatch * cols indexes x in 32 bits.
+bool warp_gemv_shape(uint32_t cols) {
+    return cols >= static_cast<uint32_t>(kWarpStage) && cols % 8 == 0 && cols <= (1u << 29);
+}
 
 template <int B>
 afx_status gemv_batch(const afx_desc* descs, const void* const* containers, const uint32_t* rows,
