@@ -70,6 +70,24 @@ def test_unit_vector_gives_a_column_exactly(afx):
         assert np.array_equal(y[0], col)
 
 
+@pytest.mark.parametrize("B", [2, 3, 4])
+def test_unit_vector_per_batch_row_gives_its_own_column_exactly(afx, B):
+    # batch row b selects column j_b: every (row, batch) sum has one nonzero
+    # product, so y[b] is W[:, j_b] exactly and a sum sent to the wrong
+    # (row, batch) slot by the reduction shows up as a wrong column
+    rows, cols = 300, 5120
+    W = synth.normal(rows * cols, seed=6).reshape(rows, cols)
+    js = [0, 5119, 2500, 4095][:B]
+    x = np.zeros((B, cols), np.uint16)
+    for b, j in enumerate(js):
+        x[b, j] = 0x3F80
+    c, d = afx.encode(W.reshape(-1))
+    y, status = gpu_gemv(afx, c, d, rows, cols, x)
+    assert status == 0
+    for b, j in enumerate(js):
+        assert np.array_equal(y[b], (W[:, j].astype(np.uint32) << 16).view(np.float32)), (b, j)
+
+
 def test_zero_activation_gives_zero(afx):
     W = synth.normal(64 * 5120, seed=2).reshape(64, 5120)
     c, d = afx.encode(W.reshape(-1))
