@@ -940,11 +940,7 @@ struct WarpSlot {
 // first-code lengths, or the state table), one WarpSlot per warp and two
 // stream buffers per warp.
 struct SharedW {
-    uint32_t limit[AFX_MAX_CODE_LEN + 1];
-    int32_t base[AFX_MAX_CODE_LEN + 1];
-    uint32_t state_base[AFX_MAX_CODE_LEN + 1];
-    uint8_t sorted[256];
-    uint8_t depth[64];               // depth of each state's node
+    alignas(16) CodeTables ct;       // the tensor's code tables, copied from the launch parameters
     alignas(16) uint16_t first[kLutSize];  // first code of a 12-bit peek: length << 8 | stage byte
     alignas(16) uint8_t tab[16];     // start of the table region
 };
@@ -996,36 +992,45 @@ __device__ __forceinline__ uint32_t stream_window(const uint32_t* stream, uint32
 // code that ends within those bits, and names the node of the bits left
 // over.  Other tensors: up to three first codes chained per 12-bit peek.
 __device__ void build_tables_w(SharedW& sh, uint8_t* tabr, const CodeTables& tab, int tid, int nthreads) {
-    for (int i = tid; i <= AFX_MAX_CODE_LEN; i += nthreads) {
-        sh.limit[i] = tab.limit[i];
-        sh.base[i] = tab.base[i];
-        sh.state_base[i] = tab.state_base[i];
+    {   // warp w copies words w, w + nwarps, ... of the launch parameters' tables;
+        // the lanes of a warp read the same word, one access for the warp
+        static_assert(sizeof(CodeTables) % 4 == 0, "CodeTables is copied as words");
+        constexpr int kWords = sizeof(CodeTables) / 4;
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(&tab);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(&sh.ct);
+        const int nw = nthreads >> 5;
+        for (int j = tid >> 5; j < kWords; j += nw) {
+            const uint32_t v = src[j];
+            if ((tid & 31) == 0) dst[j] = v;
+        }
     }
-    for (int i = tid; i < 256; i += nthreads) sh.sorted[i] = tab.sorted[i];
-    for (int i = tid; i < kMaxStates; i += nthreads) sh.depth[i] = tab.state_depth[i];
     __syncthreads();
+    const uint32_t* const limit = sh.ct.limit;
+    const int32_t* const base = sh.ct.base;
+    const uint32_t* const state_base = sh.ct.state_base;
+    const uint8_t* const sorted = sh.ct.sorted;
     for (int p0 = tid * 4; p0 < kLutSize; p0 += nthreads * 4) {
         int L = 1;
-        while (L <= kLutBits && (static_cast<uint32_t>(p0) << (24 - kLutBits)) >= sh.limit[L]) ++L;
+        while (L <= kLutBits && (static_cast<uint32_t>(p0) << (24 - kLutBits)) >= limit[L]) ++L;
         for (int j = 0; j < 4; ++j) {
             const uint32_t p = static_cast<uint32_t>(p0 + j);
             const uint32_t v = p << (24 - kLutBits);
-            while (L <= kLutBits && v >= sh.limit[L]) ++L;
+            while (L <= kLutBits && v >= limit[L]) ++L;
             uint16_t e = 0;
             if (L <= kLutBits)
-                e = static_cast<uint16_t>((L << 8) | sh.sorted[sh.base[L] + static_cast<int32_t>(v >> (24 - L))]);
+                e = static_cast<uint16_t>((L << 8) | sorted[base[L] + static_cast<int32_t>(v >> (24 - L))]);
             sh.first[p] = e;
         }
     }
     __syncthreads();
-    if (tab.fsm) {
+    if (sh.ct.fsm) {
         TabView tv{};
-        tv.limit = sh.limit;
-        tv.base = sh.base;
-        tv.sorted = sh.sorted;
+        tv.limit = limit;
+        tv.base = base;
+        tv.sorted = sorted;
         tv.first = sh.first;
         uint2* fsm = reinterpret_cast<uint2*>(tabr);
-        const uint32_t nodes = tab.n_states;
+        const uint32_t nodes = sh.ct.n_states;
         // the root row and the skip rows, code by code
         for (uint32_t i = tid; i < (1 + kSkipRows) * 256u; i += nthreads) {
             const uint32_t h = i >> 8, b = i & 255u;  // h: bits of the byte that end an earlier code
@@ -1042,8 +1047,8 @@ __device__ void build_tables_w(SharedW& sh, uint8_t* tabr, const CodeTables& tab
             }
             const uint32_t r = avail - pos;
             const uint32_t q = r ? (V << pos) >> (32 - r) : 0u;
-            const uint32_t lo_r = r ? sh.limit[r] >> (24 - r) : 0u;
-            const uint32_t next = sh.state_base[r] + q - lo_r;
+            const uint32_t lo_r = r ? limit[r] >> (24 - r) : 0u;
+            const uint32_t next = state_base[r] + q - lo_r;
             AFX_CHECK(next < nodes, kChkTableBuild);
             fsm[(h ? nodes + h - 1 : 0u) * 256u + b] = make_uint2(out, (next * kFsmRowBytes) | ((cnt * 8u) << 26));
         }
@@ -1052,16 +1057,16 @@ __device__ void build_tables_w(SharedW& sh, uint8_t* tabr, const CodeTables& tab
         // not end in it); the rest of the byte is skip row h
         for (uint32_t i = 256u + tid; i < nodes * 256u; i += nthreads) {
             const uint32_t s = i >> 8, b = i & 255u;
-            const uint32_t d = sh.depth[s];
-            const uint32_t lo_d = sh.limit[d] >> (24 - d);
-            const uint32_t p = lo_d + s - sh.state_base[d];
+            const uint32_t d = sh.ct.state_depth[s];
+            const uint32_t lo_d = limit[d] >> (24 - d);
+            const uint32_t p = lo_d + s - state_base[d];
             uint32_t len;
             const uint32_t sym = decode_first(tv, (p << (32 - d)) | (b << (24 - d)), len);
             const uint32_t h = len - d;
             uint2 e;
             if (h > 8) {  // still inside the code: the node of its first d + 8 bits
                 const uint32_t d8 = d + 8;
-                const uint32_t next = sh.state_base[d8] + ((p << 8) | b) - (sh.limit[d8] >> (24 - d8));
+                const uint32_t next = state_base[d8] + ((p << 8) | b) - (limit[d8] >> (24 - d8));
                 AFX_CHECK(next < nodes, kChkTableBuild);
                 e = make_uint2(0u, next * kFsmRowBytes);
             } else if (h == 8) {
@@ -1727,12 +1732,12 @@ __device__ __forceinline__ void restore_warps(const LaunchArgs& a, const Epi& ep
     TabView tv;
     tv.lut = reinterpret_cast<const uint32_t*>(tabr);
     tv.len0 = tabr + kLutSize * 4;
-    tv.limit = sh.limit;
-    tv.base = sh.base;
-    tv.sorted = sh.sorted;
+    tv.limit = sh.ct.limit;
+    tv.base = sh.ct.base;
+    tv.sorted = sh.ct.sorted;
     tv.first = sh.first;
     tv.fsm = reinterpret_cast<const char*>(tabr);
-    tv.depth = sh.depth;
+    tv.depth = sh.ct.state_depth;
     tv.fsm_bytes = a.tab_bytes;
 
     const uint64_t g_begin = a.total_tiles * blockIdx.x / gridDim.x;
