@@ -297,11 +297,15 @@ class ClockSampler:
 
 
 def profiled_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu capture of `kernel`, or
-    None when that capture was of another workload or the kernel source has
-    changed since (the sha256 of the source is stored with the counters)."""
+    """DRAM bytes per launch from the committed ncu capture of `kernel` on
+    this workload (profiles/<kernel>.<workload>.traffic.json, else the
+    kernel's main record), or None when no capture is of this workload or
+    the kernel source has changed since (the sha256 of the source is stored
+    with the counters)."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", f"{kernel}.traffic.json")
+    path = os.path.join(ROOT, "profiles", f"{kernel}.{workload}.traffic.json")
+    if not os.path.exists(path):
+        path = os.path.join(ROOT, "profiles", f"{kernel}.traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
