@@ -65,7 +65,7 @@ def parse_args(argv=None):
                         "4 the 2^28 adversarial tensor, 5 the layer with the 40-layer streaming leg")
     p.add_argument("--legs", default="all",
                    help="extra legs to run after the headline (comma list of e2e, zero_copy, cpu_baseline, gemv, "
-                        "stream, prefill, formats; default all)")
+                        "stream, prefill, formats, encode; default all)")
     p.add_argument("--workload", default="layer",
                    help="layer (default: one Qwen3-14B-shaped decoder layer), matrix4096, adversarial "
                         "(2^28 heavy-tailed), tensor:<name> (one tensor of the layer), layer-fp16 or layer-e4m3 "
@@ -585,7 +585,7 @@ def run_ours(args):
     }
 
     legs = set(args.legs.split(",")) if args.legs != "all" else {
-        "e2e", "zero_copy", "cpu_baseline", "gemv", "stream", "prefill", "formats"}
+        "e2e", "zero_copy", "cpu_baseline", "gemv", "stream", "prefill", "formats", "encode"}
     if not args.no_extras and "e2e" in legs:
         # every rank runs the end-to-end leg on its own GPU and host link; the
         # job's figure is all ranks' bytes over the slowest rank's time
@@ -603,6 +603,8 @@ def run_ours(args):
             line["zero_copy"] = run_zero_copy(afx, parts, dev, args)
         if "cpu_baseline" in legs:
             line["cpu_baseline"] = run_cpu_baseline(parts)
+        if "encode" in legs:
+            line["host_encode"] = run_host_encode(afx, parts)
         if args.workload == "layer":
             if "gemv" in legs:
                 line["fused_gemv"] = run_gemv_bench(afx, parts, dev_blob, offs, dev, args, weights_per_s)
@@ -627,6 +629,26 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_host_encode(afx, parts, reps: int = 2):
+    """The host side of the method, timed: the step's tensors encoded through
+    the C ABI (exponent histogram, length-limited canonical code, packing of
+    the stream and both indices), one tensor after another, each encode
+    spread over the host's threads.  Best of `reps`; the containers must
+    equal the ones the step restores."""
+    fmt = fmt_of(parts)
+    best = None
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        out = [afx.encode(w, fmt=fmt)[0] for _, w, _, _ in parts]
+        dt = time.perf_counter() - t0
+        best = dt if best is None else min(best, dt)
+    same = all(np.array_equal(o, c) for o, (_, _, c, _) in zip(out, parts))
+    n = sum(w.size for _, w, _, _ in parts)
+    return {"ms": best * 1e3, "weights_per_s": n / best, "input_gbs": elem_bytes(fmt) * n / best / 1e9,
+            "host_threads": os.cpu_count(), "containers_identical": bool(same),
+            "path": "afx.encode per tensor (afx_build_code_fmt, afx_encode_bound, afx_encode), host only"}
 
 
 def run_e2e(afx, parts, views, dev, args):

@@ -1,6 +1,7 @@
 """Host-side helpers of the bench's legs, on CPU: the comparison of the fused
 product with restore-then-GEMM picks the fastest unfused form per batch and
-skips batches that one of the two legs did not run."""
+skips batches that one of the two legs did not run; the host-encode leg
+re-encodes the step's tensors and checks the containers are the same."""
 import bench
 
 
@@ -24,3 +25,24 @@ def test_fused_vs_unfused_skips_missing_batches():
         {"tokens": 4, "sequential_ms": 1.0, "overlapped_ms": 1.0, "one_restore_launch_ms": 1.0}]})
     assert out == {}
     assert bench.fused_vs_unfused({}, {"runs": []}) == {}
+
+
+def test_host_encode_leg_reproduces_the_step_containers():
+    import numpy as np
+    from weight_streaming_canonical_gb300 import afx, synth
+    parts = []
+    for seed, n in ((1, 70_000), (2, 5120)):
+        w = synth.normal(n, seed=seed)
+        c, d = afx.encode(w)
+        parts.append((f"t{seed}", w, c, d))
+    out = bench.run_host_encode(afx, parts, reps=1)
+    assert out["containers_identical"]
+    assert out["ms"] > 0 and out["weights_per_s"] > 0
+    assert abs(out["input_gbs"] - 2 * 75_120 / (out["ms"] * 1e-3) / 1e9) < 1e-9
+    # a container that differs from what the encoder writes is reported
+    bad = list(parts)
+    c2 = parts[0][2].copy()
+    c2[-1] ^= 1
+    bad[0] = (parts[0][0], parts[0][1], c2, parts[0][3])
+    assert not bench.run_host_encode(afx, bad, reps=1)["containers_identical"]
+    assert np.array_equal(parts[0][2], afx.encode(parts[0][1])[0])
