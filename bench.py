@@ -330,14 +330,22 @@ def measured_hbm_peak():
 
 # ---- CPU oracle leg ------------------------------------------------------------------
 
-def oracle_sample(parts, slice_elems: int = 1 << 24):
-    """Containers for the CPU oracle: every tensor of the layer cut into
-    independent slices of 2**24 weights, each its own container."""
+ORACLE_SLICE = 1 << 21  # weights per oracle container
+
+
+def oracle_sample(parts, count: int, slice_elems: int = ORACLE_SLICE):
+    """Containers for the CPU oracle: the first `count` full slices of
+    slice_elems weights of the workload's tensors, in order, each encoded as
+    its own container (equal slices, so that every thread gets the same
+    work; the norm vectors, shorter than a slice, are left out)."""
     from weight_streaming_canonical_gb300 import afx
     work = []
     for name, w, c, d in parts:
-        for s in range(0, w.size, slice_elems):
-            work.append((w[s:s + slice_elems], int(d.format)))
+        for s in range(0, w.size - slice_elems + 1, slice_elems):
+            if len(work) < count:
+                work.append((w[s:s + slice_elems], int(d.format)))
+    if not work:  # every tensor is shorter than a slice: the tensors themselves
+        work = [(w, int(d.format)) for _, w, _, d in parts[:max(1, count)] if w.size]
     with cf.ThreadPoolExecutor(16) as ex:
         return list(ex.map(lambda a: afx.encode(a[0], fmt=a[1])[0], work))
 
@@ -372,11 +380,11 @@ def run_reference(args):
     if rank != 0:
         return  # rank 0 alone runs the CPU reference
     parts = build_layer(args.seed, 0, args.workload)
-    containers = oracle_sample(parts)
     threads = os.cpu_count() or 1
     n_total = sum(w.size for _, w, _, _ in parts)
-    # one step = the oracle restoring a bounded sample: 1/8 of the layer's slices
-    per_step = containers[: max(1, len(containers) // 8)]
+    # one step = the oracle restoring a bounded sample: one slice per host thread
+    per_step = oracle_sample(parts, threads)
+    threads = max(1, min(threads, len(per_step)))
     for _ in range(args.warmup):
         time_oracle(per_step, threads)
     times, weights = [], 0
@@ -386,7 +394,8 @@ def run_reference(args):
         weights = nw
     sec = sum(times) / len(times)
     value = elem_bytes(fmt_of(parts)) * weights / sec / 1e9
-    sample = f"{len(per_step)} oracle containers of <= 2^24 weights ({weights} weights) per step, from the layer's {n_total} weights"
+    sample = (f"{len(per_step)} oracle containers ({weights} weights) per step, one per thread, "
+              f"from the workload's {n_total} weights")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
@@ -1129,13 +1138,18 @@ def run_stream_bench(afx, parts, dev, args, layers=40):
 
 
 def run_cpu_baseline(parts):
-    containers = oracle_sample(parts)
-    sample = containers[: max(1, len(containers) // 4)]
+    """The CPU oracle on the host's threads over as many of the workload's
+    2^21-weight slices as divide evenly among them (every thread busy for
+    the whole sample), and one slice on one thread."""
     threads = os.cpu_count() or 1
+    slices = sum(w.size // ORACLE_SLICE for _, w, _, _ in parts)
+    sample = oracle_sample(parts, threads * max(1, slices // threads))
+    threads = max(1, min(threads, len(sample)))
     dt, nw = time_oracle(sample, threads)
     dt1, nw1 = time_oracle(sample[:1], 1)
     return {"value": elem_bytes(fmt_of(parts)) * nw / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{len(sample)} containers of <= 2^24 weights ({nw} weights) from the layer, one per thread",
+            "sample": f"{len(sample)} containers ({nw} weights) of the workload's "
+                      f"{sum(w.size for _, w, _, _ in parts)}, {len(sample) // threads} per thread on {threads} threads",
             "weights_per_s": nw / dt, "one_core_weights_per_s": nw1 / dt1, "cpu": cpu_model()}
 
 
