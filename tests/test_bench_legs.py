@@ -46,3 +46,23 @@ def test_host_encode_leg_reproduces_the_step_containers():
     bad[0] = (parts[0][0], parts[0][1], c2, parts[0][3])
     assert not bench.run_host_encode(afx, bad, reps=1)["containers_identical"]
     assert np.array_equal(parts[0][2], afx.encode(parts[0][1])[0])
+
+
+def test_cpu_baseline_keeps_every_reported_thread_busy(monkeypatch):
+    # 10 full slices and a short tensor for 4 threads: 8 slices, 2 a thread,
+    # and the short tensor is not part of the sample
+    from weight_streaming_canonical_gb300 import afx, synth
+    monkeypatch.setattr(bench.os, "cpu_count", lambda: 4)
+    parts = []
+    for seed, n in ((1, 10 * bench.ORACLE_SLICE + 123), (2, 5120)):
+        w = synth.normal(n, seed=seed)
+        c, d = afx.encode(w)
+        parts.append((f"t{seed}", w, c, d))
+    out = bench.run_cpu_baseline(parts)
+    assert out["cores"] == 4
+    assert out["sample"].startswith("8 containers (16777216 weights)")
+    assert "2 per thread on 4 threads" in out["sample"]
+    assert out["one_core_weights_per_s"] > 0 and out["weights_per_s"] > 0
+    # fewer slices than threads: one slice per busy thread, the rest not counted
+    monkeypatch.setattr(bench.os, "cpu_count", lambda: 64)
+    assert bench.run_cpu_baseline(parts)["cores"] == 10
