@@ -67,7 +67,8 @@ def parse_args(argv=None):
                    help="extra legs to run after the headline (comma list of e2e, zero_copy, cpu_baseline, gemv, "
                         "stream, prefill, formats, encode; default all)")
     p.add_argument("--workload", default="layer",
-                   help="layer (default: one Qwen3-14B-shaped decoder layer), matrix4096, adversarial "
+                   help="layer (default: one Qwen3-14B-shaped decoder layer), matrix4096, normal:<k> (one "
+                        "N(0,0.02) tensor of 2^k weights), adversarial "
                         "(2^28 heavy-tailed), tensor:<name> (one tensor of the layer), layer-fp16 or layer-e4m3 "
                         "(the layer in the other element formats)")
     args = p.parse_args(argv)
@@ -159,6 +160,11 @@ def build_layer(seed: int, rank: int = 0, workload: str = "layer"):
     elif workload.startswith("tensor:"):
         name = workload.split(":", 1)[1]
         gens = {name: lambda: synth.layer_tensor(name, seed=seed, layer=rank)}
+    elif workload.startswith("normal:"):
+        lg = int(workload.split(":", 1)[1])
+        if not 0 <= lg <= 30:
+            raise SystemExit("normal:<k> takes 0 <= k <= 30")
+        gens = {workload: lambda: synth.normal(1 << lg, seed=seed + lg + rank)}
     elif workload == "layer":
         gens = {name: (lambda nm=name: synth.layer_tensor(nm, seed=seed, layer=rank))
                 for name, _, _ in synth.LAYER_TENSORS}
@@ -193,6 +199,8 @@ def build_layer(seed: int, rank: int = 0, workload: str = "layer"):
 def workload_text(workload: str) -> str:
     if workload.startswith("tensor:"):
         return f"one tensor of the Qwen3-14B-shaped layer: {workload.split(':', 1)[1]}"
+    if workload.startswith("normal:"):
+        return f"one BF16 tensor of 2^{workload.split(':', 1)[1]} weights, N(0,0.02)"
     return WORKLOADS[workload]
 
 
