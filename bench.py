@@ -196,6 +196,18 @@ def build_layer(seed: int, rank: int = 0, workload: str = "layer"):
         return list(ex.map(one, gens.items()))
 
 
+def data_text(workload: str) -> str:
+    """What the synthetic inputs are, for the JSON line's `data`."""
+    fixed = {
+        "layer": "synthetic: seeded N(0,0.02) BF16 matrices, N(1,0.05) norms, Qwen3-14B layer shapes",
+        "model": "synthetic: seeded N(0,0.02) BF16 matrices, N(1,0.05) norms, Qwen3-14B model shapes",
+        "layer-fp16": "synthetic: seeded N(0,0.02) matrices, N(1,0.05) norms rounded to FP16, Qwen3-14B layer shapes",
+        "layer-e4m3": "synthetic: seeded N(0,1) x 448/6 matrices rounded to E4M3, Qwen3-14B layer matrix shapes",
+        "adversarial": "synthetic: seeded heavy-tailed BF16 with zeros, subnormals, infinities and NaN payloads",
+    }
+    return fixed.get(workload, "synthetic: seeded " + workload_text(workload))
+
+
 def workload_text(workload: str) -> str:
     if workload.startswith("tensor:"):
         return f"one tensor of the Qwen3-14B-shaped layer: {workload.split(':', 1)[1]}"
@@ -578,9 +590,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "u32",
-        "data": {0: "synthetic: seeded N(0,0.02) BF16 matrices, N(1,0.05) norms, Qwen3-14B layer shapes",
-                 1: "synthetic: seeded N(0,0.02) matrices, N(1,0.05) norms rounded to FP16, Qwen3-14B layer shapes",
-                 2: "synthetic: seeded N(0,1) x 448/6 matrices rounded to E4M3, Qwen3-14B layer matrix shapes"}[fmt],
+        "data": data_text(args.workload),
         "config": {"workload": workload_text(args.workload), "weights": n_total, "compressed_bytes": comp_total,
                    "bits_per_weight": 8 * comp_total / n_total,
                    "coded_exponent_bits_per_weight": sum(d.total_bits for *_, d in parts) / n_total,

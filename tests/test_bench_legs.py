@@ -66,3 +66,11 @@ def test_cpu_baseline_keeps_every_reported_thread_busy(monkeypatch):
     # fewer slices than threads: one slice per busy thread, the rest not counted
     monkeypatch.setattr(bench.os, "cpu_count", lambda: 64)
     assert bench.run_cpu_baseline(parts)["cores"] == 10
+
+
+def test_data_text_names_each_workloads_inputs():
+    assert "Qwen3-14B layer shapes" in bench.data_text("layer")
+    assert "NaN" in bench.data_text("adversarial")
+    assert "4096x4096" in bench.data_text("matrix4096")
+    assert "2^26" in bench.data_text("normal:26")
+    assert all(bench.data_text(w).startswith("synthetic") for w in bench.WORKLOADS)
