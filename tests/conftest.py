@@ -20,10 +20,19 @@ def golden_dir():
     return GOLDEN
 
 
+DEBUG_BOUNDS = os.environ.get("AFX_DEBUG_BOUNDS", "0") == "1"
+
+
 @pytest.fixture(scope="session")
 def afx():
-    """The product binding, built in-tree first if needed (nvcc cross-compiles here)."""
+    """The product binding, built in-tree first if needed (nvcc cross-compiles
+    here).  With AFX_DEBUG_BOUNDS=1 it is the bounds-checked build, and the
+    session fails at its end if any kernel's bounds check fired."""
     from weight_streaming_canonical_gb300 import build as _build
-    _build.build()
+    _build.build(debug_bounds=DEBUG_BOUNDS)
     from weight_streaming_canonical_gb300 import afx as _afx
-    return _afx
+    yield _afx
+    if DEBUG_BOUNDS:
+        bits, checked = _afx.afx_debug_bounds_report()
+        assert checked, "AFX_DEBUG_BOUNDS=1 but the loaded library does not check bounds"
+        assert bits == 0, f"bounds checks failed during the session: {bits:#x}"
