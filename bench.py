@@ -56,7 +56,8 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--seed", type=int, default=0)
-    p.add_argument("--no-extras", action="store_true", help="skip e2e and cpu_baseline legs")
+    p.add_argument("--no-extras", action="store_true",
+                   help="the headline restore only: skip every leg after it (see --legs)")
     p.add_argument("--e2e-piece-weights", type=int, default=0,
                    help="end-to-end leg: store each tensor as containers of at most this many weights "
                         "(consecutive slices), streamed one per stage; 0: one container per tensor")
