@@ -1,19 +1,26 @@
 #!/usr/bin/env python
 """Benchmark of the lossless BF16 weight restore (afx) on GB300.
 
-One step restores every tensor of one Qwen3-14B-shaped decoder layer
-(q/k/v/o, gate/up/down and the two norm vectors: 330,311,680 BF16 weights,
-0.66 GB) from containers already resident in HBM, through the C ABI
-(afx_decode per tensor, captured once in a CUDA graph and replayed).
+One step restores every tensor of the whole Qwen3-14B-shaped model (40
+decoder layers of q/k/v/o, gate/up/down and two norm vectors, plus the
+embedding and the untied LM head: 14,768,291,840 BF16 weights, 29.5 GB)
+from containers already resident in HBM, through the C ABI (one
+afx_decode_batch call, captured once in a CUDA graph and replayed).
+`--workload` picks another workload for the headline.
 
 Reported: decoded BF16 GB/s (2 bytes x weights / step time) as `value`,
 weights/s, HBM GB/s (compressed bytes read + BF16 bytes written) against
-the measured copy bandwidth, the per-launch roofline of the decode kernel,
-an end-to-end number through the C ABI from pinned host containers to a
-host BF16 result, and the CPU oracle on the host cores.
+the measured copy bandwidth, the roofline of the restore kernel, an
+end-to-end number through the C ABI from pinned host containers to a host
+BF16 result, the CPU oracle on the host cores, and (`per_config`) the
+4096x4096 matrix, the single layer and the 2^28 adversarial tensor, each
+checked bit for bit before it is timed.  The layer's further legs (fused
+GEMV, prefill, 40 streamed layers, formats, zero-copy, host encode)
+follow.
 
 `--impl reference` times the CPU oracle itself (the reference arm): the
-bit-serial decoder of the same containers on the host cores.
+bit-serial decoder on containers the oracle encodes itself, on the host
+cores.
 
 The decode is the t_unpack term of "Why Weight Offloading Slows
 Inference", Eq. (1); the break-even it must meet is that page's Eq. (2).
@@ -65,10 +72,11 @@ def parse_args(argv=None):
                    help="the five workloads by number: 1 the 4096x4096 matrix, 2 the layer, 3 the whole model, "
                         "4 the 2^28 adversarial tensor, 5 the layer with the 40-layer streaming leg")
     p.add_argument("--legs", default="all",
-                   help="extra legs to run after the headline (comma list of e2e, zero_copy, cpu_baseline, gemv, "
-                        "stream, prefill, formats, encode; default all)")
-    p.add_argument("--workload", default="layer",
-                   help="layer (default: one Qwen3-14B-shaped decoder layer), matrix4096, normal:<k> (one "
+                   help="extra legs to run after the headline (comma list of e2e, zero_copy, cpu_baseline, configs, "
+                        "gemv, stream, prefill, formats, encode; default all)")
+    p.add_argument("--workload", default="model",
+                   help="model (default: the whole Qwen3-14B-shaped model, 14.77 B weights resident), layer (one "
+                        "Qwen3-14B-shaped decoder layer), matrix4096, normal:<k> (one "
                         "N(0,0.02) tensor of 2^k weights), adversarial "
                         "(2^28 heavy-tailed), tensor:<name> (one tensor of the layer), layer-fp16 or layer-e4m3 "
                         "(the layer in the other element formats)")
@@ -150,9 +158,10 @@ def np_elem_dtype(fmt: int):
     return np.uint8 if fmt == 2 else np.uint16
 
 
-def build_layer(seed: int, rank: int = 0, workload: str = "layer"):
-    """Generate and encode the workload on the host: [(name, w, container, desc)]."""
-    from weight_streaming_canonical_gb300 import afx, synth
+def workload_generators(seed: int, rank: int = 0, workload: str = "model"):
+    """The workload's tensors in order, as {name: () -> element patterns}
+    (nothing is generated until a generator is called)."""
+    from weight_streaming_canonical_gb300 import synth
 
     if workload == "matrix4096":
         gens = {"matrix4096": lambda: synth.matrix_4096(seed=seed + rank)}
@@ -184,7 +193,14 @@ def build_layer(seed: int, rank: int = 0, workload: str = "layer"):
         gens["lm_head"] = lambda: synth.lm_head(seed=seed + rank)
     else:
         raise SystemExit(f"unknown workload {workload}")
+    return gens
 
+
+def build_layer(seed: int, rank: int = 0, workload: str = "model"):
+    """Generate and encode the workload on the host: [(name, w, container, desc)]."""
+    from weight_streaming_canonical_gb300 import afx
+
+    gens = workload_generators(seed, rank, workload)
     fmt = FMT_OF_WORKLOAD.get(workload, 0)
 
     def one(item):
@@ -354,21 +370,38 @@ def measured_hbm_peak():
 ORACLE_SLICE = 1 << 21  # weights per oracle container
 
 
-def oracle_sample(parts, count: int, slice_elems: int = ORACLE_SLICE):
+def oracle_sample(tensors, count: int, slice_elems: int = ORACLE_SLICE):
     """Containers for the CPU oracle: the first `count` full slices of
-    slice_elems weights of the workload's tensors, in order, each encoded as
-    its own container (equal slices, so that every thread gets the same
-    work; the norm vectors, shorter than a slice, are left out)."""
-    from weight_streaming_canonical_gb300 import afx
-    work = []
-    for name, w, c, d in parts:
+    slice_elems weights of the workload's tensors (an iterable of (element
+    patterns, format), read only as far as needed), in order, each encoded
+    as its own container by the oracle's own encoder (equal slices, so that
+    every thread gets the same work; the norm vectors, shorter than a slice,
+    are left out).  Nothing of the library is loaded for them."""
+    import oracle
+    work, short = [], []
+    for w, fmt in tensors:
+        w = w.reshape(-1)
+        if w.size < slice_elems and len(short) < max(1, count):
+            short.append((w, int(fmt)))
         for s in range(0, w.size - slice_elems + 1, slice_elems):
             if len(work) < count:
-                work.append((w[s:s + slice_elems], int(d.format)))
+                work.append((w[s:s + slice_elems], int(fmt)))
+        if len(work) >= count:
+            break
     if not work:  # every tensor is shorter than a slice: the tensors themselves
-        work = [(w, int(d.format)) for _, w, _, d in parts[:max(1, count)] if w.size]
+        work = [t for t in short if t[0].size]
+
+    def enc(a):
+        w, fmt = a
+        return oracle.encode(w, oracle.code_lengths(oracle.histogram(w, fmt)), fmt=fmt)
+
     with cf.ThreadPoolExecutor(16) as ex:
-        return list(ex.map(lambda a: afx.encode(a[0], fmt=a[1])[0], work))
+        return list(ex.map(enc, work))
+
+
+def part_tensors(parts):
+    """(element patterns, format) of each encoded tensor, for oracle_sample."""
+    return ((w, d.format) for _, w, _, d in parts)
 
 
 def time_oracle(containers, threads: int) -> tuple[float, int]:
@@ -400,11 +433,14 @@ def run_reference(args):
     rank, world, _ = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), 0
     if rank != 0:
         return  # rank 0 alone runs the CPU reference
-    parts = build_layer(args.seed, 0, args.workload)
+    gens = workload_generators(args.seed, 0, args.workload)
+    fmt = FMT_OF_WORKLOAD.get(args.workload, 0)
     threads = os.cpu_count() or 1
-    n_total = sum(w.size for _, w, _, _ in parts)
-    # one step = the oracle restoring a bounded sample: one slice per host thread
-    per_step = oracle_sample(parts, threads)
+    # one step = the oracle restoring a bounded sample: one slice per host
+    # thread, from the workload's first tensors (generated only as far as
+    # needed; the oracle encodes them itself)
+    per_step = oracle_sample(((np.ascontiguousarray(g()), fmt) for g in gens.values()), threads)
+    n_total = workload_weights(args.workload)
     threads = max(1, min(threads, len(per_step)))
     for _ in range(args.warmup):
         time_oracle(per_step, threads)
@@ -414,7 +450,7 @@ def run_reference(args):
         times.append(dt)
         weights = nw
     sec = sum(times) / len(times)
-    value = elem_bytes(fmt_of(parts)) * weights / sec / 1e9
+    value = elem_bytes(fmt) * weights / sec / 1e9
     sample = (f"{len(per_step)} oracle containers ({weights} weights) per step, one per thread, "
               f"from the workload's {n_total} weights")
     line = {
@@ -432,20 +468,57 @@ def run_reference(args):
 
 # ---- our arm ---------------------------------------------------------------------------
 
-def run_ours(args):
+def workload_weights(workload: str) -> int:
+    """Weights of a workload, from its shapes alone."""
+    from weight_streaming_canonical_gb300 import synth
+    if workload == "model":
+        return synth.model_weight_count()
+    if workload in ("layer", "layer-fp16"):
+        return synth.layer_weight_count()
+    if workload == "layer-e4m3":
+        return sum(synth.numel(s) for _, s, k in synth.LAYER_TENSORS if k == "matrix")
+    if workload == "matrix4096":
+        return 4096 * 4096
+    if workload == "adversarial":
+        return 1 << 28
+    if workload.startswith("normal:"):
+        return 1 << int(workload.split(":", 1)[1])
+    if workload.startswith("tensor:"):
+        name = workload.split(":", 1)[1]
+        return synth.numel(dict((n, s) for n, s, _ in synth.LAYER_TENSORS)[name])
+    raise SystemExit(f"unknown workload {workload}")
+
+
+def restore_traffic(kernel: str, workload: str, n_weights: int):
+    """DRAM bytes per step of the restore kernel: the committed capture of
+    this workload, else, for the whole model (too large to capture, 23
+    launches a step), the layer capture's bytes scaled by weights (the
+    restore's traffic is proportional to the weights: every tensor has the
+    layer's bits per weight).  None when no valid capture exists."""
+    t = profiled_traffic(kernel, workload)
+    if t is not None or workload != "model":
+        return t, "ncu capture of this workload, one launch"
+    t = profiled_traffic(kernel, "layer")
+    if t is None:
+        return None, None
+    from weight_streaming_canonical_gb300 import synth
+    return int(t * n_weights / synth.layer_weight_count()), \
+        "ncu capture of the layer (one launch) scaled to the step by weights"
+
+
+def measure_restore(afx, parts, dev, args, workload: str, world: int = 1, local: int = 0, clocks: bool = False):
+    """Uploads the workload's containers to HBM, checks one graph replay
+    of its afx_decode_batch call bit for bit against the original elements
+    on the device, then times `args.steps` replays.  Workloads whose bytes
+    fit in L2 are timed replay by replay with L2 flushed (a 512 MB write)
+    before each, outside the events; larger ones back to back.  With
+    `clocks`, the timed replays sit inside about BUSY_PAD_S seconds of the
+    same work on each side while nvidia-smi samples the clocks.  Returns
+    (result, state) with state holding the device buffers for later legs."""
     import torch
-
-    from weight_streaming_canonical_gb300 import afx
-
-    rank, world, local = dist_setup(args.gpus)
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    parts = build_layer(args.seed, rank, args.workload)
     n_total = sum(d.n for _, _, _, d in parts)
     comp_total = sum(d.container_bytes for _, _, _, d in parts)
     alg_total = sum(algorithmic_bytes(d) for _, _, _, d in parts)
-
-    # resident containers and outputs
     offs, o = [], 0
     for _, _, c, _ in parts:
         offs.append(o)
@@ -464,7 +537,6 @@ def run_ours(args):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     views = [(d, dev_blob[off:off + d.container_bytes], out[oo_:oo_ + d.n])
              for (_, _, _, d), off, oo_ in zip(parts, offs, out_offs)]
-
     descs = [d for d, _, _ in views]
     # kernel launches one afx_decode_batch call makes: up to 16 coded tensors
     # per restore launch, one fill launch per single-exponent tensor
@@ -485,7 +557,7 @@ def run_ours(args):
     with torch.cuda.graph(graph, stream=stream):
         step()
     torch.cuda.synchronize()
-    # correctness of what is timed: the restored layer equals the original bits
+    # correctness of what is timed: the restored elements equal the original bits
     with torch.cuda.stream(stream):
         out.zero_()
         graph.replay()
@@ -498,9 +570,6 @@ def run_ours(args):
     if status.item() != 0:
         raise SystemExit(f"device status {status.item()}")
 
-    # timed region: K graph replays.  A workload whose bytes would stay in L2
-    # (129 MB) between replays is timed launch by launch instead, with L2
-    # flushed before each (a 512 MB write, outside the events).
     small = comp_total + elem_bytes(fmt) * n_total < 2 * L2_BYTES
     flush = torch.empty(4 * L2_BYTES, dtype=torch.uint8, device=dev) if small else None
 
@@ -513,20 +582,19 @@ def run_ours(args):
         for _ in range(args.warmup):
             graph.replay()
     torch.cuda.synchronize()
-    # the timed steps sit inside a busy window of the same work (about
-    # BUSY_PAD_S of it on each side, outside the events), so that the clock
-    # samples, 100 ms apart, are taken under this load
-    est0, est1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        est0.record(stream)
-        for _ in range(3):
-            one_step()
-        est1.record(stream)
-    torch.cuda.synchronize()
-    pad = busy_pad_steps(est0.elapsed_time(est1) / 3)
-    barrier(world)
-    sampler = ClockSampler(local)
-    time.sleep(0.3)
+    pad, sampler = 0, None
+    if clocks:
+        est0, est1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            est0.record(stream)
+            for _ in range(3):
+                one_step()
+            est1.record(stream)
+        torch.cuda.synchronize()
+        pad = busy_pad_steps(est0.elapsed_time(est1) / 3)
+        barrier(world)
+        sampler = ClockSampler(local)
+        time.sleep(0.3)
     torch.cuda.synchronize()
     busy_t0 = time.time()
     with torch.cuda.stream(stream):
@@ -556,35 +624,59 @@ def run_ours(args):
         torch.cuda.synchronize()
         ms = start.elapsed_time(end) / args.steps
     busy_t1 = time.time()
-    clocks = sampler.stop((busy_t0, busy_t1))
-    if clocks is not None:
-        clocks["busy_pad_steps_each_side"] = pad
+    clk = sampler.stop((busy_t0, busy_t1)) if sampler is not None else None
+    if clk is not None:
+        clk["busy_pad_steps_each_side"] = pad
     barrier(world)
     ms = max_over_ranks(ms, world)
 
-    # duration of the restore kernel itself: events on its stream around each
-    # launch, the launch queued behind a busy stream so no host time is timed
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    with torch.cuda.stream(stream):
-        graph.replay()
-        for e0, e1 in ev:
-            if small:
-                flush.fill_(1)
-            e0.record(stream)
-            step()
-            e1.record(stream)
-    torch.cuda.synchronize()
-    launch_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
-    kernel_ms = statistics.median(launch_ms)
+    # The graph holds the step's restore launches and nothing else, so its
+    # replay time bounds their summed duration from above: the kernel's
+    # time per step is taken in that same window.
     peak, peak_kind = measured_hbm_peak()
-    achieved = alg_total / (kernel_ms * 1e-3) / 1e9
+    achieved = alg_total / (ms * 1e-3) / 1e9
     kernel_name = {1: "restore_store_fp16_kernel", 2: "restore_store_e4m3_kernel"}.get(fmt, "restore_store_kernel")
+    traffic, traffic_src = restore_traffic(kernel_name, workload, n_total)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": profiled_traffic(kernel_name, args.workload),
+                "traffic": traffic, "traffic_scope": "per step" + (f" ({traffic_src})" if traffic_src else ""),
                 "kernel": kernel_name, "peak_kind": peak_kind,
                 "launches_per_step": launches_per_step, "algorithmic_bytes_per_step": alg_total,
-                "kernel_ms_per_step": kernel_ms}
+                "kernel_ms_per_step": ms,
+                "kernel_time": "graph replays holding only the restore launches (the launches' summed duration "
+                               "is at most this)"}
+    res = {"ms": ms, "n": n_total, "comp": comp_total, "alg": alg_total, "fmt": fmt, "small": small,
+           "roofline": roofline, "clocks": clk, "launches_per_step": launches_per_step, "bit_exact": True,
+           "tensors": len(views)}
+    state = {"dev_blob": dev_blob, "offs": offs, "views": views, "host_blob": host_blob, "out": out}
+    return res, state
 
+
+def config_summary(workload: str, res: dict) -> dict:
+    """One workload's restore result for the per_config block."""
+    sec = res["ms"] * 1e-3
+    return {"workload": workload_text(workload), "weights": res["n"], "ms_per_step": res["ms"],
+            "weights_per_s": res["n"] / sec, "decoded_gbs": elem_bytes(res["fmt"]) * res["n"] / sec / 1e9,
+            "hbm_gbs": res["alg"] / sec / 1e9, "hbm_frac": res["roofline"]["frac"],
+            "peak_kind": res["roofline"]["peak_kind"], "bit_exact": res["bit_exact"],
+            "launches_per_step": res["launches_per_step"], "bits_per_weight": 8 * res["comp"] / res["n"],
+            "l2": "flushed before each timed replay" if res["small"] else "inputs larger than L2"}
+
+
+PER_CONFIG = (("1", "matrix4096"), ("2", "layer"), ("3", "model"), ("4", "adversarial"))
+
+
+def run_ours(args):
+    import torch
+
+    from weight_streaming_canonical_gb300 import afx
+
+    rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    parts = build_layer(args.seed, rank, args.workload)
+    res, state = measure_restore(afx, parts, dev, args, args.workload, world, local, clocks=True)
+    ms, n_total, comp_total, alg_total, fmt = res["ms"], res["n"], res["comp"], res["alg"], res["fmt"]
+    peak = res["roofline"]["peak"]
     sec = ms * 1e-3
     value, weights_per_s = job_throughput(n_total, world, ms, elem_bytes(fmt))
     line = {
@@ -597,27 +689,27 @@ def run_ours(args):
                    "coded_exponent_bits_per_weight": sum(d.total_bits for *_, d in parts) / n_total,
                    "exponent_entropy_bits_per_weight": exponent_entropy_bits(parts),
                    "l2": ("L2 flushed before each timed launch (a 512 MB write outside the events): "
-                          if small else "inputs larger than L2: ")
+                          if res["small"] else "inputs larger than L2: ")
                          + "%.0f MB compressed read and %.0f MB written per step"
                          % (comp_total / 1e6, elem_bytes(fmt) * n_total / 1e6),
-                   "launch": f"one afx_decode_batch call of {len(views)} tensors ({launches_per_step} kernel launches) "
-                             "per step, replayed from a CUDA graph",
+                   "launch": f"one afx_decode_batch call of {res['tensors']} tensors "
+                             f"({res['launches_per_step']} kernel launches) per step, replayed from a CUDA graph",
                    "parallelism": f"replicas x{world}"},
         "weights_per_s": weights_per_s,
         "hbm_gbs": alg_total * world / sec / 1e9,
         "hbm_frac": alg_total / sec / 1e9 / peak,
         "hbm_frac_of_nominal_7900_gbs": alg_total / sec / 1e9 / 7900.0,
-        "roofline": roofline,
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks,
+        "roofline": res["roofline"],
+        "gpu_launches": res["launches_per_step"] * args.steps,
+        "clocks": res["clocks"],
     }
 
     legs = set(args.legs.split(",")) if args.legs != "all" else {
-        "e2e", "zero_copy", "cpu_baseline", "gemv", "stream", "prefill", "formats", "encode"}
+        "e2e", "zero_copy", "cpu_baseline", "gemv", "stream", "prefill", "formats", "encode", "configs"}
     if not args.no_extras and "e2e" in legs:
         # every rank runs the end-to-end leg on its own GPU and host link; the
         # job's figure is all ranks' bytes over the slowest rank's time
-        e2e = run_e2e(afx, parts, views, dev, args)
+        e2e = run_e2e(afx, parts, state["views"], dev, args, host_blob=state["host_blob"], offs=state["offs"])
         e2e_ms = max_over_ranks(e2e["ms_per_step"], world)
         e2e["value"] = e2e["value"] * world * e2e["ms_per_step"] / e2e_ms
         e2e["ms_per_step"] = e2e_ms
@@ -626,32 +718,66 @@ def run_ours(args):
         if world > 1:
             e2e["ranks"] = world
         line["e2e"] = e2e
-    if not args.no_extras and rank == 0 and world == 1:  # the other legs and the CPU oracle at N = 1 only
+    extras = not args.no_extras and rank == 0 and world == 1  # the other legs and the CPU oracle at N = 1 only
+    if extras and "cpu_baseline" in legs:
+        line["cpu_baseline"] = run_cpu_baseline(parts)
+    layer_parts, layer_state, layer_value = None, None, None
+    if args.workload == "layer":
+        layer_parts, layer_state, layer_value = parts, state, value
+    else:
+        del state
+    del parts
+    if extras and "configs" in legs:
+        # every other config of the method's workloads, each bit-exact checked
+        # before it is timed; the headline's own entry repeats its numbers
+        per = {}
+        for key, wl in PER_CONFIG:
+            if wl == args.workload:
+                per[key] = config_summary(wl, res)
+                continue
+            p = build_layer(args.seed, 0, wl)
+            r, st = measure_restore(afx, p, dev, args, wl)
+            per[key] = config_summary(wl, r)
+            if wl == "layer":
+                layer_parts, layer_state, layer_value = p, st, elem_bytes(r["fmt"]) * r["n"] / (r["ms"] * 1e-3) / 1e9
+                per[key]["note"] = "the layer's extra legs below use these containers"
+            else:
+                del p, st
+            torch.cuda.empty_cache()
+        line["per_config"] = per
+    if extras and layer_parts is None and legs & {"zero_copy", "encode", "gemv", "stream", "prefill"}:
+        layer_parts = build_layer(args.seed, 0, "layer")
+        r, layer_state = measure_restore(afx, layer_parts, dev, args, "layer")
+        layer_value = elem_bytes(r["fmt"]) * r["n"] / (r["ms"] * 1e-3) / 1e9
+    if extras:
+        parts = layer_parts
+        dev_blob, offs = (layer_state["dev_blob"], layer_state["offs"]) if layer_state else (None, None)
+        lw = sum(d.n for *_, d in parts) if parts else 0
         if "zero_copy" in legs:
             line["zero_copy"] = run_zero_copy(afx, parts, dev, args)
-        if "cpu_baseline" in legs:
-            line["cpu_baseline"] = run_cpu_baseline(parts)
         if "encode" in legs:
             line["host_encode"] = run_host_encode(afx, parts)
-        if args.workload == "layer":
-            if "gemv" in legs:
-                line["fused_gemv"] = run_gemv_bench(afx, parts, dev_blob, offs, dev, args, weights_per_s)
-            if "stream" in legs:
-                line["streamed_40_layers"] = run_stream_bench(afx, parts, dev, args)
-                # "Why Weight Offloading Slows Inference", Eq. (2): compression pays
-                # when (S - S_disk) / b > t_unpack; here b is the measured link
-                S, S_disk = 2 * n_total, comp_total
-                b = line["streamed_40_layers"]["batch1"]["h2d_gbs"] * 1e9
-                line["eq2_break_even"] = {"S_bytes": S, "S_disk_bytes": S_disk, "b_link_gbs": b / 1e9,
-                                          "read_time_saved_ms": (S - S_disk) / b * 1e3, "t_unpack_ms": ms,
-                                          "pays": (S - S_disk) / b > ms * 1e-3}
-                line["residency_plan"] = run_residency_plan(afx, parts, b / 1e9, value)
-            if "prefill" in legs:
-                line["prefill"] = run_prefill_bench(afx, parts, dev_blob, offs, dev, args)
-            if "gemv" in legs and "prefill" in legs:
-                line["fused_gemv"]["vs_restore_then_gemm"] = fused_vs_unfused(line["fused_gemv"], line["prefill"])
-            if "formats" in legs:
-                line["formats"] = run_formats_bench(afx, dev, args)
+        if "gemv" in legs:
+            line["fused_gemv"] = run_gemv_bench(afx, parts, dev_blob, offs, dev, args,
+                                                layer_value * 1e9 / 2 if layer_value else None)
+        if "stream" in legs:
+            line["streamed_40_layers"] = run_stream_bench(afx, parts, dev, args)
+            # "Why Weight Offloading Slows Inference", Eq. (2): compression pays
+            # when (S - S_disk) / b > t_unpack; here b is the measured link
+            S, S_disk = 2 * lw, sum(d.container_bytes for *_, d in parts)
+            b = line["streamed_40_layers"]["batch1"]["h2d_gbs"] * 1e9
+            t_unpack_ms = 2 * lw / (layer_value * 1e9) * 1e3
+            line["eq2_break_even"] = {"S_bytes": S, "S_disk_bytes": S_disk, "b_link_gbs": b / 1e9,
+                                      "read_time_saved_ms": (S - S_disk) / b * 1e3, "t_unpack_ms": t_unpack_ms,
+                                      "pays": (S - S_disk) / b > t_unpack_ms * 1e-3,
+                                      "scope": "one Qwen3-14B-shaped layer"}
+            line["residency_plan"] = run_residency_plan(afx, parts, b / 1e9, layer_value)
+        if "prefill" in legs:
+            line["prefill"] = run_prefill_bench(afx, parts, dev_blob, offs, dev, args)
+        if "gemv" in legs and "prefill" in legs:
+            line["fused_gemv"]["vs_restore_then_gemm"] = fused_vs_unfused(line["fused_gemv"], line["prefill"])
+        if "formats" in legs:
+            line["formats"] = run_formats_bench(afx, dev, args)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -679,11 +805,12 @@ def run_host_encode(afx, parts, reps: int = 2):
             "path": "afx.encode per tensor (afx_build_code_fmt, afx_encode_bound, afx_encode), host only"}
 
 
-def run_e2e(afx, parts, views, dev, args):
+def run_e2e(afx, parts, views, dev, args, host_blob=None, offs=None):
     """Pinned host containers -> device -> BF16 back to pinned host, through
     afx_stream_run with one tensor per streamed layer: the copy of tensor
     i+1 overlaps the restore of tensor i, and the copy back of tensor i
-    (on its own stream) overlaps both."""
+    (on its own stream) overlaps both.  host_blob/offs: the containers
+    already in pinned host memory, back to back (used as they are)."""
     import torch
     fmt = fmt_of(parts)
     host_out = torch.empty(sum(d.n for _, _, _, d in parts), dtype=torch_elem_dtype(fmt)).pin_memory()
@@ -700,9 +827,12 @@ def run_e2e(afx, parts, views, dev, args):
         stream_parts = sliced
     else:
         stream_parts = parts
-    for (_, w, c, d) in stream_parts:
-        blob = torch.empty(c.size, dtype=torch.uint8).pin_memory()
-        blob.numpy()[:] = c
+    for i, (_, w, c, d) in enumerate(stream_parts):
+        if piece <= 0 and host_blob is not None:
+            blob = host_blob[offs[i]:offs[i] + c.size]
+        else:
+            blob = torch.empty(c.size, dtype=torch.uint8).pin_memory()
+            blob.numpy()[:] = c
         out = torch.empty(d.n, dtype=torch_elem_dtype(fmt), device=dev)
         op = afx.afx_op()
         op.desc = d
@@ -1162,7 +1292,7 @@ def run_cpu_baseline(parts):
     the whole sample), and one slice on one thread."""
     threads = os.cpu_count() or 1
     slices = sum(w.size // ORACLE_SLICE for _, w, _, _ in parts)
-    sample = oracle_sample(parts, threads * max(1, slices // threads))
+    sample = oracle_sample(part_tensors(parts), threads * max(1, slices // threads))
     threads = max(1, min(threads, len(sample)))
     dt, nw = time_oracle(sample, threads)
     dt1, nw1 = time_oracle(sample[:1], 1)

@@ -69,6 +69,8 @@ typedef enum afx_status {
 #define AFX_DEV_BAD_CODE 0x4  /* a bit pattern that is no codeword */
 #define AFX_DEV_BAD_SHAPE 0x8 /* GEMV rows x cols disagree with the block index */
 #define AFX_DEV_TIMEOUT 0x10  /* a staging copy did not arrive within the kernel's wait limit; work skipped */
+#define AFX_DEV_UNDRAINED 0x20 /* after a timeout, a staging copy still had not arrived when the warp stopped:
+                                  the copy may land in shared memory after the kernel's work on it ended */
 
 /* Element formats a container can hold (header field at byte 108; the hi
  * section's offset is the u64 at byte 112, 0 unless FP16).  The
@@ -248,7 +250,10 @@ afx_status afx_decode_gemv_batch(const afx_desc* descs, const void* const* conta
  * this library, held by every GPU that loads it until the process exits;
  * the call itself allocates nothing.  The first call on a device looks up
  * that array's device address (cudaGetSymbolAddress) with the device
- * current, so make that first call before any stream capture.  Every call
+ * current, so make that first call before any stream capture.  The address
+ * is kept with the ID of the context it was found in and looked up again
+ * when a call comes from another current context (for example after
+ * cudaDeviceReset, whose next call then also counts as a first call).  Every call
  * shares the one array and it keeps the last call's contents (nothing in
  * it needs to start at zero: each value read is written earlier in the same
  * call), so calls that overlap on the GPU, on any streams, race; run them
@@ -298,7 +303,11 @@ typedef struct afx_layer {
  * A decode op with out_host set also copies its restored weights to that
  * pinned host buffer, on d2h_stream (copy_stream when NULL) after the op,
  * so that copy overlaps the next layer's load and ops; give layers one
- * tensor each to overlap tensor by tensor.
+ * tensor each to overlap tensor by tensor.  An op whose device output
+ * overlaps one that an earlier layer of the call is still copying back
+ * waits for that copy, and compute_stream waits for the call's last copy
+ * back before any later work on it, so outputs may be reused within and
+ * across calls.
  * Cites: "Why Weight Offloading Slows Inference", section "Loading during
  * computation" and Figure 2 (load layer l+1 while layer l computes; a load
  * is free only if it finishes before the GPU needs it), and "Memory
@@ -331,8 +340,11 @@ afx_status afx_sync(afx_stream_t stream, uint32_t timeout_ms, const int32_t* sta
  * barrier is armed with the bytes it expects and no copy is issued.  Each
  * warp's first wait therefore gives up after wait_polls polls (1..2^22);
  * the kernel ORs AFX_DEV_TIMEOUT into *status_dev (required) and returns
- * without touching out_dev.  Nothing is left in flight, so the context stays
- * usable.  The production entry points wait up to 2^22 polls.
+ * without touching out_dev.  No copy was issued, so nothing is left in
+ * flight and the context stays usable.  The production entry points wait
+ * up to 2^22 polls; when one of their waits runs out, the warp waits for
+ * its issued copies once more (bounded) and ORs AFX_DEV_UNDRAINED as well
+ * if they still have not arrived.
  * No counterpart on the pages: this exists to test the library's own
  * bounded waits.
  * Errors: AFX_E_ARG, AFX_E_FORMAT, AFX_E_CUDA. */

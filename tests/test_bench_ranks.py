@@ -1,8 +1,11 @@
 """The bench's multi-rank host logic on CPU: two gloo ranks, the barrier, the
 max over ranks of the step time, the whole-job throughput, and the
 reference arm running on rank 0 alone."""
+import json
 import os
 import socket
+import subprocess
+import sys
 
 import pytest
 import torch.multiprocessing as mp
@@ -60,3 +63,23 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     args = bench.parse_args(["--impl", "reference", "--steps", "1", "--warmup", "3"])
     bench.run_reference(args)  # rank 1 returns at once, printing nothing
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_loads_only_the_oracle():
+    # the reference arm encodes its sample with the oracle itself: run it in
+    # a fresh process and check which shared objects of this repository it mapped
+    code = (
+        "import json, sys, bench\n"
+        "bench.run_reference(bench.parse_args(['--impl', 'reference', '--workload', 'normal:21', "
+        "'--steps', '1', '--warmup', '3']))\n"
+        "maps = open('/proc/self/maps').read()\n"
+        "print(json.dumps({'afx': 'libafx' in maps, 'orc': 'liborc' in maps}))\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True, timeout=300,
+                         env={**os.environ, "WORLD_SIZE": "1", "RANK": "0"})
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [json.loads(x) for x in out.stdout.splitlines() if x.startswith("{")]
+    ref, maps = lines[0], lines[-1]
+    assert ref["impl"] == "reference" and ref["value"] > 0
+    assert ref["config"]["weights_per_step"] == 1 << 21
+    assert maps == {"afx": False, "orc": True}

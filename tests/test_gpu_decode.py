@@ -190,6 +190,7 @@ def test_staging_wait_that_runs_out_is_flagged_and_the_gpu_stays_usable(afx, n):
     afx.afx_test_restore_stalled(d, dev, out, 2000, status)
     torch.cuda.synchronize()
     assert status.item() & afx.AFX_DEV_TIMEOUT
+    assert not status.item() & afx.AFX_DEV_UNDRAINED  # no copy was issued, so none is waited for
     assert bool((out == 0x5A5A).all())
     # the same context restores the tensor correctly afterwards
     got, st, _ = gpu_decode(afx, c, d)

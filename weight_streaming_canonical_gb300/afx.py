@@ -30,6 +30,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 AFX_OK, AFX_E_ARG, AFX_E_FORMAT, AFX_E_CORRUPT, AFX_E_CUDA, AFX_E_NOSPACE, AFX_E_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
 AFX_DEV_BAD_BLOCK, AFX_DEV_BAD_CHUNK, AFX_DEV_BAD_CODE, AFX_DEV_BAD_SHAPE = 0x1, 0x2, 0x4, 0x8
 AFX_DEV_TIMEOUT = 0x10
+AFX_DEV_UNDRAINED = 0x20
 AFX_MAX_CODE_LEN = 24
 AFX_BLOCK_CAPACITY = 32768
 AFX_HEADER_BYTES = 512

@@ -1595,16 +1595,23 @@ __device__ __forceinline__ bool warp_run(const TabView& tv, WarpSlot& ws, uint8_
                                 sub_bytes, buf ^ 1, stall);
         }
         bool arrived = true;
+        const uint32_t parity = (phases >> buf) & 1u;
         if constexpr (!host_src) {
-            arrived = mbar_wait(&ws.bar[buf], (phases >> buf) & 1u, wait_limit);
+            arrived = mbar_wait(&ws.bar[buf], parity, wait_limit);
             phases ^= 1u << buf;
         }
         if (!__all_sync(0xFFFFFFFFu, arrived)) {
-            // give up on this run: flag it and let the copy still in flight land
+            // give up on this run and flag it.  The copies this warp issued
+            // (into this buffer and, when armed, the other) may still land in
+            // shared memory: wait for both again, bounded, before the warp
+            // stops, and report it when they still have not arrived.  The
+            // failure injection issues no copies, so nothing is in flight.
             if (lane == 0) raise_status(status, AFX_DEV_TIMEOUT);
-            if (r + 1 < nrun) {
-                mbar_wait(&ws.bar[buf ^ 1], (phases >> (buf ^ 1)) & 1u, wait_limit);
-                phases ^= 1u << (buf ^ 1);
+            if (!stall) {
+                bool drained = mbar_wait(&ws.bar[buf], parity, wait_limit);
+                if (r + 1 < nrun)
+                    drained = mbar_wait(&ws.bar[buf ^ 1], (phases >> (buf ^ 1)) & 1u, wait_limit) && drained;
+                if (!__all_sync(0xFFFFFFFFu, drained) && lane == 0) raise_status(status, AFX_DEV_UNDRAINED);
             }
             return false;
         }
@@ -2480,30 +2487,71 @@ extern "C" afx_status afx_decode_gemv(const afx_desc* desc, const void* containe
 // workspace of the fused GEMV lives in one file-scope device array of
 // AFX_STATIC_WORKSPACE_BYTES that every GPU loading the library holds until
 // the process exits.  The array's name in host code is only a stand-in, so
-// its device address is looked up once per device with
-// cudaGetSymbolAddress, with that device current, on the first call made
-// on that device.
+// its device address is looked up with cudaGetSymbolAddress, with the
+// device current, on the first call made on that device.  The address
+// belongs to the context the module was loaded into: it is kept with that
+// context's ID and looked up again when the calling thread's current
+// context is another one (after cudaDeviceReset, or with a context the
+// caller created).
 
 static __device__ __align__(256) float g_static_workspace[AFX_STATIC_WORKSPACE_BYTES / sizeof(float)];
 
 namespace {
 
+struct StaticSlot {
+    void* ptr;
+    unsigned long long ctx_id;
+    bool has_id;
+};
+
 std::mutex g_static_mutex;
-void* g_static_workspace_ptr[afx::kMaxDevices] = {};
+StaticSlot g_static_slot[afx::kMaxDevices] = {};
+
+// The driver's cuCtxGetCurrent and cuCtxGetId, found through the runtime
+// (the library does not link the driver library itself).
+using CtxGetCurrentFn = int (*)(void**);
+using CtxGetIdFn = int (*)(void*, unsigned long long*);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+std::once_flag g_ctx_fns_once;
+
+// The ID of the calling thread's current context; false when there is
+// none yet or the driver does not provide the calls.
+bool current_context_id(unsigned long long* id) {
+    std::call_once(g_ctx_fns_once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f);
+    });
+    if (!g_ctx_get_current || !g_ctx_get_id) return false;
+    void* ctx = nullptr;
+    if (g_ctx_get_current(&ctx) != 0 || !ctx) return false;
+    return g_ctx_get_id(ctx, id) == 0;
+}
 
 afx_status static_workspace(void** ptr) {
     int dev = -1;
     const cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return afx_fail(AFX_E_CUDA, "cudaGetDevice", e);
     if (dev < 0 || dev >= afx::kMaxDevices) return afx_fail(AFX_E_CUDA, "device ordinal out of range", 0);
+    unsigned long long id = 0;
+    bool has_id = current_context_id(&id);
     std::lock_guard<std::mutex> lock(g_static_mutex);
-    if (!g_static_workspace_ptr[dev]) {
+    StaticSlot& slot = g_static_slot[dev];
+    if (!slot.ptr || !has_id || !slot.has_id || slot.ctx_id != id) {
         void* p = nullptr;
         const cudaError_t r = cudaGetSymbolAddress(&p, g_static_workspace);
         if (r != cudaSuccess) return afx_fail(AFX_E_CUDA, "cudaGetSymbolAddress", r);
-        g_static_workspace_ptr[dev] = p;
+        if (!has_id) has_id = current_context_id(&id);  // the lookup may have created the context
+        slot = StaticSlot{p, id, has_id};
     }
-    *ptr = g_static_workspace_ptr[dev];
+    *ptr = slot.ptr;
     return AFX_OK;
 }
 

@@ -14,7 +14,11 @@
 // ops that read it have finished, and a layer's ops start after its copy.
 // Restored tensors that go back to host memory are copied on a third
 // stream after their layer's ops, so that with a full-duplex link the copy
-// back overlaps the next layer's load.  The host never waits.
+// back overlaps the next layer's load.  An op whose output overlaps a
+// device output that an earlier layer of the call is still copying back
+// waits for that copy, and the compute stream waits for the last copy back
+// at the end of the call, so later work on it cannot overwrite an output
+// that is still being read.  The host never waits.
 #include <cuda_runtime.h>
 #include <nvtx3/nvToolsExt.h>
 
@@ -130,6 +134,26 @@ extern "C" afx_status afx_stream_run(const afx_layer* layers, uint32_t n_layers,
     AFX_STREAM_TRY(cudaEventRecord(entry.ev[0], compute), "cudaEventRecord");
     AFX_STREAM_TRY(cudaStreamWaitEvent(copy, entry.ev[0], 0), "cudaStreamWaitEvent");
 
+    // device outputs being copied back to the host, with the event that
+    // marks the end of their layer's copies
+    struct Returning {
+        const uint8_t* begin;
+        const uint8_t* end;
+        size_t event;
+    };
+    std::vector<Returning> returning;
+    EventSet returned;
+    size_t n_returned = 0;
+    for (uint32_t l = 0; l < n_layers; ++l)
+        for (uint32_t i = 0; i < layers[l].n_ops; ++i)
+            if (layers[l].ops[i].kind == AFX_OP_DECODE && layers[l].ops[i].out_host) {
+                ++n_returned;
+                break;
+            }
+    if (n_returned && !returned.create(n_returned))
+        return afx_fail(AFX_E_CUDA, "cudaEventCreateWithFlags", static_cast<int>(cudaGetLastError()));
+    size_t next_returned = 0;
+
     NvtxRange run_range("afx_stream_run");
     for (uint32_t l = 0; l < n_layers; ++l) {
         const afx_layer& L = layers[l];
@@ -144,6 +168,16 @@ extern "C" afx_status afx_stream_run(const afx_layer* layers, uint32_t n_layers,
                            "cudaMemcpyAsync");
         AFX_STREAM_TRY(cudaEventRecord(copied.ev[k], copy), "cudaEventRecord");
         AFX_STREAM_TRY(cudaStreamWaitEvent(compute, copied.ev[k], 0), "cudaStreamWaitEvent");
+        // an output still being copied back by an earlier layer is not overwritten before that copy
+        for (uint32_t i = 0; i < L.n_ops && !returning.empty(); ++i) {
+            const afx_op& op = L.ops[i];
+            const uint64_t bytes = op.kind == AFX_OP_GEMV ? uint64_t{4} * op.batch * op.rows
+                                   : op.desc.format == AFX_FMT_E4M3 ? op.desc.n : op.desc.n * sizeof(uint16_t);
+            const uint8_t* b = static_cast<const uint8_t*>(op.out_dev);
+            for (const Returning& r : returning)
+                if (bytes && b < r.end && r.begin < b + bytes)
+                    AFX_STREAM_TRY(cudaStreamWaitEvent(compute, returned.ev[r.event], 0), "cudaStreamWaitEvent");
+        }
         // consecutive ops of one kind (and one GEMV batch size) share a launch
         for (uint32_t i = 0; i < L.n_ops;) {
             uint32_t j = i + 1;
@@ -166,8 +200,16 @@ extern "C" afx_status afx_stream_run(const afx_layer* layers, uint32_t n_layers,
                 AFX_STREAM_TRY(cudaMemcpyAsync(op.out_host, op.out_dev, bytes,
                                                cudaMemcpyDeviceToHost, d2h),
                                "cudaMemcpyAsync");
+                const uint8_t* b = static_cast<const uint8_t*>(op.out_dev);
+                returning.push_back({b, b + bytes, next_returned});
             }
+            AFX_STREAM_TRY(cudaEventRecord(returned.ev[next_returned], d2h), "cudaEventRecord");
+            ++next_returned;
         }
     }
+    // later work on the compute stream (another call's ops included) comes
+    // after the copies back have read their device outputs
+    if (next_returned)
+        AFX_STREAM_TRY(cudaStreamWaitEvent(compute, returned.ev[next_returned - 1], 0), "cudaStreamWaitEvent");
     return AFX_OK;
 }
