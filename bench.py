@@ -1209,7 +1209,7 @@ def run_stream_bench(afx, parts, dev, args, layers=40):
     import torch
     blob_host = []
     for seed_shift in (0, 1):
-        ps = parts if seed_shift == 0 else build_layer(args.seed + 1)
+        ps = parts if seed_shift == 0 else build_layer(args.seed + 1, 0, "layer")
         size = sum(c.size for _, _, c, _ in ps)
         b = torch.empty(size, dtype=torch.uint8).pin_memory()
         o = 0

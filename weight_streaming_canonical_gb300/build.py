@@ -53,7 +53,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, 
     lib = LIB_DEBUG if debug_bounds else LIB
     os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
-    headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".h")]
+    headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     headers.append(os.path.join(os.path.dirname(HERE), "include", "afx.h"))
     srcs = sources()
     objs = []

@@ -1,0 +1,949 @@
+// sm_103a fused restore + tensor-core product for prefill
+// (afx_prefill_fused, afx_prefill_fused_batch).
+//
+// The operation: Y[t][r] = sum_c W[r][c] X[t][c] for the N token vectors of
+// a prompt ("Memory requirements of language model inference on a consumer
+// GPU", section "Loading one part of the model at a time": the prompt goes
+// through each layer as a whole before the answer is produced token by
+// token), with W restored from its exponent-coded container on the way ("Why
+// Weight Offloading Slows Inference", section "Lossless compression: fewer
+// bytes to read, more work to unpack": the released bits are restored before
+// compute; the restore is that page's t_unpack of Eq. (1)).  The restored
+// weights go from the decoder straight into the tensor cores' shared-memory
+// operand tiles and never reach global memory.
+//
+// Weight order.  The container holds W in tile order: 128 x 64 tiles of
+// W, row-major inside a tile, the 64-column tiles of one 128-row band (an
+// "m-tile") consecutive, the bands in order (afx_tile_order writes it).  A
+// band's weights are then one contiguous range of the stream, in the order
+// in which the product consumes its k-tiles.
+//
+// Work decomposition.  A work item is one m-tile of one matrix for one pass
+// of up to 512 tokens; the host assigns items to persistent CTAs (longest
+// first, each to the least loaded CTA), one CTA per SM.  Inside a CTA:
+//   - 16 decoding warps restore the item's sub-tiles (32 chunks each,
+//     interleaved across the warps) with the byte-step decoder of the
+//     restore kernel and write each weight into a ring of four 16 KB A
+//     tiles (128 x 64 BF16, K-major, 128-byte swizzle).  A tile is full once
+//     its 8192 weights have been counted in; the warp that completes it
+//     signals the tile's barrier.
+//   - a producer warp loads the token vectors with TMA: 16 columns x up to
+//     256 tokens per stage (32-byte swizzle), a ring of four stages;
+//   - an MMA warp issues tcgen05.mma (M = 128, N = tokens of one half, K =
+//     16) from the two rings into a float32 accumulator in tensor memory (up
+//     to 2 x 256 columns) and returns ring slots with tcgen05.commit;
+//   - four epilogue warps read the accumulator with tcgen05.ld (each its
+//     32-lane quarter) and store Y, row by row of W, coalesced across lanes.
+// Every wait is bounded; a wait that runs out sets AFX_DEV_TIMEOUT and an
+// abort flag that every role polls, copies in flight are waited for, and the
+// CTA frees its tensor memory and exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <memory>
+#include <mutex>
+#include <queue>
+#include <vector>
+
+#include "afx_warp_decode.cuh"
+
+namespace afx {
+
+constexpr int kPfDecodeWarps = 16;
+constexpr int kPfProducerWarp = kPfDecodeWarps;
+constexpr int kPfMmaWarp = kPfDecodeWarps + 1;
+constexpr int kPfEpiWarp0 = kPfDecodeWarps + 2;
+constexpr int kPfWarps = kPfDecodeWarps + 6;
+constexpr int kPfThreads = kPfWarps * 32;
+constexpr uint32_t kDecodeBarrier = 1;  // named barrier of the decoding warps
+constexpr uint32_t kTileRows = 128, kTileCols = 64, kTileElems = kTileRows * kTileCols;
+constexpr uint32_t kTileBytes = kTileElems * 2;
+constexpr uint32_t kSliceK = 16;             // K of one MMA and of one activation stage
+constexpr uint32_t kASlots = 4, kBSlots = 4;
+constexpr uint32_t kMaxHalfTokens = 256;     // N of one MMA
+constexpr uint32_t kMaxPassTokens = 2 * kMaxHalfTokens;
+constexpr int kPfMaxItems = 2048;
+constexpr int kPfMaxCtas = 256;
+
+static_assert(kPfDecodeWarps == kSubtilesPerBlock, "the decoding warps cover one block of sub-tiles per round");
+static_assert(((kPfEpiWarp0 + 0) % 4) != ((kPfEpiWarp0 + 1) % 4) && ((kPfEpiWarp0 + 2) % 4) != ((kPfEpiWarp0 + 3) % 4),
+              "the epilogue warps cover the four lane quarters of tensor memory");
+
+struct PrefillMatrix {
+    TensorArgs t;       // sections, geometry and code tables; t.y = Y [n_tokens][rows]
+    uint32_t k_tiles;   // cols / 64
+    uint32_t single;    // 1: one exponent for every weight (no coded stream)
+    uint32_t fill;      // that exponent
+};
+
+// An item: matrix << 28 | pass << 18 | m-tile.
+struct PrefillArgs {
+    CUtensorMap tmap[kMaxTensors];  // X of each matrix: [n_tokens][cols] BF16, box 16 x n_mma, 32-byte swizzle
+    PrefillMatrix m[kMaxTensors];
+    uint32_t count, n_tokens, n_mma, halves, pass_tokens, tab_bytes, tmem_cols, wait_limit, max_chunk_bytes;
+    int32_t* status;
+    uint16_t cta_begin[kPfMaxCtas + 1];
+    uint32_t items[kPfMaxItems];
+};
+
+// Control block in shared memory.
+struct PfCtl {
+    uint64_t a_full[kASlots], a_empty[kASlots];
+    uint64_t b_full[kBSlots], b_empty[kBSlots];
+    uint64_t acc_full, acc_empty, drain;
+    uint32_t a_count[kASlots];  // weights counted into each A slot's current tile
+    uint32_t tmem_base;
+    int32_t abort_flag;
+};
+
+// Shared-memory layout (offsets from a 1024-byte aligned base).
+struct PfLayout {
+    uint32_t a, b, b_stage, ctl, shw, slots, streams, wstride, total;
+};
+
+__host__ __device__ inline uint32_t round_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+__host__ __device__ inline PfLayout pf_layout(uint32_t tab_bytes, uint32_t n_mma, uint32_t max_chunk_bytes) {
+    PfLayout L;
+    L.a = 0;
+    L.b_stage = round_up(n_mma * kSliceK * 2, 1024);
+    L.b = L.a + kASlots * kTileBytes;
+    L.ctl = L.b + kBSlots * L.b_stage;
+    L.shw = round_up(L.ctl + static_cast<uint32_t>(sizeof(PfCtl)), 16);
+    L.slots = round_up(L.shw + static_cast<uint32_t>(sharedw_table_offset()) + tab_bytes, 16);
+    L.streams = L.slots + kPfDecodeWarps * static_cast<uint32_t>(sizeof(WarpSlot));
+    L.wstride = kWarpChunks * max_chunk_bytes + kStreamPad;
+    L.total = L.streams + kPfDecodeWarps * 2 * L.wstride;
+    return L;
+}
+
+// ---- tensor-core, TMA and barrier helpers ------------------------------------------
+
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t n) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
+}
+
+// OR of p over the n threads of named barrier id (a barrier as well).
+__device__ __forceinline__ bool named_red_or(uint32_t id, uint32_t n, bool p) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"(p ? 1u : 0u), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+struct DecodeSync {
+    __device__ __forceinline__ void operator()() const { named_sync(kDecodeBarrier, kPfDecodeWarps * 32); }
+};
+
+__device__ __forceinline__ void mbar_init_count(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Adds v to a shared counter with acquire-release ordering (the writes this
+// thread made or observed come before it; later reads see the others').
+__device__ __forceinline__ uint32_t atomic_add_acq_rel(uint32_t* p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;\n" : "=r"(old) : "r"(smem_u32(p)), "r"(v) : "memory");
+    return old;
+}
+
+// The 16 x rows box at (x, y) of the tensor map into shared dst, completing on bar.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint32_t x, uint32_t y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::
+            "r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+
+// Shared-memory matrix descriptors, K-major.  A: 128-byte rows, 128-byte
+// swizzle, 8-row groups 1024 bytes apart.  B: 32-byte rows, 32-byte
+// swizzle, 8-row groups 256 bytes apart.  Fields: start address >> 4
+// (bits 0-13), leading byte offset >> 4 (16-29, unused for swizzled
+// K-major), stride byte offset >> 4 (32-45), descriptor version 1 (46),
+// layout (61-63: 2 = 128-byte swizzle, 6 = 32-byte swizzle).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (uint64_t{1} << 16) | (uint64_t{1024 >> 4} << 32) |
+           (uint64_t{1} << 46) | (uint64_t{2} << 61);
+}
+
+__device__ __forceinline__ uint64_t desc_sw32(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (uint64_t{1} << 16) | (uint64_t{256 >> 4} << 32) |
+           (uint64_t{1} << 46) | (uint64_t{6} << 61);
+}
+
+// D[tmem] (+)= A * B^T: BF16 operands, float32 accumulator.
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, bool acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(acc ? 1u : 0u)
+        : "memory");
+}
+
+// bar gets one arrival once every tcgen05 operation this thread issued has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+          "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+}
+
+// Waits for phase `parity` of bar, at most limit polls, giving up early
+// once another role has raised the abort flag.  A wait that runs out raises
+// the flag and AFX_DEV_TIMEOUT.
+__device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, uint32_t limit, PfCtl& ctl, int32_t* status) {
+    for (uint32_t i = 0; i < limit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 31u) == 31u && *reinterpret_cast<volatile int32_t*>(&ctl.abort_flag)) return false;
+    }
+    *reinterpret_cast<volatile int32_t*>(&ctl.abort_flag) = 1;
+    raise_status(status, AFX_DEV_TIMEOUT);
+    return false;
+}
+
+// ---- the decoding warps: restored weights into the A ring -------------------------------
+
+// Byte offset of tile weight i (row i / 64, column i % 64) in a 128-byte
+// swizzled K-major tile: row r at r * 128, its 16-byte chunk c at
+// (c ^ (r & 7)) * 16.
+__device__ __forceinline__ uint32_t tile_offset(uint32_t i) {
+    const uint32_t r = i >> 6, c = i & 63u;
+    return (r << 7) | ((((c >> 3) ^ r) & 7u) << 4) | ((c & 7u) << 1);
+}
+
+// Writes tile weights [i0, i1) into the A slot at `tile`: the stage byte
+// of tile weight i is stage[i + d] and its sign|mantissa byte sm[i] (sm
+// points at the tile's first weight).  Groups of 8 whole weights go out as
+// 16-byte stores, one group per lane at a time; the partial groups at
+// either end (shared with neighbouring ranges) weight by weight.
+__device__ __forceinline__ void tile_write(uint8_t* tile, const uint8_t* stage, uint32_t d, const uint8_t* sm,
+                                           uint32_t i0, uint32_t i1, int lane) {
+    const uint32_t f0 = (i0 + 7) & ~7u, f1 = i1 & ~7u;
+    const uint32_t head_end = f0 < i1 ? f0 : i1;
+    for (uint32_t i = i0 + lane; i < head_end; i += 32)
+        *reinterpret_cast<uint16_t*>(tile + tile_offset(i)) = join1(stage[i + d], __ldg(sm + i));
+    const uint32_t tail0 = f1 > f0 ? f1 : f0;
+    for (uint32_t i = tail0 + lane; i < i1; i += 32)
+        *reinterpret_cast<uint16_t*>(tile + tile_offset(i)) = join1(stage[i + d], __ldg(sm + i));
+    for (uint32_t g = (f0 >> 3) + lane; g < (f1 >> 3); g += 32) {
+        const uint32_t i = g << 3;
+        const uint4 w = join8(*reinterpret_cast<const uint2*>(stage + i + d), __ldg(reinterpret_cast<const uint2*>(sm + i)));
+        *reinterpret_cast<uint4*>(tile + tile_offset(i)) = w;
+    }
+}
+
+// The range [o0, o1) of the tensor's weights (positions in the container's
+// tile order), clipped to the item's [p_lo, p_hi), into the A ring: for each
+// tile met, wait until its slot is free, write, and count the weights in;
+// the warp that completes a tile's 8192 signals its full barrier.  Returns
+// false when a wait gave up.
+__device__ __forceinline__ bool ring_write(uint8_t* ring_a, PfCtl& ctl, const uint8_t* stage, uint64_t stage_o,
+                                           const uint8_t* sm, uint64_t o0, uint64_t o1, uint64_t p_lo, uint64_t p_hi,
+                                           uint32_t q_base, uint32_t wait_limit, int32_t* status, int lane) {
+    const uint64_t c0 = o0 > p_lo ? o0 : p_lo, c1 = o1 < p_hi ? o1 : p_hi;
+    if (c0 >= c1) return true;
+    const uint32_t g0 = static_cast<uint32_t>((c0 - p_lo) / kTileElems), g1 = static_cast<uint32_t>((c1 - 1 - p_lo) / kTileElems);
+    for (uint32_t g = g0; g <= g1; ++g) {
+        const uint32_t q = q_base + g, slot = q % kASlots;
+        if (!__all_sync(0xFFFFFFFFu, pf_wait(&ctl.a_empty[slot], ((q / kASlots) & 1u) ^ 1u, wait_limit, ctl, status)))
+            return false;
+        const uint64_t t_lo = p_lo + static_cast<uint64_t>(g) * kTileElems;
+        const uint64_t a = c0 > t_lo ? c0 : t_lo, b = c1 < t_lo + kTileElems ? c1 : t_lo + kTileElems;
+        const uint32_t i0 = static_cast<uint32_t>(a - t_lo), i1 = static_cast<uint32_t>(b - t_lo);
+        AFX_CHECK(i1 <= kTileElems && a - stage_o + (i1 - i0) <= static_cast<uint64_t>(kWarpStage), kChkMergeStage);
+        tile_write(ring_a + slot * kTileBytes, stage, static_cast<uint32_t>(t_lo - stage_o), sm + t_lo, i0, i1, lane);
+        fence_proxy_async_smem();  // the tensor cores read the tile through the async proxy
+        __syncwarp();
+        if (lane == 0) {
+            const uint32_t old = atomic_add_acq_rel(&ctl.a_count[slot], i1 - i0);
+            if (old < kTileElems && old + (i1 - i0) >= kTileElems) {
+                atomic_add_acq_rel(&ctl.a_count[slot], 0u - kTileElems);
+                mbar_arrive(&ctl.a_full[slot]);
+            }
+        }
+    }
+    return true;
+}
+
+// The sub-tile holding the code of output position p: the last block whose
+// index entry is <= p (a 32-way search, one load per lane and step), then
+// the last of its 16 sub-tiles whose first code is at or before p.  Also
+// returns that sub-tile's first output position.
+__device__ __forceinline__ uint64_t find_sub_tile(const TensorArgs& t, uint64_t p, int lane) {
+    uint64_t lo = 0, hi = t.n_blocks;  // the block is in [lo, hi)
+    while (hi - lo > 1) {
+        const uint64_t step = (hi - lo + 31) / 32;
+        const uint64_t idx = lo + static_cast<uint64_t>(lane) * step;
+        const bool le = idx < hi && __ldg(t.block_index + idx) <= p;
+        const uint32_t m = __ballot_sync(0xFFFFFFFFu, le);
+        const int top = m ? 31 - __clz(static_cast<int>(m)) : 0;
+        lo = lo + static_cast<uint64_t>(top) * step;
+        hi = lo + step < hi ? lo + step : hi;
+    }
+    const uint64_t b = lo;
+    // lane l sums the counts of chunks [b * 512 + 16 l, + 16)
+    uint32_t sum = 0;
+    const uint64_t cbase = b * kThreads + static_cast<uint64_t>(lane) * 16;
+#pragma unroll 4
+    for (uint32_t j = 0; j < 16; ++j)
+        if (cbase + j < t.n_chunks) sum += __ldg(t.chunk_index + cbase + j) >> 5;
+    uint32_t inc = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+        if (lane >= d) inc += o;
+    }
+    // sub-tile k starts after lanes 0 .. 2k-1: lane 2k's exclusive prefix
+    const uint64_t base = __ldg(t.block_index + b);
+    const uint64_t start_k = base + (inc - sum);
+    const uint64_t n_sub = (t.n_chunks + kWarpChunks - 1) / kWarpChunks;
+    const bool cand = (lane & 1) == 0 && start_k <= p && b * kSubtilesPerBlock + (lane >> 1) < n_sub;
+    const uint32_t m = __ballot_sync(0xFFFFFFFFu, cand);
+    const int top = m ? 31 - __clz(static_cast<int>(m)) : 0;
+    return b * kSubtilesPerBlock + static_cast<uint64_t>(top >> 1);
+}
+
+// Output position of the first code of sub-tile s: the block's index entry
+// plus the counts of the block's chunks before it.
+__device__ __forceinline__ uint64_t sub_tile_start(const TensorArgs& t, uint64_t s, int lane) {
+    const uint64_t blk = s / kSubtilesPerBlock;
+    uint32_t pre = 0;
+    for (uint64_t c = blk * kThreads + lane; c < s * kWarpChunks; c += 32) pre += __ldg(t.chunk_index + c) >> 5;
+    return __ldg(t.block_index + blk) + warp_sum(pre);
+}
+
+// Restores the item's weights [p_lo, p_hi) of tensor t with decoding warp
+// `warp`: sub-tiles s_lo + warp, s_lo + warp + 16, ... of the sub-tiles that
+// hold them, staged one ahead by bulk copies as in the restore kernel.
+// Returns false when a wait gave up (the staging copies still in flight are
+// waited for first).
+__device__ bool pf_decode_item(const TabView& tv, WarpSlot& ws, uint8_t* wstream, uint32_t wstride,
+                               const TensorArgs& t, uint64_t p_lo, uint64_t p_hi, uint32_t q_base, uint8_t* ring_a,
+                               PfCtl& ctl, int warp, int lane, int32_t* status, uint32_t wait_limit,
+                               uint32_t& phases) {
+    const uint32_t T = t.chunk_bytes;
+    const uint32_t chunk_bits = 8u * T;
+    const uint32_t sub_bytes = kWarpChunks * T, sub_bits = 8u * sub_bytes;
+    const bool fsm = t.tab.fsm != 0;
+    const uint32_t skip_row0 = t.tab.n_states * kFsmRowBytes;
+    const uint64_t n_sub = (t.n_chunks + kWarpChunks - 1) / kWarpChunks;
+    const uint64_t n = t.n;
+    const uint64_t s_lo = find_sub_tile(t, p_lo, lane);
+    const uint64_t s_hi = find_sub_tile(t, p_hi - 1, lane) + 1;
+    uint64_t s = s_lo + static_cast<uint64_t>(warp);
+    if (s >= s_hi || s_hi > n_sub) return true;
+    const uint8_t* exp_base = reinterpret_cast<const uint8_t*>(t.exp_words);
+    if (lane == 0)
+        warp_issue_bulk(ws, wstream, t, s, s < t.n_sub_full, exp_base + s * sub_bytes,
+                        t.chunk_index + s * kWarpChunks, sub_bytes, 0, false);
+    uint64_t start = sub_tile_start(t, s, lane);
+    int buf = 0;
+    for (; s < s_hi; s += kPfDecodeWarps) {
+        const uint64_t s_next = s + kPfDecodeWarps;
+        const bool more = s_next < s_hi;
+        if (more && lane == 0)
+            warp_issue_bulk(ws, wstream + (buf ^ 1) * wstride, t, s_next, s_next < t.n_sub_full,
+                            exp_base + s_next * sub_bytes, t.chunk_index + s_next * kWarpChunks, sub_bytes, buf ^ 1,
+                            false);
+        const uint32_t parity = (phases >> buf) & 1u;
+        const bool arrived = mbar_wait(&ws.bar[buf], parity, wait_limit);
+        phases ^= 1u << buf;
+        if (!__all_sync(0xFFFFFFFFu, arrived)) {
+            // flag it, let the copies in flight land (bounded), and stop
+            if (lane == 0) {
+                raise_status(status, AFX_DEV_TIMEOUT);
+                *reinterpret_cast<volatile int32_t*>(&ctl.abort_flag) = 1;
+            }
+            bool drained = mbar_wait(&ws.bar[buf], parity, wait_limit);
+            if (more) {
+                drained = mbar_wait(&ws.bar[buf ^ 1], (phases >> (buf ^ 1)) & 1u, wait_limit) && drained;
+                phases ^= 1u << (buf ^ 1);
+            }
+            if (!__all_sync(0xFFFFFFFFu, drained) && lane == 0) raise_status(status, AFX_DEV_UNDRAINED);
+            return false;
+        }
+        const uint64_t start_next = more ? sub_tile_start(t, s_next, lane) : 0;
+        const bool full = s < t.n_sub_full;
+        const uint32_t nexist =
+            full ? 64u : static_cast<uint32_t>(min(t.n_chunks - min(t.n_chunks, s * kWarpChunks), uint64_t{64}));
+        const uint32_t entry = static_cast<uint32_t>(lane) < nexist ? ws.chunk[buf][lane] : 0u;
+        const uint32_t gap = entry & 31u;
+        uint32_t cnt = entry >> 5;
+        bool bad = false;
+        if (gap > 23u || cnt > chunk_bits - gap || cnt > static_cast<uint32_t>(kMaxChunkCodes)) {
+            bad = true;
+            cnt = 0;
+        }
+        uint32_t inc = cnt;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+            if (lane >= d) inc += o;
+        }
+        const uint32_t total = __shfl_sync(0xFFFFFFFFu, inc, 31);
+        const uint64_t o0 = start, o1 = start + total;
+        const bool in_range = o0 <= n && o1 <= n;
+        if (lane == 0) {
+            if (!in_range) {
+                raise_status(status, AFX_DEV_BAD_BLOCK);
+            } else {
+                // the block index must agree with the counts where a block ends
+                const uint64_t blk = s / kSubtilesPerBlock;
+                if (s + 1 == n_sub) {
+                    if (o1 != n || __ldg(t.block_index + t.n_blocks) != n) raise_status(status, AFX_DEV_BAD_BLOCK);
+                } else if ((s + 1) % kSubtilesPerBlock == 0 && __ldg(t.block_index + blk + 1) != o1) {
+                    raise_status(status, AFX_DEV_BAD_BLOCK);
+                }
+                if (s == 0 && o0 != 0) raise_status(status, AFX_DEV_BAD_BLOCK);
+                if (o0 < o1) {  // the raw bytes are needed after the decode
+                    const uint64_t a0 = o0 & ~uint64_t(15), a1 = (o1 + 15) & ~uint64_t(15);
+                    prefetch_l2(t.sm + a0, static_cast<uint32_t>(a1 - a0));
+                }
+            }
+        }
+        const uint32_t next = static_cast<uint32_t>(lane) + 1 < nexist ? ws.chunk[buf][lane + 1] : 0u;
+        const uint32_t* stream = reinterpret_cast<const uint32_t*>(wstream + static_cast<size_t>(buf) * wstride);
+        const uint32_t chunk_end = (lane + 1) * chunk_bits;
+        bool stepped = false;
+        FsmLane fl;
+        if (cnt && in_range) {
+            const uint32_t s_run = static_cast<uint32_t>(o0 & 7u) + (inc - cnt);
+            if (fsm) {
+                uint32_t stream_end = sub_bits;
+                if (!full) {
+                    const uint64_t bit0 = s * static_cast<uint64_t>(sub_bits);
+                    const uint64_t left = t.total_bits > bit0 ? t.total_bits - bit0 : 0;
+                    stream_end = left < sub_bits ? static_cast<uint32_t>(left) : sub_bits;
+                }
+                AFX_CHECK((lane + 1) * (T >> 2) <= wstride >> 2, kChkStreamWords);
+                if (chunk_end <= stream_end) {
+                    fsm_chunk_steps(tv, stream + lane * (T >> 2), T >> 2, gap, skip_row0, ws.stage, s_run, fl);
+                    stepped = true;
+                } else {
+                    AFX_CHECK(s_run + cnt <= static_cast<uint32_t>(kWarpStage), kChkStageRun);
+                    bad = decode_run_fsm(tv, stream, lane * (T >> 2), gap, cnt, ws.stage, s_run, next, chunk_end,
+                                         stream_end);
+                }
+            } else {
+                AFX_CHECK(s_run + cnt <= static_cast<uint32_t>(kWarpStage), kChkStageRun);
+                bad = decode_run(tv, stream, warp_stream_bytes(t, s) >> 2, lane * (T >> 2), gap, cnt, ws.stage, s_run,
+                                 next, chunk_end);
+            }
+        }
+        __syncwarp();
+        if (stepped) {
+            AFX_CHECK(reinterpret_cast<uint8_t*>(fl.wout) + 4 <= ws.stage + kWarpStage, kChkStagePending);
+            bad = fsm_chunk_finish(tv, stream, fl, cnt, chunk_end, next);
+        }
+        if (bad) raise_status(status, AFX_DEV_BAD_CHUNK);
+        __syncwarp();
+        // the sub-tile's weights go into the ring even when its stream was
+        // bad (the output is then unspecified), so that every tile completes
+        const uint64_t w0 = in_range ? o0 : 0, w1 = in_range ? o1 : 0;
+        if (!ring_write(ring_a, ctl, ws.stage, o0 & ~uint64_t(7), t.sm, w0, w1, p_lo, p_hi, q_base, wait_limit, status,
+                        lane)) {
+            if (more) {  // the next sub-tile's copies are in flight: let them land
+                const bool drained = mbar_wait(&ws.bar[buf ^ 1], (phases >> (buf ^ 1)) & 1u, wait_limit);
+                phases ^= 1u << (buf ^ 1);
+                if (!__all_sync(0xFFFFFFFFu, drained) && lane == 0) raise_status(status, AFX_DEV_UNDRAINED);
+            }
+            return false;
+        }
+        start = start_next;
+        buf ^= 1;
+        fence_proxy_async_smem();  // this buffer's reads come before the bulk copy that refills it
+        __syncwarp();
+    }
+    return true;
+}
+
+// Items of a tensor with one exponent for every weight: pieces of 2048
+// weights, interleaved across the decoding warps, joined with the constant
+// exponent (the warp's stage holds it at every index).
+__device__ bool pf_fill_item(const PrefillMatrix& pm, WarpSlot& ws, uint64_t p_lo, uint64_t p_hi, uint32_t q_base,
+                             uint8_t* ring_a, PfCtl& ctl, int warp, int lane, int32_t* status, uint32_t wait_limit) {
+    constexpr uint32_t kPiece = 2048;
+    static_assert(kPiece <= static_cast<uint32_t>(kWarpStage), "a fill piece fits the stage");
+    const uint32_t f4 = ror8(pm.fill) * 0x01010101u;
+    for (uint32_t i = lane; i < kPiece / 4; i += 32) reinterpret_cast<uint32_t*>(ws.stage)[i] = f4;
+    if (lane == 0 && warp == 0 && p_lo == 0 && __ldg(pm.t.block_index) != pm.t.n) raise_status(status, AFX_DEV_BAD_BLOCK);
+    __syncwarp();
+    for (uint64_t o = p_lo + static_cast<uint64_t>(warp) * kPiece; o < p_hi; o += kPfDecodeWarps * kPiece) {
+        const uint64_t e = o + kPiece < p_hi ? o + kPiece : p_hi;
+        if (!ring_write(ring_a, ctl, ws.stage, o, pm.t.sm, o, e, p_lo, p_hi, q_base, wait_limit, status, lane))
+            return false;
+    }
+    return true;
+}
+
+// ---- the kernel ----------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __grid_constant__ PrefillArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const PfLayout L = pf_layout(a.tab_bytes, a.n_mma, a.max_chunk_bytes);
+    uint8_t* ring_a = smem + L.a;
+    uint8_t* ring_b = smem + L.b;
+    PfCtl& ctl = *reinterpret_cast<PfCtl*>(smem + L.ctl);
+    SharedW& sh = *reinterpret_cast<SharedW*>(smem + L.shw);
+    uint8_t* tabr = smem + L.shw + sharedw_table_offset();
+    WarpSlot* slots = reinterpret_cast<WarpSlot*>(smem + L.slots);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t it0 = a.cta_begin[blockIdx.x], it1 = a.cta_begin[blockIdx.x + 1];
+    const uint32_t wait_limit = a.wait_limit ? a.wait_limit : kWaitLimit;
+    int32_t* const status = a.status;
+
+    if (threadIdx.x == 0) {
+        for (uint32_t i = 0; i < kASlots; ++i) {
+            mbar_init_count(&ctl.a_full[i], 1);
+            mbar_init_count(&ctl.a_empty[i], 1);
+            ctl.a_count[i] = 0;
+        }
+        for (uint32_t i = 0; i < kBSlots; ++i) {
+            mbar_init_count(&ctl.b_full[i], 1);
+            mbar_init_count(&ctl.b_empty[i], 1);
+        }
+        mbar_init_count(&ctl.acc_full, 1);
+        mbar_init_count(&ctl.acc_empty, 4);
+        mbar_init_count(&ctl.drain, 1);
+        ctl.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    if (warp < kPfDecodeWarps && lane == 0) {
+        mbar_init(&slots[warp].bar[0]);
+        mbar_init(&slots[warp].bar[1]);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    if (warp == kPfMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(&ctl.tmem_base)),
+                     "r"(a.tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl.tmem_base;
+
+    if (warp < kPfDecodeWarps) {
+        // ---- restore the items' weights into the A ring
+        WarpSlot& ws = slots[warp];
+        uint8_t* wstream = smem + L.streams + static_cast<size_t>(warp) * 2 * L.wstride;
+        TabView tv;
+        tv.lut = reinterpret_cast<const uint32_t*>(tabr);
+        tv.len0 = tabr + kLutSize * 4;
+        tv.limit = sh.ct.limit;
+        tv.base = sh.ct.base;
+        tv.sorted = sh.ct.sorted;
+        tv.first = sh.first;
+        tv.fsm = reinterpret_cast<const char*>(tabr);
+        tv.depth = sh.ct.state_depth;
+        tv.fsm_bytes = a.tab_bytes;
+        uint32_t phases = 0, q_base = 0;
+        int built = -1;
+        bool alive = true;
+        for (uint32_t it = it0; it < it1; ++it) {
+            const uint32_t item = a.items[it];
+            const uint32_t mi = item >> 28, mt = item & 0x3FFFFu;
+            const PrefillMatrix& pm = a.m[mi];
+            // every decoding warp has finished the previous item; all stop together
+            if (named_red_or(kDecodeBarrier, kPfDecodeWarps * 32,
+                             !alive || *reinterpret_cast<volatile int32_t*>(&ctl.abort_flag) != 0))
+                break;
+            if (!pm.single && static_cast<int>(mi) != built) {
+                build_tables_w(sh, tabr, pm.t.tab, threadIdx.x, kPfDecodeWarps * 32, DecodeSync{});
+                built = static_cast<int>(mi);
+            }
+            const uint64_t p_lo = static_cast<uint64_t>(mt) * pm.k_tiles * kTileElems;
+            const uint64_t p_hi = p_lo + static_cast<uint64_t>(pm.k_tiles) * kTileElems;
+            alive = pm.single ? pf_fill_item(pm, ws, p_lo, p_hi, q_base, ring_a, ctl, warp, lane, status, wait_limit)
+                              : pf_decode_item(tv, ws, wstream, L.wstride, pm.t, p_lo, p_hi, q_base, ring_a, ctl, warp,
+                                               lane, status, wait_limit, phases);
+            q_base += pm.k_tiles;
+        }
+    } else if (warp == kPfProducerWarp) {
+        // ---- token vectors into the B ring, in the order the MMAs take them
+        if (lane == 0) {
+            uint32_t bseq = 0;
+            bool ok = true;
+            const uint32_t stage_bytes = a.n_mma * kSliceK * 2;
+            for (uint32_t it = it0; it < it1 && ok; ++it) {
+                const uint32_t item = a.items[it];
+                const uint32_t mi = item >> 28, pass = (item >> 18) & 0x3FFu;
+                const PrefillMatrix& pm = a.m[mi];
+                const uint32_t y0 = pass * a.pass_tokens;
+                for (uint32_t g = 0; g < pm.k_tiles && ok; ++g)
+                    for (uint32_t ks = 0; ks < kTileCols / kSliceK && ok; ++ks)
+                        for (uint32_t h = 0; h < a.halves; ++h) {
+                            const uint32_t b = bseq % kBSlots;
+                            if (!pf_wait(&ctl.b_empty[b], ((bseq / kBSlots) & 1u) ^ 1u, wait_limit, ctl, status)) {
+                                ok = false;
+                                break;
+                            }
+                            mbar_expect_tx(&ctl.b_full[b], stage_bytes);
+                            tma_load_2d(ring_b + b * L.b_stage, &a.tmap[mi], g * kTileCols + ks * kSliceK,
+                                        y0 + h * a.n_mma, &ctl.b_full[b]);
+                            ++bseq;
+                        }
+            }
+            if (!ok) {  // the loads still in flight land before the CTA exits
+                for (uint32_t j = bseq > kBSlots ? bseq - kBSlots : 0; j < bseq; ++j)
+                    if (!mbar_wait(&ctl.b_full[j % kBSlots], (j / kBSlots) & 1u, wait_limit))
+                        raise_status(status, AFX_DEV_UNDRAINED);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kPfMmaWarp) {
+        // ---- the products, into the accumulator in tensor memory
+        if (lane == 0) {
+            const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((a.n_mma >> 3) << 17) | ((kTileRows >> 4) << 24);
+            uint32_t q = 0, bseq = 0, n_item = 0;
+            bool ok = true;
+            for (uint32_t it = it0; it < it1 && ok; ++it) {
+                const PrefillMatrix& pm = a.m[a.items[it] >> 28];
+                if (n_item > 0) {  // the epilogue has read the previous item's accumulator
+                    ok = pf_wait(&ctl.acc_empty, (n_item - 1) & 1u, wait_limit, ctl, status);
+                    tc_fence_after();
+                }
+                for (uint32_t g = 0; g < pm.k_tiles && ok; ++g, ++q) {
+                    const uint32_t slot = q % kASlots;
+                    if (!pf_wait(&ctl.a_full[slot], (q / kASlots) & 1u, wait_limit, ctl, status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(ring_a + slot * kTileBytes);
+                    for (uint32_t ks = 0; ks < kTileCols / kSliceK && ok; ++ks)
+                        for (uint32_t h = 0; h < a.halves; ++h) {
+                            const uint32_t b = bseq % kBSlots;
+                            if (!pf_wait(&ctl.b_full[b], (bseq / kBSlots) & 1u, wait_limit, ctl, status)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            tc_mma(tmem + h * a.n_mma, desc_sw128(a_addr + ks * kSliceK * 2),
+                                   desc_sw32(smem_u32(ring_b + b * L.b_stage)), idesc, (g | ks) != 0);
+                            tc_commit(&ctl.b_empty[b]);
+                            ++bseq;
+                        }
+                    if (ok) tc_commit(&ctl.a_empty[slot]);
+                }
+                if (ok) {
+                    tc_commit(&ctl.acc_full);
+                    ++n_item;
+                }
+            }
+            if (!ok) {  // the products in flight finish before the tensor memory is freed
+                tc_commit(&ctl.drain);
+                if (!mbar_wait(&ctl.drain, 0, wait_limit)) raise_status(status, AFX_DEV_UNDRAINED);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---- accumulator -> Y
+        const uint32_t quarter = static_cast<uint32_t>(warp) & 3u;
+        uint32_t n_item = 0;
+        for (uint32_t it = it0; it < it1; ++it) {
+            const uint32_t item = a.items[it];
+            const uint32_t mi = item >> 28, pass = (item >> 18) & 0x3FFu, mt = item & 0x3FFFFu;
+            const PrefillMatrix& pm = a.m[mi];
+            if (!__all_sync(0xFFFFFFFFu, pf_wait(&ctl.acc_full, n_item & 1u, wait_limit, ctl, status))) break;
+            tc_fence_after();
+            const uint32_t y0 = pass * a.pass_tokens;
+            const uint32_t valid = min(a.pass_tokens, a.n_tokens - y0);
+            const uint64_t rows = pm.t.rows;
+            float* y = pm.t.y + static_cast<uint64_t>(y0) * rows + static_cast<uint64_t>(mt) * kTileRows + quarter * 32 + lane;
+            for (uint32_t c0 = 0; c0 < valid; c0 += 16) {
+                uint32_t v[16];
+                tc_ld16(tmem + ((quarter * 32u) << 16) + c0, v);
+#pragma unroll
+                for (uint32_t j = 0; j < 16; ++j)
+                    if (c0 + j < valid) y[static_cast<uint64_t>(c0 + j) * rows] = __uint_as_float(v[j]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl.acc_empty);
+            ++n_item;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kPfMmaWarp) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(a.tmem_cols) : "memory");
+    }
+}
+
+}  // namespace afx
+
+// ---- host side --------------------------------------------------------------------------
+
+namespace afx {
+
+// Defined with the restore kernels (afx_decode.cu).
+void fill_tensor(const afx_desc& d, const void* container, TensorArgs& t);
+afx_status prepare_kernel(const void* func, int threads, size_t smem, int* blocks_per_sm);
+int sm_count();
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's cuTensorMapEncodeTiled, found through the runtime (the
+// library does not link the driver library itself).
+EncodeTiledFn encode_tiled() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// X [n_tokens][cols] BF16 in device memory, read as boxes of 16 columns x
+// n_mma tokens with the 32-byte swizzle the B descriptors name; rows past
+// n_tokens read as zeros.
+afx_status make_x_map(CUtensorMap* map, const uint16_t* x, uint32_t cols, uint32_t n_tokens, uint32_t n_mma) {
+    const EncodeTiledFn enc = encode_tiled();
+    if (!enc) return afx_fail(AFX_E_CUDA, "cuTensorMapEncodeTiled is not available from the driver", 0);
+    const cuuint64_t dims[2] = {cols, n_tokens};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {kSliceK, n_mma};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char msg[96];
+        snprintf(msg, sizeof msg, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+        return afx_fail(AFX_E_CUDA, msg, 0);
+    }
+    return AFX_OK;
+}
+
+bool device_memory(const void* p) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice;
+}
+
+uint32_t pow2_at_least(uint32_t v) {
+    uint32_t p = 32;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+// Tokens per MMA and halves per pass for n_tokens: one pass of up to 512
+// tokens (two halves past 256), N a multiple of 16; more tokens take passes
+// of 512.
+void token_split(uint32_t n_tokens, uint32_t* n_mma, uint32_t* halves) {
+    if (n_tokens <= kMaxHalfTokens) {
+        *halves = 1;
+        *n_mma = round_up(n_tokens, 16);
+    } else if (n_tokens <= kMaxPassTokens) {
+        *halves = 2;
+        *n_mma = round_up((n_tokens + 1) / 2, 16);
+    } else {
+        *halves = 2;
+        *n_mma = kMaxHalfTokens;
+    }
+}
+
+// One launch over items[0 .. n) (codes matrix << 28 | pass << 18 | m-tile):
+// each item to the least loaded CTA, largest first (an item costs its
+// k-tiles); each CTA takes its items in code order, so that consecutive
+// items share a matrix's decode tables.
+afx_status launch_items(PrefillArgs& pa, const std::vector<uint32_t>& codes, size_t begin, size_t end, size_t smem,
+                        cudaStream_t s) {
+    const int sms = sm_count();
+    if (sms <= 0) return afx_fail(AFX_E_CUDA, "cannot query the SM count", 0);
+    const size_t n = end - begin;
+    const uint32_t G = static_cast<uint32_t>(std::min<size_t>({n, static_cast<size_t>(sms), size_t(kPfMaxCtas)}));
+    std::vector<uint32_t> order(n);
+    for (size_t i = 0; i < n; ++i) order[i] = codes[begin + i];
+    std::stable_sort(order.begin(), order.end(), [&](uint32_t x, uint32_t y) {
+        return pa.m[x >> 28].k_tiles > pa.m[y >> 28].k_tiles;
+    });
+    using Load = std::pair<uint64_t, uint32_t>;
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+    for (uint32_t c = 0; c < G; ++c) heap.push({0, c});
+    std::vector<std::vector<uint32_t>> per(G);
+    for (uint32_t code : order) {
+        Load l = heap.top();
+        heap.pop();
+        per[l.second].push_back(code);
+        l.first += pa.m[code >> 28].k_tiles;
+        heap.push(l);
+    }
+    uint32_t k = 0;
+    for (uint32_t c = 0; c < G; ++c) {
+        std::sort(per[c].begin(), per[c].end());
+        pa.cta_begin[c] = static_cast<uint16_t>(k);
+        for (uint32_t code : per[c]) pa.items[k++] = code;
+    }
+    pa.cta_begin[G] = static_cast<uint16_t>(k);
+    prefill_fused_kernel<<<G, kPfThreads, smem, s>>>(pa);
+    AFX_CUDA_TRY(cudaGetLastError(), "prefill_fused_kernel launch");
+    return AFX_OK;
+}
+
+}  // namespace
+
+}  // namespace afx
+
+using namespace afx;
+
+extern "C" afx_status afx_tile_order(const uint16_t* w, uint32_t rows, uint32_t cols, uint16_t* out) {
+    if (!w || !out) return afx_fail(AFX_E_ARG, "null pointer", 0);
+    if (rows == 0 || cols == 0 || rows % kTileRows || cols % kTileCols)
+        return afx_fail(AFX_E_ARG, "rows must be a multiple of 128 and cols a multiple of 64", 0);
+    const uint64_t kt = cols / kTileCols;
+    for (uint64_t m = 0; m < rows / kTileRows; ++m)
+        for (uint64_t g = 0; g < kt; ++g) {
+            uint16_t* dst = out + (m * kt + g) * kTileElems;
+            const uint16_t* src = w + m * kTileRows * cols + g * kTileCols;
+            for (uint64_t r = 0; r < kTileRows; ++r)
+                std::memcpy(dst + r * kTileCols, src + r * cols, kTileCols * sizeof(uint16_t));
+        }
+    return AFX_OK;
+}
+
+extern "C" afx_status afx_prefill_fused_batch(const afx_desc* descs, const void* const* containers,
+                                              const uint32_t* rows, const uint32_t* cols, const uint16_t* const* xs,
+                                              uint32_t n_tokens, float* const* ys, uint32_t count,
+                                              afx_stream_t stream, int32_t* status) {
+    if (count == 0) return AFX_OK;
+    if (!descs || !containers || !rows || !cols || !xs || !ys) return afx_fail(AFX_E_ARG, "null array", 0);
+    if (n_tokens == 0) return afx_fail(AFX_E_ARG, "n_tokens must be at least 1", 0);
+    uint32_t n_mma = 0, halves = 0;
+    token_split(n_tokens, &n_mma, &halves);
+    const uint32_t pass_tokens = n_mma * halves;
+    const uint32_t passes = (n_tokens + pass_tokens - 1) / pass_tokens;
+    if (passes > 1024) return afx_fail(AFX_E_ARG, "n_tokens must be at most 524288", 0);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int dev = -1, optin = 0;
+    AFX_CUDA_TRY(cudaGetDevice(&dev), "cudaGetDevice");
+    AFX_CUDA_TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev), "cudaDeviceGetAttribute");
+    std::unique_ptr<PrefillArgs> pa(new PrefillArgs);
+    for (uint32_t i0 = 0; i0 < count; i0 += kMaxTensors) {
+        const uint32_t cnt = std::min<uint32_t>(count - i0, kMaxTensors);
+        std::memset(static_cast<void*>(pa.get()), 0, offsetof(PrefillArgs, cta_begin));
+        pa->count = cnt;
+        pa->n_tokens = n_tokens;
+        pa->n_mma = n_mma;
+        pa->halves = halves;
+        pa->pass_tokens = pass_tokens;
+        pa->tmem_cols = pow2_at_least(pass_tokens);
+        pa->status = status;
+        uint32_t max_T = 4;
+        std::vector<uint32_t> codes;
+        for (uint32_t k = 0; k < cnt; ++k) {
+            const uint32_t i = i0 + k;
+            const afx_desc& d = descs[i];
+            if (afx_check_desc(&d) != AFX_OK) return afx_fail(AFX_E_FORMAT, "invalid container description", 0);
+            if (d.format != AFX_FMT_BF16) return afx_fail(AFX_E_ARG, "the fused prefill product takes BF16 containers", 0);
+            if (rows[i] == 0 || cols[i] == 0 || rows[i] % kTileRows || cols[i] % kTileCols)
+                return afx_fail(AFX_E_ARG, "rows must be a multiple of 128 and cols a multiple of 64", 0);
+            if (static_cast<uint64_t>(rows[i]) * cols[i] != d.n) return afx_fail(AFX_E_ARG, "rows * cols != n", 0);
+            if (rows[i] / kTileRows > (1u << 18)) return afx_fail(AFX_E_ARG, "too many rows", 0);
+            if (d.nsym >= 2 && d.block_chunks != static_cast<uint32_t>(kThreads))
+                return afx_fail(AFX_E_FORMAT, "the decoder needs 512 chunks per block", 0);
+            if (!containers[i] || !ys[i] || !xs[i]) return afx_fail(AFX_E_ARG, "null pointer", 0);
+            if (reinterpret_cast<uintptr_t>(containers[i]) & 255u || reinterpret_cast<uintptr_t>(xs[i]) & 15u)
+                return afx_fail(AFX_E_ARG, "containers must be 256-byte and x 16-byte aligned", 0);
+            if (!device_memory(containers[i]) || !device_memory(xs[i]) || !device_memory(ys[i]))
+                return afx_fail(AFX_E_ARG, "containers, x and y must be in device memory", 0);
+            PrefillMatrix& pm = pa->m[k];
+            fill_tensor(d, containers[i], pm.t);
+            pm.t.y = ys[i];
+            pm.t.rows = rows[i];
+            pm.t.cols = cols[i];
+            pm.k_tiles = cols[i] / kTileCols;
+            pm.single = d.nsym == 1 ? 1u : 0u;
+            pm.fill = d.fill;
+            max_T = std::max(max_T, d.chunk_bytes);
+            const afx_status mst = make_x_map(&pa->tmap[k], xs[i], cols[i], n_tokens, n_mma);
+            if (mst != AFX_OK) return mst;
+            for (uint32_t p = 0; p < passes; ++p)
+                for (uint32_t mt = 0; mt < rows[i] / kTileRows; ++mt) codes.push_back(k << 28 | p << 18 | mt);
+        }
+        pa->max_chunk_bytes = max_T;
+        // decode tables: the state table where it fits beside the rings and
+        // the warps' buffers, else the 12-bit table
+        const PfLayout L0 = pf_layout(0, n_mma, max_T);
+        const int64_t budget = static_cast<int64_t>(optin) - 1024 - static_cast<int64_t>(L0.total) - 16;
+        if (budget < static_cast<int64_t>(kLutTabBytes)) return afx_fail(AFX_E_ARG, "launch needs too much shared memory", 0);
+        uint32_t tab_bytes = kLutTabBytes;
+        for (uint32_t k = 0; k < cnt; ++k) {
+            CodeTables& tab = pa->m[k].t.tab;
+            if (!tab.fsm) continue;
+            const int64_t need = static_cast<int64_t>(tab.n_states + kSkipRows) * kFsmRowBytes;
+            if (need > budget)
+                tab.fsm = 0;
+            else
+                tab_bytes = std::max<uint32_t>(tab_bytes, static_cast<uint32_t>(need));
+        }
+        pa->tab_bytes = tab_bytes;
+        const size_t smem = pf_layout(tab_bytes, n_mma, max_T).total + 1024;
+        int per_sm = 0;
+        const afx_status pst = prepare_kernel(reinterpret_cast<const void*>(prefill_fused_kernel), kPfThreads, smem, &per_sm);
+        if (pst != AFX_OK) return pst;
+        for (size_t b = 0; b < codes.size(); b += kPfMaxItems) {
+            const afx_status lst = launch_items(*pa, codes, b, std::min(codes.size(), b + kPfMaxItems), smem, s);
+            if (lst != AFX_OK) return lst;
+        }
+    }
+    return AFX_OK;
+}
+
+extern "C" afx_status afx_prefill_fused(const afx_desc* desc, const void* container, uint32_t rows, uint32_t cols,
+                                        const uint16_t* x, uint32_t n_tokens, float* y, afx_stream_t stream,
+                                        int32_t* status) {
+    if (!desc) return afx_fail(AFX_E_ARG, "null description", 0);
+    return afx_prefill_fused_batch(desc, &container, &rows, &cols, &x, n_tokens, &y, 1, stream, status);
+}
+
+// Bits of the bounds checks that fired in this module (bounds-checked
+// builds), read and cleared; afx_debug_bounds_report adds them to its own.
+extern "C" __attribute__((visibility("hidden"))) uint32_t afx_prefill_bounds_bits(void) {
+    unsigned int bits = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&bits, g_bounds_report, sizeof bits) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaMemcpyToSymbol(g_bounds_report, &zero, sizeof zero);
+    return bits;
+}
