@@ -969,10 +969,24 @@ def run_prefill_bench(afx, parts, dev_blob, offs, dev, args):
         restore_one_launch_ms = timed(lambda: afx.afx_decode_batch(descs, conts, whole_views, stream=gs), gs)
     out["restore_ms_per_matrix_launches"] = restore_ms
     out["restore_ms_one_launch"] = restore_one_launch_ms
+    # the same matrices in tile order for the fused product (encoded on the host)
+    shape_of = {name: shapes[name] for name, _, _ in mats}
+    w_of = {name: w for name, w, _, _ in parts}
+
+    def tiled(name):
+        r, cl = shape_of[name]
+        return afx.encode(afx.afx_tile_order(w_of[name], r, cl))
+
+    with cf.ThreadPoolExecutor(len(mats)) as ex:
+        tiled_parts = list(ex.map(tiled, [name for name, _, _ in mats]))
+    tdescs = [d for _, d in tiled_parts]
+    tconts = [torch.from_numpy(c).to(dev) for c, _ in tiled_parts]
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
     for n_tok in (1, 4, 128, 512, 2048):
         reps = 20 if n_tok <= 4 else 5
         xs = [torch.from_numpy(synth.activations(n_tok, cl, seed=21).view(np.int16)).to(dev) for _, cl in mshapes]
         ys = [torch.empty((n_tok, r), dtype=torch.float32, device=dev) for r, _ in mshapes]
+        yf = [torch.empty((n_tok, r), dtype=torch.float32, device=dev) for r, _ in mshapes]
 
         def sequential():
             for i, (d, c) in enumerate(zip(descs, conts)):
@@ -985,9 +999,30 @@ def run_prefill_bench(afx, parts, dev_blob, offs, dev, args):
         def one_launch():
             afx.afx_prefill_batch(descs, conts, mshapes, xs, ys, [whole, None], ws, gemm_stream=gs)
 
+        def fused():
+            afx.afx_prefill_fused_batch(tdescs, tconts, mshapes, xs, yf, stream=gs, status_dev=status)
+
         seq_ms = timed(sequential, gs, reps)
         ovl_ms = timed(overlapped, gs, reps)
         one_ms = timed(one_launch, gs, reps)
+        fused_ms = timed(fused, gs, reps)
+        # the fused products against the unfused ones (cuBLAS over the
+        # restored weights), per output within 2 x 2e-3 * sum|w x| (each side
+        # is within 2e-3 of the exact sum); the bound from a float32 product
+        # of the absolute values
+        with torch.cuda.stream(gs):
+            one_launch()
+            fused()
+        torch.cuda.synchronize()
+        agree, worst = status.item() == 0, 0.0
+        for i, (r, cl) in enumerate(mshapes):
+            wv = whole_views[i]
+            wabs = (wv.view(torch.bfloat16).float().abs()).view(r, cl)
+            bound = xs[i].view(torch.bfloat16).float().abs() @ wabs.t()
+            err = (yf[i] - ys[i]).abs()
+            worst = max(worst, float((err / bound.clamp_min(1e-30)).max()))
+            agree = agree and bool((err <= 4e-3 * bound + 1e-30).all())
+            del wabs, bound, err
         gemm_ms = max(seq_ms - restore_ms, 1e-9)
         best = min(seq_ms, ovl_ms, one_ms)
         flop = 2.0 * n_w * n_tok
@@ -996,11 +1031,19 @@ def run_prefill_bench(afx, parts, dev_blob, offs, dev, args):
                             "tokens_per_s": n_tok / (best * 1e-3), "tflops": flop / (best * 1e-3) / 1e12,
                             "gemm_tflops": flop / (gemm_ms * 1e-3) / 1e12,
                             "gemm_frac_of_bf16_peak": flop / (gemm_ms * 1e-3) / 1e12 / peak,
-                            "best_over_sum_of_parts": best / (restore_one_launch_ms + gemm_ms)})
+                            "best_over_sum_of_parts": best / (restore_one_launch_ms + gemm_ms),
+                            "fused_ms": fused_ms, "fused_tokens_per_s": n_tok / (fused_ms * 1e-3),
+                            "fused_tflops": flop / (fused_ms * 1e-3) / 1e12,
+                            "fused_weights_per_s": n_w * ((n_tok + 511) // 512) / (fused_ms * 1e-3),
+                            "unfused_best_over_fused": best / fused_ms,
+                            "fused_agrees_with_unfused": agree, "fused_worst_err_over_sum_abs": worst})
     out["path"] = ("afx_prefill / afx_prefill_batch: restore_store_kernel into scratch, cuBLAS BF16 GEMM with "
                    "float32 accumulation; sequential: restore then product per matrix on one stream; overlapped: "
                    "restore of matrix i+1 on a second stream; one restore launch: all seven restored by one "
-                   "afx_decode_batch launch, then the products; tokens_per_s and tflops from the fastest")
+                   "afx_decode_batch launch, then the products; tokens_per_s and tflops from the fastest of "
+                   "those; fused: afx_prefill_fused_batch over the tile-ordered containers (prefill_fused_kernel, "
+                   "tcgen05 products from the restored tiles in shared memory, no scratch; the weights are "
+                   "restored once per 512 tokens, counted in fused_weights_per_s)")
     return out
 
 

@@ -69,8 +69,8 @@ typedef enum afx_status {
 #define AFX_DEV_BAD_CODE 0x4  /* a bit pattern that is no codeword */
 #define AFX_DEV_BAD_SHAPE 0x8 /* GEMV rows x cols disagree with the block index */
 #define AFX_DEV_TIMEOUT 0x10  /* a staging copy did not arrive within the kernel's wait limit; work skipped */
-#define AFX_DEV_UNDRAINED 0x20 /* after a timeout, a staging copy still had not arrived when the warp stopped:
-                                  the copy may land in shared memory after the kernel's work on it ended */
+#define AFX_DEV_UNDRAINED 0x20 /* with AFX_DEV_TIMEOUT: a copy into shared memory had not arrived when the
+                                  warp gave up on it, and may land after the kernel's work on it ended */
 
 /* Element formats a container can hold (header field at byte 108; the hi
  * section's offset is the u64 at byte 112, 0 unless FP16).  The
@@ -342,9 +342,9 @@ afx_status afx_sync(afx_stream_t stream, uint32_t timeout_ms, const int32_t* sta
  * the kernel ORs AFX_DEV_TIMEOUT into *status_dev (required) and returns
  * without touching out_dev.  No copy was issued, so nothing is left in
  * flight and the context stays usable.  The production entry points wait
- * up to 2^22 polls; when one of their waits runs out, the warp waits for
- * its issued copies once more (bounded) and ORs AFX_DEV_UNDRAINED as well
- * if they still have not arrived.
+ * up to 2^22 polls; when one of their waits runs out, the warp waits
+ * (bounded) for the copy it issued into its other buffer and ORs
+ * AFX_DEV_UNDRAINED as well: the copy whose wait ran out may still land.
  * No counterpart on the pages: this exists to test the library's own
  * bounded waits.
  * Errors: AFX_E_ARG, AFX_E_FORMAT, AFX_E_CUDA. */

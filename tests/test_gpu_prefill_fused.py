@@ -125,14 +125,16 @@ def test_fused_prefill_batch_mixed_matrices(afx):
             assert ok, worst
 
 
-def test_fused_prefill_long_codes_use_the_12_bit_table(afx):
-    # a heavy-tailed matrix whose code tree is too large for the state table
+@pytest.mark.parametrize("n_exponents", [40, 60])
+def test_fused_prefill_large_code_trees_use_the_12_bit_table(afx, n_exponents):
+    # code trees with more internal nodes than the fused kernel's state table
+    # holds (40 exponents: the restore kernel's state table would hold it; 60:
+    # past every state table)
     rows, cols, n_tokens = 256, 4096, 64
-    W = synth.adversarial(rows * cols, seed=3).reshape(rows, cols)
-    W = np.where(((W >> 7) & 0xFF) == 0xFF, np.uint16(0x3C00), W)  # no infinities or NaNs in a product
+    W = synth.exponent_mix(rows * cols, n_exponents, seed=n_exponents).reshape(rows, cols)
     X = synth.activations(n_tokens, cols, seed=4)
     c, d = _tiled(afx, W)
-    assert d.nsym > 40
+    assert d.nsym == n_exponents
     ok, worst = _within(_run(afx, W, X), W, X)
     assert ok, worst
 

@@ -234,22 +234,31 @@ __device__ __forceinline__ uint32_t tile_offset(uint32_t i) {
 }
 
 // Writes tile weights [i0, i1) into the A slot at `tile`: the stage byte
-// of tile weight i is stage[i + d] and its sign|mantissa byte sm[i] (sm
-// points at the tile's first weight).  Groups of 8 whole weights go out as
-// 16-byte stores, one group per lane at a time; the partial groups at
-// either end (shared with neighbouring ranges) weight by weight.
+// of tile weight i is stage[(i + d) mod 2^32] (d is the tile's first
+// position minus the stage's, which may be negative) and its sign|mantissa
+// byte sm[i] (sm points at the tile's first weight).  Groups of 8 whole
+// weights go out as 16-byte stores, one group per lane at a time; the
+// partial groups at either end (shared with neighbouring ranges) weight by
+// weight.
 __device__ __forceinline__ void tile_write(uint8_t* tile, const uint8_t* stage, uint32_t d, const uint8_t* sm,
                                            uint32_t i0, uint32_t i1, int lane) {
     const uint32_t f0 = (i0 + 7) & ~7u, f1 = i1 & ~7u;
     const uint32_t head_end = f0 < i1 ? f0 : i1;
-    for (uint32_t i = i0 + lane; i < head_end; i += 32)
-        *reinterpret_cast<uint16_t*>(tile + tile_offset(i)) = join1(stage[i + d], __ldg(sm + i));
+    for (uint32_t i = i0 + lane; i < head_end; i += 32) {
+        const uint32_t k = i + d;  // stage index, wrapped to 32 bits
+        AFX_CHECK(k < static_cast<uint32_t>(kWarpStage) && i < kTileElems, kChkMergeStage);
+        *reinterpret_cast<uint16_t*>(tile + tile_offset(i)) = join1(stage[k], __ldg(sm + i));
+    }
     const uint32_t tail0 = f1 > f0 ? f1 : f0;
-    for (uint32_t i = tail0 + lane; i < i1; i += 32)
-        *reinterpret_cast<uint16_t*>(tile + tile_offset(i)) = join1(stage[i + d], __ldg(sm + i));
+    for (uint32_t i = tail0 + lane; i < i1; i += 32) {
+        const uint32_t k = i + d;
+        AFX_CHECK(k < static_cast<uint32_t>(kWarpStage) && i < kTileElems, kChkMergeStage);
+        *reinterpret_cast<uint16_t*>(tile + tile_offset(i)) = join1(stage[k], __ldg(sm + i));
+    }
     for (uint32_t g = (f0 >> 3) + lane; g < (f1 >> 3); g += 32) {
-        const uint32_t i = g << 3;
-        const uint4 w = join8(*reinterpret_cast<const uint2*>(stage + i + d), __ldg(reinterpret_cast<const uint2*>(sm + i)));
+        const uint32_t i = g << 3, k = i + d;
+        AFX_CHECK(k + 8 <= static_cast<uint32_t>(kWarpStage) && i + 8 <= kTileElems, kChkMergeStage);
+        const uint4 w = join8(*reinterpret_cast<const uint2*>(stage + k), __ldg(reinterpret_cast<const uint2*>(sm + i)));
         *reinterpret_cast<uint4*>(tile + tile_offset(i)) = w;
     }
 }
