@@ -73,7 +73,7 @@ def parse_args(argv=None):
                         "4 the 2^28 adversarial tensor, 5 the layer with the 40-layer streaming leg")
     p.add_argument("--legs", default="all",
                    help="extra legs to run after the headline (comma list of e2e, zero_copy, cpu_baseline, configs, "
-                        "gemv, stream, prefill, formats, encode; default all)")
+                        "gemv, stream, prefill, formats, encode, wide_trees; default all)")
     p.add_argument("--workload", default="model",
                    help="model (default: the whole Qwen3-14B-shaped model, 14.77 B weights resident), layer (one "
                         "Qwen3-14B-shaped decoder layer), matrix4096, normal:<k> (one "
@@ -705,7 +705,7 @@ def run_ours(args):
     }
 
     legs = set(args.legs.split(",")) if args.legs != "all" else {
-        "e2e", "zero_copy", "cpu_baseline", "gemv", "stream", "prefill", "formats", "encode", "configs"}
+        "e2e", "zero_copy", "cpu_baseline", "gemv", "stream", "prefill", "formats", "encode", "configs", "wide_trees"}
     if not args.no_extras and "e2e" in legs:
         # every rank runs the end-to-end leg on its own GPU and host link; the
         # job's figure is all ranks' bytes over the slowest rank's time
@@ -778,6 +778,8 @@ def run_ours(args):
             line["fused_gemv"]["vs_restore_then_gemm"] = fused_vs_unfused(line["fused_gemv"], line["prefill"])
         if "formats" in legs:
             line["formats"] = run_formats_bench(afx, dev, args)
+        if "wide_trees" in legs:
+            line["wide_trees"] = run_wide_trees_bench(afx, dev, args, layer_value * 1e9 / 2 if layer_value else None)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -1133,6 +1135,31 @@ def run_formats_bench(afx, dev, args):
         }
     out["path"] = ("afx_decode_batch of the whole set per step: restore_store_fp16_kernel (raw bytes plus the hi "
                    "section) and restore_store_e4m3_kernel (raw nibbles, byte outputs)")
+    return out
+
+
+WIDE_TREES = ((57, 0.85), (58, 0.85), (80, 0.9), (100, 0.92))
+
+
+def run_wide_trees_bench(afx, dev, args, layer_weights_per_s=None):
+    """Restore rate against the size of the code tree: one 2^27-weight tensor
+    per exponent count (57 exponents: 56 internal nodes, the largest
+    byte-step state table; 58 and more: the 12-bit multi-code table), each
+    restored by one launch, bit-exact checked, then timed."""
+    from weight_streaming_canonical_gb300 import synth
+    out = {"weights": 1 << 27, "runs": []}
+    for n_exp, ratio in WIDE_TREES:
+        w = synth.exponent_mix(1 << 27, n_exp, ratio=ratio, seed=n_exp)
+        c, d = afx.encode(w)
+        r, st = measure_restore(afx, [(f"mix{n_exp}", w, c, d)], dev, args, f"mix:{n_exp}")
+        del st
+        wps = r["n"] / (r["ms"] * 1e-3)
+        out["runs"].append({"exponents": n_exp, "internal_nodes": n_exp - 1, "ms": r["ms"], "weights_per_s": wps,
+                            "hbm_frac": r["roofline"]["frac"], "bit_exact": r["bit_exact"],
+                            "coded_bits_per_weight": d.total_bits / d.n,
+                            "decoder": "byte-step state table" if n_exp - 1 <= 56 else "12-bit multi-code table",
+                            "frac_of_layer_rate": wps / layer_weights_per_s if layer_weights_per_s else None})
+    out["path"] = "afx_decode_batch of one tensor per step (restore_store_kernel), exponent mixes of synth.exponent_mix"
     return out
 
 

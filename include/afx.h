@@ -414,15 +414,15 @@ afx_status afx_prefill_batch(const afx_desc* descs, const void* const* container
  * fewer bytes to read, more work to unpack" (the released bits are restored
  * before computation; t_unpack of Eq. (1)).
  *
- * The product reads the weights in tile order: the [rows][cols] matrix cut
- * into 128 x 64 tiles, each tile row-major, the tiles of a 128-row band in
- * column order, the bands in row order; element (r, c) at position
- * ((r / 128) * (cols / 64) + c / 64) * 8192 + (r % 128) * 64 + c % 64.
+ * The product reads the weights in slice order: the [rows][cols] matrix
+ * cut into 128 x 16 slices, each slice row-major, the slices of a 128-row
+ * band in column order, the bands in row order; element (r, c) at position
+ * ((r / 128) * (cols / 16) + c / 16) * 2048 + (r % 128) * 16 + c % 16.
  * afx_tile_order writes that order; encode its output with afx_encode as
  * usual (the container format is unchanged, only the element order). */
 
-/* out_host[tile order] = w_host[rows][cols] (row-major BF16 patterns, host
- * memory, rows a multiple of 128 and cols a multiple of 64; out_host holds
+/* out_host[slice order] = w_host[rows][cols] (row-major BF16 patterns, host
+ * memory, rows a multiple of 128 and cols a multiple of 16; out_host holds
  * rows * cols elements and must not overlap w_host).  Errors: AFX_E_ARG. */
 afx_status afx_tile_order(const uint16_t* w_host, uint32_t rows, uint32_t cols, uint16_t* out_host);
 
@@ -431,7 +431,7 @@ afx_status afx_tile_order(const uint16_t* w_host, uint32_t rows, uint32_t cols, 
  * [n_tokens][cols], row-major, 16-byte aligned; y_dev: float32
  * [n_tokens][rows], overwritten.  Products of BF16 pairs are exact and are
  * summed in float32 by the tensor cores.  rows a multiple of 128, cols a
- * multiple of 64, n_tokens >= 1 (up to 512 per pass over the weights; more
+ * multiple of 16, n_tokens >= 1 (up to 512 per pass over the weights; more
  * tokens restore the weights once per 512).  The container, x_dev and
  * y_dev in device memory (container 256-byte aligned).  Asynchronous on
  * stream; device-detected corruption or a wait past its limit sets
@@ -445,7 +445,7 @@ afx_status afx_prefill_fused(const afx_desc* desc, const void* container_dev, ui
 
 /* afx_prefill_fused over count matrices in one launch (per 16 matrices),
  * all with the same n_tokens: ys_dev[i] = W_i xs_dev[i] with W_i the
- * tile-ordered weights of containers_dev[i], [rows[i]][cols[i]].  Same
+ * slice-ordered weights of containers_dev[i], [rows[i]][cols[i]].  Same
  * rules and errors as afx_prefill_fused, per matrix. */
 afx_status afx_prefill_fused_batch(const afx_desc* descs, const void* const* containers_dev, const uint32_t* rows,
                                    const uint32_t* cols, const uint16_t* const* xs_dev, uint32_t n_tokens,

@@ -48,10 +48,11 @@ def test_byte_steps_with_32_byte_chunks(afx):
     assert d.chunk_bytes == 32 and min(l for l in d.len if l) == 4
 
 
-@pytest.mark.parametrize("nsym", [57, 58])
-def test_largest_state_table_and_the_first_tree_past_it(afx, nsym):
-    # 57 exponents: 56 internal nodes, the largest state table; 58: the 12-bit table
-    c, d = _check(afx, synth.exponent_mix(3_000_017, nsym, ratio=0.85, seed=nsym), out_pad=16)
+@pytest.mark.parametrize("nsym,ratio", [(57, 0.85), (58, 0.85), (80, 0.9), (120, 0.94)])
+def test_largest_state_table_and_the_trees_past_it(afx, nsym, ratio):
+    # 57 exponents: 56 internal nodes, the largest state table; 58, 80 and
+    # 120: the 12-bit table
+    c, d = _check(afx, synth.exponent_mix(3_000_017, nsym, ratio=ratio, seed=nsym), out_pad=16)
     assert d.nsym == nsym and min(l for l in d.len if l) >= 2
 
 

@@ -35,7 +35,7 @@ def _run(afx, W, X, status=None):
     return y.cpu().numpy()
 
 
-@pytest.mark.parametrize("shape", [(128, 64), (256, 640), (384, 5120), (1024, 640)])
+@pytest.mark.parametrize("shape", [(128, 16), (128, 64), (256, 640), (384, 5120), (1024, 48)])
 @pytest.mark.parametrize("n_tokens", [1, 17, 128, 300, 512])
 def test_fused_prefill_matches_the_oracle(afx, shape, n_tokens):
     import torch
@@ -149,7 +149,10 @@ def test_fused_prefill_refuses_bad_arguments(afx):
     with pytest.raises(afx.AfxError):  # rows not a multiple of 128
         afx.afx_prefill_fused(d, dev, 64, 128, torch.zeros((4, 128), dtype=torch.int16, device="cuda"),
                               torch.zeros((4, 64), dtype=torch.float32, device="cuda"))
-    with pytest.raises(afx.AfxError):  # x in host memory
+    with pytest.raises(afx.AfxError):  # cols not a multiple of 16
+        afx.afx_prefill_fused(d, dev, 1024, 8, torch.zeros((4, 8), dtype=torch.int16, device="cuda"),
+                              torch.zeros((4, 1024), dtype=torch.float32, device="cuda"))
+    with pytest.raises((afx.AfxError, ValueError)):  # x in host memory
         afx.afx_prefill_fused(d, dev, 128, 64, torch.zeros((4, 64), dtype=torch.int16), y)
     c2, d2 = afx.encode(synth.normal_fp16(128 * 64, seed=2), fmt=afx.AFX_FMT_FP16)
     with pytest.raises(afx.AfxError):  # FP16 elements

@@ -12,23 +12,27 @@
 // weights go from the decoder straight into the tensor cores' shared-memory
 // operand tiles and never reach global memory.
 //
-// Weight order.  The container holds W in tile order: 128 x 64 tiles of
-// W, row-major inside a tile, the 64-column tiles of one 128-row band (an
-// "m-tile") consecutive, the bands in order (afx_tile_order writes it).  A
-// band's weights are then one contiguous range of the stream, in the order
-// in which the product consumes its k-tiles.
+// Weight order.  The container holds W in slice order: 128 x 16 slices of
+// W, row-major inside a slice, the slices of one 128-row band (an "m-tile")
+// in column order, the bands in row order (afx_tile_order writes it).  A
+// band's weights are then one contiguous range of the stream, and each
+// 2048-weight slice is the A operand of one MMA (K = 16).
 //
 // Work decomposition.  A work item is one m-tile of one matrix for one pass
 // of up to 512 tokens; the host assigns items to persistent CTAs (longest
 // first, each to the least loaded CTA), one CTA per SM.  Inside a CTA:
 //   - 16 decoding warps restore the item's sub-tiles (32 chunks each,
 //     interleaved across the warps) with the byte-step decoder of the
-//     restore kernel and write each weight into a ring of four 16 KB A
-//     tiles (128 x 64 BF16, K-major, 128-byte swizzle).  A tile is full once
-//     its 8192 weights have been counted in; the warp that completes it
-//     signals the tile's barrier.
+//     restore kernel and write each weight into a ring of sixteen 4 KB A
+//     slices (128 x 16 BF16, K-major, 32-byte swizzle).  A slice is full once
+//     its 2048 weights have been counted in; the warp that completes it
+//     signals the slice's barrier.  Each warp publishes its sub-tile's code
+//     count in shared memory as soon as its scan has it; the next warps add
+//     those counts to place their own sub-tiles, so no warp reads the chunk
+//     index of other sub-tiles from global memory;
 //   - a producer warp loads the token vectors with TMA: 16 columns x up to
-//     256 tokens per stage (32-byte swizzle), a ring of four stages;
+//     256 tokens per stage (32-byte swizzle), a 32 KB ring of 4 to 64
+//     stages (more, smaller ones for fewer tokens);
 //   - an MMA warp issues tcgen05.mma (M = 128, N = tokens of one half, K =
 //     16) from the two rings into a float32 accumulator in tensor memory (up
 //     to 2 x 256 columns) and returns ring slots with tcgen05.commit;
@@ -59,10 +63,13 @@ constexpr int kPfEpiWarp0 = kPfDecodeWarps + 2;
 constexpr int kPfWarps = kPfDecodeWarps + 6;
 constexpr int kPfThreads = kPfWarps * 32;
 constexpr uint32_t kDecodeBarrier = 1;  // named barrier of the decoding warps
-constexpr uint32_t kTileRows = 128, kTileCols = 64, kTileElems = kTileRows * kTileCols;
+constexpr uint32_t kSliceK = 16;             // K of one MMA, of one A slice and of one activation stage
+constexpr uint32_t kTileRows = 128, kTileCols = kSliceK, kTileElems = kTileRows * kTileCols;  // an A slice
 constexpr uint32_t kTileBytes = kTileElems * 2;
-constexpr uint32_t kSliceK = 16;             // K of one MMA and of one activation stage
-constexpr uint32_t kASlots = 4, kBSlots = 4;
+constexpr uint32_t kASlots = 16;
+constexpr uint32_t kBRingBytes = 32768;      // the activation ring: as many stages as fit, at most kBSlotsMax
+constexpr uint32_t kBSlotsMax = 64;
+constexpr uint32_t kTotRing = 128;           // published sub-tile code counts
 constexpr uint32_t kMaxHalfTokens = 256;     // N of one MMA
 constexpr uint32_t kMaxPassTokens = 2 * kMaxHalfTokens;
 constexpr int kPfMaxItems = 2048;
@@ -74,7 +81,7 @@ static_assert(((kPfEpiWarp0 + 0) % 4) != ((kPfEpiWarp0 + 1) % 4) && ((kPfEpiWarp
 
 struct PrefillMatrix {
     TensorArgs t;       // sections, geometry and code tables; t.y = Y [n_tokens][rows]
-    uint32_t k_tiles;   // cols / 64
+    uint32_t k_tiles;   // A slices per m-tile: cols / 16
     uint32_t single;    // 1: one exponent for every weight (no coded stream)
     uint32_t fill;      // that exponent
 };
@@ -92,16 +99,17 @@ struct PrefillArgs {
 // Control block in shared memory.
 struct PfCtl {
     uint64_t a_full[kASlots], a_empty[kASlots];
-    uint64_t b_full[kBSlots], b_empty[kBSlots];
+    uint64_t b_full[kBSlotsMax], b_empty[kBSlotsMax];
     uint64_t acc_full, acc_empty, drain;
-    uint32_t a_count[kASlots];  // weights counted into each A slot's current tile
+    uint64_t totals[kTotRing];  // (ordinal + 1) << 32 | code count of a sub-tile, at ordinal % kTotRing
+    uint32_t a_count[kASlots];  // weights counted into each A slot's current slice
     uint32_t tmem_base;
     int32_t abort_flag;
 };
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
 struct PfLayout {
-    uint32_t a, b, b_stage, ctl, shw, slots, streams, wstride, total;
+    uint32_t a, b, b_stage, b_slots, ctl, shw, slots, streams, wstride, total;
 };
 
 __host__ __device__ inline uint32_t round_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
@@ -109,9 +117,14 @@ __host__ __device__ inline uint32_t round_up(uint32_t v, uint32_t a) { return (v
 __host__ __device__ inline PfLayout pf_layout(uint32_t tab_bytes, uint32_t n_mma, uint32_t max_chunk_bytes) {
     PfLayout L;
     L.a = 0;
-    L.b_stage = round_up(n_mma * kSliceK * 2, 1024);
+    // a stage holds 16 columns of the tokens of one half; small stages come
+    // many to the ring, so that the loads run as many columns ahead of the
+    // products at any token count (the ring's depth, not a load's size,
+    // covers the load latency)
+    L.b_stage = round_up(n_mma * kSliceK * 2, 256);
+    L.b_slots = kBRingBytes / L.b_stage < kBSlotsMax ? kBRingBytes / L.b_stage : kBSlotsMax;
     L.b = L.a + kASlots * kTileBytes;
-    L.ctl = L.b + kBSlots * L.b_stage;
+    L.ctl = L.b + L.b_slots * L.b_stage;
     L.shw = round_up(L.ctl + static_cast<uint32_t>(sizeof(PfCtl)), 16);
     L.slots = round_up(L.shw + static_cast<uint32_t>(sharedw_table_offset()) + tab_bytes, 16);
     L.streams = L.slots + kPfDecodeWarps * static_cast<uint32_t>(sizeof(WarpSlot));
@@ -169,17 +182,12 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
 
-// Shared-memory matrix descriptors, K-major.  A: 128-byte rows, 128-byte
-// swizzle, 8-row groups 1024 bytes apart.  B: 32-byte rows, 32-byte
-// swizzle, 8-row groups 256 bytes apart.  Fields: start address >> 4
-// (bits 0-13), leading byte offset >> 4 (16-29, unused for swizzled
-// K-major), stride byte offset >> 4 (32-45), descriptor version 1 (46),
-// layout (61-63: 2 = 128-byte swizzle, 6 = 32-byte swizzle).
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
-    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (uint64_t{1} << 16) | (uint64_t{1024 >> 4} << 32) |
-           (uint64_t{1} << 46) | (uint64_t{2} << 61);
-}
-
+// Shared-memory matrix descriptor, K-major, 32-byte rows with the 32-byte
+// swizzle, 8-row groups 256 bytes apart (both operands: the A slices the
+// decoder writes and the activation stages the TMA writes).  Fields: start
+// address >> 4 (bits 0-13), leading byte offset >> 4 (16-29, unused for
+// swizzled K-major), stride byte offset >> 4 (32-45), descriptor version 1
+// (46), layout 6 = 32-byte swizzle (61-63).
 __device__ __forceinline__ uint64_t desc_sw32(uint32_t saddr) {
     return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (uint64_t{1} << 16) | (uint64_t{256 >> 4} << 32) |
            (uint64_t{1} << 46) | (uint64_t{6} << 61);
@@ -225,21 +233,22 @@ __device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, uint32_t
 
 // ---- the decoding warps: restored weights into the A ring -------------------------------
 
-// Byte offset of tile weight i (row i / 64, column i % 64) in a 128-byte
-// swizzled K-major tile: row r at r * 128, its 16-byte chunk c at
-// (c ^ (r & 7)) * 16.
+// Byte offset of slice weight i (row i / 16, column i % 16) in a 32-byte
+// swizzled K-major slice: row r at r * 32, its 16-byte chunk c at
+// (c ^ ((r >> 2) & 1)) * 16 -- the layout the TMA writes for the
+// activations and the B descriptors name.
 __device__ __forceinline__ uint32_t tile_offset(uint32_t i) {
-    const uint32_t r = i >> 6, c = i & 63u;
-    return (r << 7) | ((((c >> 3) ^ r) & 7u) << 4) | ((c & 7u) << 1);
+    const uint32_t r = i >> 4, c = i & 15u;
+    return (r << 5) | ((((c >> 3) ^ (r >> 2)) & 1u) << 4) | ((c & 7u) << 1);
 }
 
-// Writes tile weights [i0, i1) into the A slot at `tile`: the stage byte
-// of tile weight i is stage[(i + d) mod 2^32] (d is the tile's first
-// position minus the stage's, which may be negative) and its sign|mantissa
-// byte sm[i] (sm points at the tile's first weight).  Groups of 8 whole
-// weights go out as 16-byte stores, one group per lane at a time; the
-// partial groups at either end (shared with neighbouring ranges) weight by
-// weight.
+// Writes slice weights [i0, i1) into the A slot at `tile`: the stage byte
+// of slice weight i is stage[(i + d) mod 2^32] (d is the slice's first
+// position minus the stage's, which may be negative, and need not be a
+// multiple of 8) and its sign|mantissa byte sm[i] (sm points at the slice's
+// first weight).  Groups of 8 whole weights go out as 16-byte stores, one
+// group per lane at a time; the partial groups at either end (shared with
+// neighbouring ranges) weight by weight.
 __device__ __forceinline__ void tile_write(uint8_t* tile, const uint8_t* stage, uint32_t d, const uint8_t* sm,
                                            uint32_t i0, uint32_t i1, int lane) {
     const uint32_t f0 = (i0 + 7) & ~7u, f1 = i1 & ~7u;
@@ -255,11 +264,16 @@ __device__ __forceinline__ void tile_write(uint8_t* tile, const uint8_t* stage, 
         AFX_CHECK(k < static_cast<uint32_t>(kWarpStage) && i < kTileElems, kChkMergeStage);
         *reinterpret_cast<uint16_t*>(tile + tile_offset(i)) = join1(stage[k], __ldg(sm + i));
     }
+    // the stage bytes of a group start at any byte: three aligned words,
+    // shifted into place
+    const uint32_t sh = (d & 3u) * 8u;  // i is a multiple of 8, so k & 3 == d & 3
     for (uint32_t g = (f0 >> 3) + lane; g < (f1 >> 3); g += 32) {
         const uint32_t i = g << 3, k = i + d;
         AFX_CHECK(k + 8 <= static_cast<uint32_t>(kWarpStage) && i + 8 <= kTileElems, kChkMergeStage);
-        const uint4 w = join8(*reinterpret_cast<const uint2*>(stage + k), __ldg(reinterpret_cast<const uint2*>(sm + i)));
-        *reinterpret_cast<uint4*>(tile + tile_offset(i)) = w;
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(stage + (k & ~3u));
+        const uint32_t w0 = w[0], w1 = w[1], w2 = (k & 3u) ? w[2] : 0u;
+        const uint2 r8 = make_uint2(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh));
+        *reinterpret_cast<uint4*>(tile + tile_offset(i)) = join8(r8, __ldg(reinterpret_cast<const uint2*>(sm + i)));
     }
 }
 
@@ -298,9 +312,9 @@ __device__ __forceinline__ bool ring_write(uint8_t* ring_a, PfCtl& ctl, const ui
 
 // The sub-tile holding the code of output position p: the last block whose
 // index entry is <= p (a 32-way search, one load per lane and step), then
-// the last of its 16 sub-tiles whose first code is at or before p.  Also
-// returns that sub-tile's first output position.
-__device__ __forceinline__ uint64_t find_sub_tile(const TensorArgs& t, uint64_t p, int lane) {
+// the last of its 16 sub-tiles whose first code is at or before p; *start
+// gets that sub-tile's first output position.
+__device__ __forceinline__ uint64_t find_sub_tile(const TensorArgs& t, uint64_t p, int lane, uint64_t* start) {
     uint64_t lo = 0, hi = t.n_blocks;  // the block is in [lo, hi)
     while (hi - lo > 1) {
         const uint64_t step = (hi - lo + 31) / 32;
@@ -325,32 +339,60 @@ __device__ __forceinline__ uint64_t find_sub_tile(const TensorArgs& t, uint64_t 
         if (lane >= d) inc += o;
     }
     // sub-tile k starts after lanes 0 .. 2k-1: lane 2k's exclusive prefix
-    const uint64_t base = __ldg(t.block_index + b);
-    const uint64_t start_k = base + (inc - sum);
+    const uint64_t start_k = __ldg(t.block_index + b) + (inc - sum);
     const uint64_t n_sub = (t.n_chunks + kWarpChunks - 1) / kWarpChunks;
     const bool cand = (lane & 1) == 0 && start_k <= p && b * kSubtilesPerBlock + (lane >> 1) < n_sub;
     const uint32_t m = __ballot_sync(0xFFFFFFFFu, cand);
     const int top = m ? 31 - __clz(static_cast<int>(m)) : 0;
+    *start = __shfl_sync(0xFFFFFFFFu, start_k, top);
     return b * kSubtilesPerBlock + static_cast<uint64_t>(top >> 1);
 }
 
-// Output position of the first code of sub-tile s: the block's index entry
-// plus the counts of the block's chunks before it.
-__device__ __forceinline__ uint64_t sub_tile_start(const TensorArgs& t, uint64_t s, int lane) {
-    const uint64_t blk = s / kSubtilesPerBlock;
-    uint32_t pre = 0;
-    for (uint64_t c = blk * kThreads + lane; c < s * kWarpChunks; c += 32) pre += __ldg(t.chunk_index + c) >> 5;
-    return __ldg(t.block_index + blk) + warp_sum(pre);
+// base plus the code counts of the `count` (<= 32) sub-tiles with ordinals
+// ord0 .. ord0 + count - 1, read from the published counts: lane k waits
+// until the entry of ordinal ord0 + k carries that ordinal.  Returns false
+// when a wait gave up (the abort flag or the limit).
+__device__ __forceinline__ bool add_published(PfCtl& ctl, uint32_t ord0, uint32_t count, uint64_t& base,
+                                              uint32_t wait_limit, int32_t* status, int lane) {
+    uint32_t v = 0;
+    bool ok = true;
+    if (static_cast<uint32_t>(lane) < count) {
+        const uint32_t ord = ord0 + lane;
+        const volatile uint64_t* e = &ctl.totals[ord % kTotRing];
+        uint32_t i = 0;
+        for (;; ++i) {
+            const uint64_t x = *e;
+            if (static_cast<uint32_t>(x >> 32) == ord + 1) {
+                v = static_cast<uint32_t>(x);
+                break;
+            }
+            if (i == wait_limit) {
+                ok = false;
+                *reinterpret_cast<volatile int32_t*>(&ctl.abort_flag) = 1;
+                raise_status(status, AFX_DEV_TIMEOUT);
+                break;
+            }
+            if ((i & 31u) == 31u && *reinterpret_cast<volatile int32_t*>(&ctl.abort_flag)) {
+                ok = false;
+                break;
+            }
+        }
+    }
+    base += warp_sum(v);
+    return __all_sync(0xFFFFFFFFu, ok);
 }
 
 // Restores the item's weights [p_lo, p_hi) of tensor t with decoding warp
 // `warp`: sub-tiles s_lo + warp, s_lo + warp + 16, ... of the sub-tiles that
-// hold them, staged one ahead by bulk copies as in the restore kernel.
+// hold them, staged one ahead by bulk copies as in the restore kernel.  The
+// item's sub-tiles have ordinals ord_base + (s - s_lo); each warp publishes
+// its sub-tile's code count right after the scan and places the sub-tile
+// from the counts of the sub-tiles before it (back to its own previous one).
 // Returns false when a wait gave up (the staging copies still in flight are
 // waited for first).
 __device__ bool pf_decode_item(const TabView& tv, WarpSlot& ws, uint8_t* wstream, uint32_t wstride,
-                               const TensorArgs& t, uint64_t p_lo, uint64_t p_hi, uint32_t q_base, uint8_t* ring_a,
-                               PfCtl& ctl, int warp, int lane, int32_t* status, uint32_t wait_limit,
+                               const TensorArgs& t, uint64_t p_lo, uint64_t p_hi, uint32_t q_base, uint32_t& ord_base,
+                               uint8_t* ring_a, PfCtl& ctl, int warp, int lane, int32_t* status, uint32_t wait_limit,
                                uint32_t& phases) {
     const uint32_t T = t.chunk_bytes;
     const uint32_t chunk_bits = 8u * T;
@@ -359,19 +401,24 @@ __device__ bool pf_decode_item(const TabView& tv, WarpSlot& ws, uint8_t* wstream
     const uint32_t skip_row0 = t.tab.n_states * kFsmRowBytes;
     const uint64_t n_sub = (t.n_chunks + kWarpChunks - 1) / kWarpChunks;
     const uint64_t n = t.n;
-    const uint64_t s_lo = find_sub_tile(t, p_lo, lane);
-    const uint64_t s_hi = find_sub_tile(t, p_hi - 1, lane) + 1;
+    uint64_t start, unused;
+    const uint64_t s_lo = find_sub_tile(t, p_lo, lane, &start);
+    const uint64_t s_hi = find_sub_tile(t, p_hi - 1, lane, &unused) + 1;
+    const uint32_t ord0 = ord_base;
+    ord_base += static_cast<uint32_t>(s_hi - s_lo);
     uint64_t s = s_lo + static_cast<uint64_t>(warp);
     if (s >= s_hi || s_hi > n_sub) return true;
     const uint8_t* exp_base = reinterpret_cast<const uint8_t*>(t.exp_words);
     if (lane == 0)
         warp_issue_bulk(ws, wstream, t, s, s < t.n_sub_full, exp_base + s * sub_bytes,
                         t.chunk_index + s * kWarpChunks, sub_bytes, 0, false);
-    uint64_t start = sub_tile_start(t, s, lane);
+    // the first sub-tile starts after the counts of the item's sub-tiles before it
+    uint32_t from = ord0, count = static_cast<uint32_t>(warp);
     int buf = 0;
     for (; s < s_hi; s += kPfDecodeWarps) {
         const uint64_t s_next = s + kPfDecodeWarps;
         const bool more = s_next < s_hi;
+        const uint32_t ord = ord0 + static_cast<uint32_t>(s - s_lo);
         if (more && lane == 0)
             warp_issue_bulk(ws, wstream + (buf ^ 1) * wstride, t, s_next, s_next < t.n_sub_full,
                             exp_base + s_next * sub_bytes, t.chunk_index + s_next * kWarpChunks, sub_bytes, buf ^ 1,
@@ -393,7 +440,6 @@ __device__ bool pf_decode_item(const TabView& tv, WarpSlot& ws, uint8_t* wstream
             if (!__all_sync(0xFFFFFFFFu, drained) && lane == 0) raise_status(status, AFX_DEV_UNDRAINED);
             return false;
         }
-        const uint64_t start_next = more ? sub_tile_start(t, s_next, lane) : 0;
         const bool full = s < t.n_sub_full;
         const uint32_t nexist =
             full ? 64u : static_cast<uint32_t>(min(t.n_chunks - min(t.n_chunks, s * kWarpChunks), uint64_t{64}));
@@ -412,33 +458,18 @@ __device__ bool pf_decode_item(const TabView& tv, WarpSlot& ws, uint8_t* wstream
             if (lane >= d) inc += o;
         }
         const uint32_t total = __shfl_sync(0xFFFFFFFFu, inc, 31);
-        const uint64_t o0 = start, o1 = start + total;
-        const bool in_range = o0 <= n && o1 <= n;
-        if (lane == 0) {
-            if (!in_range) {
-                raise_status(status, AFX_DEV_BAD_BLOCK);
-            } else {
-                // the block index must agree with the counts where a block ends
-                const uint64_t blk = s / kSubtilesPerBlock;
-                if (s + 1 == n_sub) {
-                    if (o1 != n || __ldg(t.block_index + t.n_blocks) != n) raise_status(status, AFX_DEV_BAD_BLOCK);
-                } else if ((s + 1) % kSubtilesPerBlock == 0 && __ldg(t.block_index + blk + 1) != o1) {
-                    raise_status(status, AFX_DEV_BAD_BLOCK);
-                }
-                if (s == 0 && o0 != 0) raise_status(status, AFX_DEV_BAD_BLOCK);
-                if (o0 < o1) {  // the raw bytes are needed after the decode
-                    const uint64_t a0 = o0 & ~uint64_t(15), a1 = (o1 + 15) & ~uint64_t(15);
-                    prefetch_l2(t.sm + a0, static_cast<uint32_t>(a1 - a0));
-                }
-            }
-        }
+        if (lane == 0)  // the next sub-tiles' warps place theirs from this count
+            *reinterpret_cast<volatile uint64_t*>(&ctl.totals[ord % kTotRing]) =
+                (static_cast<uint64_t>(ord + 1) << 32) | total;
+        // decode first, into the stage from index 0: it needs no output
+        // position, so the warps before this one have time to publish theirs
         const uint32_t next = static_cast<uint32_t>(lane) + 1 < nexist ? ws.chunk[buf][lane + 1] : 0u;
         const uint32_t* stream = reinterpret_cast<const uint32_t*>(wstream + static_cast<size_t>(buf) * wstride);
         const uint32_t chunk_end = (lane + 1) * chunk_bits;
         bool stepped = false;
         FsmLane fl;
-        if (cnt && in_range) {
-            const uint32_t s_run = static_cast<uint32_t>(o0 & 7u) + (inc - cnt);
+        if (cnt) {
+            const uint32_t s_run = inc - cnt;
             if (fsm) {
                 uint32_t stream_end = sub_bits;
                 if (!full) {
@@ -467,12 +498,8 @@ __device__ bool pf_decode_item(const TabView& tv, WarpSlot& ws, uint8_t* wstream
             bad = fsm_chunk_finish(tv, stream, fl, cnt, chunk_end, next);
         }
         if (bad) raise_status(status, AFX_DEV_BAD_CHUNK);
-        __syncwarp();
-        // the sub-tile's weights go into the ring even when its stream was
-        // bad (the output is then unspecified), so that every tile completes
-        const uint64_t w0 = in_range ? o0 : 0, w1 = in_range ? o1 : 0;
-        if (!ring_write(ring_a, ctl, ws.stage, o0 & ~uint64_t(7), t.sm, w0, w1, p_lo, p_hi, q_base, wait_limit, status,
-                        lane)) {
+        // this sub-tile starts after the published counts since `from`
+        if (!add_published(ctl, from, count, start, wait_limit, status, lane)) {
             if (more) {  // the next sub-tile's copies are in flight: let them land
                 const bool drained = mbar_wait(&ws.bar[buf ^ 1], (phases >> (buf ^ 1)) & 1u, wait_limit);
                 phases ^= 1u << (buf ^ 1);
@@ -480,7 +507,42 @@ __device__ bool pf_decode_item(const TabView& tv, WarpSlot& ws, uint8_t* wstream
             }
             return false;
         }
-        start = start_next;
+        const uint64_t o0 = start, o1 = start + total;
+        const bool in_range = o0 <= n && o1 <= n;
+        if (lane == 0) {
+            if (!in_range) {
+                raise_status(status, AFX_DEV_BAD_BLOCK);
+            } else {
+                // the block index must agree with the counts where a block ends
+                const uint64_t blk = s / kSubtilesPerBlock;
+                if (s + 1 == n_sub) {
+                    if (o1 != n || __ldg(t.block_index + t.n_blocks) != n) raise_status(status, AFX_DEV_BAD_BLOCK);
+                } else if ((s + 1) % kSubtilesPerBlock == 0 && __ldg(t.block_index + blk + 1) != o1) {
+                    raise_status(status, AFX_DEV_BAD_BLOCK);
+                }
+                if (s == 0 && o0 != 0) raise_status(status, AFX_DEV_BAD_BLOCK);
+                if (o0 < o1) {  // the raw bytes the merge reads next
+                    const uint64_t a0 = o0 & ~uint64_t(15), a1 = (o1 + 15) & ~uint64_t(15);
+                    prefetch_l2(t.sm + a0, static_cast<uint32_t>(a1 - a0));
+                }
+            }
+        }
+        __syncwarp();
+        // the sub-tile's weights go into the ring even when its stream was
+        // bad (the output is then unspecified), so that every slice completes
+        const uint64_t w0 = in_range ? o0 : 0, w1 = in_range ? o1 : 0;
+        if (!ring_write(ring_a, ctl, ws.stage, o0, t.sm, w0, w1, p_lo, p_hi, q_base, wait_limit, status, lane)) {
+            if (more) {  // the next sub-tile's copies are in flight: let them land
+                const bool drained = mbar_wait(&ws.bar[buf ^ 1], (phases >> (buf ^ 1)) & 1u, wait_limit);
+                phases ^= 1u << (buf ^ 1);
+                if (!__all_sync(0xFFFFFFFFu, drained) && lane == 0) raise_status(status, AFX_DEV_UNDRAINED);
+            }
+            return false;
+        }
+        // the next sub-tile (16 on) starts after this one and the 15 between
+        start = o1;
+        from = ord + 1;
+        count = kPfDecodeWarps - 1;
         buf ^= 1;
         fence_proxy_async_smem();  // this buffer's reads come before the bulk copy that refills it
         __syncwarp();
@@ -530,10 +592,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __gr
             mbar_init_count(&ctl.a_empty[i], 1);
             ctl.a_count[i] = 0;
         }
-        for (uint32_t i = 0; i < kBSlots; ++i) {
+        for (uint32_t i = 0; i < L.b_slots; ++i) {
             mbar_init_count(&ctl.b_full[i], 1);
             mbar_init_count(&ctl.b_empty[i], 1);
         }
+        for (uint32_t i = 0; i < kTotRing; ++i) ctl.totals[i] = 0;
         mbar_init_count(&ctl.acc_full, 1);
         mbar_init_count(&ctl.acc_empty, 4);
         mbar_init_count(&ctl.drain, 1);
@@ -570,26 +633,29 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __gr
         tv.fsm = reinterpret_cast<const char*>(tabr);
         tv.depth = sh.ct.state_depth;
         tv.fsm_bytes = a.tab_bytes;
-        uint32_t phases = 0, q_base = 0;
+        uint32_t phases = 0, q_base = 0, ord_base = 0;
         int built = -1;
-        bool alive = true;
         for (uint32_t it = it0; it < it1; ++it) {
             const uint32_t item = a.items[it];
             const uint32_t mi = item >> 28, mt = item & 0x3FFFFu;
             const PrefillMatrix& pm = a.m[mi];
-            // every decoding warp has finished the previous item; all stop together
-            if (named_red_or(kDecodeBarrier, kPfDecodeWarps * 32,
-                             !alive || *reinterpret_cast<volatile int32_t*>(&ctl.abort_flag) != 0))
-                break;
             if (!pm.single && static_cast<int>(mi) != built) {
-                build_tables_w(sh, tabr, pm.t.tab, threadIdx.x, kPfDecodeWarps * 32, DecodeSync{});
+                // every decoding warp is done with the previous tables; all
+                // build, or all skip once a wait anywhere has given up
+                if (!named_red_or(kDecodeBarrier, kPfDecodeWarps * 32,
+                                  *reinterpret_cast<volatile int32_t*>(&ctl.abort_flag) != 0))
+                    build_tables_w(sh, tabr, pm.t.tab, threadIdx.x, kPfDecodeWarps * 32, DecodeSync{});
                 built = static_cast<int>(mi);
             }
             const uint64_t p_lo = static_cast<uint64_t>(mt) * pm.k_tiles * kTileElems;
             const uint64_t p_hi = p_lo + static_cast<uint64_t>(pm.k_tiles) * kTileElems;
-            alive = pm.single ? pf_fill_item(pm, ws, p_lo, p_hi, q_base, ring_a, ctl, warp, lane, status, wait_limit)
-                              : pf_decode_item(tv, ws, wstream, L.wstride, pm.t, p_lo, p_hi, q_base, ring_a, ctl, warp,
-                                               lane, status, wait_limit, phases);
+            if (!*reinterpret_cast<volatile int32_t*>(&ctl.abort_flag)) {
+                if (pm.single)
+                    pf_fill_item(pm, ws, p_lo, p_hi, q_base, ring_a, ctl, warp, lane, status, wait_limit);
+                else
+                    pf_decode_item(tv, ws, wstream, L.wstride, pm.t, p_lo, p_hi, q_base, ord_base, ring_a, ctl, warp,
+                                   lane, status, wait_limit, phases);
+            }
             q_base += pm.k_tiles;
         }
     } else if (warp == kPfProducerWarp) {
@@ -604,22 +670,20 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __gr
                 const PrefillMatrix& pm = a.m[mi];
                 const uint32_t y0 = pass * a.pass_tokens;
                 for (uint32_t g = 0; g < pm.k_tiles && ok; ++g)
-                    for (uint32_t ks = 0; ks < kTileCols / kSliceK && ok; ++ks)
-                        for (uint32_t h = 0; h < a.halves; ++h) {
-                            const uint32_t b = bseq % kBSlots;
-                            if (!pf_wait(&ctl.b_empty[b], ((bseq / kBSlots) & 1u) ^ 1u, wait_limit, ctl, status)) {
-                                ok = false;
-                                break;
-                            }
-                            mbar_expect_tx(&ctl.b_full[b], stage_bytes);
-                            tma_load_2d(ring_b + b * L.b_stage, &a.tmap[mi], g * kTileCols + ks * kSliceK,
-                                        y0 + h * a.n_mma, &ctl.b_full[b]);
-                            ++bseq;
+                    for (uint32_t h = 0; h < a.halves; ++h) {
+                        const uint32_t b = bseq % L.b_slots;
+                        if (!pf_wait(&ctl.b_empty[b], ((bseq / L.b_slots) & 1u) ^ 1u, wait_limit, ctl, status)) {
+                            ok = false;
+                            break;
                         }
+                        mbar_expect_tx(&ctl.b_full[b], stage_bytes);
+                        tma_load_2d(ring_b + b * L.b_stage, &a.tmap[mi], g * kSliceK, y0 + h * a.n_mma, &ctl.b_full[b]);
+                        ++bseq;
+                    }
             }
             if (!ok) {  // the loads still in flight land before the CTA exits
-                for (uint32_t j = bseq > kBSlots ? bseq - kBSlots : 0; j < bseq; ++j)
-                    if (!mbar_wait(&ctl.b_full[j % kBSlots], (j / kBSlots) & 1u, wait_limit))
+                for (uint32_t j = bseq > L.b_slots ? bseq - L.b_slots : 0; j < bseq; ++j)
+                    if (!mbar_wait(&ctl.b_full[j % L.b_slots], (j / L.b_slots) & 1u, wait_limit))
                         raise_status(status, AFX_DEV_UNDRAINED);
             }
         }
@@ -643,20 +707,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __gr
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(ring_a + slot * kTileBytes);
-                    for (uint32_t ks = 0; ks < kTileCols / kSliceK && ok; ++ks)
-                        for (uint32_t h = 0; h < a.halves; ++h) {
-                            const uint32_t b = bseq % kBSlots;
-                            if (!pf_wait(&ctl.b_full[b], (bseq / kBSlots) & 1u, wait_limit, ctl, status)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            tc_mma(tmem + h * a.n_mma, desc_sw128(a_addr + ks * kSliceK * 2),
-                                   desc_sw32(smem_u32(ring_b + b * L.b_stage)), idesc, (g | ks) != 0);
-                            tc_commit(&ctl.b_empty[b]);
-                            ++bseq;
+                    const uint64_t a_desc = desc_sw32(smem_u32(ring_a + slot * kTileBytes));
+                    for (uint32_t h = 0; h < a.halves; ++h) {
+                        const uint32_t b = bseq % L.b_slots;
+                        if (!pf_wait(&ctl.b_full[b], (bseq / L.b_slots) & 1u, wait_limit, ctl, status)) {
+                            ok = false;
+                            break;
                         }
+                        tc_fence_after();
+                        tc_mma(tmem + h * a.n_mma, a_desc, desc_sw32(smem_u32(ring_b + b * L.b_stage)), idesc, g != 0);
+                        tc_commit(&ctl.b_empty[b]);
+                        ++bseq;
+                    }
                     if (ok) tc_commit(&ctl.a_empty[slot]);
                 }
                 if (ok) {
@@ -838,7 +900,7 @@ using namespace afx;
 extern "C" afx_status afx_tile_order(const uint16_t* w, uint32_t rows, uint32_t cols, uint16_t* out) {
     if (!w || !out) return afx_fail(AFX_E_ARG, "null pointer", 0);
     if (rows == 0 || cols == 0 || rows % kTileRows || cols % kTileCols)
-        return afx_fail(AFX_E_ARG, "rows must be a multiple of 128 and cols a multiple of 64", 0);
+        return afx_fail(AFX_E_ARG, "rows must be a multiple of 128 and cols a multiple of 16", 0);
     const uint64_t kt = cols / kTileCols;
     for (uint64_t m = 0; m < rows / kTileRows; ++m)
         for (uint64_t g = 0; g < kt; ++g) {
@@ -885,7 +947,7 @@ extern "C" afx_status afx_prefill_fused_batch(const afx_desc* descs, const void*
             if (afx_check_desc(&d) != AFX_OK) return afx_fail(AFX_E_FORMAT, "invalid container description", 0);
             if (d.format != AFX_FMT_BF16) return afx_fail(AFX_E_ARG, "the fused prefill product takes BF16 containers", 0);
             if (rows[i] == 0 || cols[i] == 0 || rows[i] % kTileRows || cols[i] % kTileCols)
-                return afx_fail(AFX_E_ARG, "rows must be a multiple of 128 and cols a multiple of 64", 0);
+                return afx_fail(AFX_E_ARG, "rows must be a multiple of 128 and cols a multiple of 16", 0);
             if (static_cast<uint64_t>(rows[i]) * cols[i] != d.n) return afx_fail(AFX_E_ARG, "rows * cols != n", 0);
             if (rows[i] / kTileRows > (1u << 18)) return afx_fail(AFX_E_ARG, "too many rows", 0);
             if (d.nsym >= 2 && d.block_chunks != static_cast<uint32_t>(kThreads))
