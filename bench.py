@@ -983,6 +983,8 @@ def run_prefill_bench(afx, parts, dev_blob, offs, dev, args):
         tiled_parts = list(ex.map(tiled, [name for name, _, _ in mats]))
     tdescs = [d for _, d in tiled_parts]
     tconts = [torch.from_numpy(c).to(dev) for c, _ in tiled_parts]
+    fused_ws = torch.empty(afx.afx_prefill_fused_workspace(), dtype=torch.uint8, device=dev)
+    out["fused_workspace_bytes"] = fused_ws.numel()
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     for n_tok in (1, 4, 128, 512, 2048):
         reps = 20 if n_tok <= 4 else 5
@@ -1002,7 +1004,7 @@ def run_prefill_bench(afx, parts, dev_blob, offs, dev, args):
             afx.afx_prefill_batch(descs, conts, mshapes, xs, ys, [whole, None], ws, gemm_stream=gs)
 
         def fused():
-            afx.afx_prefill_fused_batch(tdescs, tconts, mshapes, xs, yf, stream=gs, status_dev=status)
+            afx.afx_prefill_fused_batch(tdescs, tconts, mshapes, xs, yf, fused_ws, stream=gs, status_dev=status)
 
         seq_ms = timed(sequential, gs, reps)
         ovl_ms = timed(overlapped, gs, reps)
@@ -1043,9 +1045,10 @@ def run_prefill_bench(afx, parts, dev_blob, offs, dev, args):
                    "float32 accumulation; sequential: restore then product per matrix on one stream; overlapped: "
                    "restore of matrix i+1 on a second stream; one restore launch: all seven restored by one "
                    "afx_decode_batch launch, then the products; tokens_per_s and tflops from the fastest of "
-                   "those; fused: afx_prefill_fused_batch over the tile-ordered containers (prefill_fused_kernel, "
-                   "tcgen05 products from the restored tiles in shared memory, no scratch; the weights are "
-                   "restored once per 512 tokens, counted in fused_weights_per_s)")
+                   "those; fused: afx_prefill_fused_batch over the tile-ordered containers (prefill_fused_kernel: "
+                   "restored 128x64 tiles through a 256 KB ring per SM that stays in L2, TMA into shared memory, "
+                   "tcgen05 products, no restored matrix written out; the weights are restored once per 512 "
+                   "tokens, counted in fused_weights_per_s)")
     return out
 
 

@@ -406,50 +406,63 @@ afx_status afx_prefill_batch(const afx_desc* descs, const void* const* container
  *
  * The prompt's token vectors through a weight matrix with the restore fused
  * into the tensor-core product: the restored weights go from the decoder
- * into the tensor cores' shared-memory operand tiles and never reach global
- * memory, so no scratch buffer is needed.  Cites: "Memory requirements of
+ * through a small L2-resident ring to the tensor cores' shared-memory
+ * operand tiles; the restored matrix is never written out.  Cites: "Memory requirements of
  * language model inference on a consumer GPU", section "Loading one part of
  * the model at a time" (the prompt goes through each layer as a whole), and
  * "Why Weight Offloading Slows Inference", section "Lossless compression:
  * fewer bytes to read, more work to unpack" (the released bits are restored
  * before computation; t_unpack of Eq. (1)).
  *
- * The product reads the weights in slice order: the [rows][cols] matrix
- * cut into 128 x 16 slices, each slice row-major, the slices of a 128-row
- * band in column order, the bands in row order; element (r, c) at position
- * ((r / 128) * (cols / 16) + c / 16) * 2048 + (r % 128) * 16 + c % 16.
+ * The product reads the weights in tile order: the [rows][cols] matrix cut
+ * into 128 x 64 tiles, each tile row-major, the tiles of a 128-row band in
+ * column order, the bands in row order; element (r, c) at position
+ * ((r / 128) * (cols / 64) + c / 64) * 8192 + (r % 128) * 64 + c % 64.
  * afx_tile_order writes that order; encode its output with afx_encode as
  * usual (the container format is unchanged, only the element order). */
 
-/* out_host[slice order] = w_host[rows][cols] (row-major BF16 patterns, host
- * memory, rows a multiple of 128 and cols a multiple of 16; out_host holds
+/* out_host[tile order] = w_host[rows][cols] (row-major BF16 patterns, host
+ * memory, rows a multiple of 128 and cols a multiple of 64; out_host holds
  * rows * cols elements and must not overlap w_host).  Errors: AFX_E_ARG. */
 afx_status afx_tile_order(const uint16_t* w_host, uint32_t rows, uint32_t cols, uint16_t* out_host);
+
+/* Bytes of device workspace afx_prefill_fused needs on the current device:
+ * one 256 KB ring of restored tiles per CTA, one CTA per SM (38.9 MB on a
+ * 152-SM GB300).  A smaller workspace runs fewer CTAs (at least one ring).
+ * Errors: AFX_E_ARG, AFX_E_CUDA. */
+afx_status afx_prefill_fused_workspace(uint64_t* bytes);
 
 /* y_dev[t][r] = sum_c W[r][c] * x_dev[t][c] for t < n_tokens, where the
  * container holds W ([rows][cols], BF16) in tile order.  x_dev: BF16
  * [n_tokens][cols], row-major, 16-byte aligned; y_dev: float32
  * [n_tokens][rows], overwritten.  Products of BF16 pairs are exact and are
- * summed in float32 by the tensor cores.  rows a multiple of 128, cols a
- * multiple of 16, n_tokens >= 1 (up to 512 per pass over the weights; more
- * tokens restore the weights once per 512).  The container, x_dev and
- * y_dev in device memory (container 256-byte aligned).  Asynchronous on
- * stream; device-detected corruption or a wait past its limit sets
- * AFX_DEV_* bits in *status_dev (nullable; the outputs are then
- * unspecified).  Allocates nothing.
- * Errors: AFX_E_ARG (shape, alignment, memory kind, format), AFX_E_FORMAT,
- * AFX_E_CUDA. */
+ * summed in float32 by the tensor cores, in a fixed order (y_dev is
+ * bitwise reproducible).  rows a multiple of 128, cols a multiple of 64,
+ * n_tokens >= 1 (up to 512 per pass over the weights; more tokens restore
+ * the weights once per 512).  The restored weights go through the
+ * workspace (a ring of 16 tiles of 16 KB per CTA, written and read back
+ * within microseconds, so it stays in L2; no restored matrix is written
+ * out): workspace_dev, 256-byte aligned, of workspace_bytes (see
+ * afx_prefill_fused_workspace), contents ignored; calls that overlap on the
+ * GPU need their own workspaces.  The container, x_dev, y_dev and the
+ * workspace in device memory (container 256-byte aligned).  Asynchronous on
+ * stream; device-detected corruption or a wait past its limit sets AFX_DEV_*
+ * bits in *status_dev (nullable; the outputs are then unspecified).
+ * Errors: AFX_E_ARG (shape, alignment, memory kind, format), AFX_E_NOSPACE
+ * (workspace smaller than one ring), AFX_E_FORMAT, AFX_E_CUDA. */
 afx_status afx_prefill_fused(const afx_desc* desc, const void* container_dev, uint32_t rows, uint32_t cols,
-                             const uint16_t* x_dev, uint32_t n_tokens, float* y_dev, afx_stream_t stream,
-                             int32_t* status_dev);
+                             const uint16_t* x_dev, uint32_t n_tokens, float* y_dev, void* workspace_dev,
+                             uint64_t workspace_bytes, afx_stream_t stream, int32_t* status_dev);
 
 /* afx_prefill_fused over count matrices in one launch (per 16 matrices),
  * all with the same n_tokens: ys_dev[i] = W_i xs_dev[i] with W_i the
- * slice-ordered weights of containers_dev[i], [rows[i]][cols[i]].  Same
- * rules and errors as afx_prefill_fused, per matrix. */
+ * tile-ordered weights of containers_dev[i], [rows[i]][cols[i]].  One
+ * workspace for the call.  Same rules and errors as afx_prefill_fused, per
+ * matrix. */
 afx_status afx_prefill_fused_batch(const afx_desc* descs, const void* const* containers_dev, const uint32_t* rows,
                                    const uint32_t* cols, const uint16_t* const* xs_dev, uint32_t n_tokens,
-                                   float* const* ys_dev, uint32_t count, afx_stream_t stream, int32_t* status_dev);
+                                   float* const* ys_dev, uint32_t count, void* workspace_dev, uint64_t workspace_bytes,
+                                   afx_stream_t stream, int32_t* status_dev);
 
 /* ---- residency planning ------------------------------------------------
  *

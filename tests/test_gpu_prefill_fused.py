@@ -24,18 +24,24 @@ def _tiled(afx, W):
     return afx.encode(afx.afx_tile_order(W, rows, cols))
 
 
-def _run(afx, W, X, status=None):
+def _workspace(afx, rings=None):
+    import torch
+    n = afx.afx_prefill_fused_workspace() if rings is None else rings * 16 * 16384
+    return torch.empty(n, dtype=torch.uint8, device="cuda")
+
+
+def _run(afx, W, X, status=None, ws=None):
     import torch
     rows, cols = W.shape
     c, d = _tiled(afx, W)
     y = torch.full((X.shape[0], rows), float("nan"), dtype=torch.float32, device="cuda")
     afx.afx_prefill_fused(d, torch.from_numpy(c).cuda(), rows, cols, torch.from_numpy(X.view(np.int16)).cuda(), y,
-                          status_dev=status)
+                          _workspace(afx) if ws is None else ws, status_dev=status)
     torch.cuda.synchronize()
     return y.cpu().numpy()
 
 
-@pytest.mark.parametrize("shape", [(128, 16), (128, 64), (256, 640), (384, 5120), (1024, 48)])
+@pytest.mark.parametrize("shape", [(128, 64), (256, 640), (384, 5120), (1024, 192)])
 @pytest.mark.parametrize("n_tokens", [1, 17, 128, 300, 512])
 def test_fused_prefill_matches_the_oracle(afx, shape, n_tokens):
     import torch
@@ -87,9 +93,10 @@ def test_fused_prefill_is_reproducible(afx):
     dev = torch.from_numpy(c).cuda()
     xd = torch.from_numpy(X.view(np.int16)).cuda()
     outs = []
+    ws = _workspace(afx)
     for _ in range(3):
         y = torch.empty((n_tokens, rows), dtype=torch.float32, device="cuda")
-        afx.afx_prefill_fused(d, dev, rows, cols, xd, y)
+        afx.afx_prefill_fused(d, dev, rows, cols, xd, y, ws)
         torch.cuda.synchronize()
         outs.append(y.cpu().numpy())
     assert all(np.array_equal(outs[0].view(np.uint32), o.view(np.uint32)) for o in outs[1:])
@@ -114,10 +121,11 @@ def test_fused_prefill_batch_mixed_matrices(afx):
         items.append((W, X, torch.from_numpy(c).cuda(), d, torch.from_numpy(X.view(np.int16)).cuda()))
     assert items[3][3].nsym == 1
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    for _ in range(2):
+    ws = _workspace(afx)
+    for _ in range(2):  # the second call finds the first call's tiles in the workspace
         ys = [torch.full((n_tokens, r), float("nan"), dtype=torch.float32, device="cuda") for r, _ in shapes]
         afx.afx_prefill_fused_batch([it[3] for it in items], [it[2] for it in items], shapes,
-                                    [it[4] for it in items], ys, status_dev=status)
+                                    [it[4] for it in items], ys, ws, status_dev=status)
         torch.cuda.synchronize()
         assert status.item() == 0
         for (W, X, *_), y in zip(items, ys):
@@ -139,6 +147,16 @@ def test_fused_prefill_large_code_trees_use_the_12_bit_table(afx, n_exponents):
     assert ok, worst
 
 
+@pytest.mark.parametrize("rings", [1, 3])
+def test_fused_prefill_with_a_small_workspace(afx, rings):
+    # a workspace of one or three rings runs that many CTAs over all the items
+    rows, cols, n_tokens = 1024, 640, 100
+    W = synth.normal(rows * cols, seed=rings).reshape(rows, cols)
+    X = synth.activations(n_tokens, cols, seed=7)
+    ok, worst = _within(_run(afx, W, X, ws=_workspace(afx, rings)), W, X)
+    assert ok, worst
+
+
 def test_fused_prefill_refuses_bad_arguments(afx):
     import torch
     W = synth.normal(128 * 64, seed=1).reshape(128, 64)
@@ -146,18 +164,22 @@ def test_fused_prefill_refuses_bad_arguments(afx):
     dev = torch.from_numpy(c).cuda()
     x = torch.zeros((4, 64), dtype=torch.int16, device="cuda")
     y = torch.zeros((4, 128), dtype=torch.float32, device="cuda")
+    ws = _workspace(afx, 1)
     with pytest.raises(afx.AfxError):  # rows not a multiple of 128
         afx.afx_prefill_fused(d, dev, 64, 128, torch.zeros((4, 128), dtype=torch.int16, device="cuda"),
-                              torch.zeros((4, 64), dtype=torch.float32, device="cuda"))
-    with pytest.raises(afx.AfxError):  # cols not a multiple of 16
-        afx.afx_prefill_fused(d, dev, 1024, 8, torch.zeros((4, 8), dtype=torch.int16, device="cuda"),
-                              torch.zeros((4, 1024), dtype=torch.float32, device="cuda"))
+                              torch.zeros((4, 64), dtype=torch.float32, device="cuda"), ws)
+    with pytest.raises(afx.AfxError):  # cols not a multiple of 64
+        afx.afx_prefill_fused(d, dev, 256, 32, torch.zeros((4, 32), dtype=torch.int16, device="cuda"),
+                              torch.zeros((4, 256), dtype=torch.float32, device="cuda"), ws)
     with pytest.raises((afx.AfxError, ValueError)):  # x in host memory
-        afx.afx_prefill_fused(d, dev, 128, 64, torch.zeros((4, 64), dtype=torch.int16), y)
+        afx.afx_prefill_fused(d, dev, 128, 64, torch.zeros((4, 64), dtype=torch.int16), y, ws)
     c2, d2 = afx.encode(synth.normal_fp16(128 * 64, seed=2), fmt=afx.AFX_FMT_FP16)
     with pytest.raises(afx.AfxError):  # FP16 elements
-        afx.afx_prefill_fused(d2, torch.from_numpy(c2).cuda(), 128, 64, x, y)
-    afx.afx_prefill_fused(d, dev, 128, 64, x, y)  # the same call with valid arguments
+        afx.afx_prefill_fused(d2, torch.from_numpy(c2).cuda(), 128, 64, x, y, ws)
+    with pytest.raises(afx.AfxError) as err:  # a workspace smaller than one ring
+        afx.afx_prefill_fused(d, dev, 128, 64, x, y, ws[: 16 * 16384 - 256])
+    assert err.value.status == afx.AFX_E_NOSPACE
+    afx.afx_prefill_fused(d, dev, 128, 64, x, y, ws)  # the same call with valid arguments
     torch.cuda.synchronize()
 
 
@@ -178,7 +200,7 @@ def test_fused_prefill_qwen3_layer_matrices_sampled(afx, n_tokens):
     ys = [torch.full((n_tokens, r), float("nan"), dtype=torch.float32, device="cuda") for _, (r, _) in mats]
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     afx.afx_prefill_fused_batch([it[3] for it in items], [it[2] for it in items], [s for _, s in mats],
-                                [it[4] for it in items], ys, status_dev=status)
+                                [it[4] for it in items], ys, _workspace(afx), status_dev=status)
     torch.cuda.synchronize()
     assert status.item() == 0
     for (name, (rows, cols)), (W, X, *_), y in zip(mats, items, ys):

@@ -141,11 +141,12 @@ _lib.afx_prefill_batch.argtypes = [ctypes.POINTER(afx_desc), ctypes.POINTER(ctyp
                                    ctypes.POINTER(ctypes.c_void_p), _vp, _vp, _vp, _i32p]
 AFX_PREFILL_GEMM_WORKSPACE_BYTES = 32 << 20
 _lib.afx_tile_order.argtypes = [_vp, _u32, _u32, _vp]
-_lib.afx_prefill_fused.argtypes = [ctypes.POINTER(afx_desc), _vp, _u32, _u32, _vp, _u32, _vp, _vp, _i32p]
+_lib.afx_prefill_fused_workspace.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
+_lib.afx_prefill_fused.argtypes = [ctypes.POINTER(afx_desc), _vp, _u32, _u32, _vp, _u32, _vp, _vp, _u64, _vp, _i32p]
 _lib.afx_prefill_fused_batch.argtypes = [ctypes.POINTER(afx_desc), ctypes.POINTER(ctypes.c_void_p),
                                          ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint32),
                                          ctypes.POINTER(ctypes.c_void_p), _u32, ctypes.POINTER(ctypes.c_void_p), _u32,
-                                         _vp, _i32p]
+                                         _vp, _u64, _vp, _i32p]
 _lib.afx_last_error.argtypes = []
 _lib.afx_last_error.restype = ctypes.c_char_p
 _lib.afx_status_string.argtypes = [ctypes.c_int]
@@ -154,7 +155,8 @@ for _f in (_lib.afx_build_code, _lib.afx_build_code_fmt, _lib.afx_encode_bound, 
            _lib.afx_decode_batch, _lib.afx_decode_gemv_workspace, _lib.afx_decode_gemv, _lib.afx_decode_gemv_batch,
            _lib.afx_decode_gemv_static, _lib.afx_stream_run, _lib.afx_test_restore_stalled,
            _lib.afx_plan_residency, _lib.afx_debug_bounds_report, _lib.afx_prefill, _lib.afx_prefill_batch,
-           _lib.afx_tile_order, _lib.afx_prefill_fused, _lib.afx_prefill_fused_batch):
+           _lib.afx_tile_order, _lib.afx_prefill_fused, _lib.afx_prefill_fused_batch,
+           _lib.afx_prefill_fused_workspace):
     _f.restype = ctypes.c_int
 
 
@@ -406,19 +408,30 @@ def afx_tile_order(w, rows: int, cols: int) -> np.ndarray:
     return out
 
 
-def afx_prefill_fused(desc: afx_desc, container_dev, rows: int, cols: int, x_dev, y_dev, stream=None,
+def afx_prefill_fused_workspace() -> int:
+    """Bytes of device workspace afx_prefill_fused needs on the current device (one ring per SM)."""
+    v = ctypes.c_uint64()
+    _check("afx_prefill_fused_workspace", _lib.afx_prefill_fused_workspace(ctypes.byref(v)))
+    return v.value
+
+
+def afx_prefill_fused(desc: afx_desc, container_dev, rows: int, cols: int, x_dev, y_dev, workspace_dev, stream=None,
                       status_dev=None) -> None:
-    """y_dev[t] = W x_dev[t] for every token t, W restored from a tile-ordered container inside the product:
-    x_dev BF16 [n_tokens][cols], y_dev float32 [n_tokens][rows]."""
+    """y_dev[t] = W x_dev[t] for every token t, W restored from a slice-ordered container inside the product:
+    x_dev BF16 [n_tokens][cols], y_dev float32 [n_tokens][rows], workspace_dev a CUDA tensor of
+    afx_prefill_fused_workspace() bytes."""
     n_tokens = x_dev.shape[0]
     if x_dev.numel() != n_tokens * cols or y_dev.numel() != n_tokens * rows:
         raise ValueError("x_dev must be [n_tokens][cols] and y_dev [n_tokens][rows]")
     _check("afx_prefill_fused", _lib.afx_prefill_fused(ctypes.byref(desc), _dev_ptr(container_dev), rows, cols,
                                                         _dev_ptr(x_dev), n_tokens, _dev_ptr(y_dev),
+                                                        _dev_ptr(workspace_dev),
+                                                        workspace_dev.numel() * workspace_dev.element_size(),
                                                         _stream_handle(stream), _dev_ptr(status_dev)))
 
 
-def afx_prefill_fused_batch(descs, containers_dev, shapes, xs_dev, ys_dev, stream=None, status_dev=None) -> None:
+def afx_prefill_fused_batch(descs, containers_dev, shapes, xs_dev, ys_dev, workspace_dev, stream=None,
+                            status_dev=None) -> None:
     """afx_prefill_fused over several matrices (shapes = [(rows, cols)]), one launch per 16."""
     n = len(descs)
     n_tokens = xs_dev[0].shape[0]
@@ -427,6 +440,8 @@ def afx_prefill_fused_batch(descs, containers_dev, shapes, xs_dev, ys_dev, strea
     cols = (ctypes.c_uint32 * n)(*[c for _, c in shapes])
     _check("afx_prefill_fused_batch", _lib.afx_prefill_fused_batch(arr, _ptrs(containers_dev), rows, cols,
                                                                     _ptrs(xs_dev), n_tokens, _ptrs(ys_dev), n,
+                                                                    _dev_ptr(workspace_dev),
+                                                                    workspace_dev.numel() * workspace_dev.element_size(),
                                                                     _stream_handle(stream), _dev_ptr(status_dev)))
 
 

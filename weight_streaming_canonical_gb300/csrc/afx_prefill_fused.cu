@@ -8,35 +8,37 @@
 // token), with W restored from its exponent-coded container on the way ("Why
 // Weight Offloading Slows Inference", section "Lossless compression: fewer
 // bytes to read, more work to unpack": the released bits are restored before
-// compute; the restore is that page's t_unpack of Eq. (1)).  The restored
-// weights go from the decoder straight into the tensor cores' shared-memory
-// operand tiles and never reach global memory.
+// compute; the restore is that page's t_unpack of Eq. (1)).  No restored
+// matrix is ever written out: restored weights pass through a small ring
+// per CTA that stays in L2 on their way to the tensor cores.
 //
-// Weight order.  The container holds W in slice order: 128 x 16 slices of
-// W, row-major inside a slice, the slices of one 128-row band (an "m-tile")
-// in column order, the bands in row order (afx_tile_order writes it).  A
+// Weight order.  The container holds W in tile order: 128 x 64 tiles of W,
+// row-major inside a tile, the tiles of one 128-row band (an "m-tile") in
+// column order, the bands in row order (afx_tile_order writes it).  A
 // band's weights are then one contiguous range of the stream, and each
-// 2048-weight slice is the A operand of one MMA (K = 16).
+// 8192-weight tile is the A operand of four MMAs (K = 16 each).
 //
 // Work decomposition.  A work item is one m-tile of one matrix for one pass
 // of up to 512 tokens; the host assigns items to persistent CTAs (longest
-// first, each to the least loaded CTA), one CTA per SM.  Inside a CTA:
-//   - 16 decoding warps restore the item's sub-tiles (32 chunks each,
+// first, each to the least loaded CTA), one CTA per SM.
+//   - 22 decoding warps restore the item's sub-tiles (32 chunks each,
 //     interleaved across the warps) with the byte-step decoder of the
-//     restore kernel and write each weight into a ring of sixteen 4 KB A
-//     slices (128 x 16 BF16, K-major, 32-byte swizzle).  A slice is full once
-//     its 2048 weights have been counted in; the warp that completes it
-//     signals the slice's barrier.  Each warp publishes its sub-tile's code
-//     count in shared memory as soon as its scan has it; the next warps add
-//     those counts to place their own sub-tiles, so no warp reads the chunk
-//     index of other sub-tiles from global memory;
-//   - a producer warp loads the token vectors with TMA: 16 columns x up to
-//     256 tokens per stage (32-byte swizzle), a 32 KB ring of 4 to 64
-//     stages (more, smaller ones for fewer tokens);
-//   - an MMA warp issues tcgen05.mma (M = 128, N = tokens of one half, K =
-//     16) from the two rings into a float32 accumulator in tensor memory (up
-//     to 2 x 256 columns) and returns ring slots with tcgen05.commit;
-//   - four epilogue warps read the accumulator with tcgen05.ld (each its
+//     restore kernel.  A warp decodes into its stage first (that needs no
+//     output position), then places the sub-tile by adding the code counts
+//     the warps before it published in shared memory after their scans, and
+//     stores the restored weights, joined with their sign|mantissa bytes,
+//     into the CTA's ring of 16 tiles in global memory (256 KB, written and
+//     read back within microseconds, so it stays in L2) with coalesced
+//     16-byte stores.  Each store range is counted into the tile's barrier;
+//     the 8192th weight completes it;
+//   - a producer lane moves each complete tile from the ring into one of
+//     two shared-memory A stages with TMA (128-byte rows and swizzle), and
+//     a second producer lane loads the token vectors: 64 columns x up to
+//     128 tokens per stage (128-byte swizzle), a 48 KB ring of stages;
+//   - an MMA warp issues tcgen05.mma (M = 128, N = up to 128 tokens, K = 16)
+//     into up to four float32 accumulators in tensor memory (512 tokens a
+//     pass) and frees ring tiles and stages with tcgen05.commit;
+//   - four epilogue warps read the accumulators with tcgen05.ld (each its
 //     32-lane quarter) and store Y, row by row of W, coalesced across lanes.
 // Every wait is bounded; a wait that runs out sets AFX_DEV_TIMEOUT and an
 // abort flag that every role polls, copies in flight are waited for, and the
@@ -56,40 +58,44 @@
 
 namespace afx {
 
-constexpr int kPfDecodeWarps = 16;
-constexpr int kPfProducerWarp = kPfDecodeWarps;
+constexpr int kPfDecodeWarps = 22;
+constexpr int kPfProducerWarp = kPfDecodeWarps;      // lane 0: A tiles, lane 16: token vectors
 constexpr int kPfMmaWarp = kPfDecodeWarps + 1;
 constexpr int kPfEpiWarp0 = kPfDecodeWarps + 2;
 constexpr int kPfWarps = kPfDecodeWarps + 6;
 constexpr int kPfThreads = kPfWarps * 32;
-constexpr uint32_t kDecodeBarrier = 1;  // named barrier of the decoding warps
-constexpr uint32_t kSliceK = 16;             // K of one MMA, of one A slice and of one activation stage
-constexpr uint32_t kTileRows = 128, kTileCols = kSliceK, kTileElems = kTileRows * kTileCols;  // an A slice
+constexpr uint32_t kDecodeBarrier = 1;                // named barrier of the decoding warps
+constexpr uint32_t kSliceK = 16;                      // K of one MMA
+constexpr uint32_t kTileRows = 128, kTileCols = 64, kTileElems = kTileRows * kTileCols;  // an A tile
 constexpr uint32_t kTileBytes = kTileElems * 2;
-constexpr uint32_t kASlots = 16;
-constexpr uint32_t kBRingBytes = 32768;      // the activation ring: as many stages as fit, at most kBSlotsMax
-constexpr uint32_t kBSlotsMax = 64;
-constexpr uint32_t kTotRing = 128;           // published sub-tile code counts
-constexpr uint32_t kMaxHalfTokens = 256;     // N of one MMA
-constexpr uint32_t kMaxPassTokens = 2 * kMaxHalfTokens;
+constexpr uint32_t kRingTiles = 16;                  // A tiles in the CTA's ring in global memory (256 KB)
+constexpr uint32_t kAStages = 2;                      // A tiles in shared memory
+constexpr uint32_t kBRingBytes = 49152;               // the activation ring: as many stages as fit, at most kBSlotsMax
+constexpr uint32_t kBSlotsMax = 16;
+constexpr uint32_t kTotRing = 128;                    // published sub-tile code counts
+constexpr uint32_t kMaxHalfTokens = 128;              // N of one MMA
+constexpr uint32_t kMaxHalves = 4;                    // accumulators of one pass
+constexpr uint32_t kMaxPassTokens = kMaxHalves * kMaxHalfTokens;
 constexpr int kPfMaxItems = 2048;
 constexpr int kPfMaxCtas = 256;
 
-static_assert(kPfDecodeWarps == kSubtilesPerBlock, "the decoding warps cover one block of sub-tiles per round");
-static_assert(((kPfEpiWarp0 + 0) % 4) != ((kPfEpiWarp0 + 1) % 4) && ((kPfEpiWarp0 + 2) % 4) != ((kPfEpiWarp0 + 3) % 4),
-              "the epilogue warps cover the four lane quarters of tensor memory");
+static_assert(kPfThreads <= 1024, "one CTA of at most 1024 threads");
+static_assert(kPfEpiWarp0 % 4 == 0, "the epilogue warps cover the four lane quarters of tensor memory in order");
+static_assert(kPfDecodeWarps - 1 <= 32 && kTotRing >= 4 * kPfDecodeWarps, "look-back reads one count per lane");
 
 struct PrefillMatrix {
     TensorArgs t;       // sections, geometry and code tables; t.y = Y [n_tokens][rows]
-    uint32_t k_tiles;   // A slices per m-tile: cols / 16
+    uint32_t k_tiles;   // A tiles per m-tile: cols / 64
     uint32_t single;    // 1: one exponent for every weight (no coded stream)
     uint32_t fill;      // that exponent
 };
 
 // An item: matrix << 28 | pass << 18 | m-tile.
 struct PrefillArgs {
-    CUtensorMap tmap[kMaxTensors];  // X of each matrix: [n_tokens][cols] BF16, box 16 x n_mma, 32-byte swizzle
+    CUtensorMap tmap[kMaxTensors];  // X of each matrix: [n_tokens][cols] BF16, box 64 x n_mma, 128-byte swizzle
+    CUtensorMap ring_map;           // the rings: [CTAs * 16 * 128][64] BF16, box 64 x 128, 128-byte swizzle
     PrefillMatrix m[kMaxTensors];
+    uint16_t* ring;                 // CTA c's ring at ring + c * 16 * 8192
     uint32_t count, n_tokens, n_mma, halves, pass_tokens, tab_bytes, tmem_cols, wait_limit, max_chunk_bytes;
     int32_t* status;
     uint16_t cta_begin[kPfMaxCtas + 1];
@@ -98,11 +104,11 @@ struct PrefillArgs {
 
 // Control block in shared memory.
 struct PfCtl {
-    uint64_t a_full[kASlots], a_empty[kASlots];
+    uint64_t ring_full[kRingTiles], ring_empty[kRingTiles];
+    uint64_t a_full[kAStages], a_empty[kAStages];
     uint64_t b_full[kBSlotsMax], b_empty[kBSlotsMax];
-    uint64_t acc_full, acc_empty, drain;
+    uint64_t acc_full, acc_empty, drain_a, drain_b, drain_mma;
     uint64_t totals[kTotRing];  // (ordinal + 1) << 32 | code count of a sub-tile, at ordinal % kTotRing
-    uint32_t a_count[kASlots];  // weights counted into each A slot's current slice
     uint32_t tmem_base;
     int32_t abort_flag;
 };
@@ -117,13 +123,11 @@ __host__ __device__ inline uint32_t round_up(uint32_t v, uint32_t a) { return (v
 __host__ __device__ inline PfLayout pf_layout(uint32_t tab_bytes, uint32_t n_mma, uint32_t max_chunk_bytes) {
     PfLayout L;
     L.a = 0;
-    // a stage holds 16 columns of the tokens of one half; small stages come
-    // many to the ring, so that the loads run as many columns ahead of the
-    // products at any token count (the ring's depth, not a load's size,
-    // covers the load latency)
-    L.b_stage = round_up(n_mma * kSliceK * 2, 256);
+    // an activation stage holds 64 columns of the tokens of one
+    // accumulator; small stages come many to the ring
+    L.b_stage = round_up(n_mma * kTileCols * 2, 1024);
     L.b_slots = kBRingBytes / L.b_stage < kBSlotsMax ? kBRingBytes / L.b_stage : kBSlotsMax;
-    L.b = L.a + kASlots * kTileBytes;
+    L.b = L.a + kAStages * kTileBytes;
     L.ctl = L.b + L.b_slots * L.b_stage;
     L.shw = round_up(L.ctl + static_cast<uint32_t>(sizeof(PfCtl)), 16);
     L.slots = round_up(L.shw + static_cast<uint32_t>(sharedw_table_offset()) + tab_bytes, 16);
@@ -162,14 +166,6 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// Adds v to a shared counter with acquire-release ordering (the writes this
-// thread made or observed come before it; later reads see the others').
-__device__ __forceinline__ uint32_t atomic_add_acq_rel(uint32_t* p, uint32_t v) {
-    uint32_t old;
-    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;\n" : "=r"(old) : "r"(smem_u32(p)), "r"(v) : "memory");
-    return old;
-}
-
 // The 16 x rows box at (x, y) of the tensor map into shared dst, completing on bar.
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint32_t x, uint32_t y, uint64_t* bar) {
     asm volatile(
@@ -182,15 +178,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
 
-// Shared-memory matrix descriptor, K-major, 32-byte rows with the 32-byte
-// swizzle, 8-row groups 256 bytes apart (both operands: the A slices the
-// decoder writes and the activation stages the TMA writes).  Fields: start
-// address >> 4 (bits 0-13), leading byte offset >> 4 (16-29, unused for
-// swizzled K-major), stride byte offset >> 4 (32-45), descriptor version 1
-// (46), layout 6 = 32-byte swizzle (61-63).
-__device__ __forceinline__ uint64_t desc_sw32(uint32_t saddr) {
-    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (uint64_t{1} << 16) | (uint64_t{256 >> 4} << 32) |
-           (uint64_t{1} << 46) | (uint64_t{6} << 61);
+// Shared-memory matrix descriptor, K-major, 128-byte rows with the
+// 128-byte swizzle, 8-row groups 1024 bytes apart (both operands, as the
+// TMA writes them).  The K = 16 steps inside a 64-column tile start 32
+// bytes apart.  Fields: start address >> 4 (bits 0-13), leading byte
+// offset >> 4 (16-29, unused for swizzled K-major), stride byte offset >> 4
+// (32-45), descriptor version 1 (46), layout 2 = 128-byte swizzle (61-63).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (uint64_t{1} << 16) | (uint64_t{1024 >> 4} << 32) |
+           (uint64_t{1} << 46) | (uint64_t{2} << 61);
 }
 
 // D[tmem] (+)= A * B^T: BF16 operands, float32 accumulator.
@@ -218,6 +214,17 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive_count(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+// Orders this thread's earlier generic-proxy writes to global memory before
+// later async-proxy reads of them (the TMA loads of the ring).
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;\n" ::: "memory");
+}
+
 // Waits for phase `parity` of bar, at most limit polls, giving up early
 // once another role has raised the abort flag.  A wait that runs out raises
 // the flag and AFX_DEV_TIMEOUT.
@@ -231,81 +238,69 @@ __device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, uint32_t
     return false;
 }
 
-// ---- the decoding warps: restored weights into the A ring -------------------------------
+// ---- the decoding warps: restored weights into the ring ---------------------------------
 
-// Byte offset of slice weight i (row i / 16, column i % 16) in a 32-byte
-// swizzled K-major slice: row r at r * 32, its 16-byte chunk c at
-// (c ^ ((r >> 2) & 1)) * 16 -- the layout the TMA writes for the
-// activations and the B descriptors name.
-__device__ __forceinline__ uint32_t tile_offset(uint32_t i) {
-    const uint32_t r = i >> 4, c = i & 15u;
-    return (r << 5) | ((((c >> 3) ^ (r >> 2)) & 1u) << 4) | ((c & 7u) << 1);
-}
-
-// Writes slice weights [i0, i1) into the A slot at `tile`: the stage byte
-// of slice weight i is stage[(i + d) mod 2^32] (d is the slice's first
-// position minus the stage's, which may be negative, and need not be a
-// multiple of 8) and its sign|mantissa byte sm[i] (sm points at the slice's
-// first weight).  Groups of 8 whole weights go out as 16-byte stores, one
-// group per lane at a time; the partial groups at either end (shared with
-// neighbouring ranges) weight by weight.
-__device__ __forceinline__ void tile_write(uint8_t* tile, const uint8_t* stage, uint32_t d, const uint8_t* sm,
-                                           uint32_t i0, uint32_t i1, int lane) {
+// Stores tile weights [i0, i1) at dst (the tile's first weight in the
+// ring): the stage byte of tile weight i is stage[(i + d) mod 2^32] (d is
+// the tile's first position minus the stage's, which may be negative, and
+// need not be a multiple of 8) and its sign|mantissa byte sm[i] (sm points
+// at the tile's first weight).  Groups of 8 whole weights go out as 16-byte
+// stores, one group per lane at a time; the partial groups at either end
+// (shared with neighbouring ranges) weight by weight.
+__device__ __forceinline__ void tile_store(uint16_t* dst, const uint8_t* stage, uint32_t d, const uint8_t* sm,
+                                            uint32_t i0, uint32_t i1, int lane) {
     const uint32_t f0 = (i0 + 7) & ~7u, f1 = i1 & ~7u;
     const uint32_t head_end = f0 < i1 ? f0 : i1;
     for (uint32_t i = i0 + lane; i < head_end; i += 32) {
         const uint32_t k = i + d;  // stage index, wrapped to 32 bits
         AFX_CHECK(k < static_cast<uint32_t>(kWarpStage) && i < kTileElems, kChkMergeStage);
-        *reinterpret_cast<uint16_t*>(tile + tile_offset(i)) = join1(stage[k], __ldg(sm + i));
+        dst[i] = join1(stage[k], __ldg(sm + i));
     }
     const uint32_t tail0 = f1 > f0 ? f1 : f0;
     for (uint32_t i = tail0 + lane; i < i1; i += 32) {
         const uint32_t k = i + d;
         AFX_CHECK(k < static_cast<uint32_t>(kWarpStage) && i < kTileElems, kChkMergeStage);
-        *reinterpret_cast<uint16_t*>(tile + tile_offset(i)) = join1(stage[k], __ldg(sm + i));
+        dst[i] = join1(stage[k], __ldg(sm + i));
     }
     // the stage bytes of a group start at any byte: three aligned words,
-    // shifted into place
-    const uint32_t sh = (d & 3u) * 8u;  // i is a multiple of 8, so k & 3 == d & 3
+    // shifted into place (i is a multiple of 8, so k & 3 == d & 3)
+    const uint32_t sh = (d & 3u) * 8u;
     for (uint32_t g = (f0 >> 3) + lane; g < (f1 >> 3); g += 32) {
         const uint32_t i = g << 3, k = i + d;
         AFX_CHECK(k + 8 <= static_cast<uint32_t>(kWarpStage) && i + 8 <= kTileElems, kChkMergeStage);
         const uint32_t* w = reinterpret_cast<const uint32_t*>(stage + (k & ~3u));
         const uint32_t w0 = w[0], w1 = w[1], w2 = (k & 3u) ? w[2] : 0u;
         const uint2 r8 = make_uint2(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh));
-        *reinterpret_cast<uint4*>(tile + tile_offset(i)) = join8(r8, __ldg(reinterpret_cast<const uint2*>(sm + i)));
+        *reinterpret_cast<uint4*>(dst + i) = join8(r8, __ldg(reinterpret_cast<const uint2*>(sm + i)));
     }
 }
 
 // The range [o0, o1) of the tensor's weights (positions in the container's
-// tile order), clipped to the item's [p_lo, p_hi), into the A ring: for each
-// tile met, wait until its slot is free, write, and count the weights in;
-// the warp that completes a tile's 8192 signals its full barrier.  Returns
-// false when a wait gave up.
-__device__ __forceinline__ bool ring_write(uint8_t* ring_a, PfCtl& ctl, const uint8_t* stage, uint64_t stage_o,
+// tile order), clipped to the item's [p_lo, p_hi), into the CTA's ring: for
+// each tile met, wait until its ring slot is free, store, and count the
+// weights into the slot's barrier (8192 complete it).  The item's tiles
+// have sequence numbers q_base + 0, 1, ...  Returns false when a wait gave
+// up.
+__device__ __forceinline__ bool ring_store(uint16_t* ring, PfCtl& ctl, const uint8_t* stage, uint64_t stage_o,
                                            const uint8_t* sm, uint64_t o0, uint64_t o1, uint64_t p_lo, uint64_t p_hi,
                                            uint32_t q_base, uint32_t wait_limit, int32_t* status, int lane) {
     const uint64_t c0 = o0 > p_lo ? o0 : p_lo, c1 = o1 < p_hi ? o1 : p_hi;
     if (c0 >= c1) return true;
     const uint32_t g0 = static_cast<uint32_t>((c0 - p_lo) / kTileElems), g1 = static_cast<uint32_t>((c1 - 1 - p_lo) / kTileElems);
     for (uint32_t g = g0; g <= g1; ++g) {
-        const uint32_t q = q_base + g, slot = q % kASlots;
-        if (!__all_sync(0xFFFFFFFFu, pf_wait(&ctl.a_empty[slot], ((q / kASlots) & 1u) ^ 1u, wait_limit, ctl, status)))
+        const uint32_t q = q_base + g, slot = q % kRingTiles;
+        if (!__all_sync(0xFFFFFFFFu,
+                        pf_wait(&ctl.ring_empty[slot], ((q / kRingTiles) & 1u) ^ 1u, wait_limit, ctl, status)))
             return false;
         const uint64_t t_lo = p_lo + static_cast<uint64_t>(g) * kTileElems;
         const uint64_t a = c0 > t_lo ? c0 : t_lo, b = c1 < t_lo + kTileElems ? c1 : t_lo + kTileElems;
         const uint32_t i0 = static_cast<uint32_t>(a - t_lo), i1 = static_cast<uint32_t>(b - t_lo);
         AFX_CHECK(i1 <= kTileElems && a - stage_o + (i1 - i0) <= static_cast<uint64_t>(kWarpStage), kChkMergeStage);
-        tile_write(ring_a + slot * kTileBytes, stage, static_cast<uint32_t>(t_lo - stage_o), sm + t_lo, i0, i1, lane);
-        fence_proxy_async_smem();  // the tensor cores read the tile through the async proxy
+        tile_store(ring + static_cast<size_t>(slot) * kTileElems, stage, static_cast<uint32_t>(t_lo - stage_o),
+                    sm + t_lo, i0, i1, lane);
+        fence_proxy_async_global();  // the TMA reads the tile through the async proxy
         __syncwarp();
-        if (lane == 0) {
-            const uint32_t old = atomic_add_acq_rel(&ctl.a_count[slot], i1 - i0);
-            if (old < kTileElems && old + (i1 - i0) >= kTileElems) {
-                atomic_add_acq_rel(&ctl.a_count[slot], 0u - kTileElems);
-                mbar_arrive(&ctl.a_full[slot]);
-            }
-        }
+        if (lane == 0) mbar_arrive_count(&ctl.ring_full[slot], i1 - i0);
     }
     return true;
 }
@@ -383,7 +378,7 @@ __device__ __forceinline__ bool add_published(PfCtl& ctl, uint32_t ord0, uint32_
 }
 
 // Restores the item's weights [p_lo, p_hi) of tensor t with decoding warp
-// `warp`: sub-tiles s_lo + warp, s_lo + warp + 16, ... of the sub-tiles that
+// `warp`: sub-tiles s_lo + warp, s_lo + warp + 26, ... of the sub-tiles that
 // hold them, staged one ahead by bulk copies as in the restore kernel.  The
 // item's sub-tiles have ordinals ord_base + (s - s_lo); each warp publishes
 // its sub-tile's code count right after the scan and places the sub-tile
@@ -392,7 +387,7 @@ __device__ __forceinline__ bool add_published(PfCtl& ctl, uint32_t ord0, uint32_
 // waited for first).
 __device__ bool pf_decode_item(const TabView& tv, WarpSlot& ws, uint8_t* wstream, uint32_t wstride,
                                const TensorArgs& t, uint64_t p_lo, uint64_t p_hi, uint32_t q_base, uint32_t& ord_base,
-                               uint8_t* ring_a, PfCtl& ctl, int warp, int lane, int32_t* status, uint32_t wait_limit,
+                               uint16_t* ring, PfCtl& ctl, int warp, int lane, int32_t* status, uint32_t wait_limit,
                                uint32_t& phases) {
     const uint32_t T = t.chunk_bytes;
     const uint32_t chunk_bits = 8u * T;
@@ -529,9 +524,9 @@ __device__ bool pf_decode_item(const TabView& tv, WarpSlot& ws, uint8_t* wstream
         }
         __syncwarp();
         // the sub-tile's weights go into the ring even when its stream was
-        // bad (the output is then unspecified), so that every slice completes
+        // bad (the output is then unspecified), so that every tile completes
         const uint64_t w0 = in_range ? o0 : 0, w1 = in_range ? o1 : 0;
-        if (!ring_write(ring_a, ctl, ws.stage, o0, t.sm, w0, w1, p_lo, p_hi, q_base, wait_limit, status, lane)) {
+        if (!ring_store(ring, ctl, ws.stage, o0, t.sm, w0, w1, p_lo, p_hi, q_base, wait_limit, status, lane)) {
             if (more) {  // the next sub-tile's copies are in flight: let them land
                 const bool drained = mbar_wait(&ws.bar[buf ^ 1], (phases >> (buf ^ 1)) & 1u, wait_limit);
                 phases ^= 1u << (buf ^ 1);
@@ -539,7 +534,7 @@ __device__ bool pf_decode_item(const TabView& tv, WarpSlot& ws, uint8_t* wstream
             }
             return false;
         }
-        // the next sub-tile (16 on) starts after this one and the 15 between
+        // the next sub-tile (26 on) starts after this one and the 25 between
         start = o1;
         from = ord + 1;
         count = kPfDecodeWarps - 1;
@@ -554,16 +549,16 @@ __device__ bool pf_decode_item(const TabView& tv, WarpSlot& ws, uint8_t* wstream
 // weights, interleaved across the decoding warps, joined with the constant
 // exponent (the warp's stage holds it at every index).
 __device__ bool pf_fill_item(const PrefillMatrix& pm, WarpSlot& ws, uint64_t p_lo, uint64_t p_hi, uint32_t q_base,
-                             uint8_t* ring_a, PfCtl& ctl, int warp, int lane, int32_t* status, uint32_t wait_limit) {
+                             uint16_t* ring, PfCtl& ctl, int warp, int lane, int32_t* status, uint32_t wait_limit) {
     constexpr uint32_t kPiece = 2048;
-    static_assert(kPiece <= static_cast<uint32_t>(kWarpStage), "a fill piece fits the stage");
+    static_assert(kPiece + 8 <= static_cast<uint32_t>(kWarpStage), "a fill piece fits the stage");
     const uint32_t f4 = ror8(pm.fill) * 0x01010101u;
-    for (uint32_t i = lane; i < kPiece / 4; i += 32) reinterpret_cast<uint32_t*>(ws.stage)[i] = f4;
+    for (uint32_t i = lane; i < (kPiece + 8) / 4; i += 32) reinterpret_cast<uint32_t*>(ws.stage)[i] = f4;
     if (lane == 0 && warp == 0 && p_lo == 0 && __ldg(pm.t.block_index) != pm.t.n) raise_status(status, AFX_DEV_BAD_BLOCK);
     __syncwarp();
     for (uint64_t o = p_lo + static_cast<uint64_t>(warp) * kPiece; o < p_hi; o += kPfDecodeWarps * kPiece) {
         const uint64_t e = o + kPiece < p_hi ? o + kPiece : p_hi;
-        if (!ring_write(ring_a, ctl, ws.stage, o, pm.t.sm, o, e, p_lo, p_hi, q_base, wait_limit, status, lane))
+        if (!ring_store(ring, ctl, ws.stage, o, pm.t.sm, o, e, p_lo, p_hi, q_base, wait_limit, status, lane))
             return false;
     }
     return true;
@@ -575,22 +570,26 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __gr
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const PfLayout L = pf_layout(a.tab_bytes, a.n_mma, a.max_chunk_bytes);
-    uint8_t* ring_a = smem + L.a;
+    uint8_t* stage_a = smem + L.a;
     uint8_t* ring_b = smem + L.b;
     PfCtl& ctl = *reinterpret_cast<PfCtl*>(smem + L.ctl);
     SharedW& sh = *reinterpret_cast<SharedW*>(smem + L.shw);
     uint8_t* tabr = smem + L.shw + sharedw_table_offset();
     WarpSlot* slots = reinterpret_cast<WarpSlot*>(smem + L.slots);
+    uint16_t* const ring = a.ring + static_cast<size_t>(blockIdx.x) * kRingTiles * kTileElems;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t it0 = a.cta_begin[blockIdx.x], it1 = a.cta_begin[blockIdx.x + 1];
     const uint32_t wait_limit = a.wait_limit ? a.wait_limit : kWaitLimit;
     int32_t* const status = a.status;
 
     if (threadIdx.x == 0) {
-        for (uint32_t i = 0; i < kASlots; ++i) {
+        for (uint32_t i = 0; i < kRingTiles; ++i) {
+            mbar_init_count(&ctl.ring_full[i], kTileElems);  // counts weights
+            mbar_init_count(&ctl.ring_empty[i], 1);
+        }
+        for (uint32_t i = 0; i < kAStages; ++i) {
             mbar_init_count(&ctl.a_full[i], 1);
             mbar_init_count(&ctl.a_empty[i], 1);
-            ctl.a_count[i] = 0;
         }
         for (uint32_t i = 0; i < L.b_slots; ++i) {
             mbar_init_count(&ctl.b_full[i], 1);
@@ -599,7 +598,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __gr
         for (uint32_t i = 0; i < kTotRing; ++i) ctl.totals[i] = 0;
         mbar_init_count(&ctl.acc_full, 1);
         mbar_init_count(&ctl.acc_empty, 4);
-        mbar_init_count(&ctl.drain, 1);
+        mbar_init_count(&ctl.drain_mma, 1);
         ctl.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
@@ -620,7 +619,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __gr
     const uint32_t tmem = ctl.tmem_base;
 
     if (warp < kPfDecodeWarps) {
-        // ---- restore the items' weights into the A ring
+        // ---- restore the items' weights into the ring
         WarpSlot& ws = slots[warp];
         uint8_t* wstream = smem + L.streams + static_cast<size_t>(warp) * 2 * L.wstride;
         TabView tv;
@@ -651,19 +650,42 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __gr
             const uint64_t p_hi = p_lo + static_cast<uint64_t>(pm.k_tiles) * kTileElems;
             if (!*reinterpret_cast<volatile int32_t*>(&ctl.abort_flag)) {
                 if (pm.single)
-                    pf_fill_item(pm, ws, p_lo, p_hi, q_base, ring_a, ctl, warp, lane, status, wait_limit);
+                    pf_fill_item(pm, ws, p_lo, p_hi, q_base, ring, ctl, warp, lane, status, wait_limit);
                 else
-                    pf_decode_item(tv, ws, wstream, L.wstride, pm.t, p_lo, p_hi, q_base, ord_base, ring_a, ctl, warp,
+                    pf_decode_item(tv, ws, wstream, L.wstride, pm.t, p_lo, p_hi, q_base, ord_base, ring, ctl, warp,
                                    lane, status, wait_limit, phases);
             }
             q_base += pm.k_tiles;
         }
     } else if (warp == kPfProducerWarp) {
-        // ---- token vectors into the B ring, in the order the MMAs take them
         if (lane == 0) {
+            // ---- complete ring tiles into the A stages, in sequence
+            uint32_t q = 0;
+            bool ok = true;
+            for (uint32_t it = it0; it < it1 && ok; ++it) {
+                const PrefillMatrix& pm = a.m[a.items[it] >> 28];
+                for (uint32_t g = 0; g < pm.k_tiles; ++g, ++q) {
+                    const uint32_t slot = q % kRingTiles, st = q % kAStages;
+                    if (!pf_wait(&ctl.ring_full[slot], (q / kRingTiles) & 1u, wait_limit, ctl, status) ||
+                        !pf_wait(&ctl.a_empty[st], ((q / kAStages) & 1u) ^ 1u, wait_limit, ctl, status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(&ctl.a_full[st], kTileBytes);
+                    tma_load_2d(stage_a + st * kTileBytes, &a.ring_map, 0,
+                                (blockIdx.x * kRingTiles + slot) * kTileRows, &ctl.a_full[st]);
+                }
+            }
+            if (!ok) {  // the loads still in flight land before the CTA exits
+                for (uint32_t j = q > kAStages ? q - kAStages : 0; j < q; ++j)
+                    if (!mbar_wait(&ctl.a_full[j % kAStages], (j / kAStages) & 1u, wait_limit))
+                        raise_status(status, AFX_DEV_UNDRAINED);
+            }
+        } else if (lane == 16) {
+            // ---- token vectors into the B ring, in the order the MMAs take them
             uint32_t bseq = 0;
             bool ok = true;
-            const uint32_t stage_bytes = a.n_mma * kSliceK * 2;
+            const uint32_t stage_bytes = a.n_mma * kTileCols * 2;
             for (uint32_t it = it0; it < it1 && ok; ++it) {
                 const uint32_t item = a.items[it];
                 const uint32_t mi = item >> 28, pass = (item >> 18) & 0x3FFu;
@@ -677,11 +699,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __gr
                             break;
                         }
                         mbar_expect_tx(&ctl.b_full[b], stage_bytes);
-                        tma_load_2d(ring_b + b * L.b_stage, &a.tmap[mi], g * kSliceK, y0 + h * a.n_mma, &ctl.b_full[b]);
+                        tma_load_2d(ring_b + b * L.b_stage, &a.tmap[mi], g * kTileCols, y0 + h * a.n_mma, &ctl.b_full[b]);
                         ++bseq;
                     }
             }
-            if (!ok) {  // the loads still in flight land before the CTA exits
+            if (!ok) {
                 for (uint32_t j = bseq > L.b_slots ? bseq - L.b_slots : 0; j < bseq; ++j)
                     if (!mbar_wait(&ctl.b_full[j % L.b_slots], (j / L.b_slots) & 1u, wait_limit))
                         raise_status(status, AFX_DEV_UNDRAINED);
@@ -701,13 +723,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __gr
                     tc_fence_after();
                 }
                 for (uint32_t g = 0; g < pm.k_tiles && ok; ++g, ++q) {
-                    const uint32_t slot = q % kASlots;
-                    if (!pf_wait(&ctl.a_full[slot], (q / kASlots) & 1u, wait_limit, ctl, status)) {
+                    const uint32_t st = q % kAStages;
+                    if (!pf_wait(&ctl.a_full[st], (q / kAStages) & 1u, wait_limit, ctl, status)) {
                         ok = false;
                         break;
                     }
+                    mbar_arrive(&ctl.ring_empty[q % kRingTiles]);  // the TMA has read the tile: its slot is free
                     tc_fence_after();
-                    const uint64_t a_desc = desc_sw32(smem_u32(ring_a + slot * kTileBytes));
+                    const uint32_t a_addr = smem_u32(stage_a + st * kTileBytes);
                     for (uint32_t h = 0; h < a.halves; ++h) {
                         const uint32_t b = bseq % L.b_slots;
                         if (!pf_wait(&ctl.b_full[b], (bseq / L.b_slots) & 1u, wait_limit, ctl, status)) {
@@ -715,11 +738,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __gr
                             break;
                         }
                         tc_fence_after();
-                        tc_mma(tmem + h * a.n_mma, a_desc, desc_sw32(smem_u32(ring_b + b * L.b_stage)), idesc, g != 0);
+                        const uint32_t b_addr = smem_u32(ring_b + b * L.b_stage);
+#pragma unroll
+                        for (uint32_t kk = 0; kk < kTileCols / kSliceK; ++kk)
+                            tc_mma(tmem + h * a.n_mma, desc_sw128(a_addr + kk * 32), desc_sw128(b_addr + kk * 32), idesc,
+                                   (g | kk) != 0);
                         tc_commit(&ctl.b_empty[b]);
                         ++bseq;
                     }
-                    if (ok) tc_commit(&ctl.a_empty[slot]);
+                    if (ok) tc_commit(&ctl.a_empty[st]);
                 }
                 if (ok) {
                     tc_commit(&ctl.acc_full);
@@ -727,8 +754,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __gr
                 }
             }
             if (!ok) {  // the products in flight finish before the tensor memory is freed
-                tc_commit(&ctl.drain);
-                if (!mbar_wait(&ctl.drain, 0, wait_limit)) raise_status(status, AFX_DEV_UNDRAINED);
+                tc_commit(&ctl.drain_mma);
+                if (!mbar_wait(&ctl.drain_mma, 0, wait_limit)) raise_status(status, AFX_DEV_UNDRAINED);
             }
         }
         __syncwarp();
@@ -770,6 +797,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __gr
 
 }  // namespace afx
 
+
 // ---- host side --------------------------------------------------------------------------
 
 namespace afx {
@@ -801,18 +829,20 @@ EncodeTiledFn encode_tiled() {
     return fn;
 }
 
-// X [n_tokens][cols] BF16 in device memory, read as boxes of 16 columns x
-// n_mma tokens with the 32-byte swizzle the B descriptors name; rows past
-// n_tokens read as zeros.
-afx_status make_x_map(CUtensorMap* map, const uint16_t* x, uint32_t cols, uint32_t n_tokens, uint32_t n_mma) {
+// A row-major BF16 matrix [rows][cols] in device memory, read as boxes of
+// 64 columns x box_rows rows with the 128-byte swizzle the MMA descriptors
+// name; rows past the end read as zeros.  X [n_tokens][cols] (box: the
+// tokens of one accumulator) and the rings [CTAs * 16 * 128][64] (box: a
+// tile).
+afx_status make_map(CUtensorMap* map, const uint16_t* x, uint32_t cols, uint64_t rows, uint32_t box_rows) {
     const EncodeTiledFn enc = encode_tiled();
     if (!enc) return afx_fail(AFX_E_CUDA, "cuTensorMapEncodeTiled is not available from the driver", 0);
-    const cuuint64_t dims[2] = {cols, n_tokens};
+    const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-    const cuuint32_t box[2] = {kSliceK, n_mma};
+    const cuuint32_t box[2] = {kTileCols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         char msg[96];
@@ -837,18 +867,15 @@ uint32_t pow2_at_least(uint32_t v) {
     return p;
 }
 
-// Tokens per MMA and halves per pass for n_tokens: one pass of up to 512
-// tokens (two halves past 256), N a multiple of 16; more tokens take passes
-// of 512.
+// Tokens per MMA and accumulators per pass for n_tokens: one pass of up to
+// 512 tokens in up to four accumulators of at most 128 tokens each, N a
+// multiple of 16; more tokens take passes of 512.
 void token_split(uint32_t n_tokens, uint32_t* n_mma, uint32_t* halves) {
-    if (n_tokens <= kMaxHalfTokens) {
-        *halves = 1;
-        *n_mma = round_up(n_tokens, 16);
-    } else if (n_tokens <= kMaxPassTokens) {
-        *halves = 2;
-        *n_mma = round_up((n_tokens + 1) / 2, 16);
+    if (n_tokens <= kMaxPassTokens) {
+        *halves = (n_tokens + kMaxHalfTokens - 1) / kMaxHalfTokens;
+        *n_mma = round_up((n_tokens + *halves - 1) / *halves, 16);
     } else {
-        *halves = 2;
+        *halves = kMaxHalves;
         *n_mma = kMaxHalfTokens;
     }
 }
@@ -858,11 +885,9 @@ void token_split(uint32_t n_tokens, uint32_t* n_mma, uint32_t* halves) {
 // k-tiles); each CTA takes its items in code order, so that consecutive
 // items share a matrix's decode tables.
 afx_status launch_items(PrefillArgs& pa, const std::vector<uint32_t>& codes, size_t begin, size_t end, size_t smem,
-                        cudaStream_t s) {
-    const int sms = sm_count();
-    if (sms <= 0) return afx_fail(AFX_E_CUDA, "cannot query the SM count", 0);
+                        uint32_t max_ctas, cudaStream_t s) {
     const size_t n = end - begin;
-    const uint32_t G = static_cast<uint32_t>(std::min<size_t>({n, static_cast<size_t>(sms), size_t(kPfMaxCtas)}));
+    const uint32_t G = static_cast<uint32_t>(std::min<size_t>(n, max_ctas));
     std::vector<uint32_t> order(n);
     for (size_t i = 0; i < n; ++i) order[i] = codes[begin + i];
     std::stable_sort(order.begin(), order.end(), [&](uint32_t x, uint32_t y) {
@@ -900,7 +925,7 @@ using namespace afx;
 extern "C" afx_status afx_tile_order(const uint16_t* w, uint32_t rows, uint32_t cols, uint16_t* out) {
     if (!w || !out) return afx_fail(AFX_E_ARG, "null pointer", 0);
     if (rows == 0 || cols == 0 || rows % kTileRows || cols % kTileCols)
-        return afx_fail(AFX_E_ARG, "rows must be a multiple of 128 and cols a multiple of 16", 0);
+        return afx_fail(AFX_E_ARG, "rows must be a multiple of 128 and cols a multiple of 64", 0);
     const uint64_t kt = cols / kTileCols;
     for (uint64_t m = 0; m < rows / kTileRows; ++m)
         for (uint64_t g = 0; g < kt; ++g) {
@@ -912,13 +937,32 @@ extern "C" afx_status afx_tile_order(const uint16_t* w, uint32_t rows, uint32_t 
     return AFX_OK;
 }
 
+extern "C" afx_status afx_prefill_fused_workspace(uint64_t* bytes) {
+    if (!bytes) return afx_fail(AFX_E_ARG, "null pointer", 0);
+    const int sms = sm_count();
+    if (sms <= 0) return afx_fail(AFX_E_CUDA, "cannot query the SM count", 0);
+    *bytes = static_cast<uint64_t>(std::min(sms, kPfMaxCtas)) * kRingTiles * kTileBytes;
+    return AFX_OK;
+}
+
 extern "C" afx_status afx_prefill_fused_batch(const afx_desc* descs, const void* const* containers,
                                               const uint32_t* rows, const uint32_t* cols, const uint16_t* const* xs,
                                               uint32_t n_tokens, float* const* ys, uint32_t count,
-                                              afx_stream_t stream, int32_t* status) {
+                                              void* workspace, uint64_t workspace_bytes, afx_stream_t stream,
+                                              int32_t* status) {
     if (count == 0) return AFX_OK;
     if (!descs || !containers || !rows || !cols || !xs || !ys) return afx_fail(AFX_E_ARG, "null array", 0);
     if (n_tokens == 0) return afx_fail(AFX_E_ARG, "n_tokens must be at least 1", 0);
+    // the CTAs' rings: as many CTAs as the workspace holds rings, at most one per SM
+    const int sms = sm_count();
+    if (sms <= 0) return afx_fail(AFX_E_CUDA, "cannot query the SM count", 0);
+    const uint64_t ring_bytes = static_cast<uint64_t>(kRingTiles) * kTileBytes;
+    const uint32_t max_ctas = static_cast<uint32_t>(
+        std::min<uint64_t>({workspace ? workspace_bytes / ring_bytes : 0, static_cast<uint64_t>(sms),
+                            static_cast<uint64_t>(kPfMaxCtas)}));
+    if (max_ctas == 0) return afx_fail(AFX_E_NOSPACE, "the workspace must hold at least one ring (256 KB)", 0);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return afx_fail(AFX_E_ARG, "the workspace must be 256-byte aligned", 0);
+    if (!device_memory(workspace)) return afx_fail(AFX_E_ARG, "the workspace must be in device memory", 0);
     uint32_t n_mma = 0, halves = 0;
     token_split(n_tokens, &n_mma, &halves);
     const uint32_t pass_tokens = n_mma * halves;
@@ -939,6 +983,11 @@ extern "C" afx_status afx_prefill_fused_batch(const afx_desc* descs, const void*
         pa->pass_tokens = pass_tokens;
         pa->tmem_cols = pow2_at_least(pass_tokens);
         pa->status = status;
+        pa->ring = static_cast<uint16_t*>(workspace);
+        const afx_status rst =
+            make_map(&pa->ring_map, static_cast<const uint16_t*>(workspace), kTileCols,
+                     static_cast<uint64_t>(max_ctas) * kRingTiles * kTileRows, kTileRows);
+        if (rst != AFX_OK) return rst;
         uint32_t max_T = 4;
         std::vector<uint32_t> codes;
         for (uint32_t k = 0; k < cnt; ++k) {
@@ -947,7 +996,7 @@ extern "C" afx_status afx_prefill_fused_batch(const afx_desc* descs, const void*
             if (afx_check_desc(&d) != AFX_OK) return afx_fail(AFX_E_FORMAT, "invalid container description", 0);
             if (d.format != AFX_FMT_BF16) return afx_fail(AFX_E_ARG, "the fused prefill product takes BF16 containers", 0);
             if (rows[i] == 0 || cols[i] == 0 || rows[i] % kTileRows || cols[i] % kTileCols)
-                return afx_fail(AFX_E_ARG, "rows must be a multiple of 128 and cols a multiple of 16", 0);
+                return afx_fail(AFX_E_ARG, "rows must be a multiple of 128 and cols a multiple of 64", 0);
             if (static_cast<uint64_t>(rows[i]) * cols[i] != d.n) return afx_fail(AFX_E_ARG, "rows * cols != n", 0);
             if (rows[i] / kTileRows > (1u << 18)) return afx_fail(AFX_E_ARG, "too many rows", 0);
             if (d.nsym >= 2 && d.block_chunks != static_cast<uint32_t>(kThreads))
@@ -966,7 +1015,7 @@ extern "C" afx_status afx_prefill_fused_batch(const afx_desc* descs, const void*
             pm.single = d.nsym == 1 ? 1u : 0u;
             pm.fill = d.fill;
             max_T = std::max(max_T, d.chunk_bytes);
-            const afx_status mst = make_x_map(&pa->tmap[k], xs[i], cols[i], n_tokens, n_mma);
+            const afx_status mst = make_map(&pa->tmap[k], xs[i], cols[i], n_tokens, n_mma);
             if (mst != AFX_OK) return mst;
             for (uint32_t p = 0; p < passes; ++p)
                 for (uint32_t mt = 0; mt < rows[i] / kTileRows; ++mt) codes.push_back(k << 28 | p << 18 | mt);
@@ -993,7 +1042,7 @@ extern "C" afx_status afx_prefill_fused_batch(const afx_desc* descs, const void*
         const afx_status pst = prepare_kernel(reinterpret_cast<const void*>(prefill_fused_kernel), kPfThreads, smem, &per_sm);
         if (pst != AFX_OK) return pst;
         for (size_t b = 0; b < codes.size(); b += kPfMaxItems) {
-            const afx_status lst = launch_items(*pa, codes, b, std::min(codes.size(), b + kPfMaxItems), smem, s);
+            const afx_status lst = launch_items(*pa, codes, b, std::min(codes.size(), b + kPfMaxItems), smem, max_ctas, s);
             if (lst != AFX_OK) return lst;
         }
     }
@@ -1001,10 +1050,11 @@ extern "C" afx_status afx_prefill_fused_batch(const afx_desc* descs, const void*
 }
 
 extern "C" afx_status afx_prefill_fused(const afx_desc* desc, const void* container, uint32_t rows, uint32_t cols,
-                                        const uint16_t* x, uint32_t n_tokens, float* y, afx_stream_t stream,
-                                        int32_t* status) {
+                                        const uint16_t* x, uint32_t n_tokens, float* y, void* workspace,
+                                        uint64_t workspace_bytes, afx_stream_t stream, int32_t* status) {
     if (!desc) return afx_fail(AFX_E_ARG, "null description", 0);
-    return afx_prefill_fused_batch(desc, &container, &rows, &cols, &x, n_tokens, &y, 1, stream, status);
+    return afx_prefill_fused_batch(desc, &container, &rows, &cols, &x, n_tokens, &y, 1, workspace, workspace_bytes,
+                                   stream, status);
 }
 
 // Bits of the bounds checks that fired in this module (bounds-checked
