@@ -438,8 +438,11 @@ afx_status afx_prefill_fused_workspace(uint64_t* bytes);
  * [n_tokens][rows], overwritten.  Products of BF16 pairs are exact and are
  * summed in float32 by the tensor cores, in a fixed order (y_dev is
  * bitwise reproducible).  rows a multiple of 128, cols a multiple of 64,
- * n_tokens >= 1 (up to 512 per pass over the weights; more tokens restore
- * the weights once per 512).  The restored weights go through the
+ * 1 <= n_tokens <= 262144 (up to 512 per pass over the weights; more
+ * tokens restore the weights once per 512).  For balance across the SMs a
+ * 128-row band may be split in two along the columns, its two partial sums
+ * added into y_dev after a memset on the stream (two float32 additions to
+ * zero give the same bits in either order).  The restored weights go through the
  * workspace (a ring of 16 tiles of 16 KB per CTA, written and read back
  * within microseconds, so it stays in L2; no restored matrix is written
  * out): workspace_dev, 256-byte aligned, of workspace_bytes (see

@@ -90,7 +90,29 @@ struct PrefillMatrix {
     uint32_t fill;      // that exponent
 };
 
-// An item: matrix << 28 | pass << 18 | m-tile.
+// An item: matrix << 28 | pass << 19 | part << 17 | m-tile.  part 0 is the
+// whole m-tile, 1 and 2 its first and second half of the tiles (an m-tile
+// split in two along K for balance; each half's products are added into a
+// zeroed Y, and two float32 partial sums added to zero give the same bits in
+// either order).
+struct ItemInfo {
+    uint32_t mi, pass, part, mt;
+};
+
+__host__ __device__ inline ItemInfo item_info(uint32_t code) {
+    return ItemInfo{code >> 28, (code >> 19) & 0x1FFu, (code >> 17) & 3u, code & 0x1FFFFu};
+}
+
+__host__ __device__ inline uint32_t item_code(uint32_t mi, uint32_t pass, uint32_t part, uint32_t mt) {
+    return mi << 28 | pass << 19 | part << 17 | mt;
+}
+
+// The item's tiles [kb, ke) of its m-tile's k_tiles.
+__host__ __device__ inline void item_tiles(uint32_t part, uint32_t k_tiles, uint32_t* kb, uint32_t* ke) {
+    *kb = part == 2 ? k_tiles / 2 : 0;
+    *ke = part == 1 ? k_tiles / 2 : k_tiles;
+}
+
 struct PrefillArgs {
     CUtensorMap tmap[kMaxTensors];  // X of each matrix: [n_tokens][cols] BF16, box 64 x n_mma, 128-byte swizzle
     CUtensorMap ring_map;           // the rings: [CTAs * 16 * 128][64] BF16, box 64 x 128, 128-byte swizzle
@@ -635,9 +657,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __gr
         uint32_t phases = 0, q_base = 0, ord_base = 0;
         int built = -1;
         for (uint32_t it = it0; it < it1; ++it) {
-            const uint32_t item = a.items[it];
-            const uint32_t mi = item >> 28, mt = item & 0x3FFFFu;
+            const ItemInfo ii = item_info(a.items[it]);
+            const uint32_t mi = ii.mi;
             const PrefillMatrix& pm = a.m[mi];
+            uint32_t kb, ke;
+            item_tiles(ii.part, pm.k_tiles, &kb, &ke);
             if (!pm.single && static_cast<int>(mi) != built) {
                 // every decoding warp is done with the previous tables; all
                 // build, or all skip once a wait anywhere has given up
@@ -646,8 +670,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __gr
                     build_tables_w(sh, tabr, pm.t.tab, threadIdx.x, kPfDecodeWarps * 32, DecodeSync{});
                 built = static_cast<int>(mi);
             }
-            const uint64_t p_lo = static_cast<uint64_t>(mt) * pm.k_tiles * kTileElems;
-            const uint64_t p_hi = p_lo + static_cast<uint64_t>(pm.k_tiles) * kTileElems;
+            const uint64_t p_lo = (static_cast<uint64_t>(ii.mt) * pm.k_tiles + kb) * kTileElems;
+            const uint64_t p_hi = p_lo + static_cast<uint64_t>(ke - kb) * kTileElems;
             if (!*reinterpret_cast<volatile int32_t*>(&ctl.abort_flag)) {
                 if (pm.single)
                     pf_fill_item(pm, ws, p_lo, p_hi, q_base, ring, ctl, warp, lane, status, wait_limit);
@@ -655,7 +679,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __gr
                     pf_decode_item(tv, ws, wstream, L.wstride, pm.t, p_lo, p_hi, q_base, ord_base, ring, ctl, warp,
                                    lane, status, wait_limit, phases);
             }
-            q_base += pm.k_tiles;
+            q_base += ke - kb;
         }
     } else if (warp == kPfProducerWarp) {
         if (lane == 0) {
@@ -663,8 +687,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __gr
             uint32_t q = 0;
             bool ok = true;
             for (uint32_t it = it0; it < it1 && ok; ++it) {
-                const PrefillMatrix& pm = a.m[a.items[it] >> 28];
-                for (uint32_t g = 0; g < pm.k_tiles; ++g, ++q) {
+                const ItemInfo ii = item_info(a.items[it]);
+                uint32_t kb, ke;
+                item_tiles(ii.part, a.m[ii.mi].k_tiles, &kb, &ke);
+                for (uint32_t g = kb; g < ke; ++g, ++q) {
                     const uint32_t slot = q % kRingTiles, st = q % kAStages;
                     if (!pf_wait(&ctl.ring_full[slot], (q / kRingTiles) & 1u, wait_limit, ctl, status) ||
                         !pf_wait(&ctl.a_empty[st], ((q / kAStages) & 1u) ^ 1u, wait_limit, ctl, status)) {
@@ -687,11 +713,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __gr
             bool ok = true;
             const uint32_t stage_bytes = a.n_mma * kTileCols * 2;
             for (uint32_t it = it0; it < it1 && ok; ++it) {
-                const uint32_t item = a.items[it];
-                const uint32_t mi = item >> 28, pass = (item >> 18) & 0x3FFu;
-                const PrefillMatrix& pm = a.m[mi];
-                const uint32_t y0 = pass * a.pass_tokens;
-                for (uint32_t g = 0; g < pm.k_tiles && ok; ++g)
+                const ItemInfo ii = item_info(a.items[it]);
+                const uint32_t mi = ii.mi;
+                uint32_t kb, ke;
+                item_tiles(ii.part, a.m[mi].k_tiles, &kb, &ke);
+                const uint32_t y0 = ii.pass * a.pass_tokens;
+                for (uint32_t g = kb; g < ke && ok; ++g)
                     for (uint32_t h = 0; h < a.halves; ++h) {
                         const uint32_t b = bseq % L.b_slots;
                         if (!pf_wait(&ctl.b_empty[b], ((bseq / L.b_slots) & 1u) ^ 1u, wait_limit, ctl, status)) {
@@ -717,12 +744,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __gr
             uint32_t q = 0, bseq = 0, n_item = 0;
             bool ok = true;
             for (uint32_t it = it0; it < it1 && ok; ++it) {
-                const PrefillMatrix& pm = a.m[a.items[it] >> 28];
+                const ItemInfo ii = item_info(a.items[it]);
+                uint32_t kb, ke;
+                item_tiles(ii.part, a.m[ii.mi].k_tiles, &kb, &ke);
                 if (n_item > 0) {  // the epilogue has read the previous item's accumulator
                     ok = pf_wait(&ctl.acc_empty, (n_item - 1) & 1u, wait_limit, ctl, status);
                     tc_fence_after();
                 }
-                for (uint32_t g = 0; g < pm.k_tiles && ok; ++g, ++q) {
+                for (uint32_t g = 0; g < ke - kb && ok; ++g, ++q) {
                     const uint32_t st = q % kAStages;
                     if (!pf_wait(&ctl.a_full[st], (q / kAStages) & 1u, wait_limit, ctl, status)) {
                         ok = false;
@@ -764,21 +793,26 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __gr
         const uint32_t quarter = static_cast<uint32_t>(warp) & 3u;
         uint32_t n_item = 0;
         for (uint32_t it = it0; it < it1; ++it) {
-            const uint32_t item = a.items[it];
-            const uint32_t mi = item >> 28, pass = (item >> 18) & 0x3FFu, mt = item & 0x3FFFFu;
-            const PrefillMatrix& pm = a.m[mi];
+            const ItemInfo ii = item_info(a.items[it]);
+            const PrefillMatrix& pm = a.m[ii.mi];
             if (!__all_sync(0xFFFFFFFFu, pf_wait(&ctl.acc_full, n_item & 1u, wait_limit, ctl, status))) break;
             tc_fence_after();
-            const uint32_t y0 = pass * a.pass_tokens;
+            const uint32_t y0 = ii.pass * a.pass_tokens;
             const uint32_t valid = min(a.pass_tokens, a.n_tokens - y0);
             const uint64_t rows = pm.t.rows;
-            float* y = pm.t.y + static_cast<uint64_t>(y0) * rows + static_cast<uint64_t>(mt) * kTileRows + quarter * 32 + lane;
+            float* y = pm.t.y + static_cast<uint64_t>(y0) * rows + static_cast<uint64_t>(ii.mt) * kTileRows + quarter * 32 + lane;
             for (uint32_t c0 = 0; c0 < valid; c0 += 16) {
                 uint32_t v[16];
                 tc_ld16(tmem + ((quarter * 32u) << 16) + c0, v);
+                if (ii.part == 0) {
 #pragma unroll
-                for (uint32_t j = 0; j < 16; ++j)
-                    if (c0 + j < valid) y[static_cast<uint64_t>(c0 + j) * rows] = __uint_as_float(v[j]);
+                    for (uint32_t j = 0; j < 16; ++j)
+                        if (c0 + j < valid) y[static_cast<uint64_t>(c0 + j) * rows] = __uint_as_float(v[j]);
+                } else {  // one of two halves of the sum: added into the zeroed Y
+#pragma unroll
+                    for (uint32_t j = 0; j < 16; ++j)
+                        if (c0 + j < valid) atomicAdd(y + static_cast<uint64_t>(c0 + j) * rows, __uint_as_float(v[j]));
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -890,9 +924,13 @@ afx_status launch_items(PrefillArgs& pa, const std::vector<uint32_t>& codes, siz
     const uint32_t G = static_cast<uint32_t>(std::min<size_t>(n, max_ctas));
     std::vector<uint32_t> order(n);
     for (size_t i = 0; i < n; ++i) order[i] = codes[begin + i];
-    std::stable_sort(order.begin(), order.end(), [&](uint32_t x, uint32_t y) {
-        return pa.m[x >> 28].k_tiles > pa.m[y >> 28].k_tiles;
-    });
+    auto tiles_of = [&](uint32_t code) {
+        const ItemInfo ii = item_info(code);
+        uint32_t kb, ke;
+        item_tiles(ii.part, pa.m[ii.mi].k_tiles, &kb, &ke);
+        return ke - kb;
+    };
+    std::stable_sort(order.begin(), order.end(), [&](uint32_t x, uint32_t y) { return tiles_of(x) > tiles_of(y); });
     using Load = std::pair<uint64_t, uint32_t>;
     std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
     for (uint32_t c = 0; c < G; ++c) heap.push({0, c});
@@ -901,7 +939,7 @@ afx_status launch_items(PrefillArgs& pa, const std::vector<uint32_t>& codes, siz
         Load l = heap.top();
         heap.pop();
         per[l.second].push_back(code);
-        l.first += pa.m[code >> 28].k_tiles;
+        l.first += tiles_of(code);
         heap.push(l);
     }
     uint32_t k = 0;
@@ -967,7 +1005,7 @@ extern "C" afx_status afx_prefill_fused_batch(const afx_desc* descs, const void*
     token_split(n_tokens, &n_mma, &halves);
     const uint32_t pass_tokens = n_mma * halves;
     const uint32_t passes = (n_tokens + pass_tokens - 1) / pass_tokens;
-    if (passes > 1024) return afx_fail(AFX_E_ARG, "n_tokens must be at most 524288", 0);
+    if (passes > 512) return afx_fail(AFX_E_ARG, "n_tokens must be at most 262144", 0);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     int dev = -1, optin = 0;
     AFX_CUDA_TRY(cudaGetDevice(&dev), "cudaGetDevice");
@@ -998,7 +1036,7 @@ extern "C" afx_status afx_prefill_fused_batch(const afx_desc* descs, const void*
             if (rows[i] == 0 || cols[i] == 0 || rows[i] % kTileRows || cols[i] % kTileCols)
                 return afx_fail(AFX_E_ARG, "rows must be a multiple of 128 and cols a multiple of 64", 0);
             if (static_cast<uint64_t>(rows[i]) * cols[i] != d.n) return afx_fail(AFX_E_ARG, "rows * cols != n", 0);
-            if (rows[i] / kTileRows > (1u << 18)) return afx_fail(AFX_E_ARG, "too many rows", 0);
+            if (rows[i] / kTileRows > (1u << 17)) return afx_fail(AFX_E_ARG, "too many rows", 0);
             if (d.nsym >= 2 && d.block_chunks != static_cast<uint32_t>(kThreads))
                 return afx_fail(AFX_E_FORMAT, "the decoder needs 512 chunks per block", 0);
             if (!containers[i] || !ys[i] || !xs[i]) return afx_fail(AFX_E_ARG, "null pointer", 0);
@@ -1017,8 +1055,30 @@ extern "C" afx_status afx_prefill_fused_batch(const afx_desc* descs, const void*
             max_T = std::max(max_T, d.chunk_bytes);
             const afx_status mst = make_map(&pa->tmap[k], xs[i], cols[i], n_tokens, n_mma);
             if (mst != AFX_OK) return mst;
+        }
+        // items: every m-tile for every pass; an m-tile larger than half a
+        // CTA's share of all the tiles is split in two along K, and its
+        // matrix's Y is zeroed first (the two halves are added into it)
+        const int sms_now = sm_count();
+        uint64_t all_tiles = 0;
+        for (uint32_t k = 0; k < cnt; ++k)
+            all_tiles += static_cast<uint64_t>(pa->m[k].t.rows / kTileRows) * pa->m[k].k_tiles * passes;
+        const uint64_t share = all_tiles / std::max<uint64_t>(1, std::min<uint64_t>(max_ctas, sms_now > 0 ? sms_now : 1));
+        for (uint32_t k = 0; k < cnt; ++k) {
+            const PrefillMatrix& pm = pa->m[k];
+            const bool split = pm.k_tiles >= 2 && 2ull * pm.k_tiles > share;
+            if (split)
+                AFX_CUDA_TRY(cudaMemsetAsync(pm.t.y, 0, static_cast<size_t>(n_tokens) * pm.t.rows * sizeof(float), s),
+                             "cudaMemsetAsync");
             for (uint32_t p = 0; p < passes; ++p)
-                for (uint32_t mt = 0; mt < rows[i] / kTileRows; ++mt) codes.push_back(k << 28 | p << 18 | mt);
+                for (uint32_t mt = 0; mt < pm.t.rows / kTileRows; ++mt) {
+                    if (split) {
+                        codes.push_back(item_code(k, p, 1, mt));
+                        codes.push_back(item_code(k, p, 2, mt));
+                    } else {
+                        codes.push_back(item_code(k, p, 0, mt));
+                    }
+                }
         }
         pa->max_chunk_bytes = max_T;
         // decode tables: the state table where it fits beside the rings and
