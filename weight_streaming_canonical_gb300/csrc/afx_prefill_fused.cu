@@ -80,6 +80,7 @@ constexpr int kPfMaxItems = 2048;
 constexpr int kPfMaxCtas = 256;
 
 static_assert(kPfThreads <= 1024, "one CTA of at most 1024 threads");
+static_assert(kTileCols / kSliceK == 4, "four K = 16 MMAs per 64-column tile");
 static_assert(kPfEpiWarp0 % 4 == 0, "the epilogue warps cover the four lane quarters of tensor memory in order");
 static_assert(kPfDecodeWarps - 1 <= 32 && kTotRing >= 4 * kPfDecodeWarps, "look-back reads one count per lane");
 
@@ -285,15 +286,30 @@ __device__ __forceinline__ void tile_store(uint16_t* dst, const uint8_t* stage, 
         dst[i] = join1(stage[k], __ldg(sm + i));
     }
     // the stage bytes of a group start at any byte: three aligned words,
-    // shifted into place (i is a multiple of 8, so k & 3 == d & 3)
+    // shifted into place (i is a multiple of 8, so k & 3 == d & 3).  A lane
+    // takes four groups at a time and loads their sign|mantissa bytes first,
+    // so the four loads are in flight together
     const uint32_t sh = (d & 3u) * 8u;
-    for (uint32_t g = (f0 >> 3) + lane; g < (f1 >> 3); g += 32) {
-        const uint32_t i = g << 3, k = i + d;
-        AFX_CHECK(k + 8 <= static_cast<uint32_t>(kWarpStage) && i + 8 <= kTileElems, kChkMergeStage);
-        const uint32_t* w = reinterpret_cast<const uint32_t*>(stage + (k & ~3u));
-        const uint32_t w0 = w[0], w1 = w[1], w2 = (k & 3u) ? w[2] : 0u;
-        const uint2 r8 = make_uint2(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh));
-        *reinterpret_cast<uint4*>(dst + i) = join8(r8, __ldg(reinterpret_cast<const uint2*>(sm + i)));
+    const uint32_t gend = f1 >> 3;
+    for (uint32_t g0 = (f0 >> 3) + lane; g0 < gend; g0 += 128) {
+        uint2 raw[4];
+#pragma unroll
+        for (uint32_t u = 0; u < 4; ++u) {
+            const uint32_t g = g0 + 32 * u;
+            raw[u] = g < gend ? __ldg(reinterpret_cast<const uint2*>(sm + (g << 3))) : make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (uint32_t u = 0; u < 4; ++u) {
+            const uint32_t g = g0 + 32 * u;
+            if (g < gend) {
+                const uint32_t i = g << 3, k = i + d;
+                AFX_CHECK(k + 8 <= static_cast<uint32_t>(kWarpStage) && i + 8 <= kTileElems, kChkMergeStage);
+                const uint32_t* w = reinterpret_cast<const uint32_t*>(stage + (k & ~3u));
+                const uint32_t w0 = w[0], w1 = w[1], w2 = (k & 3u) ? w[2] : 0u;
+                const uint2 r8 = make_uint2(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh));
+                *reinterpret_cast<uint4*>(dst + i) = join8(r8, raw[u]);
+            }
+        }
     }
 }
 
@@ -542,6 +558,16 @@ __device__ bool pf_decode_item(const TabView& tv, WarpSlot& ws, uint8_t* wstream
                     const uint64_t a0 = o0 & ~uint64_t(15), a1 = (o1 + 15) & ~uint64_t(15);
                     prefetch_l2(t.sm + a0, static_cast<uint32_t>(a1 - a0));
                 }
+                if (more && total) {
+                    // and, one sub-tile ahead, those of this warp's next
+                    // sub-tile: it starts about 21 sub-tiles of this one's
+                    // size further on (256 weights of slack either side)
+                    const uint64_t est = o1 + static_cast<uint64_t>(kPfDecodeWarps - 1) * total;
+                    const uint64_t a0 = (est > 256 ? est - 256 : 0) & ~uint64_t(15);
+                    const uint64_t e1 = est + total + 256 < n ? est + total + 256 : n;
+                    const uint64_t a1 = (e1 + 15) & ~uint64_t(15);
+                    if (a1 > a0) prefetch_l2(t.sm + a0, static_cast<uint32_t>(a1 - a0));
+                }
             }
         }
         __syncwarp();
@@ -759,7 +785,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __gr
                     }
                     mbar_arrive(&ctl.ring_empty[q % kRingTiles]);  // the TMA has read the tile: its slot is free
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(stage_a + st * kTileBytes);
+                    const uint64_t a_desc = desc_sw128(smem_u32(stage_a + st * kTileBytes));
                     for (uint32_t h = 0; h < a.halves; ++h) {
                         const uint32_t b = bseq % L.b_slots;
                         if (!pf_wait(&ctl.b_full[b], (bseq / L.b_slots) & 1u, wait_limit, ctl, status)) {
@@ -767,11 +793,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __gr
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t b_addr = smem_u32(ring_b + b * L.b_stage);
-#pragma unroll
-                        for (uint32_t kk = 0; kk < kTileCols / kSliceK; ++kk)
-                            tc_mma(tmem + h * a.n_mma, desc_sw128(a_addr + kk * 32), desc_sw128(b_addr + kk * 32), idesc,
-                                   (g | kk) != 0);
+                        const uint64_t b_desc = desc_sw128(smem_u32(ring_b + b * L.b_stage));
+                        const uint32_t d_tmem = tmem + h * a.n_mma;
+                        // the K = 16 steps start 32 bytes apart: 2 in the
+                        // descriptors' start-address field
+                        tc_mma(d_tmem, a_desc, b_desc, idesc, g != 0);
+                        tc_mma(d_tmem, a_desc + 2, b_desc + 2, idesc, true);
+                        tc_mma(d_tmem, a_desc + 4, b_desc + 4, idesc, true);
+                        tc_mma(d_tmem, a_desc + 6, b_desc + 6, idesc, true);
                         tc_commit(&ctl.b_empty[b]);
                         ++bseq;
                     }
