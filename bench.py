@@ -337,8 +337,8 @@ def profiled_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu capture of `kernel` on
     this workload (profiles/<kernel>.<workload>.traffic.json, else the
     kernel's main record), or None when no capture is of this workload or
-    the kernel source has changed since (the sha256 of the source is stored
-    with the counters)."""
+    the kernel source has changed since (the sha256 of the source files,
+    concatenated in the record's order, is stored with the counters)."""
     import hashlib
     path = os.path.join(ROOT, "profiles", f"{kernel}.{workload}.traffic.json")
     if not os.path.exists(path):
@@ -346,8 +346,12 @@ def profiled_traffic(kernel: str, workload: str):
     try:
         with open(path) as f:
             rec = json.load(f)
-        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
+        sources = rec["source"] if isinstance(rec["source"], list) else [rec["source"]]
+        h = hashlib.sha256()
+        for src in sources:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        sha = h.hexdigest()
     except (OSError, KeyError, ValueError):
         return None
     if sha != rec.get("source_sha256") or workload != rec.get("bench_workload", "layer"):
