@@ -1145,28 +1145,59 @@ def run_formats_bench(afx, dev, args):
     return out
 
 
-WIDE_TREES = ((57, 0.85), (58, 0.85), (80, 0.9), (100, 0.92))
+WIDE_TREES = ((51, 0.85), (52, 0.85), (57, 0.85), (80, 0.9), (100, 0.92), (120, 0.94))
+TAIL_FRACTION = 1e-3  # the long-tail case: this share of the weights gets an exponent drawn from 1..254
+
+
+def long_tail_weights(n: int, seed: int = 0):
+    """N(0, 0.02) BF16 weights with a share TAIL_FRACTION of them given an
+    exponent drawn uniformly from 1..254 (the shape of a checkpoint with
+    rare outliers across the whole range): a wide code tree whose deep
+    nodes are rarely reached."""
+    import numpy as np
+    from weight_streaming_canonical_gb300 import synth
+    w = synth.normal(n, seed=seed)
+    rng = np.random.default_rng(seed + 17)
+    pick = rng.choice(n, size=int(n * TAIL_FRACTION), replace=False)
+    e = rng.integers(1, 255, size=pick.size).astype(np.uint16)
+    w[pick] = (w[pick] & np.uint16(0x807F)) | (e << np.uint16(7))
+    return w
 
 
 def run_wide_trees_bench(afx, dev, args, layer_weights_per_s=None):
     """Restore rate against the size of the code tree: one 2^27-weight tensor
-    per exponent count (57 exponents: 56 internal nodes, the largest
-    byte-step state table; 58 and more: the 12-bit multi-code table), each
-    restored by one launch, bit-exact checked, then timed."""
+    per exponent mix (geometric exponent frequencies, synth.exponent_mix),
+    and one N(0, 0.02) tensor with rare exponents across the whole range;
+    each restored by one launch, bit-exact checked, then timed.  The decoder
+    each one gets comes from afx_decode_table_kind: the whole byte-step
+    state table while its rows fit (50 internal nodes beside 32 warps
+    staging 16-byte chunks), beyond that rows for the shallowest nodes plus
+    escapes."""
     from weight_streaming_canonical_gb300 import synth
+    kinds = {afx.AFX_TABLE_FILL: "fill", afx.AFX_TABLE_LUT12: "12-bit multi-code table",
+             afx.AFX_TABLE_STATES: "byte-step state table, every node",
+             afx.AFX_TABLE_PARTIAL: "byte-step state table, shallowest nodes + escapes"}
     out = {"weights": 1 << 27, "runs": []}
-    for n_exp, ratio in WIDE_TREES:
-        w = synth.exponent_mix(1 << 27, n_exp, ratio=ratio, seed=n_exp)
+    cases = [(f"mix{n_exp}", n_exp, ratio) for n_exp, ratio in WIDE_TREES] + [("tail", None, None)]
+    for label, n_exp, ratio in cases:
+        if n_exp is None:
+            w = long_tail_weights(1 << 27, seed=3)
+        else:
+            w = synth.exponent_mix(1 << 27, n_exp, ratio=ratio, seed=n_exp)
         c, d = afx.encode(w)
-        r, st = measure_restore(afx, [(f"mix{n_exp}", w, c, d)], dev, args, f"mix:{n_exp}")
+        kind, rows = afx.afx_decode_table_kind(d)
+        r, st = measure_restore(afx, [(label, w, c, d)], dev, args, f"{label}")
         del st
         wps = r["n"] / (r["ms"] * 1e-3)
-        out["runs"].append({"exponents": n_exp, "internal_nodes": n_exp - 1, "ms": r["ms"], "weights_per_s": wps,
+        out["runs"].append({"case": label, "exponents": d.nsym, "internal_nodes": d.nsym - 1,
+                            "ratio": ratio, "ms": r["ms"], "weights_per_s": wps,
                             "hbm_frac": r["roofline"]["frac"], "bit_exact": r["bit_exact"],
-                            "coded_bits_per_weight": d.total_bits / d.n,
-                            "decoder": "byte-step state table" if n_exp - 1 <= 56 else "12-bit multi-code table",
+                            "coded_bits_per_weight": d.total_bits / d.n, "chunk_bytes": d.chunk_bytes,
+                            "decoder": kinds.get(kind, str(kind)), "state_rows": rows,
                             "frac_of_layer_rate": wps / layer_weights_per_s if layer_weights_per_s else None})
-    out["path"] = "afx_decode_batch of one tensor per step (restore_store_kernel), exponent mixes of synth.exponent_mix"
+        del w, c
+    out["path"] = ("afx_decode_batch of one tensor per step (restore_store_kernel, or restore_store_partial_kernel "
+                   "for a partial state table)")
     return out
 
 

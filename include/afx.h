@@ -202,6 +202,30 @@ afx_status afx_decode(const afx_desc* desc, const void* container_dev, void* out
 afx_status afx_decode_batch(const afx_desc* descs, const void* const* containers_dev, void* const* outs_dev,
                             uint32_t count, afx_stream_t stream, int32_t* status_dev);
 
+/* How the restore kernels on the current device decode this container when
+ * it is launched alone (a batch with a larger chunk size T can only move a
+ * tensor toward the 12-bit table):
+ *   AFX_TABLE_FILL     one exponent: no code, a fill of the raw bytes;
+ *   AFX_TABLE_LUT12    the 12-bit multi-code table (a 1-bit code, or too
+ *                      few state-table rows fit);
+ *   AFX_TABLE_STATES   the byte-step state table with a row for every
+ *                      internal node of the code tree;
+ *   AFX_TABLE_PARTIAL  the byte-step state table with rows for the *rows
+ *                      shallowest internal nodes; a code whose prefix
+ *                      reaches another node is decoded on its own (BF16
+ *                      trees with more nodes than shared memory holds rows
+ *                      for; such tensors run in launches of their own).
+ * *rows: the node rows of the state table (0 for FILL and LUT12).  Cites:
+ * "Why Weight Offloading Slows Inference", section "Lossless compression:
+ * fewer bytes to read, more work to unpack" (the decoder that sets
+ * t_unpack).  Errors: AFX_E_ARG (null pointer), AFX_E_FORMAT (desc),
+ * AFX_E_CUDA (no current device). */
+#define AFX_TABLE_FILL 0u
+#define AFX_TABLE_LUT12 1u
+#define AFX_TABLE_STATES 2u
+#define AFX_TABLE_PARTIAL 3u
+afx_status afx_decode_table_kind(const afx_desc* desc, uint32_t* kind, uint32_t* rows);
+
 /* Device workspace (bytes) that afx_decode_gemv needs for this container
  * and batch: for every run of 32 chunks (16 per block) its first weight
  * index (8 bytes) and one float per batch row for each of the two output

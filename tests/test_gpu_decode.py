@@ -48,12 +48,108 @@ def test_byte_steps_with_32_byte_chunks(afx):
     assert d.chunk_bytes == 32 and min(l for l in d.len if l) == 4
 
 
-@pytest.mark.parametrize("nsym,ratio", [(57, 0.85), (58, 0.85), (80, 0.9), (120, 0.94)])
+@pytest.mark.parametrize("nsym,ratio", [(51, 0.85), (52, 0.85), (57, 0.85), (58, 0.85), (80, 0.9), (120, 0.94),
+                                        (200, 0.97)])
 def test_largest_state_table_and_the_trees_past_it(afx, nsym, ratio):
-    # 57 exponents: 56 internal nodes, the largest state table; 58, 80 and
-    # 120: the 12-bit table
+    # with 32 warps staging 16-byte chunks, rows for 50 internal nodes fit:
+    # 51 exponents decode with the whole state table, 52 to 80 with rows for
+    # the 50 shallowest nodes and escapes at the others; 120 and 200 (32-byte
+    # chunks, escapes in most chunks) with the 12-bit table
     c, d = _check(afx, synth.exponent_mix(3_000_017, nsym, ratio=ratio, seed=nsym), out_pad=16)
     assert d.nsym == nsym and min(l for l in d.len if l) >= 2
+    expect = afx.AFX_TABLE_STATES if nsym <= 51 else afx.AFX_TABLE_PARTIAL if nsym <= 80 else afx.AFX_TABLE_LUT12
+    assert afx.afx_decode_table_kind(d)[0] == expect
+
+
+def test_table_kind_follows_the_tree(afx):
+    def kind(w, fmt=0):
+        return afx.afx_decode_table_kind(afx.encode(w, fmt=fmt)[1])
+    fill = np.full(1000, 0x3F80, dtype=np.uint16)
+    assert kind(fill) == (afx.AFX_TABLE_FILL, 0)
+    assert kind(synth.exponent_mix(100_000, 2, ratio=0.5, seed=1))[0] == afx.AFX_TABLE_LUT12  # 1-bit codes
+    normal = synth.normal(300_000, seed=1)
+    assert kind(normal) == (afx.AFX_TABLE_STATES, afx.encode(normal)[1].nsym - 1)  # every internal node
+    k51, rows = kind(synth.exponent_mix(3_000_017, 51, ratio=0.85, seed=51))
+    assert k51 == afx.AFX_TABLE_STATES and rows == 50
+    assert kind(synth.exponent_mix(3_000_017, 52, ratio=0.85, seed=52)) == (afx.AFX_TABLE_PARTIAL, rows)
+    assert kind(synth.exponent_mix(2_000_003, 90, ratio=0.9, seed=9)) == (afx.AFX_TABLE_PARTIAL, rows)
+    # a flat tree in 32-byte chunks: fewer rows fit and most codes pass a
+    # node without one, so the 12-bit table is the faster decoder
+    assert kind(synth.exponent_mix(1_500_007, 100, ratio=0.99, seed=3)) == (afx.AFX_TABLE_LUT12, 0)
+    assert kind(synth.normal_fp16(100_000, seed=2), fmt=afx.AFX_FMT_FP16)[0] == afx.AFX_TABLE_STATES
+
+
+@pytest.mark.parametrize("T", [4, 8])
+def test_partial_state_tables_small_chunks(afx, T):
+    # the escapes start at any bit of a chunk, also where a chunk is one word
+    w = synth.exponent_mix(1_500_007, 100, ratio=0.92, seed=T)
+    c, d = _check(afx, w, chunk_bytes=T, out_pad=16)
+    assert d.chunk_bytes == T and afx.afx_decode_table_kind(d)[0] == afx.AFX_TABLE_PARTIAL
+
+
+def test_partial_state_table_with_a_long_tail(afx):
+    # the layer's distribution plus rare exponents across the whole range (the
+    # shape of a checkpoint with outliers): 254 exponents, escapes are rare
+    # and the rare codes are up to 19 bits long
+    rng = np.random.default_rng(5)
+    w = synth.normal(4_000_000, seed=5)
+    pick = rng.choice(w.size, size=4000, replace=False)
+    e = rng.integers(1, 255, size=pick.size).astype(np.uint16)
+    w[pick] = (w[pick] & np.uint16(0x807F)) | (e << np.uint16(7))
+    c, d = _check(afx, w, out_pad=16)
+    assert d.nsym > 60 and d.max_len > 16 and afx.afx_decode_table_kind(d)[0] == afx.AFX_TABLE_PARTIAL
+
+
+def test_partial_state_tables_from_pinned_host_memory(afx):
+    import torch
+    w = synth.exponent_mix(2_000_003, 90, ratio=0.9, seed=9)
+    c, d = afx.encode(w)
+    assert afx.afx_decode_table_kind(d)[0] == afx.AFX_TABLE_PARTIAL
+    out = torch.full((w.size,), 0x5A5A, dtype=torch.int16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    afx.afx_decode(d, _pinned(c), out, status_dev=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert np.array_equal(out.cpu().numpy().view(np.uint16), w)
+
+
+def test_batch_mixing_partial_and_whole_state_tables(afx):
+    # wide trees go to launches of their own (70 exponents: a partial state
+    # table; 130 exponents in 32-byte chunks: the 12-bit table); the batch's
+    # outputs are all exact
+    import torch
+    ws = [synth.normal(700_001, seed=1), synth.exponent_mix(900_007, 70, ratio=0.9, seed=2),
+          synth.exponent_mix(500_009, 30, ratio=0.8, seed=3), synth.exponent_mix(1_100_003, 130, ratio=0.95, seed=4),
+          synth.adversarial(300_001, seed=5)]
+    enc = [afx.encode(w) for w in ws]
+    conts = [(_pinned(c) if i == 3 else torch.from_numpy(c).cuda()) for i, (c, _) in enumerate(enc)]
+    outs = [torch.full((w.size,), 0x5A5A, dtype=torch.int16, device="cuda") for w in ws]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    afx.afx_decode_batch([d for _, d in enc], conts, outs, status_dev=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    for w, o in zip(ws, outs):
+        assert np.array_equal(o.cpu().numpy().view(np.uint16), w)
+
+
+def test_corrupt_stream_with_a_partial_state_table(afx):
+    # flipped bits and a garbage stream: flagged (or, for a flip that still
+    # decodes to the right count, a wrong tensor), never a hang or a write
+    # outside the output
+    w = synth.exponent_mix(600_011, 90, ratio=0.9, seed=12)
+    c, d = afx.encode(w)
+    assert afx.afx_decode_table_kind(d)[0] == afx.AFX_TABLE_PARTIAL
+    rng = np.random.default_rng(4)
+    for pos in rng.integers(0, d.total_bits // 8, size=8):
+        bad = c.copy()
+        bad[d.off_exp + int(pos)] ^= 0x10
+        status, out = _decode_bad(afx, bad, d, w)
+        assert status != 0 or not np.array_equal(out, w)
+    bad = c.copy()
+    bad[d.off_exp: d.off_exp + d.n_chunks * d.chunk_bytes] = rng.integers(
+        0, 256, size=d.n_chunks * d.chunk_bytes, dtype=np.uint8)
+    status, _ = _decode_bad(afx, bad, d, w)
+    assert status != 0
 
 
 def test_gaps_that_skip_zero_one_and_two_bytes(afx):

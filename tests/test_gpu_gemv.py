@@ -165,3 +165,41 @@ def test_gemv_batch_of_products_in_one_launch(afx):
     for (W, x, _, _), y in zip(items, ys):
         y_ref, A = oracle.gemv(W, x)
         assert within_gemv_tolerance(y.cpu().numpy(), y_ref, A)
+
+
+@pytest.mark.parametrize("B", [1, 2, 4])
+def test_partial_state_table(afx, B):
+    # 90 exponents: rows for the shallowest 50 internal nodes of 89, escapes
+    # at the others (launches of their own)
+    rows, cols = 300, 5120
+    W = synth.exponent_mix(rows * cols, 90, ratio=0.9, seed=B).reshape(rows, cols)
+    x = synth.activations(B, cols, seed=B)
+    _, _, d = _check(afx, W, x)
+    assert d.nsym == 90 and afx.afx_decode_table_kind(d)[0] == afx.AFX_TABLE_PARTIAL
+
+
+def test_gemv_batch_mixing_partial_and_whole_state_tables(afx):
+    import torch
+    shapes = [(200, 5120), (150, 2560), (64, 17408), (96, 640)]
+    B = 4
+    items = []
+    for i, (r, c) in enumerate(shapes):
+        if i % 2:  # 90 exponents (a partial state table) and 130 (the 12-bit table)
+            W = synth.exponent_mix(r * c, 70 + 20 * i, ratio=0.9, seed=400 + i).reshape(r, c)
+        else:
+            W = synth.normal(r * c, seed=400 + i).reshape(r, c)
+        x = synth.activations(B, c, seed=500 + i)
+        cont, d = afx.encode(W.reshape(-1))
+        items.append((W, x, cont, d))
+    devs = [torch.from_numpy(cont).cuda() for _, _, cont, _ in items]
+    xs = [torch.from_numpy(x.view(np.int16)).cuda() for _, x, _, _ in items]
+    ys = [torch.full((B, r), float("nan"), dtype=torch.float32, device="cuda") for r, _ in shapes]
+    wss = [torch.empty(afx.afx_decode_gemv_workspace(d, B) // 4 + 4, dtype=torch.float32, device="cuda")
+           for _, _, _, d in items]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    afx.afx_decode_gemv_batch([d for *_, d in items], devs, shapes, xs, ys, wss, status_dev=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    for (W, x, _, _), y in zip(items, ys):
+        y_ref, A = oracle.gemv(W, x)
+        assert within_gemv_tolerance(y.cpu().numpy(), y_ref, A)

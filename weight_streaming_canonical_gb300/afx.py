@@ -108,6 +108,8 @@ _lib.afx_encode.argtypes = [_vp, _u64, ctypes.POINTER(afx_code), ctypes.POINTER(
 _lib.afx_parse_header.argtypes = [_vp, _u64, ctypes.POINTER(afx_desc)]
 _lib.afx_decode.argtypes = [ctypes.POINTER(afx_desc), _vp, _vp, _vp, _i32p]
 _lib.afx_decode_gemv_workspace.argtypes = [ctypes.POINTER(afx_desc), _u32, ctypes.POINTER(ctypes.c_uint64)]
+_lib.afx_decode_table_kind.argtypes = [ctypes.POINTER(afx_desc), ctypes.POINTER(ctypes.c_uint32),
+                                       ctypes.POINTER(ctypes.c_uint32)]
 _lib.afx_decode_gemv.argtypes = [ctypes.POINTER(afx_desc), _vp, _u32, _u32, _vp, _u32, _vp, _vp, _u64, _vp, _i32p]
 _PP = ctypes.POINTER(ctypes.c_void_p)
 _lib.afx_decode_batch.argtypes = [ctypes.POINTER(afx_desc), _PP, _PP, _u32, _vp, _i32p]
@@ -317,6 +319,19 @@ def afx_decode_gemv_batch(descs, containers_dev, shapes, xs_dev, ys_dev, workspa
     _check("afx_decode_gemv_batch", _lib.afx_decode_gemv_batch(
         arr, _ptrs(containers_dev), rows, cols, _ptrs(xs_dev), batch, _ptrs(ys_dev), _ptrs(workspaces_dev), wsb,
         count, _stream_handle(stream), _dev_ptr(status_dev)))
+
+
+AFX_TABLE_FILL, AFX_TABLE_LUT12, AFX_TABLE_STATES, AFX_TABLE_PARTIAL = 0, 1, 2, 3
+
+
+def afx_decode_table_kind(desc: afx_desc) -> tuple:
+    """(kind, rows): the decoder the restore kernels use for this container
+    launched alone on the current device (AFX_TABLE_*) and its state-table
+    node rows."""
+    kind, rows = ctypes.c_uint32(0), ctypes.c_uint32(0)
+    _check("afx_decode_table_kind", _lib.afx_decode_table_kind(ctypes.byref(desc), ctypes.byref(kind),
+                                                               ctypes.byref(rows)))
+    return int(kind.value), int(rows.value)
 
 
 def afx_decode_gemv_workspace(desc: afx_desc, batch: int) -> int:

@@ -36,6 +36,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstddef>
 #include <cstdio>
 #include <cstring>
@@ -493,7 +494,8 @@ struct GemvEpilogue {
 // Restores sub-tiles [s0, s1) of tensor t with one warp.  phases holds the
 // parity each of the warp's two copy barriers waits for next.  Returns false
 // when a staging copy timed out (the run is abandoned and flagged).
-template <bool host_src, class Epi>
+// kPartial: the tensor's state table holds only its shallowest nodes.
+template <bool host_src, bool kPartial, class Epi>
 __device__ __forceinline__ bool warp_run(const TabView& tv, WarpSlot& ws, uint8_t* wstream, uint32_t wstride,
                                          const TensorArgs& t, uint64_t s0, uint64_t s1, int lane, int32_t* status,
                                          uint32_t wait_limit, bool stall, uint32_t& phases, const Epi& epi) {
@@ -501,7 +503,7 @@ __device__ __forceinline__ bool warp_run(const TabView& tv, WarpSlot& ws, uint8_
     const uint32_t chunk_bits = 8u * T;
     const uint32_t sub_bytes = kWarpChunks * T, sub_bits = 8u * sub_bytes;
     const bool fsm = t.tab.fsm != 0;
-    const uint32_t skip_row0 = t.tab.n_states * kFsmRowBytes;
+    const uint32_t skip_row0 = t.tab.fsm_rows * kFsmRowBytes;
     const uint64_t n_sub = (t.n_chunks + kWarpChunks - 1) / kWarpChunks;
     const uint64_t n_full = t.n_sub_full;
     const uint8_t* const sm = t.sm;
@@ -608,7 +610,10 @@ __device__ __forceinline__ bool warp_run(const TabView& tv, WarpSlot& ws, uint8_
                 }
                 AFX_CHECK((lane + 1) * (T >> 2) <= wstride >> 2, kChkStreamWords);
                 if (chunk_end <= stream_end) {
-                    fsm_chunk_steps(tv, stream + lane * (T >> 2), T >> 2, gap, skip_row0, ws.stage, s_run, fl);
+                    if constexpr (kPartial)
+                        fsm_chunk_steps_esc(tv, stream, lane * (T >> 2), T, gap, skip_row0, ws.stage, s_run, fl);
+                    else
+                        fsm_chunk_steps(tv, stream + lane * (T >> 2), T >> 2, gap, skip_row0, ws.stage, s_run, fl);
                     stepped = true;
                 } else {  // the stream's partial last chunk
                     AFX_CHECK(s_run + cnt <= static_cast<uint32_t>(kWarpStage), kChkStageRun);
@@ -624,7 +629,7 @@ __device__ __forceinline__ bool warp_run(const TabView& tv, WarpSlot& ws, uint8_
         __syncwarp();
         if (stepped) {
             AFX_CHECK(reinterpret_cast<uint8_t*>(fl.wout) + 4 <= ws.stage + kWarpStage, kChkStagePending);
-            bad = fsm_chunk_finish(tv, stream, fl, cnt, chunk_end, next);
+            bad = fsm_chunk_finish<kPartial>(tv, stream, fl, cnt, chunk_end, next);
         }
         if (bad) raise_status(status, AFX_DEV_BAD_CHUNK);
         const bool any_bad = __any_sync(0xFFFFFFFFu, bad);
@@ -667,8 +672,11 @@ __device__ __forceinline__ bool warp_run(const TabView& tv, WarpSlot& ws, uint8_
 }
 
 // One CTA per SM (up to 32 warps) sharing one copy of the decode tables.
-// host_src: the containers are in pinned host memory.
-template <bool host_src, class Epi>
+// host_src: the containers are in pinned host memory.  kPartial: the
+// launch holds the tensors whose state tables keep only their shallowest
+// nodes (their own kernels, so that the escape checks and their registers
+// stay out of every other launch).
+template <bool host_src, bool kPartial, class Epi>
 __device__ __forceinline__ void restore_warps(const LaunchArgs& a, const Epi& epi) {
     extern __shared__ __align__(16) uint8_t smem[];
     SharedW& sh = *reinterpret_cast<SharedW*>(smem);
@@ -690,6 +698,7 @@ __device__ __forceinline__ void restore_warps(const LaunchArgs& a, const Epi& ep
     tv.fsm = reinterpret_cast<const char*>(tabr);
     tv.depth = sh.ct.state_depth;
     tv.fsm_bytes = a.tab_bytes;
+    tv.esc_base = ~0u;
 
     const uint64_t g_begin = a.total_tiles * blockIdx.x / gridDim.x;
     const uint64_t g_end = a.total_tiles * (blockIdx.x + 1) / gridDim.x;
@@ -717,8 +726,9 @@ __device__ __forceinline__ void restore_warps(const LaunchArgs& a, const Epi& ep
         const uint64_t span = se - sb;
         const uint64_t s0 = sb + span * warp / nwarps, s1 = sb + span * (warp + 1) / nwarps;
         if (alive && s0 < s1) {
-            alive = warp_run<host_src>(tv, ws, wstream, wstride, t, s0, s1, lane, a.status, wait_limit, a.stall != 0,
-                                       phases, epi);
+            if constexpr (kPartial) tv.esc_base = (t.tab.fsm_rows + kSkipRows) * kFsmRowBytes;
+            alive = warp_run<host_src, kPartial>(tv, ws, wstream, wstride, t, s0, s1, lane, a.status, wait_limit,
+                                                 a.stall != 0, phases, epi);
             // a staging wait ran out: its copy may still land in shared memory
             // after the CTA moves on (the failure injection issues no copies)
             if (!alive && !host_src && !a.stall && lane == 0) raise_status(a.status, AFX_DEV_UNDRAINED);
@@ -727,42 +737,61 @@ __device__ __forceinline__ void restore_warps(const LaunchArgs& a, const Epi& ep
 }
 
 __global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1) restore_store_kernel(const __grid_constant__ LaunchArgs a) {
-    restore_warps<false>(a, StoreEpilogue{});
+    restore_warps<false, false>(a, StoreEpilogue{});
 }
 
 // The restore from containers in pinned host memory, read over the host link.
 __global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
     restore_store_host_kernel(const __grid_constant__ LaunchArgs a) {
-    restore_warps<true>(a, StoreEpilogue{});
+    restore_warps<true, false>(a, StoreEpilogue{});
 }
 
 // The restore of E4M3 containers (raw nibbles, one byte per element), from
 // device memory and from pinned host memory.
 __global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
     restore_store_e4m3_kernel(const __grid_constant__ LaunchArgs a) {
-    restore_warps<false>(a, StoreE4M3Epilogue{});
+    restore_warps<false, false>(a, StoreE4M3Epilogue{});
 }
 
 __global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
     restore_store_e4m3_host_kernel(const __grid_constant__ LaunchArgs a) {
-    restore_warps<true>(a, StoreE4M3Epilogue{});
+    restore_warps<true, false>(a, StoreE4M3Epilogue{});
 }
 
 // The restore of FP16 containers (raw bytes plus the hi section's 3 bits per
 // element), from device memory and from pinned host memory.
 __global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
     restore_store_fp16_kernel(const __grid_constant__ LaunchArgs a) {
-    restore_warps<false>(a, StoreFP16Epilogue{});
+    restore_warps<false, false>(a, StoreFP16Epilogue{});
 }
 
 __global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
     restore_store_fp16_host_kernel(const __grid_constant__ LaunchArgs a) {
-    restore_warps<true>(a, StoreFP16Epilogue{});
+    restore_warps<true, false>(a, StoreFP16Epilogue{});
 }
 
 template <int B>
 __global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1) restore_gemv_kernel(const __grid_constant__ LaunchArgs a) {
-    restore_warps<false>(a, GemvEpilogue<B>{});
+    restore_warps<false, false>(a, GemvEpilogue<B>{});
+}
+
+// The BF16 restore and GEMV of tensors whose state tables keep only their
+// shallowest nodes (code trees with more internal nodes than shared memory
+// holds rows for).
+__global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
+    restore_store_partial_kernel(const __grid_constant__ LaunchArgs a) {
+    restore_warps<false, true>(a, StoreEpilogue{});
+}
+
+__global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
+    restore_store_host_partial_kernel(const __grid_constant__ LaunchArgs a) {
+    restore_warps<true, true>(a, StoreEpilogue{});
+}
+
+template <int B>
+__global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
+    restore_gemv_partial_kernel(const __grid_constant__ LaunchArgs a) {
+    restore_warps<false, true>(a, GemvEpilogue<B>{});
 }
 
 // Rows of the warp GEMV: the sub-tile in which a row starts adds its own
@@ -957,7 +986,8 @@ void make_tables(const afx_desc& d, CodeTables& t) {
         states += here;
     }
     t.n_states = static_cast<uint32_t>(std::min<uint64_t>(states, 0xFFFFFFFFu));
-    t.fsm = d.nsym >= 2 && min_len >= 2 && states <= static_cast<uint64_t>(kMaxStates) ? 1u : 0u;
+    t.fsm = d.nsym >= 2 && min_len >= 2 ? 1u : 0u;
+    t.fsm_rows = static_cast<uint32_t>(std::min<uint64_t>(states, kMaxStates));
 }
 
 std::mutex g_mutex;
@@ -1076,30 +1106,103 @@ constexpr uint64_t kTableBuildTiles = 5;
 // Up to 32 warps per CTA, one CTA per SM: the warp slots and stream
 // buffers are fixed by the warp count and the largest T, the rest of the
 // opt-in shared memory holds the tables.  A tensor whose state table does
-// not fit falls back to the 12-bit table.
-afx_status warp_launch_config(LaunchArgs& la, int* warps_out, size_t* smem_out) {
+// not fit keeps rows for as many of its shallowest nodes as fit (and
+// escapes at the others), or, with fewer than kMinFsmRows of them, takes
+// the 12-bit table.
+// The warp count of a launch whose largest T is max_chunk_bytes, the shared
+// memory its warps need, and how many node rows of a state table fit beside
+// them.  Returns 0 when not even one warp and the 12-bit table fit.
+int warp_shape(uint32_t max_chunk_bytes, size_t* fixed_out, size_t* fit_rows) {
     int optin = 0;
     const int dev = current_device();
-    if (dev < 0) return afx_fail(AFX_E_CUDA, "no current CUDA device", 0);
-    AFX_CUDA_TRY(cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev), "cudaDeviceGetAttribute");
+    if (dev < 0 || cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
     int warps = kRestoreMaxWarps;
     size_t fixed = 0;
     for (; warps >= 1; warps /= 2) {
         fixed = sharedw_table_offset() + static_cast<size_t>(warps) * sizeof(WarpSlot) +
-                static_cast<size_t>(warps) * 2 * (kWarpChunks * la.max_chunk_bytes + kStreamPad);
+                static_cast<size_t>(warps) * 2 * (kWarpChunks * max_chunk_bytes + kStreamPad);
         if (fixed + kLutTabBytes <= static_cast<size_t>(optin)) break;
     }
+    if (warps < 1) return 0;
+    const size_t rows = (static_cast<size_t>(optin) - fixed) / kFsmRowBytes;
+    *fixed_out = fixed;
+    *fit_rows = rows > kSkipRows ? rows - kSkipRows : 0;
+    return warps;
+}
+
+// Expected escapes per chunk of a state table with rows for the first
+// `rows` internal nodes, from the code lengths alone: symbol s stands for a
+// share 2^-len(s) of the codes; a code escapes when a byte boundary falls
+// after a prefix whose node has no row, and byte boundaries fall at each
+// depth of a code with chance 1/8, so a code escapes with chance (the
+// distinct depths mod 8 of its row-less prefixes) / 8.  Nodes are numbered
+// as make_tables numbers them: depth by depth, the prefixes at depth d
+// that are not codes being [first[d] + count[d], 2^d) in canonical order.
+double escapes_per_chunk(const afx_desc& d, size_t rows) {
+    uint64_t count[AFX_MAX_CODE_LEN + 1] = {0}, first[AFX_MAX_CODE_LEN + 1] = {0}, next[AFX_MAX_CODE_LEN + 1] = {0};
+    uint64_t lo[AFX_MAX_CODE_LEN + 1] = {0}, base[AFX_MAX_CODE_LEN + 1] = {0};
+    for (int sym = 0; sym < 256; ++sym)
+        if (d.len[sym]) ++count[d.len[sym]];
+    uint64_t nodes = 1;  // the root
+    for (uint32_t L = 1; L <= AFX_MAX_CODE_LEN; ++L) {
+        first[L] = L > 1 ? (first[L - 1] + count[L - 1]) << 1 : 0;
+        next[L] = first[L];
+        lo[L] = first[L] + count[L];
+        base[L] = nodes;
+        if (L < d.max_len) nodes += (uint64_t{1} << L) - lo[L];
+    }
+    double esc = 0.0, bits = 0.0;
+    for (int sym = 0; sym < 256; ++sym) {  // canonical order within a length: ascending symbol
+        const uint32_t L = d.len[sym];
+        if (!L) continue;
+        const uint64_t code = next[L]++;
+        uint32_t phases = 0;
+        for (uint32_t depth = 1; depth < L; ++depth)
+            if (base[depth] + (code >> (L - depth)) - lo[depth] >= rows) phases |= 1u << (depth & 7u);
+        esc += std::ldexp(static_cast<double>(__builtin_popcount(phases)) / 8.0, -static_cast<int>(L));
+        bits += std::ldexp(static_cast<double>(L), -static_cast<int>(L));
+    }
+    return bits > 0.0 ? esc * 8.0 * d.chunk_bytes / bits : 0.0;
+}
+
+// Above this many expected escapes per chunk the 12-bit table restores
+// faster than a partial state table (measured on the GB300 with geometric
+// exponent mixes: 0.07 per chunk still gains, 1.3 loses a third).
+constexpr double kMaxEscapesPerChunk = 0.1;
+
+// A tensor restored with a partial state table: byte steps apply (no 1-bit
+// code, two or more symbols), its internal nodes outnumber the rows that
+// fit beside 32 warps staging chunks of its T, at least kMinFsmRows rows
+// fit, and escapes are rare enough.  Such tensors get launches of their
+// own; the rest of the wide trees take the 12-bit table.
+bool partial_table(const afx_desc& d) {
+    if (d.format != AFX_FMT_BF16 || d.nsym < 2) return false;
+    for (int sym = 0; sym < 256; ++sym)
+        if (d.len[sym] == 1) return false;
+    size_t fixed = 0, fit = 0;
+    if (warp_shape(d.chunk_bytes, &fixed, &fit) == 0) return false;
+    const size_t rows = std::min<size_t>(fit, kMaxStates);
+    if (d.nsym - 1 <= rows || rows < kMinFsmRows) return false;
+    return escapes_per_chunk(d, rows) <= kMaxEscapesPerChunk;
+}
+
+afx_status warp_launch_config(LaunchArgs& la, int* warps_out, size_t* smem_out) {
+    if (current_device() < 0) return afx_fail(AFX_E_CUDA, "no current CUDA device", 0);
+    size_t fixed = 0, fit = 0;
+    const int warps = warp_shape(la.max_chunk_bytes, &fixed, &fit);
     if (warps < 1) return afx_fail(AFX_E_ARG, "launch needs too much shared memory", 0);
-    const size_t budget = static_cast<size_t>(optin) - fixed;
     uint32_t tab_bytes = kLutTabBytes;
     for (uint32_t i = 0; i < la.count; ++i) {
         CodeTables& tab = la.t[i].tab;
         if (!tab.fsm) continue;
-        const size_t need = static_cast<size_t>(tab.n_states + kSkipRows) * kFsmRowBytes;
-        if (need > budget)
+        const size_t rows = std::min<size_t>({tab.n_states, static_cast<size_t>(kMaxStates), fit});
+        // a partial table only in a launch of the partial kernels
+        if (rows < tab.n_states && (rows < kMinFsmRows || !la.partial)) {
             tab.fsm = 0;
-        else
-            tab_bytes = std::max<uint32_t>(tab_bytes, static_cast<uint32_t>(need));
+            continue;
+        }
+        tab.fsm_rows = static_cast<uint32_t>(rows);
+        tab_bytes = std::max<uint32_t>(tab_bytes, static_cast<uint32_t>((rows + kSkipRows) * kFsmRowBytes));
     }
     la.tab_bytes = tab_bytes;
     *warps_out = warps;
@@ -1119,10 +1222,11 @@ afx_status launch_gemv_warp(LaunchArgs& la, cudaStream_t s) {
     const afx_status st = warp_launch_config(la, &warps, &smem);
     if (st != AFX_OK) return st;
     int per_sm = 0;
-    const afx_status pst = prepare_kernel(reinterpret_cast<const void*>(restore_gemv_kernel<B>), warps * 32, smem, &per_sm);
+    void (*const kernel)(LaunchArgs) = la.partial ? restore_gemv_partial_kernel<B> : restore_gemv_kernel<B>;
+    const afx_status pst = prepare_kernel(reinterpret_cast<const void*>(kernel), warps * 32, smem, &per_sm);
     if (pst != AFX_OK) return pst;
     const uint64_t grid = std::min<uint64_t>(la.total_tiles, static_cast<uint64_t>(sms) * per_sm);
-    restore_gemv_kernel<B><<<static_cast<unsigned>(grid), warps * 32, smem, s>>>(la);
+    kernel<<<static_cast<unsigned>(grid), warps * 32, smem, s>>>(la);
     AFX_CUDA_TRY(cudaGetLastError(), "restore_gemv_kernel launch");
     const unsigned fix_blocks = static_cast<unsigned>((la.total_subs + 255) / 256);
     gemv_fixup_warp_kernel<B><<<fix_blocks, 256, 0, s>>>(la);
@@ -1144,7 +1248,8 @@ afx_status launch_restore(LaunchArgs& la, cudaStream_t s) {
         void (*const kernels[3][2])(LaunchArgs) = {{restore_store_kernel, restore_store_host_kernel},
                                                     {restore_store_fp16_kernel, restore_store_fp16_host_kernel},
                                                     {restore_store_e4m3_kernel, restore_store_e4m3_host_kernel}};
-        void (*const kernel)(LaunchArgs) = kernels[la.kind < 3 ? la.kind : 0][la.host_src ? 1 : 0];
+        void (*kernel)(LaunchArgs) = kernels[la.kind < 3 ? la.kind : 0][la.host_src ? 1 : 0];
+        if (la.partial) kernel = la.host_src ? restore_store_host_partial_kernel : restore_store_partial_kernel;
         const afx_status pst = prepare_kernel(reinterpret_cast<const void*>(kernel), warps * 32, smem, &per_sm);
         if (pst != AFX_OK) return pst;
         const uint64_t grid = std::min<uint64_t>(la.total_tiles, static_cast<uint64_t>(sms) * per_sm);
@@ -1222,9 +1327,11 @@ afx_status decode_batch(const afx_desc* descs, const void* const* containers, vo
         if (d.nsym >= 2 && d.block_chunks != static_cast<uint32_t>(kThreads))
             return afx_fail(AFX_E_ARG, "the decoder runs 512 chunks per block", 0);
     }
-    // [BF16, FP16, E4M3][device-resident containers, host-resident containers]
-    LaunchArgs lists[3][2];
-    for (int f = 0; f < 3; ++f)
+    // [BF16, FP16, E4M3, BF16 with partial state tables][device-resident
+    // containers, host-resident containers]
+    constexpr int kLists = 4, kPartialList = 3;
+    LaunchArgs lists[kLists][2];
+    for (int f = 0; f < kLists; ++f)
         for (int h = 0; h < 2; ++h) {
             LaunchArgs& la = lists[f][h];
             clear_launch(la);
@@ -1232,7 +1339,8 @@ afx_status decode_batch(const afx_desc* descs, const void* const* containers, vo
             la.wait_limit = stall_polls;
             la.stall = stall_polls != 0;
             la.host_src = static_cast<uint32_t>(h);
-            la.kind = static_cast<uint32_t>(f);
+            la.kind = static_cast<uint32_t>(f == kPartialList ? kKindBF16 : f);
+            la.partial = f == kPartialList ? 1u : 0u;
         }
     for (uint32_t i = 0; i < count; ++i) {
         const afx_desc& d = descs[i];
@@ -1244,7 +1352,8 @@ afx_status decode_batch(const afx_desc* descs, const void* const* containers, vo
         if (stall_polls && wc != Where::device)
             return afx_fail(AFX_E_ARG, "the stalled test restore needs a device-resident container", 0);
         const bool e4m3 = d.format == AFX_FMT_E4M3, fp16 = d.format == AFX_FMT_FP16;
-        LaunchArgs& la = lists[e4m3 ? kKindE4M3 : fp16 ? kKindFP16 : kKindBF16][wc == Where::host ? 1 : 0];
+        const int list = e4m3 ? kKindE4M3 : fp16 ? kKindFP16 : partial_table(d) ? kPartialList : kKindBF16;
+        LaunchArgs& la = lists[list][wc == Where::host ? 1 : 0];
         if (d.nsym == 1) {
             const int sms = sm_count();
             if (sms <= 0) return afx_fail(AFX_E_CUDA, "cannot query the SM count", 0);
@@ -1278,7 +1387,7 @@ afx_status decode_batch(const afx_desc* descs, const void* const* containers, vo
         la.total_tiles += d.n_blocks;
         la.max_chunk_bytes = std::max(la.max_chunk_bytes, d.chunk_bytes);
     }
-    for (int f = 0; f < 3; ++f)
+    for (int f = 0; f < kLists; ++f)
         for (int h = 0; h < 2; ++h) {
             const afx_status st = launch_restore<0>(lists[f][h], s);
             if (st != AFX_OK) return st;
@@ -1316,6 +1425,31 @@ extern "C" afx_status afx_debug_bounds_report(uint32_t* bits, uint32_t* checked)
     return AFX_OK;
 }
 
+extern "C" afx_status afx_decode_table_kind(const afx_desc* desc, uint32_t* kind, uint32_t* rows) {
+    if (!desc || !kind || !rows) return afx_fail(AFX_E_ARG, "null pointer", 0);
+    const afx_status st = afx_check_desc(desc);
+    if (st != AFX_OK) return afx_fail(st, "invalid container description", 0);
+    *kind = AFX_TABLE_FILL;
+    *rows = 0;
+    if (desc->nsym < 2) return AFX_OK;
+    CodeTables t;
+    make_tables(*desc, t);
+    *kind = AFX_TABLE_LUT12;
+    if (!t.fsm) return AFX_OK;
+    size_t fixed = 0, fit = 0;
+    if (current_device() < 0 || warp_shape(desc->chunk_bytes, &fixed, &fit) == 0)
+        return afx_fail(AFX_E_CUDA, "no current CUDA device", 0);
+    const size_t k = std::min<size_t>({t.n_states, static_cast<size_t>(kMaxStates), fit});
+    if (k == t.n_states) {
+        *kind = AFX_TABLE_STATES;
+        *rows = static_cast<uint32_t>(k);
+    } else if (partial_table(*desc) && k >= kMinFsmRows) {
+        *kind = AFX_TABLE_PARTIAL;
+        *rows = static_cast<uint32_t>(k);
+    }
+    return AFX_OK;
+}
+
 extern "C" afx_status afx_decode(const afx_desc* desc, const void* container, void* out, afx_stream_t stream,
                                  int32_t* status) {
     if (!desc) return afx_fail(AFX_E_ARG, "null description", 0);
@@ -1337,11 +1471,14 @@ template <int B>
 afx_status gemv_batch(const afx_desc* descs, const void* const* containers, const uint32_t* rows,
                       const uint32_t* cols, const uint16_t* const* xs, float* const* ys, void* const* workspaces,
                       uint32_t count, cudaStream_t s, int32_t* status) {
-    LaunchArgs la, lw;  // CTA-tile GEMV, warp GEMV
+    LaunchArgs la, lw, lp;  // CTA-tile GEMV, warp GEMV, warp GEMV with partial state tables
     clear_launch(la);
     clear_launch(lw);
+    clear_launch(lp);
     la.status = status;
     lw.status = status;
+    lp.status = status;
+    lp.partial = 1;
     for (uint32_t i = 0; i < count; ++i) {
         const afx_desc& d = descs[i];
         const uint8_t* base = static_cast<const uint8_t*>(containers[i]);
@@ -1356,7 +1493,7 @@ afx_status gemv_batch(const afx_desc* descs, const void* const* containers, cons
             continue;
         }
         const bool warp = warp_gemv_shape(cols[i]);
-        LaunchArgs& L = warp ? lw : la;
+        LaunchArgs& L = warp ? (partial_table(d) ? lp : lw) : la;
         if (L.count == static_cast<uint32_t>(kMaxTensors)) {
             const afx_status st = warp ? launch_gemv_warp<B>(L, s) : launch_restore<B>(L, s);
             if (st != AFX_OK) return st;
@@ -1378,7 +1515,8 @@ afx_status gemv_batch(const afx_desc* descs, const void* const* containers, cons
         L.max_chunk_bytes = std::max(L.max_chunk_bytes, d.chunk_bytes);
         L.max_rows_per_warp = std::max(L.max_rows_per_warp, t.rows_per_warp);
     }
-    const afx_status st = launch_gemv_warp<B>(lw, s);
+    afx_status st = launch_gemv_warp<B>(lw, s);
+    if (st == AFX_OK) st = launch_gemv_warp<B>(lp, s);
     if (st != AFX_OK) return st;
     return launch_restore<B>(la, s);
 }

@@ -431,7 +431,7 @@ __device__ bool pf_decode_item(const TabView& tv, WarpSlot& ws, uint8_t* wstream
     const uint32_t chunk_bits = 8u * T;
     const uint32_t sub_bytes = kWarpChunks * T, sub_bits = 8u * sub_bytes;
     const bool fsm = t.tab.fsm != 0;
-    const uint32_t skip_row0 = t.tab.n_states * kFsmRowBytes;
+    const uint32_t skip_row0 = t.tab.fsm_rows * kFsmRowBytes;
     const uint64_t n_sub = (t.n_chunks + kWarpChunks - 1) / kWarpChunks;
     const uint64_t n = t.n;
     uint64_t start, unused;
@@ -680,6 +680,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_fused_kernel(const __gr
         tv.fsm = reinterpret_cast<const char*>(tabr);
         tv.depth = sh.ct.state_depth;
         tv.fsm_bytes = a.tab_bytes;
+        tv.esc_base = ~0u;  // the state tables here hold every node
         uint32_t phases = 0, q_base = 0, ord_base = 0;
         int built = -1;
         for (uint32_t it = it0; it < it1; ++it) {
@@ -1110,8 +1111,8 @@ extern "C" afx_status afx_prefill_fused_batch(const afx_desc* descs, const void*
                 }
         }
         pa->max_chunk_bytes = max_T;
-        // decode tables: the state table where it fits beside the rings and
-        // the warps' buffers, else the 12-bit table
+        // decode tables: the state table where all of it fits beside the
+        // rings and the warps' buffers, else the 12-bit table
         const PfLayout L0 = pf_layout(0, n_mma, max_T);
         const int64_t budget = static_cast<int64_t>(optin) - 1024 - static_cast<int64_t>(L0.total) - 16;
         if (budget < static_cast<int64_t>(kLutTabBytes)) return afx_fail(AFX_E_ARG, "launch needs too much shared memory", 0);
@@ -1120,10 +1121,12 @@ extern "C" afx_status afx_prefill_fused_batch(const afx_desc* descs, const void*
             CodeTables& tab = pa->m[k].t.tab;
             if (!tab.fsm) continue;
             const int64_t need = static_cast<int64_t>(tab.n_states + kSkipRows) * kFsmRowBytes;
-            if (need > budget)
+            if (tab.n_states > static_cast<uint32_t>(kMaxStates) || need > budget) {
                 tab.fsm = 0;
-            else
+            } else {
+                tab.fsm_rows = tab.n_states;
                 tab_bytes = std::max<uint32_t>(tab_bytes, static_cast<uint32_t>(need));
+            }
         }
         pa->tab_bytes = tab_bytes;
         const size_t smem = pf_layout(tab_bytes, n_mma, max_T).total + 1024;

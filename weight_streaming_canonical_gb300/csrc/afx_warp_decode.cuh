@@ -58,6 +58,7 @@ struct CodeTables {
     uint8_t state_depth[kMaxStates];
     uint32_t n_states;  // internal nodes (nsym - 1)
     uint32_t fsm;       // 1: the restore path decodes this tensor a byte at a time
+    uint32_t fsm_rows;  // nodes held as state-table rows: the first fsm_rows (all, or the shallowest)
 };
 
 // One tensor of a launch.
@@ -93,6 +94,7 @@ struct LaunchArgs {
     uint32_t stall;            // failure injection for tests: arm the staging barriers, issue no copies
     uint32_t host_src;         // restore: the containers are in pinned host memory (restore_store_host_kernel)
     uint32_t kind;             // restore: element kind, kKindBF16 / kKindFP16 / kKindE4M3
+    uint32_t partial;          // BF16 tensors whose state tables keep only their shallowest nodes
     int32_t* status;
     TensorArgs t[kMaxTensors];
 };
@@ -662,10 +664,10 @@ __device__ __forceinline__ bool decode_tile(Shared& sh, const uint32_t* stream, 
 // crosses or ends on, so every entry of the block index is verified.  The
 // only CTA barriers are those around a rebuild of the tables.
 //
-// Byte-step decoding.  When no code is 1 bit long and the tree has at most
-// kMaxStates internal nodes, a lane decodes its chunk eight stream bits at a
-// time through a state machine whose state is the internal node reached by
-// the bits of the code in progress: entry (state, byte) holds the rotated
+// Byte-step decoding.  When no code is 1 bit long, a lane decodes its chunk
+// eight stream bits at a time through a state machine whose state is the
+// internal node reached by the bits of the code in progress: entry (state,
+// byte) holds the rotated
 // exponents of the (at most four) codes that end within the byte, their
 // count, and the next state.  Every lane steps through all T bytes of its
 // chunk from the chunk's first word, so the lanes of a warp run the same
@@ -675,7 +677,17 @@ __device__ __forceinline__ bool decode_tile(Shared& sh, const uint32_t* stream, 
 // not stepping through the first one or two bytes.  After the last byte the
 // state's depth says where the code that crosses the chunk end began; that
 // one code is decoded on its own.  The partial last chunk of a stream and
-// tensors with 1-bit codes or larger trees use the 12-bit multi-code table.
+// tensors with 1-bit codes use the 12-bit multi-code table.
+//
+// A tree with more internal nodes than shared memory holds rows for keeps
+// rows for its first fsm_rows nodes (the shallowest: numbered depth by
+// depth, they carry the most probable prefixes).  A byte that leaves the
+// code in progress at a node without a row yields an escape: the state value
+// esc_base + d, d the bits of that code read so far.  The lane then decodes
+// that one code from its first bit through the first-code table and resumes
+// byte steps at the byte where it ends (in the skip row of the bits it takes
+// there).  Only tensors with such a partial table run the loop that checks
+// for escapes; a tree whose nodes all have rows runs the plain loop.
 
 constexpr int kWarpChunks = 32;                                  // chunks per sub-tile
 constexpr int kSubtilesPerBlock = kThreads / kWarpChunks;        // 16
@@ -686,6 +698,7 @@ constexpr int kRestoreMaxWarps = 32;
 constexpr uint32_t kLutTabBytes = kLutSize * 4 + kLutSize;       // 12-bit table + first-code lengths
 constexpr uint32_t kFsmRowBytes = 256 * 8;                       // one state: 256 entries of 8 bytes
 constexpr uint32_t kSkipRows = 7;                                // rows that first drop 1..7 bits of a byte
+constexpr uint32_t kMinFsmRows = 16;                             // fewest node rows worth a partial table
 
 struct WarpSlot {
     alignas(16) uint16_t chunk[2][kWarpChunkStage];
@@ -719,6 +732,7 @@ struct TabView {
     const char* fsm;
     const uint8_t* depth;
     uint32_t fsm_bytes;  // size of the state table (bounds-checked builds)
+    uint32_t esc_base;   // state values from here are escapes (a table without every node), else ~0u
 };
 
 // One code from a 32-bit window through the first-code table (exact
@@ -798,6 +812,8 @@ __device__ void build_tables_w(SharedW& sh, uint8_t* tabr, const CodeTables& tab
         tv.first = sh.first;
         uint2* fsm = reinterpret_cast<uint2*>(tabr);
         const uint32_t nodes = sh.ct.n_states;
+        const uint32_t rows = sh.ct.fsm_rows;  // nodes with a row; a transition to another node escapes
+        const uint32_t esc_base = (rows + kSkipRows) * kFsmRowBytes;
         // the root row and the skip rows, code by code
         for (uint32_t i = tid; i < (1 + kSkipRows) * 256u; i += nthreads) {
             const uint32_t h = i >> 8, b = i & 255u;  // h: bits of the byte that end an earlier code
@@ -817,12 +833,13 @@ __device__ void build_tables_w(SharedW& sh, uint8_t* tabr, const CodeTables& tab
             const uint32_t lo_r = r ? limit[r] >> (24 - r) : 0u;
             const uint32_t next = state_base[r] + q - lo_r;
             AFX_CHECK(next < nodes, kChkTableBuild);
-            fsm[(h ? nodes + h - 1 : 0u) * 256u + b] = make_uint2(out, (next * kFsmRowBytes) | ((cnt * 8u) << 26));
+            const uint32_t go = next < rows ? next * kFsmRowBytes : esc_base + r;
+            fsm[(h ? rows + h - 1 : 0u) * 256u + b] = make_uint2(out, go | ((cnt * 8u) << 26));
         }
         sync();
         // node rows: the code in progress ends h bits into the byte (or does
         // not end in it); the rest of the byte is skip row h
-        for (uint32_t i = 256u + tid; i < nodes * 256u; i += nthreads) {
+        for (uint32_t i = 256u + tid; i < rows * 256u; i += nthreads) {
             const uint32_t s = i >> 8, b = i & 255u;
             const uint32_t d = sh.ct.state_depth[s];
             const uint32_t lo_d = limit[d] >> (24 - d);
@@ -835,11 +852,11 @@ __device__ void build_tables_w(SharedW& sh, uint8_t* tabr, const CodeTables& tab
                 const uint32_t d8 = d + 8;
                 const uint32_t next = state_base[d8] + ((p << 8) | b) - (limit[d8] >> (24 - d8));
                 AFX_CHECK(next < nodes, kChkTableBuild);
-                e = make_uint2(0u, next * kFsmRowBytes);
+                e = make_uint2(0u, next < rows ? next * kFsmRowBytes : esc_base + d8);
             } else if (h == 8) {
                 e = make_uint2(sym, 8u << 26);
             } else {
-                const uint2 rest = fsm[(nodes + h - 1) * 256u + b];
+                const uint2 rest = fsm[(rows + h - 1) * 256u + b];
                 e = make_uint2(sym | (rest.x << 8), rest.y + (8u << 26));
             }
             fsm[i] = e;
@@ -912,9 +929,10 @@ __device__ __forceinline__ bool decode_run_fsm(const TabView& tv, const uint32_t
     uint32_t acc = 0, fill = 0;
     bool bad = false;
     if (i < cnt) {
-        // whole bytes of the chunk's bits from the code at P
+        // whole bytes of the chunk's bits from the code at P (none with a
+        // partial table: its codes all go through the tail loop below)
         const uint32_t lim = min(chunk_end, stream_end);
-        const uint32_t steps = lim > P ? (lim - P) >> 3 : 0u;
+        const uint32_t steps = lim > P && tv.esc_base == ~0u ? (lim - P) >> 3 : 0u;
         uint32_t k = P >> 5;
         const uint32_t sh = P & 31u;
         uint32_t w0 = stream[k], w1 = stream[k + 1];
@@ -971,6 +989,7 @@ __device__ __forceinline__ bool decode_run_fsm(const TabView& tv, const uint32_t
 struct FsmLane {
     uint32_t* wout;
     uint32_t acc, fill, first, emitted, st;
+    uint32_t xend;  // partial tables: where a code that an escape decoded past the chunk end ends (0: none)
 };
 
 // All T bytes of a full chunk whose first word is words[0] (byte-step
@@ -1005,14 +1024,82 @@ __device__ __forceinline__ void fsm_chunk_steps(const TabView& tv, const uint32_
     fl.st = st;
 }
 
+// fsm_chunk_steps for a partial table: the same steps from stream word k0
+// (the chunk's first), four to a word while no escape comes, with each
+// escape handled where it comes.  The code an escape decodes may cross the
+// chunk end; the lane then stops there and records where it ends (fl.xend,
+// a bit of the staged stream).
+__device__ __forceinline__ void fsm_chunk_steps_esc(const TabView& tv, const uint32_t* stream, uint32_t k0,
+                                                    uint32_t nbytes, uint32_t gap, uint32_t skip_row0, uint8_t* stage,
+                                                    uint32_t s_run, FsmLane& fl) {
+    uint32_t* wout = reinterpret_cast<uint32_t*>(stage + (s_run & ~3u));
+    const uint32_t* const w_begin = wout;
+    uint32_t acc = 0, fill = 8 * (s_run & 3u);
+    const uint32_t h0 = gap & 7u;
+    uint32_t st = h0 ? skip_row0 + (h0 - 1) * kFsmRowBytes : 0u;
+    uint32_t xend = 0;
+    uint32_t j = gap >> 3;  // the next byte to step
+    while (j < nbytes) {
+        const uint32_t X = stream[k0 + (j >> 2)];
+        uint32_t done;  // bytes of this word stepped; the last of them escaped if st >= esc_base
+        if ((j & 3u) == 0) {
+            fsm_step_checked(tv, st, X >> 24, acc, fill, wout);
+            done = 1;
+            if (st < tv.esc_base) {
+                fsm_step_checked(tv, st, __byte_perm(X, 0u, 0x4442), acc, fill, wout);
+                done = 2;
+                if (st < tv.esc_base) {
+                    fsm_step_checked(tv, st, __byte_perm(X, 0u, 0x4441), acc, fill, wout);
+                    done = 3;
+                    if (st < tv.esc_base) {
+                        fsm_step_checked(tv, st, X & 0xFFu, acc, fill, wout);
+                        done = 4;
+                    }
+                }
+            }
+        } else {  // after an escape: one byte at a time up to the word boundary
+            fsm_step_checked(tv, st, (X >> (24u - 8u * (j & 3u))) & 0xFFu, acc, fill, wout);
+            done = 1;
+        }
+        j += done;
+        if (st >= tv.esc_base) {
+            // the code in progress began st - esc_base bits before byte j's start
+            const uint32_t P = 8u * j - (st - tv.esc_base);
+            uint32_t len;
+            const uint32_t sym = decode_first(tv, stream_window(stream, 32u * k0 + P), len);
+            append(sym, 8, acc, fill, wout);
+            const uint32_t e = P + len;
+            st = 0u;
+            if (e >= 8u * nbytes) {  // it ends at or past the chunk end
+                if (e > 8u * nbytes) xend = 32u * k0 + e;
+                break;
+            }
+            j = e >> 3;
+            if (e & 7u) st = skip_row0 + ((e & 7u) - 1) * kFsmRowBytes;
+        }
+    }
+    AFX_CHECK(reinterpret_cast<uint8_t*>(wout) <= stage + kWarpStage, kChkStageSteps);
+    fl.wout = wout;
+    fl.acc = acc;
+    fl.fill = fill;
+    fl.first = wout == w_begin ? (s_run & 3u) : 0u;
+    fl.emitted = 4 * static_cast<uint32_t>(wout - w_begin) + (fill >> 3) - (s_run & 3u);
+    fl.st = st;
+    fl.xend = xend;
+}
+
 // After the warp barrier: the code that crosses the chunk end (if the final
 // state is not the root), the lane's pending bytes, and the checks of the
 // count and of where the next chunk's first code begins.  Returns true when
-// the stream is not valid.
+// the stream is not valid.  kPartial: the lane ran fsm_chunk_steps_esc.
+template <bool kPartial = false>
 __device__ __forceinline__ bool fsm_chunk_finish(const TabView& tv, const uint32_t* stream, const FsmLane& fl,
                                                  uint32_t cnt, uint32_t chunk_end, uint32_t next) {
     const uint32_t d = tv.depth[fl.st / kFsmRowBytes];
     uint32_t end = chunk_end, emitted = fl.emitted, acc = fl.acc, fill = fl.fill;
+    if constexpr (kPartial) {
+        if (fl.xend) end = fl.xend;
+    }
     if (d) {
         uint32_t len;
         const uint32_t sym = decode_first(tv, stream_window(stream, chunk_end - d), len);
