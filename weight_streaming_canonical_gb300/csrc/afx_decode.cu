@@ -679,6 +679,9 @@ __device__ __forceinline__ bool warp_run(const TabView& tv, WarpSlot& ws, uint8_
 template <bool host_src, bool kPartial, class Epi>
 __device__ __forceinline__ void restore_warps(const LaunchArgs& a, const Epi& epi) {
     extern __shared__ __align__(16) uint8_t smem[];
+    // a following restore launch of the same call may take each SM as soon
+    // as this CTA leaves it (it touches other tensors; see launch_restore)
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     SharedW& sh = *reinterpret_cast<SharedW*>(smem);
     uint8_t* tabr = smem + sharedw_table_offset();
     const int nthreads = blockDim.x, nwarps = nthreads >> 5;
@@ -1234,8 +1237,13 @@ afx_status launch_gemv_warp(LaunchArgs& la, cudaStream_t s) {
     return AFX_OK;
 }
 
+// programmatic: the launch follows another restore launch of the same
+// afx_decode_batch call on this stream and may start while that one's last
+// CTAs still run.  The two touch disjoint tensors, and the first launch of
+// a call is ordered after all earlier work on the stream as usual, so this
+// one starts after that work too.
 template <int B>
-afx_status launch_restore(LaunchArgs& la, cudaStream_t s) {
+afx_status launch_restore(LaunchArgs& la, cudaStream_t s, bool programmatic = false) {
     if (la.count == 0 || la.total_tiles == 0) return AFX_OK;
     const int sms = sm_count();
     if (sms <= 0) return afx_fail(AFX_E_CUDA, "cannot query the SM count", 0);
@@ -1253,8 +1261,17 @@ afx_status launch_restore(LaunchArgs& la, cudaStream_t s) {
         const afx_status pst = prepare_kernel(reinterpret_cast<const void*>(kernel), warps * 32, smem, &per_sm);
         if (pst != AFX_OK) return pst;
         const uint64_t grid = std::min<uint64_t>(la.total_tiles, static_cast<uint64_t>(sms) * per_sm);
-        kernel<<<static_cast<unsigned>(grid), warps * 32, smem, s>>>(la);
-        AFX_CUDA_TRY(cudaGetLastError(), "restore_store_kernel launch");
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(static_cast<unsigned>(warps * 32));
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = programmatic ? 1 : 0;
+        AFX_CUDA_TRY(cudaLaunchKernelEx(&cfg, kernel, la), "restore_store_kernel launch");
         return AFX_OK;
     } else {
         size_t smem = shared_fixed_bytes() + 2 * (static_cast<size_t>(kThreads) * la.max_chunk_bytes + kStreamPad);
@@ -1342,6 +1359,7 @@ afx_status decode_batch(const afx_desc* descs, const void* const* containers, vo
             la.kind = static_cast<uint32_t>(f == kPartialList ? kKindBF16 : f);
             la.partial = f == kPartialList ? 1u : 0u;
         }
+    uint32_t restores = 0;  // restore launches made so far by this call
     for (uint32_t i = 0; i < count; ++i) {
         const afx_desc& d = descs[i];
         if (d.n == 0) continue;
@@ -1375,8 +1393,9 @@ afx_status decode_batch(const afx_desc* descs, const void* const* containers, vo
             continue;
         }
         if (la.count == static_cast<uint32_t>(kMaxTensors)) {
-            const afx_status st = launch_restore<0>(la, s);
+            const afx_status st = launch_restore<0>(la, s, restores > 0);
             if (st != AFX_OK) return st;
+            ++restores;
             reset_launch(la);
         }
         TensorArgs& t = la.t[la.count++];
@@ -1389,8 +1408,11 @@ afx_status decode_batch(const afx_desc* descs, const void* const* containers, vo
     }
     for (int f = 0; f < kLists; ++f)
         for (int h = 0; h < 2; ++h) {
-            const afx_status st = launch_restore<0>(lists[f][h], s);
+            LaunchArgs& la = lists[f][h];
+            if (la.count == 0 || la.total_tiles == 0) continue;
+            const afx_status st = launch_restore<0>(la, s, restores > 0);
             if (st != AFX_OK) return st;
+            ++restores;
         }
     return AFX_OK;
 }
