@@ -44,8 +44,9 @@
  *   1 FP16 (IEEE 754 binary16: sign, 5 exponent, 10 fraction): symbol =
  *     exponent; raw byte = sign << 7 | the 7 trailing fraction bits; the 3
  *     leading fraction bits go to a second raw section, the "hi" section,
- *     3 bits per element: element i's bits are section bits 3i .. 3i + 2
- *     (bit 0 the lowest), and section bit b is bit b % 8 of byte b / 8.
+ *     one nibble per element: element i in the low nibble of byte i / 2
+ *     for even i, the high nibble for odd i, its bit 3 zero (so the 8
+ *     nibbles of elements 8g .. 8g + 7 are the aligned word at byte 4g).
  *   2 E4M3 (OCP 8-bit floating point, E4M3: sign, 4 exponent, 3 mantissa):
  *     symbol = exponent; raw nibble = sign << 3 | mantissa, two per byte,
  *     element 2k in the low nibble of byte k.
@@ -68,7 +69,7 @@
  *     floor(i / 32); size = (chunks * T rounded up to 16) + 16 zero bytes.
  *   sm section: the raw bits, one byte per element ((sign << 7) | mantissa
  *     for BF16), or one nibble per element for E4M3 (ceil(n / 2) bytes).
- *   hi section (FP16 only, after the sm section): ceil(3n / 8) bytes.
+ *   hi section (FP16 only, after the sm section): ceil(n / 2) bytes.
  *   chunk index: one u16 per chunk of 8*T stream bits:
  *     bits 0..4  = offset of the first codeword that starts in the chunk,
  *     bits 5..15 = number of codewords that start in the chunk.
@@ -121,7 +122,7 @@ static unsigned orc_symbols_of_format(unsigned fmt) {
     return fmt == ORC_FMT_E4M3 ? 16u : fmt == ORC_FMT_FP16 ? 32u : 256u;
 }
 
-static uint64_t orc_hi_bytes(unsigned fmt, uint64_t n) { return fmt == ORC_FMT_FP16 ? (3 * n + 7) / 8 : 0; }
+static uint64_t orc_hi_bytes(unsigned fmt, uint64_t n) { return fmt == ORC_FMT_FP16 ? (n + 1) / 2 : 0; }
 
 static unsigned orc_read_elem(const void* elems, unsigned fmt, uint64_t i) {
     if (orc_elem_bytes(fmt) == 1) return ((const uint8_t*)elems)[i];
@@ -182,21 +183,11 @@ static unsigned orc_get_raw(const uint8_t* sm, unsigned fmt, uint64_t i) {
     return sm[i];
 }
 
-/* hi-section bits of element i, one bit at a time */
-static unsigned orc_get_hi(const uint8_t* hi, uint64_t i) {
-    unsigned v = 0;
-    for (unsigned b = 0; b < 3; b++) {
-        uint64_t bit = 3 * i + b;
-        v |= ((hi[bit / 8] >> (bit % 8)) & 1u) << b;
-    }
-    return v;
-}
+/* the hi-section nibble of element i (all 4 bits; bit 3 must be zero) */
+static unsigned orc_get_hi(const uint8_t* hi, uint64_t i) { return (hi[i / 2] >> (4 * (i % 2))) & 0xFu; }
 
 static void orc_put_hi(uint8_t* hi, uint64_t i, unsigned v) {
-    for (unsigned b = 0; b < 3; b++) {
-        uint64_t bit = 3 * i + b;
-        if ((v >> b) & 1u) hi[bit / 8] = (uint8_t)(hi[bit / 8] | (1u << (bit % 8)));
-    }
+    hi[i / 2] = (uint8_t)(hi[i / 2] | ((v & 0x7u) << (4 * (i % 2))));
 }
 
 /* the section starts zeroed; element i's raw bits are OR-ed in */
@@ -630,6 +621,7 @@ int orc_decode(const uint8_t* src, uint64_t src_bytes, void* out, uint64_t out_n
             e = (unsigned)found;
         }
         unsigned hi = fmt == ORC_FMT_FP16 ? orc_get_hi(src + L.off_hi, i) : 0u;
+        if (hi > 7u) { status = ORC_E_FORMAT; break; } /* a hi nibble's bit 3 is zero */
         orc_write_elem(out, fmt, i, orc_join_of(fmt, e, orc_get_raw(sm, fmt, i), hi));
     }
     if (status == ORC_OK && pos != total_bits) status = ORC_E_CORRUPT;
@@ -637,9 +629,8 @@ int orc_decode(const uint8_t* src, uint64_t src_bytes, void* out, uint64_t out_n
     if (status == ORC_OK && fmt == ORC_FMT_E4M3 && n % 2 == 1 && (sm[n / 2] >> 4) != 0)
         status = ORC_E_FORMAT; /* the unused nibble after an odd count is zero */
     if (status == ORC_OK && fmt == ORC_FMT_FP16) {
-        /* the hi section's bits past element n - 1 are zero */
-        for (uint64_t bit = 3 * n; bit < 8 * orc_hi_bytes(fmt, n); bit++)
-            if ((src[L.off_hi + bit / 8] >> (bit % 8)) & 1u) { status = ORC_E_FORMAT; break; }
+        /* the hi section's nibble past element n - 1 (an odd n) is zero */
+        if (n % 2 == 1 && (src[L.off_hi + n / 2] >> 4) != 0) status = ORC_E_FORMAT;
     }
     if (status == ORC_OK) {
         /* the stream's padding bits are zero */

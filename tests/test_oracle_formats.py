@@ -111,14 +111,14 @@ def test_fp16_raw_byte_and_hi_section_by_value():
     lens = oracle.code_lengths(oracle.histogram(bits, FP16))
     c = oracle.encode(bits, lens, fmt=FP16)
     off_sm, off_hi, off_chunk = _le(c, 64, 8), _le(c, 112, 8), _le(c, 72, 8)
-    assert off_hi >= off_sm + bits.size and off_chunk >= off_hi + (3 * bits.size + 7) // 8
+    assert off_hi >= off_sm + bits.size and off_chunk >= off_hi + (bits.size + 1) // 2
     # sign and the 7 trailing fraction bits, one byte per element
     assert c[off_sm: off_sm + bits.size].tolist() == ((sign << 7) | (frac & 0x7F)).tolist()
-    # the 3 leading fraction bits: element i at section bits 3i .. 3i + 2, lowest bit first
-    sec = np.unpackbits(c[off_hi: off_hi + (3 * bits.size + 7) // 8], bitorder="little")
-    got = sec[0: 3 * bits.size: 3] | (sec[1: 3 * bits.size: 3] << 1) | (sec[2: 3 * bits.size: 3] << 2)
-    assert got.astype(np.int64).tolist() == (frac >> 7).tolist()
-    assert not sec[3 * bits.size:].any()
+    # the 3 leading fraction bits: element i in nibble i (low nibble first), bit 3 zero
+    sec = c[off_hi: off_hi + (bits.size + 1) // 2]
+    nib = np.stack([sec & 0xF, sec >> 4], axis=1).reshape(-1)
+    assert nib[: bits.size].astype(np.int64).tolist() == (frac >> 7).tolist()
+    assert not nib[bits.size:].any()
 
 
 @pytest.mark.parametrize("T", [4, 32])
@@ -273,13 +273,17 @@ def test_e4m3_single_symbol_fill_in_range():
 
 
 def test_fp16_rejects_a_used_hi_padding_bit():
-    w = np.array([0x3C00, 0xBE00, 0x3780, 0x3C01, 0x4000], np.uint16)  # 15 hi bits in 2 bytes
+    w = np.array([0x3C00, 0xBE00, 0x3780, 0x3C01, 0x4000], np.uint16)  # 5 hi nibbles in 3 bytes
     lens = oracle.code_lengths(oracle.histogram(w, FP16))
     c = oracle.encode(w, lens, 4, 32, fmt=FP16)
     assert oracle.decode(c)[1] == oracle.OK
     c2 = c.copy()
-    c2[_le(c, 112, 8) + 1] |= 0x80  # bit 15: past element 4
+    c2[_le(c, 112, 8) + 2] |= 0x10  # the nibble past element 4
     assert oracle.decode(c2)[1] == oracle.E_FORMAT
+    for byte, bit in ((0, 0x08), (0, 0x80), (2, 0x08)):  # bit 3 of element 0's, 1's and 4's nibble
+        c4 = c.copy()
+        c4[_le(c, 112, 8) + byte] |= bit
+        assert oracle.decode(c4)[1] == oracle.E_FORMAT
     c3 = c.copy()
     c3[112] ^= 0x01  # the hi section's offset no longer matches the layout
     assert oracle.decode(c3)[1] == oracle.E_FORMAT
