@@ -81,9 +81,9 @@ typedef enum afx_status {
  *   AFX_FMT_FP16  IEEE 754 binary16; coded symbol = the 5-bit exponent, raw
  *                 byte = sign << 7 | the 7 trailing fraction bits, and the 3
  *                 leading fraction bits in a second raw section (the hi
- *                 section, afx_desc::off_hi): element i at section bits
- *                 3i .. 3i + 2, bit b of the section in bit b % 8 of byte
- *                 b / 8.
+ *                 section, afx_desc::off_hi): one nibble per element,
+ *                 element i in the low nibble of byte i / 2 for even i and
+ *                 the high nibble for odd i, bit 3 zero.
  *   AFX_FMT_E4M3  OCP 8-bit float E4M3 (bias 7, largest 448); coded symbol =
  *                 the 4-bit exponent, raw nibble = sign << 3 | 3-bit
  *                 mantissa, two per byte, element 2k in the low nibble of
@@ -120,7 +120,7 @@ typedef struct afx_desc {
     uint64_t n_blocks;        /* ceil(n_chunks / C) */
     uint64_t off_exp, exp_bytes;
     uint64_t off_sm;
-    uint64_t off_hi;          /* FP16: the hi section (3 bits per element); 0 for the other formats */
+    uint64_t off_hi;          /* FP16: the hi section (a nibble per element); 0 for the other formats */
     uint64_t off_chunk;
     uint64_t off_block;
     uint64_t container_bytes; /* whole container, a multiple of 256 */

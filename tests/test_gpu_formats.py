@@ -216,8 +216,9 @@ def test_fp16_host_resident_container(afx):
     assert status == 0 and intact and np.array_equal(out, w)
 
 
-def test_fp16_every_hi_pattern_at_every_phase(afx):
-    # the 3-bit hi fields start at every bit phase (3i mod 8) with every value
+def test_fp16_every_hi_pattern_at_every_position(afx):
+    # every hi value in both nibbles of a byte and at every element of a
+    # group of 8 (the merge's word), with groups split at both range ends
     vals = np.array([(e << 10) | (h << 7) | m for e in (13, 14, 15, 16) for h in range(8) for m in (0, 5, 127)],
                     np.uint16)
     w = np.resize(np.random.default_rng(3).permutation(vals), 8 * 97 + 5)

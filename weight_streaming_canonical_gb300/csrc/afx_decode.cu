@@ -422,7 +422,8 @@ __device__ __forceinline__ void warp_store_e4m3(const uint8_t* stage, const uint
 
 // Joins and stores `count` FP16 elements from o0 with the 32 lanes of a
 // warp, as warp_store does for BF16, with each group of 8 also taking its
-// 24 hi-section bits (3 bytes from byte 3g / 8 for the group at element g).
+// 8 hi-section nibbles (the aligned word at byte g / 2 for the group at
+// element g).
 __device__ __forceinline__ void warp_store_fp16(const uint8_t* stage, const uint8_t* sm, const uint8_t* hi,
                                                 uint16_t* out, uint64_t o0, uint32_t count, int lane) {
     const uint64_t ob0 = o0 & ~uint64_t(7);
@@ -441,13 +442,8 @@ __device__ __forceinline__ void warp_store_fp16(const uint8_t* stage, const uint
         const uint2* smp = reinterpret_cast<const uint2*>(smb + f0);
         const uint2* stp = reinterpret_cast<const uint2*>(stage + f0);
         uint4* outp = reinterpret_cast<uint4*>(outb + f0);
-        const uint8_t* hg = hi + 3 * ((ob0 + f0) >> 3);  // the first full group's 3 bytes
-        for (uint32_t j = lane; j < nfull; j += 32) {
-            const uint8_t* h = hg + 3 * j;
-            const uint32_t h24 = static_cast<uint32_t>(__ldg(h)) | (static_cast<uint32_t>(__ldg(h + 1)) << 8) |
-                                 (static_cast<uint32_t>(__ldg(h + 2)) << 16);
-            __stcs(outp + j, fp16_join8(stp[j], __ldg(smp + j), h24));
-        }
+        const uint32_t* hg = reinterpret_cast<const uint32_t*>(hi) + ((ob0 + f0) >> 3);  // the first full group's nibbles
+        for (uint32_t j = lane; j < nfull; j += 32) __stcs(outp + j, fp16_join8(stp[j], __ldg(smp + j), __ldg(hg + j)));
     }
 }
 
@@ -587,8 +583,8 @@ __device__ __forceinline__ bool warp_run(const TabView& tv, WarpSlot& ws, uint8_
                 } else {
                     const uint64_t a0 = o0 & ~uint64_t(15), a1 = (o1 + 15) & ~uint64_t(15);
                     prefetch_l2(sm + a0, static_cast<uint32_t>(a1 - a0));
-                    if constexpr (Epi::kRaw == kRawBytesHi) {  // and the hi section's bits of the range
-                        const uint64_t h0 = ((3 * o0) >> 3) & ~uint64_t(15), h1 = (((3 * o1 + 7) >> 3) + 15) & ~uint64_t(15);
+                    if constexpr (Epi::kRaw == kRawBytesHi) {  // and the hi section's nibbles of the range
+                        const uint64_t h0 = (o0 >> 1) & ~uint64_t(15), h1 = (((o1 + 1) >> 1) + 15) & ~uint64_t(15);
                         prefetch_l2(t.hi + h0, static_cast<uint32_t>(h1 - h0));
                     }
                 }
@@ -761,7 +757,7 @@ __global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
     restore_warps<true, false>(a, StoreE4M3Epilogue{});
 }
 
-// The restore of FP16 containers (raw bytes plus the hi section's 3 bits per
+// The restore of FP16 containers (raw bytes plus the hi section's nibble per
 // element), from device memory and from pinned host memory.
 __global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
     restore_store_fp16_kernel(const __grid_constant__ LaunchArgs a) {
@@ -885,7 +881,7 @@ __global__ void fill_store_kernel(const uint8_t* __restrict__ sm, const uint64_t
 
 // E4M3 with one exponent for every element: 16 elements (8 raw bytes) per
 // group; the ragged last group goes out element by element.
-// FP16 with one exponent for every element: 8 elements (8 raw bytes, 3 hi
+// FP16 with one exponent for every element: 8 elements (8 raw bytes, 4 hi
 // bytes) per group; the ragged last group goes out element by element.
 __global__ void fill_store_fp16_kernel(const uint8_t* __restrict__ raw, const uint8_t* __restrict__ hi,
                                        const uint64_t* __restrict__ block_index, uint32_t fill, uint64_t n,
@@ -897,11 +893,9 @@ __global__ void fill_store_fp16_kernel(const uint8_t* __restrict__ raw, const ui
          g += static_cast<uint64_t>(gridDim.x) * blockDim.x) {
         const uint64_t ob = g << 3;
         if (ob + 8 <= n) {
-            const uint8_t* h = hi + 3 * g;
-            const uint32_t h24 = static_cast<uint32_t>(h[0]) | (static_cast<uint32_t>(h[1]) << 8) |
-                                 (static_cast<uint32_t>(h[2]) << 16);
+            const uint32_t h32 = __ldg(reinterpret_cast<const uint32_t*>(hi) + g);
             const uint2 r8 = __ldg(reinterpret_cast<const uint2*>(raw + ob));
-            __stcs(reinterpret_cast<uint4*>(out + ob), fp16_join8(make_uint2(s4, s4), r8, h24));
+            __stcs(reinterpret_cast<uint4*>(out + ob), fp16_join8(make_uint2(s4, s4), r8, h32));
         } else {
             for (uint64_t o = ob; o < n; ++o) out[o] = fp16_join1(s1, raw[o], fp16_hi3(hi, o));
         }

@@ -126,8 +126,9 @@ unsigned symbol_range(uint32_t fmt) { return fmt == AFX_FMT_E4M3 ? 16u : fmt == 
 
 uint64_t raw_bytes(uint32_t fmt, uint64_t n) { return fmt == AFX_FMT_E4M3 ? (n + 1) / 2 : n; }
 
-// FP16's hi section: 3 bits per element.
-uint64_t hi_bytes(uint32_t fmt, uint64_t n) { return fmt == AFX_FMT_FP16 ? (3 * n + 7) / 8 : 0; }
+// FP16's hi section: one nibble per element (the 3 leading fraction bits,
+// bit 3 zero), element i in the low nibble of byte i / 2 for even i.
+uint64_t hi_bytes(uint32_t fmt, uint64_t n) { return fmt == AFX_FMT_FP16 ? (n + 1) / 2 : 0; }
 
 // The coded symbol is the exponent: BF16 bits 14..7, FP16 bits 14..10,
 // E4M3 bits 6..3.  The raw byte of the 16-bit formats is the sign and bits
@@ -333,12 +334,8 @@ afx_status afx_encode(const void* w, uint64_t n, const afx_code* code, const afx
             } else {
                 sm[i] = static_cast<uint8_t>(raw_of(fmt, v));
             }
-            if (fmt == AFX_FMT_FP16) {  // the 3 leading fraction bits, packed lowest bit first
-                const uint32_t h3 = (v >> 7) & 0x7u;
-                const uint64_t bit = 3 * i;
-                hs[bit >> 3] |= static_cast<uint8_t>(h3 << (bit & 7));
-                if ((bit & 7) > 5) hs[(bit >> 3) + 1] |= static_cast<uint8_t>(h3 >> (8 - (bit & 7)));
-            }
+            if (fmt == AFX_FMT_FP16)  // the 3 leading fraction bits, a nibble per element
+                hs[i / 2] |= static_cast<uint8_t>(((v >> 7) & 0x7u) << (4 * (i & 1)));
         }
     });
 

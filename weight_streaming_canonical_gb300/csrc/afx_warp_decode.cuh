@@ -65,7 +65,7 @@ struct CodeTables {
 struct TensorArgs {
     const uint32_t* exp_words;
     const uint8_t* sm;
-    const uint8_t* hi;         // FP16: the 3 leading fraction bits per element (nullptr otherwise)
+    const uint8_t* hi;         // FP16: the 3 leading fraction bits, a nibble per element (nullptr otherwise)
     const uint16_t* chunk_index;
     const uint64_t* block_index;
     uint64_t n, n_chunks, n_blocks, exp_bytes;
@@ -271,26 +271,20 @@ __device__ __forceinline__ uint2 fp16_join4(uint32_t s4, uint32_t r4, uint32_t f
     return make_uint2(__byte_perm(lo, hi, 0x5140), __byte_perm(lo, hi, 0x7362));
 }
 
-// The 3-bit fields of four consecutive elements (12 bits, lowest first), one per byte.
-__device__ __forceinline__ uint32_t spread3x4(uint32_t t) {
-    return (t & 0x7u) | ((t & 0x38u) << 5) | ((t & 0x1C0u) << 10) | ((t & 0xE00u) << 15);
-}
-
-// Eight FP16 elements from their stage bytes, raw bytes and the 24 hi-section
-// bits of their group (element j at bits 3j .. 3j + 2).
-__device__ __forceinline__ uint4 fp16_join8(uint2 s8, uint2 r8, uint32_t h24) {
-    const uint2 a = fp16_join4(s8.x, r8.x, spread3x4(h24 & 0xFFFu));
-    const uint2 b = fp16_join4(s8.y, r8.y, spread3x4(h24 >> 12));
+// Eight FP16 elements from their stage bytes, raw bytes and the hi-section
+// word of their group (element j in nibble j, lowest first): the nibbles
+// are spread one per byte with two byte permutes, as for E4M3's raw
+// nibbles; fp16_join4 reads bits 0..2 of each (bit 3 is zero).
+__device__ __forceinline__ uint4 fp16_join8(uint2 s8, uint2 r8, uint32_t h32) {
+    const uint32_t even = h32 & 0x0F0F0F0Fu, odd = (h32 >> 4) & 0x0F0F0F0Fu;
+    const uint2 a = fp16_join4(s8.x, r8.x, __byte_perm(even, odd, 0x5140));
+    const uint2 b = fp16_join4(s8.y, r8.y, __byte_perm(even, odd, 0x7362));
     return make_uint4(a.x, a.y, b.x, b.y);
 }
 
-// The 3 leading fraction bits of FP16 element o (two bytes read: the field
-// may straddle them; the byte after the section's last is still inside the
-// container).
+// The 3 leading fraction bits of FP16 element o: its hi-section nibble.
 __device__ __forceinline__ uint32_t fp16_hi3(const uint8_t* hi, uint64_t o) {
-    const uint64_t bit = 3 * o;
-    const uint32_t w = static_cast<uint32_t>(hi[bit >> 3]) | (static_cast<uint32_t>(hi[(bit >> 3) + 1]) << 8);
-    return (w >> (bit & 7u)) & 0x7u;
+    return (static_cast<uint32_t>(hi[o >> 1]) >> (4u * static_cast<uint32_t>(o & 1u))) & 0x7u;
 }
 
 __device__ __forceinline__ uint16_t fp16_join1(uint32_t s, uint32_t r, uint32_t h) {
