@@ -250,8 +250,11 @@ def exponent_entropy_bits(parts) -> float:
 
 def algorithmic_bytes(d) -> int:
     """Bytes a restore must move: coded symbol bits, the raw bits (a sign|mantissa
-    byte per element, plus FP16's 3 hi-section bits; a nibble for E4M3), chunk
-    and block index entries read; the elements written (2 bytes each; 1 for E4M3)."""
+    byte per element, plus FP16's 3 leading fraction bits; a nibble for E4M3),
+    chunk and block index entries read; the elements written (2 bytes each; 1
+    for E4M3).  FP16's hi section holds the 3 bits in a nibble: its fourth
+    bit is the format's padding and is not counted, so the FP16 fraction
+    errs low."""
     fmt = getattr(d, "format", 0)
     raw, out = ((d.n + 1) // 2, d.n) if fmt == 2 else (d.n, 2 * d.n)
     if fmt == 1:
