@@ -1,7 +1,8 @@
 """The bounds-checked build (AFX_DEBUG_BOUNDS=1, libafx_debug.so) on the
 restore path: across ragged sizes, the 12-bit-table path, long codes, host
-containers, E4M3 and FP16 elements, the fused GEMV and corrupt containers, no range a kernel
-touches ever leaves its buffer.  The check runs in a child process that
+containers, E4M3 and FP16 elements, partial state tables (escapes), the
+fused GEMV and corrupt containers, no range a kernel touches ever leaves
+its buffer.  The check runs in a child process that
 loads the debug library; compute-sanitizer is not available here."""
 import json
 import os
@@ -57,6 +58,18 @@ statuses.append(("e4m3 host", w.size, st, bool(np.array_equal(got, w))))
 w = synth.normal_fp16(300_001, seed=8)
 got, st = restore(*afx.encode(w, fmt=afx.AFX_FMT_FP16))
 statuses.append(("fp16", w.size, st, bool(np.array_equal(got, w))))
+# a tree past the state table (rows for its shallowest nodes, escapes)
+w = synth.exponent_mix(400_003, 90, ratio=0.9, seed=31)
+cp, dp = afx.encode(w)
+assert afx.afx_decode_table_kind(dp)[0] == afx.AFX_TABLE_PARTIAL
+got, st = restore(cp, dp)
+statuses.append(("partial", w.size, st, bool(np.array_equal(got, w))))
+got, st = restore(cp, dp, host=True)
+statuses.append(("partial host", w.size, st, bool(np.array_equal(got, w))))
+bad = cp.copy()
+bad[dp.off_exp: dp.off_exp + dp.n_chunks * dp.chunk_bytes] = np.random.default_rng(12).integers(
+    0, 256, size=dp.n_chunks * dp.chunk_bytes, dtype=np.uint8)
+statuses.append(("garbage partial", 0, restore(bad, dp)[1], None))
 # corrupt containers: must be flagged, never read or write out of range
 rng = np.random.default_rng(9)
 w = synth.normal(400_000, seed=6)
@@ -83,13 +96,24 @@ st = torch.zeros(1, dtype=torch.int32, device="cuda")
 afx.afx_decode_gemv(d, torch.from_numpy(c).cuda(), rows, cols, x, y, ws, status_dev=st)
 torch.cuda.synchronize()
 statuses.append(("gemv", rows * cols, int(st.item()), None))
+# the fused GEMV with a partial state table
+W = synth.exponent_mix(rows * cols, 90, ratio=0.9, seed=8)
+c, d = afx.encode(W)
+y4 = torch.empty((4, rows), dtype=torch.float32, device="cuda")
+x4 = torch.from_numpy(synth.activations(4, cols, seed=2).view(np.int16)).cuda()
+ws = torch.empty(afx.afx_decode_gemv_workspace(d, 4) // 4 + 4, dtype=torch.float32, device="cuda")
+st.zero_()
+afx.afx_decode_gemv(d, torch.from_numpy(c).cuda(), rows, cols, x4, y4, ws, status_dev=st)
+torch.cuda.synchronize()
+statuses.append(("gemv partial", rows * cols, int(st.item()), None))
 # randomized corruption: bytes of every section replaced, flipped or zeroed,
 # in all three formats; the kernels must flag or restore, never leave a buffer
 rng = np.random.default_rng(2026)
 fuzz_flagged = fuzz_exact = 0
 bases = [afx.encode(synth.normal(300_001, seed=21)), afx.encode(synth.normal_fp16(200_003, seed=22), fmt=1),
-         afx.encode(synth.normal_e4m3(300_007, seed=23), fmt=2), afx.encode(synth.adversarial(1 << 18, seed=24))]
-for trial in range(120):
+         afx.encode(synth.normal_e4m3(300_007, seed=23), fmt=2), afx.encode(synth.adversarial(1 << 18, seed=24)),
+         afx.encode(synth.exponent_mix(200_003, 90, ratio=0.9, seed=25))]
+for trial in range(150):
     c0, d = bases[trial % len(bases)]
     bad = c0.copy()
     section = trial % 4
@@ -123,7 +147,7 @@ def test_bounds_checked_build_reports_no_violation():
     rep = json.loads(r.stdout.strip().splitlines()[-1])
     assert rep["checked"]
     for kind, size, status, exact in rep["cases"]:
-        if kind in ("garbage stream", "chunk index", "block index"):
+        if kind in ("garbage stream", "chunk index", "block index", "garbage partial"):
             assert status != 0, kind
         elif kind == "fuzz":
             assert size > 0  # corruptions the kernels flagged

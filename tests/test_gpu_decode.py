@@ -344,6 +344,29 @@ def test_batch_of_mixed_tensors_in_one_launch(afx):
         assert np.array_equal(got[:w.size], w)
 
 
+def test_the_next_kernel_on_the_stream_sees_every_output(afx):
+    # a call of several launches (the ones after the first may start while
+    # the one before it finishes): work queued on the same stream right
+    # after it, with no synchronisation between, reads finished outputs
+    import torch
+    ws = [synth.normal(1_000_003 + 1001 * i, seed=300 + i) for i in range(40)]
+    enc = [afx.encode(w) for w in ws]
+    conts = [torch.from_numpy(c).cuda() for c, _ in enc]
+    refs = [torch.from_numpy(w.view(np.int16)).cuda() for w in ws]
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    for rep in range(3):
+        outs = [torch.full((w.size,), 0x5A5A, dtype=torch.int16, device="cuda") for w in ws]
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            afx.afx_decode_batch([d for _, d in enc], conts, outs, stream=stream, status_dev=status)
+            # compared on the device, on the same stream, before any host synchronisation
+            flags = torch.stack([(o == r).all() for o, r in zip(outs, refs)])
+        torch.cuda.synchronize()
+        assert status.item() == 0 and bool(flags.all()), rep
+
+
 def test_batch_longer_than_one_launch(afx):
     import torch
     tensors = [synth.normal(50_000 + 37 * i, seed=100 + i) for i in range(37)]  # more than 16 per launch
