@@ -1149,24 +1149,6 @@ def run_formats_bench(afx, dev, args):
 
 
 WIDE_TREES = ((51, 0.85), (52, 0.85), (57, 0.85), (80, 0.9), (100, 0.92), (120, 0.94))
-TAIL_FRACTION = 1e-3  # the long-tail case: this share of the weights gets an exponent drawn from 1..254
-
-
-def long_tail_weights(n: int, seed: int = 0):
-    """N(0, 0.02) BF16 weights with a share TAIL_FRACTION of them given an
-    exponent drawn uniformly from 1..254 (the shape of a checkpoint with
-    rare outliers across the whole range): a wide code tree whose deep
-    nodes are rarely reached."""
-    import numpy as np
-    from weight_streaming_canonical_gb300 import synth
-    w = synth.normal(n, seed=seed)
-    rng = np.random.default_rng(seed + 17)
-    pick = rng.choice(n, size=int(n * TAIL_FRACTION), replace=False)
-    e = rng.integers(1, 255, size=pick.size).astype(np.uint16)
-    w[pick] = (w[pick] & np.uint16(0x807F)) | (e << np.uint16(7))
-    return w
-
-
 def run_wide_trees_bench(afx, dev, args, layer_weights_per_s=None):
     """Restore rate against the size of the code tree: one 2^27-weight tensor
     per exponent mix (geometric exponent frequencies, synth.exponent_mix),
@@ -1184,7 +1166,7 @@ def run_wide_trees_bench(afx, dev, args, layer_weights_per_s=None):
     cases = [(f"mix{n_exp}", n_exp, ratio) for n_exp, ratio in WIDE_TREES] + [("tail", None, None)]
     for label, n_exp, ratio in cases:
         if n_exp is None:
-            w = long_tail_weights(1 << 27, seed=3)
+            w = synth.long_tail(1 << 27, seed=3)
         else:
             w = synth.exponent_mix(1 << 27, n_exp, ratio=ratio, seed=n_exp)
         c, d = afx.encode(w)

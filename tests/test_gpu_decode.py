@@ -91,11 +91,7 @@ def test_partial_state_table_with_a_long_tail(afx):
     # the layer's distribution plus rare exponents across the whole range (the
     # shape of a checkpoint with outliers): 254 exponents, escapes are rare
     # and the rare codes are up to 19 bits long
-    rng = np.random.default_rng(5)
-    w = synth.normal(4_000_000, seed=5)
-    pick = rng.choice(w.size, size=4000, replace=False)
-    e = rng.integers(1, 255, size=pick.size).astype(np.uint16)
-    w[pick] = (w[pick] & np.uint16(0x807F)) | (e << np.uint16(7))
+    w = synth.long_tail(4_000_000, seed=5)
     c, d = _check(afx, w, out_pad=16)
     assert d.nsym > 60 and d.max_len > 16 and afx.afx_decode_table_kind(d)[0] == afx.AFX_TABLE_PARTIAL
 

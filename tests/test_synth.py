@@ -76,3 +76,17 @@ def test_adversarial_mix():
     assert np.count_nonzero(w >> 15) > 0.4 * n  # both signs
     quiet = np.count_nonzero((e == 0xFF) & ((m & 0x40) != 0))
     assert 0 < quiet < nan  # quiet and signalling NaNs both present
+
+
+def test_long_tail_mix():
+    # N(0, 0.02) with 0.1 % of the weights moved to exponents across 1..254,
+    # their sign and mantissa kept; deterministic per seed
+    n = 1 << 20
+    base = synth.normal(n, seed=4)
+    w = synth.long_tail(n, seed=4)
+    assert np.array_equal(w, synth.long_tail(n, seed=4))
+    moved = np.flatnonzero(w != base)
+    assert 0.8e-3 * n < moved.size <= 1e-3 * n
+    assert np.array_equal(w[moved] & 0x807F, base[moved] & 0x807F)
+    e = (w[moved] >> 7) & 0xFF
+    assert e.min() >= 1 and e.max() <= 254 and np.unique(e).size > 200

@@ -287,6 +287,20 @@ def exponent_mix(n: int, n_exponents: int, ratio: float = 0.85, first: int = 100
     return (low & np.uint16(0x807F)) | (e << np.uint16(7))
 
 
+def long_tail(n: int, tail: float = 1e-3, seed: int = 0) -> np.ndarray:
+    """N(0, 0.02) BF16 weights with a share `tail` of them (chosen uniformly,
+    sign and mantissa kept) given an exponent drawn uniformly from 1..254:
+    the shape of a checkpoint with rare outliers across the whole range, a
+    code tree of about 250 internal nodes whose deep nodes are rarely
+    reached."""
+    w = normal(n, seed=seed)
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([int(seed), 107])))
+    pick = rng.choice(int(n), size=int(n * tail), replace=False)
+    e = rng.integers(1, 255, size=pick.size).astype(np.uint16)
+    w[pick] = (w[pick] & np.uint16(0x807F)) | (e << np.uint16(7))
+    return w
+
+
 def all_bf16_patterns() -> np.ndarray:
     """Every one of the 65,536 BF16 bit patterns, in order."""
     return np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
