@@ -795,9 +795,14 @@ __global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
 
 // Rows of the warp GEMV: the sub-tile in which a row starts adds its own
 // partial of the row and the first-row partials of the following sub-tiles
-// that still lie in the row, in sub-tile order.  One thread per sub-tile.
+// that still lie in the row, in sub-tile order.  One thread per sub-tile;
+// the following sub-tiles' starts and partials are loaded four at a time
+// (the sums still go in sub-tile order).  Launched as a programmatic
+// dependent of the GEMV kernel: it waits for that grid's completion before
+// reading anything.
 template <int B>
 __global__ void gemv_fixup_warp_kernel(const __grid_constant__ LaunchArgs a) {
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     const uint64_t g = blockIdx.x * static_cast<uint64_t>(blockDim.x) + threadIdx.x;
     if (g >= a.total_subs) return;
     uint32_t k = 0;
@@ -811,17 +816,36 @@ __global__ void gemv_fixup_warp_kernel(const __grid_constant__ LaunchArgs a) {
     const uint64_t cols = t.cols, n = t.n;
     const uint64_t o0 = ws_o0[s], o1 = s + 1 < n_sub ? ws_o0[s + 1] : n;
     if (o1 <= o0 || o1 > n) return;  // empty, or a corrupt stream the main kernel already flagged
-    const uint64_t ra = o0 / cols, r = (o1 - 1) / cols;
+    const bool narrow = o1 <= (uint64_t{1} << 32);  // 32-bit divisions
+    const uint64_t ra = narrow ? static_cast<uint32_t>(o0) / t.cols : o0 / cols;
+    const uint64_t r = narrow ? static_cast<uint32_t>(o1 - 1) / t.cols : (o1 - 1) / cols;
     const uint64_t row_start = r * cols, row_end = row_start + cols;
     if (row_start < o0 || r >= t.rows) return;  // the row began in an earlier sub-tile
     const int slot = r == ra ? 0 : 1;
     float sum[kMaxBatch];
 #pragma unroll
     for (int b = 0; b < B; ++b) sum[b] = part[(s * 2 + slot) * B + b];
-    for (uint64_t u = s + 1; u < n_sub; ++u) {
-        if (ws_o0[u] >= row_end) break;
+    constexpr int kAhead = 4;
+    bool more = true;
+    for (uint64_t u0 = s + 1; more && u0 < n_sub; u0 += kAhead) {
+        uint64_t start[kAhead];
+        float p[kAhead][kMaxBatch];
 #pragma unroll
-        for (int b = 0; b < B; ++b) sum[b] += part[(u * 2) * B + b];
+        for (int j = 0; j < kAhead; ++j) {
+            const uint64_t u = u0 + j;
+            start[j] = u < n_sub ? ws_o0[u] : row_end;
+#pragma unroll
+            for (int b = 0; b < B; ++b) p[j][b] = u < n_sub ? part[(u * 2) * B + b] : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < kAhead; ++j) {
+            if (!more || start[j] >= row_end) {
+                more = false;
+            } else {
+#pragma unroll
+                for (int b = 0; b < B; ++b) sum[b] += p[j][b];
+            }
+        }
     }
 #pragma unroll
     for (int b = 0; b < B; ++b) t.y[static_cast<uint64_t>(b) * t.rows + r] = sum[b];
@@ -1226,8 +1250,16 @@ afx_status launch_gemv_warp(LaunchArgs& la, cudaStream_t s) {
     kernel<<<static_cast<unsigned>(grid), warps * 32, smem, s>>>(la);
     AFX_CUDA_TRY(cudaGetLastError(), "restore_gemv_kernel launch");
     const unsigned fix_blocks = static_cast<unsigned>((la.total_subs + 255) / 256);
-    gemv_fixup_warp_kernel<B><<<fix_blocks, 256, 0, s>>>(la);
-    AFX_CUDA_TRY(cudaGetLastError(), "gemv_fixup_warp_kernel launch");
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(fix_blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    AFX_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemv_fixup_warp_kernel<B>, la), "gemv_fixup_warp_kernel launch");
     return AFX_OK;
 }
 
