@@ -551,6 +551,8 @@ def measure_restore(afx, parts, dev, args, workload: str, world: int = 1, local:
     launches_per_step = (coded + 15) // 16 + sum(1 for d in descs if d.nsym == 1 and d.n)
     cviews = [c for _, c, _ in views]
     oviews = [o for _, _, o in views]
+    # chunks a lane of the step's restore launches (the kernel that runs)
+    lanes = max(afx.afx_decode_chunks_a_lane(descs, cviews) + [0])
 
     def step():
         afx.afx_decode_batch(descs, cviews, oviews, status_dev=status)
@@ -643,10 +645,12 @@ def measure_restore(afx, parts, dev, args, workload: str, world: int = 1, local:
     peak, peak_kind = measured_hbm_peak()
     achieved = alg_total / (ms * 1e-3) / 1e9
     kernel_name = {1: "restore_store_fp16_kernel", 2: "restore_store_e4m3_kernel"}.get(fmt, "restore_store_kernel")
+    if lanes == 2:  # two chunks a lane
+        kernel_name = kernel_name.replace("_kernel", "_pair_kernel")
     traffic, traffic_src = restore_traffic(kernel_name, workload, n_total)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": traffic, "traffic_scope": "per step" + (f" ({traffic_src})" if traffic_src else ""),
-                "kernel": kernel_name, "peak_kind": peak_kind,
+                "kernel": kernel_name, "chunks_a_lane": lanes, "peak_kind": peak_kind,
                 "launches_per_step": launches_per_step, "algorithmic_bytes_per_step": alg_total,
                 "kernel_ms_per_step": ms,
                 "kernel_time": "graph replays holding only the restore launches (the launches' summed duration "

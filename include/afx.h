@@ -226,6 +226,28 @@ afx_status afx_decode_batch(const afx_desc* descs, const void* const* containers
 #define AFX_TABLE_PARTIAL 3u
 afx_status afx_decode_table_kind(const afx_desc* desc, uint32_t* kind, uint32_t* rows);
 
+/* How afx_decode_batch(descs, containers, ..., count, ...) would split the
+ * stream among the lanes of a warp on the current device, without
+ * launching anything: chunks[i] = 1 when container i's restore launch gives
+ * each lane one chunk (sub-tiles of 32 chunks), 2 when it gives each lane
+ * two consecutive chunks stepped as one span (sub-tiles of 64 chunks), and
+ * 0 for an empty tensor or a single-exponent fill.  Two chunks a lane are
+ * taken for BF16, FP16 and E4M3 containers in device memory whose launch
+ * gives each CTA at least 16 blocks and leaves each warp a stage that holds
+ * a 64-chunk sub-tile's codes; the environment variable
+ * AFX_CHUNKS_A_LANE=1 (or 2) forces one chunk a lane (or two wherever the
+ * stage fits, whatever the launch's size).  The fused GEMV at batch 1
+ * (afx_decode_gemv, afx_decode_gemv_batch) takes two chunks a lane by the
+ * same rules when every matrix's rows are at least as long as the stage.
+ * containers[i] is read only for
+ * where it lives (device or pinned host memory), not dereferenced.
+ * Cites: "Why Weight Offloading Slows Inference", section "Lossless
+ * compression: fewer bytes to read, more work to unpack" (the decoder that
+ * sets t_unpack).  Errors: as afx_decode_batch's host-side checks;
+ * AFX_E_ARG for a null chunks array. */
+afx_status afx_decode_chunks_a_lane(const afx_desc* descs, const void* const* containers, uint32_t count,
+                                    uint32_t* chunks);
+
 /* Device workspace (bytes) that afx_decode_gemv needs for this container
  * and batch: for every run of 32 chunks (16 per block) its first weight
  * index (8 bytes) and one float per batch row for each of the two output

@@ -113,6 +113,7 @@ _lib.afx_decode_table_kind.argtypes = [ctypes.POINTER(afx_desc), ctypes.POINTER(
 _lib.afx_decode_gemv.argtypes = [ctypes.POINTER(afx_desc), _vp, _u32, _u32, _vp, _u32, _vp, _vp, _u64, _vp, _i32p]
 _PP = ctypes.POINTER(ctypes.c_void_p)
 _lib.afx_decode_batch.argtypes = [ctypes.POINTER(afx_desc), _PP, _PP, _u32, _vp, _i32p]
+_lib.afx_decode_chunks_a_lane.argtypes = [ctypes.POINTER(afx_desc), _PP, _u32, ctypes.POINTER(ctypes.c_uint32)]
 _lib.afx_decode_gemv_batch.argtypes = [ctypes.POINTER(afx_desc), _PP, ctypes.POINTER(ctypes.c_uint32),
                                        ctypes.POINTER(ctypes.c_uint32), _PP, _u32, _PP, _PP,
                                        ctypes.POINTER(ctypes.c_uint64), _u32, _vp, _i32p]
@@ -332,6 +333,19 @@ def afx_decode_table_kind(desc: afx_desc) -> tuple:
     _check("afx_decode_table_kind", _lib.afx_decode_table_kind(ctypes.byref(desc), ctypes.byref(kind),
                                                                ctypes.byref(rows)))
     return int(kind.value), int(rows.value)
+
+
+def afx_decode_chunks_a_lane(descs, containers) -> list:
+    """For each container, the chunks a lane (1 or 2; 0 for a fill or an
+    empty tensor) that afx_decode_batch of these containers would take on
+    the current device."""
+    if len(descs) != len(containers):
+        raise ValueError("descs and containers must have the same length")
+    arr = (afx_desc * len(descs))(*descs)
+    bufs = (ctypes.c_void_p * len(containers))(*[_buf_ptr(t) for t in containers])
+    out = (ctypes.c_uint32 * max(1, len(descs)))()
+    _check("afx_decode_chunks_a_lane", _lib.afx_decode_chunks_a_lane(arr, bufs, len(descs), out))
+    return [int(out[i]) for i in range(len(descs))]
 
 
 def afx_decode_gemv_workspace(desc: afx_desc, batch: int) -> int:

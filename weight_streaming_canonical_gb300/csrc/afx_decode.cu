@@ -37,6 +37,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
 #include <cstddef>
 #include <cstdio>
 #include <cstring>
@@ -455,6 +456,7 @@ constexpr int kRawBytes = 0, kRawBytesHi = 1, kRawNibbles = 2;
 constexpr uint32_t kKindBF16 = 0, kKindFP16 = 1, kKindE4M3 = 2;
 
 struct StoreEpilogue {
+    static constexpr bool kSlots = false;  // the sub-tile index is not used
     static constexpr int kRaw = kRawBytes;
     __device__ __forceinline__ void operator()(const uint8_t* stage, const TensorArgs& t, uint64_t, uint64_t o0,
                                                uint32_t count, bool ok, int lane) const {
@@ -463,6 +465,7 @@ struct StoreEpilogue {
 };
 
 struct StoreFP16Epilogue {
+    static constexpr bool kSlots = false;  // the sub-tile index is not used
     static constexpr int kRaw = kRawBytesHi;
     __device__ __forceinline__ void operator()(const uint8_t* stage, const TensorArgs& t, uint64_t, uint64_t o0,
                                                uint32_t count, bool ok, int lane) const {
@@ -471,6 +474,7 @@ struct StoreFP16Epilogue {
 };
 
 struct StoreE4M3Epilogue {
+    static constexpr bool kSlots = false;  // the sub-tile index is not used
     static constexpr int kRaw = kRawNibbles;
     __device__ __forceinline__ void operator()(const uint8_t* stage, const TensorArgs& t, uint64_t, uint64_t o0,
                                                uint32_t count, bool ok, int lane) const {
@@ -480,10 +484,18 @@ struct StoreE4M3Epilogue {
 
 template <int B>
 struct GemvEpilogue {
+    static constexpr bool kSlots = true;  // one workspace slot per 32-chunk sub-tile index
     static constexpr int kRaw = kRawBytes;
     __device__ __forceinline__ void operator()(const uint8_t* stage, const TensorArgs& t, uint64_t s, uint64_t o0,
                                                uint32_t count, bool ok, int lane) const {
         warp_gemv<B>(stage, t, s, o0, count, ok, lane);
+    }
+    // Slot s holds no weights: its start o and zero partials.
+    __device__ __forceinline__ void empty(const TensorArgs& t, uint64_t s, uint64_t o, int lane) const {
+        uint64_t* ws_o0 = reinterpret_cast<uint64_t*>(t.ws);
+        float* part = reinterpret_cast<float*>(ws_o0 + t.n_blocks * kSubtilesPerBlock);
+        if (lane < 2 * B) part[s * 2 * B + lane] = 0.f;
+        if (lane == 0) ws_o0[s] = o;
     }
 };
 
@@ -667,6 +679,236 @@ __device__ __forceinline__ bool warp_run(const TabView& tv, WarpSlot& ws, uint8_
     return true;
 }
 
+// ---- two chunks a lane ------------------------------------------------------------
+//
+// The same restore with sub-tiles of 64 chunks: lane l steps chunks 2l and
+// 2l + 1 as one span of 2T bytes, from the first chunk's gap to the code
+// that crosses the second chunk's end.  The work done once a chunk (the gap
+// skip, the code crossing the end) and once a sub-tile (staging, scan, the
+// merge's ragged ends) is then spread over twice the weights; the
+// container is the same.  A span needs the first entry's gap and the sum of
+// the two counts: the second entry's gap is not read (a corrupt one cannot
+// change the result) and its count is checked through the sum.  Each warp
+// has one stream buffer: the next sub-tile's copy is issued as soon as the
+// lanes have read this one, and lands while the warp merges.  The stage
+// holds LaunchArgs::pair_stage bytes; a sub-tile whose codes do not fit in
+// it with kPairStageSlack to spare is decoded and merged as two halves of
+// 16 lanes.
+constexpr int kPairChunks = 2 * kWarpChunks;                   // chunks per sub-tile
+constexpr int kPairSubtilesPerBlock = kThreads / kPairChunks;  // 8
+constexpr int kPairChunkStage = 72;                            // 65 entries staged (144 bytes)
+// Stage bytes past a sub-tile's codes that its lanes may write: a lane's
+// byte steps emit up to 2 * kMaxChunkCodes + 1 codes whatever its count
+// says, and store whole words.
+constexpr uint32_t kPairStageSlack = 2 * kMaxChunkCodes + 8;
+// The smallest stage: a half's codes (16 spans) with the slack, the
+// sub-tile's offset within its group of 8 and 16 spare bytes.
+constexpr uint32_t kPairStageMin = (16 * 2 * kMaxChunkCodes + kPairStageSlack + 7 + 16 + 15) & ~15u;
+
+struct PairSlot {
+    alignas(16) uint16_t chunk[kPairChunkStage];
+    uint64_t bar;  // completion of the copies into the stream buffer and chunk
+    uint64_t unused;
+};
+static_assert(sizeof(PairSlot) % 16 == 0, "pair slots keep the stage 16-byte aligned");
+
+// Shared memory of one warp: its slot, its stage, its stream buffer.
+__host__ __device__ constexpr uint32_t pair_warp_bytes(uint32_t max_chunk_bytes, uint32_t stage) {
+    return static_cast<uint32_t>(sizeof(PairSlot)) + stage + kPairChunks * max_chunk_bytes + kStreamPad;
+}
+
+// Bytes staged for sub-tile s: its stream bytes plus the pad, and its 72
+// chunk entries, or what the sections hold of them.  Both are multiples of
+// 16.  A full sub-tile has all of them: s < n_sub_full / 2, since sub-tile s
+// is full exactly when the 32-chunk sub-tile 2s + 1 is.
+__device__ __forceinline__ uint2 pair_tile_bytes(const TensorArgs& t, uint64_t s, bool full, uint32_t sub_bytes) {
+    if (full) return make_uint2(sub_bytes + kStreamPad, kPairChunkStage * 2);
+    const uint64_t byte0 = s * sub_bytes, want = sub_bytes + kStreamPad;
+    const uint64_t avail = t.exp_bytes > byte0 ? t.exp_bytes - byte0 : 0;
+    const uint64_t cb0 = s * kPairChunks * 2;
+    const uint64_t csec = (t.n_chunks * 2 + 15) & ~uint64_t(15);
+    const uint64_t cavail = csec > cb0 ? csec - cb0 : 0;
+    return make_uint2(static_cast<uint32_t>(want < avail ? want : avail),
+                      static_cast<uint32_t>(cavail < kPairChunkStage * 2 ? cavail : kPairChunkStage * 2));
+}
+
+__device__ __forceinline__ void pair_issue_bulk(PairSlot& ps, uint8_t* stream_dst, const TensorArgs& t, uint64_t s,
+                                                bool full, uint32_t sub_bytes, bool stall) {
+    const uint2 nb = pair_tile_bytes(t, s, full, sub_bytes);
+    AFX_CHECK(nb.x <= sub_bytes + kStreamPad && nb.y <= kPairChunkStage * 2, kChkStagingBytes);
+    mbar_expect_tx(&ps.bar, nb.x + nb.y);
+    if (stall) return;  // failure injection: the bytes never come
+    if (nb.x) bulk_copy_g2s(stream_dst, reinterpret_cast<const uint8_t*>(t.exp_words) + s * sub_bytes, nb.x, &ps.bar);
+    if (nb.y) bulk_copy_g2s(ps.chunk, t.chunk_index + s * kPairChunks, nb.y, &ps.bar);
+}
+
+// Restores the 64-chunk sub-tiles [s0, s1) of tensor t with one warp
+// (device-resident containers).  phase is the parity the warp's copy
+// barrier waits for next.  Returns false when a staging copy timed out.
+// The epilogue of sub-tile s gets index 2s for its first (or only) pass
+// and 2s + 1 for its second: a GEMV keeps the workspace layout of 32-chunk
+// sub-tiles, with an empty slot 2s + 1 (no weights, zero partials) when
+// the sub-tile was merged whole.
+template <class Epi>
+__device__ __forceinline__ bool warp_run_pair(const TabView& tv, PairSlot& ps, uint8_t* stage, uint32_t stage_cap,
+                                              uint8_t* wstream, const TensorArgs& t, uint64_t s0, uint64_t s1,
+                                              int lane, int32_t* status, uint32_t wait_limit, bool stall,
+                                              uint32_t& phase, const Epi& epi) {
+    const uint32_t T = t.chunk_bytes;
+    const uint32_t chunk_bits = 8u * T, span_words = T >> 1;
+    const uint32_t sub_bytes = kPairChunks * T, sub_bits = 8u * sub_bytes;
+    const bool fsm = t.tab.fsm != 0;
+    const uint32_t skip_row0 = t.tab.fsm_rows * kFsmRowBytes;
+    const uint64_t n_sub = (t.n_chunks + kPairChunks - 1) / kPairChunks;
+    const uint64_t n_full = t.n_sub_full / 2;
+    const uint8_t* const sm = t.sm;
+    const uint64_t n = t.n;
+    // the output index of sub-tile s0's first code
+    const uint64_t blk = s0 / kPairSubtilesPerBlock;
+    uint32_t pre = 0;
+    for (uint64_t c = blk * kThreads + lane; c < s0 * kPairChunks; c += 32) pre += __ldg(t.chunk_index + c) >> 5;
+    pre = warp_sum(pre);
+    uint64_t start = __ldg(t.block_index + blk) + pre;
+    if (s0 == 0 && start != 0 && lane == 0) raise_status(status, AFX_DEV_BAD_BLOCK);
+    if (lane == 0) pair_issue_bulk(ps, wstream, t, s0, s0 < n_full, sub_bytes, stall);
+    const uint32_t* stream = reinterpret_cast<const uint32_t*>(wstream);
+    const uint32_t nrun = static_cast<uint32_t>(s1 - s0);
+    uint32_t sub_in_block = static_cast<uint32_t>(s0 % kPairSubtilesPerBlock);
+    for (uint32_t r = 0; r < nrun; ++r) {
+        const uint64_t s = s0 + r;
+        const bool arrived = mbar_wait(&ps.bar, phase, wait_limit);
+        phase ^= 1u;
+        if (!__all_sync(0xFFFFFFFFu, arrived)) {
+            // the copy may still land: the caller reports that (AFX_DEV_UNDRAINED)
+            if (lane == 0) raise_status(status, AFX_DEV_TIMEOUT);
+            return false;
+        }
+        if (r != 0 && sub_in_block == 0) {  // a block boundary inside the run
+            const uint64_t bo = __ldg(t.block_index + s / kPairSubtilesPerBlock);
+            if (bo != start) {
+                if (lane == 0) raise_status(status, AFX_DEV_BAD_BLOCK);
+                start = bo;
+            }
+        }
+        const bool full = s < n_full;
+        const uint32_t nexist = full ? static_cast<uint32_t>(kPairChunkStage)
+                                     : static_cast<uint32_t>(min(t.n_chunks - min(t.n_chunks, s * kPairChunks),
+                                                                 uint64_t{kPairChunkStage}));
+        const uint32_t ia = 2u * static_cast<uint32_t>(lane);
+        const uint32_t ea = ia < nexist ? ps.chunk[ia] : 0u;
+        const uint32_t eb = ia + 1 < nexist ? ps.chunk[ia + 1] : 0u;
+        const uint32_t next = ia + 2 < nexist ? ps.chunk[ia + 2] : 0u;
+        const uint32_t gap = ea & 31u;
+        uint32_t cnt = (ea >> 5) + (eb >> 5);
+        bool bad = false;
+        if (gap > 23u || (ea >> 5) > chunk_bits - gap || (ea >> 5) > static_cast<uint32_t>(kMaxChunkCodes) ||
+            (eb & 31u) > 23u || (eb >> 5) > chunk_bits - (eb & 31u) ||
+            (eb >> 5) > static_cast<uint32_t>(kMaxChunkCodes)) {
+            bad = true;
+            cnt = 0;
+        }
+        uint32_t inc = cnt;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, inc, d);
+            if (lane >= d) inc += o;
+        }
+        const uint32_t total = __shfl_sync(0xFFFFFFFFu, inc, 31);
+        const uint32_t half = __shfl_sync(0xFFFFFFFFu, inc, 15);  // the codes of lanes 0..15
+        // a corrupt block index can put start anywhere: start <= n keeps the
+        // end from wrapping past 2^64 back into [0, n]
+        const bool in_range = start <= n && start + total <= n;
+        if (lane == 0) {
+            const uint64_t o0 = start, o1 = start + total;
+            if (!in_range)
+                raise_status(status, AFX_DEV_BAD_BLOCK);
+            else if (o0 < o1) {  // the raw bytes are needed after the decode
+                if constexpr (Epi::kRaw == kRawNibbles) {
+                    const uint64_t a0 = (o0 >> 1) & ~uint64_t(15), a1 = (((o1 + 1) >> 1) + 15) & ~uint64_t(15);
+                    prefetch_l2(sm + a0, static_cast<uint32_t>(a1 - a0));
+                } else {
+                    const uint64_t a0 = o0 & ~uint64_t(15), a1 = (o1 + 15) & ~uint64_t(15);
+                    prefetch_l2(sm + a0, static_cast<uint32_t>(a1 - a0));
+                    if constexpr (Epi::kRaw == kRawBytesHi) {  // and the hi section's nibbles of the range
+                        const uint64_t h0 = (o0 >> 1) & ~uint64_t(15), h1 = (((o1 + 1) >> 1) + 15) & ~uint64_t(15);
+                        prefetch_l2(t.hi + h0, static_cast<uint32_t>(h1 - h0));
+                    }
+                }
+            }
+        }
+        const bool split = (static_cast<uint32_t>(start) & 7u) + total + kPairStageSlack > stage_cap;
+        for (uint32_t p = 0; p < 2u; ++p) {
+            if (p && !split) break;
+            const uint32_t before = p ? half : 0u;  // codes merged by the earlier pass
+            bool lbad = bad, stepped = false;
+            FsmLane fl;
+            if ((!split || (static_cast<uint32_t>(lane) >> 4) == p) && cnt && in_range) {
+                const uint32_t s_run = (static_cast<uint32_t>(start + before) & 7u) + (inc - cnt) - before;
+                const uint32_t span_end = (static_cast<uint32_t>(lane) + 1u) * 2u * chunk_bits;
+                AFX_CHECK(s_run + 2u * kMaxChunkCodes + 8u <= stage_cap, kChkStageRun);
+                AFX_CHECK((lane + 1) * span_words <= (sub_bytes + kStreamPad) >> 2, kChkStreamWords);
+                uint32_t stream_end = sub_bits;
+                if (!full) {
+                    const uint64_t bit0 = s * static_cast<uint64_t>(sub_bits);
+                    const uint64_t left = t.total_bits > bit0 ? t.total_bits - bit0 : 0;
+                    stream_end = left < sub_bits ? static_cast<uint32_t>(left) : sub_bits;
+                }
+                if (fsm) {
+                    if (span_end <= stream_end) {
+                        fsm_chunk_steps(tv, stream + lane * span_words, span_words, gap, skip_row0, stage, s_run, fl,
+                                        stage_cap);
+                        stepped = true;
+                    } else {  // the stream's partial last chunk
+                        lbad = decode_run_fsm(tv, stream, lane * span_words, gap, cnt, stage, s_run, next, span_end,
+                                              stream_end);
+                    }
+                } else {
+                    lbad = decode_run(tv, stream, pair_tile_bytes(t, s, full, sub_bytes).x >> 2, lane * span_words,
+                                      gap, cnt, stage, s_run, next, span_end);
+                }
+            }
+            __syncwarp();
+            if (stepped) {
+                AFX_CHECK(reinterpret_cast<uint8_t*>(fl.wout) + 4 <= stage + stage_cap, kChkStagePending);
+                lbad = fsm_chunk_finish(tv, stream, fl, cnt, (static_cast<uint32_t>(lane) + 1u) * 2u * chunk_bits,
+                                        next);
+            }
+            if (!split || p) {  // the last reads of this stream buffer: refill it
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && r + 1 < nrun) pair_issue_bulk(ps, wstream, t, s + 1, s + 1 < n_full, sub_bytes, stall);
+            }
+            if (lbad) raise_status(status, AFX_DEV_BAD_CHUNK);
+            const bool ok = !__any_sync(0xFFFFFFFFu, lbad) && in_range;
+            __syncwarp();
+            const uint32_t ptotal = split ? (p ? total - half : half) : total;
+            if (ok) {
+                AFX_CHECK(((start + before) & 7u) + ptotal <= static_cast<uint64_t>(stage_cap), kChkMergeStage);
+                AFX_CHECK(start + before + ptotal <= n, kChkMergeOutput);
+            }
+            // the pass's workspace slot (GEMV): 2s and 2s + 1, one per half;
+            // a sub-tile merged whole leaves slot 2s + 1 empty at its end
+            epi(stage, t, 2 * s + p, start + before, ptotal, ok, lane);
+            if constexpr (Epi::kSlots) {
+                if (!split) epi.empty(t, 2 * s + 1, start + total, lane);
+            }
+            __syncwarp();
+        }
+        start += total;
+        sub_in_block = (sub_in_block + 1) & (kPairSubtilesPerBlock - 1);
+    }
+    // a run that ends on a block boundary checks the block index there; the
+    // last run checks that the codes and the block index both end at n
+    if (lane == 0) {
+        if (s1 < n_sub && s1 % kPairSubtilesPerBlock == 0) {
+            if (__ldg(t.block_index + s1 / kPairSubtilesPerBlock) != start) raise_status(status, AFX_DEV_BAD_BLOCK);
+        }
+        if (s1 == n_sub && (start != n || __ldg(t.block_index + t.n_blocks) != n))
+            raise_status(status, AFX_DEV_BAD_BLOCK);
+    }
+    return true;
+}
+
 // One CTA per SM (up to 32 warps) sharing one copy of the decode tables.
 // host_src: the containers are in pinned host memory.  kPartial: the
 // launch holds the tensors whose state tables keep only their shallowest
@@ -735,6 +977,64 @@ __device__ __forceinline__ void restore_warps(const LaunchArgs& a, const Epi& ep
     }
 }
 
+// restore_warps with two chunks a lane (device-resident containers).  The
+// shared memory holds the tables, then per warp its PairSlot, its stage of
+// LaunchArgs::pair_stage bytes and its stream buffer.
+template <class Epi>
+__device__ __forceinline__ void restore_warps_pair(const LaunchArgs& a, const Epi& epi) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    SharedW& sh = *reinterpret_cast<SharedW*>(smem);
+    uint8_t* tabr = smem + sharedw_table_offset();
+    const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint8_t* wbase = tabr + a.tab_bytes + static_cast<size_t>(warp) * pair_warp_bytes(a.max_chunk_bytes, a.pair_stage);
+    PairSlot& ps = *reinterpret_cast<PairSlot*>(wbase);
+    uint8_t* stage = wbase + sizeof(PairSlot);
+    uint8_t* wstream = stage + a.pair_stage;
+    TabView tv;
+    tv.lut = reinterpret_cast<const uint32_t*>(tabr);
+    tv.len0 = tabr + kLutSize * 4;
+    tv.limit = sh.ct.limit;
+    tv.base = sh.ct.base;
+    tv.sorted = sh.ct.sorted;
+    tv.first = sh.first;
+    tv.fsm = reinterpret_cast<const char*>(tabr);
+    tv.depth = sh.ct.state_depth;
+    tv.fsm_bytes = a.tab_bytes;
+    tv.esc_base = ~0u;
+
+    const uint64_t g_begin = a.total_tiles * blockIdx.x / gridDim.x;
+    const uint64_t g_end = a.total_tiles * (blockIdx.x + 1) / gridDim.x;
+    if (g_begin >= g_end) return;
+    if (lane == 0) {
+        mbar_init(&ps.bar);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    uint32_t phase = 0;
+    const uint32_t wait_limit = a.wait_limit ? a.wait_limit : kWaitLimit;
+    bool alive = true;
+    for (uint32_t k = 0; k < a.count; ++k) {
+        const TensorArgs& t = a.t[k];
+        const uint64_t t0 = t.tile_begin, t1 = t.tile_begin + t.n_blocks;
+        if (t1 <= g_begin) continue;
+        if (t0 >= g_end) break;
+        const uint64_t b0 = (g_begin > t0 ? g_begin : t0) - t0, b1 = (g_end < t1 ? g_end : t1) - t0;
+        const uint64_t n_sub = (t.n_chunks + kPairChunks - 1) / kPairChunks;
+        const uint64_t sb = b0 * kPairSubtilesPerBlock;
+        const uint64_t se = b1 * kPairSubtilesPerBlock < n_sub ? b1 * kPairSubtilesPerBlock : n_sub;
+        __syncthreads();  // every warp is done with the previous tensor's tables
+        build_tables_w(sh, tabr, t.tab, threadIdx.x, nthreads, CtaSync{});  // ends with __syncthreads
+        const uint64_t span = se - sb;
+        const uint64_t s0 = sb + span * warp / nwarps, s1 = sb + span * (warp + 1) / nwarps;
+        if (alive && s0 < s1) {
+            alive = warp_run_pair(tv, ps, stage, a.pair_stage, wstream, t, s0, s1, lane, a.status, wait_limit,
+                                  a.stall != 0, phase, epi);
+            if (!alive && !a.stall && lane == 0) raise_status(a.status, AFX_DEV_UNDRAINED);
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1) restore_store_kernel(const __grid_constant__ LaunchArgs a) {
     restore_warps<false, false>(a, StoreEpilogue{});
 }
@@ -757,6 +1057,22 @@ __global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
     restore_warps<true, false>(a, StoreE4M3Epilogue{});
 }
 
+// The restores with two chunks a lane (device-resident containers).
+__global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
+    restore_store_pair_kernel(const __grid_constant__ LaunchArgs a) {
+    restore_warps_pair(a, StoreEpilogue{});
+}
+
+__global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
+    restore_store_fp16_pair_kernel(const __grid_constant__ LaunchArgs a) {
+    restore_warps_pair(a, StoreFP16Epilogue{});
+}
+
+__global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
+    restore_store_e4m3_pair_kernel(const __grid_constant__ LaunchArgs a) {
+    restore_warps_pair(a, StoreE4M3Epilogue{});
+}
+
 // The restore of FP16 containers (raw bytes plus the hi section's nibble per
 // element), from device memory and from pinned host memory.
 __global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
@@ -772,6 +1088,15 @@ __global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
 template <int B>
 __global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1) restore_gemv_kernel(const __grid_constant__ LaunchArgs a) {
     restore_warps<false, false>(a, GemvEpilogue<B>{});
+}
+
+// The fused GEMV with two chunks a lane (batch 1; matrices whose rows hold at
+// least LaunchArgs::pair_stage weights, so that a pass still meets at most
+// two rows).
+template <int B>
+__global__ void __launch_bounds__(kRestoreMaxWarps * 32, 1)
+    restore_gemv_pair_kernel(const __grid_constant__ LaunchArgs a) {
+    restore_warps_pair(a, GemvEpilogue<B>{});
 }
 
 // The BF16 restore and GEMV of tensors whose state tables keep only their
@@ -1231,6 +1556,54 @@ afx_status warp_launch_config(LaunchArgs& la, int* warps_out, size_t* smem_out) 
     return AFX_OK;
 }
 
+// The largest stage a warp needs with two chunks a lane: every code of a
+// sub-tile, the slack, the offset within a group of 8 and 16 spare bytes.
+constexpr uint32_t kPairStageMax = (kPairChunks * kMaxChunkCodes + kPairStageSlack + 7 + 16 + 15) & ~15u;
+
+// The stage of a restore launch with two chunks a lane, or 0 when the
+// launch keeps one chunk a lane.  Two chunks a lane pay off when
+// - each CTA has at least kPairMinBlocks blocks: a warp's share then holds
+//   several 64-chunk sub-tiles, so that the last one does not leave the
+//   SM's other warps waiting (a 4096 x 4096 matrix is 4.4 blocks a CTA);
+// - 32 warps with their stream buffers and the launch's tables leave each
+//   warp a stage that holds a sub-tile's codes, as each tensor's average
+//   code length predicts them with 5 % to spare (a sub-tile's count spreads
+//   by about 1 %) and the slack, for all but kPairMaxSplitShare of the
+//   launch's weights.  Sub-tiles that do not fit (a norm vector's 1-bit
+//   codes, say) are decoded in two halves of 16 lanes (warp_run_pair).
+// AFX_CHUNKS_A_LANE=1 in the environment keeps one chunk a lane; =2 takes
+// two wherever the stage fits, whatever the two rules say (so that tests
+// reach the two-chunk path with small and ragged tensors).
+constexpr uint64_t kPairMinBlocks = 16;
+constexpr double kPairMaxSplitShare = 0.02;
+
+uint32_t pair_stage_bytes(const LaunchArgs& la, uint64_t grid) {
+    if (la.host_src || la.partial || la.kind > kKindE4M3) return 0;
+    const char* e = std::getenv("AFX_CHUNKS_A_LANE");
+    const bool force = e && e[0] == '2' && e[1] == 0;
+    if (e && e[0] == '1' && e[1] == 0) return 0;
+    if (!force && (grid == 0 || la.total_tiles < kPairMinBlocks * grid)) return 0;
+    int optin = 0;
+    const int dev = current_device();
+    if (dev < 0 || cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return 0;
+    const size_t fixed = sharedw_table_offset() + la.tab_bytes;
+    const size_t other = pair_warp_bytes(la.max_chunk_bytes, 0);
+    if (fixed + kRestoreMaxWarps * (other + kPairStageMin) > static_cast<size_t>(optin)) return 0;
+    const size_t per_warp = (static_cast<size_t>(optin) - fixed) / kRestoreMaxWarps;
+    const uint32_t stage = static_cast<uint32_t>(std::min<size_t>((per_warp - other) & ~size_t(15), kPairStageMax));
+    double all = 0.0, split = 0.0;
+    for (uint32_t i = 0; i < la.count; ++i) {
+        const TensorArgs& t = la.t[i];
+        if (t.total_bits == 0) continue;
+        const double codes = static_cast<double>(kPairChunks) * 8.0 * t.chunk_bytes * static_cast<double>(t.n) /
+                             static_cast<double>(t.total_bits);
+        all += static_cast<double>(t.n);
+        if (codes * 1.05 + kPairStageSlack + 7 + 16 > stage) split += static_cast<double>(t.n);
+    }
+    return force || split <= kPairMaxSplitShare * all ? stage : 0;
+}
+
 // The warp GEMV (matrices whose rows hold at least kWarpStage weights, a
 // multiple of 8) and its row fix-up.
 template <int B>
@@ -1243,7 +1616,22 @@ afx_status launch_gemv_warp(LaunchArgs& la, cudaStream_t s) {
     const afx_status st = warp_launch_config(la, &warps, &smem);
     if (st != AFX_OK) return st;
     int per_sm = 0;
-    void (*const kernel)(LaunchArgs) = la.partial ? restore_gemv_partial_kernel<B> : restore_gemv_kernel<B>;
+    void (*kernel)(LaunchArgs) = la.partial ? restore_gemv_partial_kernel<B> : restore_gemv_kernel<B>;
+    // two chunks a lane at batch 1 (measured on the layer's matrices: 6 %
+    // faster at batch 1; at batch 4 the kernel's sums and loads then spill
+    // and it runs 4 % slower)
+    la.pair_stage = 0;
+    if constexpr (B == 1) {
+        la.pair_stage = pair_stage_bytes(la, std::min<uint64_t>(la.total_tiles, static_cast<uint64_t>(sms)));
+        for (uint32_t i = 0; i < la.count && la.pair_stage; ++i)
+            if (la.t[i].cols < la.pair_stage) la.pair_stage = 0;  // a pass could meet three rows
+        if (la.pair_stage) {
+            kernel = restore_gemv_pair_kernel<1>;
+            warps = kRestoreMaxWarps;
+            smem = sharedw_table_offset() + la.tab_bytes +
+                   static_cast<size_t>(kRestoreMaxWarps) * pair_warp_bytes(la.max_chunk_bytes, la.pair_stage);
+        }
+    }
     const afx_status pst = prepare_kernel(reinterpret_cast<const void*>(kernel), warps * 32, smem, &per_sm);
     if (pst != AFX_OK) return pst;
     const uint64_t grid = std::min<uint64_t>(la.total_tiles, static_cast<uint64_t>(sms) * per_sm);
@@ -1261,6 +1649,16 @@ afx_status launch_gemv_warp(LaunchArgs& la, cudaStream_t s) {
     cfg.numAttrs = 1;
     AFX_CUDA_TRY(cudaLaunchKernelEx(&cfg, gemv_fixup_warp_kernel<B>, la), "gemv_fixup_warp_kernel launch");
     return AFX_OK;
+}
+
+// The chunks a lane (1 or 2) a restore launch of la takes: the choice
+// launch_restore<0> makes, without launching.
+uint32_t restore_chunks_a_lane(LaunchArgs la) {
+    int warps = 0;
+    size_t smem = 0;
+    const int sms = sm_count();
+    if (sms <= 0 || warp_launch_config(la, &warps, &smem) != AFX_OK) return 1;
+    return pair_stage_bytes(la, std::min<uint64_t>(la.total_tiles, static_cast<uint64_t>(sms))) ? 2u : 1u;
 }
 
 // programmatic: the launch follows another restore launch of the same
@@ -1284,6 +1682,15 @@ afx_status launch_restore(LaunchArgs& la, cudaStream_t s, bool programmatic = fa
                                                     {restore_store_e4m3_kernel, restore_store_e4m3_host_kernel}};
         void (*kernel)(LaunchArgs) = kernels[la.kind < 3 ? la.kind : 0][la.host_src ? 1 : 0];
         if (la.partial) kernel = la.host_src ? restore_store_host_partial_kernel : restore_store_partial_kernel;
+        la.pair_stage = pair_stage_bytes(la, std::min<uint64_t>(la.total_tiles, static_cast<uint64_t>(sms)));
+        if (la.pair_stage) {
+            void (*const pair_kernels[3])(LaunchArgs) = {restore_store_pair_kernel, restore_store_fp16_pair_kernel,
+                                                          restore_store_e4m3_pair_kernel};
+            kernel = pair_kernels[la.kind];
+            warps = kRestoreMaxWarps;
+            smem = sharedw_table_offset() + la.tab_bytes +
+                   static_cast<size_t>(kRestoreMaxWarps) * pair_warp_bytes(la.max_chunk_bytes, la.pair_stage);
+        }
         const afx_status pst = prepare_kernel(reinterpret_cast<const void*>(kernel), warps * 32, smem, &per_sm);
         if (pst != AFX_OK) return pst;
         const uint64_t grid = std::min<uint64_t>(la.total_tiles, static_cast<uint64_t>(sms) * per_sm);
@@ -1355,17 +1762,23 @@ using namespace afx;
 namespace {
 
 // afx_decode_batch; stall_polls != 0 is the failure injection of
-// afx_test_restore_stalled.
+// afx_test_restore_stalled.  plan != nullptr: launch nothing and write, for
+// each tensor, the chunks a lane of the restore launch it would go to (0
+// for an empty tensor or a single-exponent fill); outs may then be null.
 afx_status decode_batch(const afx_desc* descs, const void* const* containers, void* const* outs, uint32_t count,
-                        afx_stream_t stream, int32_t* status, uint32_t stall_polls) {
-    if (count && (!descs || !containers || !outs)) return afx_fail(AFX_E_ARG, "null array", 0);
+                        afx_stream_t stream, int32_t* status, uint32_t stall_polls, uint32_t* plan = nullptr) {
+    if (count && (!descs || !containers || (!outs && !plan))) return afx_fail(AFX_E_ARG, "null array", 0);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     for (uint32_t i = 0; i < count; ++i) {
         const afx_desc& d = descs[i];
         const afx_status st = afx_check_desc(&d);
         if (st != AFX_OK) return afx_fail(st, "invalid container description", 0);
         if (d.n == 0) continue;
-        if (!containers[i] || !outs[i] || !aligned(containers[i], 16) || !aligned(outs[i], 16))
+        if (plan) {
+            plan[i] = 0;
+            if (!containers[i] || !aligned(containers[i], 16))
+                return afx_fail(AFX_E_ARG, "containers must be 16-byte aligned", 0);
+        } else if (!containers[i] || !outs[i] || !aligned(containers[i], 16) || !aligned(outs[i], 16))
             return afx_fail(AFX_E_ARG, "container and output must be 16-byte aligned", 0);
         if (d.nsym >= 2 && d.block_chunks != static_cast<uint32_t>(kThreads))
             return afx_fail(AFX_E_ARG, "the decoder runs 512 chunks per block", 0);
@@ -1386,11 +1799,22 @@ afx_status decode_batch(const afx_desc* descs, const void* const* containers, vo
             la.partial = f == kPartialList ? 1u : 0u;
         }
     uint32_t restores = 0;  // restore launches made so far by this call
+    uint32_t members[kLists][2][kMaxTensors];  // plan: the tensors of each list's pending launch
+    auto flush = [&](LaunchArgs& la, const uint32_t* mem) -> afx_status {
+        if (plan) {
+            const uint32_t c = restore_chunks_a_lane(la);
+            for (uint32_t k = 0; k < la.count; ++k) plan[mem[k]] = c;
+            return AFX_OK;
+        }
+        const afx_status st = launch_restore<0>(la, s, restores > 0);
+        ++restores;
+        return st;
+    };
     for (uint32_t i = 0; i < count; ++i) {
         const afx_desc& d = descs[i];
         if (d.n == 0) continue;
         const uint8_t* base = static_cast<const uint8_t*>(containers[i]);
-        const Where wc = where(containers[i]), wo = where(outs[i]);
+        const Where wc = where(containers[i]), wo = plan ? Where::device : where(outs[i]);
         if (wc == Where::unusable || wo == Where::unusable)
             return afx_fail(AFX_E_ARG, "container and output must be device memory or pinned host memory", 0);
         if (stall_polls && wc != Where::device)
@@ -1398,6 +1822,8 @@ afx_status decode_batch(const afx_desc* descs, const void* const* containers, vo
         const bool e4m3 = d.format == AFX_FMT_E4M3, fp16 = d.format == AFX_FMT_FP16;
         const int list = e4m3 ? kKindE4M3 : fp16 ? kKindFP16 : partial_table(d) ? kPartialList : kKindBF16;
         LaunchArgs& la = lists[list][wc == Where::host ? 1 : 0];
+        uint32_t* mem = members[list][wc == Where::host ? 1 : 0];
+        if (d.nsym == 1 && plan) continue;
         if (d.nsym == 1) {
             const int sms = sm_count();
             if (sms <= 0) return afx_fail(AFX_E_CUDA, "cannot query the SM count", 0);
@@ -1419,14 +1845,14 @@ afx_status decode_batch(const afx_desc* descs, const void* const* containers, vo
             continue;
         }
         if (la.count == static_cast<uint32_t>(kMaxTensors)) {
-            const afx_status st = launch_restore<0>(la, s, restores > 0);
+            const afx_status st = flush(la, mem);
             if (st != AFX_OK) return st;
-            ++restores;
             reset_launch(la);
         }
+        mem[la.count] = i;
         TensorArgs& t = la.t[la.count++];
         fill_tensor(d, containers[i], t);
-        t.out = outs[i];
+        t.out = plan ? nullptr : outs[i];
         la.total_tiles += kTableBuildTiles;
         t.tile_begin = la.total_tiles;
         la.total_tiles += d.n_blocks;
@@ -1436,9 +1862,8 @@ afx_status decode_batch(const afx_desc* descs, const void* const* containers, vo
         for (int h = 0; h < 2; ++h) {
             LaunchArgs& la = lists[f][h];
             if (la.count == 0 || la.total_tiles == 0) continue;
-            const afx_status st = launch_restore<0>(la, s, restores > 0);
+            const afx_status st = flush(la, members[f][h]);
             if (st != AFX_OK) return st;
-            ++restores;
         }
     return AFX_OK;
 }
@@ -1448,6 +1873,12 @@ afx_status decode_batch(const afx_desc* descs, const void* const* containers, vo
 extern "C" afx_status afx_decode_batch(const afx_desc* descs, const void* const* containers, void* const* outs,
                                        uint32_t count, afx_stream_t stream, int32_t* status) {
     return decode_batch(descs, containers, outs, count, stream, status, 0);
+}
+
+extern "C" afx_status afx_decode_chunks_a_lane(const afx_desc* descs, const void* const* containers, uint32_t count,
+                                               uint32_t* chunks) {
+    if (count && !chunks) return afx_fail(AFX_E_ARG, "null array", 0);
+    return decode_batch(descs, containers, nullptr, count, nullptr, nullptr, 0, chunks);
 }
 
 extern "C" afx_status afx_test_restore_stalled(const afx_desc* desc, const void* container, void* out,

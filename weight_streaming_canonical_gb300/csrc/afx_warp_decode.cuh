@@ -95,6 +95,7 @@ struct LaunchArgs {
     uint32_t host_src;         // restore: the containers are in pinned host memory (restore_store_host_kernel)
     uint32_t kind;             // restore: element kind, kKindBF16 / kKindFP16 / kKindE4M3
     uint32_t partial;          // BF16 tensors whose state tables keep only their shallowest nodes
+    uint32_t pair_stage;       // restore: 0, or two chunks a lane with a stage of this many bytes a warp
     int32_t* status;
     TensorArgs t[kMaxTensors];
 };
@@ -991,7 +992,8 @@ struct FsmLane {
 // word shared with the previous lane: that lane stores its bytes of the
 // word only after the warp barrier.
 __device__ __forceinline__ void fsm_chunk_steps(const TabView& tv, const uint32_t* words, uint32_t nwords, uint32_t gap,
-                                                uint32_t skip_row0, uint8_t* stage, uint32_t s_run, FsmLane& fl) {
+                                                uint32_t skip_row0, uint8_t* stage, uint32_t s_run, FsmLane& fl,
+                                                uint32_t stage_cap = kWarpStage) {
     uint32_t* wout = reinterpret_cast<uint32_t*>(stage + (s_run & ~3u));
     const uint32_t* const w_begin = wout;
     uint32_t acc = 0, fill = 8 * (s_run & 3u);
@@ -1009,7 +1011,7 @@ __device__ __forceinline__ void fsm_chunk_steps(const TabView& tv, const uint32_
         fsm_step_checked(tv, st, __byte_perm(X, 0u, 0x4441), acc, fill, wout);
         fsm_step_checked(tv, st, X & 0xFFu, acc, fill, wout);
     }
-    AFX_CHECK(reinterpret_cast<uint8_t*>(wout) <= stage + kWarpStage, kChkStageSteps);
+    AFX_CHECK(reinterpret_cast<uint8_t*>(wout) <= stage + stage_cap, kChkStageSteps);
     fl.wout = wout;
     fl.acc = acc;
     fl.fill = fill;
@@ -1025,7 +1027,7 @@ __device__ __forceinline__ void fsm_chunk_steps(const TabView& tv, const uint32_
 // a bit of the staged stream).
 __device__ __forceinline__ void fsm_chunk_steps_esc(const TabView& tv, const uint32_t* stream, uint32_t k0,
                                                     uint32_t nbytes, uint32_t gap, uint32_t skip_row0, uint8_t* stage,
-                                                    uint32_t s_run, FsmLane& fl) {
+                                                    uint32_t s_run, FsmLane& fl, uint32_t stage_cap = kWarpStage) {
     uint32_t* wout = reinterpret_cast<uint32_t*>(stage + (s_run & ~3u));
     const uint32_t* const w_begin = wout;
     uint32_t acc = 0, fill = 8 * (s_run & 3u);
@@ -1072,7 +1074,7 @@ __device__ __forceinline__ void fsm_chunk_steps_esc(const TabView& tv, const uin
             if (e & 7u) st = skip_row0 + ((e & 7u) - 1) * kFsmRowBytes;
         }
     }
-    AFX_CHECK(reinterpret_cast<uint8_t*>(wout) <= stage + kWarpStage, kChkStageSteps);
+    AFX_CHECK(reinterpret_cast<uint8_t*>(wout) <= stage + stage_cap, kChkStageSteps);
     fl.wout = wout;
     fl.acc = acc;
     fl.fill = fill;
