@@ -1430,6 +1430,26 @@ void fill_tensor(const afx_desc& d, const void* container, TensorArgs& t) {
         const uint64_t by_bytes = d.exp_bytes >= sub_bytes + kStreamPad ? (d.exp_bytes - kStreamPad) / sub_bytes : 0;
         t.n_sub_full = std::min(by_chunks, by_bytes);
     }
+    // The codes in a 64-chunk sub-tile: its bits over the mean code length,
+    // with the spread of a count of codes whose lengths add up to a fixed
+    // number of bits (variance bits * var(len) / mean(len)^3); the lengths'
+    // variance is taken with each code's share 2^-len (the code is
+    // complete, so the shares add up to 1).
+    t.pair_codes = 0;
+    if (d.total_bits && d.n) {
+        double mu = 0.0, m2 = 0.0;
+        for (int sym = 0; sym < 256; ++sym)
+            if (d.len[sym]) {
+                const double p = std::ldexp(1.0, -static_cast<int>(d.len[sym]));
+                mu += p * d.len[sym];
+                m2 += p * d.len[sym] * d.len[sym];
+            }
+        const double var = std::max(0.0, m2 - mu * mu);
+        const double bits = static_cast<double>(kPairChunks) * 8.0 * d.chunk_bytes;
+        const double mean_len = static_cast<double>(d.total_bits) / static_cast<double>(d.n);
+        const double codes = bits / mean_len, sd = std::sqrt(bits * var / (mean_len * mean_len * mean_len));
+        t.pair_codes = static_cast<uint32_t>(std::min(std::ceil(codes + 5.0 * sd), 65536.0));
+    }
     make_tables(d, t.tab);
 }
 
@@ -1566,11 +1586,11 @@ constexpr uint32_t kPairStageMax = (kPairChunks * kMaxChunkCodes + kPairStageSla
 //   several 64-chunk sub-tiles, so that the last one does not leave the
 //   SM's other warps waiting (a 4096 x 4096 matrix is 4.4 blocks a CTA);
 // - 32 warps with their stream buffers and the launch's tables leave each
-//   warp a stage that holds a sub-tile's codes, as each tensor's average
-//   code length predicts them with 5 % to spare (a sub-tile's count spreads
-//   by about 1 %) and the slack, for all but kPairMaxSplitShare of the
-//   launch's weights.  Sub-tiles that do not fit (a norm vector's 1-bit
-//   codes, say) are decoded in two halves of 16 lanes (warp_run_pair).
+//   warp a stage that holds a sub-tile's codes (TensorArgs::pair_codes: 5
+//   standard deviations above the mean, about 3300 for N(0, 0.02) weights)
+//   and the slack, for all but kPairMaxSplitShare of the launch's weights.
+//   Sub-tiles that do not fit (a norm vector's 1-bit codes, say) are
+//   decoded in two halves of 16 lanes (warp_run_pair).
 // AFX_CHUNKS_A_LANE=1 in the environment keeps one chunk a lane; =2 takes
 // two wherever the stage fits, whatever the two rules say (so that tests
 // reach the two-chunk path with small and ragged tensors).
@@ -1596,10 +1616,8 @@ uint32_t pair_stage_bytes(const LaunchArgs& la, uint64_t grid) {
     for (uint32_t i = 0; i < la.count; ++i) {
         const TensorArgs& t = la.t[i];
         if (t.total_bits == 0) continue;
-        const double codes = static_cast<double>(kPairChunks) * 8.0 * t.chunk_bytes * static_cast<double>(t.n) /
-                             static_cast<double>(t.total_bits);
         all += static_cast<double>(t.n);
-        if (codes * 1.05 + kPairStageSlack + 7 + 16 > stage) split += static_cast<double>(t.n);
+        if (static_cast<uint64_t>(t.pair_codes) + kPairStageSlack + 7 + 16 > stage) split += static_cast<double>(t.n);
     }
     return force || split <= kPairMaxSplitShare * all ? stage : 0;
 }

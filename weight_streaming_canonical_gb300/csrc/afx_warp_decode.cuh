@@ -75,6 +75,7 @@ struct TensorArgs {
     uint64_t sub_begin;        // warp GEMV: first sub-tile of this tensor in the launch's sub-tile list
     uint32_t chunk_bytes;      // T
     uint32_t rows_per_warp;    // GEMV: capacity of the per-warp partial table
+    uint32_t pair_codes;       // host: codes a 64-chunk sub-tile holds, 5 standard deviations above the mean
     void* out;                 // restore: n elements (uint16 BF16 / FP16, uint8 E4M3)
     const uint16_t* x;         // GEMV: [B][cols]
     float* y;                  // GEMV: [B][rows]
