@@ -1,8 +1,9 @@
 """The bounds-checked build (AFX_DEBUG_BOUNDS=1, libafx_debug.so) on the
 restore path: across ragged sizes, the 12-bit-table path, long codes, host
 containers, E4M3 and FP16 elements, partial state tables (escapes), the
-fused GEMV and corrupt containers, no range a kernel touches ever leaves
-its buffer.  The check runs in a child process that
+fused GEMV and corrupt containers, with one chunk a lane and again with
+two (sub-tiles decoded whole and in two halves), no range a kernel
+touches ever leaves its buffer.  The check runs in a child process that
 loads the debug library; compute-sanitizer is not available here."""
 import json
 import os
@@ -135,6 +136,74 @@ for trial in range(150):
         fuzz_exact += 1
 statuses.append(("fuzz", fuzz_flagged, 0, None))
 statuses.append(("fuzz_clean", fuzz_exact, 0, None))
+# the same kinds of case with two chunks a lane (64-chunk sub-tiles), forced
+# on for these small tensors; cases are tagged "2:"
+import os
+os.environ["AFX_CHUNKS_A_LANE"] = "2"
+c, d = afx.encode(synth.normal(1000, seed=3))
+assert afx.afx_decode_chunks_a_lane([d], [torch.from_numpy(c).cuda()]) == [2]
+for n in (1000, 3_000_017):
+    w = synth.normal(n, seed=n + 1)
+    got, st = restore(*afx.encode(w))
+    statuses.append(("2:normal", n, st, bool(np.array_equal(got, w))))
+w = synth.all_bf16_patterns()
+for T in (4, 32):
+    got, st = restore(*afx.encode(w, chunk_bytes=T))
+    statuses.append(("2:patterns", T, st, bool(np.array_equal(got, w))))
+w = synth.normal_e4m3(999_999, seed=4)
+got, st = restore(*afx.encode(w, fmt=afx.AFX_FMT_E4M3))
+statuses.append(("2:e4m3", w.size, st, bool(np.array_equal(got, w))))
+w = synth.normal_fp16(300_001, seed=9)
+got, st = restore(*afx.encode(w, fmt=afx.AFX_FMT_FP16))
+statuses.append(("2:fp16", w.size, st, bool(np.array_equal(got, w))))
+# sub-tiles that overflow the stage (decoded in two halves): a run of
+# weights that all share the most common exponent, and 1-bit codes
+a = synth.normal(1_500_007, seed=41)
+top = np.bincount((a >> 7) & 0xFF, minlength=256).argmax()
+mid = (np.random.default_rng(5).integers(0, 1 << 16, 65_536).astype(np.uint16) & 0x807F) | np.uint16(top << 7)
+w = np.concatenate([a, mid, synth.normal(1_200_001, seed=42)])
+got, st = restore(*afx.encode(w))
+statuses.append(("2:halves", w.size, st, bool(np.array_equal(got, w))))
+w = np.where(np.random.default_rng(6).random(1_000_001) < 0.6, 0x3F80, 0x3F00).astype(np.uint16)
+got, st = restore(*afx.encode(w))
+statuses.append(("2:one-bit", w.size, st, bool(np.array_equal(got, w))))
+w = synth.normal(400_000, seed=16)
+c, d = afx.encode(w)
+bad = c.copy()
+bad[d.off_exp: d.off_exp + d.n_chunks * d.chunk_bytes] = rng.integers(0, 256, size=d.n_chunks * d.chunk_bytes,
+                                                                        dtype=np.uint8)
+statuses.append(("2:garbage stream", 0, restore(bad, d)[1], None))
+bad = c.copy()
+idx = d.off_chunk + 2 * rng.integers(0, d.n_chunks, size=64)
+bad[idx] ^= np.uint8(0xA5)
+statuses.append(("2:chunk index", 0, restore(bad, d)[1], None))
+bad = c.copy()
+bad[d.off_block + 8: d.off_block + 16] = 0xFF
+statuses.append(("2:block index", 0, restore(bad, d)[1], None))
+# the batch-1 GEMV with two chunks a lane
+rows, cols = 96, 5120
+c, d = afx.encode(synth.normal(rows * cols, seed=17))
+x1 = torch.from_numpy(synth.activations(1, cols, seed=3).view(np.int16)).cuda()
+y1 = torch.empty((1, rows), dtype=torch.float32, device="cuda")
+ws = torch.empty(afx.afx_decode_gemv_workspace(d, 1) // 4 + 4, dtype=torch.float32, device="cuda")
+st = torch.zeros(1, dtype=torch.int32, device="cuda")
+afx.afx_decode_gemv(d, torch.from_numpy(c).cuda(), rows, cols, x1, y1, ws, status_dev=st)
+torch.cuda.synchronize()
+statuses.append(("2:gemv", rows * cols, int(st.item()), None))
+flagged = exact = 0
+for trial in range(60):
+    c0, d = bases[trial % 3]
+    bad = c0.copy()
+    lo, hi = [(d.off_exp, d.off_exp + d.exp_bytes), (d.off_sm, d.off_chunk),
+              (d.off_chunk, d.off_block), (d.off_block, d.container_bytes)][trial % 4]
+    k = int(rng.integers(1, 64))
+    bad[rng.integers(lo, hi, size=k)] ^= np.uint8(1) << rng.integers(0, 8, size=k).astype(np.uint8)
+    got, st = restore(bad, d)
+    flagged += st != 0
+    exact += st == 0
+statuses.append(("2:fuzz", flagged, 0, None))
+statuses.append(("2:fuzz_clean", exact, 0, None))
+del os.environ["AFX_CHUNKS_A_LANE"]
 bits, checked = afx.afx_debug_bounds_report()
 print(json.dumps({"bits": bits, "checked": checked, "cases": statuses}))
 """
@@ -146,7 +215,8 @@ def test_bounds_checked_build_reports_no_violation():
     assert r.returncode == 0, r.stderr[-3000:]
     rep = json.loads(r.stdout.strip().splitlines()[-1])
     assert rep["checked"]
-    for kind, size, status, exact in rep["cases"]:
+    for tagged, size, status, exact in rep["cases"]:
+        kind = tagged.split(":", 1)[-1]  # "2:" marks the cases with two chunks a lane
         if kind in ("garbage stream", "chunk index", "block index", "garbage partial"):
             assert status != 0, kind
         elif kind == "fuzz":
