@@ -1,6 +1,7 @@
 """Randomized restores on three streams at once: batches of 1 to 6 tensors
 drawn from a pool of sizes, distributions and element formats, every
-restored tensor compared with its source bit for bit, for a fixed time."""
+restored tensor compared with its source bit for bit, for a fixed time,
+with the launches' own choice of chunks a lane and with two forced."""
 import time
 
 import numpy as np
@@ -37,8 +38,13 @@ def _pool(afx, dev, rng):
     return pool
 
 
-def test_random_batches_on_three_streams_stay_bit_exact(afx):
+@pytest.mark.parametrize("lanes", ["auto", "2"])
+def test_random_batches_on_three_streams_stay_bit_exact(afx, lanes, monkeypatch):
+    # "2": every launch with two chunks a lane (forced; these tensors are
+    # too small to take it by themselves)
     import torch
+    if lanes != "auto":
+        monkeypatch.setenv("AFX_CHUNKS_A_LANE", lanes)
     rng = np.random.default_rng(12345)
     dev = torch.device("cuda:0")
     pool = _pool(afx, dev, rng)

@@ -620,6 +620,9 @@ __device__ __forceinline__ bool warp_run(const TabView& tv, WarpSlot& ws, uint8_
                 if (chunk_end <= stream_end) {
                     if constexpr (kPartial)
                         fsm_chunk_steps_esc(tv, stream, lane * (T >> 2), T, gap, skip_row0, ws.stage, s_run, fl);
+                    else if (T % 16 == 0)  // 16-byte loads of the chunk's words
+                        fsm_span_steps(tv, stream + lane * (T >> 2), T >> 2, gap, skip_row0, ws.stage, s_run, fl,
+                                       kWarpStage);
                     else
                         fsm_chunk_steps(tv, stream + lane * (T >> 2), T >> 2, gap, skip_row0, ws.stage, s_run, fl);
                     stepped = true;
@@ -855,8 +858,12 @@ __device__ __forceinline__ bool warp_run_pair(const TabView& tv, PairSlot& ps, u
                 }
                 if (fsm) {
                     if (span_end <= stream_end) {
-                        fsm_chunk_steps(tv, stream + lane * span_words, span_words, gap, skip_row0, stage, s_run, fl,
-                                        stage_cap);
+                        if (span_words % 4 == 0)
+                            fsm_span_steps(tv, stream + lane * span_words, span_words, gap, skip_row0, stage, s_run,
+                                           fl, stage_cap);
+                        else  // 4-byte chunks: a span is two words
+                            fsm_chunk_steps(tv, stream + lane * span_words, span_words, gap, skip_row0, stage, s_run,
+                                            fl, stage_cap);
                         stepped = true;
                     } else {  // the stream's partial last chunk
                         lbad = decode_run_fsm(tv, stream, lane * span_words, gap, cnt, stage, s_run, next, span_end,

@@ -1021,6 +1021,50 @@ __device__ __forceinline__ void fsm_chunk_steps(const TabView& tv, const uint32_
     fl.st = st;
 }
 
+// fsm_chunk_steps for a run of 4k words (a 16-byte chunk or larger, or a
+// two-chunk span of 8-byte chunks or larger): the words come in as 16-byte
+// loads.  The lanes' runs lie 16 or more bytes apart, so word loads put
+// four lanes (16-byte chunks) or eight (32-byte spans) on each bank and
+// the shared-memory pipe replays them; 16-byte loads of 16-byte chunks
+// are conflict-free, and of 32-byte spans take twice the minimum passes.
+__device__ __forceinline__ void fsm_span_steps(const TabView& tv, const uint32_t* words, uint32_t nwords, uint32_t gap,
+                                               uint32_t skip_row0, uint8_t* stage, uint32_t s_run, FsmLane& fl,
+                                               uint32_t stage_cap) {
+    uint32_t* wout = reinterpret_cast<uint32_t*>(stage + (s_run & ~3u));
+    const uint32_t* const w_begin = wout;
+    uint32_t acc = 0, fill = 8 * (s_run & 3u);
+    const uint32_t h = gap & 7u;
+    uint32_t st = h ? skip_row0 + (h - 1) * kFsmRowBytes : 0u;
+    auto word = [&](uint32_t X) {
+        fsm_step_checked(tv, st, X >> 24, acc, fill, wout);
+        fsm_step_checked(tv, st, __byte_perm(X, 0u, 0x4442), acc, fill, wout);
+        fsm_step_checked(tv, st, __byte_perm(X, 0u, 0x4441), acc, fill, wout);
+        fsm_step_checked(tv, st, X & 0xFFu, acc, fill, wout);
+    };
+    const uint4 X0 = *reinterpret_cast<const uint4*>(words);
+    if (gap < 8) fsm_step_checked(tv, st, X0.x >> 24, acc, fill, wout);
+    if (gap < 16) fsm_step_checked(tv, st, __byte_perm(X0.x, 0u, 0x4442), acc, fill, wout);
+    fsm_step_checked(tv, st, __byte_perm(X0.x, 0u, 0x4441), acc, fill, wout);
+    fsm_step_checked(tv, st, X0.x & 0xFFu, acc, fill, wout);
+    word(X0.y);
+    word(X0.z);
+    word(X0.w);
+    for (uint32_t w = 4; w < nwords; w += 4) {
+        const uint4 X = *reinterpret_cast<const uint4*>(words + w);
+        word(X.x);
+        word(X.y);
+        word(X.z);
+        word(X.w);
+    }
+    AFX_CHECK(reinterpret_cast<uint8_t*>(wout) <= stage + stage_cap, kChkStageSteps);
+    fl.wout = wout;
+    fl.acc = acc;
+    fl.fill = fill;
+    fl.first = wout == w_begin ? (s_run & 3u) : 0u;
+    fl.emitted = 4 * static_cast<uint32_t>(wout - w_begin) + (fill >> 3) - (s_run & 3u);
+    fl.st = st;
+}
+
 // fsm_chunk_steps for a partial table: the same steps from stream word k0
 // (the chunk's first), four to a word while no escape comes, with each
 // escape handled where it comes.  The code an escape decodes may cross the
