@@ -1,7 +1,8 @@
 """Host-side helpers of the bench's legs, on CPU: the comparison of the fused
 product with restore-then-GEMM picks the fastest unfused form per batch and
 skips batches that one of the two legs did not run; the host-encode leg
-re-encodes the step's tensors and checks the containers are the same."""
+re-encodes the step's tensors and checks the containers are the same; the
+committed traffic records name kernels and workloads that exist."""
 import bench
 
 
@@ -74,3 +75,28 @@ def test_data_text_names_each_workloads_inputs():
     assert "4096x4096" in bench.data_text("matrix4096")
     assert "2^26" in bench.data_text("normal:26")
     assert all(bench.data_text(w).startswith("synthetic") for w in bench.WORKLOADS)
+
+
+def test_every_traffic_record_names_a_kernel_and_a_workload():
+    # profiles/<kernel>[.<workload>].traffic.json: the kernel is one the
+    # sources define, the workload one the bench runs, the file name agrees
+    # with the record, and the record's sources exist
+    import glob
+    import json
+    import os
+    import re
+    recs = sorted(glob.glob(os.path.join(bench.ROOT, "profiles", "*.traffic.json")))
+    assert recs
+    src = open(os.path.join(bench.ROOT, "weight_streaming_canonical_gb300", "csrc", "afx_decode.cu")).read()
+    kernels = set(re.findall(r"\b(restore_\w*kernel)\s*\(const __grid_constant__", src))
+    assert "restore_store_pair_kernel" in kernels and "restore_store_kernel" in kernels
+    for path in recs:
+        rec = json.load(open(path))
+        name = os.path.basename(path)[: -len(".traffic.json")]
+        kernel, _, workload = name.partition(".")
+        assert rec["kernel"] == kernel and kernel in kernels, path
+        assert rec.get("bench_workload", "layer") == (workload or rec.get("bench_workload", "layer")), path
+        assert rec.get("bench_workload", "layer") in bench.WORKLOADS, path
+        assert rec["dram_bytes_per_launch"] == rec["dram_bytes_read"] + rec["dram_bytes_write"] > 0, path
+        for s in rec["source"]:
+            assert os.path.exists(os.path.join(bench.ROOT, s)), (path, s)
