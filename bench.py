@@ -1052,7 +1052,8 @@ def run_prefill_bench(afx, parts, dev_blob, offs, dev, args):
                             "fused_weights_per_s": n_w * ((n_tok + 511) // 512) / (fused_ms * 1e-3),
                             "unfused_best_over_fused": best / fused_ms,
                             "fused_agrees_with_unfused": agree, "fused_worst_err_over_sum_abs": worst})
-    out["path"] = ("afx_prefill / afx_prefill_batch: restore_store_kernel into scratch, cuBLAS BF16 GEMM with "
+    out["path"] = ("afx_prefill / afx_prefill_batch: the restore (restore_store_pair_kernel for a launch of the "
+                   "seven matrices, two chunks a lane) into scratch, cuBLAS BF16 GEMM with "
                    "float32 accumulation; sequential: restore then product per matrix on one stream; overlapped: "
                    "restore of matrix i+1 on a second stream; one restore launch: all seven restored by one "
                    "afx_decode_batch launch, then the products; tokens_per_s and tflops from the fastest of "
@@ -1185,8 +1186,9 @@ def run_wide_trees_bench(afx, dev, args, layer_weights_per_s=None):
                             "decoder": kinds.get(kind, str(kind)), "state_rows": rows,
                             "frac_of_layer_rate": wps / layer_weights_per_s if layer_weights_per_s else None})
         del w, c
-    out["path"] = ("afx_decode_batch of one tensor per step (restore_store_kernel, or restore_store_partial_kernel "
-                   "for a partial state table)")
+    out["path"] = ("afx_decode_batch of one tensor per step (restore_store_kernel, restore_store_pair_kernel where "
+                   "two chunks a lane fit beside the tables, or restore_store_partial_kernel for a partial state "
+                   "table)")
     return out
 
 
