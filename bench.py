@@ -1294,7 +1294,8 @@ def run_gemv_bench(afx, parts, dev_blob, offs, dev, args, restore_weights_per_s=
                             "peak_kind": peak_kind,
                             "frac_of_restore_rate": (n / (ms * 1e-3)) / restore_weights_per_s
                             if restore_weights_per_s else None,
-                            "launches": "one restore_gemv_kernel<B> and one row fix-up per product batch"}
+                            "launches": "one restore kernel (restore_gemv_pair_kernel<1> at batch 1, two chunks a lane; "
+                                         "restore_gemv_kernel<4> at batch 4) and one row fix-up per product batch"}
     res["weights"] = n
     res["bound"] = ("the decode's instruction rate (the same byte-step decoder as the restore), not HBM: "
                     "frac_of_restore_rate compares the product's weights/s with the restore's")
